@@ -1,0 +1,337 @@
+"""Plain fp64 CPU oracle of the DeepSeekMoE layer forward.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may import or run
+this module.  The product path (the CUDA library and its Python binding) never
+calls it and shares no code with it: not a helper, not a table, not a constant.
+
+What it computes (one token u_t at a time, all in float64 unless stated):
+
+  1. logits  l_e = <u_t, W_g[e]>                      (gate linear layer, no bias)
+  2. affinity s_e = softmax(l)_e over all E experts, or sigmoid(l_e)
+  3. selection score  sigma_e = s_e + b_e            (b only steers selection)
+  4. group-limited selection: contiguous groups of E/n_group experts, a group
+     score (max, or sum of the top-m sigma in the group), keep the topk_group
+     best groups, all other experts are ineligible
+  5. top-k of sigma among the eligible experts, ties -> lower index
+  6. gates g_j = s_{idx_j} (unbiased), optionally divided by their sum, times
+     routed_scaling_factor
+  7. out_t = sum_j g_j * FFN_{idx_j}(u_t) + FFN_shared(u_t), FFN = SwiGLU,
+     no residual term.
+
+Sources (page title, section):
+  * "DeepSeek-V2" walkthrough (xingfushuangcheng.com): the DeepSeekMoE output
+    definition for token t, the ``MoEGate`` listing (fp32 linear gate, softmax
+    over all experts, greedy / group_limited_greedy, group score = max) and the
+    ``MoE`` listing (repeat per top-k slot, per-expert FFN, gate-weighted sum
+    plus the shared experts as one SwiGLU of hidden n_shared * I).
+  * "DeepSeek大模型架构解析：MLA注意力与MoE创新设计" (intelliparadigm.com),
+    section 3.3.1: SwiGLU = w2(silu(w1 x) * w3 x) with bias-free linears.
+  * "【多模态大模型面经】 DeepSeek专题： DeepSeekMOE + MLA" (Tencent Cloud),
+    router formula: p = softmax(W_gate x), y = sum over TopK(p) of p_i E_i(x).
+  * "【Deepseek基础篇】--v3基本架构" (nxbn.cn), section 1.2: a per-expert bias is
+    added to the affinity only to pick the top-K, gate values come from the
+    unbiased affinity; node-limited routing picks nodes by the sum of the
+    highest affinities on each node; no token is dropped.
+
+Readings where the pages are silent or garbled (all listed in the design doc):
+  * Decision precision.  The ``MoEGate`` listing holds logits and scores in
+    float32 and takes ``topk`` on them.  The oracle therefore computes the
+    affinities exactly (float64), rounds them once to float32, adds the float32
+    bias in float32, and makes every comparison (group choice, top-k) on those
+    float32 values.  Equal float32 values go to the lower index.
+  * Group score "sum_top" (V3 node-limited routing, count garbled on the page):
+    the sum of the top-m selection scores of the group, summed in float32 in
+    descending order.  m = k / topk_group in the V3-shaped workloads.
+  * Experts outside the kept groups are excluded outright (not zero-filled), so
+    a negative biased score can never pull in an expert from a dropped group.
+  * A token is a near tie when the k-th and (k+1)-th eligible selection scores
+    (or the topk_group-th and next group scores) differ by less than 1e-5 times
+    the largest |score| of that token; its expert set may legitimately differ
+    between two correct implementations.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+from typing import Callable, Optional, Sequence, Tuple
+
+import numpy as np
+
+NEAR_TIE_REL = 1e-5
+
+
+@dataclass
+class OracleConfig:
+    """Plain layer hyper-parameters, named as in the ``MoEGate`` / ``MoE`` listings."""
+
+    T: int
+    d: int
+    E: int                      # n_routed_experts
+    I: int                      # routed expert hidden size
+    k: int                      # num_experts_per_tok
+    n_shared: int               # shared experts, fused as one SwiGLU of hidden n_shared*I
+    score_fn: str = "softmax"   # "softmax" | "sigmoid"
+    topk_method: str = "greedy"  # "greedy" | "group_limited_greedy"
+    n_group: int = 1
+    topk_group: int = 1
+    group_score: str = "max"    # "max" | "sum_top"
+    group_top: int = 1          # m for "sum_top"
+    norm_topk: bool = False
+    routed_scaling_factor: float = 1.0
+
+
+@dataclass
+class Routing:
+    idx: np.ndarray        # [T,k] int64, ordered by selection score desc, then index asc
+    gates: np.ndarray      # [T,k] float64
+    scores: np.ndarray     # [T,E] float64 affinities s
+    sel32: np.ndarray      # [T,E] float32 selection scores (decision values)
+    near_tie: np.ndarray   # [T] bool
+    counts: np.ndarray     # [E] int64
+
+
+# --------------------------------------------------------------------- router
+
+def gate_logits(x: np.ndarray, wg: np.ndarray) -> np.ndarray:
+    """l = x W_g^T in float64 (``MoEGate.forward``: ``F.linear`` without bias)."""
+    return np.asarray(x, np.float64) @ np.asarray(wg, np.float64).T
+
+
+def affinities(logits: np.ndarray, score_fn: str) -> np.ndarray:
+    """Token-to-expert affinity s (``MoEGate.forward`` softmax over all experts;
+    the V3 page's sigmoid affinity)."""
+    logits = np.asarray(logits, np.float64)
+    if score_fn == "softmax":
+        z = logits - logits.max(axis=1, keepdims=True)
+        ez = np.exp(z)
+        return ez / ez.sum(axis=1, keepdims=True)
+    if score_fn == "sigmoid":
+        return 1.0 / (1.0 + np.exp(-logits))
+    raise ValueError(score_fn)
+
+
+def selection_scores32(s: np.ndarray, bias: Optional[np.ndarray]) -> np.ndarray:
+    """sigma = s + b, held in float32 as the gate listing holds its scores."""
+    s32 = np.asarray(s, np.float64).astype(np.float32)
+    if bias is None:
+        return s32
+    return (s32 + np.asarray(bias, np.float32)[None, :]).astype(np.float32)
+
+
+def _group_scores32(sel32: np.ndarray, cfg: OracleConfig) -> np.ndarray:
+    T, E = sel32.shape
+    grp = sel32.reshape(T, cfg.n_group, E // cfg.n_group)
+    if cfg.group_score == "max":
+        return grp.max(axis=2)
+    if cfg.group_score == "sum_top":
+        desc = -np.sort(-grp, axis=2)          # descending within each group
+        acc = desc[:, :, 0].astype(np.float32)
+        for m in range(1, cfg.group_top):
+            acc = (acc + desc[:, :, m]).astype(np.float32)
+        return acc
+    raise ValueError(cfg.group_score)
+
+
+def _group_scores64(sel64: np.ndarray, cfg: OracleConfig) -> np.ndarray:
+    T, E = sel64.shape
+    grp = sel64.reshape(T, cfg.n_group, E // cfg.n_group)
+    if cfg.group_score == "max":
+        return grp.max(axis=2)
+    desc = -np.sort(-grp, axis=2)
+    return desc[:, :, : cfg.group_top].sum(axis=2)
+
+
+def eligible_mask(sel32: np.ndarray, cfg: OracleConfig) -> Tuple[np.ndarray, np.ndarray]:
+    """Experts a token may pick, and the kept-group matrix [T, n_group].
+
+    greedy: every expert.  group_limited_greedy (``MoEGate`` listing; the V3
+    page's node-limited routing): keep the topk_group groups with the largest
+    group score, ties -> lower group index."""
+    T, E = sel32.shape
+    if cfg.topk_method == "greedy":
+        return np.ones((T, E), bool), np.ones((T, 1), bool)
+    if cfg.topk_method != "group_limited_greedy":
+        raise ValueError(cfg.topk_method)
+    gs = _group_scores32(sel32, cfg)
+    order = np.argsort(-gs, axis=1, kind="stable")   # stable: equal -> lower index first
+    kept = np.zeros_like(gs, dtype=bool)
+    rows = np.arange(T)[:, None]
+    kept[rows, order[:, : cfg.topk_group]] = True
+    return np.repeat(kept, E // cfg.n_group, axis=1), kept
+
+
+def route(logits: np.ndarray, bias: Optional[np.ndarray], cfg: OracleConfig) -> Routing:
+    """Router of one batch: affinities, (group-limited) top-k, gate values."""
+    s = affinities(logits, cfg.score_fn)
+    T, E = s.shape
+    sel32 = selection_scores32(s, bias)
+    elig, kept = eligible_mask(sel32, cfg)
+    key = np.where(elig, sel32.astype(np.float64), -np.inf)
+    order = np.argsort(-key, axis=1, kind="stable")
+    idx = order[:, : cfg.k].astype(np.int64)
+
+    # gate values from the unbiased affinity (V3 page, section 1.2)
+    rows = np.arange(T)[:, None]
+    g = s[rows, idx]
+    if cfg.norm_topk:
+        g = g / g.sum(axis=1, keepdims=True)
+    g = g * float(cfg.routed_scaling_factor)
+
+    # near ties, judged on exact float64 selection scores
+    sel64 = s + (0.0 if bias is None else np.asarray(bias, np.float64)[None, :])
+    scale = np.abs(sel64).max(axis=1)
+    near = np.zeros(T, bool)
+    n_elig = elig.sum(axis=1)
+    if cfg.k < E:
+        e64 = np.where(elig, sel64, -np.inf)
+        desc = -np.sort(-e64, axis=1)
+        has_next = n_elig > cfg.k
+        gap = np.where(has_next, desc[:, cfg.k - 1] - desc[:, cfg.k], np.inf)
+        near |= gap < NEAR_TIE_REL * scale
+    if cfg.topk_method == "group_limited_greedy" and cfg.topk_group < cfg.n_group:
+        g64 = -np.sort(-_group_scores64(sel64, cfg), axis=1)
+        ggap = g64[:, cfg.topk_group - 1] - g64[:, cfg.topk_group]
+        near |= ggap < NEAR_TIE_REL * scale
+    counts = np.bincount(idx.ravel(), minlength=E).astype(np.int64)
+    return Routing(idx=idx, gates=g, scores=s, sel32=sel32, near_tie=near, counts=counts)
+
+
+def route_tokens(x, wg, bias, cfg: OracleConfig) -> Routing:
+    return route(gate_logits(x, wg), bias, cfg)
+
+
+# ---------------------------------------------------------------- permutation
+
+def permutation(idx: np.ndarray, E: int):
+    """Expert-contiguous order of the T*k (token, slot) assignments.
+
+    Rows of expert e are its assignments in increasing token order (each token
+    picks an expert at most once), experts in increasing id; this is the
+    per-expert gather of the ``MoE`` listing made explicit.
+    Returns counts[E], offsets[E+1], row2tok[R], tok2row[T,k]."""
+    idx = np.asarray(idx)
+    T, k = idx.shape
+    counts = np.zeros(E, np.int64)
+    for e in idx.ravel():
+        counts[e] += 1
+    offsets = np.zeros(E + 1, np.int64)
+    offsets[1:] = np.cumsum(counts)
+    nxt = offsets[:-1].copy()
+    row2tok = np.zeros(T * k, np.int64)
+    tok2row = np.zeros((T, k), np.int64)
+    # counting sort: visiting assignments in (token, slot) order keeps each
+    # expert's rows in increasing token order
+    for t in range(T):
+        for j in range(k):
+            e = idx[t, j]
+            r = nxt[e]
+            nxt[e] += 1
+            row2tok[r] = t
+            tok2row[t, j] = r
+    return counts, offsets, row2tok, tok2row
+
+
+# -------------------------------------------------------------------- experts
+
+def silu(z: np.ndarray) -> np.ndarray:
+    return z / (1.0 + np.exp(-z))
+
+
+def swiglu_ffn(u: np.ndarray, w1: np.ndarray, w3: np.ndarray, w2: np.ndarray) -> np.ndarray:
+    """FFN(u) = W2 (silu(W1 u) * (W3 u)); nn.Linear layouts W1,W3 [h,d], W2 [d,h]
+    (intelliparadigm.com page, section 3.3.1)."""
+    u = np.asarray(u, np.float64)
+    a = u @ np.asarray(w1, np.float64).T
+    b = u @ np.asarray(w3, np.float64).T
+    return (silu(a) * b) @ np.asarray(w2, np.float64).T
+
+
+ExpertFn = Callable[[int], Tuple[np.ndarray, np.ndarray, np.ndarray]]
+
+
+def experts_forward(x: np.ndarray, idx: np.ndarray, gates: np.ndarray,
+                    expert: ExpertFn, shared: Optional[Tuple[np.ndarray, np.ndarray, np.ndarray]],
+                    E: int) -> np.ndarray:
+    """out_t = sum_j g_{t,j} FFN_{idx[t,j]}(x_t) + FFN_shared(x_t) (``MoE`` listing).
+
+    ``expert(e)`` returns expert e's (W1, W3, W2); only experts some token
+    picked are requested.  No residual term is added."""
+    x = np.asarray(x, np.float64)
+    T, d = x.shape
+    out = np.zeros((T, d), np.float64)
+    for e in range(E):
+        tok, slot = np.nonzero(idx == e)
+        if tok.size == 0:
+            continue
+        w1, w3, w2 = expert(e)
+        y = swiglu_ffn(x[tok], w1, w3, w2)
+        np.add.at(out, tok, gates[tok, slot][:, None] * y)
+    if shared is not None:
+        out += swiglu_ffn(x, *shared)
+    return out
+
+
+def moe_forward(x, wg, bias, expert: ExpertFn, shared, cfg: OracleConfig,
+                idx_override: Optional[np.ndarray] = None):
+    """Whole layer for the tokens in ``x``.  ``idx_override`` re-evaluates the
+    layer with another (equally valid) expert choice, used for near-tie tokens.
+    Returns (out [T,d] float64, Routing)."""
+    r = route_tokens(x, wg, bias, cfg)
+    idx, gates = r.idx, r.gates
+    if idx_override is not None:
+        idx = np.asarray(idx_override, np.int64)
+        rows = np.arange(idx.shape[0])[:, None]
+        gates = r.scores[rows, idx]
+        if cfg.norm_topk:
+            gates = gates / gates.sum(axis=1, keepdims=True)
+        gates = gates * float(cfg.routed_scaling_factor)
+    out = experts_forward(x, idx, gates, expert, shared, cfg.E)
+    return out, Routing(idx=idx, gates=gates, scores=r.scores, sel32=r.sel32,
+                        near_tie=r.near_tie, counts=np.bincount(idx.ravel(), minlength=cfg.E))
+
+
+def stacked_experts(w1: np.ndarray, w3: np.ndarray, w2: np.ndarray) -> ExpertFn:
+    """Expert accessor over stacked [E,I,d],[E,I,d],[E,d,I] arrays."""
+    return lambda e: (w1[e], w3[e], w2[e])
+
+
+def relative_error(got: np.ndarray, ref: np.ndarray) -> float:
+    """max |got - ref| / RMS(ref), the acceptance measure for layer outputs."""
+    ref = np.asarray(ref, np.float64)
+    got = np.asarray(got, np.float64)
+    rms = float(np.sqrt(np.mean(ref * ref)))
+    return float(np.max(np.abs(got - ref))) / max(rms, 1e-300)
+
+
+def is_valid_selection(idx_row: Sequence[int], sel32_row: np.ndarray, cfg: OracleConfig) -> bool:
+    """True when ``idx_row`` is a correct top-k choice up to the near-tie
+    tolerance: every picked expert is eligible under some near-optimal group
+    choice and no unpicked eligible expert beats a picked one by more than the
+    tolerance.  Used to accept the other side's choice on near-tie tokens."""
+    sel = np.asarray(sel32_row, np.float64)
+    picked = np.asarray(list(idx_row), np.int64)
+    if len(set(picked.tolist())) != cfg.k:
+        return False
+    tol = NEAR_TIE_REL * np.abs(sel).max()
+    if cfg.topk_method == "group_limited_greedy":
+        gsize = cfg.E // cfg.n_group
+        g = _group_scores64(sel[None, :], cfg)[0]
+        groups = sorted(set((picked // gsize).tolist()))
+        if len(groups) > cfg.topk_group:
+            return False
+        thresh = np.sort(g)[::-1][cfg.topk_group - 1]
+        if any(g[x] < thresh - tol for x in groups):
+            return False
+        kept = set(groups)
+        # pad the kept set with the best remaining groups
+        for gg in np.argsort(-g, kind="stable"):
+            if len(kept) >= cfg.topk_group:
+                break
+            kept.add(int(gg))
+        elig = np.array([(e // gsize) in kept for e in range(cfg.E)])
+    else:
+        elig = np.ones(cfg.E, bool)
+    worst_picked = sel[picked].min()
+    others = np.where(elig, sel, -np.inf)
+    others[picked] = -np.inf
+    return bool(others.max() <= worst_picked + tol)

@@ -1,0 +1,300 @@
+"""Checks that pin the fp64 oracle to facts outside itself.
+
+Every check raises AssertionError when the oracle disagrees with:
+  * brute-force enumeration of expert subsets and group subsets on tiny inputs,
+    with exact rational sums (Fractions) of the float32 decision values;
+  * invariants the method guarantees (k largest affinities, kept groups,
+    sum of counts, renormalised gate sum, zero gates -> shared FFN only);
+  * special cases that reduce to textbook forms written here with torch:
+    E=1/k=1 -> plain SwiGLU sum, k=E -> the dense einsum gate fusion of the
+    intelliparadigm.com page (section 3.3.3), k=1 -> the Top-1 MoE of the
+    Tencent Cloud page, greedy == torch.topk on float64 scores;
+  * symmetries: expert relabelling, token independence, linearity in W2.
+
+The independent pieces (softmax via scipy, SwiGLU via torch.nn.functional)
+never call the oracle's own helpers.  ``tests/test_oracle_mutations.py``
+plants plausible mistakes in the oracle and checks that these pins catch them.
+"""
+from dataclasses import replace
+from fractions import Fraction
+from itertools import combinations
+
+import numpy as np
+import scipy.special
+import torch
+import torch.nn.functional as F
+
+from oracle import moe_oracle as orc
+
+
+# ------------------------------------------------------------------ helpers
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+def independent_sel32(logits, score_fn, bias):
+    if score_fn == "softmax":
+        s = scipy.special.softmax(logits, axis=1)
+    else:
+        s = scipy.special.expit(logits)
+    s32 = s.astype(np.float32)
+    if bias is not None:
+        s32 = (s32 + bias.astype(np.float32)[None, :]).astype(np.float32)
+    return s, s32
+
+
+def torch_swiglu(x, w1, w3, w2):
+    x, w1, w3, w2 = (torch.as_tensor(a, dtype=torch.float64) for a in (x, w1, w3, w2))
+    return (F.silu(x @ w1.T) * (x @ w3.T)) @ w2.T
+
+
+def _brute_group_score(vals32, score, m):
+    if score == "max":
+        return Fraction(float(max(vals32)))
+    best = max(sum(Fraction(float(v)) for v in c) for c in combinations(vals32, m))
+    return Fraction(float(np.float32(float(best))))   # the float32 rounding of the exact best sum
+
+
+def brute_force_choice(sel_row, cfg):
+    """Best k-subset (max exact sum, then lexicographically smallest) inside the
+    best topk_group-subset of groups (same rule)."""
+    E = sel_row.size
+    if cfg.topk_method == "group_limited_greedy":
+        gs = E // cfg.n_group
+        gsc = [_brute_group_score(sel_row[g * gs:(g + 1) * gs], cfg.group_score, cfg.group_top)
+               for g in range(cfg.n_group)]
+        best = None
+        for c in combinations(range(cfg.n_group), cfg.topk_group):
+            key = (sum(gsc[g] for g in c), tuple(-g for g in c))
+            if best is None or key > best[0]:
+                best = (key, c)
+        elig = [e for e in range(E) if (e // gs) in best[1]]
+    else:
+        elig = list(range(E))
+    best = None
+    for c in combinations(elig, cfg.k):
+        key = (sum(Fraction(float(sel_row[e])) for e in c), tuple(-e for e in c))
+        if best is None or key > best[0]:
+            best = (key, c)
+    return set(best[1])
+
+
+def small_layer(seed, T, d, E, I, k, n_shared, **cfgkw):
+    r = _rng(seed)
+    cfg = orc.OracleConfig(T=T, d=d, E=E, I=I, k=k, n_shared=n_shared, **cfgkw)
+    x = r.standard_normal((T, d))
+    wg = r.uniform(-1, 1, (E, d)) / np.sqrt(d)
+    w1 = r.uniform(-1, 1, (E, I, d)) / np.sqrt(d)
+    w3 = r.uniform(-1, 1, (E, I, d)) / np.sqrt(d)
+    w2 = r.uniform(-1, 1, (E, d, I)) / np.sqrt(I)
+    Is = max(1, n_shared) * I
+    shared = (r.uniform(-1, 1, (Is, d)) / np.sqrt(d), r.uniform(-1, 1, (Is, d)) / np.sqrt(d),
+              r.uniform(-1, 1, (d, Is)) / np.sqrt(Is)) if n_shared > 0 else None
+    return cfg, x, wg, (w1, w3, w2), shared
+
+
+SELECTION_CASES = [
+    dict(E=8, k=2, score_fn="softmax", topk_method="greedy"),
+    dict(E=12, k=4, score_fn="softmax", topk_method="greedy"),
+    dict(E=16, k=3, score_fn="sigmoid", topk_method="greedy", bias=True),
+    dict(E=8, k=2, score_fn="softmax", topk_method="group_limited_greedy", n_group=4, topk_group=2,
+         group_score="max"),
+    dict(E=16, k=4, score_fn="sigmoid", topk_method="group_limited_greedy", n_group=4, topk_group=2,
+         group_score="sum_top", group_top=2, bias=True),
+    dict(E=12, k=3, score_fn="softmax", topk_method="group_limited_greedy", n_group=2, topk_group=1,
+         group_score="max"),
+    dict(E=16, k=1, score_fn="sigmoid", topk_method="group_limited_greedy", n_group=2, topk_group=1,
+         group_score="sum_top", group_top=2, bias=True),
+]
+
+
+# --------------------------------------------------------------------- pins
+
+def pin_brute_force_selection(o=orc, tokens=24):
+    for ci, case in enumerate(SELECTION_CASES):
+        case = dict(case)
+        use_bias = case.pop("bias", False)
+        E = case["E"]
+        cfg = orc.OracleConfig(T=tokens, d=1, I=1, n_shared=0, **case)
+        r = _rng(100 + ci)
+        # coarse logits make exact float32 ties common, exercising the tie rule
+        logits = r.integers(-3, 4, size=(tokens, E)).astype(np.float64) * 0.5
+        logits[: tokens // 2] += r.standard_normal((tokens // 2, E))
+        bias = (r.integers(-2, 3, size=E) * 0.05).astype(np.float32) if use_bias else None
+        s, sel32 = independent_sel32(logits, cfg.score_fn, bias)
+        got = o.route(logits, bias, cfg)
+        for t in range(tokens):
+            want = brute_force_choice(sel32[t], cfg)
+            assert set(got.idx[t].tolist()) == want, (ci, t, got.idx[t], sorted(want))
+            keys = [(-float(sel32[t, e]), e) for e in got.idx[t]]
+            assert keys == sorted(keys), ("order", ci, t, got.idx[t])
+
+
+def pin_greedy_is_torch_topk(o=orc):
+    r = _rng(7)
+    for E, k, fn in [(12, 4, "softmax"), (64, 6, "softmax"), (256, 8, "sigmoid")]:
+        logits = r.standard_normal((50, E))
+        cfg = orc.OracleConfig(T=50, d=1, E=E, I=1, k=k, n_shared=0, score_fn=fn)
+        s = torch.softmax(torch.tensor(logits), dim=1) if fn == "softmax" else torch.sigmoid(torch.tensor(logits))
+        want = torch.topk(s, k, dim=1).indices.numpy()
+        got = o.route(logits, None, cfg).idx
+        for t in range(50):
+            assert set(got[t].tolist()) == set(want[t].tolist()), (E, t)
+
+
+def pin_invariants(o=orc):
+    r = _rng(11)
+    T = 40
+    for case in [dict(E=12, k=4, score_fn="softmax"),
+                 dict(E=32, k=6, score_fn="softmax", topk_method="group_limited_greedy", n_group=8,
+                      topk_group=3, group_score="max", routed_scaling_factor=16.0),
+                 dict(E=32, k=8, score_fn="sigmoid", topk_method="group_limited_greedy", n_group=8,
+                      topk_group=4, group_score="sum_top", group_top=2, norm_topk=True,
+                      routed_scaling_factor=2.5, bias=True)]:
+        case = dict(case)
+        use_bias = case.pop("bias", False)
+        E, k = case["E"], case["k"]
+        cfg = orc.OracleConfig(T=T, d=1, I=1, n_shared=0, **case)
+        logits = r.standard_normal((T, E))
+        bias = (r.standard_normal(E) * 0.1).astype(np.float32) if use_bias else None
+        s, sel32 = independent_sel32(logits, cfg.score_fn, bias)
+        got = o.route(logits, bias, cfg)
+        # counts
+        assert int(got.counts.sum()) == T * k
+        assert np.array_equal(got.counts, np.bincount(got.idx.ravel(), minlength=E))
+        # distinct experts per token
+        assert all(len(set(row.tolist())) == k for row in got.idx)
+        if cfg.topk_method == "group_limited_greedy":
+            gsz = E // cfg.n_group
+            st = torch.tensor(sel32.astype(np.float64)).view(T, cfg.n_group, gsz)
+            gsc = st.max(-1).values if cfg.group_score == "max" else st.topk(cfg.group_top, -1).values.sum(-1)
+            best = torch.topk(gsc, cfg.topk_group, dim=1).indices.numpy()
+            for t in range(T):
+                assert set((got.idx[t] // gsz).tolist()) <= set(best[t].tolist()), t
+        elif bias is None:
+            for t in range(T):
+                assert np.allclose(np.sort(s[t, got.idx[t]]), np.sort(s[t])[-k:], rtol=0, atol=0)
+        g = got.gates
+        scale = cfg.routed_scaling_factor
+        if cfg.norm_topk:
+            assert np.allclose(g.sum(1), scale, rtol=1e-12, atol=0)
+        else:
+            assert (g <= scale * (1 + 1e-12)).all() and (g.sum(1) <= scale * (1 + 1e-12)).all()
+        assert (g > 0).all()
+
+
+def pin_bias_only_steers_selection(o=orc):
+    """With a bias that does not change the chosen set, gates are unchanged."""
+    r = _rng(12)
+    T, E = 60, 32
+    cfg = orc.OracleConfig(T=T, d=1, E=E, I=1, k=8, n_shared=0, score_fn="sigmoid",
+                           topk_method="group_limited_greedy", n_group=8, topk_group=4,
+                           group_score="sum_top", group_top=2, norm_topk=True, routed_scaling_factor=2.5)
+    logits = r.standard_normal((T, E))
+    bias = (r.standard_normal(E) * 0.02).astype(np.float32)
+    a = o.route(logits, None, cfg)
+    b = o.route(logits, bias, cfg)
+    same = 0
+    for t in range(T):
+        if set(a.idx[t].tolist()) == set(b.idx[t].tolist()):
+            same += 1
+            ga = dict(zip(a.idx[t].tolist(), a.gates[t].tolist()))
+            gb = dict(zip(b.idx[t].tolist(), b.gates[t].tolist()))
+            for e in ga:
+                assert abs(ga[e] - gb[e]) <= 1e-12 * abs(ga[e]), (t, e)
+    assert same > T // 4
+
+
+def pin_zero_gates_give_shared(o=orc):
+    cfg, x, wg, (w1, w3, w2), shared = small_layer(3, 20, 16, 12, 8, 4, 2)
+    cfg = replace(cfg, routed_scaling_factor=0.0)
+    out, _ = o.moe_forward(x, wg, None, orc.stacked_experts(w1, w3, w2), shared, cfg)
+    want = torch_swiglu(x, *shared).numpy()
+    assert np.allclose(out, want, rtol=1e-12, atol=1e-14)
+
+
+def pin_group1_is_greedy(o=orc):
+    r = _rng(13)
+    logits = r.standard_normal((30, 16))
+    a = o.route(logits, None, orc.OracleConfig(T=30, d=1, E=16, I=1, k=4, n_shared=0))
+    b = o.route(logits, None, orc.OracleConfig(T=30, d=1, E=16, I=1, k=4, n_shared=0,
+                                               topk_method="group_limited_greedy", n_group=1, topk_group=1))
+    assert np.array_equal(a.idx, b.idx) and np.allclose(a.gates, b.gates, rtol=0, atol=0)
+
+
+def pin_single_expert(o=orc):
+    cfg, x, wg, (w1, w3, w2), shared = small_layer(4, 10, 12, 1, 6, 1, 2)
+    out, r = o.moe_forward(x, wg, None, orc.stacked_experts(w1, w3, w2), shared, cfg)
+    want = (torch_swiglu(x, w1[0], w3[0], w2[0]) + torch_swiglu(x, *shared)).numpy()
+    assert np.allclose(out, want, rtol=1e-12, atol=1e-13)
+
+
+def pin_dense_einsum(o=orc):
+    """k = E with softmax and scale 1: the dense gate fusion einsum('ted,te->td')."""
+    cfg, x, wg, (w1, w3, w2), shared = small_layer(5, 12, 10, 6, 7, 6, 1)
+    out, _ = o.moe_forward(x, wg, None, orc.stacked_experts(w1, w3, w2), shared, cfg)
+    xt = torch.tensor(x)
+    p = torch.softmax(xt @ torch.tensor(wg).T, dim=-1)
+    ys = torch.stack([torch_swiglu(x, w1[e], w3[e], w2[e]) for e in range(6)], dim=1)   # [T,E,d]
+    want = torch.einsum("ted,te->td", ys, p) + torch_swiglu(x, *shared)
+    assert np.allclose(out, want.numpy(), rtol=1e-11, atol=1e-13)
+
+
+def pin_top1(o=orc):
+    """k = 1: out = p_max * E_argmax(x) (+ shared), the Top-1 gated MoE."""
+    cfg, x, wg, (w1, w3, w2), shared = small_layer(6, 16, 8, 5, 4, 1, 1)
+    out, _ = o.moe_forward(x, wg, None, orc.stacked_experts(w1, w3, w2), shared, cfg)
+    xt = torch.tensor(x)
+    p = torch.softmax(xt @ torch.tensor(wg).T, dim=-1)
+    top_p, top_i = p.max(dim=-1)
+    want = torch_swiglu(x, *shared).clone()
+    for t in range(x.shape[0]):
+        e = int(top_i[t])
+        want[t] += top_p[t] * torch_swiglu(x[t:t + 1], w1[e], w3[e], w2[e])[0]
+    assert np.allclose(out, want.numpy(), rtol=1e-12, atol=1e-13)
+
+
+def pin_permutation(o=orc):
+    r = _rng(14)
+    T, E, k = 37, 9, 3
+    idx = np.stack([r.choice(E, k, replace=False) for _ in range(T)])
+    counts, offsets, row2tok, tok2row = o.permutation(idx, E)
+    flat = idx.ravel()
+    order = np.argsort(flat, kind="stable")        # sorted by expert, stable in (t, j)
+    assert np.array_equal(row2tok, order // k)
+    assert np.array_equal(counts, np.bincount(flat, minlength=E))
+    assert offsets[0] == 0 and np.array_equal(np.diff(offsets), counts)
+    inv = np.empty_like(order)
+    inv[order] = np.arange(order.size)
+    assert np.array_equal(tok2row.ravel(), inv)
+
+
+def pin_symmetries(o=orc):
+    cfg, x, wg, (w1, w3, w2), shared = small_layer(8, 24, 16, 8, 12, 3, 1,
+                                                    score_fn="sigmoid", norm_topk=True,
+                                                    routed_scaling_factor=2.5,
+                                                    topk_method="group_limited_greedy", n_group=2,
+                                                    topk_group=1, group_score="sum_top", group_top=2)
+    bias = (_rng(9).standard_normal(8) * 0.1).astype(np.float32)
+    out, r = o.moe_forward(x, wg, bias, orc.stacked_experts(w1, w3, w2), shared, cfg)
+    # relabel experts inside each group (groups keep their members)
+    perm = np.array([3, 1, 0, 2, 6, 7, 5, 4])
+    out2, r2 = o.moe_forward(x, wg[perm], bias[perm], orc.stacked_experts(w1[perm], w3[perm], w2[perm]),
+                             shared, cfg)
+    assert np.allclose(out, out2, rtol=1e-12, atol=1e-13)
+    for t in range(cfg.T):
+        assert set(perm[r2.idx[t]].tolist()) == set(r.idx[t].tolist())   # new id e' is old id perm[e']
+    # token independence
+    sub = np.array([5, 0, 17, 3])
+    out3, _ = o.moe_forward(x[sub], wg, bias, orc.stacked_experts(w1, w3, w2), shared, replace(cfg, T=4))
+    assert np.allclose(out3, out[sub], rtol=1e-12, atol=1e-13)
+    # linear in W2 and W2_s together
+    out4, _ = o.moe_forward(x, wg, bias, orc.stacked_experts(w1, w3, 2.0 * w2),
+                            (shared[0], shared[1], 2.0 * shared[2]), cfg)
+    assert np.allclose(out4, 2.0 * out, rtol=1e-12, atol=1e-13)
+
+
+ALL_PINS = [pin_brute_force_selection, pin_greedy_is_torch_topk, pin_invariants,
+            pin_bias_only_steers_selection, pin_zero_gates_give_shared, pin_group1_is_greedy,
+            pin_single_expert, pin_dense_einsum, pin_top1, pin_permutation, pin_symmetries]

@@ -1,0 +1,110 @@
+"""Plant plausible mistakes in the oracle (CPU only) and check a pin catches each.
+
+A pin set that passes a broken oracle proves nothing; each mutant below is a
+mistake someone could make while writing the oracle from the pages."""
+from dataclasses import replace
+
+import numpy as np
+import pytest
+
+from oracle import moe_oracle as orc
+from tests import oracle_pins as pins
+
+_real_route = orc.route
+_real_swiglu = orc.swiglu_ffn
+_real_experts_forward = orc.experts_forward
+_real_permutation = orc.permutation
+
+
+def _route_ties_high(logits, bias, cfg):
+    # evaluate on reversed expert ids: equal scores now go to the higher index
+    rb = None if bias is None else bias[::-1].copy()
+    r = _real_route(logits[:, ::-1].copy(), rb, cfg)
+    r.idx = cfg.E - 1 - r.idx
+    return r
+
+
+def _route_biased_gates(logits, bias, cfg):
+    r = _real_route(logits, bias, cfg)
+    rows = np.arange(r.idx.shape[0])[:, None]
+    g = r.sel32.astype(np.float64)[rows, r.idx]
+    if cfg.norm_topk:
+        g = g / g.sum(1, keepdims=True)
+    r.gates = g * cfg.routed_scaling_factor
+    return r
+
+
+def _route_no_renorm(logits, bias, cfg):
+    return _real_route(logits, bias, replace(cfg, norm_topk=False))
+
+
+def _route_softmax_over_selected(logits, bias, cfg):
+    r = _real_route(logits, bias, cfg)
+    rows = np.arange(r.idx.shape[0])[:, None]
+    sel = np.asarray(logits)[rows, r.idx]
+    e = np.exp(sel - sel.max(1, keepdims=True))
+    r.gates = e / e.sum(1, keepdims=True) * cfg.routed_scaling_factor
+    return r
+
+
+def _route_strided_groups(logits, bias, cfg):
+    # groups taken as e % n_group instead of contiguous blocks
+    E, G = cfg.E, cfg.n_group
+    perm = np.arange(E).reshape(E // G, G).T.ravel()
+    rb = None if bias is None else bias[perm].copy()
+    r = _real_route(np.asarray(logits)[:, perm], rb, cfg)
+    r.idx = perm[r.idx]
+    return r
+
+
+def _group_score_sum_all(sel32, cfg):
+    T, E = sel32.shape
+    return sel32.reshape(T, cfg.n_group, E // cfg.n_group).sum(axis=2).astype(np.float32)
+
+
+def _swiglu_swapped(u, w1, w3, w2):
+    return _real_swiglu(u, w3, w1, w2)
+
+
+def _swiglu_no_gate(u, w1, w3, w2):
+    u = np.asarray(u, np.float64)
+    return (orc.silu(u @ np.asarray(w1).T)) @ np.asarray(w2).T
+
+
+def _experts_no_shared(x, idx, gates, expert, shared, E):
+    return _real_experts_forward(x, idx, gates, expert, None, E)
+
+
+def _experts_with_residual(x, idx, gates, expert, shared, E):
+    return _real_experts_forward(x, idx, gates, expert, shared, E) + np.asarray(x, np.float64)
+
+
+def _permutation_reversed(idx, E):
+    counts, offsets, row2tok, tok2row = _real_permutation(idx, E)
+    row2tok = row2tok.copy()
+    for e in range(E):
+        a, b = offsets[e], offsets[e + 1]
+        row2tok[a:b] = row2tok[a:b][::-1]
+    return counts, offsets, row2tok, tok2row
+
+
+MUTANTS = [
+    ("route", _route_ties_high, pins.pin_brute_force_selection),
+    ("route", _route_biased_gates, pins.pin_bias_only_steers_selection),
+    ("route", _route_no_renorm, pins.pin_invariants),
+    ("route", _route_softmax_over_selected, pins.pin_top1),
+    ("route", _route_strided_groups, pins.pin_brute_force_selection),
+    ("_group_scores32", _group_score_sum_all, pins.pin_brute_force_selection),
+    ("swiglu_ffn", _swiglu_swapped, pins.pin_single_expert),
+    ("swiglu_ffn", _swiglu_no_gate, pins.pin_dense_einsum),
+    ("experts_forward", _experts_no_shared, pins.pin_zero_gates_give_shared),
+    ("experts_forward", _experts_with_residual, pins.pin_zero_gates_give_shared),
+    ("permutation", _permutation_reversed, pins.pin_permutation),
+]
+
+
+@pytest.mark.parametrize("attr,mutant,pin", MUTANTS, ids=[m[1].__name__ for m in MUTANTS])
+def test_pin_catches_mutant(monkeypatch, attr, mutant, pin):
+    monkeypatch.setattr(orc, attr, mutant)
+    with pytest.raises(AssertionError):
+        pin()

@@ -1,0 +1,412 @@
+#!/usr/bin/env python3
+"""Benchmark of the DeepSeekMoE layer forward on B300.
+
+One step = one whole layer forward (router, permutation, grouped SwiGLU
+experts, shared expert, combine) over one batch of seeded synthetic tokens,
+through the library's C ABI (moe_forward).  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the fp64 CPU oracle on host cores
+
+Multi-GPU (torchrun, one process per GPU): every rank runs its own replica of
+the layer on its own batch (tokens are independent, no collective on the
+data path); the value is all ranks' tokens over the slowest rank's time.
+"""
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from mixture_experts_layer_85_b300 import inputs  # noqa: E402
+
+METRIC = "routed tokens/s per MoE layer fwd"
+UNIT = "tokens/s"
+DEFAULT_WORKLOAD = "v3_prefill_t16384"
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(inputs.WORKLOADS))
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-sample", type=int, default=0, help="tokens in the oracle's timed sample (0 = auto)")
+    return p.parse_args(argv)
+
+
+# ------------------------------------------------------------------ ranks
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    """The slowest rank's time (every rank gets the same answer)."""
+    if world <= 1:
+        return value
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, world: int, seconds_max: float) -> float:
+    return units_per_rank * world / seconds_max
+
+
+# ----------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms in the background."""
+
+    FIELDS = ("index,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self):
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "200", "-f", self.path], stdout=subprocess.DEVNULL,
+                                         stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        uuid = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
+        except Exception:
+            pass
+        rows = []
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 10:
+                continue
+            if uuid and uuid not in f[1] and f[1].replace("GPU-", "") not in uuid:
+                continue
+            rows.append(f)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        mx = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[6 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max(float(r[4]) for r in rows if r[4].replace(".", "").isdigit())
+                if any(r[4].replace(".", "").isdigit() for r in rows) else None}
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        p = json.load(open(path))
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained", p["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "source": "fallback"}
+
+
+# --------------------------------------------------------- algorithmic work
+
+def layer_bytes(wl, counts: np.ndarray) -> float:
+    """Bytes the method must move: x in, out, W_g, idx/w, the weights of the
+    experts that received tokens, the shared weights."""
+    eb = 2 if wl.act_dtype == "bf16" else 4
+    gb = 2 if wl.gate_w_dtype == "bf16" else 4
+    touched = int((counts > 0).sum())
+    return (2 * wl.T * wl.d * eb + wl.E * wl.d * gb + wl.T * wl.k * 8
+            + touched * 3 * wl.d * wl.I * eb + 3 * wl.d * wl.I_s * eb)
+
+
+def gemm1_work(wl, counts: np.ndarray):
+    """(FLOPs, algorithmic bytes) of GEMM1 + SwiGLU: x rows of every routed
+    assignment and every token (shared), the W1/W3 rows of touched experts and
+    of the shared expert, H written."""
+    eb = 2 if wl.act_dtype == "bf16" else 4
+    flops = 2.0 * wl.R * wl.d * 2 * wl.I + 2.0 * wl.T * wl.d * 2 * wl.I_s
+    touched = int((counts > 0).sum())
+    byts = ((wl.R + wl.T) * wl.d * eb + touched * 2 * wl.I * wl.d * eb + 2 * wl.I_s * wl.d * eb
+            + (wl.R * wl.I + wl.T * wl.I_s) * eb)
+    return flops, byts
+
+
+# ----------------------------------------------------------- oracle timing
+
+def oracle_sample_size(wl, requested: int) -> int:
+    if requested > 0:
+        return min(requested, wl.T)
+    if wl.d >= 7168:
+        return min(wl.T, 8)
+    if wl.d >= 2048:
+        return min(wl.T, 16)
+    return wl.T
+
+
+def oracle_cfg(wl):
+    from oracle import moe_oracle as orc
+    return orc.OracleConfig(T=wl.T, d=wl.d, E=wl.E, I=wl.I, k=wl.k, n_shared=wl.n_shared, score_fn=wl.score_fn,
+                            topk_method=wl.topk_method, n_group=wl.n_group, topk_group=wl.topk_group,
+                            group_score=wl.group_score, group_top=wl.group_top, norm_topk=wl.norm_topk,
+                            routed_scaling_factor=wl.routed_scaling_factor)
+
+
+def time_oracle(wl, li, tokens: np.ndarray):
+    """Seconds the fp64 oracle takes for the layer on `tokens` (weights are read
+    per expert from wherever they live and widened to float64)."""
+    from oracle import moe_oracle as orc
+
+    def f64(t):
+        return t.detach().to("cpu").to(torch.float64).numpy()
+
+    cfg = oracle_cfg(wl)
+    cfg.T = int(tokens.size)
+    x = f64(li.x)[tokens]
+    wg = f64(li.wg)
+    bias = None if li.bias is None else li.bias.detach().cpu().float().numpy()
+
+    def expert(e):
+        return f64(li.w1[e]), f64(li.w3[e]), f64(li.w2[e])
+
+    shared = None if wl.n_shared == 0 else (f64(li.ws1), f64(li.ws3), f64(li.ws2))
+    t0 = time.perf_counter()
+    orc.moe_forward(x, wg, bias, expert, shared, cfg)
+    return time.perf_counter() - t0
+
+
+def host_threads() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# ---------------------------------------------------------------- our arm
+
+def run_ours(args, world, rank):
+    from mixture_experts_layer_85_b300 import _lib
+    from mixture_experts_layer_85_b300.layer import MoELayer
+
+    wl = inputs.WORKLOADS[args.workload]
+    dev = torch.device("cuda", torch.cuda.current_device())
+    li = inputs.make_inputs(wl, dev)
+    layer = MoELayer(wl, li, dev)
+    x = li.x
+    out = torch.empty((wl.T, wl.d), dtype=x.dtype, device=dev)
+    counts = torch.empty((wl.E,), dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    for _ in range(max(args.warmup, 0)):
+        layer.forward(x, out, counts=counts)
+    code, word = layer.device_status()
+    if code != 0:
+        raise RuntimeError(f"device status after warm-up: {_lib.moe_status_string(code)} ({word})")
+    torch.cuda.synchronize()
+
+    K = args.steps
+    S = _lib.MOE_FORWARD_STAGES
+    stage_ev = [torch.cuda.Event(enable_timing=True) for _ in range(K * (S + 1))]
+    _lib.moe_profile_arm(stage_ev)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler()
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    launches0 = _lib.moe_launch_count()
+    t_start.record(stream)
+    for _ in range(K):
+        layer.forward(x, out, counts=counts)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    launches = _lib.moe_launch_count() - launches0
+    barrier(world)
+    clk = clocks.stop()
+    _lib.moe_profile_arm(None)
+    code, word = layer.device_status()
+    if code != 0:
+        raise RuntimeError(f"device status after timed steps: {_lib.moe_status_string(code)} ({word})")
+
+    elapsed_s = t_start.elapsed_time(t_end) / 1e3
+    elapsed_max = max_over_ranks(elapsed_s, world)
+    value = whole_job_rate(wl.T * K, world, elapsed_max)
+    stage_ms = {}
+    for s in range(S):
+        v = [stage_ev[i * (S + 1) + s].elapsed_time(stage_ev[i * (S + 1) + s + 1]) for i in range(K)]
+        stage_ms[_lib.moe_forward_stage_name(s)] = sum(v) / len(v)
+
+    cnt = counts.cpu().numpy()
+    peaks = measured_peaks()
+    ms_step = elapsed_s * 1e3 / K
+    flops = wl.flops()
+    byts = layer_bytes(wl, cnt)
+    g1_flops, g1_bytes = gemm1_work(wl, cnt)
+    g1_s = stage_ms["gemm1_swiglu"] / 1e3
+    ridge = peaks["bf16_tflops_sustained"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    if g1_flops / g1_bytes >= ridge:
+        achieved = g1_flops / g1_s / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops_sustained"],
+                "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops_sustained"], 4),
+                "frac_of_burst_peak": round(achieved / peaks["bf16_tflops"], 4)}
+    else:
+        achieved = g1_bytes / g1_s / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(achieved / peaks["hbm_gbs"], 4)}
+    roof.update({"kernel": "grouped_gemm_kernel<EPI_SWIGLU> (GEMM1 + SwiGLU)", "traffic": None,
+                 "peak_source": peaks["source"] + (" sustained bf16" if roof["bound"] == "tensor" else " HBM copy"),
+                 "per_launch_flops": g1_flops, "per_launch_algorithmic_bytes": g1_bytes,
+                 "avg_launch_ms": round(stage_ms["gemm1_swiglu"], 4)})
+
+    # end to end through the C ABI with host buffers: H2D of x, forward, D2H of out
+    x_h = x.cpu().pin_memory()
+    out_h = torch.empty((wl.T, wl.d), dtype=x.dtype).pin_memory()
+    x_d = torch.empty_like(x)
+    for _ in range(2):
+        x_d.copy_(x_h, non_blocking=True)
+        layer.forward(x_d, out)
+        out_h.copy_(out, non_blocking=True)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    e0.record(stream)
+    for _ in range(K):
+        x_d.copy_(x_h, non_blocking=True)
+        layer.forward(x_d, out)
+        out_h.copy_(out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_s = max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
+    eb = x.element_size()
+    e2e = {"value": round(whole_job_rate(wl.T * K, world, e2e_s), 1), "unit": UNIT,
+           "h2d_bytes_per_step": wl.T * wl.d * eb, "d2h_bytes_per_step": wl.T * wl.d * eb}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        S_tok = oracle_sample_size(wl, args.cpu_sample)
+        toks = np.sort(np.random.default_rng(0).choice(wl.T, S_tok, replace=False))
+        secs = time_oracle(wl, li, toks)
+        cpu = {"value": round(S_tok / secs, 3), "unit": UNIT, "cores": torch.get_num_threads(),
+               "host_cpus": host_threads(), "kind": "oracle",
+               "sample": f"{S_tok} seeded tokens of {wl.name} through the fp64 oracle (routing + experts + shared), "
+                         f"{secs:.1f} s"}
+
+    res = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if wl.act_dtype == "bf16" else "f32", "data": "synthetic",
+        "config": {"workload": wl.name, "T": wl.T, "d": wl.d, "E": wl.E, "I": wl.I, "k": wl.k,
+                   "n_shared": wl.n_shared, "router": f"{wl.score_fn}/{wl.topk_method}",
+                   "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (expert weights and token batch exceed 126 MB)"
+                   if wl.T * wl.d * 2 > 126e6 or wl.T >= 512 else "weights larger than L2; no flush"},
+        "tflops": round(flops / (elapsed_s / K) / 1e12, 2),
+        "tflops_frac_of_peak": {"burst": round(flops / (elapsed_s / K) / 1e12 / peaks["bf16_tflops"], 4),
+                                "sustained": round(flops / (elapsed_s / K) / 1e12 / peaks["bf16_tflops_sustained"], 4)},
+        "gbs_algorithmic": round(byts / (elapsed_s / K) / 1e9, 1),
+        "gbs_frac_of_hbm": round(byts / (elapsed_s / K) / 1e9 / peaks["hbm_gbs"], 4),
+        "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()},
+        "experts_touched": int((cnt > 0).sum()),
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": int(launches),
+        "clocks": clk,
+    }
+    return res
+
+
+# ----------------------------------------------------------- reference arm
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return None
+    wl = inputs.WORKLOADS[args.workload]
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    li = inputs.make_inputs(wl, "cpu", expert_device=dev)
+    S_tok = oracle_sample_size(wl, args.cpu_sample if args.cpu_sample else (4 if wl.d >= 7168 else 0))
+    rng = np.random.default_rng(1)
+    for _ in range(max(args.warmup, 0)):
+        time_oracle(wl, li, np.sort(rng.choice(wl.T, S_tok, replace=False)))
+    total = 0.0
+    for _ in range(args.steps):
+        total += time_oracle(wl, li, np.sort(rng.choice(wl.T, S_tok, replace=False)))
+    value = S_tok * args.steps / total
+    cpu = {"value": round(value, 3), "unit": UNIT, "cores": torch.get_num_threads(), "host_cpus": host_threads(),
+           "kind": "oracle", "sample": f"{S_tok} seeded tokens of {wl.name} per step through the fp64 oracle"}
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total / args.steps * 1e3, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "T": wl.T, "d": wl.d, "E": wl.E, "I": wl.I, "k": wl.k,
+                   "n_shared": wl.n_shared, "router": f"{wl.score_fn}/{wl.topk_method}",
+                   "parallelism": "host cores"},
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    world, rank, _ = dist_setup()
+    if args.impl == "reference":
+        res = run_reference(args, world, rank)
+    else:
+        if not torch.cuda.is_available():
+            raise SystemExit("bench.py needs a CUDA GPU for --impl ours")
+        res = run_ours(args, world, rank)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,175 @@
+/*
+ * moe.h - C ABI of the DeepSeekMoE layer forward on one B300 GPU (sm_103a).
+ *
+ * The layer (DeepSeek-V2 walkthrough, "DeepSeekMoE" output definition and the
+ * MoEGate / MoE listings; V3 architecture page, section 1.2):
+ *
+ *   h'_t = sum_{j<k} g_{t,j} * FFN_{idx_{t,j}}(u_t) + FFN_shared(u_t)
+ *   FFN(u) = W2 (silu(W1 u) * (W3 u))                      (SwiGLU, no bias)
+ *
+ * with idx/g from the router: logits = u W_g^T, s = softmax (over all E) or
+ * sigmoid, selection score s + b (b steers selection only), greedy or
+ * group-limited top-k, g = s_idx (optionally renormalised) * scale.
+ * No residual term is added.
+ *
+ * Conventions shared by every call:
+ *  - All tensor pointers are DEVICE pointers, owned by the caller, 16-byte
+ *    aligned, dense row-major.  Weights use the nn.Linear layout (out x in).
+ *    The library never allocates or frees device memory.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream).  Arguments are validated on the host first; on any error the call
+ *    returns a non-zero moe_status and launches nothing.
+ *  - `ws` is the caller's workspace of at least moe_workspace_size() bytes.
+ *    Each compute call clears and then uses a device status word at its start;
+ *    moe_get_device_status() reads it (bounds violations, device-side wait
+ *    time-outs).  Kernels never trap or assert.
+ *  - Two calls sharing one `ws` must not run concurrently.
+ *  - Activation dtype (x, permuted rows, outputs) is cfg->act_dtype: MOE_F32
+ *    runs SIMT fp32 kernels; MOE_BF16 runs the tcgen05 tensor-core kernels
+ *    with fp32 accumulation.
+ */
+#ifndef MOE_B300_H
+#define MOE_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum moe_status {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,     /* null / misaligned pointer, bad size or enum   */
+  MOE_ERR_UNSUPPORTED = 2,     /* valid layer the kernels do not handle          */
+  MOE_ERR_WORKSPACE = 3,       /* ws or packed buffer smaller than required      */
+  MOE_ERR_CUDA = 4,            /* a CUDA runtime call or kernel launch failed    */
+  MOE_ERR_DEVICE_TIMEOUT = 5,  /* a device-side wait gave up (status word)       */
+  MOE_ERR_DEVICE_BOUNDS = 6    /* a device-side index was out of range           */
+} moe_status;
+
+typedef enum moe_dtype { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
+typedef enum moe_score_fn { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 } moe_score_fn;
+typedef enum moe_topk_method { MOE_TOPK_GREEDY = 0, MOE_TOPK_GROUP_LIMITED = 1 } moe_topk_method;
+typedef enum moe_group_score { MOE_GROUP_MAX = 0, MOE_GROUP_SUM_TOP = 1 } moe_group_score;
+
+/* Layer hyper-parameters (names of the MoEGate / MoE listings).
+ *   T tokens, d model dim, E routed experts (n_routed_experts), I routed
+ *   expert hidden size, k = num_experts_per_tok, n_shared shared experts fused
+ *   as one SwiGLU of hidden I_s = n_shared * I.
+ *   Group-limited routing: E/n_group contiguous experts per group; the group
+ *   score is the max selection score (MOE_GROUP_MAX, DeepSeek-V2) or the sum of
+ *   the group_top largest ones (MOE_GROUP_SUM_TOP, the V3 node-limited rule);
+ *   the topk_group best groups stay eligible.  norm_topk = 1 divides the k
+ *   gates by their sum; routed_scaling_factor multiplies them. */
+typedef struct moe_config {
+  int32_t T, d, E, I, k, n_shared;
+  int32_t score_fn;        /* moe_score_fn    */
+  int32_t topk_method;     /* moe_topk_method */
+  int32_t n_group, topk_group;
+  int32_t group_score;     /* moe_group_score */
+  int32_t group_top;
+  int32_t norm_topk;
+  float routed_scaling_factor;
+  int32_t act_dtype;       /* moe_dtype of x, experts, outputs */
+  int32_t gate_w_dtype;    /* moe_dtype of W_g                 */
+} moe_config;
+
+/* Bytes of workspace every compute call needs for `cfg`. */
+MOE_API moe_status moe_workspace_size(const moe_config* cfg, size_t* bytes);
+
+/* Bytes of the packed expert blob moe_prepack_experts() writes for `cfg`. */
+MOE_API moe_status moe_packed_size(const moe_config* cfg, size_t* bytes);
+
+/* Re-lays the expert weights for the grouped GEMMs (MoE listing: E routed
+ * SwiGLU experts + one shared SwiGLU of hidden I_s).
+ *   W1, W3 [E,I,d], W2 [E,d,I]; Ws1, Ws3 [I_s,d], Ws2 [d,I_s]; act_dtype.
+ *   `packed` (>= moe_packed_size bytes) receives W1/W3 rows interleaved in
+ *   blocks so that one 256-wide GEMM tile holds matching gate and up rows, and
+ *   copies of W2 / Ws2.  Inputs may be freed once the stream reaches this call. */
+MOE_API moe_status moe_prepack_experts(const moe_config* cfg, const void* W1, const void* W3, const void* W2,
+                               const void* Ws1, const void* Ws3, const void* Ws2,
+                               void* packed, size_t packed_bytes, void* stream);
+
+/* Router (MoEGate.forward; V3 page section 1.2 for the sigmoid score and the
+ * selection-only bias).
+ *   x [T,d] act_dtype, Wg [E,d] gate_w_dtype, bias [E] fp32 or NULL.
+ *   idx [T,k] int32 out: chosen experts ordered by selection score desc, ties
+ *   to the lower index; w [T,k] fp32 out: gate values.  Logits are fp32-exact:
+ *   bf16 x times a bf16 (or 3-way bf16-split fp32) W_g on the tensor cores
+ *   with fp32 accumulation, or SIMT fp32. */
+MOE_API moe_status moe_gate_topk(const moe_config* cfg, const void* x, const void* Wg, const float* bias,
+                         int32_t* idx, float* w, void* ws, size_t ws_bytes, void* stream);
+
+/* Dispatch (MoE listing: repeat each token k times, group rows by expert).
+ *   idx [T,k] in.  counts [E] out; offsets [E+1] out (exclusive prefix sum);
+ *   row2tok [T*k] out: token of each expert-contiguous row; tok2row [T,k] out:
+ *   row of each (token, slot); x_perm [T*k,d] act_dtype out: gathered rows.
+ *   Rows of one expert are in increasing token order (deterministic).
+ *   idx entries outside [0,E) are skipped and flagged in the status word. */
+MOE_API moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* idx, int32_t* counts,
+                       int32_t* offsets, int32_t* row2tok, int32_t* tok2row, void* x_perm,
+                       void* ws, size_t ws_bytes, void* stream);
+
+/* Experts (intelliparadigm.com page section 3.3.1 SwiGLU; MoE listing).
+ *   x_perm [T*k,d] rows grouped by expert per `offsets` [E+1] (device);
+ *   x [T,d] for the shared expert; packed = moe_prepack_experts output.
+ *   y_perm [T*k,d] out: FFN_e of each row; y_shared [T,d] out: FFN_shared(x).
+ *   bf16: GEMM1 with the fused silu(W1 u)*(W3 u) epilogue (hidden rounded to
+ *   bf16), then GEMM2; both on tcgen05 with fp32 accumulation in TMEM. */
+MOE_API moe_status moe_grouped_swiglu(const moe_config* cfg, const void* x_perm, const int32_t* offsets,
+                              const void* x, const void* packed, void* y_perm, void* y_shared,
+                              void* ws, size_t ws_bytes, void* stream);
+
+/* Combine (MoE listing: gate-weighted sum over the k slots plus the shared
+ * expert; the dense einsum form of the intelliparadigm.com page 3.3.3).
+ *   out[t] = sum_j w[t,j] * y_perm[tok2row[t,j]] + y_shared[t], accumulated in
+ *   fp32 in slot order j = 0..k-1 (deterministic), stored as act_dtype. */
+MOE_API moe_status moe_combine(const moe_config* cfg, const void* y_perm, const void* y_shared,
+                       const int32_t* tok2row, const float* w, void* out,
+                       void* ws, size_t ws_bytes, void* stream);
+
+/* The whole layer: gate_topk -> permute -> grouped_swiglu -> combine, on one
+ * stream with no host synchronisation.  idx_out [T,k], w_out [T,k] and
+ * counts_out [E] are optional copies of the routing (NULL to skip). */
+MOE_API moe_status moe_forward(const moe_config* cfg, const void* x, const void* Wg, const float* bias,
+                       const void* packed, void* out, int32_t* idx_out, float* w_out,
+                       int32_t* counts_out, void* ws, size_t ws_bytes, void* stream);
+
+/* Synchronises `stream`, reads the device status word of `ws` and returns
+ * MOE_OK, MOE_ERR_DEVICE_TIMEOUT or MOE_ERR_DEVICE_BOUNDS.  `detail` (nullable)
+ * receives the raw word. */
+MOE_API moe_status moe_get_device_status(const void* ws, void* stream, int32_t* detail);
+
+/* Human-readable name of a status code (static storage). */
+MOE_API const char* moe_status_string(moe_status s);
+
+/* Number of kernels this library has launched in the process so far. */
+MOE_API uint64_t moe_launch_count(void);
+
+/* Stage timing for benchmarks.  While armed, every moe_forward records the
+ * caller's CUDA events (cudaEvent_t, created by the caller) on its stream at
+ * the boundaries of its MOE_FORWARD_STAGES stages and once at the end, i.e.
+ * MOE_FORWARD_STAGES + 1 events per call, taken from `events` in order until
+ * `n_events` are used.  Stages: 0 router (gate GEMM + top-k), 1 permutation,
+ * 2 GEMM1 with the SwiGLU epilogue, 3 GEMM2, 4 combine.  NULL disarms.
+ * Not thread-safe; arm, run, disarm from one host thread. */
+#define MOE_FORWARD_STAGES 5
+MOE_API moe_status moe_profile_arm(void* const* events, int32_t n_events);
+
+/* Name of stage i of moe_forward ("router", "permute", ...), or NULL. */
+MOE_API const char* moe_forward_stage_name(int32_t i);
+
+/* Number of kernels one moe_forward launches for `cfg` (host-side plan). */
+MOE_API int32_t moe_forward_kernel_count(const moe_config* cfg);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_B300_H */

@@ -1,0 +1,436 @@
+// C ABI of the MoE layer library: argument checks, workspace layout and the
+// launch sequence of each call.  See include/moe.h for the contract.
+#include <atomic>
+#include <cstring>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+static std::atomic<unsigned long long> g_launches{0};
+void count_launches(int n) { g_launches.fetch_add((unsigned long long)n); }
+
+static void* const* g_prof_events = nullptr;
+static int g_prof_n = 0;
+static int g_prof_cursor = 0;
+
+void profile_mark(cudaStream_t s) {
+  if (g_prof_events != nullptr && g_prof_cursor < g_prof_n)
+    cudaEventRecord(static_cast<cudaEvent_t>(g_prof_events[g_prof_cursor++]), s);
+}
+
+namespace {
+
+constexpr int kMaxE = 256;
+constexpr int kMaxK = 16;
+constexpr int kTcGateMinT = 1024;   // below this many tokens the SIMT gate streams W_g faster
+
+struct WsLayout {
+  size_t status, logits, wsplit, chunk_counts, chunk_base, counts, offsets, row2tok, tok2row, idx, w, x_perm, h, hs,
+      y, ys, total;
+};
+
+bool is_bf16(const moe_config& c) { return c.act_dtype == MOE_BF16; }
+long long I_s(const moe_config& c) { return (long long)c.n_shared * c.I; }
+
+bool use_tc_gate(const moe_config& c) {
+  return is_bf16(c) && c.T >= kTcGateMinT && c.E % 16 == 0 && c.E <= 256;
+}
+
+WsLayout ws_layout(const moe_config& c) {
+  WsLayout L;
+  const size_t eb = dtype_bytes(c.act_dtype);
+  const size_t R = size_t(c.T) * c.k;
+  const size_t nch = size_t(permute_chunks(c.T));
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = align_up(off + bytes, 256);
+    return at;
+  };
+  L.status = take(256);
+  L.logits = take(size_t(c.T) * c.E * 4);
+  L.wsplit = take(use_tc_gate(c) && c.gate_w_dtype == MOE_F32 ? size_t(c.E) * 3 * c.d * 2 : 0);
+  L.chunk_counts = take(nch * c.E * 4);
+  L.chunk_base = take(nch * c.E * 4);
+  L.counts = take(size_t(c.E) * 4);
+  L.offsets = take(size_t(c.E + 1) * 4);
+  L.row2tok = take(R * 4);
+  L.tok2row = take(R * 4);
+  L.idx = take(R * 4);
+  L.w = take(R * 4);
+  L.x_perm = take(R * c.d * eb);
+  L.h = take(R * c.I * eb);
+  L.hs = take(size_t(c.T) * I_s(c) * eb);
+  L.y = take(R * c.d * eb);
+  L.ys = take(size_t(c.T) * c.d * eb);
+  L.total = off;
+  return L;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+moe_status check_config(const moe_config* cp) {
+  if (cp == nullptr) return MOE_ERR_INVALID_ARG;
+  const moe_config& c = *cp;
+  if (c.T < 0 || c.d <= 0 || c.E <= 0 || c.I <= 0 || c.k <= 0 || c.n_shared < 0) return MOE_ERR_INVALID_ARG;
+  if (c.act_dtype != MOE_F32 && c.act_dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+  if (c.gate_w_dtype != MOE_F32 && c.gate_w_dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+  if (c.score_fn != MOE_SCORE_SOFTMAX && c.score_fn != MOE_SCORE_SIGMOID) return MOE_ERR_INVALID_ARG;
+  if (c.topk_method != MOE_TOPK_GREEDY && c.topk_method != MOE_TOPK_GROUP_LIMITED) return MOE_ERR_INVALID_ARG;
+  if (c.k > c.E) return MOE_ERR_INVALID_ARG;
+  if ((long long)c.T * c.k > (1LL << 30)) return MOE_ERR_INVALID_ARG;
+  if (c.topk_method == MOE_TOPK_GROUP_LIMITED) {
+    if (c.n_group <= 0 || c.E % c.n_group != 0 || c.topk_group <= 0 || c.topk_group > c.n_group)
+      return MOE_ERR_INVALID_ARG;
+    if (c.group_score != MOE_GROUP_MAX && c.group_score != MOE_GROUP_SUM_TOP) return MOE_ERR_INVALID_ARG;
+    const int gsz = c.E / c.n_group;
+    if (c.group_score == MOE_GROUP_SUM_TOP && (c.group_top <= 0 || c.group_top > gsz)) return MOE_ERR_INVALID_ARG;
+    if ((long long)c.topk_group * gsz < c.k) return MOE_ERR_INVALID_ARG;
+    if (c.n_group > 32) return MOE_ERR_UNSUPPORTED;
+  }
+  if (c.E > kMaxE || c.k > kMaxK) return MOE_ERR_UNSUPPORTED;
+  if (is_bf16(c)) {
+    // tensor-core tiles: K in steps of 64, the SwiGLU tile pairs 128 W1 rows
+    // with 128 W3 rows, TMA rows 16-byte aligned
+    if (c.d % 64 != 0 || c.I % 128 != 0 || I_s(c) % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  } else {
+    if (c.d % 4 != 0) return MOE_ERR_UNSUPPORTED;
+  }
+  return MOE_OK;
+}
+
+moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+struct Ws {
+  char* base;
+  WsLayout L;
+  template <typename T>
+  T* at(size_t off) const { return reinterpret_cast<T*>(base + off); }
+  int* status() const { return at<int>(L.status); }
+};
+
+moe_status check_ws(const moe_config& c, void* ws, size_t ws_bytes, Ws* out) {
+  if (ws == nullptr || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
+  out->base = static_cast<char*>(ws);
+  out->L = ws_layout(c);
+  if (ws_bytes < out->L.total) return MOE_ERR_WORKSPACE;
+  return MOE_OK;
+}
+
+moe_status reset_status(const Ws& w, cudaStream_t s) {
+  return cuda_status(cudaMemsetAsync(w.status(), 0, sizeof(int), s));
+}
+
+moe_status run_gate(const moe_config& c, const void* x, const void* wg, const float* bias, int32_t* idx, float* w,
+                    const Ws& ws, cudaStream_t s, int* launches) {
+  float* logits = ws.at<float>(ws.L.logits);
+  cudaError_t e;
+  if (use_tc_gate(c)) {
+    GemmClass g;
+    g.A = x;
+    g.a_rows = c.T;
+    g.a_cols = c.d;
+    if (c.gate_w_dtype == MOE_F32) {
+      void* split = ws.at<void>(ws.L.wsplit);
+      e = launch_gate_split(static_cast<const float*>(wg), c.E, c.d, split, s, launches);
+      if (e != cudaSuccess) return MOE_ERR_CUDA;
+      g.B = split;
+      g.b_cols = 3LL * c.d;
+      g.K = 3 * c.d;
+    } else {
+      g.B = wg;
+      g.b_cols = c.d;
+      g.K = c.d;
+    }
+    g.b_rows = c.E;
+    g.out = logits;
+    g.ld_out = c.E;
+    g.out_rows = c.T;
+    g.N = c.E;
+    g.a_k_mod = c.d;
+    g.b_rows_per_group = 0;
+    g.mma_n = c.E;
+    e = launch_grouped_gemm(EPI_STORE_F32, g, nullptr, nullptr, 0, c.T, 0, ws.status(), (c.T + 127) / 128, s,
+                            launches);
+  } else {
+    e = launch_gate_logits_simt(c, x, wg, logits, s, launches);
+  }
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  return cuda_status(launch_topk(c, logits, bias, idx, w, s, launches));
+}
+
+moe_status run_experts(const moe_config& c, const void* x_perm, const int32_t* offsets, const void* x,
+                       const void* packed, void* y_perm, void* y_shared, const Ws& ws, cudaStream_t s,
+                       int* launches, bool mark_stages = false) {
+  const PackedLayout P = packed_layout(c);
+  const char* pb = static_cast<const char*>(packed);
+  const long long R = (long long)c.T * c.k;
+  const long long Is = I_s(c);
+  if (!is_bf16(c)) {
+    if (mark_stages) profile_mark(s);   // the SIMT path has no separate GEMM2 stage boundary
+    return cuda_status(launch_swiglu_simt_f32(c, static_cast<const float*>(x_perm), offsets,
+                                              static_cast<const float*>(x), packed, ws.at<float>(ws.L.h),
+                                              ws.at<float>(ws.L.hs), static_cast<float*>(y_perm),
+                                              static_cast<float*>(y_shared), ws.status(), s, launches));
+  }
+  void* h = ws.at<void>(ws.L.h);
+  void* hs = ws.at<void>(ws.L.hs);
+  const bool shared = Is > 0;
+  // GEMM1 + SwiGLU: [rows, d] x [2I, d]^T -> H [rows, I]
+  GemmClass r1, s1;
+  r1.A = x_perm; r1.a_rows = R; r1.a_cols = c.d;
+  r1.B = pb + P.w13; r1.b_rows = 2LL * c.E * c.I; r1.b_cols = c.d;
+  r1.out = h; r1.ld_out = c.I; r1.out_rows = R;
+  r1.N = 2 * c.I; r1.K = c.d; r1.a_k_mod = c.d; r1.b_rows_per_group = 2 * c.I; r1.mma_n = 256;
+  s1.A = x; s1.a_rows = c.T; s1.a_cols = c.d;
+  s1.B = pb + P.w13s; s1.b_rows = 2 * Is; s1.b_cols = c.d;
+  s1.out = hs; s1.ld_out = Is; s1.out_rows = c.T;
+  s1.N = int(2 * Is); s1.K = c.d; s1.a_k_mod = c.d; s1.b_rows_per_group = 0; s1.mma_n = 256;
+  const long long mt_routed = R / 128 + c.E;
+  const long long mt_shared = shared ? (c.T + 127) / 128 : 0;
+  long long tiles1 = mt_routed * ((2LL * c.I + 255) / 256) + mt_shared * ((2 * Is + 255) / 256);
+  cudaError_t e = launch_grouped_gemm(EPI_SWIGLU, r1, shared ? &s1 : nullptr, offsets, c.E, 0, c.T, ws.status(),
+                                      tiles1, s, launches);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  // GEMM2: H [rows, I] x [d, I]^T -> Y [rows, d]
+  GemmClass r2, s2;
+  r2.A = h; r2.a_rows = R; r2.a_cols = c.I;
+  r2.B = pb + P.w2; r2.b_rows = (long long)c.E * c.d; r2.b_cols = c.I;
+  r2.out = y_perm; r2.ld_out = c.d; r2.out_rows = R;
+  r2.N = c.d; r2.K = c.I; r2.a_k_mod = c.I; r2.b_rows_per_group = c.d; r2.mma_n = 256;
+  s2.A = hs; s2.a_rows = c.T; s2.a_cols = Is;
+  s2.B = pb + P.w2s; s2.b_rows = c.d; s2.b_cols = Is;
+  s2.out = y_shared; s2.ld_out = c.d; s2.out_rows = c.T;
+  s2.N = c.d; s2.K = int(Is); s2.a_k_mod = int(Is); s2.b_rows_per_group = 0; s2.mma_n = 256;
+  const long long tiles2 = (mt_routed + mt_shared) * ((c.d + 255) / 256);
+  if (mark_stages) profile_mark(s);
+  e = launch_grouped_gemm(EPI_STORE_BF16, r2, shared ? &s2 : nullptr, offsets, c.E, 0, c.T, ws.status(), tiles2, s,
+                          launches);
+  return cuda_status(e);
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+moe_status moe_workspace_size(const moe_config* cfg, size_t* bytes) {
+  moe_status st = check_config(cfg);
+  if (st != MOE_OK) return st;
+  if (bytes == nullptr) return MOE_ERR_INVALID_ARG;
+  *bytes = ws_layout(*cfg).total;
+  return MOE_OK;
+}
+
+moe_status moe_packed_size(const moe_config* cfg, size_t* bytes) {
+  moe_status st = check_config(cfg);
+  if (st != MOE_OK) return st;
+  if (bytes == nullptr) return MOE_ERR_INVALID_ARG;
+  *bytes = packed_layout(*cfg).total;
+  return MOE_OK;
+}
+
+moe_status moe_prepack_experts(const moe_config* cfg, const void* W1, const void* W3, const void* W2,
+                               const void* Ws1, const void* Ws3, const void* Ws2, void* packed, size_t packed_bytes,
+                               void* stream) {
+  moe_status st = check_config(cfg);
+  if (st != MOE_OK) return st;
+  const moe_config& c = *cfg;
+  const bool shared = I_s(c) > 0;
+  if (!W1 || !W3 || !W2 || !packed || (shared && (!Ws1 || !Ws3 || !Ws2))) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(W1) || !aligned16(W3) || !aligned16(W2) || !aligned16(packed)) return MOE_ERR_INVALID_ARG;
+  if (shared && (!aligned16(Ws1) || !aligned16(Ws3) || !aligned16(Ws2))) return MOE_ERR_INVALID_ARG;
+  if (packed_bytes < packed_layout(c).total) return MOE_ERR_WORKSPACE;
+  int n = 0;
+  cudaError_t e = launch_prepack(c, W1, W3, W2, Ws1, Ws3, Ws2, packed, static_cast<cudaStream_t>(stream), &n);
+  count_launches(n);
+  return cuda_status(e);
+}
+
+moe_status moe_gate_topk(const moe_config* cfg, const void* x, const void* Wg, const float* bias, int32_t* idx,
+                         float* w, void* ws, size_t ws_bytes, void* stream) {
+  moe_status st = check_config(cfg);
+  if (st != MOE_OK) return st;
+  const moe_config& c = *cfg;
+  if (!x || !Wg || !idx || !w || !aligned16(x) || !aligned16(Wg) || !aligned16(idx) || !aligned16(w))
+    return MOE_ERR_INVALID_ARG;
+  if (bias != nullptr && !aligned16(bias)) return MOE_ERR_INVALID_ARG;
+  Ws W;
+  if ((st = check_ws(c, ws, ws_bytes, &W)) != MOE_OK) return st;
+  if (c.T == 0) return MOE_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if ((st = reset_status(W, s)) != MOE_OK) return st;
+  int n = 0;
+  st = run_gate(c, x, Wg, bias, idx, w, W, s, &n);
+  count_launches(n);
+  return st;
+}
+
+moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* idx, int32_t* counts, int32_t* offsets,
+                       int32_t* row2tok, int32_t* tok2row, void* x_perm, void* ws, size_t ws_bytes, void* stream) {
+  moe_status st = check_config(cfg);
+  if (st != MOE_OK) return st;
+  const moe_config& c = *cfg;
+  if (!x || !idx || !counts || !offsets || !row2tok || !tok2row || !x_perm) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(idx) || !aligned16(counts) || !aligned16(offsets) || !aligned16(row2tok) ||
+      !aligned16(tok2row) || !aligned16(x_perm))
+    return MOE_ERR_INVALID_ARG;
+  Ws W;
+  if ((st = check_ws(c, ws, ws_bytes, &W)) != MOE_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (c.T == 0) {
+    // no tokens: every expert is empty
+    if (cudaMemsetAsync(offsets, 0, size_t(c.E + 1) * 4, s) != cudaSuccess) return MOE_ERR_CUDA;
+    return cuda_status(cudaMemsetAsync(counts, 0, size_t(c.E) * 4, s));
+  }
+  if ((st = reset_status(W, s)) != MOE_OK) return st;
+  int n = 0;
+  cudaError_t e = launch_permute(c, x, idx, counts, offsets, row2tok, tok2row, x_perm, W.at<int32_t>(W.L.chunk_counts),
+                                 W.at<int32_t>(W.L.chunk_base), W.status(), s, &n);
+  count_launches(n);
+  return cuda_status(e);
+}
+
+moe_status moe_grouped_swiglu(const moe_config* cfg, const void* x_perm, const int32_t* offsets, const void* x,
+                              const void* packed, void* y_perm, void* y_shared, void* ws, size_t ws_bytes,
+                              void* stream) {
+  moe_status st = check_config(cfg);
+  if (st != MOE_OK) return st;
+  const moe_config& c = *cfg;
+  if (!x_perm || !offsets || !x || !packed || !y_perm || !y_shared) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x_perm) || !aligned16(offsets) || !aligned16(x) || !aligned16(packed) || !aligned16(y_perm) ||
+      !aligned16(y_shared))
+    return MOE_ERR_INVALID_ARG;
+  Ws W;
+  if ((st = check_ws(c, ws, ws_bytes, &W)) != MOE_OK) return st;
+  if (c.T == 0) return MOE_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if ((st = reset_status(W, s)) != MOE_OK) return st;
+  int n = 0;
+  st = run_experts(c, x_perm, offsets, x, packed, y_perm, y_shared, W, s, &n);
+  count_launches(n);
+  return st;
+}
+
+moe_status moe_combine(const moe_config* cfg, const void* y_perm, const void* y_shared, const int32_t* tok2row,
+                       const float* w, void* out, void* ws, size_t ws_bytes, void* stream) {
+  moe_status st = check_config(cfg);
+  if (st != MOE_OK) return st;
+  const moe_config& c = *cfg;
+  if (!y_perm || !y_shared || !tok2row || !w || !out) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(y_perm) || !aligned16(y_shared) || !aligned16(tok2row) || !aligned16(w) || !aligned16(out))
+    return MOE_ERR_INVALID_ARG;
+  Ws W;
+  if ((st = check_ws(c, ws, ws_bytes, &W)) != MOE_OK) return st;
+  if (c.T == 0) return MOE_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if ((st = reset_status(W, s)) != MOE_OK) return st;
+  int n = 0;
+  cudaError_t e = launch_combine(c, y_perm, y_shared, tok2row, w, out, W.status(), s, &n);
+  count_launches(n);
+  return cuda_status(e);
+}
+
+moe_status moe_forward(const moe_config* cfg, const void* x, const void* Wg, const float* bias, const void* packed,
+                       void* out, int32_t* idx_out, float* w_out, int32_t* counts_out, void* ws, size_t ws_bytes,
+                       void* stream) {
+  moe_status st = check_config(cfg);
+  if (st != MOE_OK) return st;
+  const moe_config& c = *cfg;
+  if (!x || !Wg || !packed || !out) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(Wg) || !aligned16(packed) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
+  if ((bias && !aligned16(bias)) || (idx_out && !aligned16(idx_out)) || (w_out && !aligned16(w_out)) ||
+      (counts_out && !aligned16(counts_out)))
+    return MOE_ERR_INVALID_ARG;
+  Ws W;
+  if ((st = check_ws(c, ws, ws_bytes, &W)) != MOE_OK) return st;
+  if (c.T == 0) return MOE_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if ((st = reset_status(W, s)) != MOE_OK) return st;
+  int n = 0;
+  int32_t* idx = idx_out ? idx_out : W.at<int32_t>(W.L.idx);
+  float* w = w_out ? w_out : W.at<float>(W.L.w);
+  int32_t* counts = counts_out ? counts_out : W.at<int32_t>(W.L.counts);
+  int32_t* offsets = W.at<int32_t>(W.L.offsets);
+  int32_t* tok2row = W.at<int32_t>(W.L.tok2row);
+  void* x_perm = W.at<void>(W.L.x_perm);
+  void* y = W.at<void>(W.L.y);
+  void* ys = W.at<void>(W.L.ys);
+  profile_mark(s);
+  st = run_gate(c, x, Wg, bias, idx, w, W, s, &n);
+  if (st == MOE_OK) {
+    profile_mark(s);
+    cudaError_t e = launch_permute(c, x, idx, counts, offsets, W.at<int32_t>(W.L.row2tok), tok2row, x_perm,
+                                   W.at<int32_t>(W.L.chunk_counts), W.at<int32_t>(W.L.chunk_base), W.status(), s, &n);
+    st = cuda_status(e);
+  }
+  if (st == MOE_OK) {
+    profile_mark(s);
+    st = run_experts(c, x_perm, offsets, x, packed, y, ys, W, s, &n, true);
+  }
+  if (st == MOE_OK) {
+    profile_mark(s);
+    st = cuda_status(launch_combine(c, y, ys, tok2row, w, out, W.status(), s, &n));
+  }
+  if (st == MOE_OK) profile_mark(s);
+  count_launches(n);
+  return st;
+}
+
+moe_status moe_get_device_status(const void* ws, void* stream, int32_t* detail) {
+  if (ws == nullptr) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  int32_t word = 0;
+  if (cudaMemcpy(&word, ws, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+  if (detail) *detail = word;
+  if (word & DEV_TIMEOUT) return MOE_ERR_DEVICE_TIMEOUT;
+  if (word & (DEV_BAD_EXPERT | DEV_BAD_ROW)) return MOE_ERR_DEVICE_BOUNDS;
+  return MOE_OK;
+}
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+    case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+    case MOE_ERR_DEVICE_TIMEOUT: return "MOE_ERR_DEVICE_TIMEOUT";
+    case MOE_ERR_DEVICE_BOUNDS: return "MOE_ERR_DEVICE_BOUNDS";
+  }
+  return "MOE_ERR_UNKNOWN";
+}
+
+uint64_t moe_launch_count(void) { return g_launches.load(); }
+
+moe_status moe_profile_arm(void* const* events, int32_t n_events) {
+  if (events != nullptr && n_events < 0) return MOE_ERR_INVALID_ARG;
+  g_prof_events = n_events > 0 ? events : nullptr;
+  g_prof_n = events != nullptr ? n_events : 0;
+  g_prof_cursor = 0;
+  return MOE_OK;
+}
+
+const char* moe_forward_stage_name(int32_t i) {
+  static const char* names[MOE_FORWARD_STAGES] = {"router", "permute", "gemm1_swiglu", "gemm2", "combine"};
+  return (i >= 0 && i < MOE_FORWARD_STAGES) ? names[i] : nullptr;
+}
+
+int32_t moe_forward_kernel_count(const moe_config* cfg) {
+  if (check_config(cfg) != MOE_OK) return -1;
+  const moe_config& c = *cfg;
+  if (c.T == 0) return 0;
+  int n = 2;                                                        // logits + top-k
+  if (use_tc_gate(c) && c.gate_w_dtype == MOE_F32) n += 1;          // W_g split
+  n += 5;                                                           // permute: 4 + gather
+  n += 2;                                                           // GEMM1, GEMM2
+  n += 1;                                                           // combine
+  return n;
+}
+
+}  // extern "C"

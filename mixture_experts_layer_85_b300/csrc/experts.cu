@@ -1,0 +1,308 @@
+// Expert weight packing, the SIMT fp32 expert path, and the combine.
+//
+// SwiGLU expert: FFN(u) = W2 (silu(W1 u) * (W3 u)) with nn.Linear layouts
+// (intelliparadigm.com page, section 3.3.1).  The MoE listing of the
+// DeepSeek-V2 walkthrough sums the k routed expert outputs weighted by their
+// gates and adds the shared experts, fused as one SwiGLU of hidden
+// n_shared * I, evaluated on every token; no residual is added.
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+// W1/W3 [G,H,d] -> W13 [G,2H,d]: for each block of `bi` hidden units, the W1
+// rows followed by the matching W3 rows.
+__global__ void interleave_w13_kernel(const uint4* __restrict__ w1, const uint4* __restrict__ w3,
+                                      uint4* __restrict__ dst, long long G, int H, int bi, int vec_per_row) {
+  const long long rows = G * 2LL * H;
+  const long long n = rows * vec_per_row;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+    const long long row = i / vec_per_row;
+    const int v = int(i % vec_per_row);
+    const long long g = row / (2LL * H);
+    const int p = int(row % (2LL * H));
+    const int blk = p / (2 * bi), r = p % (2 * bi);
+    const uint4* src = (r < bi ? w1 : w3) + ((g * H + (long long)blk * bi + (r % bi)) * vec_per_row);
+    dst[i] = src[v];
+  }
+}
+
+__device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
+
+// Expert of routed row r: the last e with offsets[e] <= r.
+__device__ __forceinline__ int expert_of_row(const int32_t* __restrict__ offsets, int E, long long r) {
+  int lo = 0, hi = E - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (offsets[mid] <= r) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+struct SimtArgs {
+  long long R;
+  int T, d, E, I, Is, bi, bis;
+};
+
+// fp32 GEMM1 + SwiGLU, one thread per (row, hidden unit).  Rows [0,R) are the
+// routed rows, rows [R, R+T) are the tokens for the shared expert.
+__global__ void swiglu_simt_h_kernel(const float* __restrict__ x_perm, const int32_t* __restrict__ offsets,
+                                     const float* __restrict__ x, const float* __restrict__ w13,
+                                     const float* __restrict__ w13s, SimtArgs a, float* __restrict__ h,
+                                     float* __restrict__ hs, int* status) {
+  const long long n_routed = a.R * a.I;
+  const long long n = n_routed + (long long)a.T * a.Is;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+    const float* xr;
+    const float* wa;
+    const float* wb;
+    float* dst;
+    if (i < n_routed) {
+      const long long r = i / a.I;
+      const int u = int(i % a.I);
+      const int e = expert_of_row(offsets, a.E, r);
+      if (r >= offsets[a.E]) {
+        flag_status(status, DEV_BAD_ROW);
+        continue;
+      }
+      xr = x_perm + r * a.d;
+      const long long base = (long long)e * 2 * a.I + (u / a.bi) * 2LL * a.bi + (u % a.bi);
+      wa = w13 + base * a.d;
+      wb = w13 + (base + a.bi) * a.d;
+      dst = h + r * a.I + u;
+    } else {
+      const long long j = i - n_routed;
+      const long long t = j / a.Is;
+      const int u = int(j % a.Is);
+      xr = x + t * a.d;
+      const long long base = (u / a.bis) * 2LL * a.bis + (u % a.bis);
+      wa = w13s + base * a.d;
+      wb = w13s + (base + a.bis) * a.d;
+      dst = hs + t * a.Is + u;
+    }
+    float s1 = 0.0f, s3 = 0.0f;
+    for (int c = 0; c < a.d; ++c) {
+      const float xv = xr[c];
+      s1 = fmaf(xv, wa[c], s1);
+      s3 = fmaf(xv, wb[c], s3);
+    }
+    *dst = silu(s1) * s3;
+  }
+}
+
+// fp32 GEMM2, one thread per (row, output feature).
+__global__ void swiglu_simt_y_kernel(const float* __restrict__ h, const float* __restrict__ hs,
+                                     const int32_t* __restrict__ offsets, const float* __restrict__ w2,
+                                     const float* __restrict__ w2s, SimtArgs a, float* __restrict__ y,
+                                     float* __restrict__ ys) {
+  const long long n_routed = a.R * a.d;
+  const long long n = n_routed + (long long)a.T * a.d;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+    const float* hr;
+    const float* wr;
+    float* dst;
+    int H;
+    if (i < n_routed) {
+      const long long r = i / a.d;
+      const int c = int(i % a.d);
+      if (r >= offsets[a.E]) continue;
+      const int e = expert_of_row(offsets, a.E, r);
+      hr = h + r * a.I;
+      wr = w2 + ((long long)e * a.d + c) * a.I;
+      dst = y + r * a.d + c;
+      H = a.I;
+    } else {
+      const long long j = i - n_routed;
+      const long long t = j / a.d;
+      const int c = int(j % a.d);
+      hr = hs + t * a.Is;
+      wr = w2s + (long long)c * a.Is;
+      dst = ys + t * a.d + c;
+      H = a.Is;
+    }
+    float acc = 0.0f;
+    for (int u = 0; u < H; ++u) acc = fmaf(hr[u], wr[u], acc);
+    *dst = acc;
+  }
+}
+
+template <typename T> struct Vec16;
+template <> struct Vec16<float> {
+  static constexpr int N = 4;
+  static __device__ __forceinline__ void load(const uint4& v, float* f) {
+    f[0] = __uint_as_float(v.x);
+    f[1] = __uint_as_float(v.y);
+    f[2] = __uint_as_float(v.z);
+    f[3] = __uint_as_float(v.w);
+  }
+  static __device__ __forceinline__ uint4 store(const float* f) {
+    return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]), __float_as_uint(f[3]));
+  }
+};
+template <> struct Vec16<__nv_bfloat16> {
+  static constexpr int N = 8;
+  static __device__ __forceinline__ void load(const uint4& v, float* f) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      f[2 * i] = __uint_as_float(w[i] << 16);
+      f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+  }
+  static __device__ __forceinline__ uint4 store(const float* f) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      __nv_bfloat162 b = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+      w[i] = *reinterpret_cast<uint32_t*>(&b);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+  }
+};
+
+// out[t] = sum_j w[t,j] * y_perm[tok2row[t,j]] + y_shared[t], fp32 accumulation
+// in slot order.  One block per token (grid-stride), 16-byte vectors.
+template <typename T, int MAXK>
+__global__ void __launch_bounds__(128) combine_kernel(const uint4* __restrict__ y_perm, const uint4* __restrict__ y_shared,
+                                                      const int32_t* __restrict__ tok2row, const float* __restrict__ w,
+                                                      int Tn, int k, long long R, int vec_per_row,
+                                                      uint4* __restrict__ out, int* status) {
+  constexpr int N = Vec16<T>::N;
+  for (int t = blockIdx.x; t < Tn; t += gridDim.x) {
+    long long rows[MAXK];
+    float g[MAXK];
+#pragma unroll
+    for (int j = 0; j < MAXK; ++j) {
+      rows[j] = -1;
+      g[j] = 0.0f;
+      if (j < k) {
+        const long long r = tok2row[(long long)t * k + j];
+        if (r >= 0 && r < R) {
+          rows[j] = r;
+          g[j] = w[(long long)t * k + j];
+        } else if (threadIdx.x == 0) {
+          flag_status(status, DEV_BAD_ROW);
+        }
+      }
+    }
+    for (int v = threadIdx.x; v < vec_per_row; v += blockDim.x) {
+      float acc[N];
+#pragma unroll
+      for (int i = 0; i < N; ++i) acc[i] = 0.0f;
+#pragma unroll
+      for (int j = 0; j < MAXK; ++j) {
+        if (rows[j] >= 0) {
+          float f[N];
+          Vec16<T>::load(y_perm[rows[j] * vec_per_row + v], f);
+#pragma unroll
+          for (int i = 0; i < N; ++i) acc[i] = fmaf(g[j], f[i], acc[i]);
+        }
+      }
+      if (y_shared != nullptr) {
+        float f[N];
+        Vec16<T>::load(y_shared[(long long)t * vec_per_row + v], f);
+#pragma unroll
+        for (int i = 0; i < N; ++i) acc[i] += f[i];
+      }
+      out[(long long)t * vec_per_row + v] = Vec16<T>::store(acc);
+    }
+  }
+}
+
+}  // namespace
+
+PackedLayout packed_layout(const moe_config& c) {
+  PackedLayout L;
+  const size_t eb = dtype_bytes(c.act_dtype);
+  const long long Is = (long long)c.n_shared * c.I;
+  L.bi = (c.I % 128 == 0) ? 128 : c.I;
+  L.bis = (Is % 128 == 0) ? 128 : int(Is > 0 ? Is : 1);
+  size_t off = 0;
+  L.w13 = off;
+  off = align_up(off + size_t(c.E) * 2 * c.I * c.d * eb, 256);
+  L.w2 = off;
+  off = align_up(off + size_t(c.E) * c.d * c.I * eb, 256);
+  L.w13s = off;
+  off = align_up(off + size_t(2 * Is) * c.d * eb, 256);
+  L.w2s = off;
+  off = align_up(off + size_t(c.d) * Is * eb, 256);
+  L.total = off;
+  return L;
+}
+
+cudaError_t launch_prepack(const moe_config& c, const void* W1, const void* W3, const void* W2,
+                           const void* Ws1, const void* Ws3, const void* Ws2, void* packed, cudaStream_t s,
+                           int* launches) {
+  const PackedLayout L = packed_layout(c);
+  const size_t eb = dtype_bytes(c.act_dtype);
+  const int vec = int(size_t(c.d) * eb / 16);
+  char* base = static_cast<char*>(packed);
+  const long long Is = (long long)c.n_shared * c.I;
+  auto grid_for = [](long long n) { long long g = (n + 255) / 256; return int(g < 8192 ? g : 8192); };
+  interleave_w13_kernel<<<grid_for((long long)c.E * 2 * c.I * vec), 256, 0, s>>>(
+      static_cast<const uint4*>(W1), static_cast<const uint4*>(W3), reinterpret_cast<uint4*>(base + L.w13), c.E, c.I,
+      L.bi, vec);
+  if (launches) ++*launches;
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  e = cudaMemcpyAsync(base + L.w2, W2, size_t(c.E) * c.d * c.I * eb, cudaMemcpyDeviceToDevice, s);
+  if (e != cudaSuccess) return e;
+  if (Is > 0) {
+    interleave_w13_kernel<<<grid_for(2 * Is * vec), 256, 0, s>>>(
+        static_cast<const uint4*>(Ws1), static_cast<const uint4*>(Ws3), reinterpret_cast<uint4*>(base + L.w13s), 1,
+        int(Is), L.bis, vec);
+    if (launches) ++*launches;
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    e = cudaMemcpyAsync(base + L.w2s, Ws2, size_t(c.d) * Is * eb, cudaMemcpyDeviceToDevice, s);
+  }
+  return e;
+}
+
+cudaError_t launch_swiglu_simt_f32(const moe_config& c, const float* x_perm, const int32_t* offsets,
+                                   const float* x, const void* packed, float* h, float* hs, float* y, float* ys,
+                                   int* status, cudaStream_t s, int* launches) {
+  const PackedLayout L = packed_layout(c);
+  const char* base = static_cast<const char*>(packed);
+  SimtArgs a;
+  a.R = (long long)c.T * c.k;
+  a.T = c.T;
+  a.d = c.d;
+  a.E = c.E;
+  a.I = c.I;
+  a.Is = c.n_shared * c.I;
+  a.bi = L.bi;
+  a.bis = L.bis;
+  const long long n1 = a.R * a.I + (long long)a.T * a.Is;
+  const long long n2 = (a.R + a.T) * a.d;
+  auto grid_for = [](long long n) { long long g = (n + 255) / 256; return int(g < 65535 ? g : 65535); };
+  swiglu_simt_h_kernel<<<grid_for(n1), 256, 0, s>>>(x_perm, offsets, x, reinterpret_cast<const float*>(base + L.w13),
+                                                    reinterpret_cast<const float*>(base + L.w13s), a, h, hs, status);
+  swiglu_simt_y_kernel<<<grid_for(n2), 256, 0, s>>>(h, hs, offsets, reinterpret_cast<const float*>(base + L.w2),
+                                                    reinterpret_cast<const float*>(base + L.w2s), a, y, ys);
+  if (launches) *launches += 2;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const moe_config& c, const void* y_perm, const void* y_shared, const int32_t* tok2row,
+                           const float* w, void* out, int* status, cudaStream_t s, int* launches) {
+  const int vec = int(size_t(c.d) * dtype_bytes(c.act_dtype) / 16);
+  const int grid = c.T < 65535 ? c.T : 65535;
+  const long long R = (long long)c.T * c.k;
+  auto yp = static_cast<const uint4*>(y_perm);
+  // without shared experts there is no shared term to add
+  auto ys = c.n_shared > 0 ? static_cast<const uint4*>(y_shared) : nullptr;
+  auto o = static_cast<uint4*>(out);
+  if (c.act_dtype == MOE_BF16) {
+    if (c.k <= 8) combine_kernel<__nv_bfloat16, 8><<<grid, 128, 0, s>>>(yp, ys, tok2row, w, c.T, c.k, R, vec, o, status);
+    else combine_kernel<__nv_bfloat16, 16><<<grid, 128, 0, s>>>(yp, ys, tok2row, w, c.T, c.k, R, vec, o, status);
+  } else {
+    if (c.k <= 8) combine_kernel<float, 8><<<grid, 128, 0, s>>>(yp, ys, tok2row, w, c.T, c.k, R, vec, o, status);
+    else combine_kernel<float, 16><<<grid, 128, 0, s>>>(yp, ys, tok2row, w, c.T, c.k, R, vec, o, status);
+  }
+  if (launches) ++*launches;
+  return cudaGetLastError();
+}
+
+}  // namespace moe

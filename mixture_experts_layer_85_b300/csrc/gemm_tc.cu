@@ -1,0 +1,474 @@
+// Grouped bf16 GEMM on the 5th-generation tensor cores (tcgen05 + TMEM + TMA),
+// with the SwiGLU epilogue of the routed experts fused in.
+//
+//   D[g] = A[g] * B[g]^T   A: rows of group g (K-major), B: the group's weight
+//   rows (nn.Linear layout, K-major), fp32 accumulation in tensor memory.
+//
+// The expert FFN is w2(silu(w1 x) * w3 x) (intelliparadigm.com page, section
+// 3.3.1); the MoE listing of the DeepSeek-V2 walkthrough runs it per expert on
+// the rows routed to that expert, plus the shared experts on every token.
+// Here all experts run in one persistent launch: group sizes live on the
+// device (the permutation's offsets) and every CTA derives the same tile list
+// from them, so no host synchronisation is needed.
+//
+// CTA layout (192 threads, one CTA per SM):
+//   warp 0      TMA producer: A tile 128x64 and B tile <=256x64 per stage
+//               into a 4-deep shared-memory ring (128-byte swizzle)
+//   warp 1      TMEM allocator + single-thread tcgen05.mma issuer
+//               (M=128, N<=256, K=16 per instruction)
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator, SwiGLU or plain
+//               conversion, stores to global memory
+// Two 256-column accumulators in TMEM let the epilogue of tile i overlap the
+// main loop of tile i+1.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "internal.h"
+#include "tc_ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;
+constexpr int STAGES = 4;
+constexpr int THREADS = 192;
+constexpr int A_BYTES = BM * BK * 2;
+constexpr int B_BYTES = BN * BK * 2;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int MAX_GROUPS = 272;
+constexpr uint32_t TMEM_COLS = 512;
+
+struct Params {
+  CUtensorMap tmA[2];
+  CUtensorMap tmB[2];
+  void* out[2];
+  long long ld_out[2];
+  long long out_rows[2];
+  int N[2], K[2], a_k_mod[2], b_step[2], mma_n[2];
+  const int32_t* offsets;
+  int num_routed;
+  int rows_single0;
+  int shared_rows;
+  int* status;
+};
+
+struct Ctrl {
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+  int ngroups;
+  int g0;
+  int tile_start[MAX_GROUPS + 1];
+  int row_start[MAX_GROUPS];
+  int rows[MAX_GROUPS];
+};
+
+constexpr size_t kSmemBytes = 1024 + size_t(STAGES) * STAGE_BYTES + sizeof(Ctrl);
+static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+// More than half of an SM's shared memory: at most one CTA per SM, so the
+// full-TMEM allocation below can never wait on another resident CTA.
+static_assert(kSmemBytes > 114 * 1024, "one CTA per SM");
+
+struct TileInfo {
+  int cls, g, m_blk, n_blk, row_start, rows;
+};
+
+__device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+__device__ __forceinline__ int group_tiles(const Params& p, int cls, int rows) {
+  return cdiv(rows, BM) * cdiv(p.N[cls], BN);
+}
+
+// Warp-cooperative: per-group row ranges and the exclusive prefix of tiles.
+__device__ void build_schedule(Ctrl* c, const Params& p, int lane) {
+  const int g0 = p.num_routed > 0 ? p.num_routed : (p.rows_single0 > 0 ? 1 : 0);
+  const int ng = g0 + (p.shared_rows > 0 ? 1 : 0);
+  const int per = cdiv(ng, 32);
+  const int lo = min(ng, lane * per), hi = min(ng, lo + per);
+  int local = 0;
+  for (int g = lo; g < hi; ++g) {
+    const int cls = g < g0 ? 0 : 1;
+    int rs = 0, rows = 0;
+    if (cls == 0) {
+      if (p.num_routed > 0) {
+        rs = p.offsets[g];
+        rows = p.offsets[g + 1] - rs;
+      } else {
+        rows = p.rows_single0;
+      }
+    } else {
+      rows = p.shared_rows;
+    }
+    if (rows < 0 || rs < 0 || (long long)rs + rows > p.out_rows[cls]) {
+      flag_status(p.status, DEV_BAD_ROW);
+      rs = 0;
+      rows = 0;
+    }
+    c->row_start[g] = rs;
+    c->rows[g] = rows;
+    local += group_tiles(p, cls, rows);
+  }
+  int incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  int run = incl - local;
+  for (int g = lo; g < hi; ++g) {
+    c->tile_start[g] = run;
+    run += group_tiles(p, g < g0 ? 0 : 1, c->rows[g]);
+  }
+  if (lane == 31) {
+    c->tile_start[ng] = incl;
+    c->ngroups = ng;
+    c->g0 = g0;
+  }
+}
+
+// Tile -> (group, m block, n block).  Within a group, the block order keeps
+// the operand that is re-read the most resident in L2: groups with more row
+// blocks than column blocks walk columns fastest (the A rows are re-used),
+// others walk rows fastest (the weight tile is re-used).
+__device__ __forceinline__ TileInfo tile_info(const Ctrl* c, const Params& p, int tile) {
+  int lo = 0, hi = c->ngroups - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (c->tile_start[mid] <= tile) lo = mid;
+    else hi = mid - 1;
+  }
+  TileInfo t;
+  t.g = lo;
+  t.cls = lo < c->g0 ? 0 : 1;
+  t.row_start = c->row_start[lo];
+  t.rows = c->rows[lo];
+  const int local = tile - c->tile_start[lo];
+  const int mb = cdiv(t.rows, BM), nb = cdiv(p.N[t.cls], BN);
+  if (mb > nb) {
+    t.m_blk = local / nb;
+    t.n_blk = local % nb;
+  } else {
+    t.n_blk = local / mb;
+    t.m_blk = local % mb;
+  }
+  return t;
+}
+
+__device__ void producer(Ctrl* c, const Params& p, uint8_t* stages, int total) {
+  volatile int* ab = &c->abort;
+  int stage = 0;
+  uint32_t phase = 0;
+  uint32_t issued = 0, issued_par = 0;
+  bool ok = true;
+  for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+    const TileInfo t = tile_info(c, p, tile);
+    const int a_row = t.row_start + t.m_blk * BM;
+    const int b_row = (t.cls == 0 ? t.g * p.b_step[0] : 0) + t.n_blk * BN;
+    const int nk = p.K[t.cls] / BK;
+    const uint32_t bytes = A_BYTES + uint32_t(p.mma_n[t.cls]) * BK * 2;
+    for (int kb = 0; kb < nk; ++kb) {
+      if (!mbar_wait(&c->empty[stage], phase ^ 1u, ab, p.status)) {
+        ok = false;
+        break;
+      }
+      uint8_t* sa = stages + stage * STAGE_BYTES;
+      mbar_arrive_expect_tx(&c->full[stage], bytes);
+      const int kc = kb * BK;
+      tma_load_2d(sa, &p.tmA[t.cls], &c->full[stage], kc % p.a_k_mod[t.cls], a_row);
+      tma_load_2d(sa + A_BYTES, &p.tmB[t.cls], &c->full[stage], kc, b_row);
+      issued |= 1u << stage;
+      issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
+      if (++stage == STAGES) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+  }
+  // Every issued copy must land before the CTA exits (normally all of them
+  // were already consumed by the MMA thread and these waits return at once).
+  for (int s = 0; s < STAGES; ++s)
+    if (issued & (1u << s)) mbar_wait(&c->full[s], (issued_par >> s) & 1u, nullptr, p.status);
+}
+
+__device__ void mma_issuer(Ctrl* c, const Params& p, uint8_t* stages, uint32_t tmem, int total) {
+  volatile int* ab = &c->abort;
+  int stage = 0;
+  uint32_t phase = 0;
+  int local = 0;
+  bool ok = true;
+  for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x, ++local) {
+    const TileInfo t = tile_info(c, p, tile);
+    const int acc = local & 1;
+    const uint32_t acc_par = uint32_t(local >> 1) & 1u;
+    if (!mbar_wait(&c->tempty[acc], acc_par ^ 1u, ab, p.status)) break;
+    tc_fence_after();
+    const uint32_t d_tmem = tmem + uint32_t(acc * BN);
+    const uint32_t idesc = idesc_bf16_f32(BM, p.mma_n[t.cls]);
+    const int nk = p.K[t.cls] / BK;
+    for (int kb = 0; kb < nk; ++kb) {
+      if (!mbar_wait(&c->full[stage], phase, ab, p.status)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t a0 = smem_u32(stages + stage * STAGE_BYTES);
+      const uint32_t b0 = a0 + A_BYTES;
+#pragma unroll
+      for (int kk = 0; kk < BK / 16; ++kk)
+        mma_bf16_ss(d_tmem, sw128_kmajor_desc(a0 + kk * 32), sw128_kmajor_desc(b0 + kk * 32), idesc,
+                    (kb | kk) != 0 ? 1u : 0u);
+      mma_commit(&c->empty[stage]);
+      if (++stage == STAGES) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+    if (ok) mma_commit(&c->tfull[acc]);
+  }
+  // All MMAs this thread issued complete before TMEM is released.
+  mma_commit(&c->drain);
+  mbar_wait(&c->drain, 0u, nullptr, p.status);
+}
+
+__device__ __forceinline__ float silu_f(float z) { return z / (1.0f + __expf(-z)); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+template <int EPI>
+__device__ void epilogue(Ctrl* c, const Params& p, uint32_t tmem, int total, int warp, int lane) {
+  volatile int* ab = &c->abort;
+  const int q = warp & 3;  // the TMEM lane quarter this warp may read
+  const int r_in_tile = q * 32 + lane;
+  int local = 0;
+  for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++local) {
+    const TileInfo t = tile_info(c, p, tile);
+    const int acc = local & 1;
+    const uint32_t acc_par = uint32_t(local >> 1) & 1u;
+    // One lane waits and the verdict is broadcast, so the warp-collective
+    // TMEM loads below are always executed by the whole warp.
+    int ok = 1;
+    if (lane == 0) ok = mbar_wait(&c->tfull[acc], acc_par, ab, p.status) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (!ok) break;
+    tc_fence_after();
+    const int row_local = t.m_blk * BM + r_in_tile;
+    const bool valid = row_local < t.rows;
+    const long long grow = (long long)t.row_start + row_local;
+    const uint32_t tbase = tmem + uint32_t(acc * BN) + (uint32_t(q * 32) << 16);
+    if constexpr (EPI == EPI_SWIGLU) {
+      // Tile columns [0,128) hold W1 rows, [128,256) the matching W3 rows.
+      __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out[t.cls]) + grow * p.ld_out[t.cls];
+      const int col0 = t.n_blk * (BN / 2);
+#pragma unroll 1
+      for (int cc = 0; cc < BN / 2; cc += 16) {
+        float g[16], u[16];
+        tmem_ld16(tbase + cc, g);
+        tmem_ld16(tbase + BN / 2 + cc, u);
+        if (valid) {
+          uint32_t w[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            w[i] = pack_bf16x2(silu_f(g[2 * i]) * u[2 * i], silu_f(g[2 * i + 1]) * u[2 * i + 1]);
+          uint4* dst = reinterpret_cast<uint4*>(orow + col0 + cc);
+          dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+          dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        }
+      }
+    } else {
+      const int col0 = t.n_blk * BN;
+      const int ncol = min(BN, p.N[t.cls] - col0);
+      const int nld = min(p.mma_n[t.cls], BN);
+#pragma unroll 1
+      for (int cc = 0; cc < nld; cc += 16) {
+        float v[16];
+        tmem_ld16(tbase + cc, v);
+        if (valid && cc < ncol) {
+          if constexpr (EPI == EPI_STORE_BF16) {
+            __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out[t.cls]) + grow * p.ld_out[t.cls] + col0 + cc;
+            if (cc + 16 <= ncol) {
+              uint32_t w[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) w[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+              uint4* dst = reinterpret_cast<uint4*>(orow);
+              dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+              dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 16; ++i)
+                if (cc + i < ncol) orow[i] = __float2bfloat16_rn(v[i]);
+            }
+          } else {
+            float* orow = static_cast<float*>(p.out[t.cls]) + grow * p.ld_out[t.cls] + col0 + cc;
+            if (cc + 16 <= ncol) {
+              float4* dst = reinterpret_cast<float4*>(orow);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 16; ++i)
+                if (cc + i < ncol) orow[i] = v[i];
+            }
+          }
+        }
+      }
+    }
+    tc_fence_before();
+    mbar_arrive(&c->tempty[acc]);
+  }
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const __grid_constant__ Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* stages = base;
+  Ctrl* c = reinterpret_cast<Ctrl*>(base + size_t(STAGES) * STAGE_BYTES);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&c->full[s], 1);
+      mbar_init(&c->empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&c->tfull[a], 1);
+      mbar_init(&c->tempty[a], 128);
+    }
+    mbar_init(&c->drain, 1);
+    c->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&p.tmA[0]);
+    tma_prefetch_desc(&p.tmB[0]);
+    tma_prefetch_desc(&p.tmA[1]);
+    tma_prefetch_desc(&p.tmB[1]);
+  }
+  if (warp == 1) {
+    tmem_alloc(&c->tmem_base, TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (warp == 2) build_schedule(c, p, lane);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  const uint32_t tmem = c->tmem_base;
+  const int total = c->tile_start[c->ngroups];
+  if (warp == 0) {
+    if (lane == 0) producer(c, p, stages, total);
+  } else if (warp == 1) {
+    if (lane == 0) mma_issuer(c, p, stages, tmem, total);
+  } else {
+    epilogue<EPI>(c, p, tmem, total, warp, lane);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// bf16 [rows, cols] row-major, box = 64 columns x box_rows rows, 128-byte swizzle.
+bool encode_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, uint32_t box_rows) {
+  auto enc = tensor_map_encoder();
+  if (enc == nullptr || rows <= 0 || cols <= 0) return false;
+  cuuint64_t dims[2] = {cuuint64_t(cols), cuuint64_t(rows)};
+  cuuint64_t strides[1] = {cuuint64_t(cols) * 2};
+  cuuint32_t box[2] = {64u, box_rows};
+  cuuint32_t es[2] = {1u, 1u};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int EPI>
+cudaError_t launch_epi(const Params& p, int grid, cudaStream_t stream) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         int(kSmemBytes));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  grouped_gemm_kernel<EPI><<<grid, THREADS, kSmemBytes, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int num_sms() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  static int cached_dev = -1, cached_n = 0;
+  if (dev != cached_dev) {
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cached_dev = dev;
+    cached_n = n > 0 ? n : 1;
+  }
+  return cached_n;
+}
+
+cudaError_t launch_grouped_gemm(int epi, const GemmClass& c0, const GemmClass* c1, const int32_t* offsets,
+                                int num_routed, int rows_single0, int shared_rows, int* status,
+                                long long max_tiles, cudaStream_t stream, int* launches) {
+  if (max_tiles <= 0) return cudaSuccess;
+  Params p;
+  memset(&p, 0, sizeof(p));
+  const GemmClass* cls[2] = {&c0, c1 != nullptr ? c1 : &c0};
+  for (int i = 0; i < 2; ++i) {
+    const GemmClass& g = *cls[i];
+    if (!encode_map(&p.tmA[i], g.A, g.a_rows, g.a_cols, BM)) return cudaErrorInvalidValue;
+    if (!encode_map(&p.tmB[i], g.B, g.b_rows, g.b_cols, uint32_t(g.mma_n))) return cudaErrorInvalidValue;
+    p.out[i] = g.out;
+    p.ld_out[i] = g.ld_out;
+    p.out_rows[i] = g.out_rows;
+    p.N[i] = g.N;
+    p.K[i] = g.K;
+    p.a_k_mod[i] = g.a_k_mod > 0 ? g.a_k_mod : g.K;
+    p.b_step[i] = g.b_rows_per_group;
+    p.mma_n[i] = g.mma_n;
+  }
+  p.offsets = offsets;
+  p.num_routed = num_routed;
+  p.rows_single0 = rows_single0;
+  p.shared_rows = c1 != nullptr ? shared_rows : 0;
+  p.status = status;
+  const int grid = int(max_tiles < num_sms() ? max_tiles : num_sms());
+  cudaError_t e;
+  switch (epi) {
+    case EPI_SWIGLU: e = launch_epi<EPI_SWIGLU>(p, grid, stream); break;
+    case EPI_STORE_BF16: e = launch_epi<EPI_STORE_BF16>(p, grid, stream); break;
+    default: e = launch_epi<EPI_STORE_F32>(p, grid, stream); break;
+  }
+  if (e == cudaSuccess && launches) ++*launches;
+  return e;
+}
+
+}  // namespace moe

@@ -1,0 +1,79 @@
+// Host-side launchers shared between the kernel files and the C ABI (api.cu).
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+#include "common.cuh"
+
+namespace moe {
+
+// ---------------------------------------------------------------- grouped GEMM
+// One operand class of the grouped GEMM: A [a_rows, K'] and B [b_rows, K] bf16,
+// both K-major (row-major with K contiguous).  Class 0 holds either the routed
+// groups (rows of group g start at offsets[g]) or a single group of
+// `rows_single0` rows; class 1 holds one group (the shared expert, T rows).
+struct GemmClass {
+  const void* A = nullptr;
+  int64_t a_rows = 0, a_cols = 0;
+  const void* B = nullptr;
+  int64_t b_rows = 0, b_cols = 0;
+  void* out = nullptr;
+  int64_t ld_out = 0;       // output row stride in elements
+  int64_t out_rows = 0;     // rows of the output buffer (store bound)
+  int N = 0;                // columns of D before the epilogue
+  int K = 0;                // reduction length (multiple of 64)
+  int a_k_mod = 0;          // A column = k % a_k_mod (K-split gate); = K otherwise
+  int b_rows_per_group = 0; // B row step between consecutive groups of the class
+  int mma_n = 256;          // MMA N (<= 256, multiple of 16); B box rows
+};
+
+enum EpiMode : int { EPI_SWIGLU = 0, EPI_STORE_BF16 = 1, EPI_STORE_F32 = 2 };
+
+int num_sms();
+
+// Records the next armed profiling event on `s` (no-op when disarmed).
+void profile_mark(cudaStream_t s);
+
+cudaError_t launch_grouped_gemm(int epi, const GemmClass& c0, const GemmClass* c1, const int32_t* offsets,
+                                int num_routed, int rows_single0, int shared_rows, int* status,
+                                long long max_tiles, cudaStream_t stream, int* launches);
+
+// ---------------------------------------------------------------------- router
+cudaError_t launch_gate_split(const float* wg, int E, int d, void* wsplit, cudaStream_t s, int* launches);
+cudaError_t launch_gate_logits_simt(const moe_config& c, const void* x, const void* wg, float* logits,
+                                    cudaStream_t s, int* launches);
+cudaError_t launch_topk(const moe_config& c, const float* logits, const float* bias, int32_t* idx, float* w,
+                        cudaStream_t s, int* launches);
+
+// ---------------------------------------------------------------- permutation
+int permute_chunks(int T);
+cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* idx, int32_t* counts,
+                           int32_t* offsets, int32_t* row2tok, int32_t* tok2row, void* x_perm,
+                           int32_t* chunk_counts, int32_t* chunk_base, int* status, cudaStream_t s,
+                           int* launches);
+
+// -------------------------------------------------------------------- experts
+cudaError_t launch_prepack(const moe_config& c, const void* W1, const void* W3, const void* W2,
+                           const void* Ws1, const void* Ws3, const void* Ws2, void* packed, cudaStream_t s,
+                           int* launches);
+cudaError_t launch_swiglu_simt_f32(const moe_config& c, const float* x_perm, const int32_t* offsets,
+                                   const float* x, const void* packed, float* h, float* hs, float* y,
+                                    float* ys, int* status, cudaStream_t s, int* launches);
+
+// -------------------------------------------------------------------- combine
+cudaError_t launch_combine(const moe_config& c, const void* y_perm, const void* y_shared,
+                           const int32_t* tok2row, const float* w, void* out, int* status, cudaStream_t s,
+                           int* launches);
+
+// Packed expert blob layout (byte offsets, each 256-byte aligned).
+struct PackedLayout {
+  size_t w13 = 0, w2 = 0, w13s = 0, w2s = 0, total = 0;
+  int bi = 0, bis = 0;   // interleave block of W1/W3 rows (routed, shared)
+};
+PackedLayout packed_layout(const moe_config& c);
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+inline size_t dtype_bytes(int dt) { return dt == MOE_BF16 ? 2 : 4; }
+
+}  // namespace moe

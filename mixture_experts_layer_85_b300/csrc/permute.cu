@@ -1,0 +1,192 @@
+// Dispatch of the (token, slot) assignments into expert-contiguous rows.
+//
+// The MoE listing of the DeepSeek-V2 walkthrough repeats every token k times
+// and, for each expert, gathers the rows routed to it.  Here that gather is a
+// deterministic counting sort: rows of expert e are its tokens in increasing
+// order, experts in increasing id, so counts, offsets and the row order are
+// exactly reproducible.
+//
+//   1. count    per 128-token chunk: a 128-bit token mask per expert in shared
+//               memory (atomicOr), popcounts -> chunk_counts[chunk][e]
+//   2. scan     one block per expert: chunk_base[chunk][e] (rank of the
+//               chunk's first token within expert e) and counts[e]; then one
+//               block: offsets[e] = exclusive prefix sum of counts
+//   3. scatter  per chunk: rank of a token inside its expert = popcount of the
+//               mask bits of earlier tokens -> row2tok / tok2row
+//   4. gather   x rows -> x_perm rows, 16-byte vectors, grid over all SMs
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int CHUNK = 128;   // tokens per chunk = 4 mask words per expert
+constexpr int WORDS = CHUNK / 32;
+constexpr int MAX_E = 256;
+
+__device__ __forceinline__ void build_masks(uint32_t (*mask)[WORDS], const int32_t* __restrict__ idx, int T, int E,
+                                            int k, int chunk, int* status) {
+  for (int i = threadIdx.x; i < E * WORDS; i += blockDim.x) mask[i / WORDS][i % WORDS] = 0u;
+  __syncthreads();
+  const int t = chunk * CHUNK + threadIdx.x;
+  if (t < T) {
+    for (int j = 0; j < k; ++j) {
+      const int e = idx[(long long)t * k + j];
+      if (e < 0 || e >= E) {
+        flag_status(status, DEV_BAD_EXPERT);
+        continue;
+      }
+      atomicOr(&mask[e][threadIdx.x >> 5], 1u << (threadIdx.x & 31));
+    }
+  }
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(CHUNK) permute_count_kernel(const int32_t* __restrict__ idx, int T, int E, int k,
+                                                              int32_t* __restrict__ chunk_counts, int* status) {
+  __shared__ uint32_t mask[MAX_E][WORDS];
+  build_masks(mask, idx, T, E, k, blockIdx.x, status);
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int n = 0;
+#pragma unroll
+    for (int w = 0; w < WORDS; ++w) n += __popc(mask[e][w]);
+    chunk_counts[(long long)blockIdx.x * E + e] = n;
+  }
+}
+
+// Block-wide exclusive scan of one int per thread (blockDim.x <= 1024).
+__device__ __forceinline__ int block_exclusive_scan(int v, int* total_out) {
+  __shared__ int warp_tot[32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int u = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += u;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  int before = 0, all = 0;
+  const int nw = (blockDim.x + 31) >> 5;
+  for (int w = 0; w < nw; ++w) {
+    if (w < warp) before += warp_tot[w];
+    all += warp_tot[w];
+  }
+  __syncthreads();
+  *total_out = all;
+  return before + incl - v;
+}
+
+// One block per expert: exclusive scan over chunks -> chunk_base[chunk][e]
+// (row of the chunk's first token within expert e), counts[e].
+__global__ void __launch_bounds__(CHUNK) permute_chunk_scan_kernel(const int32_t* __restrict__ chunk_counts,
+                                                                   int nchunks, int E,
+                                                                   int32_t* __restrict__ chunk_base,
+                                                                   int32_t* __restrict__ counts) {
+  const int e = blockIdx.x;
+  int carry = 0;
+  for (int c0 = 0; c0 < nchunks; c0 += blockDim.x) {
+    const int c = c0 + threadIdx.x;
+    const int v = c < nchunks ? chunk_counts[(long long)c * E + e] : 0;
+    int tot;
+    const int ex = block_exclusive_scan(v, &tot);
+    if (c < nchunks) chunk_base[(long long)c * E + e] = carry + ex;
+    carry += tot;
+  }
+  if (threadIdx.x == 0) counts[e] = carry;
+}
+
+// One block: offsets = exclusive prefix sum of counts over experts (E <= 256).
+__global__ void __launch_bounds__(256) permute_offsets_kernel(const int32_t* __restrict__ counts, int E,
+                                                              int32_t* __restrict__ offsets) {
+  const int e = threadIdx.x;
+  int tot;
+  const int ex = block_exclusive_scan(e < E ? counts[e] : 0, &tot);
+  if (e < E) offsets[e] = ex;
+  if (e == 0) offsets[E] = tot;
+}
+
+__global__ void __launch_bounds__(CHUNK) permute_scatter_kernel(const int32_t* __restrict__ idx, int T, int E, int k,
+                                                                const int32_t* __restrict__ chunk_base,
+                                                                const int32_t* __restrict__ offsets,
+                                                                int32_t* __restrict__ row2tok,
+                                                                int32_t* __restrict__ tok2row, int* status) {
+  __shared__ uint32_t mask[MAX_E][WORDS];
+  build_masks(mask, idx, T, E, k, blockIdx.x, nullptr);
+  const int t = blockIdx.x * CHUNK + threadIdx.x;
+  if (t >= T) return;
+  const int w = threadIdx.x >> 5;
+  const uint32_t below = (1u << (threadIdx.x & 31)) - 1u;
+  const long long R = (long long)T * k;
+  for (int j = 0; j < k; ++j) {
+    const int e = idx[(long long)t * k + j];
+    if (e < 0 || e >= E) {
+      tok2row[(long long)t * k + j] = -1;
+      continue;
+    }
+    int rank = __popc(mask[e][w] & below);
+    for (int ww = 0; ww < w; ++ww) rank += __popc(mask[e][ww]);
+    const long long row = (long long)offsets[e] + chunk_base[(long long)blockIdx.x * E + e] + rank;
+    if (row < 0 || row >= R) {
+      flag_status(status, DEV_BAD_ROW);
+      tok2row[(long long)t * k + j] = -1;
+      continue;
+    }
+    row2tok[row] = t;
+    tok2row[(long long)t * k + j] = (int32_t)row;
+  }
+}
+
+// x_perm[r] = x[row2tok[r]]; one warp per row, 16-byte vectors.
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ row2tok,
+                                                          long long R, int T, int vec_per_row, uint4* __restrict__ x_perm,
+                                                          int* status) {
+  const int lane = threadIdx.x & 31;
+  const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
+  for (long long r = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < R; r += warps) {
+    const int t = row2tok[r];
+    if (t < 0 || t >= T) {
+      if (lane == 0) flag_status(status, DEV_BAD_ROW);
+      continue;
+    }
+    const uint4* src = x + (long long)t * vec_per_row;
+    uint4* dst = x_perm + r * vec_per_row;
+    int v = lane;
+    for (; v + 96 < vec_per_row; v += 128) {
+      const uint4 a = src[v], b = src[v + 32], c = src[v + 64], d = src[v + 96];
+      dst[v] = a;
+      dst[v + 32] = b;
+      dst[v + 64] = c;
+      dst[v + 96] = d;
+    }
+    for (; v < vec_per_row; v += 32) dst[v] = src[v];
+  }
+}
+
+}  // namespace
+
+int permute_chunks(int T) { return (T + CHUNK - 1) / CHUNK; }
+
+cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* idx, int32_t* counts,
+                           int32_t* offsets, int32_t* row2tok, int32_t* tok2row, void* x_perm,
+                           int32_t* chunk_counts, int32_t* chunk_base, int* status, cudaStream_t s,
+                           int* launches) {
+  const int nch = permute_chunks(c.T);
+  permute_count_kernel<<<nch, CHUNK, 0, s>>>(idx, c.T, c.E, c.k, chunk_counts, status);
+  permute_chunk_scan_kernel<<<c.E, CHUNK, 0, s>>>(chunk_counts, nch, c.E, chunk_base, counts);
+  permute_offsets_kernel<<<1, 256, 0, s>>>(counts, c.E, offsets);
+  permute_scatter_kernel<<<nch, CHUNK, 0, s>>>(idx, c.T, c.E, c.k, chunk_base, offsets, row2tok, tok2row, status);
+  if (launches) *launches += 4;
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || x == nullptr || x_perm == nullptr) return e;
+  const long long R = (long long)c.T * c.k;
+  const int vec = int((size_t)c.d * dtype_bytes(c.act_dtype) / 16);
+  long long blocks = (R + 7) / 8;
+  const long long cap = 8LL * num_sms();
+  if (blocks > cap) blocks = cap;
+  gather_rows_kernel<<<(int)blocks, 256, 0, s>>>(static_cast<const uint4*>(x), row2tok, R, c.T, vec,
+                                                  static_cast<uint4*>(x_perm), status);
+  if (launches) ++*launches;
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -209,3 +209,39 @@ def small_workload(base: Workload, **kw) -> Workload:
     """A reduced copy of a workload for fast parity cases (same routing rules)."""
     name = kw.pop("name", base.name + "_small")
     return replace(base, name=name, **kw)
+
+
+# ------------------------------------------------------- stage-level test data
+SEED_STAGE = 1000
+
+
+def random_idx(T: int, E: int, k: int, seed: int, one_hot_expert: Optional[int] = None) -> torch.Tensor:
+    """[T,k] int32 expert choices, k distinct experts per token, seeded.  With
+    ``one_hot_expert`` every token's first choice is that expert (a degenerate,
+    maximally skewed load)."""
+    g = _gen(SEED_STAGE + seed)
+    keys = torch.rand((T, E), generator=g)
+    if one_hot_expert is not None:
+        keys[:, one_hot_expert] = -1.0
+    return keys.argsort(dim=1)[:, :k].to(torch.int32).contiguous()
+
+
+def random_rows(n: int, d: int, seed: int, dtype: torch.dtype = torch.bfloat16) -> torch.Tensor:
+    g = _gen(SEED_STAGE + seed)
+    return torch.randn((n, d), generator=g).to(dtype)
+
+
+def random_gates(T: int, k: int, seed: int) -> torch.Tensor:
+    g = _gen(SEED_STAGE + seed)
+    return torch.rand((T, k), generator=g).contiguous()
+
+
+def random_counts(E: int, R: int, seed: int) -> torch.Tensor:
+    """[E] int32 row counts summing to R: some experts empty, one large."""
+    g = _gen(SEED_STAGE + seed)
+    w = torch.rand((E,), generator=g)
+    w[torch.randperm(E, generator=g)[: max(1, E // 4)]] = 0.0
+    w[int(torch.randint(E, (1,), generator=g))] += w.sum() + 1.0
+    c = torch.floor(w / w.sum() * R).to(torch.int64)
+    c[int(torch.argmax(w))] += R - int(c.sum())
+    return c.to(torch.int32)

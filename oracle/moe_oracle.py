@@ -271,6 +271,21 @@ def experts_forward(x: np.ndarray, idx: np.ndarray, gates: np.ndarray,
     return out
 
 
+def combine(y_rows: np.ndarray, y_shared: Optional[np.ndarray], tok2row: np.ndarray,
+            gates: np.ndarray) -> np.ndarray:
+    """out_t = sum_j g_{t,j} * y_rows[tok2row[t,j]] + y_shared[t]: the ``MoE``
+    listing's gate-weighted sum over the k slots of a token plus the shared
+    experts, with the slot rows stored in expert-contiguous order."""
+    y_rows = np.asarray(y_rows, np.float64)
+    T, k = tok2row.shape
+    out = np.zeros((T, y_rows.shape[1]), np.float64)
+    for j in range(k):
+        out += np.asarray(gates, np.float64)[:, j:j + 1] * y_rows[tok2row[:, j]]
+    if y_shared is not None:
+        out += np.asarray(y_shared, np.float64)
+    return out
+
+
 def moe_forward(x, wg, bias, expert: ExpertFn, shared, cfg: OracleConfig,
                 idx_override: Optional[np.ndarray] = None):
     """Whole layer for the tokens in ``x``.  ``idx_override`` re-evaluates the

@@ -295,6 +295,23 @@ def pin_symmetries(o=orc):
     assert np.allclose(out4, 2.0 * out, rtol=1e-12, atol=1e-13)
 
 
+def pin_combine(o=orc):
+    """Rows in (token, slot) order: combine is the listing's
+    (y.view(T,k,d) * w[..., None]).sum(1) + shared, written here with torch."""
+    r = _rng(15)
+    T, k, d = 11, 3, 5
+    y = r.standard_normal((T * k, d))
+    ys = r.standard_normal((T, d))
+    g = r.uniform(0, 1, (T, k))
+    tok2row = np.arange(T * k).reshape(T, k)
+    want = (torch.tensor(y).view(T, k, d) * torch.tensor(g)[..., None]).sum(1) + torch.tensor(ys)
+    assert np.allclose(o.combine(y, ys, tok2row, g), want.numpy(), rtol=1e-13, atol=1e-14)
+    # any row order: permuting the stored rows together with tok2row changes nothing
+    perm = r.permutation(T * k)
+    inv = np.argsort(perm)
+    assert np.allclose(o.combine(y[perm], ys, inv[tok2row], g), want.numpy(), rtol=1e-13, atol=1e-14)
+
+
 ALL_PINS = [pin_brute_force_selection, pin_greedy_is_torch_topk, pin_invariants,
             pin_bias_only_steers_selection, pin_zero_gates_give_shared, pin_group1_is_greedy,
-            pin_single_expert, pin_dense_einsum, pin_top1, pin_permutation, pin_symmetries]
+            pin_single_expert, pin_dense_einsum, pin_top1, pin_permutation, pin_symmetries, pin_combine]

@@ -1,0 +1,287 @@
+"""Parity of the CUDA library (through the C ABI) with the fp64 CPU oracle.
+
+Every input comes from the seeded generator; the oracle sees byte-identical
+copies.  Acceptance (layer spec): expert indices set-exact on every token that
+is not a near tie (near-tie tokens are counted and their GPU choice must be a
+valid top-k); gate values within 1e-5 relative; counts / offsets / row order
+bit-exact; outputs max|GPU - oracle| / RMS(oracle) <= 2e-2 (bf16) or 1e-4
+(fp32).  Small cases span several tiles with ragged tails and are checked on
+every token; the full-size workloads run in the benchmark's launch
+configuration and are checked on all routing decisions and on sampled
+output rows."""
+import numpy as np
+import pytest
+import torch
+
+from mixture_experts_layer_85_b300 import _lib, inputs
+from mixture_experts_layer_85_b300.layer import MoELayer
+from oracle import moe_oracle as orc
+from tests._cfg import expert_accessor, f64, oracle_cfg
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"bf16": 2e-2, "f32": 1e-4}
+GATE_RTOL = 1e-5
+
+W = inputs.WORKLOADS
+SMALL = {
+    # softmax greedy, fp32 gate weight split over three bf16 MMAs (T >= 1024)
+    "v2lite_small_t1037": inputs.small_workload(W["v2lite_t4096"], name="v2lite_small_t1037", T=1037, d=384,
+                                                E=16, I=256, k=6, n_shared=2),
+    # softmax group-limited (max), scale 16, SIMT gate
+    "v2_small_t515": inputs.small_workload(W["v2_t8192"], name="v2_small_t515", T=515, d=256, E=32, I=128,
+                                           n_group=8, topk_group=3),
+    # sigmoid + bias, group-limited sum of top-2, renormalised, scale 2.5
+    "v3_small_t333": inputs.small_workload(W["v3_prefill_t16384"], name="v3_small_t333", T=333, d=512, E=64,
+                                           I=256, n_group=8, topk_group=4),
+    # tensor-core gate path with bf16 gate weights, ragged last tile
+    "v3_small_t1100": inputs.small_workload(W["v3_prefill_t16384"], name="v3_small_t1100", T=1100, d=512,
+                                            E=64, I=128, n_group=8, topk_group=4),
+    # decode-sized batches
+    "v3_small_t1": inputs.small_workload(W["v3_prefill_t16384"], name="v3_small_t1", T=1, d=512, E=64, I=256,
+                                         n_group=8, topk_group=4),
+    "v3_small_t3": inputs.small_workload(W["v3_prefill_t16384"], name="v3_small_t3", T=3, d=512, E=64, I=256,
+                                         n_group=8, topk_group=4),
+}
+
+
+def _np(t):
+    return t.detach().cpu().numpy()
+
+
+def oracle_route(li, wl):
+    bias = None if li.bias is None else _np(li.bias.float())
+    return orc.route(orc.gate_logits(f64(li.x), f64(li.wg)), bias, oracle_cfg(wl))
+
+
+def check_routing(gidx, gw, r, wl):
+    """Returns (near-tie tokens, near-tie tokens whose choice differs)."""
+    cfg = oracle_cfg(wl)
+    gidx = np.asarray(gidx, np.int64)
+    same = (np.sort(gidx, 1) == np.sort(r.idx, 1)).all(1)
+    near = r.near_tie
+    bad = ~same & ~near
+    assert not bad.any(), f"expert sets differ on {int(bad.sum())} non-tie tokens, e.g. {np.nonzero(bad)[0][:5]}"
+    differ = ~same & near
+    for t in np.nonzero(differ)[0]:
+        assert orc.is_valid_selection(gidx[t], r.sel32[t], cfg), t
+    # gate values, matched per expert, on tokens with the same set
+    og = np.take_along_axis(r.gates, np.argsort(r.idx, 1), 1)
+    gg = np.take_along_axis(np.asarray(gw, np.float64), np.argsort(gidx, 1), 1)
+    rel = np.abs(gg - og) / np.maximum(np.abs(og), 1e-30)
+    assert rel[same].max(initial=0.0) <= GATE_RTOL, rel[same].max()
+    # reported order: selection score descending (up to the tie tolerance)
+    sel = r.scores + (0.0 if r.sel32 is None else (r.sel32.astype(np.float64) - r.scores.astype(np.float32)))
+    rows = np.arange(gidx.shape[0])[:, None]
+    s_ord = r.sel32.astype(np.float64)[rows, gidx]
+    tol = orc.NEAR_TIE_REL * np.abs(r.sel32).max(1, keepdims=True)
+    assert (np.diff(s_ord, axis=1) <= tol).all()
+    return int(near.sum()), int(differ.sum())
+
+
+def check_counts(gcounts, gidx, r, wl, n_differ):
+    gcounts = np.asarray(gcounts, np.int64)
+    assert gcounts.sum() == wl.T * wl.k
+    assert np.array_equal(gcounts, np.bincount(np.asarray(gidx).ravel(), minlength=wl.E))
+    assert np.abs(gcounts - r.counts).sum() <= 2 * wl.k * n_differ
+
+
+def shared_of(li):
+    return None if li.wl.n_shared == 0 else (f64(li.ws1), f64(li.ws3), f64(li.ws2))
+
+
+def run_layer(wl, li):
+    layer = MoELayer(wl, li, "cuda")
+    T, k, E = wl.T, wl.k, wl.E
+    idx = torch.full((T, k), -7, dtype=torch.int32, device="cuda")
+    w = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    counts = torch.empty((E,), dtype=torch.int32, device="cuda")
+    out = layer.forward(li.x, idx=idx, w=w, counts=counts)
+    code, word = layer.device_status()
+    assert code == _lib.MOE_OK, (_lib.moe_status_string(code), word)
+    return layer, out, idx, w, counts
+
+
+def check_layer(wl, li, out, idx, w, counts, sample=None):
+    r = oracle_route(li, wl)
+    gidx, gw = _np(idx), _np(w)
+    n_near, n_differ = check_routing(gidx, gw, r, wl)
+    check_counts(_np(counts), gidx, r, wl, n_differ)
+    toks = np.arange(wl.T) if sample is None else sample
+    keep = np.array([np.array_equal(np.sort(gidx[t]), np.sort(r.idx[t])) for t in toks])
+    toks = toks[keep]
+    x = f64(li.x)[toks]
+    want = orc.experts_forward(x, r.idx[toks], r.gates[toks], expert_accessor(li.w1, li.w3, li.w2), shared_of(li),
+                               wl.E)
+    got = f64(out)[toks]
+    err = orc.relative_error(got, want)
+    assert err <= TOL[wl.act_dtype], err
+    return {"near_tie": n_near, "near_tie_differ": n_differ, "err": err, "checked_tokens": int(toks.size)}
+
+
+# ----------------------------------------------------------------- full layer
+
+def test_tiny_fp32_layer():
+    wl = W["tiny_fp32_t128"]
+    li = inputs.make_inputs(wl, "cuda")
+    _, out, idx, w, counts = run_layer(wl, li)
+    info = check_layer(wl, li, out, idx, w, counts)
+    assert info["err"] <= 1e-4
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_small_bf16_layer(name):
+    wl = SMALL[name]
+    li = inputs.make_inputs(wl, "cuda")
+    _, out, idx, w, counts = run_layer(wl, li)
+    check_layer(wl, li, out, idx, w, counts)
+
+
+FULL = ["v2lite_t4096", "v2_t8192", "v3_prefill_t16384", "v3_decode_t1", "v3_decode_t8", "v3_decode_t64",
+        "v3_decode_t512"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_layer(name):
+    """Full workload in the benchmark's launch configuration: every routing
+    decision against the oracle, sampled output rows against the oracle."""
+    wl = W[name]
+    li = inputs.make_inputs(wl, "cuda")
+    _, out, idx, w, counts = run_layer(wl, li)
+    n_sample = min(wl.T, 24 if wl.d >= 7168 else 48)
+    sample = np.sort(np.random.default_rng(7).choice(wl.T, n_sample, replace=False))
+    info = check_layer(wl, li, out, idx, w, counts, sample=sample)
+    print(name, info)
+    del li, out
+    torch.cuda.empty_cache()
+
+
+def test_forward_equals_staged_calls():
+    """moe_forward == gate_topk -> permute -> grouped_swiglu -> combine, bit for bit."""
+    wl = SMALL["v3_small_t333"]
+    li = inputs.make_inputs(wl, "cuda")
+    layer = MoELayer(wl, li, "cuda")
+    out = layer.forward(li.x)
+    o = layer.forward_staged(li.x)
+    torch.cuda.synchronize()
+    assert torch.equal(out, o["out"])
+
+
+def test_deterministic_across_runs():
+    wl = SMALL["v2_small_t515"]
+    li = inputs.make_inputs(wl, "cuda")
+    layer = MoELayer(wl, li, "cuda")
+    a = layer.forward(li.x).clone()
+    b = layer.forward(li.x)
+    assert torch.equal(a, b)
+
+
+# ------------------------------------------------------------ stage by stage
+
+@pytest.mark.parametrize("name", ["v2lite_t4096", "v2_t8192", "v3_prefill_t16384"])
+def test_gate_topk_full_size(name):
+    wl = W[name]
+    li_x = inputs.make_tokens(wl)
+    wg, bias = inputs.make_router(wl)
+    cfg = _lib.make_config(wl)
+    ws = torch.empty(_lib.moe_workspace_size(cfg), dtype=torch.uint8, device="cuda")
+    idx = torch.empty((wl.T, wl.k), dtype=torch.int32, device="cuda")
+    w = torch.empty((wl.T, wl.k), dtype=torch.float32, device="cuda")
+    _lib.moe_gate_topk(cfg, li_x.cuda(), wg.cuda(), None if bias is None else bias.cuda(), idx, w, ws)
+    assert _lib.moe_get_device_status(ws)[0] == _lib.MOE_OK
+    r = orc.route(orc.gate_logits(f64(li_x), f64(wg)), None if bias is None else bias.numpy(), oracle_cfg(wl))
+    n_near, _ = check_routing(_np(idx), _np(w), r, wl)
+    assert n_near <= max(2, wl.T // 1000)
+
+
+@pytest.mark.parametrize("T,E,k,one_hot", [(1, 256, 8, None), (5, 12, 4, None), (128, 64, 6, None),
+                                           (129, 64, 6, None), (4133, 256, 8, None), (300, 16, 1, 3),
+                                           (777, 160, 6, 0)])
+def test_permute_bit_exact(T, E, k, one_hot):
+    wl = inputs.small_workload(W["v2lite_t4096"], name="perm", T=T, d=128, E=E, I=128, k=k)
+    cfg = _lib.make_config(wl)
+    idx = inputs.random_idx(T, E, k, seed=T + E, one_hot_expert=one_hot)
+    x = inputs.random_rows(T, wl.d, seed=T)
+    ws = torch.empty(_lib.moe_workspace_size(cfg), dtype=torch.uint8, device="cuda")
+    dev = {n: torch.empty(s, dtype=torch.int32, device="cuda") for n, s in
+           [("counts", (E,)), ("offsets", (E + 1,)), ("row2tok", (T * k,)), ("tok2row", (T, k))]}
+    x_perm = torch.empty((T * k, wl.d), dtype=torch.bfloat16, device="cuda")
+    _lib.moe_permute(cfg, x.cuda(), idx.cuda(), dev["counts"], dev["offsets"], dev["row2tok"], dev["tok2row"],
+                     x_perm, ws)
+    assert _lib.moe_get_device_status(ws)[0] == _lib.MOE_OK
+    counts, offsets, row2tok, tok2row = orc.permutation(idx.numpy(), E)
+    assert np.array_equal(_np(dev["counts"]), counts)
+    assert np.array_equal(_np(dev["offsets"]), offsets)
+    assert np.array_equal(_np(dev["row2tok"]), row2tok)
+    assert np.array_equal(_np(dev["tok2row"]), tok2row)
+    assert torch.equal(x_perm.cpu(), x[torch.from_numpy(row2tok)])
+
+
+@pytest.mark.parametrize("name,seed", [("v3_small_t333", 1), ("v2lite_small_t1037", 2), ("v3_small_t1", 3)])
+def test_grouped_swiglu_rows(name, seed):
+    """Experts on seeded rows with seeded group sizes (empty experts, one big)."""
+    wl = SMALL[name]
+    cfg = _lib.make_config(wl)
+    R = wl.T * wl.k
+    counts = inputs.random_counts(wl.E, R, seed)
+    offsets = torch.zeros(wl.E + 1, dtype=torch.int32)
+    offsets[1:] = torch.cumsum(counts, 0)
+    x_perm = inputs.random_rows(R, wl.d, seed)
+    x = inputs.random_rows(wl.T, wl.d, seed + 100)
+    w1, w3, w2, ws1, ws3, ws2 = inputs.make_experts(wl, "cuda")
+    packed = torch.empty(_lib.moe_packed_size(cfg), dtype=torch.uint8, device="cuda")
+    _lib.moe_prepack_experts(cfg, w1, w3, w2, ws1, ws3, ws2, packed)
+    ws = torch.empty(_lib.moe_workspace_size(cfg), dtype=torch.uint8, device="cuda")
+    y = torch.empty((R, wl.d), dtype=torch.bfloat16, device="cuda")
+    ys = torch.empty((wl.T, wl.d), dtype=torch.bfloat16, device="cuda")
+    _lib.moe_grouped_swiglu(cfg, x_perm.cuda(), offsets.cuda(), x.cuda(), packed, y, ys, ws)
+    assert _lib.moe_get_device_status(ws)[0] == _lib.MOE_OK
+    want = np.zeros((R, wl.d))
+    xp = f64(x_perm)
+    for e in range(wl.E):
+        a, b = int(offsets[e]), int(offsets[e + 1])
+        if b > a:
+            want[a:b] = orc.swiglu_ffn(xp[a:b], f64(w1[e]), f64(w3[e]), f64(w2[e]))
+    assert orc.relative_error(f64(y), want) <= TOL["bf16"]
+    want_s = orc.swiglu_ffn(f64(x), f64(ws1), f64(ws3), f64(ws2))
+    assert orc.relative_error(f64(ys), want_s) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_combine(dtype):
+    T, k, d = 301, 6, 256
+    wl = inputs.small_workload(W["v2lite_t4096"], name="comb", T=T, d=d, E=16, I=128, k=k, act_dtype=dtype)
+    cfg = _lib.make_config(wl)
+    tdt = inputs.torch_dtype(dtype)
+    y = inputs.random_rows(T * k, d, 11, tdt)
+    ys = inputs.random_rows(T, d, 12, tdt)
+    g = inputs.random_gates(T, k, 13)
+    tok2row = torch.randperm(T * k, generator=torch.Generator().manual_seed(14)).view(T, k).to(torch.int32)
+    ws = torch.empty(_lib.moe_workspace_size(cfg), dtype=torch.uint8, device="cuda")
+    out = torch.empty((T, d), dtype=tdt, device="cuda")
+    _lib.moe_combine(cfg, y.cuda(), ys.cuda(), tok2row.cuda(), g.cuda(), out, ws)
+    assert _lib.moe_get_device_status(ws)[0] == _lib.MOE_OK
+    want = orc.combine(f64(y), f64(ys), tok2row.numpy().astype(np.int64), g.double().numpy())
+    assert orc.relative_error(f64(out), want) <= TOL[dtype]
+
+
+def test_out_of_range_expert_is_flagged_not_faulted():
+    """An idx entry outside [0,E) is skipped by the permutation and reported
+    through the status word; the context stays usable."""
+    T, E, k = 64, 16, 2
+    wl = inputs.small_workload(W["v2lite_t4096"], name="bad", T=T, d=128, E=E, I=128, k=k)
+    cfg = _lib.make_config(wl)
+    idx = inputs.random_idx(T, E, k, seed=5)
+    idx[7, 1] = E + 3
+    ws = torch.empty(_lib.moe_workspace_size(cfg), dtype=torch.uint8, device="cuda")
+    row2tok = torch.full((T * k,), -1, dtype=torch.int32, device="cuda")
+    bufs = [torch.zeros(s, dtype=torch.int32, device="cuda") for s in [(E,), (E + 1,), (T, k)]]
+    x_perm = torch.zeros((T * k, wl.d), dtype=torch.bfloat16, device="cuda")
+    _lib.moe_permute(cfg, inputs.random_rows(T, wl.d, 1).cuda(), idx.cuda(), bufs[0], bufs[1], row2tok, bufs[2],
+                     x_perm, ws)
+    code, word = _lib.moe_get_device_status(ws)
+    assert code == _lib.MOE_ERR_DEVICE_BOUNDS and word != 0
+    assert int(bufs[0].sum()) == T * k - 1
+    # the context is still fine
+    torch.cuda.synchronize()
+    assert float(torch.ones(4, device="cuda").sum()) == 4.0

@@ -1,0 +1,102 @@
+"""The C ABI library on the CPU: it loads, exports every declared symbol, and
+rejects bad arguments on the host before any launch (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from mixture_experts_layer_85_b300 import _lib, inputs
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_symbols():
+    src = open(os.path.join(ROOT, "include", "moe.h")).read()
+    return re.findall(r"^MOE_API\s+[\w\s\*]+?\b(moe_\w+)\(", src, flags=re.M)
+
+
+def test_exports_every_declared_symbol():
+    names = declared_symbols()
+    assert len(names) >= 12
+    lib = ctypes.CDLL(_lib.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert sorted(names) == sorted(_lib.EXPORTED)
+
+
+def test_status_strings():
+    for code in range(7):
+        assert _lib.moe_status_string(code).startswith("MOE_")
+    assert _lib.moe_status_string(99) == "MOE_ERR_UNKNOWN"
+
+
+@pytest.mark.parametrize("name", inputs.CONFIG_ORDER)
+def test_sizes_for_every_workload(name):
+    wl = inputs.WORKLOADS[name]
+    cfg = _lib.make_config(wl)
+    ws = _lib.moe_workspace_size(cfg)
+    pk = _lib.moe_packed_size(cfg)
+    eb = 2 if wl.act_dtype == "bf16" else 4
+    # packed blob holds all expert weights exactly once (plus alignment)
+    weights = (3 * wl.E * wl.I * wl.d + 3 * wl.I_s * wl.d) * eb
+    assert weights <= pk <= weights + 4 * 256
+    # workspace holds at least the permuted rows, hidden and outputs
+    assert ws >= (2 * wl.R * wl.d + wl.R * wl.I) * eb
+    assert _lib.moe_forward_kernel_count(cfg) >= 9
+
+
+def _cfg(**kw):
+    c = _lib.make_config(inputs.WORKLOADS["v3_prefill_t16384"])
+    for k, v in kw.items():
+        setattr(c, k, v)
+    return c
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(E=0), _lib.MOE_ERR_INVALID_ARG),
+    (dict(k=300), _lib.MOE_ERR_INVALID_ARG),
+    (dict(act_dtype=7), _lib.MOE_ERR_INVALID_ARG),
+    (dict(n_group=3), _lib.MOE_ERR_INVALID_ARG),            # 256 % 3 != 0
+    (dict(topk_group=9), _lib.MOE_ERR_INVALID_ARG),         # > n_group
+    (dict(topk_group=1, k=40), _lib.MOE_ERR_INVALID_ARG),   # k > experts in kept groups
+    (dict(group_top=0), _lib.MOE_ERR_INVALID_ARG),
+    (dict(T=-1), _lib.MOE_ERR_INVALID_ARG),
+    (dict(T=1 << 28), _lib.MOE_ERR_INVALID_ARG),            # T*k overflows the row index
+    (dict(E=512, n_group=8), _lib.MOE_ERR_UNSUPPORTED),
+    (dict(I=2000), _lib.MOE_ERR_UNSUPPORTED),               # bf16 tiles need I % 128 == 0
+    (dict(d=7000), _lib.MOE_ERR_UNSUPPORTED),
+])
+def test_bad_config_rejected(kw, code):
+    c = _cfg(**kw)
+    n = ctypes.c_size_t(0)
+    assert _lib.raw_call("moe_workspace_size", ctypes.byref(c), ctypes.byref(n)) == code
+
+
+def test_null_and_misaligned_pointers_rejected_before_launch():
+    c = _cfg(T=64)
+    ws_need = _lib.moe_workspace_size(c)
+    fake = 1 << 40                     # never dereferenced: validation fails first
+    assert _lib.raw_call("moe_forward", ctypes.byref(c), None, fake, None, fake, fake, None, None, None,
+                         fake, ws_need, None) == _lib.MOE_ERR_INVALID_ARG
+    assert _lib.raw_call("moe_forward", ctypes.byref(c), fake + 8, fake, None, fake, fake, None, None, None,
+                         fake, ws_need, None) == _lib.MOE_ERR_INVALID_ARG
+    assert _lib.raw_call("moe_forward", ctypes.byref(c), fake, fake, None, fake, fake, None, None, None,
+                         fake, ws_need - 1, None) == _lib.MOE_ERR_WORKSPACE
+    assert _lib.raw_call("moe_gate_topk", ctypes.byref(c), fake, fake, None, None, fake, fake, ws_need,
+                         None) == _lib.MOE_ERR_INVALID_ARG
+    assert _lib.raw_call("moe_prepack_experts", ctypes.byref(c), fake, fake, fake, fake, fake, fake, fake, 16,
+                         None) == _lib.MOE_ERR_WORKSPACE
+    assert _lib.raw_call("moe_combine", None, fake, fake, fake, fake, fake, fake, ws_need,
+                         None) == _lib.MOE_ERR_INVALID_ARG
+
+
+def test_empty_batch_launches_nothing():
+    c = _cfg(T=0)
+    before = _lib.moe_launch_count()
+    fake = 1 << 40
+    ws = _lib.moe_workspace_size(c)
+    assert _lib.raw_call("moe_forward", ctypes.byref(c), fake, fake, None, fake, fake, None, None, None,
+                         fake, ws, None) == _lib.MOE_OK
+    assert _lib.moe_forward_kernel_count(c) == 0
+    assert _lib.moe_launch_count() == before

@@ -14,6 +14,7 @@ _real_route = orc.route
 _real_swiglu = orc.swiglu_ffn
 _real_experts_forward = orc.experts_forward
 _real_permutation = orc.permutation
+_real_combine = orc.combine
 
 
 def _route_ties_high(logits, bias, cfg):
@@ -88,6 +89,10 @@ def _permutation_reversed(idx, E):
     return counts, offsets, row2tok, tok2row
 
 
+def _combine_slot_swap(y_rows, y_shared, tok2row, gates):
+    return _real_combine(y_rows, y_shared, tok2row, gates[:, ::-1])
+
+
 MUTANTS = [
     ("route", _route_ties_high, pins.pin_brute_force_selection),
     ("route", _route_biased_gates, pins.pin_bias_only_steers_selection),
@@ -100,6 +105,7 @@ MUTANTS = [
     ("experts_forward", _experts_no_shared, pins.pin_zero_gates_give_shared),
     ("experts_forward", _experts_with_residual, pins.pin_zero_gates_give_shared),
     ("permutation", _permutation_reversed, pins.pin_permutation),
+    ("combine", _combine_slot_swap, pins.pin_combine),
 ]
 
 

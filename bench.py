@@ -158,9 +158,10 @@ def layer_bytes(wl, counts: np.ndarray) -> float:
     """Bytes the method must move: x in, out, W_g, idx/w, the weights of the
     experts that received tokens, the shared weights."""
     eb = 2 if wl.act_dtype == "bf16" else 4
+    ob = 2 if wl.out_dtype == "bf16" else 4
     gb = 2 if wl.gate_w_dtype == "bf16" else 4
     touched = int((counts > 0).sum())
-    return (2 * wl.T * wl.d * eb + wl.E * wl.d * gb + wl.T * wl.k * 8
+    return (wl.T * wl.d * (eb + ob) + wl.E * wl.d * gb + wl.T * wl.k * 8
             + touched * 3 * wl.d * wl.I * eb + 3 * wl.d * wl.I_s * eb)
 
 
@@ -237,7 +238,7 @@ def run_ours(args, world, rank):
     li = inputs.make_inputs(wl, dev)
     layer = MoELayer(wl, li, dev)
     x = li.x
-    out = torch.empty((wl.T, wl.d), dtype=x.dtype, device=dev)
+    out = torch.empty((wl.T, wl.d), dtype=inputs.torch_dtype(wl.out_dtype), device=dev)
     counts = torch.empty((wl.E,), dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream()
 
@@ -305,7 +306,7 @@ def run_ours(args, world, rank):
 
     # end to end through the C ABI with host buffers: H2D of x, forward, D2H of out
     x_h = x.cpu().pin_memory()
-    out_h = torch.empty((wl.T, wl.d), dtype=x.dtype).pin_memory()
+    out_h = torch.empty((wl.T, wl.d), dtype=out.dtype).pin_memory()
     x_d = torch.empty_like(x)
     for _ in range(2):
         x_d.copy_(x_h, non_blocking=True)
@@ -325,7 +326,7 @@ def run_ours(args, world, rank):
     e2e_s = max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
     eb = x.element_size()
     e2e = {"value": round(whole_job_rate(wl.T * K, world, e2e_s), 1), "unit": UNIT,
-           "h2d_bytes_per_step": wl.T * wl.d * eb, "d2h_bytes_per_step": wl.T * wl.d * eb}
+           "h2d_bytes_per_step": wl.T * wl.d * eb, "d2h_bytes_per_step": wl.T * wl.d * out.element_size()}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -24,9 +24,12 @@
  *    moe_get_device_status() reads it (bounds violations, device-side wait
  *    time-outs).  Kernels never trap or assert.
  *  - Two calls sharing one `ws` must not run concurrently.
- *  - Activation dtype (x, permuted rows, outputs) is cfg->act_dtype: MOE_F32
- *    runs SIMT fp32 kernels; MOE_BF16 runs the tcgen05 tensor-core kernels
- *    with fp32 accumulation.
+ *  - Activation dtype (x, permuted rows, expert outputs) is cfg->act_dtype:
+ *    MOE_F32 runs SIMT fp32 kernels; MOE_BF16 runs the tcgen05 tensor-core
+ *    kernels with fp32 accumulation.  Expert outputs are stored in act_dtype
+ *    (the MoE listing casts each expert's output to x.dtype); the gate-weighted
+ *    sum is formed in fp32 and stored as cfg->out_dtype (MOE_F32 keeps the
+ *    listing's fp32 result of multiplying by the fp32 gate weights).
  */
 #ifndef MOE_B300_H
 #define MOE_B300_H
@@ -77,8 +80,9 @@ typedef struct moe_config {
   int32_t group_top;
   int32_t norm_topk;
   float routed_scaling_factor;
-  int32_t act_dtype;       /* moe_dtype of x, experts, outputs */
-  int32_t gate_w_dtype;    /* moe_dtype of W_g                 */
+  int32_t act_dtype;       /* moe_dtype of x, expert weights and rows */
+  int32_t gate_w_dtype;    /* moe_dtype of W_g                        */
+  int32_t out_dtype;       /* moe_dtype of the layer output h'        */
 } moe_config;
 
 /* Bytes of workspace every compute call needs for `cfg`. */
@@ -130,7 +134,7 @@ MOE_API moe_status moe_grouped_swiglu(const moe_config* cfg, const void* x_perm,
 /* Combine (MoE listing: gate-weighted sum over the k slots plus the shared
  * expert; the dense einsum form of the intelliparadigm.com page 3.3.3).
  *   out[t] = sum_j w[t,j] * y_perm[tok2row[t,j]] + y_shared[t], accumulated in
- *   fp32 in slot order j = 0..k-1 (deterministic), stored as act_dtype. */
+ *   fp32 in slot order j = 0..k-1 (deterministic), stored as out_dtype. */
 MOE_API moe_status moe_combine(const moe_config* cfg, const void* y_perm, const void* y_shared,
                        const int32_t* tok2row, const float* w, void* out,
                        void* ws, size_t ws_bytes, void* stream);

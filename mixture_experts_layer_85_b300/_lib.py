@@ -39,7 +39,7 @@ class moe_config(ctypes.Structure):
                 ("topk_method", ctypes.c_int32), ("n_group", ctypes.c_int32), ("topk_group", ctypes.c_int32),
                 ("group_score", ctypes.c_int32), ("group_top", ctypes.c_int32), ("norm_topk", ctypes.c_int32),
                 ("routed_scaling_factor", ctypes.c_float), ("act_dtype", ctypes.c_int32),
-                ("gate_w_dtype", ctypes.c_int32)]
+                ("gate_w_dtype", ctypes.c_int32), ("out_dtype", ctypes.c_int32)]
 
 
 _P = ctypes.c_void_p
@@ -100,6 +100,7 @@ def make_config(wl, T: Optional[int] = None) -> moe_config:
     c.routed_scaling_factor = wl.routed_scaling_factor
     c.act_dtype = MOE_BF16 if wl.act_dtype == "bf16" else MOE_F32
     c.gate_w_dtype = MOE_BF16 if wl.gate_w_dtype == "bf16" else MOE_F32
+    c.out_dtype = MOE_BF16 if wl.out_dtype == "bf16" else MOE_F32
     return c
 
 

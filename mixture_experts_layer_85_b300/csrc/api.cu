@@ -77,6 +77,7 @@ moe_status check_config(const moe_config* cp) {
   if (c.T < 0 || c.d <= 0 || c.E <= 0 || c.I <= 0 || c.k <= 0 || c.n_shared < 0) return MOE_ERR_INVALID_ARG;
   if (c.act_dtype != MOE_F32 && c.act_dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
   if (c.gate_w_dtype != MOE_F32 && c.gate_w_dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+  if (c.out_dtype != MOE_F32 && c.out_dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
   if (c.score_fn != MOE_SCORE_SOFTMAX && c.score_fn != MOE_SCORE_SIGMOID) return MOE_ERR_INVALID_ARG;
   if (c.topk_method != MOE_TOPK_GREEDY && c.topk_method != MOE_TOPK_GROUP_LIMITED) return MOE_ERR_INVALID_ARG;
   if (c.k > c.E) return MOE_ERR_INVALID_ARG;

@@ -161,13 +161,37 @@ template <> struct Vec16<__nv_bfloat16> {
   }
 };
 
+template <typename O, int N> struct StoreN;
+template <> struct StoreN<float, 8> {
+  static __device__ __forceinline__ void st(float* p, const float* f) {
+    reinterpret_cast<float4*>(p)[0] = make_float4(f[0], f[1], f[2], f[3]);
+    reinterpret_cast<float4*>(p)[1] = make_float4(f[4], f[5], f[6], f[7]);
+  }
+};
+template <> struct StoreN<float, 4> {
+  static __device__ __forceinline__ void st(float* p, const float* f) {
+    reinterpret_cast<float4*>(p)[0] = make_float4(f[0], f[1], f[2], f[3]);
+  }
+};
+template <> struct StoreN<__nv_bfloat16, 8> {
+  static __device__ __forceinline__ void st(__nv_bfloat16* p, const float* f) {
+    *reinterpret_cast<uint4*>(p) = Vec16<__nv_bfloat16>::store(f);
+  }
+};
+template <> struct StoreN<__nv_bfloat16, 4> {
+  static __device__ __forceinline__ void st(__nv_bfloat16* p, const float* f) {
+    __nv_bfloat162 a = __floats2bfloat162_rn(f[0], f[1]), b = __floats2bfloat162_rn(f[2], f[3]);
+    *reinterpret_cast<uint2*>(p) = make_uint2(*reinterpret_cast<uint32_t*>(&a), *reinterpret_cast<uint32_t*>(&b));
+  }
+};
+
 // out[t] = sum_j w[t,j] * y_perm[tok2row[t,j]] + y_shared[t], fp32 accumulation
-// in slot order.  One block per token (grid-stride), 16-byte vectors.
-template <typename T, int MAXK>
+// in slot order.  One block per token (grid-stride), 16-byte vector loads.
+template <typename T, typename O, int MAXK>
 __global__ void __launch_bounds__(128) combine_kernel(const uint4* __restrict__ y_perm, const uint4* __restrict__ y_shared,
                                                       const int32_t* __restrict__ tok2row, const float* __restrict__ w,
                                                       int Tn, int k, long long R, int vec_per_row,
-                                                      uint4* __restrict__ out, int* status) {
+                                                      O* __restrict__ out, int* status) {
   constexpr int N = Vec16<T>::N;
   for (int t = blockIdx.x; t < Tn; t += gridDim.x) {
     long long rows[MAXK];
@@ -205,9 +229,21 @@ __global__ void __launch_bounds__(128) combine_kernel(const uint4* __restrict__ 
 #pragma unroll
         for (int i = 0; i < N; ++i) acc[i] += f[i];
       }
-      out[(long long)t * vec_per_row + v] = Vec16<T>::store(acc);
+      StoreN<O, N>::st(out + ((long long)t * vec_per_row + v) * N, acc);
     }
   }
+}
+
+template <typename T, typename O>
+cudaError_t combine_typed(const moe_config& c, const uint4* yp, const uint4* ys, const int32_t* tok2row, const float* w,
+                          void* out, int* status, cudaStream_t s) {
+  const int vec = int(size_t(c.d) * sizeof(T) / 16);
+  const int grid = c.T < 65535 ? c.T : 65535;
+  const long long R = (long long)c.T * c.k;
+  O* o = static_cast<O*>(out);
+  if (c.k <= 8) combine_kernel<T, O, 8><<<grid, 128, 0, s>>>(yp, ys, tok2row, w, c.T, c.k, R, vec, o, status);
+  else combine_kernel<T, O, 16><<<grid, 128, 0, s>>>(yp, ys, tok2row, w, c.T, c.k, R, vec, o, status);
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -287,22 +323,18 @@ cudaError_t launch_swiglu_simt_f32(const moe_config& c, const float* x_perm, con
 
 cudaError_t launch_combine(const moe_config& c, const void* y_perm, const void* y_shared, const int32_t* tok2row,
                            const float* w, void* out, int* status, cudaStream_t s, int* launches) {
-  const int vec = int(size_t(c.d) * dtype_bytes(c.act_dtype) / 16);
-  const int grid = c.T < 65535 ? c.T : 65535;
-  const long long R = (long long)c.T * c.k;
   auto yp = static_cast<const uint4*>(y_perm);
   // without shared experts there is no shared term to add
   auto ys = c.n_shared > 0 ? static_cast<const uint4*>(y_shared) : nullptr;
-  auto o = static_cast<uint4*>(out);
-  if (c.act_dtype == MOE_BF16) {
-    if (c.k <= 8) combine_kernel<__nv_bfloat16, 8><<<grid, 128, 0, s>>>(yp, ys, tok2row, w, c.T, c.k, R, vec, o, status);
-    else combine_kernel<__nv_bfloat16, 16><<<grid, 128, 0, s>>>(yp, ys, tok2row, w, c.T, c.k, R, vec, o, status);
-  } else {
-    if (c.k <= 8) combine_kernel<float, 8><<<grid, 128, 0, s>>>(yp, ys, tok2row, w, c.T, c.k, R, vec, o, status);
-    else combine_kernel<float, 16><<<grid, 128, 0, s>>>(yp, ys, tok2row, w, c.T, c.k, R, vec, o, status);
-  }
+  cudaError_t e;
+  if (c.act_dtype == MOE_BF16)
+    e = c.out_dtype == MOE_F32 ? combine_typed<__nv_bfloat16, float>(c, yp, ys, tok2row, w, out, status, s)
+                               : combine_typed<__nv_bfloat16, __nv_bfloat16>(c, yp, ys, tok2row, w, out, status, s);
+  else
+    e = c.out_dtype == MOE_F32 ? combine_typed<float, float>(c, yp, ys, tok2row, w, out, status, s)
+                               : combine_typed<float, __nv_bfloat16>(c, yp, ys, tok2row, w, out, status, s);
   if (launches) ++*launches;
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace moe

@@ -63,6 +63,7 @@ class Workload:
     act_dtype: str = "bf16"              # "f32" | "bf16"
     gate_w_dtype: str = "f32"            # "f32" | "bf16"
     bias: str = "none"                   # "none" | "normal0.1" | "zipf"
+    out_dtype: str = "f32"               # layer output h' ("f32": the listing's fp32 weighted sum)
 
     @property
     def I_s(self) -> int:

@@ -19,6 +19,7 @@ class MoELayer:
         self.cfg = _lib.make_config(wl)
         self.device = torch.device(device)
         self.act = torch_dtype(wl.act_dtype)
+        self.out_dtype = torch_dtype(wl.out_dtype)
         self.wg = li.wg.to(self.device)
         self.bias = None if li.bias is None else li.bias.to(self.device, torch.float32).contiguous()
         self.packed = torch.empty(_lib.moe_packed_size(self.cfg), dtype=torch.uint8, device=self.device)
@@ -30,7 +31,7 @@ class MoELayer:
     def forward(self, x: torch.Tensor, out: Optional[torch.Tensor] = None, idx=None, w=None, counts=None,
                 stream=None) -> torch.Tensor:
         if out is None:
-            out = torch.empty((self.wl.T, self.wl.d), dtype=self.act, device=self.device)
+            out = torch.empty((self.wl.T, self.wl.d), dtype=self.out_dtype, device=self.device)
         _lib.moe_forward(self.cfg, x, self.wg, self.bias, self.packed, out, self.ws, idx, w, counts, stream)
         return out
 
@@ -49,7 +50,7 @@ class MoELayer:
             "x_perm": torch.empty((T * k, d), dtype=self.act, device=dev),
             "y_perm": torch.empty((T * k, d), dtype=self.act, device=dev),
             "y_shared": torch.empty((T, d), dtype=self.act, device=dev),
-            "out": torch.empty((T, d), dtype=self.act, device=dev),
+            "out": torch.empty((T, d), dtype=self.out_dtype, device=dev),
         }
         rec = (lambda i: events[i].record(stream)) if events is not None else (lambda i: None)
         rec(0)

@@ -26,10 +26,10 @@
  *  - Two calls sharing one `ws` must not run concurrently.
  *  - Activation dtype (x, permuted rows, expert outputs) is cfg->act_dtype:
  *    MOE_F32 runs SIMT fp32 kernels; MOE_BF16 runs the tcgen05 tensor-core
- *    kernels with fp32 accumulation.  Expert outputs are stored in act_dtype
- *    (the MoE listing casts each expert's output to x.dtype); the gate-weighted
- *    sum is formed in fp32 and stored as cfg->out_dtype (MOE_F32 keeps the
- *    listing's fp32 result of multiplying by the fp32 gate weights).
+ *    kernels with fp32 accumulation.  The SwiGLU hidden state is stored in
+ *    act_dtype; expert outputs (y_perm, y_shared) are stored in fp32; the
+ *    gate-weighted sum is formed in fp32 and stored as cfg->out_dtype (MOE_F32
+ *    is the MoE listing's fp32 result of multiplying by the fp32 gates).
  */
 #ifndef MOE_B300_H
 #define MOE_B300_H
@@ -124,7 +124,8 @@ MOE_API moe_status moe_permute(const moe_config* cfg, const void* x, const int32
 /* Experts (intelliparadigm.com page section 3.3.1 SwiGLU; MoE listing).
  *   x_perm [T*k,d] rows grouped by expert per `offsets` [E+1] (device);
  *   x [T,d] for the shared expert; packed = moe_prepack_experts output.
- *   y_perm [T*k,d] out: FFN_e of each row; y_shared [T,d] out: FFN_shared(x).
+ *   y_perm [T*k,d] fp32 out: FFN_e of each row; y_shared [T,d] fp32 out:
+ *   FFN_shared(x).
  *   bf16: GEMM1 with the fused silu(W1 u)*(W3 u) epilogue (hidden rounded to
  *   bf16), then GEMM2; both on tcgen05 with fp32 accumulation in TMEM. */
 MOE_API moe_status moe_grouped_swiglu(const moe_config* cfg, const void* x_perm, const int32_t* offsets,
@@ -133,6 +134,7 @@ MOE_API moe_status moe_grouped_swiglu(const moe_config* cfg, const void* x_perm,
 
 /* Combine (MoE listing: gate-weighted sum over the k slots plus the shared
  * expert; the dense einsum form of the intelliparadigm.com page 3.3.3).
+ *   y_perm [T*k,d], y_shared [T,d] fp32 (moe_grouped_swiglu's outputs).
  *   out[t] = sum_j w[t,j] * y_perm[tok2row[t,j]] + y_shared[t], accumulated in
  *   fp32 in slot order j = 0..k-1 (deterministic), stored as out_dtype. */
 MOE_API moe_status moe_combine(const moe_config* cfg, const void* y_perm, const void* y_shared,

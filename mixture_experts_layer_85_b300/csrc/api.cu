@@ -63,8 +63,8 @@ WsLayout ws_layout(const moe_config& c) {
   L.x_perm = take(R * c.d * eb);
   L.h = take(R * c.I * eb);
   L.hs = take(size_t(c.T) * I_s(c) * eb);
-  L.y = take(R * c.d * eb);
-  L.ys = take(size_t(c.T) * c.d * eb);
+  L.y = take(R * c.d * 4);
+  L.ys = take(size_t(c.T) * c.d * 4);
   L.total = off;
   return L;
 }
@@ -195,7 +195,7 @@ moe_status run_experts(const moe_config& c, const void* x_perm, const int32_t* o
   cudaError_t e = launch_grouped_gemm(EPI_SWIGLU, r1, shared ? &s1 : nullptr, offsets, c.E, 0, c.T, ws.status(),
                                       tiles1, s, launches);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
-  // GEMM2: H [rows, I] x [d, I]^T -> Y [rows, d]
+  // GEMM2: H [rows, I] x [d, I]^T -> Y [rows, d], stored fp32
   GemmClass r2, s2;
   r2.A = h; r2.a_rows = R; r2.a_cols = c.I;
   r2.B = pb + P.w2; r2.b_rows = (long long)c.E * c.d; r2.b_cols = c.I;
@@ -207,7 +207,7 @@ moe_status run_experts(const moe_config& c, const void* x_perm, const int32_t* o
   s2.N = c.d; s2.K = int(Is); s2.a_k_mod = int(Is); s2.b_rows_per_group = 0; s2.mma_n = 256;
   const long long tiles2 = (mt_routed + mt_shared) * ((c.d + 255) / 256);
   if (mark_stages) profile_mark(s);
-  e = launch_grouped_gemm(EPI_STORE_BF16, r2, shared ? &s2 : nullptr, offsets, c.E, 0, c.T, ws.status(), tiles2, s,
+  e = launch_grouped_gemm(EPI_STORE_F32, r2, shared ? &s2 : nullptr, offsets, c.E, 0, c.T, ws.status(), tiles2, s,
                           launches);
   return cuda_status(e);
 }

@@ -326,13 +326,9 @@ cudaError_t launch_combine(const moe_config& c, const void* y_perm, const void* 
   auto yp = static_cast<const uint4*>(y_perm);
   // without shared experts there is no shared term to add
   auto ys = c.n_shared > 0 ? static_cast<const uint4*>(y_shared) : nullptr;
-  cudaError_t e;
-  if (c.act_dtype == MOE_BF16)
-    e = c.out_dtype == MOE_F32 ? combine_typed<__nv_bfloat16, float>(c, yp, ys, tok2row, w, out, status, s)
-                               : combine_typed<__nv_bfloat16, __nv_bfloat16>(c, yp, ys, tok2row, w, out, status, s);
-  else
-    e = c.out_dtype == MOE_F32 ? combine_typed<float, float>(c, yp, ys, tok2row, w, out, status, s)
-                               : combine_typed<float, __nv_bfloat16>(c, yp, ys, tok2row, w, out, status, s);
+  // expert outputs are fp32 for every activation dtype
+  cudaError_t e = c.out_dtype == MOE_F32 ? combine_typed<float, float>(c, yp, ys, tok2row, w, out, status, s)
+                                         : combine_typed<float, __nv_bfloat16>(c, yp, ys, tok2row, w, out, status, s);
   if (launches) ++*launches;
   return e;
 }

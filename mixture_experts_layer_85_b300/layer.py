@@ -48,8 +48,8 @@ class MoELayer:
             "row2tok": torch.empty((T * k,), dtype=torch.int32, device=dev),
             "tok2row": torch.empty((T, k), dtype=torch.int32, device=dev),
             "x_perm": torch.empty((T * k, d), dtype=self.act, device=dev),
-            "y_perm": torch.empty((T * k, d), dtype=self.act, device=dev),
-            "y_shared": torch.empty((T, d), dtype=self.act, device=dev),
+            "y_perm": torch.empty((T * k, d), dtype=torch.float32, device=dev),
+            "y_shared": torch.empty((T, d), dtype=torch.float32, device=dev),
             "out": torch.empty((T, d), dtype=self.out_dtype, device=dev),
         }
         rec = (lambda i: events[i].record(stream)) if events is not None else (lambda i: None)

@@ -231,8 +231,8 @@ def test_grouped_swiglu_rows(name, seed):
     packed = torch.empty(_lib.moe_packed_size(cfg), dtype=torch.uint8, device="cuda")
     _lib.moe_prepack_experts(cfg, w1, w3, w2, ws1, ws3, ws2, packed)
     ws = torch.empty(_lib.moe_workspace_size(cfg), dtype=torch.uint8, device="cuda")
-    y = torch.empty((R, wl.d), dtype=torch.bfloat16, device="cuda")
-    ys = torch.empty((wl.T, wl.d), dtype=torch.bfloat16, device="cuda")
+    y = torch.empty((R, wl.d), dtype=torch.float32, device="cuda")
+    ys = torch.empty((wl.T, wl.d), dtype=torch.float32, device="cuda")
     _lib.moe_grouped_swiglu(cfg, x_perm.cuda(), offsets.cuda(), x.cuda(), packed, y, ys, ws)
     assert _lib.moe_get_device_status(ws)[0] == _lib.MOE_OK
     want = np.zeros((R, wl.d))
@@ -252,9 +252,8 @@ def test_combine(dtype, out_dtype):
     wl = inputs.small_workload(W["v2lite_t4096"], name="comb", T=T, d=d, E=16, I=128, k=k, act_dtype=dtype,
                                out_dtype=out_dtype)
     cfg = _lib.make_config(wl)
-    tdt = inputs.torch_dtype(dtype)
-    y = inputs.random_rows(T * k, d, 11, tdt)
-    ys = inputs.random_rows(T, d, 12, tdt)
+    y = inputs.random_rows(T * k, d, 11, torch.float32)      # expert outputs are fp32
+    ys = inputs.random_rows(T, d, 12, torch.float32)
     g = inputs.random_gates(T, k, 13)
     tok2row = torch.randperm(T * k, generator=torch.Generator().manual_seed(14)).view(T, k).to(torch.int32)
     ws = torch.empty(_lib.moe_workspace_size(cfg), dtype=torch.uint8, device="cuda")

@@ -35,7 +35,7 @@ bool is_bf16(const moe_config& c) { return c.act_dtype == MOE_BF16; }
 long long I_s(const moe_config& c) { return (long long)c.n_shared * c.I; }
 
 bool use_tc_gate(const moe_config& c) {
-  return is_bf16(c) && c.T >= kTcGateMinT && c.E % 16 == 0 && c.E <= 256;
+  return is_bf16(c) && c.T >= kTcGateMinT && c.E <= 256;
 }
 
 WsLayout ws_layout(const moe_config& c) {
@@ -152,9 +152,9 @@ moe_status run_gate(const moe_config& c, const void* x, const void* wg, const fl
     g.N = c.E;
     g.a_k_mod = c.d;
     g.b_rows_per_group = 0;
-    g.mma_n = c.E;
-    e = launch_grouped_gemm(EPI_STORE_F32, g, nullptr, nullptr, 0, c.T, 0, ws.status(), (c.T + 127) / 128, s,
-                            launches);
+    g.mma_n = 128;   // 128-column tiles with fp32 promotion of the partial sums
+    e = launch_grouped_gemm(EPI_GATE_F32, g, nullptr, nullptr, 0, c.T, 0, ws.status(),
+                            (long long)((c.T + 127) / 128) * ((c.E + 127) / 128), s, launches);
   } else {
     e = launch_gate_logits_simt(c, x, wg, logits, s, launches);
   }

@@ -30,7 +30,7 @@ namespace moe {
 namespace {
 
 constexpr int BM = 128;
-constexpr int BN = 256;
+constexpr int BN = 256;        // widest tile; TMEM accumulator stride
 constexpr int BK = 64;
 constexpr int STAGES = 4;
 constexpr int THREADS = 192;
@@ -79,13 +79,27 @@ struct TileInfo {
   int cls, g, m_blk, n_blk, row_start, rows;
 };
 
+// Tile width and accumulation chunk of each epilogue mode.  EPI_GATE_F32 keeps
+// 128-column tiles so that an epilogue thread can hold a whole accumulator row
+// in registers, and restarts the tensor-core accumulation every PROMOTE_KB
+// k-blocks: each 256-long partial sum is added into the registers with fp32
+// round-to-nearest, so the result carries the error of 256-long tensor-core
+// sums only, not of a d-long one.
+constexpr int PROMOTE_KB = 4;
+template <int EPI> struct Mode {
+  static constexpr int kBN = EPI == EPI_GATE_F32 ? 128 : BN;
+  static constexpr int kChunk = EPI == EPI_GATE_F32 ? PROMOTE_KB : (1 << 30);
+};
+
 __device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
 
+template <int EPI>
 __device__ __forceinline__ int group_tiles(const Params& p, int cls, int rows) {
-  return cdiv(rows, BM) * cdiv(p.N[cls], BN);
+  return cdiv(rows, BM) * cdiv(p.N[cls], Mode<EPI>::kBN);
 }
 
 // Warp-cooperative: per-group row ranges and the exclusive prefix of tiles.
+template <int EPI>
 __device__ void build_schedule(Ctrl* c, const Params& p, int lane) {
   const int g0 = p.num_routed > 0 ? p.num_routed : (p.rows_single0 > 0 ? 1 : 0);
   const int ng = g0 + (p.shared_rows > 0 ? 1 : 0);
@@ -112,7 +126,7 @@ __device__ void build_schedule(Ctrl* c, const Params& p, int lane) {
     }
     c->row_start[g] = rs;
     c->rows[g] = rows;
-    local += group_tiles(p, cls, rows);
+    local += group_tiles<EPI>(p, cls, rows);
   }
   int incl = local;
 #pragma unroll
@@ -123,7 +137,7 @@ __device__ void build_schedule(Ctrl* c, const Params& p, int lane) {
   int run = incl - local;
   for (int g = lo; g < hi; ++g) {
     c->tile_start[g] = run;
-    run += group_tiles(p, g < g0 ? 0 : 1, c->rows[g]);
+    run += group_tiles<EPI>(p, g < g0 ? 0 : 1, c->rows[g]);
   }
   if (lane == 31) {
     c->tile_start[ng] = incl;
@@ -136,6 +150,7 @@ __device__ void build_schedule(Ctrl* c, const Params& p, int lane) {
 // the operand that is re-read the most resident in L2: groups with more row
 // blocks than column blocks walk columns fastest (the A rows are re-used),
 // others walk rows fastest (the weight tile is re-used).
+template <int EPI>
 __device__ __forceinline__ TileInfo tile_info(const Ctrl* c, const Params& p, int tile) {
   int lo = 0, hi = c->ngroups - 1;
   while (lo < hi) {
@@ -149,7 +164,7 @@ __device__ __forceinline__ TileInfo tile_info(const Ctrl* c, const Params& p, in
   t.row_start = c->row_start[lo];
   t.rows = c->rows[lo];
   const int local = tile - c->tile_start[lo];
-  const int mb = cdiv(t.rows, BM), nb = cdiv(p.N[t.cls], BN);
+  const int mb = cdiv(t.rows, BM), nb = cdiv(p.N[t.cls], Mode<EPI>::kBN);
   if (mb > nb) {
     t.m_blk = local / nb;
     t.n_blk = local % nb;
@@ -160,6 +175,7 @@ __device__ __forceinline__ TileInfo tile_info(const Ctrl* c, const Params& p, in
   return t;
 }
 
+template <int EPI>
 __device__ void producer(Ctrl* c, const Params& p, uint8_t* stages, int total) {
   volatile int* ab = &c->abort;
   int stage = 0;
@@ -167,9 +183,9 @@ __device__ void producer(Ctrl* c, const Params& p, uint8_t* stages, int total) {
   uint32_t issued = 0, issued_par = 0;
   bool ok = true;
   for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-    const TileInfo t = tile_info(c, p, tile);
+    const TileInfo t = tile_info<EPI>(c, p, tile);
     const int a_row = t.row_start + t.m_blk * BM;
-    const int b_row = (t.cls == 0 ? t.g * p.b_step[0] : 0) + t.n_blk * BN;
+    const int b_row = (t.cls == 0 ? t.g * p.b_step[0] : 0) + t.n_blk * Mode<EPI>::kBN;
     const int nk = p.K[t.cls] / BK;
     const uint32_t bytes = A_BYTES + uint32_t(p.mma_n[t.cls]) * BK * 2;
     for (int kb = 0; kb < nk; ++kb) {
@@ -196,40 +212,51 @@ __device__ void producer(Ctrl* c, const Params& p, uint8_t* stages, int total) {
     if (issued & (1u << s)) mbar_wait(&c->full[s], (issued_par >> s) & 1u, nullptr, p.status);
 }
 
+// Each tile's k-blocks are issued in chunks of Mode<EPI>::kChunk (one chunk
+// per tile unless the mode promotes partial sums); every chunk accumulates
+// into one of the two TMEM buffers and is handed to the epilogue on tfull.
+template <int EPI>
 __device__ void mma_issuer(Ctrl* c, const Params& p, uint8_t* stages, uint32_t tmem, int total) {
   volatile int* ab = &c->abort;
   int stage = 0;
   uint32_t phase = 0;
-  int local = 0;
+  int chunk_ctr = 0;
   bool ok = true;
-  for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x, ++local) {
-    const TileInfo t = tile_info(c, p, tile);
-    const int acc = local & 1;
-    const uint32_t acc_par = uint32_t(local >> 1) & 1u;
-    if (!mbar_wait(&c->tempty[acc], acc_par ^ 1u, ab, p.status)) break;
-    tc_fence_after();
-    const uint32_t d_tmem = tmem + uint32_t(acc * BN);
+  for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+    const TileInfo t = tile_info<EPI>(c, p, tile);
     const uint32_t idesc = idesc_bf16_f32(BM, p.mma_n[t.cls]);
     const int nk = p.K[t.cls] / BK;
-    for (int kb = 0; kb < nk; ++kb) {
-      if (!mbar_wait(&c->full[stage], phase, ab, p.status)) {
+    const int ck = Mode<EPI>::kChunk < nk ? Mode<EPI>::kChunk : nk;
+    for (int kb0 = 0; ok && kb0 < nk; kb0 += ck, ++chunk_ctr) {
+      const int acc = chunk_ctr & 1;
+      const uint32_t acc_par = uint32_t(chunk_ctr >> 1) & 1u;
+      if (!mbar_wait(&c->tempty[acc], acc_par ^ 1u, ab, p.status)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const uint32_t a0 = smem_u32(stages + stage * STAGE_BYTES);
-      const uint32_t b0 = a0 + A_BYTES;
+      const uint32_t d_tmem = tmem + uint32_t(acc * BN);
+      const int kend = kb0 + ck < nk ? kb0 + ck : nk;
+      for (int kb = kb0; kb < kend; ++kb) {
+        if (!mbar_wait(&c->full[stage], phase, ab, p.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a0 = smem_u32(stages + stage * STAGE_BYTES);
+        const uint32_t b0 = a0 + A_BYTES;
 #pragma unroll
-      for (int kk = 0; kk < BK / 16; ++kk)
-        mma_bf16_ss(d_tmem, sw128_kmajor_desc(a0 + kk * 32), sw128_kmajor_desc(b0 + kk * 32), idesc,
-                    (kb | kk) != 0 ? 1u : 0u);
-      mma_commit(&c->empty[stage]);
-      if (++stage == STAGES) {
-        stage = 0;
-        phase ^= 1u;
+        for (int kk = 0; kk < BK / 16; ++kk)
+          mma_bf16_ss(d_tmem, sw128_kmajor_desc(a0 + kk * 32), sw128_kmajor_desc(b0 + kk * 32), idesc,
+                      (kb != kb0 || kk != 0) ? 1u : 0u);
+        mma_commit(&c->empty[stage]);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
       }
+      if (ok) mma_commit(&c->tfull[acc]);
     }
-    if (ok) mma_commit(&c->tfull[acc]);
   }
   // All MMAs this thread issued complete before TMEM is released.
   mma_commit(&c->drain);
@@ -243,86 +270,133 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// One lane waits and the verdict is broadcast, so the warp-collective TMEM
+// loads that follow are always executed by the whole warp.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* ab, int* status, int lane) {
+  int ok = 1;
+  if (lane == 0) ok = mbar_wait(bar, parity, ab, status) ? 1 : 0;
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
 template <int EPI>
 __device__ void epilogue(Ctrl* c, const Params& p, uint32_t tmem, int total, int warp, int lane) {
   volatile int* ab = &c->abort;
   const int q = warp & 3;  // the TMEM lane quarter this warp may read
   const int r_in_tile = q * 32 + lane;
-  int local = 0;
-  for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++local) {
-    const TileInfo t = tile_info(c, p, tile);
-    const int acc = local & 1;
-    const uint32_t acc_par = uint32_t(local >> 1) & 1u;
-    // One lane waits and the verdict is broadcast, so the warp-collective
-    // TMEM loads below are always executed by the whole warp.
-    int ok = 1;
-    if (lane == 0) ok = mbar_wait(&c->tfull[acc], acc_par, ab, p.status) ? 1 : 0;
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    if (!ok) break;
-    tc_fence_after();
+  int chunk_ctr = 0;
+  bool ok = true;
+  for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+    const TileInfo t = tile_info<EPI>(c, p, tile);
     const int row_local = t.m_blk * BM + r_in_tile;
     const bool valid = row_local < t.rows;
     const long long grow = (long long)t.row_start + row_local;
-    const uint32_t tbase = tmem + uint32_t(acc * BN) + (uint32_t(q * 32) << 16);
-    if constexpr (EPI == EPI_SWIGLU) {
-      // Tile columns [0,128) hold W1 rows, [128,256) the matching W3 rows.
-      __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out[t.cls]) + grow * p.ld_out[t.cls];
-      const int col0 = t.n_blk * (BN / 2);
-#pragma unroll 1
-      for (int cc = 0; cc < BN / 2; cc += 16) {
-        float g[16], u[16];
-        tmem_ld16(tbase + cc, g);
-        tmem_ld16(tbase + BN / 2 + cc, u);
-        if (valid) {
-          uint32_t w[8];
+    if constexpr (EPI == EPI_GATE_F32) {
+      // sum of the tile's 256-long partial products, fp32 round-to-nearest
+      const int nk = p.K[t.cls] / BK;
+      const int nchunks = cdiv(nk, PROMOTE_KB);
+      float racc[128];
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            w[i] = pack_bf16x2(silu_f(g[2 * i]) * u[2 * i], silu_f(g[2 * i + 1]) * u[2 * i + 1]);
-          uint4* dst = reinterpret_cast<uint4*>(orow + col0 + cc);
-          dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-          dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+      for (int i = 0; i < 128; ++i) racc[i] = 0.0f;
+      for (int ch = 0; ch < nchunks; ++ch, ++chunk_ctr) {
+        const int acc = chunk_ctr & 1;
+        if (!warp_wait(&c->tfull[acc], uint32_t(chunk_ctr >> 1) & 1u, ab, p.status, lane)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t tbase = tmem + uint32_t(acc * BN) + (uint32_t(q * 32) << 16);
+#pragma unroll
+        for (int cc = 0; cc < 128; cc += 16) {
+          float v[16];
+          tmem_ld16(tbase + cc, v);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) racc[cc + i] = __fadd_rn(racc[cc + i], v[i]);
+        }
+        tc_fence_before();
+        mbar_arrive(&c->tempty[acc]);
+      }
+      if (ok && valid) {
+        const int col0 = t.n_blk * 128;
+        const int ncol = min(128, p.N[t.cls] - col0);
+        float* orow = static_cast<float*>(p.out[t.cls]) + grow * p.ld_out[t.cls] + col0;
+        if (ncol == 128) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            reinterpret_cast<float4*>(orow)[i] =
+                make_float4(racc[4 * i], racc[4 * i + 1], racc[4 * i + 2], racc[4 * i + 3]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 128; ++i)
+            if (i < ncol) orow[i] = racc[i];
         }
       }
+      continue;
     } else {
-      const int col0 = t.n_blk * BN;
-      const int ncol = min(BN, p.N[t.cls] - col0);
-      const int nld = min(p.mma_n[t.cls], BN);
+      const int acc = chunk_ctr & 1;
+      if (!warp_wait(&c->tfull[acc], uint32_t(chunk_ctr >> 1) & 1u, ab, p.status, lane)) break;
+      ++chunk_ctr;
+      tc_fence_after();
+      const uint32_t tbase = tmem + uint32_t(acc * BN) + (uint32_t(q * 32) << 16);
+      if constexpr (EPI == EPI_SWIGLU) {
+        // Tile columns [0,128) hold W1 rows, [128,256) the matching W3 rows.
+        __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out[t.cls]) + grow * p.ld_out[t.cls];
+        const int col0 = t.n_blk * (BN / 2);
 #pragma unroll 1
-      for (int cc = 0; cc < nld; cc += 16) {
-        float v[16];
-        tmem_ld16(tbase + cc, v);
-        if (valid && cc < ncol) {
-          if constexpr (EPI == EPI_STORE_BF16) {
-            __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out[t.cls]) + grow * p.ld_out[t.cls] + col0 + cc;
-            if (cc + 16 <= ncol) {
-              uint32_t w[8];
+        for (int cc = 0; cc < BN / 2; cc += 16) {
+          float g[16], u[16];
+          tmem_ld16(tbase + cc, g);
+          tmem_ld16(tbase + BN / 2 + cc, u);
+          if (valid) {
+            uint32_t w[8];
 #pragma unroll
-              for (int i = 0; i < 8; ++i) w[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
-              uint4* dst = reinterpret_cast<uint4*>(orow);
-              dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-              dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+            for (int i = 0; i < 8; ++i)
+              w[i] = pack_bf16x2(silu_f(g[2 * i]) * u[2 * i], silu_f(g[2 * i + 1]) * u[2 * i + 1]);
+            uint4* dst = reinterpret_cast<uint4*>(orow + col0 + cc);
+            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+            dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+          }
+        }
+      } else {
+        const int col0 = t.n_blk * BN;
+        const int ncol = min(BN, p.N[t.cls] - col0);
+        const int nld = min(p.mma_n[t.cls], BN);
+#pragma unroll 1
+        for (int cc = 0; cc < nld; cc += 16) {
+          float v[16];
+          tmem_ld16(tbase + cc, v);
+          if (valid && cc < ncol) {
+            if constexpr (EPI == EPI_STORE_BF16) {
+              __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out[t.cls]) + grow * p.ld_out[t.cls] + col0 + cc;
+              if (cc + 16 <= ncol) {
+                uint32_t w[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) w[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+                uint4* dst = reinterpret_cast<uint4*>(orow);
+                dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+              } else {
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                  if (cc + i < ncol) orow[i] = __float2bfloat16_rn(v[i]);
+              }
             } else {
+              float* orow = static_cast<float*>(p.out[t.cls]) + grow * p.ld_out[t.cls] + col0 + cc;
+              if (cc + 16 <= ncol) {
+                float4* dst = reinterpret_cast<float4*>(orow);
 #pragma unroll
-              for (int i = 0; i < 16; ++i)
-                if (cc + i < ncol) orow[i] = __float2bfloat16_rn(v[i]);
-            }
-          } else {
-            float* orow = static_cast<float*>(p.out[t.cls]) + grow * p.ld_out[t.cls] + col0 + cc;
-            if (cc + 16 <= ncol) {
-              float4* dst = reinterpret_cast<float4*>(orow);
+                for (int i = 0; i < 4; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+              } else {
 #pragma unroll
-              for (int i = 0; i < 4; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-            } else {
-#pragma unroll
-              for (int i = 0; i < 16; ++i)
-                if (cc + i < ncol) orow[i] = v[i];
+                for (int i = 0; i < 16; ++i)
+                  if (cc + i < ncol) orow[i] = v[i];
+              }
             }
           }
         }
       }
+      tc_fence_before();
+      mbar_arrive(&c->tempty[acc]);
     }
-    tc_fence_before();
-    mbar_arrive(&c->tempty[acc]);
   }
 }
 
@@ -357,7 +431,7 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const __grid_c
     tmem_alloc(&c->tmem_base, TMEM_COLS);
     tmem_relinquish();
   }
-  if (warp == 2) build_schedule(c, p, lane);
+  if (warp == 2) build_schedule<EPI>(c, p, lane);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -365,9 +439,9 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const __grid_c
   const uint32_t tmem = c->tmem_base;
   const int total = c->tile_start[c->ngroups];
   if (warp == 0) {
-    if (lane == 0) producer(c, p, stages, total);
+    if (lane == 0) producer<EPI>(c, p, stages, total);
   } else if (warp == 1) {
-    if (lane == 0) mma_issuer(c, p, stages, tmem, total);
+    if (lane == 0) mma_issuer<EPI>(c, p, stages, tmem, total);
   } else {
     epilogue<EPI>(c, p, tmem, total, warp, lane);
   }
@@ -465,7 +539,8 @@ cudaError_t launch_grouped_gemm(int epi, const GemmClass& c0, const GemmClass* c
   switch (epi) {
     case EPI_SWIGLU: e = launch_epi<EPI_SWIGLU>(p, grid, stream); break;
     case EPI_STORE_BF16: e = launch_epi<EPI_STORE_BF16>(p, grid, stream); break;
-    default: e = launch_epi<EPI_STORE_F32>(p, grid, stream); break;
+    case EPI_STORE_F32: e = launch_epi<EPI_STORE_F32>(p, grid, stream); break;
+    default: e = launch_epi<EPI_GATE_F32>(p, grid, stream); break;
   }
   if (e == cudaSuccess && launches) ++*launches;
   return e;

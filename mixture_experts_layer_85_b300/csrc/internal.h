@@ -28,7 +28,7 @@ struct GemmClass {
   int mma_n = 256;          // MMA N (<= 256, multiple of 16); B box rows
 };
 
-enum EpiMode : int { EPI_SWIGLU = 0, EPI_STORE_BF16 = 1, EPI_STORE_F32 = 2 };
+enum EpiMode : int { EPI_SWIGLU = 0, EPI_STORE_BF16 = 1, EPI_STORE_F32 = 2, EPI_GATE_F32 = 3 };
 
 int num_sms();
 

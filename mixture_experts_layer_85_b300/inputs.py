@@ -104,6 +104,13 @@ for _w in [
 ]:
     WORKLOADS[_w.name] = _w
 
+# A V3-shaped layer cut to 8 experts and 1024 tokens (1.4 GB of weights):
+# the case the kernel profiler captures, still larger than L2.
+WORKLOADS["v3_profile_e8_t1024"] = Workload(
+    name="v3_profile_e8_t1024", T=1024, d=7168, E=8, I=2048, k=4, n_shared=1, score_fn="sigmoid",
+    topk_method="group_limited_greedy", n_group=4, topk_group=2, group_score="sum_top", group_top=2,
+    norm_topk=True, routed_scaling_factor=2.5, act_dtype="bf16", gate_w_dtype="bf16", bias="normal0.1")
+
 CONFIG_ORDER = ["tiny_fp32_t128", "v2lite_t4096", "v2_t8192", "v3_prefill_t16384",
                 "v3_decode_t1", "v3_decode_t8", "v3_decode_t64", "v3_decode_t512"]
 DECODE_T = (1, 8, 64, 512)

@@ -148,6 +148,30 @@ MOE_API moe_status moe_forward(const moe_config* cfg, const void* x, const void*
                        const void* packed, void* out, int32_t* idx_out, float* w_out,
                        int32_t* counts_out, void* ws, size_t ws_bytes, void* stream);
 
+/* Dispatch without any device allocation (the pages have no counterpart: it
+ * exists for callers, not for the method).  Same inputs, outputs and results
+ * as moe_permute, but the per-chunk scratch lives in a fixed array inside the
+ * library's device image instead of a caller workspace.  Meant for callers
+ * that cannot call cudaMalloc or hand out workspace: plug-ins whose device
+ * memory belongs to a host framework's arena, processes held to a hard memory
+ * budget, and latency-critical loops that must not risk cudaMalloc's
+ * device-wide blocking or its failure under fragmentation.
+ *   Limit: permute_chunks(T) * E <= 32768, with 128 tokens per chunk (e.g.
+ *   T <= 16384 with E = 256); larger sizes return MOE_ERR_WORKSPACE without
+ *   launching.  The array (~256 KB) is held on every device that loads the
+ *   library until the process exits.
+ *   device_status [1] int32 (device, nullable) receives this call's status
+ *   word (as read by moe_get_device_status for the workspace calls).
+ *   The first call on each device looks up the array's device address with
+ *   cudaGetSymbolAddress; make that first call before any stream capture.
+ *   All calls share the one array, so calls whose kernels overlap on the GPU
+ *   (other streams, other host threads) race: serialise them.  No cudaMalloc,
+ *   cudaFree or allocating library routine is called. */
+MOE_API moe_status moe_permute_noalloc(const moe_config* cfg, const void* x, const int32_t* idx,
+                                       int32_t* counts, int32_t* offsets, int32_t* row2tok,
+                                       int32_t* tok2row, void* x_perm, int32_t* device_status,
+                                       void* stream);
+
 /* Synchronises `stream`, reads the device status word of `ws` and returns
  * MOE_OK, MOE_ERR_DEVICE_TIMEOUT or MOE_ERR_DEVICE_BOUNDS.  `detail` (nullable)
  * receives the raw word. */

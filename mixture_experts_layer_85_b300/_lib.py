@@ -29,7 +29,8 @@ MOE_GROUP_MAX, MOE_GROUP_SUM_TOP = 0, 1
 
 EXPORTED = ["moe_workspace_size", "moe_packed_size", "moe_prepack_experts", "moe_gate_topk", "moe_permute",
             "moe_grouped_swiglu", "moe_combine", "moe_forward", "moe_get_device_status", "moe_status_string",
-            "moe_launch_count", "moe_forward_kernel_count", "moe_profile_arm", "moe_forward_stage_name"]
+            "moe_launch_count", "moe_forward_kernel_count", "moe_profile_arm", "moe_forward_stage_name",
+            "moe_permute_noalloc"]
 MOE_FORWARD_STAGES = 5
 
 
@@ -60,6 +61,7 @@ _sigs = {
     "moe_forward_kernel_count": [_CFG],
     "moe_profile_arm": [ctypes.POINTER(_P), ctypes.c_int32],
     "moe_forward_stage_name": [ctypes.c_int32],
+    "moe_permute_noalloc": [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P],
 }
 for _name, _args in _sigs.items():
     _f = getattr(_lib, _name)
@@ -162,6 +164,13 @@ def moe_forward(cfg, x, Wg, bias, packed, out, ws, idx_out=None, w_out=None, cou
     _check(_lib.moe_forward(ctypes.byref(cfg), _ptr(x), _ptr(Wg), _ptr(bias), _ptr(packed), _ptr(out),
                             _ptr(idx_out), _ptr(w_out), _ptr(counts_out), _ptr(ws), ws.numel() * ws.element_size(),
                             _stream(stream)), "moe_forward")
+
+
+def moe_permute_noalloc(cfg, x, idx, counts, offsets, row2tok, tok2row, x_perm, device_status=None, stream=None):
+    """moe_permute without a workspace: scratch in the library's fixed device array."""
+    _check(_lib.moe_permute_noalloc(ctypes.byref(cfg), _ptr(x), _ptr(idx), _ptr(counts), _ptr(offsets),
+                                    _ptr(row2tok), _ptr(tok2row), _ptr(x_perm), _ptr(device_status),
+                                    _stream(stream)), "moe_permute_noalloc")
 
 
 def moe_get_device_status(ws, stream=None) -> tuple:

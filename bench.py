@@ -13,6 +13,7 @@ the layer on its own batch (tokens are independent, no collective on the
 data path); the value is all ranks' tokens over the slowest rank's time.
 """
 import argparse
+import datetime
 import json
 import math
 import os
@@ -38,7 +39,7 @@ DEFAULT_WORKLOAD = "v3_prefill_t16384"
 def parse_args(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--steps", type=int, default=50)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(inputs.WORKLOADS))
@@ -88,11 +89,14 @@ def whole_job_rate(units_per_rank: float, world: int, seconds_max: float) -> flo
 # ----------------------------------------------------------------- clocks
 
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 200 ms in the background."""
+    """nvidia-smi clocks / throttle reasons sampled every 50 ms in the background;
+    stop(t0, t1) keeps the samples whose timestamps fall in the host-time window
+    [t0, t1] of the timed region (padded by one sampling interval)."""
 
-    FIELDS = ("index,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    INTERVAL_MS = 50
 
     def __init__(self):
         self.proc = None
@@ -103,15 +107,27 @@ class ClockSampler:
             fd, self.path = tempfile.mkstemp(suffix=".csv")
             os.close(fd)
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                                          "-lms", "200", "-f", self.path], stdout=subprocess.DEVNULL,
+                                          "-lms", str(self.INTERVAL_MS), "-f", self.path], stdout=subprocess.DEVNULL,
                                          stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
+            return
+        # the timed region starts once the sampler is producing rows
+        t0 = time.time()
+        while time.time() - t0 < 5.0 and os.path.getsize(self.path) == 0:
+            time.sleep(0.02)
 
-    def stop(self):
+    @staticmethod
+    def _num(s):
+        try:
+            return float(s)
+        except ValueError:
+            return None
+
+    def stop(self, t0: float, t1: float):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        time.sleep(0.25)
+        time.sleep(2 * self.INTERVAL_MS / 1e3)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
@@ -122,25 +138,31 @@ class ClockSampler:
             uuid = str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
         except Exception:
             pass
+        pad = self.INTERVAL_MS / 1e3
         rows = []
         for line in open(self.path):
             f = [x.strip() for x in line.split(",")]
-            if len(f) < 10:
+            if len(f) < 11:
                 continue
-            if uuid and uuid not in f[1] and f[1].replace("GPU-", "") not in uuid:
+            if uuid and uuid not in f[2] and f[2].replace("GPU-", "") not in uuid:
                 continue
-            rows.append(f)
+            try:
+                ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                continue
+            if t0 - pad <= ts <= t1 + pad:
+                rows.append(f[1:])
         os.unlink(self.path)
         if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        sm = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
-        mx = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples inside the timed region"]}
+        sm = [v for v in (self._num(r[2]) for r in rows) if v is not None]
+        mx = [v for v in (self._num(r[3]) for r in rows) if v is not None]
+        pw = [v for v in (self._num(r[4]) for r in rows) if v is not None]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in rows for i in range(4) if r[6 + i].lower().startswith("active")})
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(rows),
-                "power_w_max": max(float(r[4]) for r in rows if r[4].replace(".", "").isdigit())
-                if any(r[4].replace(".", "").isdigit() for r in rows) else None}
+                "reasons": reasons, "samples": len(rows), "power_w_max": max(pw) if pw else None,
+                "power_w_median": statistics.median(pw) if pw else None}
 
 
 def measured_peaks():
@@ -227,6 +249,55 @@ def host_threads() -> int:
         return os.cpu_count() or 1
 
 
+def time_end_to_end(layer, x, out_dtype, K, stream, world) -> float:
+    """Seconds for K pipelined steps of host tokens -> layer -> host output."""
+    T, d = x.shape
+    x_h = x.cpu().pin_memory()
+    out_h = [torch.empty((T, d), dtype=out_dtype).pin_memory() for _ in range(2)]
+    x_d = [torch.empty_like(x) for _ in range(2)]
+    out_d = [torch.empty((T, d), dtype=out_dtype, device=x.device) for _ in range(2)]
+    h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def run(n, e0=None):
+        fwd_done = [torch.cuda.Event() for _ in range(2)]
+        h2d_done = [torch.cuda.Event() for _ in range(2)]
+        d2h_done = [torch.cuda.Event() for _ in range(2)]
+        used = [False, False]
+        if e0 is not None:
+            h2d.wait_event(e0)
+        for i in range(n):
+            s = i % 2
+            if used[s]:
+                h2d.wait_event(fwd_done[s])
+            with torch.cuda.stream(h2d):
+                x_d[s].copy_(x_h, non_blocking=True)
+            h2d_done[s].record(h2d)
+            stream.wait_event(h2d_done[s])
+            if used[s]:
+                stream.wait_event(d2h_done[s])
+            layer.forward(x_d[s], out_d[s], stream=stream)
+            fwd_done[s].record(stream)
+            d2h.wait_event(fwd_done[s])
+            with torch.cuda.stream(d2h):
+                out_h[s].copy_(out_d[s], non_blocking=True)
+            d2h_done[s].record(d2h)
+            used[s] = True
+        for s in range(2):
+            if used[s]:
+                stream.wait_event(d2h_done[s])
+
+    run(2)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    e0.record(stream)
+    run(K, e0)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
+
+
 # ---------------------------------------------------------------- our arm
 
 def run_ours(args, world, rank):
@@ -259,16 +330,17 @@ def run_ours(args, world, rank):
     barrier(world)
     torch.cuda.synchronize()
     clocks.start()
-    time.sleep(0.3)
     launches0 = _lib.moe_launch_count()
+    host_t0 = time.time()
     t_start.record(stream)
     for _ in range(K):
         layer.forward(x, out, counts=counts)
     t_end.record(stream)
     torch.cuda.synchronize()
+    host_t1 = time.time()
     launches = _lib.moe_launch_count() - launches0
     barrier(world)
-    clk = clocks.stop()
+    clk = clocks.stop(host_t0, host_t1)
     _lib.moe_profile_arm(None)
     code, word = layer.device_status()
     if code != 0:
@@ -304,29 +376,15 @@ def run_ours(args, world, rank):
                  "per_launch_flops": g1_flops, "per_launch_algorithmic_bytes": g1_bytes,
                  "avg_launch_ms": round(stage_ms["gemm1_swiglu"], 4)})
 
-    # end to end through the C ABI with host buffers: H2D of x, forward, D2H of out
-    x_h = x.cpu().pin_memory()
-    out_h = torch.empty((wl.T, wl.d), dtype=out.dtype).pin_memory()
-    x_d = torch.empty_like(x)
-    for _ in range(2):
-        x_d.copy_(x_h, non_blocking=True)
-        layer.forward(x_d, out)
-        out_h.copy_(out, non_blocking=True)
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    barrier(world)
-    e0.record(stream)
-    for _ in range(K):
-        x_d.copy_(x_h, non_blocking=True)
-        layer.forward(x_d, out)
-        out_h.copy_(out, non_blocking=True)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_s = max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
+    # end to end through the C ABI with host buffers: every step copies its
+    # tokens host -> device, runs the layer and copies h' device -> host.  Two
+    # buffer slots and two copy streams let step i's copies overlap the
+    # neighbouring steps' forwards, as a serving loop would run them.
+    e2e_s = time_end_to_end(layer, x, out.dtype, K, stream, world)
     eb = x.element_size()
     e2e = {"value": round(whole_job_rate(wl.T * K, world, e2e_s), 1), "unit": UNIT,
-           "h2d_bytes_per_step": wl.T * wl.d * eb, "d2h_bytes_per_step": wl.T * wl.d * out.element_size()}
+           "h2d_bytes_per_step": wl.T * wl.d * eb, "d2h_bytes_per_step": wl.T * wl.d * out.element_size(),
+           "overlap": "H2D of step i+1 and D2H of step i-1 overlap the forward of step i (2 slots)"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -24,7 +24,10 @@ namespace {
 
 constexpr int kMaxE = 256;
 constexpr int kMaxK = 16;
-constexpr int kTcGateMinT = 1024;   // below this many tokens the SIMT gate streams W_g faster
+// The tensor-core gate splits K until its output tiles cover the GPU about
+// twice (a fixed figure, so workspace sizes do not depend on the device).
+constexpr int kGateTargetTiles = 296;
+constexpr int kGatePromoteK = 256;   // K per fp32-promoted tensor-core partial sum
 
 struct WsLayout {
   size_t status, logits, wsplit, chunk_counts, chunk_base, counts, offsets, row2tok, tok2row, idx, w, x_perm, h, hs,
@@ -35,7 +38,20 @@ bool is_bf16(const moe_config& c) { return c.act_dtype == MOE_BF16; }
 long long I_s(const moe_config& c) { return (long long)c.n_shared * c.I; }
 
 bool use_tc_gate(const moe_config& c) {
-  return is_bf16(c) && c.T >= kTcGateMinT && c.E <= 256;
+  return is_bf16(c) && c.E <= 256;
+}
+
+// K ranges of the tensor-core gate: each writes one fp32 partial plane of the
+// logits, which the top-k kernel adds in order.  Decode-sized batches have only
+// a few output tiles, so they split K the most.
+int gate_ksplit(const moe_config& c) {
+  if (!use_tc_gate(c) || c.T == 0) return 1;
+  const long long tiles = (long long)((c.T + 127) / 128) * ((c.E + 127) / 128);
+  const int K = c.gate_w_dtype == MOE_F32 ? 3 * c.d : c.d;
+  const int nchunks = (K + kGatePromoteK - 1) / kGatePromoteK;
+  long long want = (kGateTargetTiles + tiles - 1) / tiles;
+  if (want > nchunks) want = nchunks;
+  return want < 1 ? 1 : int(want);
 }
 
 WsLayout ws_layout(const moe_config& c) {
@@ -50,7 +66,7 @@ WsLayout ws_layout(const moe_config& c) {
     return at;
   };
   L.status = take(256);
-  L.logits = take(size_t(c.T) * c.E * 4);
+  L.logits = take(size_t(gate_ksplit(c)) * c.T * c.E * 4);
   L.wsplit = take(use_tc_gate(c) && c.gate_w_dtype == MOE_F32 ? size_t(c.E) * 3 * c.d * 2 : 0);
   L.chunk_counts = take(nch * c.E * 4);
   L.chunk_base = take(nch * c.E * 4);
@@ -93,8 +109,8 @@ moe_status check_config(const moe_config* cp) {
   }
   if (c.E > kMaxE || c.k > kMaxK) return MOE_ERR_UNSUPPORTED;
   if (is_bf16(c)) {
-    // tensor-core tiles: K in steps of 64, the SwiGLU tile pairs 128 W1 rows
-    // with 128 W3 rows, TMA rows 16-byte aligned
+    // tensor-core tiles: K in steps of 64 (d, I and I_s); whole 256-row weight
+    // tiles of interleaved W1/W3 rows per expert (I and I_s multiples of 128)
     if (c.d % 64 != 0 || c.I % 128 != 0 || I_s(c) % 128 != 0) return MOE_ERR_UNSUPPORTED;
   } else {
     if (c.d % 4 != 0) return MOE_ERR_UNSUPPORTED;
@@ -153,13 +169,15 @@ moe_status run_gate(const moe_config& c, const void* x, const void* wg, const fl
     g.a_k_mod = c.d;
     g.b_rows_per_group = 0;
     g.mma_n = 128;   // 128-column tiles with fp32 promotion of the partial sums
+    g.ksplit = gate_ksplit(c);
+    g.split_stride = (long long)c.T * c.E;
     e = launch_grouped_gemm(EPI_GATE_F32, g, nullptr, nullptr, 0, c.T, 0, ws.status(),
-                            (long long)((c.T + 127) / 128) * ((c.E + 127) / 128), s, launches);
+                            (long long)((c.T + 127) / 128) * ((c.E + 127) / 128) * g.ksplit, s, launches);
   } else {
     e = launch_gate_logits_simt(c, x, wg, logits, s, launches);
   }
   if (e != cudaSuccess) return MOE_ERR_CUDA;
-  return cuda_status(launch_topk(c, logits, bias, idx, w, s, launches));
+  return cuda_status(launch_topk(c, logits, gate_ksplit(c), (long long)c.T * c.E, bias, idx, w, s, launches));
 }
 
 moe_status run_experts(const moe_config& c, const void* x_perm, const int32_t* offsets, const void* x,
@@ -179,36 +197,28 @@ moe_status run_experts(const moe_config& c, const void* x_perm, const int32_t* o
   void* h = ws.at<void>(ws.L.h);
   void* hs = ws.at<void>(ws.L.hs);
   const bool shared = Is > 0;
-  // GEMM1 + SwiGLU: [rows, d] x [2I, d]^T -> H [rows, I]
-  GemmClass r1, s1;
-  r1.A = x_perm; r1.a_rows = R; r1.a_cols = c.d;
-  r1.B = pb + P.w13; r1.b_rows = 2LL * c.E * c.I; r1.b_cols = c.d;
-  r1.out = h; r1.ld_out = c.I; r1.out_rows = R;
-  r1.N = 2 * c.I; r1.K = c.d; r1.a_k_mod = c.d; r1.b_rows_per_group = 2 * c.I; r1.mma_n = 256;
-  s1.A = x; s1.a_rows = c.T; s1.a_cols = c.d;
-  s1.B = pb + P.w13s; s1.b_rows = 2 * Is; s1.b_cols = c.d;
-  s1.out = hs; s1.ld_out = Is; s1.out_rows = c.T;
-  s1.N = int(2 * Is); s1.K = c.d; s1.a_k_mod = c.d; s1.b_rows_per_group = 0; s1.mma_n = 256;
-  const long long mt_routed = R / 128 + c.E;
-  const long long mt_shared = shared ? (c.T + 127) / 128 : 0;
-  long long tiles1 = mt_routed * ((2LL * c.I + 255) / 256) + mt_shared * ((2 * Is + 255) / 256);
-  cudaError_t e = launch_grouped_gemm(EPI_SWIGLU, r1, shared ? &s1 : nullptr, offsets, c.E, 0, c.T, ws.status(),
-                                      tiles1, s, launches);
+  // Upper bounds of the pair tiles (256 tokens x 256 weight rows) for sizing the grid.
+  const long long tb_routed = R / 256 + c.E;
+  const long long tb_shared = shared ? (c.T + 255) / 256 : 0;
+  // GEMM1 + SwiGLU: H[rows, I] = silu(X W1^T) * (X W3^T), packed W1/W3 rows [2I, d] per expert
+  PairClass r1, s1;
+  r1.W = pb + P.w13; r1.w_rows = 2LL * c.E * c.I; r1.X = x_perm; r1.x_rows = R; r1.K = c.d;
+  r1.M = 2 * c.I; r1.w_step = 2 * c.I; r1.out = h; r1.ld_out = c.I; r1.out_rows = R;
+  s1.W = pb + P.w13s; s1.w_rows = 2 * Is; s1.X = x; s1.x_rows = c.T; s1.K = c.d;
+  s1.M = int(2 * Is); s1.w_step = 0; s1.out = hs; s1.ld_out = Is; s1.out_rows = c.T;
+  const long long tiles1 = tb_routed * ((2LL * c.I + 255) / 256) + tb_shared * ((2 * Is + 255) / 256);
+  cudaError_t e = launch_pair_gemm(EPI_PAIR_SWIGLU, r1, shared ? &s1 : nullptr, offsets, c.E, c.T, ws.status(), tiles1,
+                                   s, launches);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
-  // GEMM2: H [rows, I] x [d, I]^T -> Y [rows, d], stored fp32
-  GemmClass r2, s2;
-  r2.A = h; r2.a_rows = R; r2.a_cols = c.I;
-  r2.B = pb + P.w2; r2.b_rows = (long long)c.E * c.d; r2.b_cols = c.I;
-  r2.out = y_perm; r2.ld_out = c.d; r2.out_rows = R;
-  r2.N = c.d; r2.K = c.I; r2.a_k_mod = c.I; r2.b_rows_per_group = c.d; r2.mma_n = 256;
-  s2.A = hs; s2.a_rows = c.T; s2.a_cols = Is;
-  s2.B = pb + P.w2s; s2.b_rows = c.d; s2.b_cols = Is;
-  s2.out = y_shared; s2.ld_out = c.d; s2.out_rows = c.T;
-  s2.N = c.d; s2.K = int(Is); s2.a_k_mod = int(Is); s2.b_rows_per_group = 0; s2.mma_n = 256;
-  const long long tiles2 = (mt_routed + mt_shared) * ((c.d + 255) / 256);
+  // GEMM2: Y[rows, d] = H W2^T (fp32), W2 [d, I] per expert
+  PairClass r2, s2;
+  r2.W = pb + P.w2; r2.w_rows = (long long)c.E * c.d; r2.X = h; r2.x_rows = R; r2.K = c.I;
+  r2.M = c.d; r2.w_step = c.d; r2.out = y_perm; r2.ld_out = c.d; r2.out_rows = R;
+  s2.W = pb + P.w2s; s2.w_rows = c.d; s2.X = hs; s2.x_rows = c.T; s2.K = int(Is);
+  s2.M = c.d; s2.w_step = 0; s2.out = y_shared; s2.ld_out = c.d; s2.out_rows = c.T;
+  const long long tiles2 = (tb_routed + tb_shared) * ((c.d + 255) / 256);
   if (mark_stages) profile_mark(s);
-  e = launch_grouped_gemm(EPI_STORE_F32, r2, shared ? &s2 : nullptr, offsets, c.E, 0, c.T, ws.status(), tiles2, s,
-                          launches);
+  e = launch_pair_gemm(EPI_PAIR_F32, r2, shared ? &s2 : nullptr, offsets, c.E, c.T, ws.status(), tiles2, s, launches);
   return cuda_status(e);
 }
 
@@ -428,7 +438,7 @@ int32_t moe_forward_kernel_count(const moe_config* cfg) {
   if (c.T == 0) return 0;
   int n = 2;                                                        // logits + top-k
   if (use_tc_gate(c) && c.gate_w_dtype == MOE_F32) n += 1;          // W_g split
-  n += 5;                                                           // permute: 4 + gather
+  n += permute_launches(c.T) + 1;                                   // permute + gather
   n += 2;                                                           // GEMM1, GEMM2
   n += 1;                                                           // combine
   return n;

@@ -252,8 +252,9 @@ PackedLayout packed_layout(const moe_config& c) {
   PackedLayout L;
   const size_t eb = dtype_bytes(c.act_dtype);
   const long long Is = (long long)c.n_shared * c.I;
-  L.bi = (c.I % 128 == 0) ? 128 : c.I;
-  L.bis = (Is % 128 == 0) ? 128 : int(Is > 0 ? Is : 1);
+  // blocks of 16 hidden units: W1 rows, then the W3 rows of the same units
+  L.bi = (c.I % 16 == 0) ? 16 : c.I;
+  L.bis = (Is % 16 == 0) ? 16 : int(Is > 0 ? Is : 1);
   size_t off = 0;
   L.w13 = off;
   off = align_up(off + size_t(c.E) * 2 * c.I * c.d * eb, 256);

@@ -77,6 +77,8 @@ constexpr int MAX_NGROUP = 32;
 struct TopkArgs {
   int T, E, k, score_fn, method, n_group, topk_group, group_score, group_top, norm;
   float scale;
+  int nsplit;          // partial logit planes to add, in order
+  long long plane;     // elements between planes
 };
 
 // One warp per token.  Lane l holds experts l, l+32, l+64, ...
@@ -94,7 +96,13 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
 #pragma unroll
   for (int i = 0; i < MAXV; ++i) {
     const int e = lane + 32 * i;
-    lg[i] = e < a.E ? lrow[e] : NEG;
+    if (e < a.E) {
+      float v = lrow[e];
+      for (int sp = 1; sp < a.nsplit; ++sp) v = __fadd_rn(v, lrow[sp * a.plane + e]);
+      lg[i] = v;
+    } else {
+      lg[i] = NEG;
+    }
   }
   if (a.score_fn == MOE_SCORE_SOFTMAX) {
     float m = NEG;
@@ -268,9 +276,11 @@ cudaError_t launch_gate_logits_simt(const moe_config& c, const void* x, const vo
   return e;
 }
 
-cudaError_t launch_topk(const moe_config& c, const float* logits, const float* bias, int32_t* idx, float* w,
-                        cudaStream_t s, int* launches) {
+cudaError_t launch_topk(const moe_config& c, const float* logits, int nsplit, long long plane, const float* bias,
+                        int32_t* idx, float* w, cudaStream_t s, int* launches) {
   TopkArgs a;
+  a.nsplit = nsplit;
+  a.plane = plane;
   a.T = c.T;
   a.E = c.E;
   a.k = c.k;

@@ -1,0 +1,486 @@
+// Expert GEMMs of the routed and shared SwiGLU experts on CTA pairs
+// (tcgen05.mma.cta_group::2 + TMEM + TMA), with the SwiGLU epilogue fused.
+//
+// The expert FFN is w2(silu(w1 x) * w3 x) (intelliparadigm.com page, section
+// 3.3.1); the MoE listing of the DeepSeek-V2 walkthrough runs it per expert on
+// the rows routed to that expert, plus the shared experts on every token.
+//
+// Operand roles are swapped with respect to the layer's "tokens x weights^T":
+//
+//   D[f][j] = sum_k W[f][k] * X[j][k]
+//     W: 256 weight rows of one group (M, split 128/128 over the CTA pair)
+//     X: up to 256 token rows of the same group (N, split N/2 per CTA)
+//
+// so the ragged dimension (tokens per expert) is the MMA's N, which comes in
+// steps of 16, not the M of 128 or 256 rows: a group of n tokens costs
+// ceil(n/16)*16 columns of tensor-core work instead of ceil(n/128)*128 rows.
+// The pair shares each B (token) tile between its two SMs, so an SM loads
+// 32 KB of operands per 128x256x64 block of work instead of 48 KB.
+//
+//   GEMM1 (EPI_PAIR_SWIGLU): W = packed W1/W3 rows interleaved in blocks of 16
+//     (rows 32q..32q+15 of a CTA's 128 hold W1 features, 32q+16..32q+31 the W3
+//     rows of the same features), X = token rows; the epilogue pairs lane l
+//     with lane l+16 by a warp shuffle and stores H[token][f] in bf16.
+//   GEMM2 (EPI_PAIR_F32): W = W2 rows, X = H rows; Y[token][f] in fp32.
+//
+// Both classes of groups run in one persistent launch: class 0 = the routed
+// experts (group g = rows offsets[g] .. offsets[g+1] of the permuted tokens,
+// sizes read on the device), class 1 = the shared expert over all T tokens.
+//
+// CTA layout (192 threads, one CTA per SM, clusters of two CTAs):
+//   warp 0      TMA producer of this CTA's halves (6-stage ring, 128-byte
+//               swizzle); completion bytes are counted on rank 0's barrier
+//   warp 1      tensor-memory allocation (both CTAs); on rank 0 one thread
+//               issues the M=256 MMAs and commits to both CTAs' barriers
+//   warps 2..5  epilogue: tcgen05.ld of this CTA's 128 accumulator rows
+// Two 256-column accumulators per CTA let the epilogue overlap the next
+// tile's main loop.  Every wait is bounded; a CTA that gives up flags the
+// status word and tells its peer to stop too.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "internal.h"
+#include "tc_ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int PM = 128;               // weight rows per CTA
+constexpr int PAIR_M = 2 * PM;        // weight rows per pair tile
+constexpr int PN = 256;               // token columns per pair tile at most
+constexpr int XB = PN / 2;            // token rows loaded by each CTA
+constexpr int BK = 64;
+constexpr int STAGES = 6;
+constexpr int THREADS = 192;
+constexpr int A_BYTES = PM * BK * 2;
+constexpr int B_BYTES = XB * BK * 2;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int GUARD_BYTES = 16384;    // slack after the ring, never addressed by the pipeline
+constexpr int MAX_GROUPS = 272;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t ACC_STRIDE = 256;  // columns between the two accumulators
+constexpr int EPI_WARPS = 4;
+
+struct PairParams {
+  CUtensorMap tmW[2];
+  CUtensorMap tmX[2];
+  void* out[2];
+  long long ld_out[2];
+  long long out_rows[2];
+  int M[2];          // output features of one group (its weight rows)
+  int K[2];          // reduction length (multiple of 64)
+  int w_step[2];     // weight rows between consecutive groups of the class
+  const int32_t* offsets;
+  int num_routed;
+  int shared_rows;
+  int* status;
+};
+
+struct PairCtrl {
+  uint64_t full[STAGES];     // rank 0: both CTAs' operand bytes of a stage landed
+  uint64_t empty[STAGES];    // each CTA: the MMAs that read a stage completed
+  uint64_t tfull[2];         // each CTA: an accumulator buffer is complete
+  uint64_t tempty[2];        // rank 0: both CTAs' epilogues drained a buffer
+  uint64_t drain;            // rank 0: every issued MMA completed
+  uint32_t tmem_base;
+  int abort;
+  int ngroups;
+  int g0;
+  int tile_start[MAX_GROUPS + 1];
+  int row_start[MAX_GROUPS];
+  int rows[MAX_GROUPS];
+};
+
+constexpr size_t kPairSmem = 1024 + size_t(STAGES) * STAGE_BYTES + GUARD_BYTES + sizeof(PairCtrl);
+static_assert(kPairSmem <= 227 * 1024, "shared memory budget");
+// More than half of an SM's shared memory: one CTA per SM, so the full
+// tensor-memory allocation never waits on another resident CTA.
+static_assert(kPairSmem > 114 * 1024, "one CTA per SM");
+
+struct PairTile {
+  int cls, g, fb, tb, row_start, rows;
+  int n_valid;   // token rows of this tile
+  int n_mma;     // MMA N = n_valid rounded up to 16
+};
+
+__device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+__device__ __forceinline__ int pair_group_tiles(const PairParams& p, int cls, int rows) {
+  return cdiv(rows, PN) * cdiv(p.M[cls], PAIR_M);
+}
+
+// Warp-cooperative: per-group row ranges and the exclusive prefix of tiles.
+__device__ void pair_schedule(PairCtrl* c, const PairParams& p, int lane) {
+  const int g0 = p.num_routed;
+  const int ng = g0 + (p.shared_rows > 0 ? 1 : 0);
+  const int per = cdiv(ng, 32);
+  const int lo = min(ng, lane * per), hi = min(ng, lo + per);
+  int local = 0;
+  for (int g = lo; g < hi; ++g) {
+    const int cls = g < g0 ? 0 : 1;
+    int rs = 0, rows = 0;
+    if (cls == 0) {
+      rs = p.offsets[g];
+      rows = p.offsets[g + 1] - rs;
+    } else {
+      rows = p.shared_rows;
+    }
+    if (rows < 0 || rs < 0 || (long long)rs + rows > p.out_rows[cls]) {
+      flag_status(p.status, DEV_BAD_ROW);
+      rs = 0;
+      rows = 0;
+    }
+    c->row_start[g] = rs;
+    c->rows[g] = rows;
+    local += pair_group_tiles(p, cls, rows);
+  }
+  int incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  int run = incl - local;
+  for (int g = lo; g < hi; ++g) {
+    c->tile_start[g] = run;
+    run += pair_group_tiles(p, g < g0 ? 0 : 1, c->rows[g]);
+  }
+  if (lane == 31) {
+    c->tile_start[ng] = incl;
+    c->ngroups = ng;
+    c->g0 = g0;
+  }
+}
+
+// Tile -> (group, weight block, token block).  Within a group the block order
+// keeps the operand that is re-read the most resident in L2: with more token
+// blocks than weight blocks the token block is the outer loop (its rows are
+// re-used by every weight block), otherwise the weight block is.
+__device__ __forceinline__ PairTile pair_tile(const PairCtrl* c, const PairParams& p, int tile) {
+  int lo = 0, hi = c->ngroups - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (c->tile_start[mid] <= tile) lo = mid;
+    else hi = mid - 1;
+  }
+  PairTile t;
+  t.g = lo;
+  t.cls = lo < c->g0 ? 0 : 1;
+  t.row_start = c->row_start[lo];
+  t.rows = c->rows[lo];
+  const int local = tile - c->tile_start[lo];
+  const int tbn = cdiv(t.rows, PN), fbn = cdiv(p.M[t.cls], PAIR_M);
+  if (tbn > fbn) {
+    t.tb = local / fbn;
+    t.fb = local % fbn;
+  } else {
+    t.fb = local / tbn;
+    t.tb = local % tbn;
+  }
+  t.n_valid = min(PN, t.rows - t.tb * PN);
+  t.n_mma = (t.n_valid + 15) & ~15;
+  return t;
+}
+
+// Bounded wait; on giving up it flags the status word and stops both CTAs.
+__device__ __forceinline__ bool pair_wait(uint64_t* bar, uint32_t parity, PairCtrl* c, uint32_t peer_abort,
+                                          int* status, bool cluster_scope = false) {
+  if (cluster_scope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
+  volatile int* ab = &c->abort;
+  const unsigned long long t0 = globaltimer_ns();
+  uint32_t n = 0;
+  while (true) {
+    if (cluster_scope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
+    if ((++n & 63u) == 0u) {
+      if (*ab) return false;
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        *ab = 1;
+        st_remote_u32(peer_abort, 1u);
+        flag_status(status, DEV_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ void pair_producer(PairCtrl* c, const PairParams& p, uint8_t* stages, int total, uint32_t rank,
+                              uint32_t peer_abort) {
+  int stage = 0;
+  uint32_t phase = 0;
+  uint32_t issued = 0, issued_par = 0;
+  bool ok = true;
+  for (int tile = (int)cluster_id_x(); ok && tile < total; tile += (int)cluster_count_x()) {
+    const PairTile t = pair_tile(c, p, tile);
+    const int w_row = (t.cls == 0 ? t.g * p.w_step[0] : 0) + t.fb * PAIR_M + int(rank) * PM;
+    const int x_row = t.row_start + t.tb * PN + int(rank) * (t.n_mma / 2);
+    const int nk = p.K[t.cls] / BK;
+    for (int kb = 0; kb < nk; ++kb) {
+      if (!pair_wait(&c->empty[stage], phase ^ 1u, c, peer_abort, p.status)) {
+        ok = false;
+        break;
+      }
+      uint8_t* sa = stages + stage * STAGE_BYTES;
+      if (rank == 0) mbar_arrive_expect_tx(&c->full[stage], 2u * STAGE_BYTES);
+      const uint32_t fb = map_to_rank(smem_u32(&c->full[stage]), 0);   // rank 0's barrier
+      const int kc = kb * BK;
+      tma_load_2d_pair(sa, &p.tmW[t.cls], fb, kc, w_row);
+      tma_load_2d_pair(sa + A_BYTES, &p.tmX[t.cls], fb, kc, x_row);
+      issued |= 1u << stage;
+      issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
+      if (++stage == STAGES) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+  }
+  // The last copy into each stage was consumed (so it landed) before this CTA
+  // may leave; on the normal path these waits return at once.
+  for (int s = 0; s < STAGES; ++s)
+    if (issued & (1u << s)) pair_wait(&c->empty[s], (issued_par >> s) & 1u, c, peer_abort, p.status);
+}
+
+__device__ void pair_mma(PairCtrl* c, const PairParams& p, uint8_t* stages, uint32_t tmem, int total,
+                         uint32_t peer_abort) {
+  int stage = 0;
+  uint32_t phase = 0;
+  int ctr = 0;
+  bool ok = true;
+  for (int tile = (int)cluster_id_x(); ok && tile < total; tile += (int)cluster_count_x(), ++ctr) {
+    const PairTile t = pair_tile(c, p, tile);
+    const uint32_t idesc = idesc_bf16_f32(PAIR_M, t.n_mma);
+    const int acc = ctr & 1;
+    if (!pair_wait(&c->tempty[acc], (uint32_t(ctr >> 1) & 1u) ^ 1u, c, peer_abort, p.status, true)) break;
+    tc_fence_after();
+    const uint32_t d_tmem = tmem + uint32_t(acc) * ACC_STRIDE;
+    const int nk = p.K[t.cls] / BK;
+    for (int kb = 0; kb < nk; ++kb) {
+      if (!pair_wait(&c->full[stage], phase, c, peer_abort, p.status)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t a0 = smem_u32(stages + stage * STAGE_BYTES);
+      const uint32_t b0 = a0 + A_BYTES;
+#pragma unroll
+      for (int kk = 0; kk < BK / 16; ++kk)
+        mma_bf16_pair(d_tmem, sw128_kmajor_desc(a0 + kk * 32), sw128_kmajor_desc(b0 + kk * 32), idesc,
+                      (kb | kk) != 0 ? 1u : 0u);
+      mma_commit_pair(&c->empty[stage], 0x3);
+      if (++stage == STAGES) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+    if (ok) mma_commit_pair(&c->tfull[acc], 0x3);
+  }
+  // Every MMA issued here completes before tensor memory is released.
+  mma_commit_pair(&c->drain, 0x1);
+  pair_wait(&c->drain, 0u, c, peer_abort, p.status);
+}
+
+__device__ __forceinline__ float silu_f(float z) { return z / (1.0f + __expf(-z)); }
+
+// One lane waits and the verdict is broadcast, so the warp-collective tensor
+// memory loads that follow run on the whole warp.
+__device__ __forceinline__ bool pair_warp_wait(uint64_t* bar, uint32_t parity, PairCtrl* c, uint32_t peer_abort,
+                                               int* status, int lane) {
+  int ok = 1;
+  if (lane == 0) ok = pair_wait(bar, parity, c, peer_abort, status) ? 1 : 0;
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+template <int EPI>
+__device__ void pair_epilogue(PairCtrl* c, const PairParams& p, uint32_t tmem, int total, int warp, int lane,
+                              uint32_t rank, uint32_t peer_abort) {
+  const int q = warp & 3;   // the tensor-memory lane quarter this warp may read
+  int ctr = 0;
+  for (int tile = (int)cluster_id_x(); tile < total; tile += (int)cluster_count_x(), ++ctr) {
+    const PairTile t = pair_tile(c, p, tile);
+    const int acc = ctr & 1;
+    if (!pair_warp_wait(&c->tfull[acc], uint32_t(ctr >> 1) & 1u, c, peer_abort, p.status, lane)) break;
+    tc_fence_after();
+    const uint32_t tbase = tmem + uint32_t(acc) * ACC_STRIDE + (uint32_t(q * 32) << 16);
+    const long long row0 = (long long)t.row_start + (long long)t.tb * PN;
+    const int ncols = (t.n_valid + 15) & ~15;
+    if constexpr (EPI == EPI_PAIR_SWIGLU) {
+      // lane l < 16: W1 row of feature f; lane l + 16: the W3 row of the same f
+      const int f = t.fb * (PAIR_M / 2) + int(rank) * (PM / 2) + q * 16 + (lane & 15);
+      __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out[t.cls]) + f;
+      const long long ld = p.ld_out[t.cls];
+      const bool lo_half = lane < 16;
+#pragma unroll 1
+      for (int cc = 0; cc < ncols; cc += 16) {
+        float v[16];
+        tmem_ld16(tbase + cc, v);
+        // lanes < 16 keep tokens cc..cc+7, lanes >= 16 tokens cc+8..cc+15
+        float mine[8], other[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float send = lo_half ? v[8 + i] : v[i];
+          other[i] = __shfl_xor_sync(0xffffffffu, send, 16);
+          mine[i] = lo_half ? v[i] : v[8 + i];
+        }
+        const int j0 = cc + (lo_half ? 0 : 8);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float g = lo_half ? mine[i] : other[i];
+          const float u = lo_half ? other[i] : mine[i];
+          if (j0 + i < t.n_valid) out[(row0 + j0 + i) * ld] = __float2bfloat16_rn(silu_f(g) * u);
+        }
+      }
+    } else {
+      const int f = t.fb * PAIR_M + int(rank) * PM + q * 32 + lane;
+      const bool fvalid = f < p.M[t.cls];
+      float* out = static_cast<float*>(p.out[t.cls]) + f;
+      const long long ld = p.ld_out[t.cls];
+#pragma unroll 1
+      for (int cc = 0; cc < ncols; cc += 16) {
+        float v[16];
+        tmem_ld16(tbase + cc, v);
+        if (fvalid) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            if (cc + i < t.n_valid) out[(row0 + cc + i) * ld] = v[i];
+        }
+      }
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive_remote(map_to_rank(smem_u32(&c->tempty[acc]), 0));
+  }
+}
+
+template <int EPI>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
+    pair_gemm_kernel(const __grid_constant__ PairParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* stages = base;
+  PairCtrl* c = reinterpret_cast<PairCtrl*>(base + size_t(STAGES) * STAGE_BYTES + GUARD_BYTES);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const uint32_t peer_abort = map_to_rank(smem_u32(&c->abort), rank ^ 1u);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&c->full[s], 1);
+      mbar_init(&c->empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&c->tfull[a], 1);
+      mbar_init(&c->tempty[a], 2 * EPI_WARPS);
+    }
+    mbar_init(&c->drain, 1);
+    c->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&p.tmW[0]);
+    tma_prefetch_desc(&p.tmX[0]);
+    tma_prefetch_desc(&p.tmW[1]);
+    tma_prefetch_desc(&p.tmX[1]);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(&c->tmem_base, TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  if (warp == 2) pair_schedule(c, p, lane);
+  tc_fence_before();
+  // both CTAs' barriers, tensor memory and tile tables are ready
+  cluster_sync_all();
+  tc_fence_after();
+
+  const uint32_t tmem = c->tmem_base;
+  const int total = c->tile_start[c->ngroups];
+  if (warp == 0) {
+    if (lane == 0) pair_producer(c, p, stages, total, rank, peer_abort);
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) pair_mma(c, p, stages, tmem, total, peer_abort);
+  } else {
+    pair_epilogue<EPI>(c, p, tmem, total, warp, lane, rank, peer_abort);
+  }
+  tc_fence_before();
+  // neither CTA leaves while the other may still signal its barriers
+  cluster_sync_all();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, TMEM_COLS);
+  }
+}
+
+// bf16 [rows, cols] row-major, box = 64 columns x 128 rows, 128-byte swizzle.
+bool encode_pair_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols) {
+  auto enc = tensor_map_encoder();
+  if (enc == nullptr || rows <= 0 || cols <= 0) return false;
+  cuuint64_t dims[2] = {cuuint64_t(cols), cuuint64_t(rows)};
+  cuuint64_t strides[1] = {cuuint64_t(cols) * 2};
+  cuuint32_t box[2] = {64u, 128u};
+  cuuint32_t es[2] = {1u, 1u};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int EPI>
+cudaError_t launch_pair_epi(const PairParams& p, long long max_tiles, cudaStream_t stream) {
+  static int max_clusters = -1;
+  if (max_clusters < 0) {
+    cudaError_t e = cudaFuncSetAttribute(pair_gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         int(kPairSmem));
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * (num_sms() / 2), 1, 1);
+    cfg.blockDim = dim3(THREADS, 1, 1);
+    cfg.dynamicSmemBytes = kPairSmem;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, pair_gemm_kernel<EPI>, &cfg) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      n = num_sms() / 2;
+    }
+    max_clusters = n;
+  }
+  const long long pairs = max_tiles < max_clusters ? max_tiles : max_clusters;
+  pair_gemm_kernel<EPI><<<int(2 * pairs), THREADS, kPairSmem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_pair_gemm(int epi, const PairClass& c0, const PairClass* c1, const int32_t* offsets, int num_routed,
+                             int shared_rows, int* status, long long max_tiles, cudaStream_t stream, int* launches) {
+  if (max_tiles <= 0) return cudaSuccess;
+  PairParams p;
+  memset(&p, 0, sizeof(p));
+  const PairClass* cls[2] = {&c0, c1 != nullptr ? c1 : &c0};
+  for (int i = 0; i < 2; ++i) {
+    const PairClass& g = *cls[i];
+    if (g.K % BK != 0) return cudaErrorInvalidValue;
+    if (!encode_pair_map(&p.tmW[i], g.W, g.w_rows, g.K)) return cudaErrorInvalidValue;
+    if (!encode_pair_map(&p.tmX[i], g.X, g.x_rows, g.K)) return cudaErrorInvalidValue;
+    p.out[i] = g.out;
+    p.ld_out[i] = g.ld_out;
+    p.out_rows[i] = g.out_rows;
+    p.M[i] = g.M;
+    p.K[i] = g.K;
+    p.w_step[i] = g.w_step;
+  }
+  p.offsets = offsets;
+  p.num_routed = num_routed;
+  p.shared_rows = c1 != nullptr ? shared_rows : 0;
+  p.status = status;
+  if (num_routed + 1 > MAX_GROUPS) return cudaErrorInvalidValue;
+  cudaError_t e = epi == EPI_PAIR_SWIGLU ? launch_pair_epi<EPI_PAIR_SWIGLU>(p, max_tiles, stream)
+                                         : launch_pair_epi<EPI_PAIR_F32>(p, max_tiles, stream);
+  if (e == cudaSuccess && launches) ++*launches;
+  return e;
+}
+
+}  // namespace moe

@@ -1,25 +1,24 @@
-// Grouped bf16 GEMM on the 5th-generation tensor cores (tcgen05 + TMEM + TMA),
-// with the SwiGLU epilogue of the routed experts fused in.
+// Router gate GEMM on the 5th-generation tensor cores (tcgen05 + TMEM + TMA):
 //
-//   D[g] = A[g] * B[g]^T   A: rows of group g (K-major), B: the group's weight
-//   rows (nn.Linear layout, K-major), fp32 accumulation in tensor memory.
+//   logits[t][e] = sum_c x[t][c] * W_g[e][c]
 //
-// The expert FFN is w2(silu(w1 x) * w3 x) (intelliparadigm.com page, section
-// 3.3.1); the MoE listing of the DeepSeek-V2 walkthrough runs it per expert on
-// the rows routed to that expert, plus the shared experts on every token.
-// Here all experts run in one persistent launch: group sizes live on the
-// device (the permutation's offsets) and every CTA derives the same tile list
-// from them, so no host synchronisation is needed.
+// The MoEGate listing of the DeepSeek-V2 walkthrough computes the logits in
+// fp32.  bf16 x times bf16 W_g (or times each bf16 part of an fp32 W_g split
+// three ways along K) gives exact products, and the tensor cores accumulate
+// them in fp32; every 256-long partial sum is then added into registers with
+// fp32 round-to-nearest, so the logits carry the rounding of 256-long sums
+// only.  For small batches K is split into ranges whose fp32 partial planes
+// the top-k kernel adds in order.
 //
-// CTA layout (192 threads, one CTA per SM):
-//   warp 0      TMA producer: A tile 128x64 and B tile <=256x64 per stage
-//               into a 4-deep shared-memory ring (128-byte swizzle)
+// Persistent CTAs, one per SM (192 threads):
+//   warp 0      TMA producer: A tile 128x64 (tokens), B tile 128x64 (W_g rows)
+//               per stage into a 4-deep shared-memory ring (128-byte swizzle)
 //   warp 1      TMEM allocator + single-thread tcgen05.mma issuer
-//               (M=128, N<=256, K=16 per instruction)
-//   warps 2..5  epilogue: tcgen05.ld of the accumulator, SwiGLU or plain
-//               conversion, stores to global memory
-// Two 256-column accumulators in TMEM let the epilogue of tile i overlap the
-// main loop of tile i+1.
+//               (M=128, N=128, K=16 per instruction)
+//   warps 2..5  epilogue: tcgen05.ld of the partial sums, fp32 accumulation
+//               in registers, stores of the logits
+// Two accumulators in TMEM let the epilogue of one chunk overlap the MMAs of
+// the next.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -47,6 +46,8 @@ struct Params {
   long long ld_out[2];
   long long out_rows[2];
   int N[2], K[2], a_k_mod[2], b_step[2], mma_n[2];
+  int ksplit;                 // EPI_GATE_F32: K ranges per output tile (partial planes)
+  long long split_stride;     // elements between consecutive partial planes
   const int32_t* offsets;
   int num_routed;
   int rows_single0;
@@ -77,6 +78,8 @@ static_assert(kSmemBytes > 114 * 1024, "one CTA per SM");
 
 struct TileInfo {
   int cls, g, m_blk, n_blk, row_start, rows;
+  int kb_lo, kb_hi;   // k-block range of this tile
+  int ks;             // partial plane (split index) of the output
 };
 
 // Tile width and accumulation chunk of each epilogue mode.  EPI_GATE_F32 keeps
@@ -94,8 +97,13 @@ template <int EPI> struct Mode {
 __device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
 
 template <int EPI>
+__device__ __forceinline__ int splits(const Params& p) {
+  return EPI == EPI_GATE_F32 ? p.ksplit : 1;
+}
+
+template <int EPI>
 __device__ __forceinline__ int group_tiles(const Params& p, int cls, int rows) {
-  return cdiv(rows, BM) * cdiv(p.N[cls], Mode<EPI>::kBN);
+  return cdiv(rows, BM) * cdiv(p.N[cls], Mode<EPI>::kBN) * splits<EPI>(p);
 }
 
 // Warp-cooperative: per-group row ranges and the exclusive prefix of tiles.
@@ -163,8 +171,23 @@ __device__ __forceinline__ TileInfo tile_info(const Ctrl* c, const Params& p, in
   t.cls = lo < c->g0 ? 0 : 1;
   t.row_start = c->row_start[lo];
   t.rows = c->rows[lo];
-  const int local = tile - c->tile_start[lo];
+  int local = tile - c->tile_start[lo];
   const int mb = cdiv(t.rows, BM), nb = cdiv(p.N[t.cls], Mode<EPI>::kBN);
+  // K split (gate mode): the split index is the slowest, and each split owns
+  // a contiguous run of whole promotion chunks
+  const int nk = p.K[t.cls] / BK;
+  const int ns = splits<EPI>(p);
+  t.ks = local / (mb * nb);
+  local -= t.ks * mb * nb;
+  if (ns > 1) {
+    const int nch = cdiv(nk, Mode<EPI>::kChunk);
+    const int c_lo = t.ks * nch / ns, c_hi = (t.ks + 1) * nch / ns;
+    t.kb_lo = c_lo * Mode<EPI>::kChunk;
+    t.kb_hi = min(nk, c_hi * Mode<EPI>::kChunk);
+  } else {
+    t.kb_lo = 0;
+    t.kb_hi = nk;
+  }
   if (mb > nb) {
     t.m_blk = local / nb;
     t.n_blk = local % nb;
@@ -186,9 +209,8 @@ __device__ void producer(Ctrl* c, const Params& p, uint8_t* stages, int total) {
     const TileInfo t = tile_info<EPI>(c, p, tile);
     const int a_row = t.row_start + t.m_blk * BM;
     const int b_row = (t.cls == 0 ? t.g * p.b_step[0] : 0) + t.n_blk * Mode<EPI>::kBN;
-    const int nk = p.K[t.cls] / BK;
     const uint32_t bytes = A_BYTES + uint32_t(p.mma_n[t.cls]) * BK * 2;
-    for (int kb = 0; kb < nk; ++kb) {
+    for (int kb = t.kb_lo; kb < t.kb_hi; ++kb) {
       if (!mbar_wait(&c->empty[stage], phase ^ 1u, ab, p.status)) {
         ok = false;
         break;
@@ -225,9 +247,9 @@ __device__ void mma_issuer(Ctrl* c, const Params& p, uint8_t* stages, uint32_t t
   for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
     const TileInfo t = tile_info<EPI>(c, p, tile);
     const uint32_t idesc = idesc_bf16_f32(BM, p.mma_n[t.cls]);
-    const int nk = p.K[t.cls] / BK;
-    const int ck = Mode<EPI>::kChunk < nk ? Mode<EPI>::kChunk : nk;
-    for (int kb0 = 0; ok && kb0 < nk; kb0 += ck, ++chunk_ctr) {
+    const int nk = t.kb_hi;
+    const int ck = Mode<EPI>::kChunk < nk - t.kb_lo ? Mode<EPI>::kChunk : nk - t.kb_lo;
+    for (int kb0 = t.kb_lo; ok && kb0 < nk; kb0 += ck, ++chunk_ctr) {
       const int acc = chunk_ctr & 1;
       const uint32_t acc_par = uint32_t(chunk_ctr >> 1) & 1u;
       if (!mbar_wait(&c->tempty[acc], acc_par ^ 1u, ab, p.status)) {
@@ -263,13 +285,6 @@ __device__ void mma_issuer(Ctrl* c, const Params& p, uint8_t* stages, uint32_t t
   mbar_wait(&c->drain, 0u, nullptr, p.status);
 }
 
-__device__ __forceinline__ float silu_f(float z) { return z / (1.0f + __expf(-z)); }
-
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
-
 // One lane waits and the verdict is broadcast, so the warp-collective TMEM
 // loads that follow are always executed by the whole warp.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* ab, int* status, int lane) {
@@ -290,10 +305,9 @@ __device__ void epilogue(Ctrl* c, const Params& p, uint32_t tmem, int total, int
     const int row_local = t.m_blk * BM + r_in_tile;
     const bool valid = row_local < t.rows;
     const long long grow = (long long)t.row_start + row_local;
-    if constexpr (EPI == EPI_GATE_F32) {
+    {
       // sum of the tile's 256-long partial products, fp32 round-to-nearest
-      const int nk = p.K[t.cls] / BK;
-      const int nchunks = cdiv(nk, PROMOTE_KB);
+      const int nchunks = cdiv(t.kb_hi - t.kb_lo, PROMOTE_KB);
       float racc[128];
 #pragma unroll
       for (int i = 0; i < 128; ++i) racc[i] = 0.0f;
@@ -318,7 +332,7 @@ __device__ void epilogue(Ctrl* c, const Params& p, uint32_t tmem, int total, int
       if (ok && valid) {
         const int col0 = t.n_blk * 128;
         const int ncol = min(128, p.N[t.cls] - col0);
-        float* orow = static_cast<float*>(p.out[t.cls]) + grow * p.ld_out[t.cls] + col0;
+        float* orow = static_cast<float*>(p.out[t.cls]) + t.ks * p.split_stride + grow * p.ld_out[t.cls] + col0;
         if (ncol == 128) {
 #pragma unroll
           for (int i = 0; i < 32; ++i)
@@ -330,72 +344,6 @@ __device__ void epilogue(Ctrl* c, const Params& p, uint32_t tmem, int total, int
             if (i < ncol) orow[i] = racc[i];
         }
       }
-      continue;
-    } else {
-      const int acc = chunk_ctr & 1;
-      if (!warp_wait(&c->tfull[acc], uint32_t(chunk_ctr >> 1) & 1u, ab, p.status, lane)) break;
-      ++chunk_ctr;
-      tc_fence_after();
-      const uint32_t tbase = tmem + uint32_t(acc * BN) + (uint32_t(q * 32) << 16);
-      if constexpr (EPI == EPI_SWIGLU) {
-        // Tile columns [0,128) hold W1 rows, [128,256) the matching W3 rows.
-        __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out[t.cls]) + grow * p.ld_out[t.cls];
-        const int col0 = t.n_blk * (BN / 2);
-#pragma unroll 1
-        for (int cc = 0; cc < BN / 2; cc += 16) {
-          float g[16], u[16];
-          tmem_ld16(tbase + cc, g);
-          tmem_ld16(tbase + BN / 2 + cc, u);
-          if (valid) {
-            uint32_t w[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-              w[i] = pack_bf16x2(silu_f(g[2 * i]) * u[2 * i], silu_f(g[2 * i + 1]) * u[2 * i + 1]);
-            uint4* dst = reinterpret_cast<uint4*>(orow + col0 + cc);
-            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-            dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-          }
-        }
-      } else {
-        const int col0 = t.n_blk * BN;
-        const int ncol = min(BN, p.N[t.cls] - col0);
-        const int nld = min(p.mma_n[t.cls], BN);
-#pragma unroll 1
-        for (int cc = 0; cc < nld; cc += 16) {
-          float v[16];
-          tmem_ld16(tbase + cc, v);
-          if (valid && cc < ncol) {
-            if constexpr (EPI == EPI_STORE_BF16) {
-              __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out[t.cls]) + grow * p.ld_out[t.cls] + col0 + cc;
-              if (cc + 16 <= ncol) {
-                uint32_t w[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) w[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
-                uint4* dst = reinterpret_cast<uint4*>(orow);
-                dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-              } else {
-#pragma unroll
-                for (int i = 0; i < 16; ++i)
-                  if (cc + i < ncol) orow[i] = __float2bfloat16_rn(v[i]);
-              }
-            } else {
-              float* orow = static_cast<float*>(p.out[t.cls]) + grow * p.ld_out[t.cls] + col0 + cc;
-              if (cc + 16 <= ncol) {
-                float4* dst = reinterpret_cast<float4*>(orow);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-              } else {
-#pragma unroll
-                for (int i = 0; i < 16; ++i)
-                  if (cc + i < ncol) orow[i] = v[i];
-              }
-            }
-          }
-        }
-      }
-      tc_fence_before();
-      mbar_arrive(&c->tempty[acc]);
     }
   }
 }
@@ -455,6 +403,8 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const __grid_c
 }
 
 // ------------------------------------------------------------------- host side
+}  // namespace
+
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   if (fn == nullptr) {
@@ -467,6 +417,8 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   }
   return fn;
 }
+
+namespace {
 
 // bf16 [rows, cols] row-major, box = 64 columns x box_rows rows, 128-byte swizzle.
 bool encode_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, uint32_t box_rows) {
@@ -529,6 +481,8 @@ cudaError_t launch_grouped_gemm(int epi, const GemmClass& c0, const GemmClass* c
     p.b_step[i] = g.b_rows_per_group;
     p.mma_n[i] = g.mma_n;
   }
+  p.ksplit = c0.ksplit > 0 ? c0.ksplit : 1;
+  p.split_stride = c0.split_stride;
   p.offsets = offsets;
   p.num_routed = num_routed;
   p.rows_single0 = rows_single0;
@@ -536,12 +490,8 @@ cudaError_t launch_grouped_gemm(int epi, const GemmClass& c0, const GemmClass* c
   p.status = status;
   const int grid = int(max_tiles < num_sms() ? max_tiles : num_sms());
   cudaError_t e;
-  switch (epi) {
-    case EPI_SWIGLU: e = launch_epi<EPI_SWIGLU>(p, grid, stream); break;
-    case EPI_STORE_BF16: e = launch_epi<EPI_STORE_BF16>(p, grid, stream); break;
-    case EPI_STORE_F32: e = launch_epi<EPI_STORE_F32>(p, grid, stream); break;
-    default: e = launch_epi<EPI_GATE_F32>(p, grid, stream); break;
-  }
+  if (epi != EPI_GATE_F32) return cudaErrorInvalidValue;
+  e = launch_epi<EPI_GATE_F32>(p, grid, stream);
   if (e == cudaSuccess && launches) ++*launches;
   return e;
 }

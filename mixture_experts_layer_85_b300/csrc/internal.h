@@ -1,5 +1,7 @@
 // Host-side launchers shared between the kernel files and the C ABI (api.cu).
 #pragma once
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -26,11 +28,16 @@ struct GemmClass {
   int a_k_mod = 0;          // A column = k % a_k_mod (K-split gate); = K otherwise
   int b_rows_per_group = 0; // B row step between consecutive groups of the class
   int mma_n = 256;          // MMA N (<= 256, multiple of 16); B box rows
+  int ksplit = 1;           // EPI_GATE_F32 only: K ranges, one fp32 partial plane each
+  int64_t split_stride = 0; // elements between partial planes
 };
 
-enum EpiMode : int { EPI_SWIGLU = 0, EPI_STORE_BF16 = 1, EPI_STORE_F32 = 2, EPI_GATE_F32 = 3 };
+enum EpiMode : int { EPI_GATE_F32 = 3 };
 
 int num_sms();
+
+// cuTensorMapEncodeTiled from the driver (nullptr when unavailable).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 
 // Records the next armed profiling event on `s` (no-op when disarmed).
 void profile_mark(cudaStream_t s);
@@ -39,15 +46,41 @@ cudaError_t launch_grouped_gemm(int epi, const GemmClass& c0, const GemmClass* c
                                 int num_routed, int rows_single0, int shared_rows, int* status,
                                 long long max_tiles, cudaStream_t stream, int* launches);
 
+// ------------------------------------------------------- expert GEMMs (pairs)
+// One operand class of the CTA-pair expert GEMM, D = W * X^T per group: W
+// [w_rows, K] weight rows (group g of class 0 starts at row g * w_step; M rows
+// per group), X [x_rows, K] token rows (class 0: rows offsets[g] ..
+// offsets[g+1]; class 1: one group of shared_rows rows), both bf16 K-major.
+struct PairClass {
+  const void* W = nullptr;
+  int64_t w_rows = 0;
+  const void* X = nullptr;
+  int64_t x_rows = 0;
+  int K = 0;               // multiple of 64
+  int M = 0;               // weight rows (output features before SwiGLU) per group
+  int w_step = 0;
+  void* out = nullptr;     // [rows, M/2] bf16 (SwiGLU) or [rows, M] fp32
+  int64_t ld_out = 0;
+  int64_t out_rows = 0;
+};
+
+enum PairEpi : int { EPI_PAIR_SWIGLU = 0, EPI_PAIR_F32 = 1 };
+
+cudaError_t launch_pair_gemm(int epi, const PairClass& c0, const PairClass* c1, const int32_t* offsets, int num_routed,
+                             int shared_rows, int* status, long long max_tiles, cudaStream_t stream, int* launches);
+
 // ---------------------------------------------------------------------- router
 cudaError_t launch_gate_split(const float* wg, int E, int d, void* wsplit, cudaStream_t s, int* launches);
 cudaError_t launch_gate_logits_simt(const moe_config& c, const void* x, const void* wg, float* logits,
                                     cudaStream_t s, int* launches);
-cudaError_t launch_topk(const moe_config& c, const float* logits, const float* bias, int32_t* idx, float* w,
-                        cudaStream_t s, int* launches);
+// logits: `nsplit` fp32 partial planes of [T,E], `plane` elements apart, summed
+// in plane order before scoring (nsplit = 1: plain logits).
+cudaError_t launch_topk(const moe_config& c, const float* logits, int nsplit, long long plane, const float* bias,
+                        int32_t* idx, float* w, cudaStream_t s, int* launches);
 
 // ---------------------------------------------------------------- permutation
 int permute_chunks(int T);
+int permute_launches(int T);   // kernels of steps 1-3 (the gather is one more)
 cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* idx, int32_t* counts,
                            int32_t* offsets, int32_t* row2tok, int32_t* tok2row, void* x_perm,
                            int32_t* chunk_counts, int32_t* chunk_base, int* status, cudaStream_t s,

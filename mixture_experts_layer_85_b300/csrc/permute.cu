@@ -14,6 +14,11 @@
 //   3. scatter  per chunk: rank of a token inside its expert = popcount of the
 //               mask bits of earlier tokens -> row2tok / tok2row
 //   4. gather   x rows -> x_perm rows, 16-byte vectors, grid over all SMs
+//
+// Decode-sized batches (T <= SMALL_T) run steps 1-3 in one block instead
+// (permute_small_kernel: the same masks and ranks over 1024-token chunks taken
+// in order), so the dispatch costs two launches, not five.  Its results are
+// identical to the multi-block path.
 #include "internal.h"
 
 namespace moe {
@@ -136,6 +141,85 @@ __global__ void __launch_bounds__(CHUNK) permute_scatter_kernel(const int32_t* _
   }
 }
 
+constexpr int SMALL_BLOCK = 1024;           // tokens per chunk of the one-block path
+constexpr int SMALL_WORDS = SMALL_BLOCK / 32;
+constexpr int SMALL_T = 4 * SMALL_BLOCK;
+
+// Steps 1-3 in one block of SMALL_BLOCK threads (thread = token of the chunk).
+__global__ void __launch_bounds__(SMALL_BLOCK) permute_small_kernel(const int32_t* __restrict__ idx, int T, int E,
+                                                                    int k, int32_t* __restrict__ counts,
+                                                                    int32_t* __restrict__ offsets,
+                                                                    int32_t* __restrict__ row2tok,
+                                                                    int32_t* __restrict__ tok2row, int* status) {
+  __shared__ uint32_t mask[MAX_E][SMALL_WORDS];
+  __shared__ int base[MAX_E];
+  const int tid = threadIdx.x;
+  const int w = tid >> 5;
+  const uint32_t below = (1u << (tid & 31)) - 1u;
+  const int nch = (T + SMALL_BLOCK - 1) / SMALL_BLOCK;
+  const long long R = (long long)T * k;
+  if (tid < MAX_E) base[tid] = 0;
+  // pass 0 counts, pass 1 ranks; each pass walks the chunks in token order
+  for (int pass = 0; pass < 2; ++pass) {
+    for (int ch = 0; ch < nch; ++ch) {
+      for (int i = tid; i < E * SMALL_WORDS; i += SMALL_BLOCK) mask[i / SMALL_WORDS][i % SMALL_WORDS] = 0u;
+      __syncthreads();
+      const int t = ch * SMALL_BLOCK + tid;
+      if (t < T) {
+        for (int j = 0; j < k; ++j) {
+          const int e = idx[(long long)t * k + j];
+          if (e < 0 || e >= E) {
+            if (pass == 0) flag_status(status, DEV_BAD_EXPERT);
+            continue;
+          }
+          atomicOr(&mask[e][w], 1u << (tid & 31));
+        }
+      }
+      __syncthreads();
+      if (pass == 1 && t < T) {
+        for (int j = 0; j < k; ++j) {
+          const int e = idx[(long long)t * k + j];
+          if (e < 0 || e >= E) {
+            tok2row[(long long)t * k + j] = -1;
+            continue;
+          }
+          int rank = __popc(mask[e][w] & below);
+          for (int ww = 0; ww < w; ++ww) rank += __popc(mask[e][ww]);
+          const long long row = (long long)base[e] + rank;
+          if (row < 0 || row >= R) {
+            flag_status(status, DEV_BAD_ROW);
+            tok2row[(long long)t * k + j] = -1;
+            continue;
+          }
+          row2tok[row] = t;
+          tok2row[(long long)t * k + j] = (int32_t)row;
+        }
+      }
+      __syncthreads();
+      if (tid < E) {
+        int n = 0;
+        for (int ww = 0; ww < SMALL_WORDS; ++ww) n += __popc(mask[tid][ww]);
+        base[tid] += n;
+      }
+      __syncthreads();
+    }
+    if (pass == 0) {
+      // base holds the counts: turn them into offsets
+      int tot;
+      const int cnt = tid < E ? base[tid] : 0;
+      const int ex = block_exclusive_scan(cnt, &tot);
+      if (tid < E) {
+        counts[tid] = cnt;
+        offsets[tid] = ex;
+      }
+      if (tid == 0) offsets[E] = tot;
+      __syncthreads();
+      if (tid < E) base[tid] = ex;
+      __syncthreads();
+    }
+  }
+}
+
 // x_perm[r] = x[row2tok[r]]; one warp per row, 16-byte vectors.
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ row2tok,
                                                           long long R, int T, int vec_per_row, uint4* __restrict__ x_perm,
@@ -165,17 +249,23 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
 }  // namespace
 
 int permute_chunks(int T) { return (T + CHUNK - 1) / CHUNK; }
+int permute_launches(int T) { return T <= SMALL_T ? 1 : 4; }
 
 cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* idx, int32_t* counts,
                            int32_t* offsets, int32_t* row2tok, int32_t* tok2row, void* x_perm,
                            int32_t* chunk_counts, int32_t* chunk_base, int* status, cudaStream_t s,
                            int* launches) {
   const int nch = permute_chunks(c.T);
-  permute_count_kernel<<<nch, CHUNK, 0, s>>>(idx, c.T, c.E, c.k, chunk_counts, status);
-  permute_chunk_scan_kernel<<<c.E, CHUNK, 0, s>>>(chunk_counts, nch, c.E, chunk_base, counts);
-  permute_offsets_kernel<<<1, 256, 0, s>>>(counts, c.E, offsets);
-  permute_scatter_kernel<<<nch, CHUNK, 0, s>>>(idx, c.T, c.E, c.k, chunk_base, offsets, row2tok, tok2row, status);
-  if (launches) *launches += 4;
+  if (c.T <= SMALL_T) {
+    permute_small_kernel<<<1, SMALL_BLOCK, 0, s>>>(idx, c.T, c.E, c.k, counts, offsets, row2tok, tok2row, status);
+    if (launches) *launches += 1;
+  } else {
+    permute_count_kernel<<<nch, CHUNK, 0, s>>>(idx, c.T, c.E, c.k, chunk_counts, status);
+    permute_chunk_scan_kernel<<<c.E, CHUNK, 0, s>>>(chunk_counts, nch, c.E, chunk_base, counts);
+    permute_offsets_kernel<<<1, 256, 0, s>>>(counts, c.E, offsets);
+    permute_scatter_kernel<<<nch, CHUNK, 0, s>>>(idx, c.T, c.E, c.k, chunk_base, offsets, row2tok, tok2row, status);
+    if (launches) *launches += 4;
+  }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || x == nullptr || x_perm == nullptr) return e;
   const long long R = (long long)c.T * c.k;

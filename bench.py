@@ -249,6 +249,32 @@ def host_threads() -> int:
         return os.cpu_count() or 1
 
 
+def time_end_to_end_serial(layer, x, out_dtype, K, stream, world) -> float:
+    """Seconds for K steps of host tokens -> layer -> host output on one stream."""
+    T, d = x.shape
+    x_h = x.cpu().pin_memory()
+    out_h = torch.empty((T, d), dtype=out_dtype).pin_memory()
+    x_d = torch.empty_like(x)
+    out_d = torch.empty((T, d), dtype=out_dtype, device=x.device)
+
+    def run(n):
+        for _ in range(n):
+            x_d.copy_(x_h, non_blocking=True)
+            layer.forward(x_d, out_d, stream=stream)
+            out_h.copy_(out_d, non_blocking=True)
+
+    run(2)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    e0.record(stream)
+    run(K)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
+
+
 def time_end_to_end(layer, x, out_dtype, K, stream, world) -> float:
     """Seconds for K pipelined steps of host tokens -> layer -> host output."""
     T, d = x.shape
@@ -322,8 +348,6 @@ def run_ours(args, world, rank):
 
     K = args.steps
     S = _lib.MOE_FORWARD_STAGES
-    stage_ev = [torch.cuda.Event(enable_timing=True) for _ in range(K * (S + 1))]
-    _lib.moe_profile_arm(stage_ev)
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler()
@@ -341,7 +365,6 @@ def run_ours(args, world, rank):
     launches = _lib.moe_launch_count() - launches0
     barrier(world)
     clk = clocks.stop(host_t0, host_t1)
-    _lib.moe_profile_arm(None)
     code, word = layer.device_status()
     if code != 0:
         raise RuntimeError(f"device status after timed steps: {_lib.moe_status_string(code)} ({word})")
@@ -349,9 +372,19 @@ def run_ours(args, world, rank):
     elapsed_s = t_start.elapsed_time(t_end) / 1e3
     elapsed_max = max_over_ranks(elapsed_s, world)
     value = whole_job_rate(wl.T * K, world, elapsed_max)
+
+    # Stage breakdown in a separate pass: events recorded between the stages
+    # split the kernels' launch overlap, so they stay out of the timed steps.
+    n_prof = max(3, min(K, 10))
+    stage_ev = [torch.cuda.Event(enable_timing=True) for _ in range(n_prof * (S + 1))]
+    _lib.moe_profile_arm(stage_ev)
+    for _ in range(n_prof):
+        layer.forward(x, out, counts=counts)
+    torch.cuda.synchronize()
+    _lib.moe_profile_arm(None)
     stage_ms = {}
     for s in range(S):
-        v = [stage_ev[i * (S + 1) + s].elapsed_time(stage_ev[i * (S + 1) + s + 1]) for i in range(K)]
+        v = [stage_ev[i * (S + 1) + s].elapsed_time(stage_ev[i * (S + 1) + s + 1]) for i in range(n_prof)]
         stage_ms[_lib.moe_forward_stage_name(s)] = sum(v) / len(v)
 
     cnt = counts.cpu().numpy()
@@ -380,11 +413,27 @@ def run_ours(args, world, rank):
     # tokens host -> device, runs the layer and copies h' device -> host.  Two
     # buffer slots and two copy streams let step i's copies overlap the
     # neighbouring steps' forwards, as a serving loop would run them.
-    e2e_s = time_end_to_end(layer, x, out.dtype, K, stream, world)
+    # Small batches move few bytes and the cross-stream hand-offs cost more
+    # than they hide, so both loops are timed and the faster one is reported
+    # under its name.
+    e2e_pipe = time_end_to_end(layer, x, out.dtype, K, stream, world)
+    e2e_serial = time_end_to_end_serial(layer, x, out.dtype, K, stream, world)
+    e2e_s = min(e2e_pipe, e2e_serial)
     eb = x.element_size()
     e2e = {"value": round(whole_job_rate(wl.T * K, world, e2e_s), 1), "unit": UNIT,
            "h2d_bytes_per_step": wl.T * wl.d * eb, "d2h_bytes_per_step": wl.T * wl.d * out.element_size(),
-           "overlap": "H2D of step i+1 and D2H of step i-1 overlap the forward of step i (2 slots)"}
+           "loop": ("pipelined: H2D of step i+1 and D2H of step i-1 overlap the forward of step i (2 slots)"
+                    if e2e_pipe <= e2e_serial else "serial: H2D, forward, D2H in order on one stream"),
+           "pipelined_value": round(whole_job_rate(wl.T * K, world, e2e_pipe), 1),
+           "serial_value": round(whole_job_rate(wl.T * K, world, e2e_serial), 1)}
+
+    # host-side cost of one moe_forward call (argument checks, tensor maps, launches)
+    torch.cuda.synchronize()
+    h0 = time.perf_counter()
+    for _ in range(10):
+        layer.forward(x, out, counts=counts)
+    host_us = (time.perf_counter() - h0) / 10 * 1e6
+    torch.cuda.synchronize()
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -416,6 +465,7 @@ def run_ours(args, world, rank):
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": int(launches),
+        "host_us_per_forward_call": round(host_us, 1),
         "clocks": clk,
     }
     return res

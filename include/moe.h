@@ -172,6 +172,21 @@ MOE_API moe_status moe_permute_noalloc(const moe_config* cfg, const void* x, con
                                        int32_t* tok2row, void* x_perm, int32_t* device_status,
                                        void* stream);
 
+/* Auxiliary-loss-free load balancing after a layer step (V3 architecture
+ * page, section 1.2), with the load statistics of the balance-loss listing
+ * (Tencent Cloud DeepSeek page).
+ *   counts [E] int32 (device): assignments per expert of the step, e.g.
+ *   moe_forward's counts_out.  bias [E] fp32 (device), updated in place with
+ *   one fp32 addition: b_e - gamma when counts_e * E > sum(counts) (the expert
+ *   took more than the mean), b_e + gamma when it took fewer, unchanged at the
+ *   mean.  stats [3] fp32 (device, nullable): the unbiased standard deviation
+ *   of the load fractions counts / sum(counts), and the largest and smallest
+ *   count divided by the mean count.  device_status [1] int32 (device,
+ *   nullable): set to a non-zero DEV bit if a count is negative (treated as
+ *   zero).  One single-block kernel; no workspace; gamma must be finite. */
+MOE_API moe_status moe_balance_update(const moe_config* cfg, const int32_t* counts, float* bias, float gamma,
+                                      float* stats, int32_t* device_status, void* stream);
+
 /* Synchronises `stream`, reads the device status word of `ws` and returns
  * MOE_OK, MOE_ERR_DEVICE_TIMEOUT or MOE_ERR_DEVICE_BOUNDS.  `detail` (nullable)
  * receives the raw word. */

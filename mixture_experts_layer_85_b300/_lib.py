@@ -30,7 +30,7 @@ MOE_GROUP_MAX, MOE_GROUP_SUM_TOP = 0, 1
 EXPORTED = ["moe_workspace_size", "moe_packed_size", "moe_prepack_experts", "moe_gate_topk", "moe_permute",
             "moe_grouped_swiglu", "moe_combine", "moe_forward", "moe_get_device_status", "moe_status_string",
             "moe_launch_count", "moe_forward_kernel_count", "moe_profile_arm", "moe_forward_stage_name",
-            "moe_permute_noalloc"]
+            "moe_permute_noalloc", "moe_balance_update"]
 MOE_FORWARD_STAGES = 5
 
 
@@ -62,6 +62,7 @@ _sigs = {
     "moe_profile_arm": [ctypes.POINTER(_P), ctypes.c_int32],
     "moe_forward_stage_name": [ctypes.c_int32],
     "moe_permute_noalloc": [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P],
+    "moe_balance_update": [_CFG, _P, _P, ctypes.c_float, _P, _P, _P],
 }
 for _name, _args in _sigs.items():
     _f = getattr(_lib, _name)
@@ -171,6 +172,12 @@ def moe_permute_noalloc(cfg, x, idx, counts, offsets, row2tok, tok2row, x_perm, 
     _check(_lib.moe_permute_noalloc(ctypes.byref(cfg), _ptr(x), _ptr(idx), _ptr(counts), _ptr(offsets),
                                     _ptr(row2tok), _ptr(tok2row), _ptr(x_perm), _ptr(device_status),
                                     _stream(stream)), "moe_permute_noalloc")
+
+
+def moe_balance_update(cfg, counts, bias, gamma: float, stats=None, device_status=None, stream=None):
+    """Aux-loss-free bias update from per-expert counts (bias updated in place)."""
+    _check(_lib.moe_balance_update(ctypes.byref(cfg), _ptr(counts), _ptr(bias), float(gamma), _ptr(stats),
+                                   _ptr(device_status), _stream(stream)), "moe_balance_update")
 
 
 def moe_get_device_status(ws, stream=None) -> tuple:

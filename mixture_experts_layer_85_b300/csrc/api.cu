@@ -208,7 +208,7 @@ moe_status run_experts(const moe_config& c, const void* x_perm, const int32_t* o
   s1.M = int(2 * Is); s1.w_step = 0; s1.out = hs; s1.ld_out = Is; s1.out_rows = c.T;
   const long long tiles1 = tb_routed * ((2LL * c.I + 255) / 256) + tb_shared * ((2 * Is + 255) / 256);
   cudaError_t e = launch_pair_gemm(EPI_PAIR_SWIGLU, r1, shared ? &s1 : nullptr, offsets, c.E, c.T, ws.status(), tiles1,
-                                   s, launches);
+                                   s, launches, true);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   // GEMM2: Y[rows, d] = H W2^T (fp32), W2 [d, I] per expert
   PairClass r2, s2;
@@ -218,7 +218,8 @@ moe_status run_experts(const moe_config& c, const void* x_perm, const int32_t* o
   s2.M = c.d; s2.w_step = 0; s2.out = y_shared; s2.ld_out = c.d; s2.out_rows = c.T;
   const long long tiles2 = (tb_routed + tb_shared) * ((c.d + 255) / 256);
   if (mark_stages) profile_mark(s);
-  e = launch_pair_gemm(EPI_PAIR_F32, r2, shared ? &s2 : nullptr, offsets, c.E, c.T, ws.status(), tiles2, s, launches);
+  e = launch_pair_gemm(EPI_PAIR_F32, r2, shared ? &s2 : nullptr, offsets, c.E, c.T, ws.status(), tiles2, s, launches,
+                       false);
   return cuda_status(e);
 }
 
@@ -390,6 +391,22 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const void* Wg, con
   if (st == MOE_OK) profile_mark(s);
   count_launches(n);
   return st;
+}
+
+moe_status moe_balance_update(const moe_config* cfg, const int32_t* counts, float* bias, float gamma, float* stats,
+                              int32_t* device_status, void* stream) {
+  moe_status st = check_config(cfg);
+  if (st != MOE_OK) return st;
+  if (!counts || !bias || !aligned16(counts) || !aligned16(bias)) return MOE_ERR_INVALID_ARG;
+  if (stats != nullptr && !aligned16(stats)) return MOE_ERR_INVALID_ARG;
+  if (!(gamma == gamma) || gamma > 3.0e38f || gamma < -3.0e38f) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (device_status != nullptr && cudaMemsetAsync(device_status, 0, sizeof(int32_t), s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  int n = 0;
+  cudaError_t e = launch_balance_update(*cfg, counts, bias, gamma, stats, device_status, s, &n);
+  count_launches(n);
+  return cuda_status(e);
 }
 
 moe_status moe_get_device_status(const void* ws, void* stream, int32_t* detail) {

@@ -25,6 +25,16 @@ __device__ __forceinline__ unsigned long long globaltimer_ns() {
   return t;
 }
 
+// Programmatic dependent launch.  Every kernel of the layer lets the next
+// kernel of the stream begin launching as soon as all of its own CTAs are
+// running, and waits for its predecessor grid to complete (with its memory
+// visible) before it reads that grid's outputs or writes anything the
+// predecessor might still read.  Without the launch attribute both are no-ops.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void flag_status(int* status, int bits) {
   if (status) atomicOr(status, bits);
 }

@@ -186,13 +186,17 @@ template <> struct StoreN<__nv_bfloat16, 4> {
 };
 
 // out[t] = sum_j w[t,j] * y_perm[tok2row[t,j]] + y_shared[t], fp32 accumulation
-// in slot order.  One block per token (grid-stride), 16-byte vector loads.
+// in slot order.  Blocks stride over tokens; blockIdx.y splits each row into
+// gridDim.y slices so that small batches still spread over the GPU.  16-byte
+// vector loads.
 template <typename T, typename O, int MAXK>
 __global__ void __launch_bounds__(128) combine_kernel(const uint4* __restrict__ y_perm, const uint4* __restrict__ y_shared,
                                                       const int32_t* __restrict__ tok2row, const float* __restrict__ w,
                                                       int Tn, int k, long long R, int vec_per_row,
                                                       O* __restrict__ out, int* status) {
   constexpr int N = Vec16<T>::N;
+  pdl_launch_dependents();
+  pdl_wait();
   for (int t = blockIdx.x; t < Tn; t += gridDim.x) {
     long long rows[MAXK];
     float g[MAXK];
@@ -210,7 +214,9 @@ __global__ void __launch_bounds__(128) combine_kernel(const uint4* __restrict__ 
         }
       }
     }
-    for (int v = threadIdx.x; v < vec_per_row; v += blockDim.x) {
+    const int per = (vec_per_row + gridDim.y - 1) / gridDim.y;
+    const int v_end = min(vec_per_row, int(blockIdx.y + 1) * per);
+    for (int v = blockIdx.y * per + threadIdx.x; v < v_end; v += blockDim.x) {
       float acc[N];
 #pragma unroll
       for (int i = 0; i < N; ++i) acc[i] = 0.0f;
@@ -238,12 +244,15 @@ template <typename T, typename O>
 cudaError_t combine_typed(const moe_config& c, const uint4* yp, const uint4* ys, const int32_t* tok2row, const float* w,
                           void* out, int* status, cudaStream_t s) {
   const int vec = int(size_t(c.d) * sizeof(T) / 16);
-  const int grid = c.T < 65535 ? c.T : 65535;
+  const int gx = c.T < 65535 ? c.T : 65535;
+  // row slices of at least 128 vectors until the grid covers the SMs twice
+  int gy = 1;
+  while ((long long)gx * gy < 2LL * num_sms() && (vec + 2 * gy - 1) / (2 * gy) >= 128) gy *= 2;
+  const dim3 grid(gx, gy);
   const long long R = (long long)c.T * c.k;
   O* o = static_cast<O*>(out);
-  if (c.k <= 8) combine_kernel<T, O, 8><<<grid, 128, 0, s>>>(yp, ys, tok2row, w, c.T, c.k, R, vec, o, status);
-  else combine_kernel<T, O, 16><<<grid, 128, 0, s>>>(yp, ys, tok2row, w, c.T, c.k, R, vec, o, status);
-  return cudaGetLastError();
+  if (c.k <= 8) return launch_pdl(combine_kernel<T, O, 8>, grid, dim3(128), 0, s, yp, ys, tok2row, w, c.T, c.k, R, vec, o, status);
+  return launch_pdl(combine_kernel<T, O, 16>, grid, dim3(128), 0, s, yp, ys, tok2row, w, c.T, c.k, R, vec, o, status);
 }
 
 }  // namespace

@@ -19,6 +19,8 @@ namespace {
 // fp32 W_g -> [hi | mid | lo] bf16 along K, so that x . w = x . hi + x . mid + x . lo
 // exactly in fp32 products (bf16 x times bf16 parts) for the tensor-core gate.
 __global__ void gate_split_kernel(const float* __restrict__ wg, int E, int d, __nv_bfloat16* __restrict__ out) {
+  pdl_launch_dependents();
+  pdl_wait();
   const long long n = (long long)E * d;
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
     const long long e = i / d, c = i % d;
@@ -72,7 +74,6 @@ __global__ void __launch_bounds__(256) gate_logits_simt_kernel(const TX* __restr
 }
 
 constexpr int MAXV = 8;        // experts per lane (E <= 256)
-constexpr int MAX_NGROUP = 32;
 
 struct TopkArgs {
   int T, E, k, score_fn, method, n_group, topk_group, group_score, group_top, norm;
@@ -81,28 +82,50 @@ struct TopkArgs {
   long long plane;     // elements between planes
 };
 
-// One warp per token.  Lane l holds experts l, l+32, l+64, ...
-__global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ logits, const float* __restrict__ bias,
-                                                   TopkArgs a, int32_t* __restrict__ idx_out,
-                                                   float* __restrict__ w_out) {
+constexpr int TOPK_WARPS = 8;   // tokens per block
+
+// Block of TOPK_WARPS warps, one token per warp.  First the whole block forms
+// the logits of its tokens in shared memory (partial planes added in plane
+// order, loads batched so they are in flight together); then lane l of a
+// token's warp holds experts l, l+32, l+64, ...
+__global__ void __launch_bounds__(TOPK_WARPS * 32) topk_kernel(const float* __restrict__ logits,
+                                                               const float* __restrict__ bias, TopkArgs a,
+                                                               int32_t* __restrict__ idx_out,
+                                                               float* __restrict__ w_out) {
+  __shared__ float lg_s[TOPK_WARPS][MAXV * 32];
+  pdl_launch_dependents();
+  pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x * (blockDim.x >> 5) + warp;
+  const int t0 = blockIdx.x * TOPK_WARPS;
+  for (int i = threadIdx.x; i < TOPK_WARPS * a.E; i += blockDim.x) {
+    const int tt = i / a.E, e = i - tt * a.E;
+    float v = 0.0f;
+    if (t0 + tt < a.T) {
+      const float* p = logits + (long long)(t0 + tt) * a.E + e;
+      v = p[0];
+      int sp = 1;
+      for (; sp + 8 <= a.nsplit; sp += 8) {
+        float u[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) u[j] = p[(sp + j) * a.plane];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v = __fadd_rn(v, u[j]);
+      }
+      for (; sp < a.nsplit; ++sp) v = __fadd_rn(v, p[sp * a.plane]);
+    }
+    lg_s[tt][e] = v;
+  }
+  __syncthreads();
+  const int t = t0 + warp;
   if (t >= a.T) return;
   const float NEG = -INFINITY;
   float s[MAXV], sel[MAXV];
-  const float* lrow = logits + (long long)t * a.E;
 
   float lg[MAXV];
 #pragma unroll
   for (int i = 0; i < MAXV; ++i) {
     const int e = lane + 32 * i;
-    if (e < a.E) {
-      float v = lrow[e];
-      for (int sp = 1; sp < a.nsplit; ++sp) v = __fadd_rn(v, lrow[sp * a.plane + e]);
-      lg[i] = v;
-    } else {
-      lg[i] = NEG;
-    }
+    lg[i] = e < a.E ? lg_s[warp][e] : NEG;
   }
   if (a.score_fn == MOE_SCORE_SOFTMAX) {
     float m = NEG;
@@ -138,8 +161,9 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
   if (a.method == MOE_TOPK_GROUP_LIMITED && a.topk_group < a.n_group) {
     const int gsz = a.E / a.n_group;
     uint32_t kept = 0;   // bit g: group g stays eligible (same in every lane)
-    float gscore[MAX_NGROUP];
+    float my_gscore = NEG;   // lane g holds the score of group g
     for (int g = 0; g < a.n_group; ++g) {
+      float gscore;
       if (a.group_score == MOE_GROUP_MAX) {
         float m = NEG;
 #pragma unroll
@@ -147,7 +171,7 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
           const int e = lane + 32 * i;
           if ((elig >> i & 1u) && e / gsz == g) m = fmaxf(m, sel[i]);
         }
-        gscore[g] = warp_max(m);
+        gscore = warp_max(m);
       } else {
         // sum of the group's top-m scores, in descending order, in fp32
         uint32_t used = 0;
@@ -167,14 +191,16 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
           if (id != 0x7fffffff && (id & 31) == lane) used |= 1u << (id >> 5);
           acc = (r == 0) ? v : __fadd_rn(acc, v);
         }
-        gscore[g] = acc;
+        gscore = acc;
       }
+      if (lane == g) my_gscore = gscore;
     }
+    // the topk_group best groups; equal scores go to the lower group index
     for (int r = 0; r < a.topk_group; ++r) {
-      int best = -1;
-      for (int g = 0; g < a.n_group; ++g)
-        if (!(kept >> g & 1u) && (best < 0 || gscore[g] > gscore[best])) best = g;
-      kept |= 1u << best;
+      float v = (lane < a.n_group && !(kept >> lane & 1u)) ? my_gscore : NEG;
+      int id = lane < a.n_group && !(kept >> lane & 1u) ? lane : 0x7fffffff;
+      warp_argmax(v, id);
+      kept |= 1u << id;
     }
 #pragma unroll
     for (int i = 0; i < MAXV; ++i) {
@@ -227,9 +253,9 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
 cudaError_t launch_gate_split(const float* wg, int E, int d, void* wsplit, cudaStream_t s, int* launches) {
   const long long n = (long long)E * d;
   const int grid = (int)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
-  gate_split_kernel<<<grid, 256, 0, s>>>(wg, E, d, static_cast<__nv_bfloat16*>(wsplit));
+  cudaError_t e = launch_pdl(gate_split_kernel, dim3(grid), dim3(256), 0, s, wg, E, d, static_cast<__nv_bfloat16*>(wsplit));
   if (launches) ++*launches;
-  return cudaGetLastError();
+  return e;
 }
 
 template <typename TX, typename TW, int TB>
@@ -292,10 +318,10 @@ cudaError_t launch_topk(const moe_config& c, const float* logits, int nsplit, lo
   a.group_top = c.group_top;
   a.norm = c.norm_topk;
   a.scale = c.routed_scaling_factor;
-  const int warps = 8;
-  topk_kernel<<<(c.T + warps - 1) / warps, warps * 32, 0, s>>>(logits, bias, a, idx, w);
+  cudaError_t e = launch_pdl(topk_kernel, dim3((c.T + TOPK_WARPS - 1) / TOPK_WARPS), dim3(TOPK_WARPS * 32), 0, s,
+                             logits, bias, a, idx, w);
   if (launches) ++*launches;
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace moe

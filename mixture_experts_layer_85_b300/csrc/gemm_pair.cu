@@ -27,9 +27,13 @@
 // experts (group g = rows offsets[g] .. offsets[g+1] of the permuted tokens,
 // sizes read on the device), class 1 = the shared expert over all T tokens.
 //
+// Each TMA copy moves two k-blocks (3-D tensor maps: 64 columns x rows x 2
+// k-blocks): a copy instruction has a fixed cost in the copy engine, so fewer,
+// larger copies raise the rate at which an SM's shared memory fills.
+//
 // CTA layout (192 threads, one CTA per SM, clusters of two CTAs):
-//   warp 0      TMA producer of this CTA's halves (6-stage ring, 128-byte
-//               swizzle); completion bytes are counted on rank 0's barrier
+//   warp 0      TMA producer of this CTA's halves (3-stage ring of 2 k-blocks,
+//               128-byte swizzle); completion bytes count on rank 0's barrier
 //   warp 1      tensor-memory allocation (both CTAs); on rank 0 one thread
 //               issues the M=256 MMAs and commits to both CTAs' barriers
 //   warps 2..5  epilogue: tcgen05.ld of this CTA's 128 accumulator rows
@@ -49,25 +53,31 @@ constexpr int PM = 128;               // weight rows per CTA
 constexpr int PAIR_M = 2 * PM;        // weight rows per pair tile
 constexpr int PN = 256;               // token columns per pair tile at most
 constexpr int XB = PN / 2;            // token rows loaded by each CTA
-constexpr int BK = 64;
-constexpr int STAGES = 6;
-constexpr int THREADS = 192;
-constexpr int A_BYTES = PM * BK * 2;
-constexpr int B_BYTES = XB * BK * 2;
+constexpr int BK = 64;                // K of one k-block (one 128-byte swizzle row)
+constexpr int KB_STAGE = 2;           // k-blocks per stage and per TMA copy
+constexpr int STAGES = 3;
+constexpr int THREADS = 224;
+constexpr int A_KB_BYTES = PM * BK * 2;          // one k-block of this CTA's weight rows
+constexpr int B_KB_BYTES = XB * BK * 2;          // one k-block of this CTA's token rows
+constexpr int A_BYTES = KB_STAGE * A_KB_BYTES;
+constexpr int B_BYTES = KB_STAGE * B_KB_BYTES;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int GUARD_BYTES = 16384;    // slack after the ring, never addressed by the pipeline
+constexpr int XSMALL = 32;                       // token rows of the small box (decode-sized tiles)
+constexpr int XS_KB_BYTES = XSMALL * BK * 2;
 constexpr int MAX_GROUPS = 272;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_STRIDE = 256;  // columns between the two accumulators
 constexpr int EPI_WARPS = 4;
 
 struct PairParams {
-  CUtensorMap tmW[2];
-  CUtensorMap tmX[2];
+  CUtensorMap tmW[2];     // weights: 64 x 128 rows x 2 k-blocks
+  CUtensorMap tmX[2];     // tokens: 64 x 128 rows x 2 k-blocks
+  CUtensorMap tmXs[2];    // tokens: 64 x 32 rows x 2 k-blocks
   void* out[2];
   long long ld_out[2];
   long long out_rows[2];
   int M[2];          // output features of one group (its weight rows)
+  int early_shared;  // shared-expert tiles run before the predecessor grid completes
   int K[2];          // reduction length (multiple of 64)
   int w_step[2];     // weight rows between consecutive groups of the class
   const int32_t* offsets;
@@ -84,14 +94,15 @@ struct PairCtrl {
   uint64_t drain;            // rank 0: every issued MMA completed
   uint32_t tmem_base;
   int abort;
-  int ngroups;
-  int g0;
+  int shared_tiles;          // tiles [0, shared_tiles): the shared expert
+  int routed_tiles;          // then the routed experts' tiles
+  int routed_ready;          // the routed tile table is built
   int tile_start[MAX_GROUPS + 1];
   int row_start[MAX_GROUPS];
   int rows[MAX_GROUPS];
 };
 
-constexpr size_t kPairSmem = 1024 + size_t(STAGES) * STAGE_BYTES + GUARD_BYTES + sizeof(PairCtrl);
+constexpr size_t kPairSmem = 1024 + size_t(STAGES) * STAGE_BYTES + sizeof(PairCtrl);
 static_assert(kPairSmem <= 227 * 1024, "shared memory budget");
 // More than half of an SM's shared memory: one CTA per SM, so the full
 // tensor-memory allocation never waits on another resident CTA.
@@ -109,30 +120,24 @@ __device__ __forceinline__ int pair_group_tiles(const PairParams& p, int cls, in
   return cdiv(rows, PN) * cdiv(p.M[cls], PAIR_M);
 }
 
-// Warp-cooperative: per-group row ranges and the exclusive prefix of tiles.
+// Warp-cooperative: row ranges of the routed groups (from the dispatch
+// offsets) and the exclusive prefix of their tiles.
 __device__ void pair_schedule(PairCtrl* c, const PairParams& p, int lane) {
-  const int g0 = p.num_routed;
-  const int ng = g0 + (p.shared_rows > 0 ? 1 : 0);
+  const int ng = p.num_routed;
   const int per = cdiv(ng, 32);
   const int lo = min(ng, lane * per), hi = min(ng, lo + per);
   int local = 0;
   for (int g = lo; g < hi; ++g) {
-    const int cls = g < g0 ? 0 : 1;
-    int rs = 0, rows = 0;
-    if (cls == 0) {
-      rs = p.offsets[g];
-      rows = p.offsets[g + 1] - rs;
-    } else {
-      rows = p.shared_rows;
-    }
-    if (rows < 0 || rs < 0 || (long long)rs + rows > p.out_rows[cls]) {
+    int rs = p.offsets[g];
+    int rows = p.offsets[g + 1] - rs;
+    if (rows < 0 || rs < 0 || (long long)rs + rows > p.out_rows[0]) {
       flag_status(p.status, DEV_BAD_ROW);
       rs = 0;
       rows = 0;
     }
     c->row_start[g] = rs;
     c->rows[g] = rows;
-    local += pair_group_tiles(p, cls, rows);
+    local += pair_group_tiles(p, 0, rows);
   }
   int incl = local;
 #pragma unroll
@@ -143,32 +148,42 @@ __device__ void pair_schedule(PairCtrl* c, const PairParams& p, int lane) {
   int run = incl - local;
   for (int g = lo; g < hi; ++g) {
     c->tile_start[g] = run;
-    run += pair_group_tiles(p, g < g0 ? 0 : 1, c->rows[g]);
+    run += pair_group_tiles(p, 0, c->rows[g]);
   }
   if (lane == 31) {
     c->tile_start[ng] = incl;
-    c->ngroups = ng;
-    c->g0 = g0;
+    c->routed_tiles = incl;
   }
 }
 
-// Tile -> (group, weight block, token block).  Within a group the block order
+// Tile numbering: [0, shared_tiles) the shared expert (class 1), then the
+// routed experts (class 0) in expert order.  Within a group the block order
 // keeps the operand that is re-read the most resident in L2: with more token
 // blocks than weight blocks the token block is the outer loop (its rows are
 // re-used by every weight block), otherwise the weight block is.
 __device__ __forceinline__ PairTile pair_tile(const PairCtrl* c, const PairParams& p, int tile) {
-  int lo = 0, hi = c->ngroups - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (c->tile_start[mid] <= tile) lo = mid;
-    else hi = mid - 1;
-  }
   PairTile t;
-  t.g = lo;
-  t.cls = lo < c->g0 ? 0 : 1;
-  t.row_start = c->row_start[lo];
-  t.rows = c->rows[lo];
-  const int local = tile - c->tile_start[lo];
+  int local;
+  if (tile < c->shared_tiles) {
+    t.g = 0;
+    t.cls = 1;
+    t.row_start = 0;
+    t.rows = p.shared_rows;
+    local = tile;
+  } else {
+    const int rt = tile - c->shared_tiles;
+    int lo = 0, hi = p.num_routed - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (c->tile_start[mid] <= rt) lo = mid;
+      else hi = mid - 1;
+    }
+    t.g = lo;
+    t.cls = 0;
+    t.row_start = c->row_start[lo];
+    t.rows = c->rows[lo];
+    local = rt - c->tile_start[lo];
+  }
   const int tbn = cdiv(t.rows, PN), fbn = cdiv(p.M[t.cls], PAIR_M);
   if (tbn > fbn) {
     t.tb = local / fbn;
@@ -180,6 +195,28 @@ __device__ __forceinline__ PairTile pair_tile(const PairCtrl* c, const PairParam
   t.n_valid = min(PN, t.rows - t.tb * PN);
   t.n_mma = (t.n_valid + 15) & ~15;
   return t;
+}
+
+// Whether `tile` exists.  Shared-expert tiles need nothing; a routed tile
+// needs the routed table, which is built once the dispatch has completed
+// (bounded wait on the flag).
+__device__ __forceinline__ bool pair_tile_exists(PairCtrl* c, int tile, int* status) {
+  if (tile < c->shared_tiles) return true;
+  volatile int* ready = &c->routed_ready;
+  if (!*ready) {
+    const unsigned long long t0 = globaltimer_ns();
+    while (!*ready) {
+      if (*reinterpret_cast<volatile int*>(&c->abort)) return false;
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        c->abort = 1;
+        flag_status(status, DEV_TIMEOUT);
+        return false;
+      }
+      __nanosleep(64);
+    }
+  }
+  __threadfence_block();
+  return tile < c->shared_tiles + c->routed_tiles;
 }
 
 // Bounded wait; on giving up it flags the status word and stops both CTAs.
@@ -203,28 +240,36 @@ __device__ __forceinline__ bool pair_wait(uint64_t* bar, uint32_t parity, PairCt
   }
 }
 
-__device__ void pair_producer(PairCtrl* c, const PairParams& p, uint8_t* stages, int total, uint32_t rank,
+__device__ void pair_producer(PairCtrl* c, const PairParams& p, uint8_t* stages, uint32_t rank,
                               uint32_t peer_abort) {
   int stage = 0;
   uint32_t phase = 0;
   uint32_t issued = 0, issued_par = 0;
   bool ok = true;
-  for (int tile = (int)cluster_id_x(); ok && tile < total; tile += (int)cluster_count_x()) {
+  bool waited = !p.early_shared;
+  for (int tile = (int)cluster_id_x(); ok && pair_tile_exists(c, tile, p.status); tile += (int)cluster_count_x()) {
     const PairTile t = pair_tile(c, p, tile);
+    if (t.cls == 0 && !waited) {
+      pdl_wait();   // the permuted token rows come from the preceding grid
+      waited = true;
+    }
     const int w_row = (t.cls == 0 ? t.g * p.w_step[0] : 0) + t.fb * PAIR_M + int(rank) * PM;
     const int x_row = t.row_start + t.tb * PN + int(rank) * (t.n_mma / 2);
-    const int nk = p.K[t.cls] / BK;
-    for (int kb = 0; kb < nk; ++kb) {
+    const int nks = (p.K[t.cls] / BK + KB_STAGE - 1) / KB_STAGE;   // stages of this tile
+    const bool small = t.n_mma / 2 <= XSMALL;
+    const CUtensorMap* xmap = small ? &p.tmXs[t.cls] : &p.tmX[t.cls];
+    // both CTAs' full boxes (a k-block past K reads as zeros and still counts)
+    const uint32_t bytes = 2u * uint32_t(A_BYTES + KB_STAGE * (small ? XS_KB_BYTES : B_KB_BYTES));
+    for (int ks = 0; ks < nks; ++ks) {
       if (!pair_wait(&c->empty[stage], phase ^ 1u, c, peer_abort, p.status)) {
         ok = false;
         break;
       }
       uint8_t* sa = stages + stage * STAGE_BYTES;
-      if (rank == 0) mbar_arrive_expect_tx(&c->full[stage], 2u * STAGE_BYTES);
+      if (rank == 0) mbar_arrive_expect_tx(&c->full[stage], bytes);
       const uint32_t fb = map_to_rank(smem_u32(&c->full[stage]), 0);   // rank 0's barrier
-      const int kc = kb * BK;
-      tma_load_2d_pair(sa, &p.tmW[t.cls], fb, kc, w_row);
-      tma_load_2d_pair(sa + A_BYTES, &p.tmX[t.cls], fb, kc, x_row);
+      tma_load_3d_pair(sa, &p.tmW[t.cls], fb, w_row, ks * KB_STAGE);
+      tma_load_3d_pair(sa + A_BYTES, xmap, fb, x_row, ks * KB_STAGE);
       issued |= 1u << stage;
       issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
       if (++stage == STAGES) {
@@ -239,21 +284,22 @@ __device__ void pair_producer(PairCtrl* c, const PairParams& p, uint8_t* stages,
     if (issued & (1u << s)) pair_wait(&c->empty[s], (issued_par >> s) & 1u, c, peer_abort, p.status);
 }
 
-__device__ void pair_mma(PairCtrl* c, const PairParams& p, uint8_t* stages, uint32_t tmem, int total,
-                         uint32_t peer_abort) {
+__device__ void pair_mma(PairCtrl* c, const PairParams& p, uint8_t* stages, uint32_t tmem, uint32_t peer_abort) {
   int stage = 0;
   uint32_t phase = 0;
   int ctr = 0;
   bool ok = true;
-  for (int tile = (int)cluster_id_x(); ok && tile < total; tile += (int)cluster_count_x(), ++ctr) {
+  for (int tile = (int)cluster_id_x(); ok && pair_tile_exists(c, tile, p.status);
+       tile += (int)cluster_count_x(), ++ctr) {
     const PairTile t = pair_tile(c, p, tile);
     const uint32_t idesc = idesc_bf16_f32(PAIR_M, t.n_mma);
     const int acc = ctr & 1;
     if (!pair_wait(&c->tempty[acc], (uint32_t(ctr >> 1) & 1u) ^ 1u, c, peer_abort, p.status, true)) break;
     tc_fence_after();
     const uint32_t d_tmem = tmem + uint32_t(acc) * ACC_STRIDE;
-    const int nk = p.K[t.cls] / BK;
-    for (int kb = 0; kb < nk; ++kb) {
+    const int nks = (p.K[t.cls] / BK + KB_STAGE - 1) / KB_STAGE;
+    const uint32_t b_kb = t.n_mma / 2 <= XSMALL ? XS_KB_BYTES : B_KB_BYTES;
+    for (int ks = 0; ks < nks; ++ks) {
       if (!pair_wait(&c->full[stage], phase, c, peer_abort, p.status)) {
         ok = false;
         break;
@@ -262,9 +308,11 @@ __device__ void pair_mma(PairCtrl* c, const PairParams& p, uint8_t* stages, uint
       const uint32_t a0 = smem_u32(stages + stage * STAGE_BYTES);
       const uint32_t b0 = a0 + A_BYTES;
 #pragma unroll
-      for (int kk = 0; kk < BK / 16; ++kk)
-        mma_bf16_pair(d_tmem, sw128_kmajor_desc(a0 + kk * 32), sw128_kmajor_desc(b0 + kk * 32), idesc,
-                      (kb | kk) != 0 ? 1u : 0u);
+      for (int j = 0; j < KB_STAGE; ++j)
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk)
+          mma_bf16_pair(d_tmem, sw128_kmajor_desc(a0 + j * A_KB_BYTES + kk * 32),
+                        sw128_kmajor_desc(b0 + j * b_kb + kk * 32), idesc, (ks | j | kk) != 0 ? 1u : 0u);
       mma_commit_pair(&c->empty[stage], 0x3);
       if (++stage == STAGES) {
         stage = 0;
@@ -290,11 +338,14 @@ __device__ __forceinline__ bool pair_warp_wait(uint64_t* bar, uint32_t parity, P
 }
 
 template <int EPI>
-__device__ void pair_epilogue(PairCtrl* c, const PairParams& p, uint32_t tmem, int total, int warp, int lane,
-                              uint32_t rank, uint32_t peer_abort) {
+__device__ void pair_epilogue(PairCtrl* c, const PairParams& p, uint32_t tmem, int warp, int lane, uint32_t rank,
+                              uint32_t peer_abort) {
   const int q = warp & 3;   // the tensor-memory lane quarter this warp may read
   int ctr = 0;
-  for (int tile = (int)cluster_id_x(); tile < total; tile += (int)cluster_count_x(), ++ctr) {
+  for (int tile = (int)cluster_id_x();; tile += (int)cluster_count_x(), ++ctr) {
+    int exists = 0;
+    if (lane == 0) exists = pair_tile_exists(c, tile, p.status) ? 1 : 0;
+    if (!__shfl_sync(0xffffffffu, exists, 0)) break;
     const PairTile t = pair_tile(c, p, tile);
     const int acc = ctr & 1;
     if (!pair_warp_wait(&c->tfull[acc], uint32_t(ctr >> 1) & 1u, c, peer_abort, p.status, lane)) break;
@@ -356,7 +407,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stages = base;
-  PairCtrl* c = reinterpret_cast<PairCtrl*>(base + size_t(STAGES) * STAGE_BYTES + GUARD_BYTES);
+  PairCtrl* c = reinterpret_cast<PairCtrl*>(base + size_t(STAGES) * STAGE_BYTES);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
   const uint32_t peer_abort = map_to_rank(smem_u32(&c->abort), rank ^ 1u);
@@ -372,32 +423,44 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     }
     mbar_init(&c->drain, 1);
     c->abort = 0;
+    c->routed_ready = 0;
+    c->routed_tiles = 0;
+    c->shared_tiles = p.shared_rows > 0 ? cdiv(p.shared_rows, PN) * cdiv(p.M[1], PAIR_M) : 0;
     fence_mbar_init();
+    pdl_launch_dependents();
   }
   if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&p.tmW[0]);
-    tma_prefetch_desc(&p.tmX[0]);
-    tma_prefetch_desc(&p.tmW[1]);
-    tma_prefetch_desc(&p.tmX[1]);
+    for (int i = 0; i < 2; ++i) {
+      tma_prefetch_desc(&p.tmW[i]);
+      tma_prefetch_desc(&p.tmX[i]);
+      tma_prefetch_desc(&p.tmXs[i]);
+    }
   }
   if (warp == 1) {
     tmem_alloc_pair(&c->tmem_base, TMEM_COLS);
     tmem_relinquish_pair();
   }
-  if (warp == 2) pair_schedule(c, p, lane);
   tc_fence_before();
-  // both CTAs' barriers, tensor memory and tile tables are ready
+  // both CTAs' barriers and tensor memory are ready
   cluster_sync_all();
   tc_fence_after();
+  // Without early shared tiles every input comes from the preceding grid.
+  if (!p.early_shared) pdl_wait();
 
   const uint32_t tmem = c->tmem_base;
-  const int total = c->tile_start[c->ngroups];
   if (warp == 0) {
-    if (lane == 0) pair_producer(c, p, stages, total, rank, peer_abort);
+    if (lane == 0) pair_producer(c, p, stages, rank, peer_abort);
   } else if (warp == 1) {
-    if (lane == 0 && rank == 0) pair_mma(c, p, stages, tmem, total, peer_abort);
+    if (lane == 0 && rank == 0) pair_mma(c, p, stages, tmem, peer_abort);
+  } else if (warp < 2 + EPI_WARPS) {
+    pair_epilogue<EPI>(c, p, tmem, warp, lane, rank, peer_abort);
   } else {
-    pair_epilogue<EPI>(c, p, tmem, total, warp, lane, rank, peer_abort);
+    // scheduler warp: the routed table needs the dispatch offsets
+    if (p.early_shared) pdl_wait();
+    pair_schedule(c, p, lane);
+    __syncwarp();
+    __threadfence_block();
+    if (lane == 0) *reinterpret_cast<volatile int*>(&c->routed_ready) = 1;
   }
   tc_fence_before();
   // neither CTA leaves while the other may still signal its barriers
@@ -408,19 +471,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   }
 }
 
-// bf16 [rows, cols] row-major, box = 64 columns x 128 rows, 128-byte swizzle.
-bool encode_pair_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols) {
-  auto enc = tensor_map_encoder();
-  if (enc == nullptr || rows <= 0 || cols <= 0) return false;
-  cuuint64_t dims[2] = {cuuint64_t(cols), cuuint64_t(rows)};
-  cuuint64_t strides[1] = {cuuint64_t(cols) * 2};
-  cuuint32_t box[2] = {64u, 128u};
-  cuuint32_t es[2] = {1u, 1u};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
 
 template <int EPI>
 cudaError_t launch_pair_epi(const PairParams& p, long long max_tiles, cudaStream_t stream) {
@@ -448,14 +498,14 @@ cudaError_t launch_pair_epi(const PairParams& p, long long max_tiles, cudaStream
     max_clusters = n;
   }
   const long long pairs = max_tiles < max_clusters ? max_tiles : max_clusters;
-  pair_gemm_kernel<EPI><<<int(2 * pairs), THREADS, kPairSmem, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(pair_gemm_kernel<EPI>, dim3(int(2 * pairs)), dim3(THREADS), kPairSmem, stream, p);
 }
 
 }  // namespace
 
 cudaError_t launch_pair_gemm(int epi, const PairClass& c0, const PairClass* c1, const int32_t* offsets, int num_routed,
-                             int shared_rows, int* status, long long max_tiles, cudaStream_t stream, int* launches) {
+                             int shared_rows, int* status, long long max_tiles, cudaStream_t stream, int* launches,
+                             bool early_shared) {
   if (max_tiles <= 0) return cudaSuccess;
   PairParams p;
   memset(&p, 0, sizeof(p));
@@ -463,8 +513,9 @@ cudaError_t launch_pair_gemm(int epi, const PairClass& c0, const PairClass* c1, 
   for (int i = 0; i < 2; ++i) {
     const PairClass& g = *cls[i];
     if (g.K % BK != 0) return cudaErrorInvalidValue;
-    if (!encode_pair_map(&p.tmW[i], g.W, g.w_rows, g.K)) return cudaErrorInvalidValue;
-    if (!encode_pair_map(&p.tmX[i], g.X, g.x_rows, g.K)) return cudaErrorInvalidValue;
+    if (!encode_bf16_map(&p.tmW[i], g.W, g.w_rows, g.K, PM, KB_STAGE)) return cudaErrorInvalidValue;
+    if (!encode_bf16_map(&p.tmX[i], g.X, g.x_rows, g.K, XB, KB_STAGE)) return cudaErrorInvalidValue;
+    if (!encode_bf16_map(&p.tmXs[i], g.X, g.x_rows, g.K, XSMALL, KB_STAGE)) return cudaErrorInvalidValue;
     p.out[i] = g.out;
     p.ld_out[i] = g.ld_out;
     p.out_rows[i] = g.out_rows;
@@ -476,7 +527,8 @@ cudaError_t launch_pair_gemm(int epi, const PairClass& c0, const PairClass* c1, 
   p.num_routed = num_routed;
   p.shared_rows = c1 != nullptr ? shared_rows : 0;
   p.status = status;
-  if (num_routed + 1 > MAX_GROUPS) return cudaErrorInvalidValue;
+  p.early_shared = early_shared ? 1 : 0;
+  if (num_routed < 1 || num_routed + 1 > MAX_GROUPS) return cudaErrorInvalidValue;
   cudaError_t e = epi == EPI_PAIR_SWIGLU ? launch_pair_epi<EPI_PAIR_SWIGLU>(p, max_tiles, stream)
                                          : launch_pair_epi<EPI_PAIR_F32>(p, max_tiles, stream);
   if (e == cudaSuccess && launches) ++*launches;

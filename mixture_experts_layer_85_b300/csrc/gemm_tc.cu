@@ -22,6 +22,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <mutex>
+
 #include "internal.h"
 #include "tc_ptx.cuh"
 
@@ -380,9 +382,12 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const __grid_c
     tmem_relinquish();
   }
   if (warp == 2) build_schedule<EPI>(c, p, lane);
+  if (threadIdx.x == 0) pdl_launch_dependents();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // the inputs (tokens) come from earlier work in the stream
+  pdl_wait();
 
   const uint32_t tmem = c->tmem_base;
   const int total = c->tile_start[c->ngroups];
@@ -418,21 +423,73 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
+// bf16 [rows, cols] row-major, 128-byte swizzle.  box_kblocks = 1: a 2-D map
+// with 64-column x box_rows boxes.  box_kblocks > 1: a 3-D view
+// (64 columns, rows, cols / 64 k-blocks) whose box covers box_kblocks
+// consecutive k-blocks of box_rows rows, stored k-block after k-block.
+// Encoded maps are kept in a small table keyed by their arguments, so repeated
+// layer calls on the same buffers skip the driver call (a host-side cost that
+// dominates decode-sized steps).
+bool encode_bf16_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, uint32_t box_rows,
+                     uint32_t box_kblocks) {
+  struct Entry {
+    const void* ptr;
+    int64_t rows, cols;
+    uint32_t box, kbs;
+    CUtensorMap map;
+  };
+  constexpr int kEntries = 64;
+  static Entry table[kEntries];
+  static int filled = 0, next = 0;
+  static std::mutex mu;
+  if (rows <= 0 || cols <= 0) return false;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < filled; ++i) {
+      const Entry& e = table[i];
+      if (e.ptr == ptr && e.rows == rows && e.cols == cols && e.box == box_rows && e.kbs == box_kblocks) {
+        *m = e.map;
+        return true;
+      }
+    }
+  }
+  auto enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  CUresult r;
+  if (box_kblocks <= 1) {
+    cuuint64_t dims[2] = {cuuint64_t(cols), cuuint64_t(rows)};
+    cuuint64_t strides[1] = {cuuint64_t(cols) * 2};
+    cuuint32_t box[2] = {64u, box_rows};
+    cuuint32_t es[2] = {1u, 1u};
+    r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else {
+    if (cols % 64 != 0) return false;
+    cuuint64_t dims[3] = {64u, cuuint64_t(rows), cuuint64_t(cols / 64)};
+    cuuint64_t strides[2] = {cuuint64_t(cols) * 2, 128u};
+    cuuint32_t box[3] = {64u, box_rows, box_kblocks};
+    cuuint32_t es[3] = {1u, 1u, 1u};
+    r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  }
+  if (r != CUDA_SUCCESS) return false;
+  std::lock_guard<std::mutex> lock(mu);
+  Entry& e = table[next];
+  e.ptr = ptr;
+  e.rows = rows;
+  e.cols = cols;
+  e.box = box_rows;
+  e.kbs = box_kblocks;
+  e.map = *m;
+  next = (next + 1) % kEntries;
+  if (filled < kEntries) ++filled;
+  return true;
+}
+
 namespace {
 
-// bf16 [rows, cols] row-major, box = 64 columns x box_rows rows, 128-byte swizzle.
-bool encode_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, uint32_t box_rows) {
-  auto enc = tensor_map_encoder();
-  if (enc == nullptr || rows <= 0 || cols <= 0) return false;
-  cuuint64_t dims[2] = {cuuint64_t(cols), cuuint64_t(rows)};
-  cuuint64_t strides[1] = {cuuint64_t(cols) * 2};
-  cuuint32_t box[2] = {64u, box_rows};
-  cuuint32_t es[2] = {1u, 1u};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
 
 template <int EPI>
 cudaError_t launch_epi(const Params& p, int grid, cudaStream_t stream) {
@@ -443,8 +500,7 @@ cudaError_t launch_epi(const Params& p, int grid, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  grouped_gemm_kernel<EPI><<<grid, THREADS, kSmemBytes, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(grouped_gemm_kernel<EPI>, dim3(grid), dim3(THREADS), kSmemBytes, stream, p);
 }
 
 }  // namespace
@@ -470,8 +526,8 @@ cudaError_t launch_grouped_gemm(int epi, const GemmClass& c0, const GemmClass* c
   const GemmClass* cls[2] = {&c0, c1 != nullptr ? c1 : &c0};
   for (int i = 0; i < 2; ++i) {
     const GemmClass& g = *cls[i];
-    if (!encode_map(&p.tmA[i], g.A, g.a_rows, g.a_cols, BM)) return cudaErrorInvalidValue;
-    if (!encode_map(&p.tmB[i], g.B, g.b_rows, g.b_cols, uint32_t(g.mma_n))) return cudaErrorInvalidValue;
+    if (!encode_bf16_map(&p.tmA[i], g.A, g.a_rows, g.a_cols, BM, 1)) return cudaErrorInvalidValue;
+    if (!encode_bf16_map(&p.tmB[i], g.B, g.b_rows, g.b_cols, uint32_t(g.mma_n), 1)) return cudaErrorInvalidValue;
     p.out[i] = g.out;
     p.ld_out[i] = g.ld_out;
     p.out_rows[i] = g.out_rows;

@@ -10,6 +10,25 @@
 
 namespace moe {
 
+// Launch with programmatic stream serialization: the kernel may start while
+// its predecessor in the stream is still running (it calls pdl_wait() before
+// depending on it).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // ---------------------------------------------------------------- grouped GEMM
 // One operand class of the grouped GEMM: A [a_rows, K'] and B [b_rows, K] bf16,
 // both K-major (row-major with K contiguous).  Class 0 holds either the routed
@@ -39,6 +58,12 @@ int num_sms();
 // cuTensorMapEncodeTiled from the driver (nullptr when unavailable).
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 
+// bf16 tensor map of a row-major [rows, cols] buffer, 128-byte swizzle, boxes
+// of 64 columns x box_rows rows x box_kblocks consecutive 64-column k-blocks
+// (box_kblocks = 1: a plain 2-D map).  Cached by argument.
+bool encode_bf16_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, uint32_t box_rows,
+                     uint32_t box_kblocks);
+
 // Records the next armed profiling event on `s` (no-op when disarmed).
 void profile_mark(cudaStream_t s);
 
@@ -66,8 +91,11 @@ struct PairClass {
 
 enum PairEpi : int { EPI_PAIR_SWIGLU = 0, EPI_PAIR_F32 = 1 };
 
+// early_shared: the shared expert's tiles (class 1) run first and may start
+// before the preceding grid in the stream completes; routed tiles wait for it.
 cudaError_t launch_pair_gemm(int epi, const PairClass& c0, const PairClass* c1, const int32_t* offsets, int num_routed,
-                             int shared_rows, int* status, long long max_tiles, cudaStream_t stream, int* launches);
+                             int shared_rows, int* status, long long max_tiles, cudaStream_t stream, int* launches,
+                             bool early_shared);
 
 // ---------------------------------------------------------------------- router
 cudaError_t launch_gate_split(const float* wg, int E, int d, void* wsplit, cudaStream_t s, int* launches);
@@ -98,6 +126,10 @@ cudaError_t launch_swiglu_simt_f32(const moe_config& c, const float* x_perm, con
 cudaError_t launch_combine(const moe_config& c, const void* y_perm, const void* y_shared,
                            const int32_t* tok2row, const float* w, void* out, int* status, cudaStream_t s,
                            int* launches);
+
+// ----------------------------------------------------------- load balancing
+cudaError_t launch_balance_update(const moe_config& c, const int32_t* counts, float* bias, float gamma, float* stats,
+                                  int* status, cudaStream_t s, int* launches);
 
 // Packed expert blob layout (byte offsets, each 256-byte aligned).
 struct PackedLayout {

@@ -13,7 +13,8 @@
 //               block: offsets[e] = exclusive prefix sum of counts
 //   3. scatter  per chunk: rank of a token inside its expert = popcount of the
 //               mask bits of earlier tokens -> row2tok / tok2row
-//   4. gather   x rows -> x_perm rows, 16-byte vectors, grid over all SMs
+//   4. gather   x rows -> x_perm rows: each token's row is read once and
+//               written to its k destination rows (16-byte vectors)
 //
 // Decode-sized batches (T <= SMALL_T) run steps 1-3 in one block instead
 // (permute_small_kernel: the same masks and ranks over 1024-token chunks taken
@@ -48,6 +49,8 @@ __device__ __forceinline__ void build_masks(uint32_t (*mask)[WORDS], const int32
 
 __global__ void __launch_bounds__(CHUNK) permute_count_kernel(const int32_t* __restrict__ idx, int T, int E, int k,
                                                               int32_t* __restrict__ chunk_counts, int* status) {
+  pdl_launch_dependents();
+  pdl_wait();
   __shared__ uint32_t mask[MAX_E][WORDS];
   build_masks(mask, idx, T, E, k, blockIdx.x, status);
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
@@ -87,6 +90,8 @@ __global__ void __launch_bounds__(CHUNK) permute_chunk_scan_kernel(const int32_t
                                                                    int nchunks, int E,
                                                                    int32_t* __restrict__ chunk_base,
                                                                    int32_t* __restrict__ counts) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int e = blockIdx.x;
   int carry = 0;
   for (int c0 = 0; c0 < nchunks; c0 += blockDim.x) {
@@ -103,6 +108,8 @@ __global__ void __launch_bounds__(CHUNK) permute_chunk_scan_kernel(const int32_t
 // One block: offsets = exclusive prefix sum of counts over experts (E <= 256).
 __global__ void __launch_bounds__(256) permute_offsets_kernel(const int32_t* __restrict__ counts, int E,
                                                               int32_t* __restrict__ offsets) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int e = threadIdx.x;
   int tot;
   const int ex = block_exclusive_scan(e < E ? counts[e] : 0, &tot);
@@ -115,6 +122,8 @@ __global__ void __launch_bounds__(CHUNK) permute_scatter_kernel(const int32_t* _
                                                                 const int32_t* __restrict__ offsets,
                                                                 int32_t* __restrict__ row2tok,
                                                                 int32_t* __restrict__ tok2row, int* status) {
+  pdl_launch_dependents();
+  pdl_wait();
   __shared__ uint32_t mask[MAX_E][WORDS];
   build_masks(mask, idx, T, E, k, blockIdx.x, nullptr);
   const int t = blockIdx.x * CHUNK + threadIdx.x;
@@ -151,6 +160,8 @@ __global__ void __launch_bounds__(SMALL_BLOCK) permute_small_kernel(const int32_
                                                                     int32_t* __restrict__ offsets,
                                                                     int32_t* __restrict__ row2tok,
                                                                     int32_t* __restrict__ tok2row, int* status) {
+  pdl_launch_dependents();
+  pdl_wait();
   __shared__ uint32_t mask[MAX_E][SMALL_WORDS];
   __shared__ int base[MAX_E];
   const int tid = threadIdx.x;
@@ -220,29 +231,43 @@ __global__ void __launch_bounds__(SMALL_BLOCK) permute_small_kernel(const int32_
   }
 }
 
-// x_perm[r] = x[row2tok[r]]; one warp per row, 16-byte vectors.
-__global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ row2tok,
-                                                          long long R, int T, int vec_per_row, uint4* __restrict__ x_perm,
-                                                          int* status) {
+// x_perm[tok2row[t][j]] = x[t] for every slot j: one warp per token reads the
+// row once (chunks of 8 vectors per lane) and stores it k times, so x streams
+// from memory once and the k copies are plain writes.
+constexpr int GATHER_CHUNK = 8;   // 16-byte vectors per lane per chunk
+__global__ void __launch_bounds__(256) gather_tokens_kernel(const uint4* __restrict__ x,
+                                                            const int32_t* __restrict__ tok2row, int T, int k,
+                                                            long long R, int vec_per_row, uint4* __restrict__ x_perm,
+                                                            int* status) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
-  for (long long r = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < R; r += warps) {
-    const int t = row2tok[r];
-    if (t < 0 || t >= T) {
-      if (lane == 0) flag_status(status, DEV_BAD_ROW);
-      continue;
+  for (long long t = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < T; t += warps) {
+    const int32_t* rows = tok2row + t * k;
+    const uint4* src = x + t * vec_per_row;
+    for (int v0 = 0; v0 < vec_per_row; v0 += 32 * GATHER_CHUNK) {
+      uint4 buf[GATHER_CHUNK];
+#pragma unroll
+      for (int i = 0; i < GATHER_CHUNK; ++i) {
+        const int v = v0 + i * 32 + lane;
+        if (v < vec_per_row) buf[i] = src[v];
+      }
+      for (int j = 0; j < k; ++j) {
+        const long long r = rows[j];   // warp-uniform, cached after the first chunk
+        if (r < 0) continue;           // an expert index the dispatch already flagged
+        if (r >= R) {
+          if (lane == 0 && v0 == 0) flag_status(status, DEV_BAD_ROW);
+          continue;
+        }
+        uint4* dst = x_perm + r * vec_per_row;
+#pragma unroll
+        for (int i = 0; i < GATHER_CHUNK; ++i) {
+          const int v = v0 + i * 32 + lane;
+          if (v < vec_per_row) dst[v] = buf[i];
+        }
+      }
     }
-    const uint4* src = x + (long long)t * vec_per_row;
-    uint4* dst = x_perm + r * vec_per_row;
-    int v = lane;
-    for (; v + 96 < vec_per_row; v += 128) {
-      const uint4 a = src[v], b = src[v + 32], c = src[v + 64], d = src[v + 96];
-      dst[v] = a;
-      dst[v + 32] = b;
-      dst[v + 64] = c;
-      dst[v + 96] = d;
-    }
-    for (; v < vec_per_row; v += 32) dst[v] = src[v];
   }
 }
 
@@ -257,26 +282,33 @@ cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* id
                            int* launches) {
   const int nch = permute_chunks(c.T);
   if (c.T <= SMALL_T) {
-    permute_small_kernel<<<1, SMALL_BLOCK, 0, s>>>(idx, c.T, c.E, c.k, counts, offsets, row2tok, tok2row, status);
+    cudaError_t e = launch_pdl(permute_small_kernel, dim3(1), dim3(SMALL_BLOCK), 0, s, idx, c.T, c.E, c.k, counts,
+                               offsets, row2tok, tok2row, status);
     if (launches) *launches += 1;
+    if (e != cudaSuccess) return e;
   } else {
-    permute_count_kernel<<<nch, CHUNK, 0, s>>>(idx, c.T, c.E, c.k, chunk_counts, status);
-    permute_chunk_scan_kernel<<<c.E, CHUNK, 0, s>>>(chunk_counts, nch, c.E, chunk_base, counts);
-    permute_offsets_kernel<<<1, 256, 0, s>>>(counts, c.E, offsets);
-    permute_scatter_kernel<<<nch, CHUNK, 0, s>>>(idx, c.T, c.E, c.k, chunk_base, offsets, row2tok, tok2row, status);
+    cudaError_t e = launch_pdl(permute_count_kernel, dim3(nch), dim3(CHUNK), 0, s, idx, c.T, c.E, c.k, chunk_counts,
+                               status);
+    if (e == cudaSuccess)
+      e = launch_pdl(permute_chunk_scan_kernel, dim3(c.E), dim3(CHUNK), 0, s, chunk_counts, nch, c.E, chunk_base,
+                     counts);
+    if (e == cudaSuccess) e = launch_pdl(permute_offsets_kernel, dim3(1), dim3(256), 0, s, counts, c.E, offsets);
+    if (e == cudaSuccess)
+      e = launch_pdl(permute_scatter_kernel, dim3(nch), dim3(CHUNK), 0, s, idx, c.T, c.E, c.k, chunk_base, offsets,
+                     row2tok, tok2row, status);
     if (launches) *launches += 4;
+    if (e != cudaSuccess) return e;
   }
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess || x == nullptr || x_perm == nullptr) return e;
+  if (x == nullptr || x_perm == nullptr) return cudaSuccess;
   const long long R = (long long)c.T * c.k;
   const int vec = int((size_t)c.d * dtype_bytes(c.act_dtype) / 16);
-  long long blocks = (R + 7) / 8;
+  long long blocks = (c.T + 7) / 8;
   const long long cap = 8LL * num_sms();
   if (blocks > cap) blocks = cap;
-  gather_rows_kernel<<<(int)blocks, 256, 0, s>>>(static_cast<const uint4*>(x), row2tok, R, c.T, vec,
-                                                  static_cast<uint4*>(x_perm), status);
+  cudaError_t e = launch_pdl(gather_tokens_kernel, dim3((int)blocks), dim3(256), 0, s, static_cast<const uint4*>(x),
+                             tok2row, c.T, c.k, R, vec, static_cast<uint4*>(x_perm), status);
   if (launches) ++*launches;
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace moe

@@ -18,6 +18,8 @@ What it computes (one token u_t at a time, all in float64 unless stated):
      routed_scaling_factor
   7. out_t = sum_j g_j * FFN_{idx_j}(u_t) + FFN_shared(u_t), FFN = SwiGLU,
      no residual term.
+  8. after a step (training-time load balancing): the selection bias of
+     every expert moves by gamma toward balance, and the load statistics.
 
 Sources (page title, section):
   * "DeepSeek-V2" walkthrough (xingfushuangcheng.com): the DeepSeekMoE output
@@ -32,7 +34,11 @@ Sources (page title, section):
   * "【Deepseek基础篇】--v3基本架构" (nxbn.cn), section 1.2: a per-expert bias is
     added to the affinity only to pick the top-K, gate values come from the
     unbiased affinity; node-limited routing picks nodes by the sum of the
-    highest affinities on each node; no token is dropped.
+    highest affinities on each node; no token is dropped; after each step the
+    bias of an overloaded expert is lowered by the bias update speed gamma and
+    that of an underloaded expert raised by gamma.
+  * Tencent Cloud page, the balance-loss listing: load = per-expert counts of
+    the top-k choices normalised to sum 1, and its standard deviation.
 
 Readings where the pages are silent or garbled (all listed in the design doc):
   * Decision precision.  The ``MoEGate`` listing holds logits and scores in
@@ -45,6 +51,10 @@ Readings where the pages are silent or garbled (all listed in the design doc):
     descending order.  m = k / topk_group in the V3-shaped workloads.
   * Experts outside the kept groups are excluded outright (not zero-filled), so
     a negative biased score can never pull in an expert from a dropped group.
+  * Overloaded / underloaded (step 8): more / fewer assignments than the mean
+    T*k/E, decided exactly on integers; an expert at exactly the mean keeps its
+    bias.  The bias is float32 and moves by one float32 addition.  The load
+    standard deviation is the unbiased one (the listing's torch .std()).
   * A token is a near tie when the k-th and (k+1)-th eligible selection scores
     (or the topk_group-th and next group scores) differ by less than 1e-5 times
     the largest |score| of that token; its expert set may legitimately differ
@@ -350,3 +360,39 @@ def is_valid_selection(idx_row: Sequence[int], sel32_row: np.ndarray, cfg: Oracl
     others = np.where(elig, sel, -np.inf)
     others[picked] = -np.inf
     return bool(others.max() <= worst_picked + tol)
+
+
+# ------------------------------------------------------------ load balancing
+
+def balance_update(counts, bias32, gamma: float):
+    """Step 8: the bias after one auxiliary-loss-free balancing step and the
+    load statistics.
+
+    "v3基本架构" page, section 1.2: at the end of a step an overloaded expert's
+    bias is lowered by gamma and an underloaded expert's bias raised by gamma.
+    Tencent Cloud balance-loss listing: load = counts / sum(counts) and its
+    standard deviation.
+
+    Returns (new bias as float32 [E], stats float64 [3]) with stats =
+    (unbiased std of the load fractions, max count / mean count,
+    min count / mean count)."""
+    c = np.asarray(counts, dtype=np.int64)
+    E = c.size
+    total = int(c.sum())
+    b = np.asarray(bias32, dtype=np.float32)
+    g = np.float32(gamma)
+    new = b.copy()
+    for e in range(E):
+        if c[e] * E > total:        # took more than the mean T*k/E
+            new[e] = np.float32(b[e] - g)
+        elif c[e] * E < total:      # took fewer
+            new[e] = np.float32(b[e] + g)
+    stats = np.zeros(3)
+    if total > 0:
+        load = c.astype(np.float64) / total
+        if E > 1:
+            stats[0] = np.sqrt(((load - load.mean()) ** 2).sum() / (E - 1))
+        mean = total / E
+        stats[1] = c.max() / mean
+        stats[2] = c.min() / mean
+    return new, stats

@@ -9,7 +9,9 @@ Every check raises AssertionError when the oracle disagrees with:
     E=1/k=1 -> plain SwiGLU sum, k=E -> the dense einsum gate fusion of the
     intelliparadigm.com page (section 3.3.3), k=1 -> the Top-1 MoE of the
     Tencent Cloud page, greedy == torch.topk on float64 scores;
-  * symmetries: expert relabelling, token independence, linearity in W2.
+  * symmetries: expert relabelling, token independence, linearity in W2;
+  * the balancing step (bias +/- gamma, load statistics) against hand-worked
+    counts, closed forms and exact rational rounding bounds.
 
 The independent pieces (softmax via scipy, SwiGLU via torch.nn.functional)
 never call the oracle's own helpers.  ``tests/test_oracle_mutations.py``
@@ -312,6 +314,52 @@ def pin_combine(o=orc):
     assert np.allclose(o.combine(y[perm], ys, inv[tok2row], g), want.numpy(), rtol=1e-13, atol=1e-14)
 
 
+def pin_balance_update(o=orc):
+    """V3 page section 1.2: overloaded experts lose gamma, underloaded ones
+    gain gamma, an expert at the mean keeps its bias; the Tencent Cloud
+    listing's load = counts / sum and its (unbiased) std."""
+    g = np.float32(0.001)
+    # hand-worked: counts 3,1,2,2 (mean 2): signs -,+,0,0; loads .375,.125,.25,.25,
+    # squared deviations 2 * (1/8)^2 = 1/32 over E-1 = 3 -> std = sqrt(1/96)
+    b0 = np.array([0.0, 0.0, 0.5, -0.25], np.float32)
+    nb, st = o.balance_update([3, 1, 2, 2], b0, g)
+    assert nb.dtype == np.float32
+    assert nb[2] == b0[2] and nb[3] == b0[3]
+    assert nb[0] < b0[0] and nb[1] > b0[1]
+    assert abs(st[0] - (1.0 / 96.0) ** 0.5) < 1e-15 and st[1] == 1.5 and st[2] == 0.5
+    # uniform load: nothing moves, std 0, max = min = mean
+    nb, st = o.balance_update([7] * 16, np.linspace(-1, 1, 16).astype(np.float32), g)
+    assert np.array_equal(nb, np.linspace(-1, 1, 16).astype(np.float32))
+    assert st[0] == 0.0 and st[1] == 1.0 and st[2] == 1.0
+    # two experts a > b: std of (a, b)/(a+b) is |a-b| / (a+b) / sqrt(2)
+    nb, st = o.balance_update([9, 3], np.zeros(2, np.float32), g)
+    assert abs(st[0] - 6 / 12 / 2 ** 0.5) < 1e-15
+    assert nb[0] == -g and nb[1] == g
+    # random counts: each moved bias is b +/- gamma correctly rounded to float32
+    r = _rng(21)
+    for _ in range(20):
+        E = int(r.integers(2, 257))
+        c = r.integers(0, 50, E)
+        b = (r.standard_normal(E) * 0.1).astype(np.float32)
+        nb, st = o.balance_update(c, b, g)
+        tot = int(c.sum())
+        for e in range(E):
+            want = Fraction(float(b[e]))
+            if c[e] * E > tot:
+                want -= Fraction(float(g))
+            elif c[e] * E < tot:
+                want += Fraction(float(g))
+            else:
+                assert nb[e] == b[e]
+                continue
+            got = Fraction(float(nb[e]))
+            ulp = Fraction(float(np.spacing(np.float32(abs(float(nb[e]))))))
+            assert abs(got - want) <= ulp / 2
+        if tot:
+            assert abs(st[1] - c.max() * E / tot) < 1e-12 and abs(st[2] - c.min() * E / tot) < 1e-12
+
+
 ALL_PINS = [pin_brute_force_selection, pin_greedy_is_torch_topk, pin_invariants,
             pin_bias_only_steers_selection, pin_zero_gates_give_shared, pin_group1_is_greedy,
-            pin_single_expert, pin_dense_einsum, pin_top1, pin_permutation, pin_symmetries, pin_combine]
+            pin_single_expert, pin_dense_einsum, pin_top1, pin_permutation, pin_symmetries, pin_combine,
+            pin_balance_update]

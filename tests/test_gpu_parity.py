@@ -284,3 +284,36 @@ def test_out_of_range_expert_is_flagged_not_faulted():
     # the context is still fine
     torch.cuda.synchronize()
     assert float(torch.ones(4, device="cuda").sum()) == 4.0
+
+
+# ------------------------------------------------------------ load balancing
+
+@pytest.mark.parametrize("case", ["forward_counts", "synthetic"])
+def test_balance_update(case):
+    """moe_balance_update == the oracle's balancing step: the float32 bias bit
+    for bit, the load statistics within 1e-6 relative."""
+    gamma = 0.001
+    if case == "forward_counts":
+        wl = SMALL["v3_small_t333"]
+        li = inputs.make_inputs(wl, "cuda")
+        _, _, _, _, counts = run_layer(wl, li)
+        bias0 = li.bias.float().clone()
+    else:
+        wl = inputs.small_workload(W["v3_prefill_t16384"], name="bal", T=96, d=512, E=64, I=128)
+        c = torch.randint(0, 30, (wl.E,), generator=torch.Generator().manual_seed(3), dtype=torch.int32)
+        c[5] = int(c.sum() - c[5]) // (wl.E - 1)          # some experts at or near the mean
+        tot = int(c.sum())
+        c[7] = tot // wl.E if tot % wl.E == 0 else c[7]
+        counts = c.cuda()
+        bias0 = (torch.randn(wl.E, generator=torch.Generator().manual_seed(4)) * 0.1).float().cuda()
+    cfg = _lib.make_config(wl)
+    bias = bias0.clone()
+    stats = torch.zeros(4, dtype=torch.float32, device="cuda")
+    status = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    _lib.moe_balance_update(cfg, counts, bias, gamma, stats, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    want_b, want_s = orc.balance_update(_np(counts), _np(bias0), gamma)
+    assert np.array_equal(_np(bias), want_b)
+    got_s = _np(stats)[:3].astype(np.float64)
+    assert np.allclose(got_s, want_s, rtol=1e-6, atol=1e-9), (got_s, want_s)

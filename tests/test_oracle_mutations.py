@@ -15,6 +15,7 @@ _real_swiglu = orc.swiglu_ffn
 _real_experts_forward = orc.experts_forward
 _real_permutation = orc.permutation
 _real_combine = orc.combine
+_real_balance = orc.balance_update
 
 
 def _route_ties_high(logits, bias, cfg):
@@ -93,6 +94,28 @@ def _combine_slot_swap(y_rows, y_shared, tok2row, gates):
     return _real_combine(y_rows, y_shared, tok2row, gates[:, ::-1])
 
 
+def _balance_wrong_direction(counts, bias32, gamma):
+    return _real_balance(counts, bias32, -gamma)
+
+
+def _balance_biased_std(counts, bias32, gamma):
+    nb, st = _real_balance(counts, bias32, gamma)
+    E = len(counts)
+    st = st.copy()
+    st[0] *= ((E - 1) / E) ** 0.5
+    return nb, st
+
+
+def _balance_mean_counts_as_over(counts, bias32, gamma):
+    # an expert exactly at the mean treated as overloaded
+    c = np.asarray(counts, np.int64)
+    nb, st = _real_balance(counts, bias32, gamma)
+    at_mean = c * c.size == c.sum()
+    nb = nb.copy()
+    nb[at_mean] = (np.asarray(bias32, np.float32)[at_mean] - np.float32(gamma)).astype(np.float32)
+    return nb, st
+
+
 MUTANTS = [
     ("route", _route_ties_high, pins.pin_brute_force_selection),
     ("route", _route_biased_gates, pins.pin_bias_only_steers_selection),
@@ -106,6 +129,9 @@ MUTANTS = [
     ("experts_forward", _experts_with_residual, pins.pin_zero_gates_give_shared),
     ("permutation", _permutation_reversed, pins.pin_permutation),
     ("combine", _combine_slot_swap, pins.pin_combine),
+    ("balance_update", _balance_wrong_direction, pins.pin_balance_update),
+    ("balance_update", _balance_biased_std, pins.pin_balance_update),
+    ("balance_update", _balance_mean_counts_as_over, pins.pin_balance_update),
 ]
 
 

@@ -93,9 +93,9 @@ class ClockSampler:
     stop(t0, t1) keeps the samples whose timestamps fall in the host-time window
     [t0, t1] of the timed region (padded by one sampling interval)."""
 
-    FIELDS = ("timestamp,index,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,uuid,clocks.sm,clocks.max.sm,power.draw.instant,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,power.limit")
     INTERVAL_MS = 50
 
     def __init__(self):
@@ -142,7 +142,7 @@ class ClockSampler:
         rows = []
         for line in open(self.path):
             f = [x.strip() for x in line.split(",")]
-            if len(f) < 11:
+            if len(f) < 12:
                 continue
             if uuid and uuid not in f[2] and f[2].replace("GPU-", "") not in uuid:
                 continue
@@ -160,9 +160,11 @@ class ClockSampler:
         pw = [v for v in (self._num(r[4]) for r in rows) if v is not None]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in rows for i in range(4) if r[6 + i].lower().startswith("active")})
+        lim = [v for v in (self._num(r[10]) for r in rows) if v is not None]
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(rows), "power_w_max": max(pw) if pw else None,
-                "power_w_median": statistics.median(pw) if pw else None}
+                "reasons": reasons, "samples": len(rows), "power_w_instant_max": max(pw) if pw else None,
+                "power_w_instant_median": statistics.median(pw) if pw else None,
+                "power_limit_w": max(lim) if lim else None}
 
 
 def measured_peaks():

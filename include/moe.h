@@ -203,9 +203,11 @@ MOE_API uint64_t moe_launch_count(void);
  * the boundaries of its MOE_FORWARD_STAGES stages and once at the end, i.e.
  * MOE_FORWARD_STAGES + 1 events per call, taken from `events` in order until
  * `n_events` are used.  Stages: 0 router (gate GEMM + top-k), 1 permutation,
- * 2 GEMM1 with the SwiGLU epilogue, 3 GEMM2, 4 combine.  NULL disarms.
+ * 2 experts (GEMM1 with the SwiGLU epilogue and GEMM2, one launch on the
+ * tensor-core path), 3 combine.  NULL disarms.  The events split the
+ * kernels' launch overlap, so armed calls run slightly slower.
  * Not thread-safe; arm, run, disarm from one host thread. */
-#define MOE_FORWARD_STAGES 5
+#define MOE_FORWARD_STAGES 4
 MOE_API moe_status moe_profile_arm(void* const* events, int32_t n_events);
 
 /* Name of stage i of moe_forward ("router", "permute", ...), or NULL. */

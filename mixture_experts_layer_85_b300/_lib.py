@@ -31,7 +31,7 @@ EXPORTED = ["moe_workspace_size", "moe_packed_size", "moe_prepack_experts", "moe
             "moe_grouped_swiglu", "moe_combine", "moe_forward", "moe_get_device_status", "moe_status_string",
             "moe_launch_count", "moe_forward_kernel_count", "moe_profile_arm", "moe_forward_stage_name",
             "moe_permute_noalloc", "moe_balance_update"]
-MOE_FORWARD_STAGES = 5
+MOE_FORWARD_STAGES = 4
 
 
 class moe_config(ctypes.Structure):

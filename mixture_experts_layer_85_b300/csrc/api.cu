@@ -31,7 +31,7 @@ constexpr int kGatePromoteK = 256;   // K per fp32-promoted tensor-core partial 
 
 struct WsLayout {
   size_t status, logits, wsplit, chunk_counts, chunk_base, counts, offsets, row2tok, tok2row, idx, w, x_perm, h, hs,
-      y, ys, total;
+      y, ys, done, total;
 };
 
 bool is_bf16(const moe_config& c) { return c.act_dtype == MOE_BF16; }
@@ -81,6 +81,7 @@ WsLayout ws_layout(const moe_config& c) {
   L.hs = take(size_t(c.T) * I_s(c) * eb);
   L.y = take(R * c.d * 4);
   L.ys = take(size_t(c.T) * c.d * 4);
+  L.done = take(size_t(c.E + 1) * 4);   // per-group GEMM1 completion counters
   L.total = off;
   return L;
 }
@@ -182,13 +183,12 @@ moe_status run_gate(const moe_config& c, const void* x, const void* wg, const fl
 
 moe_status run_experts(const moe_config& c, const void* x_perm, const int32_t* offsets, const void* x,
                        const void* packed, void* y_perm, void* y_shared, const Ws& ws, cudaStream_t s,
-                       int* launches, bool mark_stages = false) {
+                       int* launches, bool counters_zeroed = false) {
   const PackedLayout P = packed_layout(c);
   const char* pb = static_cast<const char*>(packed);
   const long long R = (long long)c.T * c.k;
   const long long Is = I_s(c);
   if (!is_bf16(c)) {
-    if (mark_stages) profile_mark(s);   // the SIMT path has no separate GEMM2 stage boundary
     return cuda_status(launch_swiglu_simt_f32(c, static_cast<const float*>(x_perm), offsets,
                                               static_cast<const float*>(x), packed, ws.at<float>(ws.L.h),
                                               ws.at<float>(ws.L.hs), static_cast<float*>(y_perm),
@@ -196,31 +196,30 @@ moe_status run_experts(const moe_config& c, const void* x_perm, const int32_t* o
   }
   void* h = ws.at<void>(ws.L.h);
   void* hs = ws.at<void>(ws.L.hs);
-  const bool shared = Is > 0;
-  // Upper bounds of the pair tiles (256 tokens x 256 weight rows) for sizing the grid.
-  const long long tb_routed = R / 256 + c.E;
-  const long long tb_shared = shared ? (c.T + 255) / 256 : 0;
+  int* done = ws.at<int>(ws.L.done);
+  if (!counters_zeroed && cudaMemsetAsync(done, 0, size_t(c.E + 1) * 4, s) != cudaSuccess) return MOE_ERR_CUDA;
+  PairClass cls[4];
   // GEMM1 + SwiGLU: H[rows, I] = silu(X W1^T) * (X W3^T), packed W1/W3 rows [2I, d] per expert
-  PairClass r1, s1;
+  PairClass& r1 = cls[0];
   r1.W = pb + P.w13; r1.w_rows = 2LL * c.E * c.I; r1.X = x_perm; r1.x_rows = R; r1.K = c.d;
   r1.M = 2 * c.I; r1.w_step = 2 * c.I; r1.out = h; r1.ld_out = c.I; r1.out_rows = R;
+  PairClass& s1 = cls[1];
   s1.W = pb + P.w13s; s1.w_rows = 2 * Is; s1.X = x; s1.x_rows = c.T; s1.K = c.d;
   s1.M = int(2 * Is); s1.w_step = 0; s1.out = hs; s1.ld_out = Is; s1.out_rows = c.T;
-  const long long tiles1 = tb_routed * ((2LL * c.I + 255) / 256) + tb_shared * ((2 * Is + 255) / 256);
-  cudaError_t e = launch_pair_gemm(EPI_PAIR_SWIGLU, r1, shared ? &s1 : nullptr, offsets, c.E, c.T, ws.status(), tiles1,
-                                   s, launches, true);
-  if (e != cudaSuccess) return MOE_ERR_CUDA;
   // GEMM2: Y[rows, d] = H W2^T (fp32), W2 [d, I] per expert
-  PairClass r2, s2;
+  PairClass& r2 = cls[2];
   r2.W = pb + P.w2; r2.w_rows = (long long)c.E * c.d; r2.X = h; r2.x_rows = R; r2.K = c.I;
   r2.M = c.d; r2.w_step = c.d; r2.out = y_perm; r2.ld_out = c.d; r2.out_rows = R;
+  PairClass& s2 = cls[3];
   s2.W = pb + P.w2s; s2.w_rows = c.d; s2.X = hs; s2.x_rows = c.T; s2.K = int(Is);
   s2.M = c.d; s2.w_step = 0; s2.out = y_shared; s2.ld_out = c.d; s2.out_rows = c.T;
-  const long long tiles2 = (tb_routed + tb_shared) * ((c.d + 255) / 256);
-  if (mark_stages) profile_mark(s);
-  e = launch_pair_gemm(EPI_PAIR_F32, r2, shared ? &s2 : nullptr, offsets, c.E, c.T, ws.status(), tiles2, s, launches,
-                       false);
-  return cuda_status(e);
+  // upper bound of the pair tiles (256 tokens x 256 weight rows), for sizing the grid
+  const long long tb_routed = R / 256 + c.E;
+  const long long tb_shared = Is > 0 ? (c.T + 255) / 256 : 0;
+  const long long tiles = tb_routed * ((2LL * c.I + 255) / 256 + (c.d + 255) / 256) +
+                          tb_shared * ((2 * Is + 255) / 256 + (c.d + 255) / 256);
+  return cuda_status(launch_pair_experts(cls, offsets, c.E, Is > 0 ? c.T : 0, done, ws.status(), tiles, s,
+                                         launches));
 }
 
 }  // namespace
@@ -376,8 +375,11 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const void* Wg, con
   st = run_gate(c, x, Wg, bias, idx, w, W, s, &n);
   if (st == MOE_OK) {
     profile_mark(s);
+    // the gather also zeroes the expert GEMMs' completion counters
+    const bool tc = is_bf16(c);
     cudaError_t e = launch_permute(c, x, idx, counts, offsets, W.at<int32_t>(W.L.row2tok), tok2row, x_perm,
-                                   W.at<int32_t>(W.L.chunk_counts), W.at<int32_t>(W.L.chunk_base), W.status(), s, &n);
+                                   W.at<int32_t>(W.L.chunk_counts), W.at<int32_t>(W.L.chunk_base), W.status(), s, &n,
+                                   tc ? W.at<int>(W.L.done) : nullptr, tc ? c.E + 1 : 0);
     st = cuda_status(e);
   }
   if (st == MOE_OK) {
@@ -445,7 +447,7 @@ moe_status moe_profile_arm(void* const* events, int32_t n_events) {
 }
 
 const char* moe_forward_stage_name(int32_t i) {
-  static const char* names[MOE_FORWARD_STAGES] = {"router", "permute", "gemm1_swiglu", "gemm2", "combine"};
+  static const char* names[MOE_FORWARD_STAGES] = {"router", "permute", "experts", "combine"};
   return (i >= 0 && i < MOE_FORWARD_STAGES) ? names[i] : nullptr;
 }
 
@@ -456,7 +458,7 @@ int32_t moe_forward_kernel_count(const moe_config* cfg) {
   int n = 2;                                                        // logits + top-k
   if (use_tc_gate(c) && c.gate_w_dtype == MOE_F32) n += 1;          // W_g split
   n += permute_launches(c.T) + 1;                                   // permute + gather
-  n += 2;                                                           // GEMM1, GEMM2
+  n += is_bf16(c) ? 1 : 2;                                          // expert GEMMs (fused on bf16)
   n += 1;                                                           // combine
   return n;
 }

@@ -1,5 +1,6 @@
 // Expert GEMMs of the routed and shared SwiGLU experts on CTA pairs
-// (tcgen05.mma.cta_group::2 + TMEM + TMA), with the SwiGLU epilogue fused.
+// (tcgen05.mma.cta_group::2 + TMEM + TMA): both GEMMs of the expert FFN in one
+// persistent launch, the SwiGLU fused into the first one's epilogue.
 //
 // The expert FFN is w2(silu(w1 x) * w3 x) (intelliparadigm.com page, section
 // 3.3.1); the MoE listing of the DeepSeek-V2 walkthrough runs it per expert on
@@ -12,31 +13,37 @@
 //     X: up to 256 token rows of the same group (N, split N/2 per CTA)
 //
 // so the ragged dimension (tokens per expert) is the MMA's N, which comes in
-// steps of 16, not the M of 128 or 256 rows: a group of n tokens costs
-// ceil(n/16)*16 columns of tensor-core work instead of ceil(n/128)*128 rows.
-// The pair shares each B (token) tile between its two SMs, so an SM loads
-// 32 KB of operands per 128x256x64 block of work instead of 48 KB.
+// steps of 16: a group of n tokens costs ceil(n/16)*16 columns of tensor work.
+// The pair shares each token tile between its two SMs.
 //
-//   GEMM1 (EPI_PAIR_SWIGLU): W = packed W1/W3 rows interleaved in blocks of 16
-//     (rows 32q..32q+15 of a CTA's 128 hold W1 features, 32q+16..32q+31 the W3
-//     rows of the same features), X = token rows; the epilogue pairs lane l
-//     with lane l+16 by a warp shuffle and stores H[token][f] in bf16.
-//   GEMM2 (EPI_PAIR_F32): W = W2 rows, X = H rows; Y[token][f] in fp32.
+//   phase 1 (GEMM1): W = packed W1/W3 rows interleaved in blocks of 16 (rows
+//     32q..32q+15 of a CTA's 128 hold W1 features, 32q+16..32q+31 the W3 rows
+//     of the same features), X = token rows; the epilogue pairs lane l with
+//     lane l+16 by a warp shuffle and stores H[token][f] = silu(g)*u in bf16.
+//   phase 2 (GEMM2): W = W2 rows, X = H rows; Y[token][f] in fp32.
 //
-// Both classes of groups run in one persistent launch: class 0 = the routed
-// experts (group g = rows offsets[g] .. offsets[g+1] of the permuted tokens,
-// sizes read on the device), class 1 = the shared expert over all T tokens.
+// Tiles are numbered [GEMM1 shared][GEMM1 routed][GEMM2 shared][GEMM2 routed]
+// and dealt round-robin to the clusters.  A GEMM2 tile of a group waits on a
+// per-group counter that every CTA bumps (release) after storing its part of
+// a GEMM1 tile of that group, so GEMM2 work starts expert by expert while
+// other clusters still run GEMM1 tiles; every cluster finishes its own GEMM1
+// tiles before its first GEMM2 tile, so the waits always resolve.  The
+// shared expert's GEMM1 tiles need only x and may start before the preceding
+// dispatch kernel completes (programmatic dependent launch); routed tiles
+// wait for the routed tile table, which a scheduler warp builds from the
+// dispatch offsets once that kernel has completed.
 //
 // Each TMA copy moves two k-blocks (3-D tensor maps: 64 columns x rows x 2
 // k-blocks): a copy instruction has a fixed cost in the copy engine, so fewer,
 // larger copies raise the rate at which an SM's shared memory fills.
 //
-// CTA layout (192 threads, one CTA per SM, clusters of two CTAs):
+// CTA layout (224 threads, one CTA per SM, clusters of two CTAs):
 //   warp 0      TMA producer of this CTA's halves (3-stage ring of 2 k-blocks,
 //               128-byte swizzle); completion bytes count on rank 0's barrier
 //   warp 1      tensor-memory allocation (both CTAs); on rank 0 one thread
 //               issues the M=256 MMAs and commits to both CTAs' barriers
 //   warps 2..5  epilogue: tcgen05.ld of this CTA's 128 accumulator rows
+//   warp 6      tile scheduler (routed tile tables)
 // Two 256-column accumulators per CTA let the epilogue overlap the next
 // tile's main loop.  Every wait is bounded; a CTA that gives up flags the
 // status word and tells its peer to stop too.
@@ -69,20 +76,23 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_STRIDE = 256;  // columns between the two accumulators
 constexpr int EPI_WARPS = 4;
 
+// Operand classes: GEMM1 routed, GEMM1 shared, GEMM2 routed, GEMM2 shared.
+constexpr int C1R = 0, C1S = 1, C2R = 2, C2S = 3, NCLS = 4;
+
 struct PairParams {
-  CUtensorMap tmW[2];     // weights: 64 x 128 rows x 2 k-blocks
-  CUtensorMap tmX[2];     // tokens: 64 x 128 rows x 2 k-blocks
-  CUtensorMap tmXs[2];    // tokens: 64 x 32 rows x 2 k-blocks
-  void* out[2];
-  long long ld_out[2];
-  long long out_rows[2];
-  int M[2];          // output features of one group (its weight rows)
-  int early_shared;  // shared-expert tiles run before the predecessor grid completes
-  int K[2];          // reduction length (multiple of 64)
-  int w_step[2];     // weight rows between consecutive groups of the class
+  CUtensorMap tmW[NCLS];     // weights: 64 x 128 rows x 2 k-blocks
+  CUtensorMap tmX[NCLS];     // tokens: 64 x 128 rows x 2 k-blocks
+  CUtensorMap tmXs[NCLS];    // tokens: 64 x 32 rows x 2 k-blocks
+  void* out[NCLS];
+  long long ld_out[NCLS];
+  long long out_rows[NCLS];
+  int M[NCLS];          // weight rows of one group (GEMM1: 2 x hidden, GEMM2: d)
+  int K[NCLS];          // reduction length (multiple of 64)
+  int w_step[NCLS];     // weight rows between consecutive groups of the class
   const int32_t* offsets;
   int num_routed;
-  int shared_rows;
+  int shared_rows;      // tokens of the shared expert (0: none)
+  int* done;            // [num_routed + 1] GEMM1 completion counters, zero at launch
   int* status;
 };
 
@@ -94,10 +104,9 @@ struct PairCtrl {
   uint64_t drain;            // rank 0: every issued MMA completed
   uint32_t tmem_base;
   int abort;
-  int shared_tiles;          // tiles [0, shared_tiles): the shared expert
-  int routed_tiles;          // then the routed experts' tiles
-  int routed_ready;          // the routed tile table is built
-  int tile_start[MAX_GROUPS + 1];
+  int seg[5];                // tile numbers where the four segments start, and the total
+  int routed_ready;          // the routed tile tables (and seg[2..4]) are built
+  int tile_start[2][MAX_GROUPS + 1];   // per phase: exclusive prefix of routed tiles
   int row_start[MAX_GROUPS];
   int rows[MAX_GROUPS];
 };
@@ -109,7 +118,9 @@ static_assert(kPairSmem <= 227 * 1024, "shared memory budget");
 static_assert(kPairSmem > 114 * 1024, "one CTA per SM");
 
 struct PairTile {
-  int cls, g, fb, tb, row_start, rows;
+  int cls;       // operand class (C1R, C1S, C2R, C2S)
+  int g;         // group: routed expert, or num_routed for the shared expert
+  int fb, tb, row_start, rows;
   int n_valid;   // token rows of this tile
   int n_mma;     // MMA N = n_valid rounded up to 16
 };
@@ -120,69 +131,89 @@ __device__ __forceinline__ int pair_group_tiles(const PairParams& p, int cls, in
   return cdiv(rows, PN) * cdiv(p.M[cls], PAIR_M);
 }
 
+// GEMM1 counter value at which a group's hidden rows are complete: every
+// epilogue warp of both CTAs bumps it once per GEMM1 tile of the group.
+__device__ __forceinline__ int gemm1_need(const PairParams& p, int cls1, int rows) {
+  return 2 * EPI_WARPS * pair_group_tiles(p, cls1, rows);
+}
+
 // Warp-cooperative: row ranges of the routed groups (from the dispatch
-// offsets) and the exclusive prefix of their tiles.
+// offsets), the exclusive prefix of their tiles in both phases, and the
+// segment boundaries that depend on them.
 __device__ void pair_schedule(PairCtrl* c, const PairParams& p, int lane) {
   const int ng = p.num_routed;
   const int per = cdiv(ng, 32);
   const int lo = min(ng, lane * per), hi = min(ng, lo + per);
-  int local = 0;
+  int local1 = 0, local2 = 0;
   for (int g = lo; g < hi; ++g) {
     int rs = p.offsets[g];
     int rows = p.offsets[g + 1] - rs;
-    if (rows < 0 || rs < 0 || (long long)rs + rows > p.out_rows[0]) {
+    if (rows < 0 || rs < 0 || (long long)rs + rows > p.out_rows[C1R]) {
       flag_status(p.status, DEV_BAD_ROW);
       rs = 0;
       rows = 0;
     }
     c->row_start[g] = rs;
     c->rows[g] = rows;
-    local += pair_group_tiles(p, 0, rows);
+    local1 += pair_group_tiles(p, C1R, rows);
+    local2 += pair_group_tiles(p, C2R, rows);
   }
-  int incl = local;
+  int incl1 = local1, incl2 = local2;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const int v = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += v;
+    const int v1 = __shfl_up_sync(0xffffffffu, incl1, o);
+    const int v2 = __shfl_up_sync(0xffffffffu, incl2, o);
+    if (lane >= o) {
+      incl1 += v1;
+      incl2 += v2;
+    }
   }
-  int run = incl - local;
+  int run1 = incl1 - local1, run2 = incl2 - local2;
   for (int g = lo; g < hi; ++g) {
-    c->tile_start[g] = run;
-    run += pair_group_tiles(p, 0, c->rows[g]);
+    c->tile_start[0][g] = run1;
+    c->tile_start[1][g] = run2;
+    run1 += pair_group_tiles(p, C1R, c->rows[g]);
+    run2 += pair_group_tiles(p, C2R, c->rows[g]);
   }
   if (lane == 31) {
-    c->tile_start[ng] = incl;
-    c->routed_tiles = incl;
+    c->tile_start[0][ng] = incl1;
+    c->tile_start[1][ng] = incl2;
+    // seg[0] = 0 and seg[1] = GEMM1 shared tiles were set at start-up
+    c->seg[2] = c->seg[1] + incl1;
+    c->seg[3] = c->seg[2] + (p.shared_rows > 0 ? pair_group_tiles(p, C2S, p.shared_rows) : 0);
+    c->seg[4] = c->seg[3] + incl2;
   }
 }
 
-// Tile numbering: [0, shared_tiles) the shared expert (class 1), then the
-// routed experts (class 0) in expert order.  Within a group the block order
-// keeps the operand that is re-read the most resident in L2: with more token
-// blocks than weight blocks the token block is the outer loop (its rows are
-// re-used by every weight block), otherwise the weight block is.
+// Tile number -> class, group, weight block and token block.  Within a group
+// the block order keeps the operand that is re-read the most resident in L2:
+// with more token blocks than weight blocks the token block is the outer loop
+// (its rows are re-used by every weight block), otherwise the weight block is.
 __device__ __forceinline__ PairTile pair_tile(const PairCtrl* c, const PairParams& p, int tile) {
   PairTile t;
   int local;
-  if (tile < c->shared_tiles) {
-    t.g = 0;
-    t.cls = 1;
+  int seg = 0;
+  if (tile >= c->seg[1]) seg = tile < c->seg[2] ? 1 : (tile < c->seg[3] ? 2 : 3);
+  local = tile - c->seg[seg];
+  if (seg == 0 || seg == 2) {
+    t.cls = seg == 0 ? C1S : C2S;
+    t.g = p.num_routed;
     t.row_start = 0;
     t.rows = p.shared_rows;
-    local = tile;
   } else {
-    const int rt = tile - c->shared_tiles;
+    const int ph = seg == 1 ? 0 : 1;
+    const int* ts = c->tile_start[ph];
     int lo = 0, hi = p.num_routed - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
-      if (c->tile_start[mid] <= rt) lo = mid;
+      if (ts[mid] <= local) lo = mid;
       else hi = mid - 1;
     }
+    t.cls = ph == 0 ? C1R : C2R;
     t.g = lo;
-    t.cls = 0;
     t.row_start = c->row_start[lo];
     t.rows = c->rows[lo];
-    local = rt - c->tile_start[lo];
+    local -= ts[lo];
   }
   const int tbn = cdiv(t.rows, PN), fbn = cdiv(p.M[t.cls], PAIR_M);
   if (tbn > fbn) {
@@ -197,11 +228,9 @@ __device__ __forceinline__ PairTile pair_tile(const PairCtrl* c, const PairParam
   return t;
 }
 
-// Whether `tile` exists.  Shared-expert tiles need nothing; a routed tile
-// needs the routed table, which is built once the dispatch has completed
-// (bounded wait on the flag).
-__device__ __forceinline__ bool pair_tile_exists(PairCtrl* c, int tile, int* status) {
-  if (tile < c->shared_tiles) return true;
+// Bounded wait on the routed tile tables (built by the scheduler warp once
+// the dispatch has completed).  Returns false when it gave up.
+__device__ __forceinline__ bool wait_routed_ready(PairCtrl* c, int* status) {
   volatile int* ready = &c->routed_ready;
   if (!*ready) {
     const unsigned long long t0 = globaltimer_ns();
@@ -216,7 +245,15 @@ __device__ __forceinline__ bool pair_tile_exists(PairCtrl* c, int tile, int* sta
     }
   }
   __threadfence_block();
-  return tile < c->shared_tiles + c->routed_tiles;
+  return true;
+}
+
+// Whether `tile` exists.  GEMM1 shared-expert tiles need nothing; any other
+// tile needs the routed tables.
+__device__ __forceinline__ bool pair_tile_exists(PairCtrl* c, int tile, int* status) {
+  if (tile < c->seg[1]) return true;
+  if (!wait_routed_ready(c, status)) return false;
+  return tile < c->seg[4];
 }
 
 // Bounded wait; on giving up it flags the status word and stops both CTAs.
@@ -246,14 +283,38 @@ __device__ void pair_producer(PairCtrl* c, const PairParams& p, uint8_t* stages,
   uint32_t phase = 0;
   uint32_t issued = 0, issued_par = 0;
   bool ok = true;
-  bool waited = !p.early_shared;
+  bool waited = false;
+  int ready_group = -1;   // GEMM2 group whose hidden rows are known complete
   for (int tile = (int)cluster_id_x(); ok && pair_tile_exists(c, tile, p.status); tile += (int)cluster_count_x()) {
     const PairTile t = pair_tile(c, p, tile);
-    if (t.cls == 0 && !waited) {
+    if (t.cls == C1R && !waited) {
       pdl_wait();   // the permuted token rows come from the preceding grid
       waited = true;
     }
-    const int w_row = (t.cls == 0 ? t.g * p.w_step[0] : 0) + t.fb * PAIR_M + int(rank) * PM;
+    if ((t.cls == C2R || t.cls == C2S) && t.g != ready_group) {
+      // the group's GEMM1 tiles (any cluster) have stored its hidden rows
+      const int need = gemm1_need(p, t.cls == C2R ? C1R : C1S, t.rows);
+      const unsigned long long t0 = globaltimer_ns();
+      while (ld_acquire_gpu(p.done + t.g) < need) {
+        if (*reinterpret_cast<volatile int*>(&c->abort)) {
+          ok = false;
+          break;
+        }
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+          c->abort = 1;
+          st_remote_u32(peer_abort, 1u);
+          flag_status(p.status, DEV_TIMEOUT);
+          ok = false;
+          break;
+        }
+        __nanosleep(128);
+      }
+      if (!ok) break;
+      fence_proxy_async_global();   // the copy engine reads what the acquire made visible
+      ready_group = t.g;
+    }
+    const bool routed = t.cls == C1R || t.cls == C2R;
+    const int w_row = (routed ? t.g * p.w_step[t.cls] : 0) + t.fb * PAIR_M + int(rank) * PM;
     const int x_row = t.row_start + t.tb * PN + int(rank) * (t.n_mma / 2);
     const int nks = (p.K[t.cls] / BK + KB_STAGE - 1) / KB_STAGE;   // stages of this tile
     const bool small = t.n_mma / 2 <= XSMALL;
@@ -337,7 +398,6 @@ __device__ __forceinline__ bool pair_warp_wait(uint64_t* bar, uint32_t parity, P
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
-template <int EPI>
 __device__ void pair_epilogue(PairCtrl* c, const PairParams& p, uint32_t tmem, int warp, int lane, uint32_t rank,
                               uint32_t peer_abort) {
   const int q = warp & 3;   // the tensor-memory lane quarter this warp may read
@@ -353,7 +413,8 @@ __device__ void pair_epilogue(PairCtrl* c, const PairParams& p, uint32_t tmem, i
     const uint32_t tbase = tmem + uint32_t(acc) * ACC_STRIDE + (uint32_t(q * 32) << 16);
     const long long row0 = (long long)t.row_start + (long long)t.tb * PN;
     const int ncols = (t.n_valid + 15) & ~15;
-    if constexpr (EPI == EPI_PAIR_SWIGLU) {
+    const bool gemm1 = t.cls == C1R || t.cls == C1S;
+    if (gemm1) {
       // lane l < 16: W1 row of feature f; lane l + 16: the W3 row of the same f
       const int f = t.fb * (PAIR_M / 2) + int(rank) * (PM / 2) + q * 16 + (lane & 15);
       __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out[t.cls]) + f;
@@ -398,10 +459,18 @@ __device__ void pair_epilogue(PairCtrl* c, const PairParams& p, uint32_t tmem, i
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive_remote(map_to_rank(smem_u32(&c->tempty[acc]), 0));
+    if (gemm1) {
+      // publish this warp's part of the tile: the lanes' stores, then one
+      // release increment of the group's counter.  The counters are zeroed by
+      // the preceding grid, so the increment waits for the routed tables
+      // (built after that grid completed).
+      __threadfence();
+      __syncwarp();
+      if (lane == 0 && wait_routed_ready(c, p.status)) red_release_gpu_add(p.done + t.g, 1);
+    }
   }
 }
 
-template <int EPI>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     pair_gemm_kernel(const __grid_constant__ PairParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -424,13 +493,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     mbar_init(&c->drain, 1);
     c->abort = 0;
     c->routed_ready = 0;
-    c->routed_tiles = 0;
-    c->shared_tiles = p.shared_rows > 0 ? cdiv(p.shared_rows, PN) * cdiv(p.M[1], PAIR_M) : 0;
+    c->seg[0] = 0;
+    c->seg[1] = p.shared_rows > 0 ? pair_group_tiles(p, C1S, p.shared_rows) : 0;
     fence_mbar_init();
     pdl_launch_dependents();
   }
   if (warp == 0 && lane == 0) {
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < NCLS; ++i) {
       tma_prefetch_desc(&p.tmW[i]);
       tma_prefetch_desc(&p.tmX[i]);
       tma_prefetch_desc(&p.tmXs[i]);
@@ -444,8 +513,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   // both CTAs' barriers and tensor memory are ready
   cluster_sync_all();
   tc_fence_after();
-  // Without early shared tiles every input comes from the preceding grid.
-  if (!p.early_shared) pdl_wait();
 
   const uint32_t tmem = c->tmem_base;
   if (warp == 0) {
@@ -453,10 +520,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   } else if (warp == 1) {
     if (lane == 0 && rank == 0) pair_mma(c, p, stages, tmem, peer_abort);
   } else if (warp < 2 + EPI_WARPS) {
-    pair_epilogue<EPI>(c, p, tmem, warp, lane, rank, peer_abort);
+    pair_epilogue(c, p, tmem, warp, lane, rank, peer_abort);
   } else {
-    // scheduler warp: the routed table needs the dispatch offsets
-    if (p.early_shared) pdl_wait();
+    // scheduler warp: the routed tables need the dispatch offsets
+    pdl_wait();
     pair_schedule(c, p, lane);
     __syncwarp();
     __threadfence_block();
@@ -471,12 +538,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   }
 }
 
-
-template <int EPI>
-cudaError_t launch_pair_epi(const PairParams& p, long long max_tiles, cudaStream_t stream) {
+cudaError_t launch_pair(const PairParams& p, long long max_tiles, cudaStream_t stream) {
   static int max_clusters = -1;
   if (max_clusters < 0) {
-    cudaError_t e = cudaFuncSetAttribute(pair_gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(pair_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          int(kPairSmem));
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -491,27 +556,29 @@ cudaError_t launch_pair_epi(const PairParams& p, long long max_tiles, cudaStream
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, pair_gemm_kernel<EPI>, &cfg) != cudaSuccess || n <= 0) {
+    if (cudaOccupancyMaxActiveClusters(&n, pair_gemm_kernel, &cfg) != cudaSuccess || n <= 0) {
       cudaGetLastError();
       n = num_sms() / 2;
     }
     max_clusters = n;
   }
+  // every cluster must be resident at once: GEMM2 tiles wait for GEMM1 tiles
+  // of other clusters
   const long long pairs = max_tiles < max_clusters ? max_tiles : max_clusters;
-  return launch_pdl(pair_gemm_kernel<EPI>, dim3(int(2 * pairs)), dim3(THREADS), kPairSmem, stream, p);
+  return launch_pdl(pair_gemm_kernel, dim3(int(2 * pairs)), dim3(THREADS), kPairSmem, stream, p);
 }
 
 }  // namespace
 
-cudaError_t launch_pair_gemm(int epi, const PairClass& c0, const PairClass* c1, const int32_t* offsets, int num_routed,
-                             int shared_rows, int* status, long long max_tiles, cudaStream_t stream, int* launches,
-                             bool early_shared) {
+cudaError_t launch_pair_experts(const PairClass cls[4], const int32_t* offsets, int num_routed, int shared_rows,
+                                int* done, int* status, long long max_tiles, cudaStream_t stream, int* launches) {
   if (max_tiles <= 0) return cudaSuccess;
+  if (num_routed < 1 || num_routed + 1 > MAX_GROUPS || done == nullptr) return cudaErrorInvalidValue;
   PairParams p;
   memset(&p, 0, sizeof(p));
-  const PairClass* cls[2] = {&c0, c1 != nullptr ? c1 : &c0};
-  for (int i = 0; i < 2; ++i) {
-    const PairClass& g = *cls[i];
+  for (int i = 0; i < NCLS; ++i) {
+    // without a shared expert its classes repeat the routed ones (never used)
+    const PairClass& g = (shared_rows > 0 || i == C1R || i == C2R) ? cls[i] : cls[i - 1];
     if (g.K % BK != 0) return cudaErrorInvalidValue;
     if (!encode_bf16_map(&p.tmW[i], g.W, g.w_rows, g.K, PM, KB_STAGE)) return cudaErrorInvalidValue;
     if (!encode_bf16_map(&p.tmX[i], g.X, g.x_rows, g.K, XB, KB_STAGE)) return cudaErrorInvalidValue;
@@ -525,12 +592,10 @@ cudaError_t launch_pair_gemm(int epi, const PairClass& c0, const PairClass* c1, 
   }
   p.offsets = offsets;
   p.num_routed = num_routed;
-  p.shared_rows = c1 != nullptr ? shared_rows : 0;
+  p.shared_rows = shared_rows;
+  p.done = done;
   p.status = status;
-  p.early_shared = early_shared ? 1 : 0;
-  if (num_routed < 1 || num_routed + 1 > MAX_GROUPS) return cudaErrorInvalidValue;
-  cudaError_t e = epi == EPI_PAIR_SWIGLU ? launch_pair_epi<EPI_PAIR_SWIGLU>(p, max_tiles, stream)
-                                         : launch_pair_epi<EPI_PAIR_F32>(p, max_tiles, stream);
+  cudaError_t e = launch_pair(p, max_tiles, stream);
   if (e == cudaSuccess && launches) ++*launches;
   return e;
 }

@@ -89,13 +89,13 @@ struct PairClass {
   int64_t out_rows = 0;
 };
 
-enum PairEpi : int { EPI_PAIR_SWIGLU = 0, EPI_PAIR_F32 = 1 };
-
-// early_shared: the shared expert's tiles (class 1) run first and may start
-// before the preceding grid in the stream completes; routed tiles wait for it.
-cudaError_t launch_pair_gemm(int epi, const PairClass& c0, const PairClass* c1, const int32_t* offsets, int num_routed,
-                             int shared_rows, int* status, long long max_tiles, cudaStream_t stream, int* launches,
-                             bool early_shared);
+// Both expert GEMMs in one launch.  cls = {GEMM1 routed, GEMM1 shared, GEMM2
+// routed, GEMM2 shared}; GEMM1 outputs bf16 silu(W1 x) * (W3 x) (W = packed
+// W1/W3 rows, 16-row interleave), GEMM2 fp32.  done [num_routed + 1] must be
+// zero when the launch starts (per-group GEMM1 completion counters).  The
+// shared expert's GEMM1 tiles may run before the preceding grid completes.
+cudaError_t launch_pair_experts(const PairClass cls[4], const int32_t* offsets, int num_routed, int shared_rows,
+                                int* done, int* status, long long max_tiles, cudaStream_t stream, int* launches);
 
 // ---------------------------------------------------------------------- router
 cudaError_t launch_gate_split(const float* wg, int E, int d, void* wsplit, cudaStream_t s, int* launches);
@@ -109,10 +109,12 @@ cudaError_t launch_topk(const moe_config& c, const float* logits, int nsplit, lo
 // ---------------------------------------------------------------- permutation
 int permute_chunks(int T);
 int permute_launches(int T);   // kernels of steps 1-3 (the gather is one more)
+// zero [n_zero] (nullable): counters the gather kernel clears for the expert
+// GEMMs that follow it.
 cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* idx, int32_t* counts,
                            int32_t* offsets, int32_t* row2tok, int32_t* tok2row, void* x_perm,
                            int32_t* chunk_counts, int32_t* chunk_base, int* status, cudaStream_t s,
-                           int* launches);
+                           int* launches, int* zero = nullptr, int n_zero = 0);
 
 // -------------------------------------------------------------------- experts
 cudaError_t launch_prepack(const moe_config& c, const void* W1, const void* W3, const void* W2,

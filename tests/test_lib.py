@@ -44,10 +44,14 @@ def test_sizes_for_every_workload(name):
     # workspace holds at least the permuted rows, hidden and outputs
     assert ws >= (2 * wl.R * wl.d + wl.R * wl.I) * eb
     # router (+ the fp32 gate-weight split on the tensor-core path), dispatch
-    # (one block up to 4096 tokens, four kernels above), gather, two GEMMs, combine
-    gate = 2 + (1 if wl.act_dtype == "bf16" and wl.gate_w_dtype == "f32" else 0)
+    # (one block up to 4096 tokens, four kernels above), gather, the expert
+    # GEMMs (one fused launch on the tensor-core path, two SIMT kernels in fp32),
+    # combine
+    bf16 = wl.act_dtype == "bf16"
+    gate = 2 + (1 if bf16 and wl.gate_w_dtype == "f32" else 0)
     dispatch = 1 if wl.T <= 4096 else 4
-    assert _lib.moe_forward_kernel_count(cfg) == gate + dispatch + 1 + 2 + 1
+    experts = 1 if bf16 else 2
+    assert _lib.moe_forward_kernel_count(cfg) == gate + dispatch + 1 + experts + 1
 
 
 def _cfg(**kw):

@@ -218,7 +218,7 @@ moe_status run_experts(const moe_config& c, const void* x_perm, const int32_t* o
   const long long tb_shared = Is > 0 ? (c.T + 255) / 256 : 0;
   const long long tiles = tb_routed * ((2LL * c.I + 255) / 256 + (c.d + 255) / 256) +
                           tb_shared * ((2 * Is + 255) / 256 + (c.d + 255) / 256);
-  return cuda_status(launch_pair_experts(cls, offsets, c.E, Is > 0 ? c.T : 0, done, ws.status(), tiles, s,
+  return cuda_status(launch_pair_experts(cls, offsets, c.E, Is > 0 ? c.T : 0, c.T, done, ws.status(), tiles, s,
                                          launches));
 }
 

@@ -160,6 +160,9 @@ __global__ void __launch_bounds__(TOPK_WARPS * 32) topk_kernel(const float* __re
 
   if (a.method == MOE_TOPK_GROUP_LIMITED && a.topk_group < a.n_group) {
     const int gsz = a.E / a.n_group;
+    int gid[MAXV];   // group of each slot (contiguous blocks of gsz experts)
+#pragma unroll
+    for (int i = 0; i < MAXV; ++i) gid[i] = (lane + 32 * i) / gsz;
     uint32_t kept = 0;   // bit g: group g stays eligible (same in every lane)
     float my_gscore = NEG;   // lane g holds the score of group g
     for (int g = 0; g < a.n_group; ++g) {
@@ -167,11 +170,34 @@ __global__ void __launch_bounds__(TOPK_WARPS * 32) topk_kernel(const float* __re
       if (a.group_score == MOE_GROUP_MAX) {
         float m = NEG;
 #pragma unroll
-        for (int i = 0; i < MAXV; ++i) {
-          const int e = lane + 32 * i;
-          if ((elig >> i & 1u) && e / gsz == g) m = fmaxf(m, sel[i]);
-        }
+        for (int i = 0; i < MAXV; ++i)
+          if ((elig >> i & 1u) && gid[i] == g) m = fmaxf(m, sel[i]);
         gscore = warp_max(m);
+      } else if (a.group_top == 2) {
+        // the group's two largest scores: each lane's pair, then a butterfly
+        // merge of sorted pairs; their fp32 sum
+        float v1 = NEG, v2 = NEG;
+#pragma unroll
+        for (int i = 0; i < MAXV; ++i) {
+          if ((elig >> i & 1u) && gid[i] == g) {
+            const float x = sel[i];
+            if (x > v1) {
+              v2 = v1;
+              v1 = x;
+            } else if (x > v2) {
+              v2 = x;
+            }
+          }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const float b1 = __shfl_xor_sync(0xffffffffu, v1, o);
+          const float b2 = __shfl_xor_sync(0xffffffffu, v2, o);
+          const float hi = fmaxf(v1, b1);
+          v2 = fmaxf(fminf(v1, b1), fmaxf(v2, b2));
+          v1 = hi;
+        }
+        gscore = __fadd_rn(v1, v2);
       } else {
         // sum of the group's top-m scores, in descending order, in fp32
         uint32_t used = 0;
@@ -182,7 +208,7 @@ __global__ void __launch_bounds__(TOPK_WARPS * 32) topk_kernel(const float* __re
 #pragma unroll
           for (int i = 0; i < MAXV; ++i) {
             const int e = lane + 32 * i;
-            if ((elig >> i & 1u) && !(used >> i & 1u) && e / gsz == g && (sel[i] > v || (sel[i] == v && e < id))) {
+            if ((elig >> i & 1u) && !(used >> i & 1u) && gid[i] == g && (sel[i] > v || (sel[i] == v && e < id))) {
               v = sel[i];
               id = e;
             }
@@ -203,10 +229,8 @@ __global__ void __launch_bounds__(TOPK_WARPS * 32) topk_kernel(const float* __re
       kept |= 1u << id;
     }
 #pragma unroll
-    for (int i = 0; i < MAXV; ++i) {
-      const int e = lane + 32 * i;
-      if ((elig >> i & 1u) && !(kept >> (e / gsz) & 1u)) elig &= ~(1u << i);
-    }
+    for (int i = 0; i < MAXV; ++i)
+      if ((elig >> i & 1u) && !(kept >> gid[i] & 1u)) elig &= ~(1u << i);
   }
 
   // k rounds of warp arg-max over the eligible, not yet chosen experts

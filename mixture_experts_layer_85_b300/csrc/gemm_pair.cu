@@ -62,15 +62,22 @@ constexpr int PN = 256;               // token columns per pair tile at most
 constexpr int XB = PN / 2;            // token rows loaded by each CTA
 constexpr int BK = 64;                // K of one k-block (one 128-byte swizzle row)
 constexpr int KB_STAGE = 2;           // k-blocks per stage and per TMA copy
-constexpr int STAGES = 3;
+// Ring geometry.  Regular launches: 3 stages of 64 KB (weights 32 KB + tokens
+// 32 KB per CTA).  Decode-sized launches (every group at most 64 tokens, so
+// every tile uses the 32-row token box): 5 stages of 40 KB, a deeper queue of
+// weight copies for streaming-bound work.
+constexpr int MAX_STAGES = 5;
 constexpr int THREADS = 224;
 constexpr int A_KB_BYTES = PM * BK * 2;          // one k-block of this CTA's weight rows
 constexpr int B_KB_BYTES = XB * BK * 2;          // one k-block of this CTA's token rows
 constexpr int A_BYTES = KB_STAGE * A_KB_BYTES;
 constexpr int B_BYTES = KB_STAGE * B_KB_BYTES;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int RING_BYTES = 200 * 1024;
 constexpr int XSMALL = 32;                       // token rows of the small box (decode-sized tiles)
 constexpr int XS_KB_BYTES = XSMALL * BK * 2;
+constexpr int SMALL_STAGE_BYTES = A_BYTES + KB_STAGE * XS_KB_BYTES;
+static_assert(3 * STAGE_BYTES <= RING_BYTES && MAX_STAGES * SMALL_STAGE_BYTES <= RING_BYTES, "ring");
 constexpr int MAX_GROUPS = 272;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_STRIDE = 256;  // columns between the two accumulators
@@ -94,11 +101,13 @@ struct PairParams {
   int shared_rows;      // tokens of the shared expert (0: none)
   int* done;            // [num_routed + 1] GEMM1 completion counters, zero at launch
   int* status;
+  int stages;           // ring depth (3, or MAX_STAGES for decode-sized launches)
+  int stage_bytes;      // bytes of one stage in this CTA's shared memory
 };
 
 struct PairCtrl {
-  uint64_t full[STAGES];     // rank 0: both CTAs' operand bytes of a stage landed
-  uint64_t empty[STAGES];    // each CTA: the MMAs that read a stage completed
+  uint64_t full[MAX_STAGES];   // rank 0: both CTAs' operand bytes of a stage landed
+  uint64_t empty[MAX_STAGES];  // each CTA: the MMAs that read a stage completed
   uint64_t tfull[2];         // each CTA: an accumulator buffer is complete
   uint64_t tempty[2];        // rank 0: both CTAs' epilogues drained a buffer
   uint64_t drain;            // rank 0: every issued MMA completed
@@ -111,7 +120,7 @@ struct PairCtrl {
   int rows[MAX_GROUPS];
 };
 
-constexpr size_t kPairSmem = 1024 + size_t(STAGES) * STAGE_BYTES + sizeof(PairCtrl);
+constexpr size_t kPairSmem = 1024 + size_t(RING_BYTES) + sizeof(PairCtrl);
 static_assert(kPairSmem <= 227 * 1024, "shared memory budget");
 // More than half of an SM's shared memory: one CTA per SM, so the full
 // tensor-memory allocation never waits on another resident CTA.
@@ -326,14 +335,14 @@ __device__ void pair_producer(PairCtrl* c, const PairParams& p, uint8_t* stages,
         ok = false;
         break;
       }
-      uint8_t* sa = stages + stage * STAGE_BYTES;
+      uint8_t* sa = stages + stage * p.stage_bytes;
       if (rank == 0) mbar_arrive_expect_tx(&c->full[stage], bytes);
       const uint32_t fb = map_to_rank(smem_u32(&c->full[stage]), 0);   // rank 0's barrier
       tma_load_3d_pair(sa, &p.tmW[t.cls], fb, w_row, ks * KB_STAGE);
       tma_load_3d_pair(sa + A_BYTES, xmap, fb, x_row, ks * KB_STAGE);
       issued |= 1u << stage;
       issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
-      if (++stage == STAGES) {
+      if (++stage == p.stages) {
         stage = 0;
         phase ^= 1u;
       }
@@ -341,7 +350,7 @@ __device__ void pair_producer(PairCtrl* c, const PairParams& p, uint8_t* stages,
   }
   // The last copy into each stage was consumed (so it landed) before this CTA
   // may leave; on the normal path these waits return at once.
-  for (int s = 0; s < STAGES; ++s)
+  for (int s = 0; s < p.stages; ++s)
     if (issued & (1u << s)) pair_wait(&c->empty[s], (issued_par >> s) & 1u, c, peer_abort, p.status);
 }
 
@@ -366,7 +375,7 @@ __device__ void pair_mma(PairCtrl* c, const PairParams& p, uint8_t* stages, uint
         break;
       }
       tc_fence_after();
-      const uint32_t a0 = smem_u32(stages + stage * STAGE_BYTES);
+      const uint32_t a0 = smem_u32(stages + stage * p.stage_bytes);
       const uint32_t b0 = a0 + A_BYTES;
 #pragma unroll
       for (int j = 0; j < KB_STAGE; ++j)
@@ -375,7 +384,7 @@ __device__ void pair_mma(PairCtrl* c, const PairParams& p, uint8_t* stages, uint
           mma_bf16_pair(d_tmem, sw128_kmajor_desc(a0 + j * A_KB_BYTES + kk * 32),
                         sw128_kmajor_desc(b0 + j * b_kb + kk * 32), idesc, (ks | j | kk) != 0 ? 1u : 0u);
       mma_commit_pair(&c->empty[stage], 0x3);
-      if (++stage == STAGES) {
+      if (++stage == p.stages) {
         stage = 0;
         phase ^= 1u;
       }
@@ -476,13 +485,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stages = base;
-  PairCtrl* c = reinterpret_cast<PairCtrl*>(base + size_t(STAGES) * STAGE_BYTES);
+  PairCtrl* c = reinterpret_cast<PairCtrl*>(base + size_t(RING_BYTES));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
   const uint32_t peer_abort = map_to_rank(smem_u32(&c->abort), rank ^ 1u);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < MAX_STAGES; ++s) {
       mbar_init(&c->full[s], 1);
       mbar_init(&c->empty[s], 1);
     }
@@ -571,7 +580,8 @@ cudaError_t launch_pair(const PairParams& p, long long max_tiles, cudaStream_t s
 }  // namespace
 
 cudaError_t launch_pair_experts(const PairClass cls[4], const int32_t* offsets, int num_routed, int shared_rows,
-                                int* done, int* status, long long max_tiles, cudaStream_t stream, int* launches) {
+                                int max_group_rows, int* done, int* status, long long max_tiles, cudaStream_t stream,
+                                int* launches) {
   if (max_tiles <= 0) return cudaSuccess;
   if (num_routed < 1 || num_routed + 1 > MAX_GROUPS || done == nullptr) return cudaErrorInvalidValue;
   PairParams p;
@@ -595,6 +605,11 @@ cudaError_t launch_pair_experts(const PairClass cls[4], const int32_t* offsets, 
   p.shared_rows = shared_rows;
   p.done = done;
   p.status = status;
+  // A group never holds more tokens than the batch, so with at most 64 tokens
+  // every tile takes the 32-row token box: use the deeper ring of small stages.
+  const bool small = max_group_rows <= 2 * XSMALL;
+  p.stages = small ? MAX_STAGES : 3;
+  p.stage_bytes = small ? SMALL_STAGE_BYTES : STAGE_BYTES;
   cudaError_t e = launch_pair(p, max_tiles, stream);
   if (e == cudaSuccess && launches) ++*launches;
   return e;

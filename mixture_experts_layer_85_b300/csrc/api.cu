@@ -37,6 +37,12 @@ struct WsLayout {
 bool is_bf16(const moe_config& c) { return c.act_dtype == MOE_BF16; }
 long long I_s(const moe_config& c) { return (long long)c.n_shared * c.I; }
 
+// Both expert GEMMs in one launch pays off when GEMM1 has few tile rounds, so
+// its last partial round would leave SMs idle (decode-sized batches); large
+// batches run the GEMMs as two launches (measured faster on B300 there).
+constexpr long long kFuseMaxRows = 8192;   // T * k
+bool fuse_expert_gemms(const moe_config& c) { return (long long)c.T * c.k <= kFuseMaxRows; }
+
 bool use_tc_gate(const moe_config& c) {
   return is_bf16(c) && c.E <= 256;
 }
@@ -197,7 +203,8 @@ moe_status run_experts(const moe_config& c, const void* x_perm, const int32_t* o
   void* h = ws.at<void>(ws.L.h);
   void* hs = ws.at<void>(ws.L.hs);
   int* done = ws.at<int>(ws.L.done);
-  if (!counters_zeroed && cudaMemsetAsync(done, 0, size_t(c.E + 1) * 4, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (!counters_zeroed && fuse_expert_gemms(c) && cudaMemsetAsync(done, 0, size_t(c.E + 1) * 4, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
   PairClass cls[4];
   // GEMM1 + SwiGLU: H[rows, I] = silu(X W1^T) * (X W3^T), packed W1/W3 rows [2I, d] per expert
   PairClass& r1 = cls[0];
@@ -216,9 +223,18 @@ moe_status run_experts(const moe_config& c, const void* x_perm, const int32_t* o
   // upper bound of the pair tiles (256 tokens x 256 weight rows), for sizing the grid
   const long long tb_routed = R / 256 + c.E;
   const long long tb_shared = Is > 0 ? (c.T + 255) / 256 : 0;
-  const long long tiles = tb_routed * ((2LL * c.I + 255) / 256 + (c.d + 255) / 256) +
-                          tb_shared * ((2 * Is + 255) / 256 + (c.d + 255) / 256);
-  return cuda_status(launch_pair_experts(cls, offsets, c.E, Is > 0 ? c.T : 0, c.T, done, ws.status(), tiles, s,
+  const long long tiles1 = tb_routed * ((2LL * c.I + 255) / 256) + tb_shared * ((2 * Is + 255) / 256);
+  const long long tiles2 = (tb_routed + tb_shared) * ((c.d + 255) / 256);
+  const int shared_rows = Is > 0 ? c.T : 0;
+  if (fuse_expert_gemms(c)) {
+    // one launch: GEMM2 tiles start expert by expert while GEMM1 finishes
+    return cuda_status(launch_pair_experts(cls, offsets, c.E, shared_rows, c.T, 3, done, ws.status(),
+                                           tiles1 + tiles2, s, launches));
+  }
+  cudaError_t e = launch_pair_experts(cls, offsets, c.E, shared_rows, c.T, 1, nullptr, ws.status(), tiles1, s,
+                                      launches);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  return cuda_status(launch_pair_experts(cls, offsets, c.E, shared_rows, c.T, 2, nullptr, ws.status(), tiles2, s,
                                          launches));
 }
 
@@ -458,7 +474,7 @@ int32_t moe_forward_kernel_count(const moe_config* cfg) {
   int n = 2;                                                        // logits + top-k
   if (use_tc_gate(c) && c.gate_w_dtype == MOE_F32) n += 1;          // W_g split
   n += permute_launches(c.T) + 1;                                   // permute + gather
-  n += is_bf16(c) ? 1 : 2;                                          // expert GEMMs (fused on bf16)
+  n += is_bf16(c) ? (fuse_expert_gemms(c) ? 1 : 2) : 2;              // expert GEMMs
   n += 1;                                                           // combine
   return n;
 }

@@ -99,7 +99,8 @@ struct PairParams {
   const int32_t* offsets;
   int num_routed;
   int shared_rows;      // tokens of the shared expert (0: none)
-  int* done;            // [num_routed + 1] GEMM1 completion counters, zero at launch
+  int phases;           // bit 0: GEMM1 tiles, bit 1: GEMM2 tiles in this launch
+  int* done;            // [num_routed + 1] GEMM1 completion counters, zero at launch (both phases only)
   int* status;
   int stages;           // ring depth (3, or MAX_STAGES for decode-sized launches)
   int stage_bytes;      // bytes of one stage in this CTA's shared memory
@@ -188,9 +189,10 @@ __device__ void pair_schedule(PairCtrl* c, const PairParams& p, int lane) {
     c->tile_start[0][ng] = incl1;
     c->tile_start[1][ng] = incl2;
     // seg[0] = 0 and seg[1] = GEMM1 shared tiles were set at start-up
-    c->seg[2] = c->seg[1] + incl1;
-    c->seg[3] = c->seg[2] + (p.shared_rows > 0 ? pair_group_tiles(p, C2S, p.shared_rows) : 0);
-    c->seg[4] = c->seg[3] + incl2;
+    const bool g1 = p.phases & 1, g2 = p.phases & 2;
+    c->seg[2] = c->seg[1] + (g1 ? incl1 : 0);
+    c->seg[3] = c->seg[2] + (g2 && p.shared_rows > 0 ? pair_group_tiles(p, C2S, p.shared_rows) : 0);
+    c->seg[4] = c->seg[3] + (g2 ? incl2 : 0);
   }
 }
 
@@ -300,7 +302,7 @@ __device__ void pair_producer(PairCtrl* c, const PairParams& p, uint8_t* stages,
       pdl_wait();   // the permuted token rows come from the preceding grid
       waited = true;
     }
-    if ((t.cls == C2R || t.cls == C2S) && t.g != ready_group) {
+    if ((t.cls == C2R || t.cls == C2S) && p.phases == 3 && t.g != ready_group) {
       // the group's GEMM1 tiles (any cluster) have stored its hidden rows
       const int need = gemm1_need(p, t.cls == C2R ? C1R : C1S, t.rows);
       const unsigned long long t0 = globaltimer_ns();
@@ -468,7 +470,7 @@ __device__ void pair_epilogue(PairCtrl* c, const PairParams& p, uint32_t tmem, i
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive_remote(map_to_rank(smem_u32(&c->tempty[acc]), 0));
-    if (gemm1) {
+    if (gemm1 && p.phases == 3) {
       // publish this warp's part of the tile: the lanes' stores, then one
       // release increment of the group's counter.  The counters are zeroed by
       // the preceding grid, so the increment waits for the routed tables
@@ -503,7 +505,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     c->abort = 0;
     c->routed_ready = 0;
     c->seg[0] = 0;
-    c->seg[1] = p.shared_rows > 0 ? pair_group_tiles(p, C1S, p.shared_rows) : 0;
+    c->seg[1] = (p.phases & 1) && p.shared_rows > 0 ? pair_group_tiles(p, C1S, p.shared_rows) : 0;
     fence_mbar_init();
     pdl_launch_dependents();
   }
@@ -522,6 +524,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   // both CTAs' barriers and tensor memory are ready
   cluster_sync_all();
   tc_fence_after();
+  // A GEMM2-only launch reads the hidden rows of the preceding GEMM1 launch.
+  if (p.phases == 2) pdl_wait();
 
   const uint32_t tmem = c->tmem_base;
   if (warp == 0) {
@@ -580,10 +584,11 @@ cudaError_t launch_pair(const PairParams& p, long long max_tiles, cudaStream_t s
 }  // namespace
 
 cudaError_t launch_pair_experts(const PairClass cls[4], const int32_t* offsets, int num_routed, int shared_rows,
-                                int max_group_rows, int* done, int* status, long long max_tiles, cudaStream_t stream,
-                                int* launches) {
+                                int max_group_rows, int phases, int* done, int* status, long long max_tiles,
+                                cudaStream_t stream, int* launches) {
   if (max_tiles <= 0) return cudaSuccess;
-  if (num_routed < 1 || num_routed + 1 > MAX_GROUPS || done == nullptr) return cudaErrorInvalidValue;
+  if (num_routed < 1 || num_routed + 1 > MAX_GROUPS || phases < 1 || phases > 3) return cudaErrorInvalidValue;
+  if (phases == 3 && done == nullptr) return cudaErrorInvalidValue;
   PairParams p;
   memset(&p, 0, sizeof(p));
   for (int i = 0; i < NCLS; ++i) {
@@ -604,6 +609,7 @@ cudaError_t launch_pair_experts(const PairClass cls[4], const int32_t* offsets, 
   p.num_routed = num_routed;
   p.shared_rows = shared_rows;
   p.done = done;
+  p.phases = phases;
   p.status = status;
   // A group never holds more tokens than the batch, so with at most 64 tokens
   // every tile takes the 32-row token box: use the deeper ring of small stages.

@@ -89,15 +89,17 @@ struct PairClass {
   int64_t out_rows = 0;
 };
 
-// Both expert GEMMs in one launch.  cls = {GEMM1 routed, GEMM1 shared, GEMM2
-// routed, GEMM2 shared}; GEMM1 outputs bf16 silu(W1 x) * (W3 x) (W = packed
-// W1/W3 rows, 16-row interleave), GEMM2 fp32.  max_group_rows: an upper bound
-// of any group's rows (the batch size T).  done [num_routed + 1] must be zero
-// when the launch starts (per-group GEMM1 completion counters).  The shared
-// expert's GEMM1 tiles may run before the preceding grid completes.
+// The expert GEMMs.  cls = {GEMM1 routed, GEMM1 shared, GEMM2 routed, GEMM2
+// shared}; GEMM1 outputs bf16 silu(W1 x) * (W3 x) (W = packed W1/W3 rows,
+// 16-row interleave), GEMM2 fp32.  phases: 1 = GEMM1 tiles, 2 = GEMM2 tiles,
+// 3 = both in one launch, GEMM2 tiles of a group waiting on per-group GEMM1
+// completion counters done [num_routed + 1], which must then be zero when the
+// launch starts.  max_group_rows: an upper bound of any group's rows (the
+// batch size T).  The shared expert's GEMM1 tiles may run before the
+// preceding grid completes.
 cudaError_t launch_pair_experts(const PairClass cls[4], const int32_t* offsets, int num_routed, int shared_rows,
-                                int max_group_rows, int* done, int* status, long long max_tiles, cudaStream_t stream,
-                                int* launches);
+                                int max_group_rows, int phases, int* done, int* status, long long max_tiles,
+                                cudaStream_t stream, int* launches);
 
 // ---------------------------------------------------------------------- router
 cudaError_t launch_gate_split(const float* wg, int E, int d, void* wsplit, cudaStream_t s, int* launches);

@@ -184,9 +184,18 @@ def layer_bytes(wl, counts: np.ndarray) -> float:
     eb = 2 if wl.act_dtype == "bf16" else 4
     ob = 2 if wl.out_dtype == "bf16" else 4
     gb = 2 if wl.gate_w_dtype == "bf16" else 4
+    wb = expert_weight_bytes(wl)
     touched = int((counts > 0).sum())
     return (wl.T * wl.d * (eb + ob) + wl.E * wl.d * gb + wl.T * wl.k * 8
-            + touched * 3 * wl.d * wl.I * eb + 3 * wl.d * wl.I_s * eb)
+            + touched * 3 * wl.d * wl.I * wb + 3 * wl.d * wl.I_s * wb)
+
+
+def expert_weight_bytes(wl) -> float:
+    """Bytes per stored expert weight: the activation dtype, or one e4m3 byte
+    plus a 4-byte scale per 64 weights."""
+    if wl.expert_w_dtype == "fp8":
+        return 1.0 + 4.0 / 64.0
+    return 2 if wl.act_dtype == "bf16" else 4
 
 
 def experts_work(wl, counts: np.ndarray):
@@ -196,9 +205,10 @@ def experts_work(wl, counts: np.ndarray):
     shared expert, the hidden rows written and read back, the fp32 expert
     outputs written."""
     eb = 2 if wl.act_dtype == "bf16" else 4
+    wb = expert_weight_bytes(wl)
     flops = 6.0 * wl.R * wl.d * wl.I + 6.0 * wl.T * wl.d * wl.I_s
     touched = int((counts > 0).sum())
-    byts = ((wl.R + wl.T) * wl.d * eb + touched * 3 * wl.I * wl.d * eb + 3 * wl.I_s * wl.d * eb
+    byts = ((wl.R + wl.T) * wl.d * eb + touched * 3 * wl.I * wl.d * wb + 3 * wl.I_s * wl.d * wb
             + 2 * (wl.R * wl.I + wl.T * wl.I_s) * eb + (wl.R + wl.T) * wl.d * 4)
     return flops, byts
 
@@ -455,6 +465,7 @@ def run_ours(args, world, rank):
         "vs_baseline": None, "dtype": "bf16" if wl.act_dtype == "bf16" else "f32", "data": "synthetic",
         "config": {"workload": wl.name, "T": wl.T, "d": wl.d, "E": wl.E, "I": wl.I, "k": wl.k,
                    "n_shared": wl.n_shared, "router": f"{wl.score_fn}/{wl.topk_method}",
+                   "expert_weights": "fp8 e4m3, 64-wide blocks" if wl.expert_w_dtype == "fp8" else wl.act_dtype,
                    "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (expert weights and token batch exceed 126 MB)"
                    if wl.T * wl.d * 2 > 126e6 or wl.T >= 512 else "weights larger than L2; no flush"},

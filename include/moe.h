@@ -57,7 +57,7 @@ typedef enum moe_status {
   MOE_ERR_DEVICE_BOUNDS = 6    /* a device-side index was out of range           */
 } moe_status;
 
-typedef enum moe_dtype { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
+typedef enum moe_dtype { MOE_F32 = 0, MOE_BF16 = 1, MOE_FP8_E4M3 = 2 } moe_dtype;
 typedef enum moe_score_fn { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 } moe_score_fn;
 typedef enum moe_topk_method { MOE_TOPK_GREEDY = 0, MOE_TOPK_GROUP_LIMITED = 1 } moe_topk_method;
 typedef enum moe_group_score { MOE_GROUP_MAX = 0, MOE_GROUP_SUM_TOP = 1 } moe_group_score;
@@ -83,6 +83,13 @@ typedef struct moe_config {
   int32_t act_dtype;       /* moe_dtype of x, expert weights and rows */
   int32_t gate_w_dtype;    /* moe_dtype of W_g                        */
   int32_t out_dtype;       /* moe_dtype of the layer output h'        */
+  int32_t expert_w_dtype;  /* storage of the packed expert weights: act_dtype, or
+                              MOE_FP8_E4M3 (with MOE_BF16 activations): FP8
+                              e4m3 values with one power-of-two scale per 64
+                              consecutive weights of a row (intelliparadigm.com
+                              page section 4, block quantisation; d and I
+                              multiples of 128).  The GEMMs dequantize to bf16
+                              exactly and multiply on the bf16 tensor cores. */
 } moe_config;
 
 /* Bytes of workspace every compute call needs for `cfg`. */
@@ -95,8 +102,10 @@ MOE_API moe_status moe_packed_size(const moe_config* cfg, size_t* bytes);
  * SwiGLU experts + one shared SwiGLU of hidden I_s).
  *   W1, W3 [E,I,d], W2 [E,d,I]; Ws1, Ws3 [I_s,d], Ws2 [d,I_s]; act_dtype.
  *   `packed` (>= moe_packed_size bytes) receives W1/W3 rows interleaved in
- *   blocks so that one 256-wide GEMM tile holds matching gate and up rows, and
- *   copies of W2 / Ws2.  Inputs may be freed once the stream reaches this call. */
+ *   blocks of 16 so that one GEMM tile holds matching gate and up rows, and
+ *   W2 / Ws2; with expert_w_dtype = MOE_FP8_E4M3 every matrix is quantised
+ *   block by block on the way (1 byte per weight plus a 4-byte scale per 64).
+ *   Inputs may be freed once the stream reaches this call. */
 MOE_API moe_status moe_prepack_experts(const moe_config* cfg, const void* W1, const void* W3, const void* W2,
                                const void* Ws1, const void* Ws3, const void* Ws2,
                                void* packed, size_t packed_bytes, void* stream);

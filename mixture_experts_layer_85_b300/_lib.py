@@ -22,7 +22,7 @@ _lib = ctypes.CDLL(LIB_PATH)
 
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE, MOE_ERR_CUDA, \
     MOE_ERR_DEVICE_TIMEOUT, MOE_ERR_DEVICE_BOUNDS = range(7)
-MOE_F32, MOE_BF16 = 0, 1
+MOE_F32, MOE_BF16, MOE_FP8_E4M3 = 0, 1, 2
 MOE_SCORE_SOFTMAX, MOE_SCORE_SIGMOID = 0, 1
 MOE_TOPK_GREEDY, MOE_TOPK_GROUP_LIMITED = 0, 1
 MOE_GROUP_MAX, MOE_GROUP_SUM_TOP = 0, 1
@@ -40,7 +40,8 @@ class moe_config(ctypes.Structure):
                 ("topk_method", ctypes.c_int32), ("n_group", ctypes.c_int32), ("topk_group", ctypes.c_int32),
                 ("group_score", ctypes.c_int32), ("group_top", ctypes.c_int32), ("norm_topk", ctypes.c_int32),
                 ("routed_scaling_factor", ctypes.c_float), ("act_dtype", ctypes.c_int32),
-                ("gate_w_dtype", ctypes.c_int32), ("out_dtype", ctypes.c_int32)]
+                ("gate_w_dtype", ctypes.c_int32), ("out_dtype", ctypes.c_int32),
+                ("expert_w_dtype", ctypes.c_int32)]
 
 
 _P = ctypes.c_void_p
@@ -104,6 +105,7 @@ def make_config(wl, T: Optional[int] = None) -> moe_config:
     c.act_dtype = MOE_BF16 if wl.act_dtype == "bf16" else MOE_F32
     c.gate_w_dtype = MOE_BF16 if wl.gate_w_dtype == "bf16" else MOE_F32
     c.out_dtype = MOE_BF16 if wl.out_dtype == "bf16" else MOE_F32
+    c.expert_w_dtype = MOE_FP8_E4M3 if wl.expert_w_dtype == "fp8" else c.act_dtype
     return c
 
 

@@ -5,6 +5,8 @@
 // DeepSeek-V2 walkthrough sums the k routed expert outputs weighted by their
 // gates and adds the shared experts, fused as one SwiGLU of hidden
 // n_shared * I, evaluated on every token; no residual is added.
+#include <cuda_fp8.h>
+
 #include "internal.h"
 
 namespace moe {
@@ -24,6 +26,73 @@ __global__ void interleave_w13_kernel(const uint4* __restrict__ w1, const uint4*
     const int blk = p / (2 * bi), r = p % (2 * bi);
     const uint4* src = (r < bi ? w1 : w3) + ((g * H + (long long)blk * bi + (r % bi)) * vec_per_row);
     dst[i] = src[v];
+  }
+}
+
+// Block quantisation to FP8 e4m3 (intelliparadigm.com page, section 4): one
+// thread per run of 64 consecutive weights of an output row.  The scale is the
+// smallest power of two with max|w| <= 448 * scale (amax = f * 2^x with f in
+// [0.5, 1): 2^(x-9) when f <= 0.875, else 2^(x-8); 1 for an all-zero run), so
+// w / scale is exact and the e4m3 value times the scale is a bf16 number.
+// Output row p of a [G, R_out, cols] matrix comes from src_a (or, for the
+// interleaved W1/W3 layout, from W1 or W3 by the same rule as
+// interleave_w13_kernel).
+__global__ void quantize_fp8_kernel(const __nv_bfloat16* __restrict__ src_a, const __nv_bfloat16* __restrict__ src_b,
+                                    long long G, int H, int bi, int cols, uint8_t* __restrict__ dst_q,
+                                    float* __restrict__ dst_scale) {
+  const int nb = cols / 64;
+  const long long rows_out = src_b != nullptr ? G * 2LL * H : G * (long long)H;
+  const long long n = rows_out * nb;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+    const long long row = i / nb;
+    const int b = int(i % nb);
+    const __nv_bfloat16* src;
+    if (src_b != nullptr) {
+      const long long g = row / (2LL * H);
+      const int p = int(row % (2LL * H));
+      const int blk = p / (2 * bi), r = p % (2 * bi);
+      src = (r < bi ? src_a : src_b) + (g * H + (long long)blk * bi + (r % bi)) * cols;
+    } else {
+      src = src_a + row * cols;
+    }
+    const uint4* s4 = reinterpret_cast<const uint4*>(src + b * 64);
+    uint4 v[8];
+    float amax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      v[j] = s4[j];
+      const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&v[j]);
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const float2 f = __bfloat1622float2(h2[t]);
+        amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+      }
+    }
+    int x = 0;
+    const float f = frexpf(amax, &x);
+    const int e = amax == 0.0f ? 0 : (f <= 0.875f ? x - 9 : x - 8);
+    const float inv = ldexpf(1.0f, -e);   // exact power of two
+    uint32_t out[16];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&v[j]);
+      uint32_t lo = 0, hi = 0;
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const float2 w = __bfloat1622float2(h2[t]);
+        const uint32_t q0 = __nv_cvt_float_to_fp8(w.x * inv, __NV_SATFINITE, __NV_E4M3);
+        const uint32_t q1 = __nv_cvt_float_to_fp8(w.y * inv, __NV_SATFINITE, __NV_E4M3);
+        const uint32_t pair = q0 | (q1 << 8);
+        if (t < 2) lo |= pair << (16 * t);
+        else hi |= pair << (16 * (t - 2));
+      }
+      out[2 * j] = lo;
+      out[2 * j + 1] = hi;
+    }
+    uint4* d4 = reinterpret_cast<uint4*>(dst_q + row * cols + b * 64);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) d4[j] = make_uint4(out[4 * j], out[4 * j + 1], out[4 * j + 2], out[4 * j + 3]);
+    dst_scale[row * nb + b] = ldexpf(1.0f, e);
   }
 }
 
@@ -259,20 +328,27 @@ cudaError_t combine_typed(const moe_config& c, const uint4* yp, const uint4* ys,
 
 PackedLayout packed_layout(const moe_config& c) {
   PackedLayout L;
-  const size_t eb = dtype_bytes(c.act_dtype);
+  L.fp8 = c.expert_w_dtype == MOE_FP8_E4M3;
+  const size_t eb = L.fp8 ? 1 : dtype_bytes(c.act_dtype);
+  const size_t sb = L.fp8 ? 4 : 0;   // scale bytes per 64 weights
   const long long Is = (long long)c.n_shared * c.I;
   // blocks of 16 hidden units: W1 rows, then the W3 rows of the same units
   L.bi = (c.I % 16 == 0) ? 16 : c.I;
   L.bis = (Is % 16 == 0) ? 16 : int(Is > 0 ? Is : 1);
   size_t off = 0;
-  L.w13 = off;
-  off = align_up(off + size_t(c.E) * 2 * c.I * c.d * eb, 256);
-  L.w2 = off;
-  off = align_up(off + size_t(c.E) * c.d * c.I * eb, 256);
-  L.w13s = off;
-  off = align_up(off + size_t(2 * Is) * c.d * eb, 256);
-  L.w2s = off;
-  off = align_up(off + size_t(c.d) * Is * eb, 256);
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = align_up(off + bytes, 256);
+    return at;
+  };
+  L.w13 = take(size_t(c.E) * 2 * c.I * c.d * eb);
+  L.w13_sc = take(size_t(c.E) * 2 * c.I * (c.d / 64) * sb);
+  L.w2 = take(size_t(c.E) * c.d * c.I * eb);
+  L.w2_sc = take(size_t(c.E) * c.d * (c.I / 64) * sb);
+  L.w13s = take(size_t(2 * Is) * c.d * eb);
+  L.w13s_sc = take(size_t(2 * Is) * (c.d / 64) * sb);
+  L.w2s = take(size_t(c.d) * Is * eb);
+  L.w2s_sc = take(size_t(c.d) * (Is / 64) * sb);
   L.total = off;
   return L;
 }
@@ -286,6 +362,22 @@ cudaError_t launch_prepack(const moe_config& c, const void* W1, const void* W3, 
   char* base = static_cast<char*>(packed);
   const long long Is = (long long)c.n_shared * c.I;
   auto grid_for = [](long long n) { long long g = (n + 255) / 256; return int(g < 8192 ? g : 8192); };
+  if (L.fp8) {
+    using bf = __nv_bfloat16;
+    auto q = [&](const void* a, const void* b, long long G, int H, int bi, int cols, size_t off_q, size_t off_s) {
+      const long long rows = b != nullptr ? G * 2LL * H : G * (long long)H;
+      quantize_fp8_kernel<<<grid_for(rows * (cols / 64)), 256, 0, s>>>(
+          static_cast<const bf*>(a), static_cast<const bf*>(b), G, H, bi, cols,
+          reinterpret_cast<uint8_t*>(base + off_q), reinterpret_cast<float*>(base + off_s));
+      if (launches) ++*launches;
+      return cudaGetLastError();
+    };
+    cudaError_t e = q(W1, W3, c.E, c.I, L.bi, c.d, L.w13, L.w13_sc);
+    if (e == cudaSuccess) e = q(W2, nullptr, 1, c.E * c.d, 1, c.I, L.w2, L.w2_sc);
+    if (e == cudaSuccess && Is > 0) e = q(Ws1, Ws3, 1, int(Is), L.bis, c.d, L.w13s, L.w13s_sc);
+    if (e == cudaSuccess && Is > 0) e = q(Ws2, nullptr, 1, c.d, 1, int(Is), L.w2s, L.w2s_sc);
+    return e;
+  }
   interleave_w13_kernel<<<grid_for((long long)c.E * 2 * c.I * vec), 256, 0, s>>>(
       static_cast<const uint4*>(W1), static_cast<const uint4*>(W3), reinterpret_cast<uint4*>(base + L.w13), c.E, c.I,
       L.bi, vec);

@@ -50,6 +50,9 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
 #include "internal.h"
 #include "tc_ptx.cuh"
 
@@ -82,6 +85,12 @@ constexpr int MAX_GROUPS = 272;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_STRIDE = 256;  // columns between the two accumulators
 constexpr int EPI_WARPS = 4;
+// FP8 weights: converter warps dequantize each stage's e4m3 weight tile (one
+// 128-byte row of 128 weights per thread) into the bf16 A buffer.
+constexpr int CONV_WARPS = 4;
+constexpr int THREADS_FP8 = THREADS + 32 * CONV_WARPS;
+constexpr int F8_BYTES = PM * 128;    // one stage of e4m3 weights: 128 rows x 128 k
+constexpr int MAX_F8 = 8;
 
 // Operand classes: GEMM1 routed, GEMM1 shared, GEMM2 routed, GEMM2 shared.
 constexpr int C1R = 0, C1S = 1, C2R = 2, C2S = 3, NCLS = 4;
@@ -104,6 +113,11 @@ struct PairParams {
   int* status;
   int stages;           // ring depth (3, or MAX_STAGES for decode-sized launches)
   int stage_bytes;      // bytes of one stage in this CTA's shared memory
+  // FP8 weights
+  CUtensorMap tmW8[NCLS];   // e4m3 weights: 128 bytes x 128 rows boxes
+  const float* wsc[NCLS];   // block scales [w_rows, K / 64]
+  int nf;                   // e4m3 staging slots
+  int f8_off;               // byte offset of the staging ring
 };
 
 struct PairCtrl {
@@ -112,6 +126,8 @@ struct PairCtrl {
   uint64_t tfull[2];         // each CTA: an accumulator buffer is complete
   uint64_t tempty[2];        // rank 0: both CTAs' epilogues drained a buffer
   uint64_t drain;            // rank 0: every issued MMA completed
+  uint64_t f8_full[MAX_F8];  // FP8: an e4m3 weight tile landed (this CTA)
+  uint64_t f8_empty[MAX_F8]; // FP8: the converters released a staging slot (this CTA)
   uint32_t tmem_base;
   int abort;
   int seg[5];                // tile numbers where the four segments start, and the total
@@ -356,6 +372,193 @@ __device__ void pair_producer(PairCtrl* c, const PairParams& p, uint8_t* stages,
     if (issued & (1u << s)) pair_wait(&c->empty[s], (issued_par >> s) & 1u, c, peer_abort, p.status);
 }
 
+// Position of one stage in a CTA's tile sequence (used by the FP8 producer,
+// which runs two cursors over the same sequence).
+struct StageCursor {
+  int tile, ks, nks;
+  long long seq;   // stages before this one in the sequence
+  bool valid;
+  PairTile t;
+};
+
+__device__ __forceinline__ void cursor_load(StageCursor& cur, PairCtrl* c, const PairParams& p) {
+  cur.valid = pair_tile_exists(c, cur.tile, p.status);
+  if (cur.valid) {
+    cur.t = pair_tile(c, p, cur.tile);
+    cur.ks = 0;
+    cur.nks = (p.K[cur.t.cls] / BK + KB_STAGE - 1) / KB_STAGE;
+  }
+}
+
+__device__ __forceinline__ void cursor_next(StageCursor& cur, PairCtrl* c, const PairParams& p) {
+  ++cur.seq;
+  if (++cur.ks == cur.nks) {
+    cur.tile += (int)cluster_count_x();
+    cursor_load(cur, c, p);
+  }
+}
+
+__device__ __forceinline__ int weight_row(const PairParams& p, const PairTile& t, uint32_t rank) {
+  const bool routed = t.cls == C1R || t.cls == C2R;
+  return (routed ? t.g * p.w_step[t.cls] : 0) + t.fb * PAIR_M + int(rank) * PM;
+}
+
+// FP8 producer: the e4m3 weight tiles run up to nf stages ahead into the
+// staging ring (this CTA's own barriers); the token tiles follow the bf16
+// path into the stage ring, after the converters of both CTAs and the token
+// copies have filled a stage the MMA consumes it.
+__device__ void pair_producer_fp8(PairCtrl* c, const PairParams& p, uint8_t* stages, uint32_t rank,
+                                  uint32_t peer_abort) {
+  uint8_t* f8 = stages + p.f8_off;
+  StageCursor fc, bc;
+  fc.tile = bc.tile = (int)cluster_id_x();
+  fc.seq = bc.seq = 0;
+  cursor_load(fc, c, p);
+  cursor_load(bc, c, p);
+  bool waited = false;
+  int ready_group = -1;
+  bool ok = true;
+  unsigned long long idle_since = 0;
+  while (ok && bc.valid) {
+    bool did = false;
+    if (fc.valid && fc.seq < bc.seq + p.nf) {
+      const int slot = int(fc.seq % p.nf);
+      const uint32_t par = (uint32_t(fc.seq / p.nf) & 1u) ^ 1u;
+      if (mbar_try_wait(&c->f8_empty[slot], par)) {
+        mbar_arrive_expect_tx(&c->f8_full[slot], F8_BYTES);
+        tma_load_2d(f8 + size_t(slot) * F8_BYTES, &p.tmW8[fc.t.cls], &c->f8_full[slot], fc.ks * 128,
+                    weight_row(p, fc.t, rank));
+        cursor_next(fc, c, p);
+        did = true;
+      }
+    }
+    if (!did) {
+      const PairTile& t = bc.t;
+      if (bc.ks == 0) {
+        if (t.cls == C1R && !waited) {
+          pdl_wait();   // the permuted token rows come from the preceding grid
+          waited = true;
+        }
+        if ((t.cls == C2R || t.cls == C2S) && p.phases == 3 && t.g != ready_group) {
+          const int need = gemm1_need(p, t.cls == C2R ? C1R : C1S, t.rows);
+          if (ld_acquire_gpu(p.done + t.g) >= need) {
+            fence_proxy_async_global();
+            ready_group = t.g;
+          }
+        }
+      }
+      const bool dep_ok = !((t.cls == C2R || t.cls == C2S) && p.phases == 3 && t.g != ready_group);
+      const int stage = int(bc.seq % p.stages);
+      const uint32_t par = (uint32_t(bc.seq / p.stages) & 1u) ^ 1u;
+      if (dep_ok && mbar_try_wait(&c->empty[stage], par)) {
+        uint8_t* sa = stages + size_t(stage) * p.stage_bytes;
+        const bool small = t.n_mma / 2 <= XSMALL;
+        const CUtensorMap* xmap = small ? &p.tmXs[t.cls] : &p.tmX[t.cls];
+        const uint32_t bytes = 2u * uint32_t(KB_STAGE * (small ? XS_KB_BYTES : B_KB_BYTES));
+        if (rank == 0) mbar_arrive_expect_tx(&c->full[stage], bytes);
+        const uint32_t fb = map_to_rank(smem_u32(&c->full[stage]), 0);
+        const int x_row = t.row_start + t.tb * PN + int(rank) * (t.n_mma / 2);
+        tma_load_3d_pair(sa + A_BYTES, xmap, fb, x_row, bc.ks * KB_STAGE);
+        cursor_next(bc, c, p);
+        did = true;
+      }
+    }
+    if (did) {
+      idle_since = 0;
+    } else {
+      const unsigned long long now = globaltimer_ns();
+      if (idle_since == 0) idle_since = now;
+      if (*reinterpret_cast<volatile int*>(&c->abort)) ok = false;
+      if (now - idle_since > kWaitLimitNs) {
+        c->abort = 1;
+        st_remote_u32(peer_abort, 1u);
+        flag_status(p.status, DEV_TIMEOUT);
+        ok = false;
+      }
+    }
+  }
+  // every copy issued into the rings was consumed before this CTA may leave
+  const long long nf_done = fc.seq, nb_done = bc.seq;
+  for (int s = 0; s < p.nf && s < nf_done; ++s) {
+    const long long last = nf_done - 1 - ((nf_done - 1 - s) % p.nf);
+    pair_wait(&c->f8_empty[s], uint32_t(last / p.nf) & 1u, c, peer_abort, p.status);
+  }
+  for (int s = 0; s < p.stages && s < nb_done; ++s) {
+    const long long last = nb_done - 1 - ((nb_done - 1 - s) % p.stages);
+    pair_wait(&c->empty[s], uint32_t(last / p.stages) & 1u, c, peer_abort, p.status);
+  }
+}
+
+// FP8 converter warps: thread i of the four warps owns weight row i of this
+// CTA's 128.  Per stage it reads the row's 128 e4m3 bytes (128-byte swizzle),
+// multiplies by the two block scales (powers of two, so exact) and writes 128
+// bf16 values into the stage's A buffer in the MMA's swizzled K-major layout,
+// then hands the stage to the MMA issuer on the even CTA.
+__device__ void pair_converter(PairCtrl* c, const PairParams& p, uint8_t* stages, int cw, int lane, uint32_t rank,
+                               uint32_t peer_abort) {
+  uint8_t* f8 = stages + p.f8_off;
+  const int r = cw * 32 + lane;   // weight row within this CTA's 128
+  const int sw = r & 7;           // 128-byte swizzle phase of that row
+  long long seq = 0;
+  bool ok = true;
+  for (int tile = (int)cluster_id_x(); ok; tile += (int)cluster_count_x()) {
+    int exists = 0;
+    if (lane == 0) exists = pair_tile_exists(c, tile, p.status) ? 1 : 0;
+    if (!__shfl_sync(0xffffffffu, exists, 0)) break;
+    const PairTile t = pair_tile(c, p, tile);
+    const int K = p.K[t.cls];
+    const int nblk = K / 64;
+    const float* sc = p.wsc[t.cls] + (long long)(weight_row(p, t, rank) + r) * nblk;
+    const int nks = (K / BK + KB_STAGE - 1) / KB_STAGE;
+    for (int ks = 0; ks < nks; ++ks, ++seq) {
+      const int slot = int(seq % p.nf), stage = int(seq % p.stages);
+      int good = 1;
+      if (lane == 0) {
+        good = pair_wait(&c->f8_full[slot], uint32_t(seq / p.nf) & 1u, c, peer_abort, p.status) &&
+               pair_wait(&c->empty[stage], (uint32_t(seq / p.stages) & 1u) ^ 1u, c, peer_abort, p.status);
+      }
+      if (!__shfl_sync(0xffffffffu, good, 0)) {
+        ok = false;
+        break;
+      }
+      const float s0 = sc[2 * ks];
+      const float s1 = 2 * ks + 1 < nblk ? sc[2 * ks + 1] : 0.0f;
+      const uint8_t* src = f8 + size_t(slot) * F8_BYTES + r * 128;
+      uint8_t* dst = stages + size_t(stage) * p.stage_bytes + r * 128;
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch) {
+        // 16 weights k = 16 ch .. 16 ch + 15 of the stage
+        const uint4 q = *reinterpret_cast<const uint4*>(src + ((ch ^ sw) << 4));
+        const float scale = ch < 4 ? s0 : s1;
+        const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
+        uint32_t o[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2(__nv_fp8x2_storage_t(qw[i] & 0xffffu), __NV_E4M3);
+          const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2(__nv_fp8x2_storage_t(qw[i] >> 16), __NV_E4M3);
+          const float2 a = __half22float2(__half2(lo)), b = __half22float2(__half2(hi));
+          const __nv_bfloat162 x = __floats2bfloat162_rn(a.x * scale, a.y * scale);
+          const __nv_bfloat162 y = __floats2bfloat162_rn(b.x * scale, b.y * scale);
+          o[2 * i] = *reinterpret_cast<const uint32_t*>(&x);
+          o[2 * i + 1] = *reinterpret_cast<const uint32_t*>(&y);
+        }
+        // bf16 k-block ch / 4, 16-byte chunks 2 (ch % 4) and 2 (ch % 4) + 1 of row r
+        uint8_t* kb = dst + (ch >> 2) * A_KB_BYTES;
+        const int j = (ch & 3) * 2;
+        *reinterpret_cast<uint4*>(kb + ((j ^ sw) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<uint4*>(kb + (((j + 1) ^ sw) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+      }
+      // the tensor cores read the A buffer through the async proxy
+      fence_proxy_async_shared();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&c->f8_empty[slot]);
+        mbar_arrive_remote(map_to_rank(smem_u32(&c->full[stage]), 0));
+      }
+    }
+  }
+}
+
 __device__ void pair_mma(PairCtrl* c, const PairParams& p, uint8_t* stages, uint32_t tmem, uint32_t peer_abort) {
   int stage = 0;
   uint32_t phase = 0;
@@ -482,7 +685,8 @@ __device__ void pair_epilogue(PairCtrl* c, const PairParams& p, uint32_t tmem, i
   }
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
+template <bool FP8>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FP8 ? THREADS_FP8 : THREADS, 1)
     pair_gemm_kernel(const __grid_constant__ PairParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -494,8 +698,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < MAX_STAGES; ++s) {
-      mbar_init(&c->full[s], 1);
+      // FP8: the even CTA's producer (token bytes) and the converter warps of both CTAs
+      mbar_init(&c->full[s], FP8 ? 1 + 2 * CONV_WARPS : 1);
       mbar_init(&c->empty[s], 1);
+    }
+    if (FP8) {
+      for (int s = 0; s < MAX_F8; ++s) {
+        mbar_init(&c->f8_full[s], 1);
+        mbar_init(&c->f8_empty[s], CONV_WARPS);
+      }
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&c->tfull[a], 1);
@@ -514,6 +725,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       tma_prefetch_desc(&p.tmW[i]);
       tma_prefetch_desc(&p.tmX[i]);
       tma_prefetch_desc(&p.tmXs[i]);
+      if (FP8) tma_prefetch_desc(&p.tmW8[i]);
     }
   }
   if (warp == 1) {
@@ -529,11 +741,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 
   const uint32_t tmem = c->tmem_base;
   if (warp == 0) {
-    if (lane == 0) pair_producer(c, p, stages, rank, peer_abort);
+    if (lane == 0) {
+      if (FP8) pair_producer_fp8(c, p, stages, rank, peer_abort);
+      else pair_producer(c, p, stages, rank, peer_abort);
+    }
   } else if (warp == 1) {
     if (lane == 0 && rank == 0) pair_mma(c, p, stages, tmem, peer_abort);
   } else if (warp < 2 + EPI_WARPS) {
     pair_epilogue(c, p, tmem, warp, lane, rank, peer_abort);
+  } else if (warp >= THREADS / 32) {
+    pair_converter(c, p, stages, warp - THREADS / 32, lane, rank, peer_abort);
   } else {
     // scheduler warp: the routed tables need the dispatch offsets
     pdl_wait();
@@ -551,15 +768,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   }
 }
 
+template <bool FP8>
 cudaError_t launch_pair(const PairParams& p, long long max_tiles, cudaStream_t stream) {
+  constexpr int kThreads = FP8 ? THREADS_FP8 : THREADS;
   static int max_clusters = -1;
   if (max_clusters < 0) {
-    cudaError_t e = cudaFuncSetAttribute(pair_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(pair_gemm_kernel<FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          int(kPairSmem));
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * (num_sms() / 2), 1, 1);
-    cfg.blockDim = dim3(THREADS, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = kPairSmem;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeClusterDimension;
@@ -569,7 +788,7 @@ cudaError_t launch_pair(const PairParams& p, long long max_tiles, cudaStream_t s
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, pair_gemm_kernel, &cfg) != cudaSuccess || n <= 0) {
+    if (cudaOccupancyMaxActiveClusters(&n, pair_gemm_kernel<FP8>, &cfg) != cudaSuccess || n <= 0) {
       cudaGetLastError();
       n = num_sms() / 2;
     }
@@ -578,14 +797,14 @@ cudaError_t launch_pair(const PairParams& p, long long max_tiles, cudaStream_t s
   // every cluster must be resident at once: GEMM2 tiles wait for GEMM1 tiles
   // of other clusters
   const long long pairs = max_tiles < max_clusters ? max_tiles : max_clusters;
-  return launch_pdl(pair_gemm_kernel, dim3(int(2 * pairs)), dim3(THREADS), kPairSmem, stream, p);
+  return launch_pdl(pair_gemm_kernel<FP8>, dim3(int(2 * pairs)), dim3(kThreads), kPairSmem, stream, p);
 }
 
 }  // namespace
 
 cudaError_t launch_pair_experts(const PairClass cls[4], const int32_t* offsets, int num_routed, int shared_rows,
                                 int max_group_rows, int phases, int* done, int* status, long long max_tiles,
-                                cudaStream_t stream, int* launches) {
+                                cudaStream_t stream, int* launches, bool fp8) {
   if (max_tiles <= 0) return cudaSuccess;
   if (num_routed < 1 || num_routed + 1 > MAX_GROUPS || phases < 1 || phases > 3) return cudaErrorInvalidValue;
   if (phases == 3 && done == nullptr) return cudaErrorInvalidValue;
@@ -595,7 +814,14 @@ cudaError_t launch_pair_experts(const PairClass cls[4], const int32_t* offsets, 
     // without a shared expert its classes repeat the routed ones (never used)
     const PairClass& g = (shared_rows > 0 || i == C1R || i == C2R) ? cls[i] : cls[i - 1];
     if (g.K % BK != 0) return cudaErrorInvalidValue;
-    if (!encode_bf16_map(&p.tmW[i], g.W, g.w_rows, g.K, PM, KB_STAGE)) return cudaErrorInvalidValue;
+    if (fp8) {
+      // e4m3 bytes [w_rows, K], one 128-byte row of 128 weights per box row
+      if (g.W_scale == nullptr || g.K % 128 != 0) return cudaErrorInvalidValue;
+      if (!encode_tiled_map(&p.tmW8[i], g.W, g.w_rows, g.K, 1, PM, 1)) return cudaErrorInvalidValue;
+      p.wsc[i] = g.W_scale;
+    } else if (!encode_bf16_map(&p.tmW[i], g.W, g.w_rows, g.K, PM, KB_STAGE)) {
+      return cudaErrorInvalidValue;
+    }
     if (!encode_bf16_map(&p.tmX[i], g.X, g.x_rows, g.K, XB, KB_STAGE)) return cudaErrorInvalidValue;
     if (!encode_bf16_map(&p.tmXs[i], g.X, g.x_rows, g.K, XSMALL, KB_STAGE)) return cudaErrorInvalidValue;
     p.out[i] = g.out;
@@ -614,9 +840,20 @@ cudaError_t launch_pair_experts(const PairClass cls[4], const int32_t* offsets, 
   // A group never holds more tokens than the batch, so with at most 64 tokens
   // every tile takes the 32-row token box: use the deeper ring of small stages.
   const bool small = max_group_rows <= 2 * XSMALL;
-  p.stages = small ? MAX_STAGES : 3;
   p.stage_bytes = small ? SMALL_STAGE_BYTES : STAGE_BYTES;
-  cudaError_t e = launch_pair(p, max_tiles, stream);
+  cudaError_t e;
+  if (fp8) {
+    // two bf16 stages (A written by the converters, tokens by TMA) and a deep
+    // ring of e4m3 weight tiles behind them
+    p.stages = 2;
+    p.f8_off = 2 * p.stage_bytes;
+    p.nf = (RING_BYTES - p.f8_off) / F8_BYTES;
+    if (p.nf > MAX_F8) p.nf = MAX_F8;
+    e = launch_pair<true>(p, max_tiles, stream);
+  } else {
+    p.stages = small ? MAX_STAGES : 3;
+    e = launch_pair<false>(p, max_tiles, stream);
+  }
   if (e == cudaSuccess && launches) ++*launches;
   return e;
 }

@@ -432,10 +432,18 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 // dominates decode-sized steps).
 bool encode_bf16_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, uint32_t box_rows,
                      uint32_t box_kblocks) {
+  return encode_tiled_map(m, ptr, rows, cols, 2, box_rows, box_kblocks);
+}
+
+// bf16 (elem_bytes 2) or byte-sized (elem_bytes 1) elements; the box's inner
+// extent is always one 128-byte swizzle row (64 bf16 or 128 bytes).
+bool encode_tiled_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int elem_bytes,
+                      uint32_t box_rows, uint32_t box_kblocks) {
   struct Entry {
     const void* ptr;
     int64_t rows, cols;
     uint32_t box, kbs;
+    int eb;
     CUtensorMap map;
   };
   constexpr int kEntries = 64;
@@ -447,7 +455,8 @@ bool encode_bf16_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols
     std::lock_guard<std::mutex> lock(mu);
     for (int i = 0; i < filled; ++i) {
       const Entry& e = table[i];
-      if (e.ptr == ptr && e.rows == rows && e.cols == cols && e.box == box_rows && e.kbs == box_kblocks) {
+      if (e.ptr == ptr && e.rows == rows && e.cols == cols && e.box == box_rows && e.kbs == box_kblocks &&
+          e.eb == elem_bytes) {
         *m = e.map;
         return true;
       }
@@ -455,24 +464,25 @@ bool encode_bf16_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols
   }
   auto enc = tensor_map_encoder();
   if (enc == nullptr) return false;
+  if (elem_bytes != 1 && elem_bytes != 2) return false;
+  const CUtensorMapDataType dt = elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  const cuuint32_t inner = 128u / cuuint32_t(elem_bytes);
   CUresult r;
   if (box_kblocks <= 1) {
     cuuint64_t dims[2] = {cuuint64_t(cols), cuuint64_t(rows)};
-    cuuint64_t strides[1] = {cuuint64_t(cols) * 2};
-    cuuint32_t box[2] = {64u, box_rows};
+    cuuint64_t strides[1] = {cuuint64_t(cols) * elem_bytes};
+    cuuint32_t box[2] = {inner, box_rows};
     cuuint32_t es[2] = {1u, 1u};
-    r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    r = enc(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   } else {
-    if (cols % 64 != 0) return false;
-    cuuint64_t dims[3] = {64u, cuuint64_t(rows), cuuint64_t(cols / 64)};
-    cuuint64_t strides[2] = {cuuint64_t(cols) * 2, 128u};
-    cuuint32_t box[3] = {64u, box_rows, box_kblocks};
+    if (cols % inner != 0) return false;
+    cuuint64_t dims[3] = {inner, cuuint64_t(rows), cuuint64_t(cols / inner)};
+    cuuint64_t strides[2] = {cuuint64_t(cols) * elem_bytes, 128u};
+    cuuint32_t box[3] = {inner, box_rows, box_kblocks};
     cuuint32_t es[3] = {1u, 1u, 1u};
-    r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    r = enc(m, dt, 3, const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   }
   if (r != CUDA_SUCCESS) return false;
   std::lock_guard<std::mutex> lock(mu);
@@ -482,6 +492,7 @@ bool encode_bf16_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols
   e.cols = cols;
   e.box = box_rows;
   e.kbs = box_kblocks;
+  e.eb = elem_bytes;
   e.map = *m;
   next = (next + 1) % kEntries;
   if (filled < kEntries) ++filled;

@@ -63,6 +63,10 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 // (box_kblocks = 1: a plain 2-D map).  Cached by argument.
 bool encode_bf16_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, uint32_t box_rows,
                      uint32_t box_kblocks);
+// The same for elem_bytes 1 (bytes: FP8 weights) or 2 (bf16); the inner box
+// extent is one 128-byte row.
+bool encode_tiled_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int elem_bytes,
+                      uint32_t box_rows, uint32_t box_kblocks);
 
 // Records the next armed profiling event on `s` (no-op when disarmed).
 void profile_mark(cudaStream_t s);
@@ -78,6 +82,7 @@ cudaError_t launch_grouped_gemm(int epi, const GemmClass& c0, const GemmClass* c
 // offsets[g+1]; class 1: one group of shared_rows rows), both bf16 K-major.
 struct PairClass {
   const void* W = nullptr;
+  const float* W_scale = nullptr;   // FP8 weights: scales [w_rows, K / 64] (W is then e4m3 bytes)
   int64_t w_rows = 0;
   const void* X = nullptr;
   int64_t x_rows = 0;
@@ -97,9 +102,11 @@ struct PairClass {
 // launch starts.  max_group_rows: an upper bound of any group's rows (the
 // batch size T).  The shared expert's GEMM1 tiles may run before the
 // preceding grid completes.
+// fp8: the weights are e4m3 blocks (PairClass::W_scale), dequantized to bf16
+// in shared memory by converter warps before each MMA.
 cudaError_t launch_pair_experts(const PairClass cls[4], const int32_t* offsets, int num_routed, int shared_rows,
                                 int max_group_rows, int phases, int* done, int* status, long long max_tiles,
-                                cudaStream_t stream, int* launches);
+                                cudaStream_t stream, int* launches, bool fp8 = false);
 
 // ---------------------------------------------------------------------- router
 cudaError_t launch_gate_split(const float* wg, int E, int d, void* wsplit, cudaStream_t s, int* launches);
@@ -138,8 +145,12 @@ cudaError_t launch_balance_update(const moe_config& c, const int32_t* counts, fl
                                   int* status, cudaStream_t s, int* launches);
 
 // Packed expert blob layout (byte offsets, each 256-byte aligned).
+// FP8 layout (expert_w_dtype = MOE_FP8_E4M3): each matrix is stored as e4m3
+// bytes [rows, cols] followed by fp32 scales [rows, cols / 64] (offsets *_sc).
 struct PackedLayout {
   size_t w13 = 0, w2 = 0, w13s = 0, w2s = 0, total = 0;
+  size_t w13_sc = 0, w2_sc = 0, w13s_sc = 0, w2s_sc = 0;
+  bool fp8 = false;
   int bi = 0, bis = 0;   // interleave block of W1/W3 rows (routed, shared)
 };
 PackedLayout packed_layout(const moe_config& c);

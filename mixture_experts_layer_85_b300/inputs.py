@@ -64,6 +64,7 @@ class Workload:
     gate_w_dtype: str = "f32"            # "f32" | "bf16"
     bias: str = "none"                   # "none" | "normal0.1" | "zipf"
     out_dtype: str = "f32"               # layer output h' ("f32": the listing's fp32 weighted sum)
+    expert_w_dtype: str = "act"          # packed expert weights: "act" (as activations) | "fp8" (e4m3 blocks)
 
     @property
     def I_s(self) -> int:
@@ -103,6 +104,14 @@ for _w in [
     _v3(1, "zipf"), _v3(8, "zipf"), _v3(64, "zipf"), _v3(512, "zipf"),
 ]:
     WORKLOADS[_w.name] = _w
+
+# FP8 expert weights (e4m3 blocks of 64 with power-of-two scales) of the
+# decode and prefill layers.
+for _T in (1, 8, 64, 512):
+    _w = replace(WORKLOADS[f"v3_decode_t{_T}"], name=f"v3_decode_fp8_t{_T}", expert_w_dtype="fp8")
+    WORKLOADS[_w.name] = _w
+WORKLOADS["v3_prefill_fp8_t16384"] = replace(WORKLOADS["v3_prefill_t16384"], name="v3_prefill_fp8_t16384",
+                                             expert_w_dtype="fp8")
 
 # A V3-shaped layer cut to 8 experts and 1024 tokens (1.4 GB of weights):
 # the case the kernel profiler captures, still larger than L2.

@@ -20,6 +20,9 @@ What it computes (one token u_t at a time, all in float64 unless stated):
      no residual term.
   8. after a step (training-time load balancing): the selection bias of
      every expert moves by gamma toward balance, and the load statistics.
+  9. FP8 expert weights: each run of 64 consecutive weights along a row is
+     stored as FP8 e4m3 values times one power-of-two scale; the layer then
+     computes steps 1-7 with the dequantized weights.
 
 Sources (page title, section):
   * "DeepSeek-V2" walkthrough (xingfushuangcheng.com): the DeepSeekMoE output
@@ -39,6 +42,10 @@ Sources (page title, section):
     that of an underloaded expert raised by gamma.
   * Tencent Cloud page, the balance-loss listing: load = per-expert counts of
     the top-k choices normalised to sum 1, and its standard deviation.
+  * intelliparadigm.com page, section 4 (FP8 quantisation): weights quantised
+    block by block (a block of 64 consecutive values, its own scale from the
+    block's largest magnitude), experts quantised independently, GEMM inputs
+    dequantised before the multiplication, accumulation in higher precision.
 
 Readings where the pages are silent or garbled (all listed in the design doc):
   * Decision precision.  The ``MoEGate`` listing holds logits and scores in
@@ -55,6 +62,11 @@ Readings where the pages are silent or garbled (all listed in the design doc):
     T*k/E, decided exactly on integers; an expert at exactly the mean keeps its
     bias.  The bias is float32 and moves by one float32 addition.  The load
     standard deviation is the unbiased one (the listing's torch .std()).
+  * FP8 weights (step 9): the section's listing rounds to an integer range
+    (+-127) although it is titled FP8; here the values are FP8 e4m3 (largest
+    finite 448, round to nearest even) and each block's scale is the smallest
+    power of two with max|w| <= 448 * scale, so a dequantized weight is exactly
+    a bf16 number.
   * A token is a near tie when the k-th and (k+1)-th eligible selection scores
     (or the topk_group-th and next group scores) differ by less than 1e-5 times
     the largest |score| of that token; its expert set may legitimately differ
@@ -396,3 +408,52 @@ def balance_update(counts, bias32, gamma: float):
         stats[1] = c.max() / mean
         stats[2] = c.min() / mean
     return new, stats
+
+
+# --------------------------------------------------------- FP8 expert weights
+
+E4M3_MAX = 448.0
+FP8_BLOCK = 64
+
+
+def e4m3_round(v: np.ndarray) -> np.ndarray:
+    """Nearest FP8 e4m3 value of each float64 (ties to even mantissa), for
+    |v| <= 448.  e4m3: sign, 4 exponent bits (bias 7), 3 mantissa bits; normal
+    values from 2^-6 up, subnormals are multiples of 2^-9."""
+    v = np.asarray(v, np.float64)
+    a = np.abs(v)
+    _, x = np.frexp(np.where(a > 0, a, 1.0))       # a = f * 2^x, f in [0.5, 1)
+    e = np.maximum(x - 1, -6)                       # binade 2^e <= a < 2^(e+1), clamped to the subnormal step
+    step = np.ldexp(1.0, (e - 3).astype(np.int64))  # spacing of e4m3 values in that binade
+    q = np.round(a / step) * step                   # a / step is exact; np.round ties to even
+    return np.copysign(np.minimum(q, E4M3_MAX), v)
+
+
+def quantize_fp8_blocks(w: np.ndarray):
+    """Step 9: w [rows, cols] (cols a multiple of 64) -> (q, scale): q [rows, cols]
+    the e4m3 values, scale [rows, cols/64] the blocks' powers of two, with
+    w ~= q * scale.  The scale is the smallest power of two with
+    max|w| <= 448 * scale over the block (1 for an all-zero block)."""
+    w = np.asarray(w, np.float64)
+    rows, cols = w.shape
+    blocks = w.reshape(rows, cols // FP8_BLOCK, FP8_BLOCK)
+    amax = np.abs(blocks).max(axis=2)
+    f, x = np.frexp(amax)                           # amax = f * 2^x
+    # amax <= 448 * 2^e  <=>  f * 2^x <= 1.75 * 2^(8 + e)
+    e = np.where(f <= 0.875, x - 9, x - 8)
+    e = np.where(amax == 0, 0, e).astype(np.int64)
+    scale = np.ldexp(1.0, e)
+    q = e4m3_round(blocks / scale[..., None])
+    return q.reshape(rows, cols), scale
+
+
+def dequantize_fp8_blocks(q: np.ndarray, scale: np.ndarray) -> np.ndarray:
+    rows, cols = q.shape
+    return (np.asarray(q, np.float64).reshape(rows, cols // FP8_BLOCK, FP8_BLOCK)
+            * np.asarray(scale, np.float64)[..., None]).reshape(rows, cols)
+
+
+def fp8_dequantized(w: np.ndarray) -> np.ndarray:
+    """The weights the FP8 layer computes with (step 9)."""
+    q, s = quantize_fp8_blocks(w)
+    return dequantize_fp8_blocks(q, s)

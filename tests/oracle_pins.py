@@ -11,7 +11,10 @@ Every check raises AssertionError when the oracle disagrees with:
     Tencent Cloud page, greedy == torch.topk on float64 scores;
   * symmetries: expert relabelling, token independence, linearity in W2;
   * the balancing step (bias +/- gamma, load statistics) against hand-worked
-    counts, closed forms and exact rational rounding bounds.
+    counts, closed forms and exact rational rounding bounds;
+  * the FP8 block quantisation against torch's float8_e4m3fn conversion, the
+    minimality of the power-of-two scale, the e4m3 error bound and exactness
+    in bf16.
 
 The independent pieces (softmax via scipy, SwiGLU via torch.nn.functional)
 never call the oracle's own helpers.  ``tests/test_oracle_mutations.py``
@@ -359,7 +362,43 @@ def pin_balance_update(o=orc):
             assert abs(st[1] - c.max() * E / tot) < 1e-12 and abs(st[2] - c.min() * E / tot) < 1e-12
 
 
+def pin_fp8_quantization(o=orc):
+    """intelliparadigm.com section 4: blocks of 64 values, one scale per block;
+    e4m3 values (torch's float8_e4m3fn cast rounds to nearest even)."""
+    r = _rng(31)
+    # e4m3 rounding of values inside the format's range agrees with torch's cast
+    v = np.concatenate([r.uniform(-448, 448, 4000), r.uniform(-1, 1, 4000), r.uniform(-2 ** -6, 2 ** -6, 4000),
+                        np.array([0.0, 448.0, -448.0, 240.0, 232.0, 1.0625, 1.1875, 2 ** -10, 3 * 2 ** -10])])
+    want = torch.tensor(v).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(o.e4m3_round(v), want)
+    # blocks: bf16-valued weights of very different magnitudes, one zero block
+    w = (r.standard_normal((6, 256)) * np.exp2(r.integers(-12, 4, (6, 1)))).astype(np.float32)
+    w = torch.tensor(w).to(torch.bfloat16).double().numpy()
+    w[2, 64:128] = 0.0
+    q, s = o.quantize_fp8_blocks(w)
+    assert q.shape == w.shape and s.shape == (6, 4)
+    amax = np.abs(w.reshape(6, 4, 64)).max(2)
+    nz = amax > 0
+    # smallest power of two that brings the block inside +-448
+    assert np.all(np.log2(s) == np.round(np.log2(s)))
+    assert np.all(amax[nz] <= 448 * s[nz]) and np.all(amax[nz] > 224 * s[nz])
+    assert s[2, 1] == 1.0 and np.all(q[2, 64:128] == 0)
+    # every q is an e4m3 value, and the dequantized weight is a bf16 number
+    assert np.array_equal(torch.tensor(q).to(torch.float8_e4m3fn).to(torch.float64).numpy(), q)
+    wd = o.dequantize_fp8_blocks(q, s)
+    assert np.array_equal(torch.tensor(wd).to(torch.bfloat16).double().numpy(), wd)
+    # error: at most half an e4m3 spacing of the value's binade (3 mantissa bits)
+    sc = np.repeat(s, 64, axis=1)
+    a = np.abs(w) / sc
+    _, x = np.frexp(np.where(a > 0, a, 1.0))
+    half_step = np.ldexp(1.0, np.maximum(x - 1, -6) - 4) * sc
+    assert np.all(np.abs(wd - w) <= half_step)
+    # values already of the form e4m3 * 2^k come back unchanged
+    exact = np.tile(np.array([448.0, -1.0, 0.125, 3.5] * 16), (1, 1)) * 2.0 ** -5
+    assert np.array_equal(o.fp8_dequantized(exact), exact)
+
+
 ALL_PINS = [pin_brute_force_selection, pin_greedy_is_torch_topk, pin_invariants,
             pin_bias_only_steers_selection, pin_zero_gates_give_shared, pin_group1_is_greedy,
             pin_single_expert, pin_dense_einsum, pin_top1, pin_permutation, pin_symmetries, pin_combine,
-            pin_balance_update]
+            pin_balance_update, pin_fp8_quantization]

@@ -317,3 +317,104 @@ def test_balance_update(case):
     assert np.array_equal(_np(bias), want_b)
     got_s = _np(stats)[:3].astype(np.float64)
     assert np.allclose(got_s, want_s, rtol=1e-6, atol=1e-9), (got_s, want_s)
+
+
+# ------------------------------------------------------------ FP8 expert weights
+
+def _fp8_copy(wl):
+    return inputs.small_workload(wl, name=wl.name + "_fp8", expert_w_dtype="fp8")
+
+
+def _split_fp8_blob(packed, shape_rows, cols, off_q, off_s):
+    """e4m3 values and scales of one packed matrix, read back as float64."""
+    q = packed[off_q: off_q + shape_rows * cols].view(torch.float8_e4m3fn).to(torch.float64)
+    s = packed[off_s: off_s + shape_rows * (cols // 64) * 4].view(torch.float32).to(torch.float64)
+    return q.view(shape_rows, cols).cpu().numpy(), s.view(shape_rows, cols // 64).cpu().numpy()
+
+
+def test_fp8_prepack_matches_oracle_quantization():
+    """moe_prepack_experts with FP8 weights: e4m3 bytes and block scales of every
+    matrix bit for bit equal to the oracle's block quantisation (W2 and the
+    shared W2 here; W1/W3 rows are the same rule in the interleaved order)."""
+    wl = _fp8_copy(SMALL["v3_small_t333"])
+    cfg = _lib.make_config(wl)
+    w1, w3, w2, ws1, ws3, ws2 = inputs.make_experts(wl, "cuda")
+    packed = torch.empty(_lib.moe_packed_size(cfg), dtype=torch.uint8, device="cuda")
+    _lib.moe_prepack_experts(cfg, w1, w3, w2, ws1, ws3, ws2, packed)
+    torch.cuda.synchronize()
+    E, I, d, Is = wl.E, wl.I, wl.d, wl.I_s
+    al = lambda v: (v + 255) // 256 * 256
+    o_w13 = 0
+    o_w13sc = al(o_w13 + E * 2 * I * d)
+    o_w2 = al(o_w13sc + E * 2 * I * (d // 64) * 4)
+    o_w2sc = al(o_w2 + E * d * I)
+    o_w13s = al(o_w2sc + E * d * (I // 64) * 4)
+    o_w13ssc = al(o_w13s + 2 * Is * d)
+    o_w2s = al(o_w13ssc + 2 * Is * (d // 64) * 4)
+    o_w2ssc = al(o_w2s + d * Is)
+    assert al(o_w2ssc + d * (Is // 64) * 4) == packed.numel()
+    q, s = _split_fp8_blob(packed, E * d, I, o_w2, o_w2sc)
+    wq, ws = orc.quantize_fp8_blocks(f64(w2).reshape(E * d, I))
+    assert np.array_equal(q, wq) and np.array_equal(s, ws)
+    q, s = _split_fp8_blob(packed, d, Is, o_w2s, o_w2ssc)
+    wq, ws = orc.quantize_fp8_blocks(f64(ws2))
+    assert np.array_equal(q, wq) and np.array_equal(s, ws)
+    # W13: rows in the 16-row interleave (16 W1 rows, then the 16 W3 rows of the same units)
+    q, s = _split_fp8_blob(packed, E * 2 * I, d, o_w13, o_w13sc)
+    w13 = torch.stack([w1, w3], 1).view(E, 2, I // 16, 16, d).transpose(1, 2).reshape(E * 2 * I, d)
+    wq, ws = orc.quantize_fp8_blocks(f64(w13))
+    assert np.array_equal(q, wq) and np.array_equal(s, ws)
+
+
+def _dq(t):
+    """FP8 block dequantisation of one matrix (what the FP8 layer computes with)."""
+    return orc.fp8_dequantized(f64(t))
+
+
+def _dequantized_accessor(li):
+    """Per-expert dequantised float64 weights, made lazily one expert at a time
+    (a full-size layer's weights would not fit in host memory as float64)."""
+    cache = {}
+
+    def get(e):
+        if e not in cache:
+            cache.clear()
+            cache[e] = (_dq(li.w1[e]), _dq(li.w3[e]), _dq(li.w2[e]))
+        return cache[e]
+    return get
+
+
+def _dequantized_shared(li):
+    return _dq(li.ws1), _dq(li.ws3), _dq(li.ws2)
+
+
+@pytest.mark.parametrize("name", ["v3_small_t333", "v2lite_small_t1037", "v3_small_t1", "v3_small_t3",
+                                  "v3_small_t1100"])
+def test_fp8_layer_matches_oracle_on_dequantized_weights(name):
+    wl = _fp8_copy(SMALL[name])
+    li = inputs.make_inputs(wl, "cuda")
+    _, out, idx, w, counts = run_layer(wl, li)
+    r = oracle_route(li, wl)
+    check_routing(_np(idx), _np(w), r, wl)
+    keep = np.array([np.array_equal(np.sort(_np(idx)[t]), np.sort(r.idx[t])) for t in range(wl.T)])
+    toks = np.arange(wl.T)[keep]
+    want = orc.experts_forward(f64(li.x)[toks], r.idx[toks], r.gates[toks], _dequantized_accessor(li),
+                               _dequantized_shared(li), wl.E)
+    assert orc.relative_error(f64(out)[toks], want) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("name", ["v3_decode_t1", "v3_decode_t64"])
+def test_fp8_full_size_decode(name):
+    wl = _fp8_copy(W[name])
+    li = inputs.make_inputs(wl, "cuda")
+    _, out, idx, w, counts = run_layer(wl, li)
+    r = oracle_route(li, wl)
+    check_routing(_np(idx), _np(w), r, wl)
+    sample = np.sort(np.random.default_rng(7).choice(wl.T, min(wl.T, 12), replace=False))
+    keep = np.array([np.array_equal(np.sort(_np(idx)[t]), np.sort(r.idx[t])) for t in sample])
+    toks = sample[keep]
+    want = orc.experts_forward(f64(li.x)[toks], r.idx[toks], r.gates[toks], _dequantized_accessor(li),
+                               _dequantized_shared(li), wl.E)
+    assert orc.relative_error(f64(out)[toks], want) <= TOL["bf16"]
+    del li, out
+    torch.cuda.empty_cache()

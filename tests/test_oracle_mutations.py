@@ -16,6 +16,8 @@ _real_experts_forward = orc.experts_forward
 _real_permutation = orc.permutation
 _real_combine = orc.combine
 _real_balance = orc.balance_update
+_real_e4m3 = orc.e4m3_round
+_real_quant = orc.quantize_fp8_blocks
 
 
 def _route_ties_high(logits, bias, cfg):
@@ -116,6 +118,26 @@ def _balance_mean_counts_as_over(counts, bias32, gamma):
     return nb, st
 
 
+def _e4m3_ties_away(v):
+    # round half away from zero instead of to even
+    v = np.asarray(v, np.float64)
+    a = np.abs(v)
+    _, x = np.frexp(np.where(a > 0, a, 1.0))
+    step = np.ldexp(1.0, (np.maximum(x - 1, -6) - 3).astype(np.int64))
+    return np.copysign(np.minimum(np.floor(a / step + 0.5) * step, 448.0), v)
+
+
+def _quant_scale_from_127(w):
+    # the listing's integer range taken literally: scale = 2^ceil(log2(amax / 127))
+    w = np.asarray(w, np.float64)
+    rows, cols = w.shape
+    b = w.reshape(rows, cols // 64, 64)
+    amax = np.abs(b).max(2)
+    e = np.where(amax > 0, np.ceil(np.log2(np.where(amax > 0, amax, 1.0) / 127.0)), 0.0)
+    s = np.exp2(e)
+    return orc.e4m3_round(b / s[..., None]).reshape(rows, cols), s
+
+
 MUTANTS = [
     ("route", _route_ties_high, pins.pin_brute_force_selection),
     ("route", _route_biased_gates, pins.pin_bias_only_steers_selection),
@@ -132,6 +154,8 @@ MUTANTS = [
     ("balance_update", _balance_wrong_direction, pins.pin_balance_update),
     ("balance_update", _balance_biased_std, pins.pin_balance_update),
     ("balance_update", _balance_mean_counts_as_over, pins.pin_balance_update),
+    ("e4m3_round", _e4m3_ties_away, pins.pin_fp8_quantization),
+    ("quantize_fp8_blocks", _quant_scale_from_127, pins.pin_fp8_quantization),
 ]
 
 

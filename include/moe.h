@@ -104,7 +104,12 @@ MOE_API moe_status moe_packed_size(const moe_config* cfg, size_t* bytes);
  *   `packed` (>= moe_packed_size bytes) receives W1/W3 rows interleaved in
  *   blocks of 16 so that one GEMM tile holds matching gate and up rows, and
  *   W2 / Ws2; with expert_w_dtype = MOE_FP8_E4M3 every matrix is quantised
- *   block by block on the way (1 byte per weight plus a 4-byte scale per 64).
+ *   block by block on the way and stored as the expert GEMM's shared-memory
+ *   images: per tile of 128 rows (same row order), cols/128 stage blocks of
+ *   17408 bytes, each the tile's 128 x 128 e4m3 values (row r at byte r*128,
+ *   its 16-byte chunk c at chunk position c ^ (r % 8)) followed by their fp32
+ *   scales [2][128] (64-value block h of row r at [h][r]); a zero tile
+ *   follows each matrix's last row.  FP8 needs d and I multiples of 128.
  *   Inputs may be freed once the stream reaches this call. */
 MOE_API moe_status moe_prepack_experts(const moe_config* cfg, const void* W1, const void* W3, const void* W2,
                                const void* Ws1, const void* Ws3, const void* Ws2,

@@ -102,7 +102,8 @@ moe_status check_config(const moe_config* cp) {
   if (c.gate_w_dtype != MOE_F32 && c.gate_w_dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
   if (c.out_dtype != MOE_F32 && c.out_dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
   if (c.expert_w_dtype != c.act_dtype && c.expert_w_dtype != MOE_FP8_E4M3) return MOE_ERR_INVALID_ARG;
-  if (c.expert_w_dtype == MOE_FP8_E4M3 && (c.act_dtype != MOE_BF16 || c.d % 128 != 0)) return MOE_ERR_UNSUPPORTED;
+  if (c.expert_w_dtype == MOE_FP8_E4M3 && (c.act_dtype != MOE_BF16 || c.d % 128 != 0 || c.I % 128 != 0))
+    return MOE_ERR_UNSUPPORTED;
   if (c.score_fn != MOE_SCORE_SOFTMAX && c.score_fn != MOE_SCORE_SIGMOID) return MOE_ERR_INVALID_ARG;
   if (c.topk_method != MOE_TOPK_GREEDY && c.topk_method != MOE_TOPK_GROUP_LIMITED) return MOE_ERR_INVALID_ARG;
   if (c.k > c.E) return MOE_ERR_INVALID_ARG;
@@ -210,22 +211,17 @@ moe_status run_experts(const moe_config& c, const void* x_perm, const int32_t* o
   PairClass cls[4];
   // GEMM1 + SwiGLU: H[rows, I] = silu(X W1^T) * (X W3^T), packed W1/W3 rows [2I, d] per expert
   const bool fp8 = P.fp8;
-  auto sc = [&](size_t off) { return fp8 ? reinterpret_cast<const float*>(pb + off) : nullptr; };
   PairClass& r1 = cls[0];
-  r1.W_scale = sc(P.w13_sc);
   r1.W = pb + P.w13; r1.w_rows = 2LL * c.E * c.I; r1.X = x_perm; r1.x_rows = R; r1.K = c.d;
   r1.M = 2 * c.I; r1.w_step = 2 * c.I; r1.out = h; r1.ld_out = c.I; r1.out_rows = R;
   PairClass& s1 = cls[1];
-  s1.W_scale = sc(P.w13s_sc);
   s1.W = pb + P.w13s; s1.w_rows = 2 * Is; s1.X = x; s1.x_rows = c.T; s1.K = c.d;
   s1.M = int(2 * Is); s1.w_step = 0; s1.out = hs; s1.ld_out = Is; s1.out_rows = c.T;
   // GEMM2: Y[rows, d] = H W2^T (fp32), W2 [d, I] per expert
   PairClass& r2 = cls[2];
-  r2.W_scale = sc(P.w2_sc);
   r2.W = pb + P.w2; r2.w_rows = (long long)c.E * c.d; r2.X = h; r2.x_rows = R; r2.K = c.I;
   r2.M = c.d; r2.w_step = c.d; r2.out = y_perm; r2.ld_out = c.d; r2.out_rows = R;
   PairClass& s2 = cls[3];
-  s2.W_scale = sc(P.w2s_sc);
   s2.W = pb + P.w2s; s2.w_rows = c.d; s2.X = hs; s2.x_rows = c.T; s2.K = int(Is);
   s2.M = c.d; s2.w_step = 0; s2.out = y_shared; s2.ld_out = c.d; s2.out_rows = c.T;
   // upper bound of the pair tiles (256 tokens x 256 weight rows), for sizing the grid

@@ -37,15 +37,23 @@ __global__ void interleave_w13_kernel(const uint4* __restrict__ w1, const uint4*
 // Output row p of a [G, R_out, cols] matrix comes from src_a (or, for the
 // interleaved W1/W3 layout, from W1 or W3 by the same rule as
 // interleave_w13_kernel).
+//
+// Output layout (the shared-memory image the expert GEMM consumes, so one bulk
+// copy moves a stage): rows in tiles of 128, each tile a run of cols / 128
+// stage blocks of FP8_STAGE_BYTES:
+//   bytes [0, 16384): row r's 128 e4m3 values at r * 128, its 16-byte chunk c
+//     (values 16c .. 16c + 15 of the stage) at chunk position c ^ (r % 8)
+//     (the 128-byte swizzle);
+//   bytes [16384, 17408): fp32 scales [2][128], [h][r] for the stage's 64-value
+//     block h of row r.
 __global__ void quantize_fp8_kernel(const __nv_bfloat16* __restrict__ src_a, const __nv_bfloat16* __restrict__ src_b,
-                                    long long G, int H, int bi, int cols, uint8_t* __restrict__ dst_q,
-                                    float* __restrict__ dst_scale) {
-  const int nb = cols / 64;
+                                    long long G, int H, int bi, int cols, uint8_t* __restrict__ dst) {
+  const int nb = cols / 64, n_st = cols / 128;
   const long long rows_out = src_b != nullptr ? G * 2LL * H : G * (long long)H;
   const long long n = rows_out * nb;
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
-    const long long row = i / nb;
-    const int b = int(i % nb);
+    const long long row = i % rows_out;
+    const int b = int(i / rows_out);
     const __nv_bfloat16* src;
     if (src_b != nullptr) {
       const long long g = row / (2LL * H);
@@ -89,10 +97,15 @@ __global__ void quantize_fp8_kernel(const __nv_bfloat16* __restrict__ src_a, con
       out[2 * j] = lo;
       out[2 * j + 1] = hi;
     }
-    uint4* d4 = reinterpret_cast<uint4*>(dst_q + row * cols + b * 64);
+    const int r = int(row % 128), st = b / 2, h = b % 2;
+    uint8_t* blk = dst + ((row / 128) * n_st + st) * (long long)FP8_STAGE_BYTES;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) d4[j] = make_uint4(out[4 * j], out[4 * j + 1], out[4 * j + 2], out[4 * j + 3]);
-    dst_scale[row * nb + b] = ldexpf(1.0f, e);
+    for (int q = 0; q < 4; ++q) {
+      const int c = 4 * h + q;
+      *reinterpret_cast<uint4*>(blk + r * 128 + ((c ^ (r & 7)) << 4)) =
+          make_uint4(out[4 * q], out[4 * q + 1], out[4 * q + 2], out[4 * q + 3]);
+    }
+    reinterpret_cast<float*>(blk + FP8_IMAGE_BYTES)[h * 128 + r] = ldexpf(1.0f, e);
   }
 }
 
@@ -329,8 +342,7 @@ cudaError_t combine_typed(const moe_config& c, const uint4* yp, const uint4* ys,
 PackedLayout packed_layout(const moe_config& c) {
   PackedLayout L;
   L.fp8 = c.expert_w_dtype == MOE_FP8_E4M3;
-  const size_t eb = L.fp8 ? 1 : dtype_bytes(c.act_dtype);
-  const size_t sb = L.fp8 ? 4 : 0;   // scale bytes per 64 weights
+  const size_t eb = dtype_bytes(c.act_dtype);
   const long long Is = (long long)c.n_shared * c.I;
   // blocks of 16 hidden units: W1 rows, then the W3 rows of the same units
   L.bi = (c.I % 16 == 0) ? 16 : c.I;
@@ -341,14 +353,17 @@ PackedLayout packed_layout(const moe_config& c) {
     off = align_up(off + bytes, 256);
     return at;
   };
-  L.w13 = take(size_t(c.E) * 2 * c.I * c.d * eb);
-  L.w13_sc = take(size_t(c.E) * 2 * c.I * (c.d / 64) * sb);
-  L.w2 = take(size_t(c.E) * c.d * c.I * eb);
-  L.w2_sc = take(size_t(c.E) * c.d * (c.I / 64) * sb);
-  L.w13s = take(size_t(2 * Is) * c.d * eb);
-  L.w13s_sc = take(size_t(2 * Is) * (c.d / 64) * sb);
-  L.w2s = take(size_t(c.d) * Is * eb);
-  L.w2s_sc = take(size_t(c.d) * (Is / 64) * sb);
+  if (L.fp8) {
+    L.w13 = take(fp8_tiled_bytes(2LL * c.E * c.I, c.d));
+    L.w2 = take(fp8_tiled_bytes((long long)c.E * c.d, c.I));
+    L.w13s = take(Is > 0 ? fp8_tiled_bytes(2 * Is, c.d) : 0);
+    L.w2s = take(Is > 0 ? fp8_tiled_bytes(c.d, Is) : 0);
+  } else {
+    L.w13 = take(size_t(c.E) * 2 * c.I * c.d * eb);
+    L.w2 = take(size_t(c.E) * c.d * c.I * eb);
+    L.w13s = take(size_t(2 * Is) * c.d * eb);
+    L.w2s = take(size_t(c.d) * Is * eb);
+  }
   L.total = off;
   return L;
 }
@@ -364,18 +379,22 @@ cudaError_t launch_prepack(const moe_config& c, const void* W1, const void* W3, 
   auto grid_for = [](long long n) { long long g = (n + 255) / 256; return int(g < 8192 ? g : 8192); };
   if (L.fp8) {
     using bf = __nv_bfloat16;
-    auto q = [&](const void* a, const void* b, long long G, int H, int bi, int cols, size_t off_q, size_t off_s) {
+    auto q = [&](const void* a, const void* b, long long G, int H, int bi, int cols, size_t off) {
       const long long rows = b != nullptr ? G * 2LL * H : G * (long long)H;
+      uint8_t* dst = reinterpret_cast<uint8_t*>(base + off);
+      // the tile past the last row (read by the odd CTA of a pair at the end) is zero
+      const size_t tile = size_t(cols / 128) * FP8_STAGE_BYTES;
+      cudaError_t e = cudaMemsetAsync(dst + size_t(rows / 128) * tile, 0, tile, s);
+      if (e != cudaSuccess) return e;
       quantize_fp8_kernel<<<grid_for(rows * (cols / 64)), 256, 0, s>>>(
-          static_cast<const bf*>(a), static_cast<const bf*>(b), G, H, bi, cols,
-          reinterpret_cast<uint8_t*>(base + off_q), reinterpret_cast<float*>(base + off_s));
+          static_cast<const bf*>(a), static_cast<const bf*>(b), G, H, bi, cols, dst);
       if (launches) ++*launches;
       return cudaGetLastError();
     };
-    cudaError_t e = q(W1, W3, c.E, c.I, L.bi, c.d, L.w13, L.w13_sc);
-    if (e == cudaSuccess) e = q(W2, nullptr, 1, c.E * c.d, 1, c.I, L.w2, L.w2_sc);
-    if (e == cudaSuccess && Is > 0) e = q(Ws1, Ws3, 1, int(Is), L.bis, c.d, L.w13s, L.w13s_sc);
-    if (e == cudaSuccess && Is > 0) e = q(Ws2, nullptr, 1, c.d, 1, int(Is), L.w2s, L.w2s_sc);
+    cudaError_t e = q(W1, W3, c.E, c.I, L.bi, c.d, L.w13);
+    if (e == cudaSuccess) e = q(W2, nullptr, 1, c.E * c.d, 1, c.I, L.w2);
+    if (e == cudaSuccess && Is > 0) e = q(Ws1, Ws3, 1, int(Is), L.bis, c.d, L.w13s);
+    if (e == cudaSuccess && Is > 0) e = q(Ws2, nullptr, 1, c.d, 1, int(Is), L.w2s);
     return e;
   }
   interleave_w13_kernel<<<grid_for((long long)c.E * 2 * c.I * vec), 256, 0, s>>>(

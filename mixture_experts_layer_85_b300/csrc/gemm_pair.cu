@@ -76,21 +76,29 @@ constexpr int B_KB_BYTES = XB * BK * 2;          // one k-block of this CTA's to
 constexpr int A_BYTES = KB_STAGE * A_KB_BYTES;
 constexpr int B_BYTES = KB_STAGE * B_KB_BYTES;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int RING_BYTES = 200 * 1024;
+constexpr int RING_BYTES = 216 * 1024;
 constexpr int XSMALL = 32;                       // token rows of the small box (decode-sized tiles)
 constexpr int XS_KB_BYTES = XSMALL * BK * 2;
+constexpr int XTINY = 8;                         // token rows of the tiny box (tiles of at most 16 tokens)
+constexpr int XT_KB_BYTES = XTINY * BK * 2;
 constexpr int SMALL_STAGE_BYTES = A_BYTES + KB_STAGE * XS_KB_BYTES;
 static_assert(3 * STAGE_BYTES <= RING_BYTES && MAX_STAGES * SMALL_STAGE_BYTES <= RING_BYTES, "ring");
 constexpr int MAX_GROUPS = 272;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_STRIDE = 256;  // columns between the two accumulators
 constexpr int EPI_WARPS = 4;
-// FP8 weights: converter warps dequantize each stage's e4m3 weight tile (one
-// 128-byte row of 128 weights per thread) into the bf16 A buffer.
-constexpr int CONV_WARPS = 4;
+// FP8 weights: converter warps dequantize each stage's e4m3 weight image into
+// the bf16 A buffer, two threads per weight row (one k-block each).  A slot of
+// the FP8 ring holds up to two consecutive stages of one tile: their weight
+// images (one bulk copy; FP8_STAGE_BYTES each, a multiple of 1024 as the
+// swizzled operand reads need) and then their token tiles.
+constexpr int CONV_WARPS = 8;
 constexpr int THREADS_FP8 = THREADS + 32 * CONV_WARPS;
-constexpr int F8_BYTES = PM * 128;    // one stage of e4m3 weights: 128 rows x 128 k
-constexpr int MAX_F8 = 8;
+static_assert(FP8_IMAGE_BYTES == PM * 128 && FP8_STAGE_BYTES % 1024 == 0 && CONV_WARPS * 32 == KB_STAGE * PM,
+              "converter geometry");
+constexpr int MAX_F8 = 4;           // slots
+constexpr int MAX_SPS = 2;          // stages per slot
+constexpr int MAX_FULL = MAX_F8 * MAX_SPS > MAX_STAGES ? MAX_F8 * MAX_SPS : MAX_STAGES;
 
 // Operand classes: GEMM1 routed, GEMM1 shared, GEMM2 routed, GEMM2 shared.
 constexpr int C1R = 0, C1S = 1, C2R = 2, C2S = 3, NCLS = 4;
@@ -99,6 +107,7 @@ struct PairParams {
   CUtensorMap tmW[NCLS];     // weights: 64 x 128 rows x 2 k-blocks
   CUtensorMap tmX[NCLS];     // tokens: 64 x 128 rows x 2 k-blocks
   CUtensorMap tmXs[NCLS];    // tokens: 64 x 32 rows x 2 k-blocks
+  CUtensorMap tmXt[NCLS];    // tokens: 64 x 8 rows x 2 k-blocks
   void* out[NCLS];
   long long ld_out[NCLS];
   long long out_rows[NCLS];
@@ -111,23 +120,25 @@ struct PairParams {
   int phases;           // bit 0: GEMM1 tiles, bit 1: GEMM2 tiles in this launch
   int* done;            // [num_routed + 1] GEMM1 completion counters, zero at launch (both phases only)
   int* status;
-  int stages;           // ring depth (3, or MAX_STAGES for decode-sized launches)
-  int stage_bytes;      // bytes of one stage in this CTA's shared memory
+  int stages;           // ring depth (3, or MAX_STAGES for decode-sized launches; FP8: bf16 A buffers)
+  int stage_bytes;      // bytes of one stage in this CTA's shared memory (FP8: of one A buffer)
   // FP8 weights
-  CUtensorMap tmW8[NCLS];   // e4m3 weights: 128 bytes x 128 rows boxes
-  const float* wsc[NCLS];   // block scales [w_rows, K / 64]
-  int nf;                   // e4m3 staging slots
-  int f8_off;               // byte offset of the staging ring
+  const void* wimg[NCLS];   // FP8 stage images of the class's weights
+  int nf;                   // FP8 slots
+  int sps;                  // FP8 stages per slot (1 or 2)
+  int f8_off;               // byte offset of the slot ring
+  int slot_bytes;           // bytes of one slot
+  int x_kb_bytes;           // bytes of one k-block of the largest token box of the launch
 };
 
 struct PairCtrl {
-  uint64_t full[MAX_STAGES];   // rank 0: both CTAs' operand bytes of a stage landed
-  uint64_t empty[MAX_STAGES];  // each CTA: the MMAs that read a stage completed
+  uint64_t full[MAX_FULL];     // rank 0: both CTAs' operands of a stage are ready
+  uint64_t empty[MAX_STAGES];  // each CTA: the MMAs that read a stage (FP8: an A buffer) completed
   uint64_t tfull[2];         // each CTA: an accumulator buffer is complete
   uint64_t tempty[2];        // rank 0: both CTAs' epilogues drained a buffer
   uint64_t drain;            // rank 0: every issued MMA completed
-  uint64_t f8_full[MAX_F8];  // FP8: an e4m3 weight tile landed (this CTA)
-  uint64_t f8_empty[MAX_F8]; // FP8: the converters released a staging slot (this CTA)
+  uint64_t f8_full[MAX_F8];  // FP8: a slot's weight images landed (this CTA)
+  uint64_t f8_empty[MAX_F8]; // FP8: the MMAs that read a slot completed (this CTA)
   uint32_t tmem_base;
   int abort;
   int seg[5];                // tile numbers where the four segments start, and the total
@@ -152,6 +163,15 @@ struct PairTile {
 };
 
 __device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+// Token box of a tile: this CTA's n_mma / 2 rows fit the tiny (8), small (32)
+// or full (128) box; one k-block of it in shared memory takes the returned bytes.
+__device__ __forceinline__ int x_kb_bytes(int n_mma) {
+  return n_mma / 2 <= XTINY ? XT_KB_BYTES : (n_mma / 2 <= XSMALL ? XS_KB_BYTES : B_KB_BYTES);
+}
+__device__ __forceinline__ const CUtensorMap* x_map(const PairParams& p, int cls, int n_mma) {
+  return n_mma / 2 <= XTINY ? &p.tmXt[cls] : (n_mma / 2 <= XSMALL ? &p.tmXs[cls] : &p.tmX[cls]);
+}
 
 __device__ __forceinline__ int pair_group_tiles(const PairParams& p, int cls, int rows) {
   return cdiv(rows, PN) * cdiv(p.M[cls], PAIR_M);
@@ -344,10 +364,9 @@ __device__ void pair_producer(PairCtrl* c, const PairParams& p, uint8_t* stages,
     const int w_row = (routed ? t.g * p.w_step[t.cls] : 0) + t.fb * PAIR_M + int(rank) * PM;
     const int x_row = t.row_start + t.tb * PN + int(rank) * (t.n_mma / 2);
     const int nks = (p.K[t.cls] / BK + KB_STAGE - 1) / KB_STAGE;   // stages of this tile
-    const bool small = t.n_mma / 2 <= XSMALL;
-    const CUtensorMap* xmap = small ? &p.tmXs[t.cls] : &p.tmX[t.cls];
+    const CUtensorMap* xmap = x_map(p, t.cls, t.n_mma);
     // both CTAs' full boxes (a k-block past K reads as zeros and still counts)
-    const uint32_t bytes = 2u * uint32_t(A_BYTES + KB_STAGE * (small ? XS_KB_BYTES : B_KB_BYTES));
+    const uint32_t bytes = 2u * uint32_t(A_BYTES + KB_STAGE * x_kb_bytes(t.n_mma));
     for (int ks = 0; ks < nks; ++ks) {
       if (!pair_wait(&c->empty[stage], phase ^ 1u, c, peer_abort, p.status)) {
         ok = false;
@@ -372,164 +391,143 @@ __device__ void pair_producer(PairCtrl* c, const PairParams& p, uint8_t* stages,
     if (issued & (1u << s)) pair_wait(&c->empty[s], (issued_par >> s) & 1u, c, peer_abort, p.status);
 }
 
-// Position of one stage in a CTA's tile sequence (used by the FP8 producer,
-// which runs two cursors over the same sequence).
-struct StageCursor {
-  int tile, ks, nks;
-  long long seq;   // stages before this one in the sequence
-  bool valid;
-  PairTile t;
+// Position in a ring of n barriers/buffers and the parity of its current use,
+// advanced one step at a time (no division on the per-stage path).
+struct RingPos {
+  int i = 0;
+  uint32_t par = 0;
+  __device__ __forceinline__ void next(int n) {
+    if (++i == n) {
+      i = 0;
+      par ^= 1u;
+    }
+  }
 };
-
-__device__ __forceinline__ void cursor_load(StageCursor& cur, PairCtrl* c, const PairParams& p) {
-  cur.valid = pair_tile_exists(c, cur.tile, p.status);
-  if (cur.valid) {
-    cur.t = pair_tile(c, p, cur.tile);
-    cur.ks = 0;
-    cur.nks = (p.K[cur.t.cls] / BK + KB_STAGE - 1) / KB_STAGE;
-  }
-}
-
-__device__ __forceinline__ void cursor_next(StageCursor& cur, PairCtrl* c, const PairParams& p) {
-  ++cur.seq;
-  if (++cur.ks == cur.nks) {
-    cur.tile += (int)cluster_count_x();
-    cursor_load(cur, c, p);
-  }
-}
 
 __device__ __forceinline__ int weight_row(const PairParams& p, const PairTile& t, uint32_t rank) {
   const bool routed = t.cls == C1R || t.cls == C2R;
   return (routed ? t.g * p.w_step[t.cls] : 0) + t.fb * PAIR_M + int(rank) * PM;
 }
 
-// FP8 producer: the e4m3 weight tiles run up to nf stages ahead into the
-// staging ring (this CTA's own barriers); the token tiles follow the bf16
-// path into the stage ring, after the converters of both CTAs and the token
-// copies have filled a stage the MMA consumes it.
+// FP8 producer.  Each slot of the ring takes up to sps consecutive stages of
+// one tile: their weight images in one bulk copy (this CTA's barrier) and
+// their token tiles (completion counted on the even CTA's per-stage barriers,
+// like the bf16 path), issued together so that a token tile never queues
+// behind weight copies of later stages.  The converters turn each image into
+// a bf16 A buffer; the MMAs of the slot's last stage free the slot.
 __device__ void pair_producer_fp8(PairCtrl* c, const PairParams& p, uint8_t* stages, uint32_t rank,
                                   uint32_t peer_abort) {
-  uint8_t* f8 = stages + p.f8_off;
-  StageCursor fc, bc;
-  fc.tile = bc.tile = (int)cluster_id_x();
-  fc.seq = bc.seq = 0;
-  cursor_load(fc, c, p);
-  cursor_load(bc, c, p);
+  uint8_t* ring = stages + p.f8_off;
+  RingPos slot, fpos;                 // slot ring; per-stage barriers full[0 .. nf * sps)
+  const int nfull = p.nf * p.sps;
+  uint32_t used = 0, used_par = 0;    // slots written, and the parity of their last use
+  bool ok = true;
   bool waited = false;
   int ready_group = -1;
-  bool ok = true;
-  unsigned long long idle_since = 0;
-  while (ok && bc.valid) {
-    bool did = false;
-    if (fc.valid && fc.seq < bc.seq + p.nf) {
-      const int slot = int(fc.seq % p.nf);
-      const uint32_t par = (uint32_t(fc.seq / p.nf) & 1u) ^ 1u;
-      if (mbar_try_wait(&c->f8_empty[slot], par)) {
-        mbar_arrive_expect_tx(&c->f8_full[slot], F8_BYTES);
-        tma_load_2d(f8 + size_t(slot) * F8_BYTES, &p.tmW8[fc.t.cls], &c->f8_full[slot], fc.ks * 128,
-                    weight_row(p, fc.t, rank));
-        cursor_next(fc, c, p);
-        did = true;
-      }
+  for (int tile = (int)cluster_id_x(); ok && pair_tile_exists(c, tile, p.status); tile += (int)cluster_count_x()) {
+    const PairTile t = pair_tile(c, p, tile);
+    if (t.cls == C1R && !waited) {
+      pdl_wait();   // the permuted token rows come from the preceding grid
+      waited = true;
     }
-    if (!did) {
-      const PairTile& t = bc.t;
-      if (bc.ks == 0) {
-        if (t.cls == C1R && !waited) {
-          pdl_wait();   // the permuted token rows come from the preceding grid
-          waited = true;
+    if ((t.cls == C2R || t.cls == C2S) && p.phases == 3 && t.g != ready_group) {
+      // the group's GEMM1 tiles (any cluster) have stored its hidden rows
+      const int need = gemm1_need(p, t.cls == C2R ? C1R : C1S, t.rows);
+      const unsigned long long t0 = globaltimer_ns();
+      while (ld_acquire_gpu(p.done + t.g) < need) {
+        if (*reinterpret_cast<volatile int*>(&c->abort)) {
+          ok = false;
+          break;
         }
-        if ((t.cls == C2R || t.cls == C2S) && p.phases == 3 && t.g != ready_group) {
-          const int need = gemm1_need(p, t.cls == C2R ? C1R : C1S, t.rows);
-          if (ld_acquire_gpu(p.done + t.g) >= need) {
-            fence_proxy_async_global();
-            ready_group = t.g;
-          }
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+          c->abort = 1;
+          st_remote_u32(peer_abort, 1u);
+          flag_status(p.status, DEV_TIMEOUT);
+          ok = false;
+          break;
         }
+        __nanosleep(128);
       }
-      const bool dep_ok = !((t.cls == C2R || t.cls == C2S) && p.phases == 3 && t.g != ready_group);
-      const int stage = int(bc.seq % p.stages);
-      const uint32_t par = (uint32_t(bc.seq / p.stages) & 1u) ^ 1u;
-      if (dep_ok && mbar_try_wait(&c->empty[stage], par)) {
-        uint8_t* sa = stages + size_t(stage) * p.stage_bytes;
-        const bool small = t.n_mma / 2 <= XSMALL;
-        const CUtensorMap* xmap = small ? &p.tmXs[t.cls] : &p.tmX[t.cls];
-        const uint32_t bytes = 2u * uint32_t(KB_STAGE * (small ? XS_KB_BYTES : B_KB_BYTES));
-        if (rank == 0) mbar_arrive_expect_tx(&c->full[stage], bytes);
-        const uint32_t fb = map_to_rank(smem_u32(&c->full[stage]), 0);
-        const int x_row = t.row_start + t.tb * PN + int(rank) * (t.n_mma / 2);
-        tma_load_3d_pair(sa + A_BYTES, xmap, fb, x_row, bc.ks * KB_STAGE);
-        cursor_next(bc, c, p);
-        did = true;
-      }
+      if (!ok) break;
+      fence_proxy_async_global();   // the copy engine reads what the acquire made visible
+      ready_group = t.g;
     }
-    if (did) {
-      idle_since = 0;
-    } else {
-      const unsigned long long now = globaltimer_ns();
-      if (idle_since == 0) idle_since = now;
-      if (*reinterpret_cast<volatile int*>(&c->abort)) ok = false;
-      if (now - idle_since > kWaitLimitNs) {
-        c->abort = 1;
-        st_remote_u32(peer_abort, 1u);
-        flag_status(p.status, DEV_TIMEOUT);
+    const int nks = p.K[t.cls] / 128;   // stages of this tile (K is a multiple of 128)
+    const uint8_t* wsrc = static_cast<const uint8_t*>(p.wimg[t.cls]) +
+                          size_t(weight_row(p, t, rank) / PM) * size_t(nks) * FP8_STAGE_BYTES;
+    const int x_row = t.row_start + t.tb * PN + int(rank) * (t.n_mma / 2);
+    const CUtensorMap* xmap = x_map(p, t.cls, t.n_mma);
+    const uint32_t xbytes = 2u * uint32_t(KB_STAGE * x_kb_bytes(t.n_mma));
+    for (int ks = 0; ks < nks; ks += p.sps) {
+      const int n_in = min(p.sps, nks - ks);
+      if (!pair_wait(&c->f8_empty[slot.i], slot.par ^ 1u, c, peer_abort, p.status)) {
         ok = false;
+        break;
       }
+      uint8_t* dst = ring + size_t(slot.i) * p.slot_bytes;
+      const uint32_t wbytes = uint32_t(n_in) * FP8_STAGE_BYTES;
+      mbar_arrive_expect_tx(&c->f8_full[slot.i], wbytes);
+      bulk_load(dst, wsrc + size_t(ks) * FP8_STAGE_BYTES, wbytes, &c->f8_full[slot.i]);
+      uint8_t* xdst = dst + p.sps * FP8_STAGE_BYTES;
+      for (int j = 0; j < n_in; ++j) {
+        uint64_t* fb = &c->full[fpos.i];
+        if (rank == 0) mbar_arrive_expect_tx(fb, xbytes);
+        tma_load_3d_pair(xdst + j * KB_STAGE * p.x_kb_bytes, xmap, map_to_rank(smem_u32(fb), 0), x_row,
+                         (ks + j) * KB_STAGE);
+        fpos.next(nfull);
+      }
+      used |= 1u << slot.i;
+      used_par = (used_par & ~(1u << slot.i)) | (slot.par << slot.i);
+      slot.next(p.nf);
     }
   }
-  // every copy issued into the rings was consumed before this CTA may leave
-  const long long nf_done = fc.seq, nb_done = bc.seq;
-  for (int s = 0; s < p.nf && s < nf_done; ++s) {
-    const long long last = nf_done - 1 - ((nf_done - 1 - s) % p.nf);
-    pair_wait(&c->f8_empty[s], uint32_t(last / p.nf) & 1u, c, peer_abort, p.status);
-  }
-  for (int s = 0; s < p.stages && s < nb_done; ++s) {
-    const long long last = nb_done - 1 - ((nb_done - 1 - s) % p.stages);
-    pair_wait(&c->empty[s], uint32_t(last / p.stages) & 1u, c, peer_abort, p.status);
-  }
+  // The last copies into each slot were consumed (so they landed) before this
+  // CTA may leave; on the normal path these waits return at once.
+  for (int s = 0; s < p.nf; ++s)
+    if (used & (1u << s)) pair_wait(&c->f8_empty[s], (used_par >> s) & 1u, c, peer_abort, p.status);
 }
 
-// FP8 converter warps: thread i of the four warps owns weight row i of this
-// CTA's 128.  Per stage it reads the row's 128 e4m3 bytes (128-byte swizzle),
-// multiplies by the two block scales (powers of two, so exact) and writes 128
-// bf16 values into the stage's A buffer in the MMA's swizzled K-major layout,
-// then hands the stage to the MMA issuer on the even CTA.
-__device__ void pair_converter(PairCtrl* c, const PairParams& p, uint8_t* stages, int cw, int lane, uint32_t rank,
+// FP8 converter warps: thread i of the eight warps owns k-block i / 128 of
+// weight row i % 128 of this CTA's 128.  Per stage it reads the row's 64 e4m3
+// bytes of that k-block (128-byte swizzle) and the block's scale (a power of
+// two, so the products are exact), writes 64 bf16 values into a free A buffer
+// in the MMA's swizzled K-major layout, then tells the MMA issuer on the even
+// CTA (on the stage's barrier, which also counts the token tile's bytes).
+__device__ void pair_converter(PairCtrl* c, const PairParams& p, uint8_t* stages, int cw, int lane,
                                uint32_t peer_abort) {
-  uint8_t* f8 = stages + p.f8_off;
-  const int r = cw * 32 + lane;   // weight row within this CTA's 128
+  uint8_t* ring = stages + p.f8_off;
+  const int ct = cw * 32 + lane;
+  const int r = ct % PM;          // weight row within this CTA's 128
+  const int h = ct / PM;          // k-block of the stage
   const int sw = r & 7;           // 128-byte swizzle phase of that row
-  long long seq = 0;
+  RingPos slot, stage, fpos;      // slot ring, A buffers, per-stage barriers
+  const int nfull = p.nf * p.sps;
   bool ok = true;
   for (int tile = (int)cluster_id_x(); ok; tile += (int)cluster_count_x()) {
     int exists = 0;
     if (lane == 0) exists = pair_tile_exists(c, tile, p.status) ? 1 : 0;
     if (!__shfl_sync(0xffffffffu, exists, 0)) break;
     const PairTile t = pair_tile(c, p, tile);
-    const int K = p.K[t.cls];
-    const int nblk = K / 64;
-    const float* sc = p.wsc[t.cls] + (long long)(weight_row(p, t, rank) + r) * nblk;
-    const int nks = (K / BK + KB_STAGE - 1) / KB_STAGE;
-    for (int ks = 0; ks < nks; ++ks, ++seq) {
-      const int slot = int(seq % p.nf), stage = int(seq % p.stages);
+    const int nks = p.K[t.cls] / 128;
+    for (int ks = 0; ks < nks; ++ks) {
+      const int half = ks & (p.sps - 1);   // sps is 1 or 2
       int good = 1;
       if (lane == 0) {
-        good = pair_wait(&c->f8_full[slot], uint32_t(seq / p.nf) & 1u, c, peer_abort, p.status) &&
-               pair_wait(&c->empty[stage], (uint32_t(seq / p.stages) & 1u) ^ 1u, c, peer_abort, p.status);
+        good = (half != 0 || pair_wait(&c->f8_full[slot.i], slot.par, c, peer_abort, p.status)) &&
+               pair_wait(&c->empty[stage.i], stage.par ^ 1u, c, peer_abort, p.status);
       }
       if (!__shfl_sync(0xffffffffu, good, 0)) {
         ok = false;
         break;
       }
-      const float s0 = sc[2 * ks];
-      const float s1 = 2 * ks + 1 < nblk ? sc[2 * ks + 1] : 0.0f;
-      const uint8_t* src = f8 + size_t(slot) * F8_BYTES + r * 128;
-      uint8_t* dst = stages + size_t(stage) * p.stage_bytes + r * 128;
+      const uint8_t* src = ring + size_t(slot.i) * p.slot_bytes + size_t(half) * FP8_STAGE_BYTES;
+      const float scale = reinterpret_cast<const float*>(src + FP8_IMAGE_BYTES)[h * PM + r];
+      src += r * 128;
+      uint8_t* kb = stages + size_t(stage.i) * p.stage_bytes + h * A_KB_BYTES + r * 128;
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
-        // 16 weights k = 16 ch .. 16 ch + 15 of the stage
-        const uint4 q = *reinterpret_cast<const uint4*>(src + ((ch ^ sw) << 4));
-        const float scale = ch < 4 ? s0 : s1;
+      for (int q4 = 0; q4 < 4; ++q4) {
+        // weights 16 q4 .. 16 q4 + 15 of the k-block: e4m3 chunk 4 h + q4
+        const uint4 q = *reinterpret_cast<const uint4*>(src + (((4 * h + q4) ^ sw) << 4));
         const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
         uint32_t o[8];
 #pragma unroll
@@ -542,26 +540,31 @@ __device__ void pair_converter(PairCtrl* c, const PairParams& p, uint8_t* stages
           o[2 * i] = *reinterpret_cast<const uint32_t*>(&x);
           o[2 * i + 1] = *reinterpret_cast<const uint32_t*>(&y);
         }
-        // bf16 k-block ch / 4, 16-byte chunks 2 (ch % 4) and 2 (ch % 4) + 1 of row r
-        uint8_t* kb = dst + (ch >> 2) * A_KB_BYTES;
-        const int j = (ch & 3) * 2;
+        // bf16 16-byte chunks 2 q4 and 2 q4 + 1 of row r of k-block h
+        const int j = 2 * q4;
         *reinterpret_cast<uint4*>(kb + ((j ^ sw) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
         *reinterpret_cast<uint4*>(kb + (((j + 1) ^ sw) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
       }
       // the tensor cores read the A buffer through the async proxy
       fence_proxy_async_shared();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&c->f8_empty[slot]);
-        mbar_arrive_remote(map_to_rank(smem_u32(&c->full[stage]), 0));
-      }
+      if (lane == 0) mbar_arrive_remote(map_to_rank(smem_u32(&c->full[fpos.i]), 0));
+      stage.next(p.stages);
+      fpos.next(nfull);
+      if (half == p.sps - 1 || ks == nks - 1) slot.next(p.nf);
     }
   }
 }
 
+// FP8: the A operand comes from the A buffers in turn, the token tile from the
+// stage's part of its slot; the MMAs' completion frees the A buffer, and after
+// the slot's last stage the slot.
+template <bool FP8>
 __device__ void pair_mma(PairCtrl* c, const PairParams& p, uint8_t* stages, uint32_t tmem, uint32_t peer_abort) {
   int stage = 0;
   uint32_t phase = 0;
+  int slot = 0;
+  RingPos fpos;   // FP8: per-stage barriers full[0 .. nf * sps)
   int ctr = 0;
   bool ok = true;
   for (int tile = (int)cluster_id_x(); ok && pair_tile_exists(c, tile, p.status);
@@ -573,15 +576,18 @@ __device__ void pair_mma(PairCtrl* c, const PairParams& p, uint8_t* stages, uint
     tc_fence_after();
     const uint32_t d_tmem = tmem + uint32_t(acc) * ACC_STRIDE;
     const int nks = (p.K[t.cls] / BK + KB_STAGE - 1) / KB_STAGE;
-    const uint32_t b_kb = t.n_mma / 2 <= XSMALL ? XS_KB_BYTES : B_KB_BYTES;
+    const uint32_t b_kb = uint32_t(x_kb_bytes(t.n_mma));
     for (int ks = 0; ks < nks; ++ks) {
-      if (!pair_wait(&c->full[stage], phase, c, peer_abort, p.status)) {
+      const int half = FP8 ? (ks & (p.sps - 1)) : 0;
+      if (!pair_wait(&c->full[FP8 ? fpos.i : stage], FP8 ? fpos.par : phase, c, peer_abort, p.status)) {
         ok = false;
         break;
       }
       tc_fence_after();
       const uint32_t a0 = smem_u32(stages + stage * p.stage_bytes);
-      const uint32_t b0 = a0 + A_BYTES;
+      const uint32_t b0 = FP8 ? smem_u32(stages + p.f8_off + size_t(slot) * p.slot_bytes +
+                                         size_t(p.sps) * FP8_STAGE_BYTES + size_t(half) * KB_STAGE * p.x_kb_bytes)
+                              : a0 + A_BYTES;
 #pragma unroll
       for (int j = 0; j < KB_STAGE; ++j)
 #pragma unroll
@@ -592,6 +598,13 @@ __device__ void pair_mma(PairCtrl* c, const PairParams& p, uint8_t* stages, uint
       if (++stage == p.stages) {
         stage = 0;
         phase ^= 1u;
+      }
+      if (FP8) {
+        fpos.next(p.nf * p.sps);
+        if (half == p.sps - 1 || ks == nks - 1) {
+          mma_commit_pair(&c->f8_empty[slot], 0x3);
+          if (++slot == p.nf) slot = 0;
+        }
       }
     }
     if (ok) mma_commit_pair(&c->tfull[acc], 0x3);
@@ -697,15 +710,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FP8 ? THREADS_FP8 : 
   const uint32_t peer_abort = map_to_rank(smem_u32(&c->abort), rank ^ 1u);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < MAX_STAGES; ++s) {
-      // FP8: the even CTA's producer (token bytes) and the converter warps of both CTAs
-      mbar_init(&c->full[s], FP8 ? 1 + 2 * CONV_WARPS : 1);
-      mbar_init(&c->empty[s], 1);
-    }
+    // FP8: the even CTA's producer (token bytes) and the converter warps of both CTAs
+    for (int s = 0; s < MAX_FULL; ++s) mbar_init(&c->full[s], FP8 ? 1 + 2 * CONV_WARPS : 1);
+    for (int s = 0; s < MAX_STAGES; ++s) mbar_init(&c->empty[s], 1);
     if (FP8) {
       for (int s = 0; s < MAX_F8; ++s) {
         mbar_init(&c->f8_full[s], 1);
-        mbar_init(&c->f8_empty[s], CONV_WARPS);
+        mbar_init(&c->f8_empty[s], 1);
       }
     }
     for (int a = 0; a < 2; ++a) {
@@ -725,7 +736,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FP8 ? THREADS_FP8 : 
       tma_prefetch_desc(&p.tmW[i]);
       tma_prefetch_desc(&p.tmX[i]);
       tma_prefetch_desc(&p.tmXs[i]);
-      if (FP8) tma_prefetch_desc(&p.tmW8[i]);
+      tma_prefetch_desc(&p.tmXt[i]);
     }
   }
   if (warp == 1) {
@@ -746,11 +757,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FP8 ? THREADS_FP8 : 
       else pair_producer(c, p, stages, rank, peer_abort);
     }
   } else if (warp == 1) {
-    if (lane == 0 && rank == 0) pair_mma(c, p, stages, tmem, peer_abort);
+    if (lane == 0 && rank == 0) pair_mma<FP8>(c, p, stages, tmem, peer_abort);
   } else if (warp < 2 + EPI_WARPS) {
     pair_epilogue(c, p, tmem, warp, lane, rank, peer_abort);
   } else if (warp >= THREADS / 32) {
-    pair_converter(c, p, stages, warp - THREADS / 32, lane, rank, peer_abort);
+    pair_converter(c, p, stages, warp - THREADS / 32, lane, peer_abort);
   } else {
     // scheduler warp: the routed tables need the dispatch offsets
     pdl_wait();
@@ -815,15 +826,16 @@ cudaError_t launch_pair_experts(const PairClass cls[4], const int32_t* offsets, 
     const PairClass& g = (shared_rows > 0 || i == C1R || i == C2R) ? cls[i] : cls[i - 1];
     if (g.K % BK != 0) return cudaErrorInvalidValue;
     if (fp8) {
-      // e4m3 bytes [w_rows, K], one 128-byte row of 128 weights per box row
-      if (g.W_scale == nullptr || g.K % 128 != 0) return cudaErrorInvalidValue;
-      if (!encode_tiled_map(&p.tmW8[i], g.W, g.w_rows, g.K, 1, PM, 1)) return cudaErrorInvalidValue;
-      p.wsc[i] = g.W_scale;
+      // stage images of 128-row tiles (a zero tile follows the last row)
+      if (g.K % 128 != 0 || g.w_rows % PM != 0 || reinterpret_cast<uintptr_t>(g.W) % 16 != 0)
+        return cudaErrorInvalidValue;
+      p.wimg[i] = g.W;
     } else if (!encode_bf16_map(&p.tmW[i], g.W, g.w_rows, g.K, PM, KB_STAGE)) {
       return cudaErrorInvalidValue;
     }
     if (!encode_bf16_map(&p.tmX[i], g.X, g.x_rows, g.K, XB, KB_STAGE)) return cudaErrorInvalidValue;
     if (!encode_bf16_map(&p.tmXs[i], g.X, g.x_rows, g.K, XSMALL, KB_STAGE)) return cudaErrorInvalidValue;
+    if (!encode_bf16_map(&p.tmXt[i], g.X, g.x_rows, g.K, XTINY, KB_STAGE)) return cudaErrorInvalidValue;
     p.out[i] = g.out;
     p.ld_out[i] = g.ld_out;
     p.out_rows[i] = g.out_rows;
@@ -843,11 +855,18 @@ cudaError_t launch_pair_experts(const PairClass cls[4], const int32_t* offsets, 
   p.stage_bytes = small ? SMALL_STAGE_BYTES : STAGE_BYTES;
   cudaError_t e;
   if (fp8) {
-    // two bf16 stages (A written by the converters, tokens by TMA) and a deep
-    // ring of e4m3 weight tiles behind them
+    // two bf16 A buffers (written by the converters) and a ring of slots,
+    // each holding the weight images and token tiles of sps stages: decode-
+    // sized launches take two stages per slot (groups of at most 16 tokens:
+    // 4 slots of 38 KB; at most 64: 3 of 50 KB), others one (3 slots of 49 KB)
+    const bool tiny = max_group_rows <= 2 * XTINY;
     p.stages = 2;
-    p.f8_off = 2 * p.stage_bytes;
-    p.nf = (RING_BYTES - p.f8_off) / F8_BYTES;
+    p.stage_bytes = A_BYTES;
+    p.f8_off = 2 * A_BYTES;
+    p.sps = small ? 2 : 1;
+    p.x_kb_bytes = tiny ? XT_KB_BYTES : (small ? XS_KB_BYTES : B_KB_BYTES);
+    p.slot_bytes = p.sps * (FP8_STAGE_BYTES + KB_STAGE * p.x_kb_bytes);
+    p.nf = (RING_BYTES - p.f8_off) / p.slot_bytes;
     if (p.nf > MAX_F8) p.nf = MAX_F8;
     e = launch_pair<true>(p, max_tiles, stream);
   } else {

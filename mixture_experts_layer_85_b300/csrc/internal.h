@@ -68,6 +68,7 @@ bool encode_bf16_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols
 bool encode_tiled_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int elem_bytes,
                       uint32_t box_rows, uint32_t box_kblocks);
 
+
 // Records the next armed profiling event on `s` (no-op when disarmed).
 void profile_mark(cudaStream_t s);
 
@@ -81,8 +82,7 @@ cudaError_t launch_grouped_gemm(int epi, const GemmClass& c0, const GemmClass* c
 // per group), X [x_rows, K] token rows (class 0: rows offsets[g] ..
 // offsets[g+1]; class 1: one group of shared_rows rows), both bf16 K-major.
 struct PairClass {
-  const void* W = nullptr;
-  const float* W_scale = nullptr;   // FP8 weights: scales [w_rows, K / 64] (W is then e4m3 bytes)
+  const void* W = nullptr;   // bf16 rows, or FP8 stage images (fp8_tiled_bytes layout)
   int64_t w_rows = 0;
   const void* X = nullptr;
   int64_t x_rows = 0;
@@ -102,8 +102,8 @@ struct PairClass {
 // launch starts.  max_group_rows: an upper bound of any group's rows (the
 // batch size T).  The shared expert's GEMM1 tiles may run before the
 // preceding grid completes.
-// fp8: the weights are e4m3 blocks (PairClass::W_scale), dequantized to bf16
-// in shared memory by converter warps before each MMA.
+// fp8: the weights are FP8 stage images (one bulk copy per stage), dequantized
+// to bf16 in shared memory by converter warps before each MMA.
 cudaError_t launch_pair_experts(const PairClass cls[4], const int32_t* offsets, int num_routed, int shared_rows,
                                 int max_group_rows, int phases, int* done, int* status, long long max_tiles,
                                 cudaStream_t stream, int* launches, bool fp8 = false);
@@ -144,12 +144,19 @@ cudaError_t launch_combine(const moe_config& c, const void* y_perm, const void* 
 cudaError_t launch_balance_update(const moe_config& c, const int32_t* counts, float* bias, float gamma, float* stats,
                                   int* status, cudaStream_t s, int* launches);
 
+// FP8 expert weights are stored as the expert GEMM's shared-memory images:
+// tiles of 128 rows, each a run of cols / 128 stage blocks of FP8_STAGE_BYTES
+// (128 x 128 e4m3 values with the 128-byte swizzle, then their fp32 scales
+// [2][128]), plus one zero tile after the last row.
+constexpr int FP8_IMAGE_BYTES = 128 * 128;
+constexpr int FP8_STAGE_BYTES = FP8_IMAGE_BYTES + 2 * 128 * 4;
+inline size_t fp8_tiled_bytes(long long rows, long long cols) {
+  return size_t(rows / 128 + 1) * size_t(cols / 128) * FP8_STAGE_BYTES;
+}
+
 // Packed expert blob layout (byte offsets, each 256-byte aligned).
-// FP8 layout (expert_w_dtype = MOE_FP8_E4M3): each matrix is stored as e4m3
-// bytes [rows, cols] followed by fp32 scales [rows, cols / 64] (offsets *_sc).
 struct PackedLayout {
   size_t w13 = 0, w2 = 0, w13s = 0, w2s = 0, total = 0;
-  size_t w13_sc = 0, w2_sc = 0, w13s_sc = 0, w2s_sc = 0;
   bool fp8 = false;
   int bi = 0, bis = 0;   // interleave block of W1/W3 rows (routed, shared)
 };

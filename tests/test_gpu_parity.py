@@ -325,17 +325,37 @@ def _fp8_copy(wl):
     return inputs.small_workload(wl, name=wl.name + "_fp8", expert_w_dtype="fp8")
 
 
-def _split_fp8_blob(packed, shape_rows, cols, off_q, off_s):
-    """e4m3 values and scales of one packed matrix, read back as float64."""
-    q = packed[off_q: off_q + shape_rows * cols].view(torch.float8_e4m3fn).to(torch.float64)
-    s = packed[off_s: off_s + shape_rows * (cols // 64) * 4].view(torch.float32).to(torch.float64)
-    return q.view(shape_rows, cols).cpu().numpy(), s.view(shape_rows, cols // 64).cpu().numpy()
+FP8_STAGE = 128 * 128 + 2 * 128 * 4   # one stage image: 128 x 128 e4m3 values, then fp32 scales [2][128]
+
+
+def _fp8_tiled_bytes(rows, cols):
+    return (rows // 128 + 1) * (cols // 128) * FP8_STAGE
+
+
+def _decode_fp8_tiles(packed, off, rows, cols):
+    """e4m3 values [rows, cols] and scales [rows, cols / 64] (float64) of one
+    matrix stored as stage images: 128-row tiles of cols / 128 stages, each a
+    128-byte-swizzled 128 x 128 byte image (16-byte chunk c of row r at chunk
+    position c ^ (r % 8)) followed by its scales [2][128]; one zero tile
+    follows the last row."""
+    nst, tiles = cols // 128, rows // 128 + 1
+    blob = packed[off: off + tiles * nst * FP8_STAGE].view(tiles, nst, FP8_STAGE)
+    img = blob[:, :, :128 * 128].reshape(tiles, nst, 128, 8, 16)
+    r = torch.arange(128, device=blob.device)
+    pos = torch.arange(8, device=blob.device)[None, :] ^ (r[:, None] % 8)          # [128 rows, 8 logical chunks]
+    logical = img[:, :, r[:, None], pos, :]                                            # [tiles, nst, 128, 8, 16]
+    q = logical.permute(0, 2, 1, 3, 4).reshape(tiles * 128, cols).contiguous()
+    sc = blob[:, :, 128 * 128:].contiguous().view(torch.float32).view(tiles, nst, 2, 128)
+    sc = sc.permute(0, 3, 1, 2).reshape(tiles * 128, cols // 64)
+    assert int(q[rows:].count_nonzero()) == 0 and int(sc[rows:].count_nonzero()) == 0   # the zero tile
+    qf = q[:rows].view(torch.float8_e4m3fn).to(torch.float64).cpu().numpy()
+    return qf, sc[:rows].to(torch.float64).cpu().numpy()
 
 
 def test_fp8_prepack_matches_oracle_quantization():
     """moe_prepack_experts with FP8 weights: e4m3 bytes and block scales of every
-    matrix bit for bit equal to the oracle's block quantisation (W2 and the
-    shared W2 here; W1/W3 rows are the same rule in the interleaved order)."""
+    matrix bit for bit equal to the oracle's block quantisation, decoded from
+    the stage-image layout the expert GEMM streams."""
     wl = _fp8_copy(SMALL["v3_small_t333"])
     cfg = _lib.make_config(wl)
     w1, w3, w2, ws1, ws3, ws2 = inputs.make_experts(wl, "cuda")
@@ -345,22 +365,18 @@ def test_fp8_prepack_matches_oracle_quantization():
     E, I, d, Is = wl.E, wl.I, wl.d, wl.I_s
     al = lambda v: (v + 255) // 256 * 256
     o_w13 = 0
-    o_w13sc = al(o_w13 + E * 2 * I * d)
-    o_w2 = al(o_w13sc + E * 2 * I * (d // 64) * 4)
-    o_w2sc = al(o_w2 + E * d * I)
-    o_w13s = al(o_w2sc + E * d * (I // 64) * 4)
-    o_w13ssc = al(o_w13s + 2 * Is * d)
-    o_w2s = al(o_w13ssc + 2 * Is * (d // 64) * 4)
-    o_w2ssc = al(o_w2s + d * Is)
-    assert al(o_w2ssc + d * (Is // 64) * 4) == packed.numel()
-    q, s = _split_fp8_blob(packed, E * d, I, o_w2, o_w2sc)
+    o_w2 = al(o_w13 + _fp8_tiled_bytes(E * 2 * I, d))
+    o_w13s = al(o_w2 + _fp8_tiled_bytes(E * d, I))
+    o_w2s = al(o_w13s + _fp8_tiled_bytes(2 * Is, d))
+    assert al(o_w2s + _fp8_tiled_bytes(d, Is)) == packed.numel()
+    q, s = _decode_fp8_tiles(packed, o_w2, E * d, I)
     wq, ws = orc.quantize_fp8_blocks(f64(w2).reshape(E * d, I))
     assert np.array_equal(q, wq) and np.array_equal(s, ws)
-    q, s = _split_fp8_blob(packed, d, Is, o_w2s, o_w2ssc)
+    q, s = _decode_fp8_tiles(packed, o_w2s, d, Is)
     wq, ws = orc.quantize_fp8_blocks(f64(ws2))
     assert np.array_equal(q, wq) and np.array_equal(s, ws)
     # W13: rows in the 16-row interleave (16 W1 rows, then the 16 W3 rows of the same units)
-    q, s = _split_fp8_blob(packed, E * 2 * I, d, o_w13, o_w13sc)
+    q, s = _decode_fp8_tiles(packed, o_w13, E * 2 * I, d)
     w13 = torch.stack([w1, w3], 1).view(E, 2, I // 16, 16, d).transpose(1, 2).reshape(E * 2 * I, d)
     wq, ws = orc.quantize_fp8_blocks(f64(w13))
     assert np.array_equal(q, wq) and np.array_equal(s, ws)
@@ -388,10 +404,19 @@ def _dequantized_shared(li):
     return _dq(li.ws1), _dq(li.ws3), _dq(li.ws2)
 
 
+# FP8 decode-sized cases whose tiles have an odd number of 128-deep stages (d = I = 384)
+FP8_ODD = {
+    "v3_odd_t5": inputs.small_workload(W["v3_prefill_t16384"], name="v3_odd_t5", T=5, d=384, E=64, I=384,
+                                       n_group=8, topk_group=4),
+    "v3_odd_t40": inputs.small_workload(W["v3_prefill_t16384"], name="v3_odd_t40", T=40, d=384, E=64, I=384,
+                                        n_group=8, topk_group=4),
+}
+
+
 @pytest.mark.parametrize("name", ["v3_small_t333", "v2lite_small_t1037", "v3_small_t1", "v3_small_t3",
-                                  "v3_small_t1100"])
+                                  "v3_small_t1100", "v3_odd_t5", "v3_odd_t40"])
 def test_fp8_layer_matches_oracle_on_dequantized_weights(name):
-    wl = _fp8_copy(SMALL[name])
+    wl = _fp8_copy(SMALL[name] if name in SMALL else FP8_ODD[name])
     li = inputs.make_inputs(wl, "cuda")
     _, out, idx, w, counts = run_layer(wl, li)
     r = oracle_route(li, wl)

@@ -88,13 +88,16 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_STRIDE = 256;  // columns between the two accumulators
 constexpr int EPI_WARPS = 4;
 // FP8 weights: converter warps dequantize each stage's e4m3 weight image into
-// the bf16 A buffer, two threads per weight row (one k-block each).  A slot of
+// the bf16 A buffer, four threads per weight row (32 weights each).  A slot of
 // the FP8 ring holds up to two consecutive stages of one tile: their weight
 // images (one bulk copy; FP8_STAGE_BYTES each, a multiple of 1024 as the
 // swizzled operand reads need) and then their token tiles.
-constexpr int CONV_WARPS = 8;
+constexpr int CONV_WARPS = 16;
 constexpr int THREADS_FP8 = THREADS + 32 * CONV_WARPS;
-static_assert(FP8_IMAGE_BYTES == PM * 128 && FP8_STAGE_BYTES % 1024 == 0 && CONV_WARPS * 32 == KB_STAGE * PM,
+constexpr int CONV_TPR = CONV_WARPS * 32 / PM;   // converter threads per weight row
+constexpr int CONV_CPT = 8 / CONV_TPR;           // 16-weight chunks of a stage row per thread
+static_assert(FP8_IMAGE_BYTES == PM * 128 && FP8_STAGE_BYTES % 1024 == 0 && CONV_TPR * CONV_CPT == 8 &&
+                  CONV_CPT <= 4,
               "converter geometry");
 constexpr int MAX_F8 = 4;           // slots
 constexpr int MAX_SPS = 2;          // stages per slot
@@ -487,19 +490,22 @@ __device__ void pair_producer_fp8(PairCtrl* c, const PairParams& p, uint8_t* sta
     if (used & (1u << s)) pair_wait(&c->f8_empty[s], (used_par >> s) & 1u, c, peer_abort, p.status);
 }
 
-// FP8 converter warps: thread i of the eight warps owns k-block i / 128 of
-// weight row i % 128 of this CTA's 128.  Per stage it reads the row's 64 e4m3
-// bytes of that k-block (128-byte swizzle) and the block's scale (a power of
-// two, so the products are exact), writes 64 bf16 values into a free A buffer
-// in the MMA's swizzled K-major layout, then tells the MMA issuer on the even
-// CTA (on the stage's barrier, which also counts the token tile's bytes).
+// FP8 converter warps: thread i owns 16-weight chunks (i / 128) * CONV_CPT ..
+// of weight row i % 128 of this CTA's 128 (all in one 64-weight k-block).
+// Per stage it reads those e4m3 bytes (128-byte swizzle) and the block's scale
+// (a power of two, so the products are exact), writes the bf16 values into a
+// free A buffer in the MMA's swizzled K-major layout, then tells the MMA
+// issuer on the even CTA (on the stage's barrier, which also counts the token
+// tile's bytes).  The arrival orders the writes at CTA scope only: each CTA's
+// tensor core reads its own A rows, so the data never crosses CTAs.
 __device__ void pair_converter(PairCtrl* c, const PairParams& p, uint8_t* stages, int cw, int lane,
                                uint32_t peer_abort) {
   uint8_t* ring = stages + p.f8_off;
   const int ct = cw * 32 + lane;
-  const int r = ct % PM;          // weight row within this CTA's 128
-  const int h = ct / PM;          // k-block of the stage
-  const int sw = r & 7;           // 128-byte swizzle phase of that row
+  const int r = ct % PM;                  // weight row within this CTA's 128
+  const int c0 = (ct / PM) * CONV_CPT;    // first 16-weight chunk of the stage row
+  const int h = c0 / 4;                   // its k-block
+  const int sw = r & 7;                   // 128-byte swizzle phase of that row
   RingPos slot, stage, fpos;      // slot ring, A buffers, per-stage barriers
   const int nfull = p.nf * p.sps;
   bool ok = true;
@@ -525,9 +531,10 @@ __device__ void pair_converter(PairCtrl* c, const PairParams& p, uint8_t* stages
       src += r * 128;
       uint8_t* kb = stages + size_t(stage.i) * p.stage_bytes + h * A_KB_BYTES + r * 128;
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        // weights 16 q4 .. 16 q4 + 15 of the k-block: e4m3 chunk 4 h + q4
-        const uint4 q = *reinterpret_cast<const uint4*>(src + (((4 * h + q4) ^ sw) << 4));
+      for (int qc = 0; qc < CONV_CPT; ++qc) {
+        // e4m3 chunk c0 + qc of the stage row: weights 16 q4 .. 16 q4 + 15 of k-block h
+        const int q4 = (c0 + qc) & 3;
+        const uint4 q = *reinterpret_cast<const uint4*>(src + (((c0 + qc) ^ sw) << 4));
         const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
         uint32_t o[8];
 #pragma unroll
@@ -548,7 +555,7 @@ __device__ void pair_converter(PairCtrl* c, const PairParams& p, uint8_t* stages
       // the tensor cores read the A buffer through the async proxy
       fence_proxy_async_shared();
       __syncwarp();
-      if (lane == 0) mbar_arrive_remote(map_to_rank(smem_u32(&c->full[fpos.i]), 0));
+      if (lane == 0) mbar_arrive_remote_cta(map_to_rank(smem_u32(&c->full[fpos.i]), 0));
       stage.next(p.stages);
       fpos.next(nfull);
       if (half == p.sps - 1 || ks == nks - 1) slot.next(p.nf);

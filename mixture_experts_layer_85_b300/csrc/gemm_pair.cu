@@ -86,6 +86,13 @@ static_assert(3 * STAGE_BYTES <= RING_BYTES && MAX_STAGES * SMALL_STAGE_BYTES <=
 constexpr int MAX_GROUPS = 272;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_STRIDE = 256;  // columns between the two accumulators
+// FP8 decode-sized launches keep the converted A operand in tensor memory:
+// accumulators of at most 64 columns (tiles of at most 64 tokens), then
+// A_TMEM_STAGES buffers of 64 columns (128 rows x 128 bf16 each).
+constexpr uint32_t ACC_STRIDE_SMALL = 64;
+constexpr uint32_t A_TMEM_COL0 = 2 * ACC_STRIDE_SMALL;
+constexpr int A_TMEM_STAGES = 4;
+static_assert(A_TMEM_COL0 + 64 * A_TMEM_STAGES <= TMEM_COLS, "tensor memory budget");
 constexpr int EPI_WARPS = 4;
 // FP8 weights: converter warps dequantize each stage's e4m3 weight image into
 // the bf16 A buffer, four threads per weight row (32 weights each).  A slot of
@@ -99,7 +106,7 @@ constexpr int CONV_CPT = 8 / CONV_TPR;           // 16-weight chunks of a stage 
 static_assert(FP8_IMAGE_BYTES == PM * 128 && FP8_STAGE_BYTES % 1024 == 0 && CONV_TPR * CONV_CPT == 8 &&
                   CONV_CPT <= 4,
               "converter geometry");
-constexpr int MAX_F8 = 4;           // slots
+constexpr int MAX_F8 = 6;           // slots
 constexpr int MAX_SPS = 2;          // stages per slot
 constexpr int MAX_FULL = MAX_F8 * MAX_SPS > MAX_STAGES ? MAX_F8 * MAX_SPS : MAX_STAGES;
 
@@ -132,6 +139,8 @@ struct PairParams {
   int f8_off;               // byte offset of the slot ring
   int slot_bytes;           // bytes of one slot
   int x_kb_bytes;           // bytes of one k-block of the largest token box of the launch
+  int a_tmem;               // FP8: the converted A operand lives in tensor memory (A_TMEM_STAGES buffers)
+  uint32_t acc_stride;      // tensor-memory columns between the two accumulators
 };
 
 struct PairCtrl {
@@ -490,6 +499,22 @@ __device__ void pair_producer_fp8(PairCtrl* c, const PairParams& p, uint8_t* sta
     if (used & (1u << s)) pair_wait(&c->f8_empty[s], (used_par >> s) & 1u, c, peer_abort, p.status);
 }
 
+// 16 e4m3 values (k order) times a power-of-two scale -> 8 words of bf16 pairs
+// (exact: e4m3 -> f16 -> f32 conversions are exact and so is the product).
+__device__ __forceinline__ void convert_e4m3x16(const uint4 q, float scale, uint32_t* o) {
+  const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2(__nv_fp8x2_storage_t(qw[i] & 0xffffu), __NV_E4M3);
+    const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2(__nv_fp8x2_storage_t(qw[i] >> 16), __NV_E4M3);
+    const float2 a = __half22float2(__half2(lo)), b = __half22float2(__half2(hi));
+    const __nv_bfloat162 x = __floats2bfloat162_rn(a.x * scale, a.y * scale);
+    const __nv_bfloat162 y = __floats2bfloat162_rn(b.x * scale, b.y * scale);
+    o[2 * i] = *reinterpret_cast<const uint32_t*>(&x);
+    o[2 * i + 1] = *reinterpret_cast<const uint32_t*>(&y);
+  }
+}
+
 // FP8 converter warps: thread i owns 16-weight chunks (i / 128) * CONV_CPT ..
 // of weight row i % 128 of this CTA's 128 (all in one 64-weight k-block).
 // Per stage it reads those e4m3 bytes (128-byte swizzle) and the block's scale
@@ -498,14 +523,19 @@ __device__ void pair_producer_fp8(PairCtrl* c, const PairParams& p, uint8_t* sta
 // issuer on the even CTA (on the stage's barrier, which also counts the token
 // tile's bytes).  The arrival orders the writes at CTA scope only: each CTA's
 // tensor core reads its own A rows, so the data never crosses CTAs.
-__device__ void pair_converter(PairCtrl* c, const PairParams& p, uint8_t* stages, int cw, int lane,
+// With A in tensor memory the warp's lane quarter fixes its rows (warp % 4),
+// and the four warps of a quarter take 32 weights of the stage row each; a
+// thread writes its 16 columns with one tcgen05.st.
+__device__ void pair_converter(PairCtrl* c, const PairParams& p, uint8_t* stages, uint32_t tmem, int warp, int lane,
                                uint32_t peer_abort) {
   uint8_t* ring = stages + p.f8_off;
+  const int cw = warp - THREADS / 32;
   const int ct = cw * 32 + lane;
-  const int r = ct % PM;                  // weight row within this CTA's 128
-  const int c0 = (ct / PM) * CONV_CPT;    // first 16-weight chunk of the stage row
+  const int r = p.a_tmem ? (warp & 3) * 32 + lane : ct % PM;   // weight row within this CTA's 128
+  const int c0 = p.a_tmem ? (cw / 4) * CONV_CPT : (ct / PM) * CONV_CPT;   // first 16-weight chunk
   const int h = c0 / 4;                   // its k-block
   const int sw = r & 7;                   // 128-byte swizzle phase of that row
+  const uint32_t a_lane = uint32_t((warp & 3) * 32) << 16;
   RingPos slot, stage, fpos;      // slot ring, A buffers, per-stage barriers
   const int nfull = p.nf * p.sps;
   bool ok = true;
@@ -529,24 +559,34 @@ __device__ void pair_converter(PairCtrl* c, const PairParams& p, uint8_t* stages
       const uint8_t* src = ring + size_t(slot.i) * p.slot_bytes + size_t(half) * FP8_STAGE_BYTES;
       const float scale = reinterpret_cast<const float*>(src + FP8_IMAGE_BYTES)[h * PM + r];
       src += r * 128;
+      if (p.a_tmem) {
+        // the MMAs that read this A buffer completed (empty wait above)
+        tc_fence_after();
+        uint32_t o[16];
+#pragma unroll
+        for (int qc = 0; qc < CONV_CPT; ++qc) {
+          const uint4 q = *reinterpret_cast<const uint4*>(src + (((c0 + qc) ^ sw) << 4));
+          convert_e4m3x16(q, scale, o + 8 * qc);
+        }
+        // 32 bf16 = 16 columns at k offset 16 * c0 of the stage
+        tmem_st16(tmem + a_lane + A_TMEM_COL0 + uint32_t(stage.i) * 64u + uint32_t(c0) * 8u, o);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote_cta(map_to_rank(smem_u32(&c->full[fpos.i]), 0));
+        stage.next(p.stages);
+        fpos.next(nfull);
+        if (half == p.sps - 1 || ks == nks - 1) slot.next(p.nf);
+        continue;
+      }
       uint8_t* kb = stages + size_t(stage.i) * p.stage_bytes + h * A_KB_BYTES + r * 128;
 #pragma unroll
       for (int qc = 0; qc < CONV_CPT; ++qc) {
         // e4m3 chunk c0 + qc of the stage row: weights 16 q4 .. 16 q4 + 15 of k-block h
         const int q4 = (c0 + qc) & 3;
         const uint4 q = *reinterpret_cast<const uint4*>(src + (((c0 + qc) ^ sw) << 4));
-        const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
         uint32_t o[8];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2(__nv_fp8x2_storage_t(qw[i] & 0xffffu), __NV_E4M3);
-          const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2(__nv_fp8x2_storage_t(qw[i] >> 16), __NV_E4M3);
-          const float2 a = __half22float2(__half2(lo)), b = __half22float2(__half2(hi));
-          const __nv_bfloat162 x = __floats2bfloat162_rn(a.x * scale, a.y * scale);
-          const __nv_bfloat162 y = __floats2bfloat162_rn(b.x * scale, b.y * scale);
-          o[2 * i] = *reinterpret_cast<const uint32_t*>(&x);
-          o[2 * i + 1] = *reinterpret_cast<const uint32_t*>(&y);
-        }
+        convert_e4m3x16(q, scale, o);
         // bf16 16-byte chunks 2 q4 and 2 q4 + 1 of row r of k-block h
         const int j = 2 * q4;
         *reinterpret_cast<uint4*>(kb + ((j ^ sw) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
@@ -581,7 +621,7 @@ __device__ void pair_mma(PairCtrl* c, const PairParams& p, uint8_t* stages, uint
     const int acc = ctr & 1;
     if (!pair_wait(&c->tempty[acc], (uint32_t(ctr >> 1) & 1u) ^ 1u, c, peer_abort, p.status, true)) break;
     tc_fence_after();
-    const uint32_t d_tmem = tmem + uint32_t(acc) * ACC_STRIDE;
+    const uint32_t d_tmem = tmem + uint32_t(acc) * p.acc_stride;
     const int nks = (p.K[t.cls] / BK + KB_STAGE - 1) / KB_STAGE;
     const uint32_t b_kb = uint32_t(x_kb_bytes(t.n_mma));
     for (int ks = 0; ks < nks; ++ks) {
@@ -595,12 +635,23 @@ __device__ void pair_mma(PairCtrl* c, const PairParams& p, uint8_t* stages, uint
       const uint32_t b0 = FP8 ? smem_u32(stages + p.f8_off + size_t(slot) * p.slot_bytes +
                                          size_t(p.sps) * FP8_STAGE_BYTES + size_t(half) * KB_STAGE * p.x_kb_bytes)
                               : a0 + A_BYTES;
+      if (FP8 && p.a_tmem) {
+        // A buffer `stage` in tensor memory: 8 columns per 16 k
+        const uint32_t a_t = tmem + A_TMEM_COL0 + uint32_t(stage) * 64u;
 #pragma unroll
-      for (int j = 0; j < KB_STAGE; ++j)
+        for (int j = 0; j < KB_STAGE; ++j)
 #pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk)
-          mma_bf16_pair(d_tmem, sw128_kmajor_desc(a0 + j * A_KB_BYTES + kk * 32),
-                        sw128_kmajor_desc(b0 + j * b_kb + kk * 32), idesc, (ks | j | kk) != 0 ? 1u : 0u);
+          for (int kk = 0; kk < BK / 16; ++kk)
+            mma_bf16_pair_ta(d_tmem, a_t + uint32_t(j * 32 + kk * 8), sw128_kmajor_desc(b0 + j * b_kb + kk * 32),
+                             idesc, (ks | j | kk) != 0 ? 1u : 0u);
+      } else {
+#pragma unroll
+        for (int j = 0; j < KB_STAGE; ++j)
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)
+            mma_bf16_pair(d_tmem, sw128_kmajor_desc(a0 + j * A_KB_BYTES + kk * 32),
+                          sw128_kmajor_desc(b0 + j * b_kb + kk * 32), idesc, (ks | j | kk) != 0 ? 1u : 0u);
+      }
       mma_commit_pair(&c->empty[stage], 0x3);
       if (++stage == p.stages) {
         stage = 0;
@@ -644,7 +695,7 @@ __device__ void pair_epilogue(PairCtrl* c, const PairParams& p, uint32_t tmem, i
     const int acc = ctr & 1;
     if (!pair_warp_wait(&c->tfull[acc], uint32_t(ctr >> 1) & 1u, c, peer_abort, p.status, lane)) break;
     tc_fence_after();
-    const uint32_t tbase = tmem + uint32_t(acc) * ACC_STRIDE + (uint32_t(q * 32) << 16);
+    const uint32_t tbase = tmem + uint32_t(acc) * p.acc_stride + (uint32_t(q * 32) << 16);
     const long long row0 = (long long)t.row_start + (long long)t.tb * PN;
     const int ncols = (t.n_valid + 15) & ~15;
     const bool gemm1 = t.cls == C1R || t.cls == C1S;
@@ -768,7 +819,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FP8 ? THREADS_FP8 : 
   } else if (warp < 2 + EPI_WARPS) {
     pair_epilogue(c, p, tmem, warp, lane, rank, peer_abort);
   } else if (warp >= THREADS / 32) {
-    pair_converter(c, p, stages, warp - THREADS / 32, lane, peer_abort);
+    pair_converter(c, p, stages, tmem, warp, lane, peer_abort);
   } else {
     // scheduler warp: the routed tables need the dispatch offsets
     pdl_wait();
@@ -866,10 +917,15 @@ cudaError_t launch_pair_experts(const PairClass cls[4], const int32_t* offsets, 
     // each holding the weight images and token tiles of sps stages: decode-
     // sized launches take two stages per slot (groups of at most 16 tokens:
     // 4 slots of 38 KB; at most 64: 3 of 50 KB), others one (3 slots of 49 KB)
+    // Decode-sized launches put the A buffers in tensor memory (the
+    // accumulators need at most 64 columns there), which leaves all of the
+    // ring to the slots: 5 of 38 KB (groups of at most 16 tokens) or 4 of 50 KB.
     const bool tiny = max_group_rows <= 2 * XTINY;
-    p.stages = 2;
-    p.stage_bytes = A_BYTES;
-    p.f8_off = 2 * A_BYTES;
+    p.a_tmem = small ? 1 : 0;
+    p.acc_stride = small ? ACC_STRIDE_SMALL : ACC_STRIDE;
+    p.stages = small ? A_TMEM_STAGES : 2;
+    p.stage_bytes = small ? 0 : A_BYTES;
+    p.f8_off = small ? 0 : 2 * A_BYTES;
     p.sps = small ? 2 : 1;
     p.x_kb_bytes = tiny ? XT_KB_BYTES : (small ? XS_KB_BYTES : B_KB_BYTES);
     p.slot_bytes = p.sps * (FP8_STAGE_BYTES + KB_STAGE * p.x_kb_bytes);
@@ -878,6 +934,7 @@ cudaError_t launch_pair_experts(const PairClass cls[4], const int32_t* offsets, 
     e = launch_pair<true>(p, max_tiles, stream);
   } else {
     p.stages = small ? MAX_STAGES : 3;
+    p.acc_stride = ACC_STRIDE;
     e = launch_pair<false>(p, max_tiles, stream);
   }
   if (e == cudaSuccess && launches) ++*launches;

@@ -120,6 +120,14 @@ WORKLOADS["v3_profile_e8_t1024"] = Workload(
     topk_method="group_limited_greedy", n_group=4, topk_group=2, group_score="sum_top", group_top=2,
     norm_topk=True, routed_scaling_factor=2.5, act_dtype="bf16", gate_w_dtype="bf16", bias="normal0.1")
 
+# A V3-shaped decode step (one token, top-8) over 16 experts with FP8 weights
+# (0.7 GB of e4m3 weights): the profiler's case for the FP8 expert kernel.
+WORKLOADS["v3_profile_fp8_e16_t1"] = Workload(
+    name="v3_profile_fp8_e16_t1", T=1, d=7168, E=16, I=2048, k=8, n_shared=1, score_fn="sigmoid",
+    topk_method="group_limited_greedy", n_group=1, topk_group=1, group_score="sum_top", group_top=2,
+    norm_topk=True, routed_scaling_factor=2.5, act_dtype="bf16", gate_w_dtype="bf16", bias="zipf",
+    expert_w_dtype="fp8")
+
 CONFIG_ORDER = ["tiny_fp32_t128", "v2lite_t4096", "v2_t8192", "v3_prefill_t16384",
                 "v3_decode_t1", "v3_decode_t8", "v3_decode_t64", "v3_decode_t512"]
 DECODE_T = (1, 8, 64, 512)

@@ -23,6 +23,10 @@ What it computes (one token u_t at a time, all in float64 unless stated):
   9. FP8 expert weights: each run of 64 consecutive weights along a row is
      stored as FP8 e4m3 values times one power-of-two scale; the layer then
      computes steps 1-7 with the dequantized weights.
+ 10. backward (training): the gradient of <dout, out> with respect to x, W_g
+     and every expert weight, by the chain rule through steps 7, 6 and 2 with
+     the expert choice of step 5 held fixed (a choice is piecewise constant in
+     the inputs; the selection bias carries no gradient).
 
 Sources (page title, section):
   * "DeepSeek-V2" walkthrough (xingfushuangcheng.com): the DeepSeekMoE output
@@ -457,3 +461,105 @@ def fp8_dequantized(w: np.ndarray) -> np.ndarray:
     """The weights the FP8 layer computes with (step 9)."""
     q, s = quantize_fp8_blocks(w)
     return dequantize_fp8_blocks(q, s)
+
+
+# ------------------------------------------------------------------- backward
+
+def silu_grad(z: np.ndarray) -> np.ndarray:
+    """d silu / dz = sigma(z) * (1 + z * (1 - sigma(z)))."""
+    sg = 1.0 / (1.0 + np.exp(-z))
+    return sg * (1.0 + z * (1.0 - sg))
+
+
+def swiglu_backward(u: np.ndarray, w1, w3, w2, dy: np.ndarray):
+    """Gradients of y = W2 (silu(W1 u) * (W3 u)) for rows u [n,d] and upstream
+    dy [n,d]: returns (du [n,d], dW1 [h,d], dW3 [h,d], dW2 [d,h])."""
+    u = np.asarray(u, np.float64)
+    w1 = np.asarray(w1, np.float64)
+    w3 = np.asarray(w3, np.float64)
+    w2 = np.asarray(w2, np.float64)
+    dy = np.asarray(dy, np.float64)
+    a = u @ w1.T
+    b = u @ w3.T
+    h = silu(a) * b
+    dw2 = dy.T @ h
+    dh = dy @ w2
+    da = dh * b * silu_grad(a)
+    db = dh * silu(a)
+    du = da @ w1 + db @ w3
+    return du, da.T @ u, db.T @ u, dw2
+
+
+def gate_backward(dg: np.ndarray, s: np.ndarray, idx: np.ndarray, cfg: OracleConfig) -> np.ndarray:
+    """d L / d logits [T,E] from d L / d g [T,k]: through step 6 (g = c * raw /
+    sum(raw) or c * raw, raw = s at the chosen experts) and step 2 (sigmoid, or
+    softmax over all E experts)."""
+    dg = np.asarray(dg, np.float64)
+    s = np.asarray(s, np.float64)
+    T, k = dg.shape
+    rows = np.arange(T)[:, None]
+    raw = s[rows, idx]
+    c = float(cfg.routed_scaling_factor)
+    if cfg.norm_topk:
+        ssum = raw.sum(axis=1, keepdims=True)
+        draw = c * (dg / ssum - np.sum(dg * raw, axis=1, keepdims=True) / (ssum * ssum))
+    else:
+        draw = c * dg
+    ds = np.zeros_like(s)
+    np.add.at(ds, (np.repeat(np.arange(T), k), np.asarray(idx).ravel()), draw.ravel())
+    if cfg.score_fn == "sigmoid":
+        return ds * s * (1.0 - s)
+    return s * (ds - np.sum(ds * s, axis=1, keepdims=True))
+
+
+def moe_backward(x, wg, bias, w1, w3, w2, shared, dout, cfg: OracleConfig,
+                 idx_override: Optional[np.ndarray] = None):
+    """Gradient of L = <dout, out> for the layer of ``moe_forward`` (step 10).
+
+    w1, w3 [E,I,d] and w2 [E,d,I] are the routed experts, ``shared`` the
+    shared expert's (W1, W3, W2) or None.  Returns a dict with dx [T,d],
+    dwg [E,d], dw1, dw3, dw2 (stacked like the weights) and dws1, dws3, dws2,
+    plus the Routing used."""
+    x = np.asarray(x, np.float64)
+    wg = np.asarray(wg, np.float64)
+    dout = np.asarray(dout, np.float64)
+    T, d = x.shape
+    E, k = cfg.E, cfg.k
+    logits = gate_logits(x, wg)
+    r = route(logits, bias, cfg)
+    idx = r.idx if idx_override is None else np.asarray(idx_override, np.int64)
+    s = r.scores
+    rows = np.arange(T)[:, None]
+    raw = s[rows, idx]                                   # [T,k] unbiased affinities of the choice
+    ssum = raw.sum(axis=1, keepdims=True)
+    c = float(cfg.routed_scaling_factor)
+    gates = c * (raw / ssum if cfg.norm_topk else raw)
+
+    dx = np.zeros((T, d), np.float64)
+    dw1 = np.zeros(np.shape(w1), np.float64)
+    dw3 = np.zeros(np.shape(w3), np.float64)
+    dw2 = np.zeros(np.shape(w2), np.float64)
+    dg = np.zeros((T, k), np.float64)
+    for e in range(E):
+        tok, slot = np.nonzero(idx == e)
+        if tok.size == 0:
+            continue
+        y = swiglu_ffn(x[tok], w1[e], w3[e], w2[e])       # expert output rows
+        dg[tok, slot] = np.sum(dout[tok] * y, axis=1)     # d L / d g_{t,j}
+        dy = gates[tok, slot][:, None] * dout[tok]
+        du, g1, g3, g2 = swiglu_backward(x[tok], w1[e], w3[e], w2[e], dy)
+        np.add.at(dx, tok, du)
+        dw1[e] += g1
+        dw3[e] += g3
+        dw2[e] += g2
+    out = {"dw1": dw1, "dw3": dw3, "dw2": dw2, "dws1": None, "dws3": None, "dws2": None}
+    if shared is not None:
+        du, g1, g3, g2 = swiglu_backward(x, *shared, dout)
+        dx += du
+        out.update(dws1=g1, dws3=g3, dws2=g2)
+
+    dl = gate_backward(dg, s, idx, cfg)
+    dx += dl @ wg
+    out.update(dx=dx, dwg=dl.T @ x, routing=r)
+    return out
+

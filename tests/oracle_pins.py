@@ -398,7 +398,59 @@ def pin_fp8_quantization(o=orc):
     assert np.array_equal(o.fp8_dequantized(exact), exact)
 
 
-ALL_PINS = [pin_brute_force_selection, pin_greedy_is_torch_topk, pin_invariants,
+def _fd_case(seed, score_fn):
+    """A small layer with well separated routing decisions."""
+    g = _rng(seed)
+    if score_fn == "softmax":
+        cfg = orc.OracleConfig(T=6, d=10, E=6, I=5, k=2, n_shared=2, score_fn="softmax",
+                               topk_method="greedy", routed_scaling_factor=1.0)
+        bias = None
+    else:
+        cfg = orc.OracleConfig(T=6, d=10, E=8, I=5, k=3, n_shared=1, score_fn="sigmoid",
+                               topk_method="group_limited_greedy", n_group=4, topk_group=2,
+                               group_score="sum_top", group_top=2, norm_topk=True, routed_scaling_factor=2.5)
+        bias = g.normal(0, 0.1, cfg.E).astype(np.float32)
+    T, d, E, I, Is = cfg.T, cfg.d, cfg.E, cfg.I, cfg.n_shared * cfg.I
+    p = {"x": g.normal(0, 1, (T, d)), "wg": g.normal(0, 0.5, (E, d)),
+         "w1": g.normal(0, 0.4, (E, I, d)), "w3": g.normal(0, 0.4, (E, I, d)), "w2": g.normal(0, 0.4, (E, d, I)),
+         "ws1": g.normal(0, 0.4, (Is, d)), "ws3": g.normal(0, 0.4, (Is, d)), "ws2": g.normal(0, 0.4, (d, Is))}
+    dout = g.normal(0, 1, (T, d))
+    return cfg, bias, p, dout
+
+
+def _fd_loss(o, cfg, bias, p, dout):
+    out, r = o.moe_forward(p["x"], p["wg"], bias, o.stacked_experts(p["w1"], p["w3"], p["w2"]),
+                           (p["ws1"], p["ws3"], p["ws2"]), cfg)
+    return float(np.sum(dout * out)), r.idx
+
+
+def pin_backward_finite_differences(o=orc):
+    """The oracle's gradients against central differences of the oracle's own
+    fp64 forward, in random directions, for every parameter (softmax greedy
+    router without renormalisation; sigmoid group-limited router with bias,
+    renormalisation and scaling).  The routing decisions must not change within
+    the step (checked)."""
+    h = 1e-6
+    for seed, score_fn in ((11, "softmax"), (12, "sigmoid")):
+        cfg, bias, p, dout = _fd_case(seed, score_fn)
+        grads = o.moe_backward(p["x"], p["wg"], bias, p["w1"], p["w3"], p["w2"], (p["ws1"], p["ws3"], p["ws2"]),
+                               dout, cfg)
+        _, idx0 = _fd_loss(o, cfg, bias, p, dout)
+        g = _rng(seed + 100)
+        for name, gname in (("x", "dx"), ("wg", "dwg"), ("w1", "dw1"), ("w3", "dw3"), ("w2", "dw2"),
+                            ("ws1", "dws1"), ("ws3", "dws3"), ("ws2", "dws2")):
+            v = g.normal(0, 1, p[name].shape)
+            plus = dict(p, **{name: p[name] + h * v})
+            minus = dict(p, **{name: p[name] - h * v})
+            lp, ip = _fd_loss(o, cfg, bias, plus, dout)
+            lm, im = _fd_loss(o, cfg, bias, minus, dout)
+            assert np.array_equal(ip, idx0) and np.array_equal(im, idx0), (name, "routing changed")
+            fd = (lp - lm) / (2 * h)
+            an = float(np.sum(grads[gname] * v))
+            assert abs(fd - an) <= 1e-6 * max(1.0, abs(an)), (score_fn, name, fd, an)
+
+
+ALL_PINS = [pin_backward_finite_differences, pin_brute_force_selection, pin_greedy_is_torch_topk, pin_invariants,
             pin_bias_only_steers_selection, pin_zero_gates_give_shared, pin_group1_is_greedy,
             pin_single_expert, pin_dense_einsum, pin_top1, pin_permutation, pin_symmetries, pin_combine,
             pin_balance_update, pin_fp8_quantization]

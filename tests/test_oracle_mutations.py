@@ -138,6 +138,32 @@ def _quant_scale_from_127(w):
     return orc.e4m3_round(b / s[..., None]).reshape(rows, cols), s
 
 
+def _silu_grad_sigma_only(z):
+    return 1.0 / (1.0 + np.exp(-z))
+
+
+def _swiglu_backward_w1_w3_swapped(u, w1, w3, w2, dy):
+    return _ORIG_SWIGLU_BACKWARD(u, w3, w1, w2, dy)
+
+
+def _gate_backward_no_renorm_term(dg, s, idx, cfg):
+    import dataclasses
+    return _ORIG_GATE_BACKWARD(dg, s, idx, dataclasses.replace(cfg, norm_topk=False)) if cfg.norm_topk else \
+        _ORIG_GATE_BACKWARD(dg, s, idx, cfg)
+
+
+def _gate_backward_softmax_diag(dg, s, idx, cfg):
+    import dataclasses
+    if cfg.score_fn != "softmax":
+        return _ORIG_GATE_BACKWARD(dg, s, idx, cfg)
+    # sigmoid-style diagonal Jacobian applied to softmax affinities
+    return _ORIG_GATE_BACKWARD(dg, s, idx, dataclasses.replace(cfg, score_fn="sigmoid"))
+
+
+_ORIG_SWIGLU_BACKWARD = orc.swiglu_backward
+_ORIG_GATE_BACKWARD = orc.gate_backward
+
+
 MUTANTS = [
     ("route", _route_ties_high, pins.pin_brute_force_selection),
     ("route", _route_biased_gates, pins.pin_bias_only_steers_selection),
@@ -156,6 +182,10 @@ MUTANTS = [
     ("balance_update", _balance_mean_counts_as_over, pins.pin_balance_update),
     ("e4m3_round", _e4m3_ties_away, pins.pin_fp8_quantization),
     ("quantize_fp8_blocks", _quant_scale_from_127, pins.pin_fp8_quantization),
+    ("silu_grad", _silu_grad_sigma_only, pins.pin_backward_finite_differences),
+    ("swiglu_backward", _swiglu_backward_w1_w3_swapped, pins.pin_backward_finite_differences),
+    ("gate_backward", _gate_backward_no_renorm_term, pins.pin_backward_finite_differences),
+    ("gate_backward", _gate_backward_softmax_diag, pins.pin_backward_finite_differences),
 ]
 
 

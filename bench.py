@@ -45,6 +45,8 @@ def parse_args(argv=None):
     p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(inputs.WORKLOADS))
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-sample", type=int, default=0, help="tokens in the oracle's timed sample (0 = auto)")
+    p.add_argument("--pass", dest="pass_", choices=["forward", "backward"], default="forward",
+                   help="backward: time moe_backward (gradients of the layer) instead of the forward")
     return p.parse_args(argv)
 
 
@@ -488,6 +490,72 @@ def run_ours(args, world, rank):
 
 # ----------------------------------------------------------- reference arm
 
+def run_backward(args, world, rank):
+    """Layer backward (moe_backward) on the workload: W warm-ups, then K timed
+    calls bracketed by CUDA events on the stream (each call synchronises the
+    stream once to read the group sizes, inside the timed region)."""
+    from mixture_experts_layer_85_b300 import _lib
+
+    wl = inputs.WORKLOADS[args.workload]
+    dev = torch.device("cuda", torch.cuda.current_device())
+    li = inputs.make_inputs(wl, dev)
+    cfg = _lib.make_config(wl)
+    g = torch.Generator().manual_seed(4242)
+    dout = torch.randn((wl.T, wl.d), generator=g).to(inputs.torch_dtype(wl.out_dtype)).to(dev)
+    E, I, d, Is = wl.E, wl.I, wl.d, wl.I_s
+    f32 = dict(dtype=torch.float32, device=dev)
+    grads = [torch.empty((wl.T, d), **f32), torch.empty((E, d), **f32), torch.empty((E, I, d), **f32),
+             torch.empty((E, I, d), **f32), torch.empty((E, d, I), **f32), torch.empty((Is, d), **f32),
+             torch.empty((Is, d), **f32), torch.empty((d, Is), **f32)]
+    ws = torch.empty(_lib.moe_backward_workspace_size(cfg), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        _lib.moe_backward(cfg, li.x, li.wg, li.bias, li.w1, li.w3, li.w2, li.ws1, li.ws3, li.ws2, dout, *grads, ws)
+
+    for _ in range(max(args.warmup, 0)):
+        step()
+    torch.cuda.synchronize()
+    K = args.steps
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler()
+    barrier(world)
+    clocks.start()
+    host_t0 = time.time()
+    t0.record(stream)
+    for _ in range(K):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    host_t1 = time.time()
+    barrier(world)
+    clk = clocks.stop(host_t0, host_t1)
+    code, word = _lib.moe_get_device_status(ws)
+    if code != 0:
+        raise RuntimeError(f"device status after timed steps: {_lib.moe_status_string(code)} ({word})")
+    elapsed = max_over_ranks(t0.elapsed_time(t1) / 1e3, world)
+    # algorithmic FLOPs: the expert GEMMs of the forward recomputation (6 d I
+    # per routed row and per token for the shared expert) and of the backward
+    # proper (twice that: data and weight gradients), plus the router's
+    # logits, d logits -> dW_g and dx (2 d E per token each)
+    fwd = 6.0 * d * I * wl.T * wl.k + 6.0 * d * Is * wl.T
+    flops = 3.0 * fwd + 6.0 * d * E * wl.T
+    peaks = measured_peaks()
+    tflops = flops / (elapsed / K) / 1e12
+    return {"metric": "tokens/s per MoE layer bwd", "value": round(whole_job_rate(wl.T * K, world, elapsed), 1),
+            "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+            "ms_per_step": round(elapsed / K * 1e3, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": wl.name, "T": wl.T, "d": d, "E": E, "I": I, "k": wl.k, "n_shared": wl.n_shared,
+                       "pass": "backward", "parallelism": f"replicas x{world}"},
+            "tflops": round(tflops, 2),
+            "roofline": {"bound": "tensor", "achieved": round(tflops, 2), "peak": peaks["bf16_tflops_sustained"],
+                         "unit": "TFLOP/s", "frac": round(tflops / peaks["bf16_tflops_sustained"], 4),
+                         "kernel": "whole backward (cuBLAS expert GEMMs + own kernels)", "traffic": None,
+                         "peak_source": peaks["source"] + " sustained bf16"},
+            "clocks": clk}
+
+
 def run_reference(args, world, rank):
     if rank != 0:
         return None
@@ -524,7 +592,7 @@ def main(argv=None):
     else:
         if not torch.cuda.is_available():
             raise SystemExit("bench.py needs a CUDA GPU for --impl ours")
-        res = run_ours(args, world, rank)
+        res = run_backward(args, world, rank) if args.pass_ == "backward" else run_ours(args, world, rank)
     if rank == 0 and res is not None:
         print(json.dumps(res), flush=True)
     if world > 1:

@@ -186,6 +186,37 @@ MOE_API moe_status moe_permute_noalloc(const moe_config* cfg, const void* x, con
                                        int32_t* tok2row, void* x_perm, int32_t* device_status,
                                        void* stream);
 
+/* Bytes of workspace moe_backward needs for `cfg` (the forward's workspace
+ * plus the backward's buffers).  bf16 activations and bf16 expert weights
+ * only (MOE_ERR_UNSUPPORTED otherwise). */
+MOE_API moe_status moe_backward_workspace_size(const moe_config* cfg, size_t* bytes);
+
+/* Backward of the layer: the gradient of L = <dout, out> with respect to x,
+ * W_g and every expert weight, by the chain rule through the gate-weighted sum
+ * and the shared expert (MoE listing), the SwiGLU experts (intelliparadigm.com
+ * page section 3.3.1), the gate values (renormalised and scaled, V3 page
+ * section 1.2) and the affinities (softmax over all experts or sigmoid), with
+ * the expert choice of the forward held fixed (the selection bias carries no
+ * gradient).
+ *   x [T,d] bf16, Wg [E,d] gate_w_dtype, bias [E] fp32 or NULL (as for
+ *   moe_gate_topk: the routing is recomputed with the forward's kernels).
+ *   W1, W3 [E,I,d], W2 [E,d,I], Ws1, Ws3 [I_s,d], Ws2 [d,I_s]: the unpacked
+ *   bf16 weights (as given to moe_prepack_experts; Ws* unused when
+ *   n_shared = 0).  dout [T,d] out_dtype: the upstream gradient.
+ *   Outputs (device, fp32, written, not accumulated): dx [T,d], dWg [E,d],
+ *   dW1, dW3 [E,I,d], dW2 [E,d,I], dWs1, dWs3 [I_s,d], dWs2 [d,I_s].
+ *   ws: >= moe_backward_workspace_size bytes, 16-byte aligned.
+ * The per-expert matrix products run in cuBLAS (bf16 operands, fp32
+ * accumulation and outputs); the routed rows' intermediate gradients are
+ * rounded to bf16 before their products, as the forward rounds H.  The call
+ * reads the group sizes back to the host and so synchronises `stream` once.
+ * All pointers 16-byte aligned. */
+MOE_API moe_status moe_backward(const moe_config* cfg, const void* x, const void* Wg, const float* bias,
+                                const void* W1, const void* W3, const void* W2, const void* Ws1,
+                                const void* Ws3, const void* Ws2, const void* dout, float* dx, float* dWg,
+                                float* dW1, float* dW3, float* dW2, float* dWs1, float* dWs3, float* dWs2,
+                                void* ws, size_t ws_bytes, void* stream);
+
 /* Auxiliary-loss-free load balancing after a layer step (V3 architecture
  * page, section 1.2), with the load statistics of the balance-loss listing
  * (Tencent Cloud DeepSeek page).

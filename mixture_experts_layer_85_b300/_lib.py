@@ -30,7 +30,7 @@ MOE_GROUP_MAX, MOE_GROUP_SUM_TOP = 0, 1
 EXPORTED = ["moe_workspace_size", "moe_packed_size", "moe_prepack_experts", "moe_gate_topk", "moe_permute",
             "moe_grouped_swiglu", "moe_combine", "moe_forward", "moe_get_device_status", "moe_status_string",
             "moe_launch_count", "moe_forward_kernel_count", "moe_profile_arm", "moe_forward_stage_name",
-            "moe_permute_noalloc", "moe_balance_update"]
+            "moe_permute_noalloc", "moe_balance_update", "moe_backward_workspace_size", "moe_backward"]
 MOE_FORWARD_STAGES = 4
 
 
@@ -64,6 +64,8 @@ _sigs = {
     "moe_forward_stage_name": [ctypes.c_int32],
     "moe_permute_noalloc": [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P],
     "moe_balance_update": [_CFG, _P, _P, ctypes.c_float, _P, _P, _P],
+    "moe_backward_workspace_size": [_CFG, ctypes.POINTER(_SZ)],
+    "moe_backward": [_CFG] + [_P] * 19 + [_SZ, _P],
 }
 for _name, _args in _sigs.items():
     _f = getattr(_lib, _name)
@@ -180,6 +182,22 @@ def moe_balance_update(cfg, counts, bias, gamma: float, stats=None, device_statu
     """Aux-loss-free bias update from per-expert counts (bias updated in place)."""
     _check(_lib.moe_balance_update(ctypes.byref(cfg), _ptr(counts), _ptr(bias), float(gamma), _ptr(stats),
                                    _ptr(device_status), _stream(stream)), "moe_balance_update")
+
+
+def moe_backward_workspace_size(cfg: moe_config) -> int:
+    n = _SZ(0)
+    _check(_lib.moe_backward_workspace_size(ctypes.byref(cfg), ctypes.byref(n)), "moe_backward_workspace_size")
+    return n.value
+
+
+def moe_backward(cfg, x, Wg, bias, W1, W3, W2, Ws1, Ws3, Ws2, dout, dx, dWg, dW1, dW3, dW2, dWs1, dWs3, dWs2, ws,
+                 stream=None):
+    """Gradients of <dout, out> (fp32 outputs written in place); synchronises the stream once."""
+    _check(_lib.moe_backward(ctypes.byref(cfg), _ptr(x), _ptr(Wg), _ptr(bias), _ptr(W1), _ptr(W3), _ptr(W2),
+                             _ptr(Ws1), _ptr(Ws3), _ptr(Ws2), _ptr(dout), _ptr(dx), _ptr(dWg), _ptr(dW1), _ptr(dW3),
+                             _ptr(dW2), _ptr(dWs1), _ptr(dWs3), _ptr(dWs2), _ptr(ws), ws.numel() * ws.element_size(),
+                             _stream(stream)),
+           "moe_backward")
 
 
 def moe_get_device_status(ws, stream=None) -> tuple:

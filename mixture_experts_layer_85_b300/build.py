@@ -14,7 +14,7 @@ NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "-DMOE_BUILD", "-I", os.path.join(ROOT, "include")]
-SOURCES = ["api.cu", "gate.cu", "permute.cu", "gemm_tc.cu", "gemm_pair.cu", "experts.cu", "balance.cu", "permute_noalloc.cu"]
+SOURCES = ["api.cu", "gate.cu", "permute.cu", "gemm_tc.cu", "gemm_pair.cu", "experts.cu", "balance.cu", "permute_noalloc.cu", "backward.cu"]
 
 
 def _newest_input():
@@ -42,7 +42,9 @@ def build(force: bool = False, verbose: bool = False) -> str:
     with ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 1)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
     tmp = LIB + ".tmp"
-    r = subprocess.run([NVCC, *ARCH, "-shared", "-o", tmp, *objs], capture_output=True, text=True)
+    r = subprocess.run([NVCC, *ARCH, "-shared", "-o", tmp, *objs, "-lcublas", "-Xlinker", "-rpath",
+                        "-Xlinker", os.path.join(os.path.dirname(os.path.dirname(NVCC)), "lib64")],
+                       capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr}")
     os.replace(tmp, LIB)

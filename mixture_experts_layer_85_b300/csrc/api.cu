@@ -415,6 +415,117 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const void* Wg, con
   return st;
 }
 
+moe_status moe_backward_workspace_size(const moe_config* cfg, size_t* bytes) {
+  moe_status st = check_config(cfg);
+  if (st != MOE_OK) return st;
+  if (bytes == nullptr) return MOE_ERR_INVALID_ARG;
+  const moe_config& c = *cfg;
+  if (!is_bf16(c) || c.expert_w_dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  *bytes = ws_layout(c).total + backward_extra_bytes(c);
+  return MOE_OK;
+}
+
+moe_status moe_backward(const moe_config* cfg, const void* x, const void* Wg, const float* bias, const void* W1,
+                        const void* W3, const void* W2, const void* Ws1, const void* Ws3, const void* Ws2,
+                        const void* dout, float* dx, float* dWg, float* dW1, float* dW3, float* dW2, float* dWs1,
+                        float* dWs3, float* dWs2, void* ws, size_t ws_bytes, void* stream) {
+  moe_status st = check_config(cfg);
+  if (st != MOE_OK) return st;
+  const moe_config& c = *cfg;
+  if (!is_bf16(c) || c.expert_w_dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  const bool shared = c.n_shared > 0;
+  const void* need[] = {x, Wg, W1, W3, W2, dout, dx, dWg, dW1, dW3, dW2};
+  for (const void* q : need)
+    if (q == nullptr || !aligned16(q)) return MOE_ERR_INVALID_ARG;
+  if (shared) {
+    const void* need_s[] = {Ws1, Ws3, Ws2, dWs1, dWs3, dWs2};
+    for (const void* q : need_s)
+      if (q == nullptr || !aligned16(q)) return MOE_ERR_INVALID_ARG;
+  }
+  if (bias && !aligned16(bias)) return MOE_ERR_INVALID_ARG;
+  if (ws == nullptr || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
+  Ws W;
+  W.base = static_cast<char*>(ws);
+  W.L = ws_layout(c);
+  const BwdLayout B = backward_layout(c, W.L.total);
+  if (ws_bytes < W.L.total + B.total) return MOE_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (c.T == 0) {
+    // no token: every gradient is zero
+    const long long Is = I_s(c);
+    const struct {
+      void* p;
+      size_t n;
+    } z[] = {{dWg, size_t(c.E) * c.d}, {dW1, size_t(c.E) * c.I * c.d}, {dW3, size_t(c.E) * c.I * c.d},
+             {dW2, size_t(c.E) * c.d * c.I}, {dWs1, size_t(Is) * c.d}, {dWs3, size_t(Is) * c.d},
+             {dWs2, size_t(c.d) * Is}};
+    for (const auto& q : z)
+      if (q.p && q.n && cudaMemsetAsync(q.p, 0, q.n * sizeof(float), s) != cudaSuccess) return MOE_ERR_CUDA;
+    return MOE_OK;
+  }
+  if ((st = reset_status(W, s)) != MOE_OK) return st;
+  int n = 0;
+  int32_t* idx = W.at<int32_t>(W.L.idx);
+  float* w = W.at<float>(W.L.w);
+  st = run_gate(c, x, Wg, bias, idx, w, W, s, &n);
+  if (st == MOE_OK)
+    st = cuda_status(launch_permute(c, x, idx, W.at<int32_t>(W.L.counts), W.at<int32_t>(W.L.offsets),
+                                    W.at<int32_t>(W.L.row2tok), W.at<int32_t>(W.L.tok2row), W.at<void>(W.L.x_perm),
+                                    W.at<int32_t>(W.L.chunk_counts), W.at<int32_t>(W.L.chunk_base), W.status(), s, &n,
+                                    nullptr, 0));
+  count_launches(n);
+  if (st != MOE_OK) return st;
+  BwdPtrs p;
+  p.x = x;
+  p.Wg = Wg;
+  p.W1 = W1;
+  p.W3 = W3;
+  p.W2 = W2;
+  p.Ws1 = Ws1;
+  p.Ws3 = Ws3;
+  p.Ws2 = Ws2;
+  p.dout = dout;
+  p.dx = dx;
+  p.dWg = dWg;
+  p.dW1 = dW1;
+  p.dW3 = dW3;
+  p.dW2 = dW2;
+  p.dWs1 = dWs1;
+  p.dWs3 = dWs3;
+  p.dWs2 = dWs2;
+  p.idx = idx;
+  p.gates = w;
+  p.offsets = W.at<int32_t>(W.L.offsets);
+  p.row2tok = W.at<int32_t>(W.L.row2tok);
+  p.tok2row = W.at<int32_t>(W.L.tok2row);
+  p.x_perm = W.at<void>(W.L.x_perm);
+  p.Y = W.at<float>(W.L.y);
+  char* b = W.base;
+  p.G = reinterpret_cast<float*>(b + B.G);
+  p.U = reinterpret_cast<float*>(b + B.U);
+  p.dH = reinterpret_cast<float*>(b + B.dH);
+  p.dXr = reinterpret_cast<float*>(b + B.dXr);
+  p.Gs = reinterpret_cast<float*>(b + B.Gs);
+  p.Us = reinterpret_cast<float*>(b + B.Us);
+  p.dHs = reinterpret_cast<float*>(b + B.dHs);
+  p.dXs = reinterpret_cast<float*>(b + B.dXs);
+  p.dout32 = reinterpret_cast<float*>(b + B.dout32);
+  p.x32 = reinterpret_cast<float*>(b + B.x32);
+  p.wg32 = reinterpret_cast<float*>(b + B.wg32);
+  p.logits = reinterpret_cast<float*>(b + B.logits);
+  p.dl = reinterpret_cast<float*>(b + B.dl);
+  p.dg = reinterpret_cast<float*>(b + B.dg);
+  p.Hb = reinterpret_cast<__nv_bfloat16*>(b + B.Hb);
+  p.dYb = reinterpret_cast<__nv_bfloat16*>(b + B.dYb);
+  p.dGb = reinterpret_cast<__nv_bfloat16*>(b + B.dGb);
+  p.dUb = reinterpret_cast<__nv_bfloat16*>(b + B.dUb);
+  p.Hsb = reinterpret_cast<__nv_bfloat16*>(b + B.Hsb);
+  p.dGsb = reinterpret_cast<__nv_bfloat16*>(b + B.dGsb);
+  p.dUsb = reinterpret_cast<__nv_bfloat16*>(b + B.dUsb);
+  p.doutb = reinterpret_cast<__nv_bfloat16*>(b + B.doutb);
+  return cuda_status(run_backward_core(c, p, s));
+}
+
 moe_status moe_balance_update(const moe_config* cfg, const int32_t* counts, float* bias, float gamma, float* stats,
                               int32_t* device_status, void* stream) {
   moe_status st = check_config(cfg);

@@ -2,6 +2,7 @@
 #pragma once
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -161,6 +162,30 @@ struct PackedLayout {
   int bi = 0, bis = 0;   // interleave block of W1/W3 rows (routed, shared)
 };
 PackedLayout packed_layout(const moe_config& c);
+
+// --------------------------------------------------------------- backward
+// Backward-only workspace (byte offsets from `base`, 256-byte aligned).
+struct BwdLayout {
+  size_t G, U, Hb, dYb, dH, dGb, dUb, dXr, Gs, Us, Hsb, dHs, dGsb, dUsb, dXs, dout32, doutb, x32, wg32, logits, dl,
+      dg, total;
+};
+BwdLayout backward_layout(const moe_config& c, size_t base);
+size_t backward_extra_bytes(const moe_config& c);
+
+// Pointers of one backward call: the caller's tensors, the forward dispatch
+// (idx, gates, offsets, row2tok, tok2row, x_perm) and the scratch buffers.
+struct BwdPtrs {
+  const void *x, *Wg, *W1, *W3, *W2, *Ws1, *Ws3, *Ws2, *dout;
+  float *dx, *dWg, *dW1, *dW3, *dW2, *dWs1, *dWs3, *dWs2;
+  const int32_t *idx, *offsets, *row2tok, *tok2row;
+  const float* gates;
+  const void* x_perm;
+  float* Y;   // [T*k, d] fp32 expert outputs (recomputed)
+  float *G, *U, *dH, *dXr, *Gs, *Us, *dHs, *dXs, *dout32, *x32, *wg32, *logits, *dl, *dg;
+  __nv_bfloat16 *Hb, *dYb, *dGb, *dUb, *Hsb, *dGsb, *dUsb, *doutb;
+};
+// Everything after the dispatch: synchronises `s` once (group sizes).
+cudaError_t run_backward_core(const moe_config& c, const BwdPtrs& p, cudaStream_t s);
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 inline size_t dtype_bytes(int dt) { return dt == MOE_BF16 ? 2 : 4; }

@@ -1,0 +1,114 @@
+"""moe_backward (the layer's gradients) against the oracle's backward, which is
+pinned by central finite differences of the fp64 forward.
+
+The backward recomputes the routing with the forward's kernels; the test reads
+that choice through moe_gate_topk (same kernels, same result), checks it
+against the oracle's routing rules, and runs the oracle backward on the same
+choice.  Every gradient is compared element by element.  The library rounds
+the operands of each product to bf16 (H, the gate-weighted upstream rows, dG
+and dU; x and the weights are bf16 already): 2^-9 relative each, two to three
+on every path, so an element of a sum over n rows is off by about
+2^-8 * sum_r |term_r|, a few times 2^-8 of the element when the terms cancel.
+Acceptance: the relative Frobenius error ||got - ref|| / ||ref|| <= TOL_FRO of
+every gradient and of every used expert's slice (measured: 1.6e-3 to 2.4e-3,
+the 2^-9 level), and, as a coarse bound on single elements of dx, dW_g and the
+shared expert's gradients, max |got - ref| / RMS(ref) <= TOL_MAX.  A routed
+expert's weight gradient is a sum over its few rows (one row at T=1: an outer
+product), whose largest elements sit too far out in the tail of the RMS for
+that bound; its elements are covered by the per-expert Frobenius bound."""
+import numpy as np
+import pytest
+import torch
+
+from mixture_experts_layer_85_b300 import _lib, inputs
+from oracle import moe_oracle as orc
+from tests._cfg import f64, oracle_cfg
+
+pytestmark = pytest.mark.gpu
+
+TOL_FRO = 1e-2
+TOL_MAX = 1e-1
+W = inputs.WORKLOADS
+CASES = {
+    # softmax greedy, fp32 gate weight, two shared experts
+    "v2lite_bwd_t37": inputs.small_workload(W["v2lite_t4096"], name="v2lite_bwd_t37", T=37, d=256, E=16, I=128, k=6,
+                                            n_shared=2),
+    # softmax group-limited (max), scale 16
+    "v2_bwd_t29": inputs.small_workload(W["v2_t8192"], name="v2_bwd_t29", T=29, d=256, E=32, I=128, n_group=8,
+                                        topk_group=3),
+    # sigmoid + bias, group-limited sum of top-2, renormalised, scale 2.5
+    "v3_bwd_t53": inputs.small_workload(W["v3_prefill_t16384"], name="v3_bwd_t53", T=53, d=256, E=32, I=128,
+                                        n_group=8, topk_group=4),
+    "v3_bwd_t53_bf16out": inputs.small_workload(W["v3_prefill_t16384"], name="v3_bwd_t53_bf16out", T=53, d=256,
+                                                E=32, I=128, n_group=8, topk_group=4, out_dtype="bf16"),
+    # one token: most experts receive no row (their gradients are exact zeros)
+    "v3_bwd_t1": inputs.small_workload(W["v3_decode_t1"], name="v3_bwd_t1", T=1, d=256, E=32, I=128, n_group=8,
+                                       topk_group=4),
+}
+
+
+def _run(wl):
+    li = inputs.make_inputs(wl, "cuda")
+    cfg = _lib.make_config(wl)
+    g = torch.Generator().manual_seed(4242)
+    dout = torch.randn((wl.T, wl.d), generator=g).to(torch.bfloat16 if wl.out_dtype == "bf16" else torch.float32)
+    dout = dout.cuda()
+    E, I, d, Is = wl.E, wl.I, wl.d, wl.I_s
+    f32 = dict(dtype=torch.float32, device="cuda")
+    outs = {"dx": torch.empty((wl.T, d), **f32), "dwg": torch.empty((E, d), **f32),
+            "dw1": torch.full((E, I, d), float("nan"), **f32), "dw3": torch.full((E, I, d), float("nan"), **f32),
+            "dw2": torch.full((E, d, I), float("nan"), **f32), "dws1": torch.empty((Is, d), **f32),
+            "dws3": torch.empty((Is, d), **f32), "dws2": torch.empty((d, Is), **f32)}
+    ws = torch.empty(_lib.moe_backward_workspace_size(cfg), dtype=torch.uint8, device="cuda")
+    _lib.moe_backward(cfg, li.x, li.wg, li.bias, li.w1, li.w3, li.w2, li.ws1, li.ws3, li.ws2, dout,
+                      outs["dx"], outs["dwg"], outs["dw1"], outs["dw3"], outs["dw2"], outs["dws1"], outs["dws3"],
+                      outs["dws2"], ws)
+    torch.cuda.synchronize()
+    code, word = _lib.moe_get_device_status(ws)
+    assert code == _lib.MOE_OK, (_lib.moe_status_string(code), word)
+    # the routing the backward used (same kernels)
+    idx = torch.empty((wl.T, wl.k), dtype=torch.int32, device="cuda")
+    w = torch.empty((wl.T, wl.k), dtype=torch.float32, device="cuda")
+    fws = torch.empty(_lib.moe_workspace_size(cfg), dtype=torch.uint8, device="cuda")
+    _lib.moe_gate_topk(cfg, li.x, li.wg, li.bias, idx, w, fws)
+    torch.cuda.synchronize()
+    return li, dout, outs, idx.cpu().numpy().astype(np.int64)
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_backward_matches_oracle(name):
+    wl = CASES[name]
+    li, dout, outs, gidx = _run(wl)
+    cfg = oracle_cfg(wl)
+    bias = None if li.bias is None else li.bias.float().cpu().numpy()
+    r = orc.route(orc.gate_logits(f64(li.x), f64(li.wg)), bias, cfg)
+    same = (np.sort(gidx, 1) == np.sort(r.idx, 1)).all(1)
+    assert (same | r.near_tie).all(), "expert sets differ on non-tie tokens"
+    for t in np.nonzero(~same)[0]:
+        assert orc.is_valid_selection(gidx[t], r.sel32[t], cfg), t
+    shared = (f64(li.ws1), f64(li.ws3), f64(li.ws2)) if wl.n_shared else None
+    ref = orc.moe_backward(f64(li.x), f64(li.wg), bias, f64(li.w1), f64(li.w3), f64(li.w2), shared, f64(dout), cfg,
+                           idx_override=gidx)
+
+    def fro(got, want):
+        return float(np.linalg.norm(got - want) / max(np.linalg.norm(want), 1e-300))
+
+    used = np.zeros(wl.E, bool)
+    used[np.unique(gidx)] = True
+    errs = {}
+    for key in ("dx", "dwg", "dw1", "dw3", "dw2", "dws1", "dws3", "dws2"):
+        if ref[key] is None:
+            continue
+        got = f64(outs[key])
+        assert np.isfinite(got).all(), key
+        errs[key] = (fro(got, ref[key]), orc.relative_error(got, ref[key]))
+        if key in ("dw1", "dw3", "dw2"):
+            worst = max(fro(got[e], ref[key][e]) for e in np.nonzero(used)[0])
+            assert worst <= TOL_FRO, (key, "per expert", worst)
+            # experts without a routed row: their gradients are exact zeros
+            assert not got[~used].any(), key
+    print(name, {k: f"fro {a:.1e} max {b:.1e}" for k, (a, b) in errs.items()})
+    for key, (a, b) in errs.items():
+        assert a <= TOL_FRO, (key, a)
+        if key not in ("dw1", "dw3", "dw2"):
+            assert b <= TOL_MAX, (key, b)

@@ -674,7 +674,7 @@ __device__ void pair_mma(PairCtrl* c, const PairParams& p, uint8_t* stages, uint
 
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + __expf(-z)); }
 
-// One lane waits and the verdict is broadcast, so the warp-collective tensor
+// One lane waits and the result is broadcast, so the warp-collective tensor
 // memory loads that follow run on the whole warp.
 __device__ __forceinline__ bool pair_warp_wait(uint64_t* bar, uint32_t parity, PairCtrl* c, uint32_t peer_abort,
                                                int* status, int lane) {

@@ -287,7 +287,7 @@ __device__ void mma_issuer(Ctrl* c, const Params& p, uint8_t* stages, uint32_t t
   mbar_wait(&c->drain, 0u, nullptr, p.status);
 }
 
-// One lane waits and the verdict is broadcast, so the warp-collective TMEM
+// One lane waits and the result is broadcast, so the warp-collective TMEM
 // loads that follow are always executed by the whole warp.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* ab, int* status, int lane) {
   int ok = 1;

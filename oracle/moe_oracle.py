@@ -51,7 +51,7 @@ Sources (page title, section):
     block's largest magnitude), experts quantised independently, GEMM inputs
     dequantised before the multiplication, accumulation in higher precision.
 
-Readings where the pages are silent or garbled (all listed in the design doc):
+Readings where the pages are silent or garbled:
   * Decision precision.  The ``MoEGate`` listing holds logits and scores in
     float32 and takes ``topk`` on them.  The oracle therefore computes the
     affinities exactly (float64), rounds them once to float32, adds the float32

@@ -108,3 +108,31 @@ def test_empty_batch_launches_nothing():
                          fake, ws, None) == _lib.MOE_OK
     assert _lib.moe_forward_kernel_count(c) == 0
     assert _lib.moe_launch_count() == before
+
+
+def test_backward_workspace_and_argument_checks():
+    """moe_backward: bf16 layers with bf16 expert weights only; its workspace
+    holds the forward's; null, misaligned or short arguments are rejected
+    before any launch."""
+    c = _cfg(T=64)
+    need = _lib.moe_backward_workspace_size(c)
+    assert need > _lib.moe_workspace_size(c)
+    for kw in (dict(act_dtype=_lib.MOE_F32, gate_w_dtype=_lib.MOE_F32, out_dtype=_lib.MOE_F32,
+                    expert_w_dtype=_lib.MOE_F32),
+               dict(expert_w_dtype=_lib.MOE_FP8_E4M3)):
+        bad = _cfg(T=64, **kw)
+        n = ctypes.c_size_t(0)
+        assert _lib.raw_call("moe_backward_workspace_size", ctypes.byref(bad), ctypes.byref(n)) == \
+            _lib.MOE_ERR_UNSUPPORTED
+    fake = 1 << 40                     # never dereferenced: validation fails first
+    ptrs = [fake] * 18                 # x, Wg, bias, W1, W3, W2, Ws1, Ws3, Ws2, dout, dx, dWg, dW1..dWs2
+    before = _lib.moe_launch_count()
+    args = list(ptrs)
+    args[0] = None                     # x
+    assert _lib.raw_call("moe_backward", ctypes.byref(c), *args, fake, need, None) == _lib.MOE_ERR_INVALID_ARG
+    args = list(ptrs)
+    args[11] = fake + 4                # dWg misaligned
+    assert _lib.raw_call("moe_backward", ctypes.byref(c), *args, fake, need, None) == _lib.MOE_ERR_INVALID_ARG
+    assert _lib.raw_call("moe_backward", ctypes.byref(c), *ptrs, fake, need - 1, None) == _lib.MOE_ERR_WORKSPACE
+    assert _lib.moe_launch_count() == before
+

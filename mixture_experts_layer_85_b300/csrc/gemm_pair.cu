@@ -44,9 +44,13 @@
 //               issues the M=256 MMAs and commits to both CTAs' barriers
 //   warps 2..5  epilogue: tcgen05.ld of this CTA's 128 accumulator rows
 //   warp 6      tile scheduler (routed tile tables)
-// Two 256-column accumulators per CTA let the epilogue overlap the next
-// tile's main loop.  Every wait is bounded; a CTA that gives up flags the
-// status word and tells its peer to stop too.
+//   warps 7..22 FP8 weights only (736 threads): converter warps that turn
+//               each stage's e4m3 weight image into the bf16 A operand (in
+//               shared memory, or in tensor memory for decode-sized launches)
+// Two accumulators per CTA (256 columns each; 64 for FP8 decode-sized
+// launches) let the epilogue overlap the next tile's main loop.  Every wait
+// is bounded; a CTA that gives up flags the status word and tells its peer to
+// stop too.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 

@@ -210,6 +210,8 @@ MOE_API moe_status moe_backward_workspace_size(const moe_config* cfg, size_t* by
  * accumulation and outputs); the routed rows' intermediate gradients are
  * rounded to bf16 before their products, as the forward rounds H.  The call
  * reads the group sizes back to the host and so synchronises `stream` once.
+ * All calls share one cuBLAS handle (created on the first call, its stream set
+ * per call): serialise backward calls made from several host threads.
  * All pointers 16-byte aligned. */
 MOE_API moe_status moe_backward(const moe_config* cfg, const void* x, const void* Wg, const float* bias,
                                 const void* W1, const void* W3, const void* W2, const void* Ws1,

@@ -450,7 +450,33 @@ def pin_backward_finite_differences(o=orc):
             assert abs(fd - an) <= 1e-6 * max(1.0, abs(an)), (score_fn, name, fd, an)
 
 
-ALL_PINS = [pin_backward_finite_differences, pin_brute_force_selection, pin_greedy_is_torch_topk, pin_invariants,
+def pin_backward_homogeneity(o=orc):
+    """Exact identities of the gradient (Euler's theorem for homogeneous
+    functions): the output is linear in (W2, Ws2) jointly and in (W3, Ws3)
+    jointly, so sum <dW, W> over each pair equals <dout, out>; gradients are
+    linear in dout; with k = 1 and renormalisation the gate is the constant
+    routed_scaling_factor, so the router's gradient (dW_g) vanishes."""
+    for seed, score_fn in ((21, "softmax"), (22, "sigmoid")):
+        cfg, bias, p, dout = _fd_case(seed, score_fn)
+        shared = (p["ws1"], p["ws3"], p["ws2"])
+        gr = o.moe_backward(p["x"], p["wg"], bias, p["w1"], p["w3"], p["w2"], shared, dout, cfg)
+        loss, _ = _fd_loss(o, cfg, bias, p, dout)
+        e2 = float(np.sum(gr["dw2"] * p["w2"]) + np.sum(gr["dws2"] * p["ws2"]))
+        e3 = float(np.sum(gr["dw3"] * p["w3"]) + np.sum(gr["dws3"] * p["ws3"]))
+        assert abs(e2 - loss) <= 1e-10 * max(1.0, abs(loss)), (score_fn, e2, loss)
+        assert abs(e3 - loss) <= 1e-10 * max(1.0, abs(loss)), (score_fn, e3, loss)
+        g2 = o.moe_backward(p["x"], p["wg"], bias, p["w1"], p["w3"], p["w2"], shared, 2.0 * dout, cfg)
+        for key in ("dx", "dwg", "dw1", "dw3", "dw2", "dws1", "dws3", "dws2"):
+            assert np.allclose(g2[key], 2.0 * gr[key], rtol=1e-12, atol=1e-12), key
+    import dataclasses
+    cfg, bias, p, dout = _fd_case(23, "sigmoid")
+    cfg1 = dataclasses.replace(cfg, k=1, topk_method="greedy", n_group=1, topk_group=1, norm_topk=True)
+    g1 = o.moe_backward(p["x"], p["wg"], None, p["w1"], p["w3"], p["w2"], (p["ws1"], p["ws3"], p["ws2"]), dout,
+                        cfg1)
+    assert np.abs(g1["dwg"]).max() <= 1e-12 * max(1.0, np.abs(g1["dw1"]).max()), np.abs(g1["dwg"]).max()
+
+
+ALL_PINS = [pin_backward_finite_differences, pin_backward_homogeneity, pin_brute_force_selection, pin_greedy_is_torch_topk, pin_invariants,
             pin_bias_only_steers_selection, pin_zero_gates_give_shared, pin_group1_is_greedy,
             pin_single_expert, pin_dense_einsum, pin_top1, pin_permutation, pin_symmetries, pin_combine,
             pin_balance_update, pin_fp8_quantization]

@@ -160,6 +160,13 @@ def _gate_backward_softmax_diag(dg, s, idx, cfg):
     return _ORIG_GATE_BACKWARD(dg, s, idx, dataclasses.replace(cfg, score_fn="sigmoid"))
 
 
+def _swiglu_backward_dw2_from_gate(u, w1, w3, w2, dy):
+    du, g1, g3, g2 = _ORIG_SWIGLU_BACKWARD(u, w1, w3, w2, dy)
+    # dW2 from silu(W1 u) alone (the up projection dropped)
+    a = np.asarray(u, np.float64) @ np.asarray(w1, np.float64).T
+    return du, g1, g3, np.asarray(dy, np.float64).T @ orc.silu(a)
+
+
 _ORIG_SWIGLU_BACKWARD = orc.swiglu_backward
 _ORIG_GATE_BACKWARD = orc.gate_backward
 
@@ -186,6 +193,8 @@ MUTANTS = [
     ("swiglu_backward", _swiglu_backward_w1_w3_swapped, pins.pin_backward_finite_differences),
     ("gate_backward", _gate_backward_no_renorm_term, pins.pin_backward_finite_differences),
     ("gate_backward", _gate_backward_softmax_diag, pins.pin_backward_finite_differences),
+    ("swiglu_backward", _swiglu_backward_dw2_from_gate, pins.pin_backward_homogeneity),
+    ("gate_backward", _gate_backward_no_renorm_term, pins.pin_backward_homogeneity),
 ]
 
 

@@ -79,6 +79,7 @@ Readings where the pages are silent or garbled:
 from __future__ import annotations
 
 from dataclasses import dataclass
+from itertools import combinations
 from typing import Callable, Optional, Sequence, Tuple
 
 import numpy as np
@@ -205,6 +206,19 @@ def route(logits: np.ndarray, bias: Optional[np.ndarray], cfg: OracleConfig) -> 
 
     # near ties, judged on exact float64 selection scores
     sel64 = s + (0.0 if bias is None else np.asarray(bias, np.float64)[None, :])
+    near = near_ties(sel64, elig, cfg)
+    counts = np.bincount(idx.ravel(), minlength=E).astype(np.int64)
+    return Routing(idx=idx, gates=g, scores=s, sel32=sel32, near_tie=near, counts=counts)
+
+
+def near_ties(sel64: np.ndarray, elig: np.ndarray, cfg: OracleConfig) -> np.ndarray:
+    """[T] bool: tokens whose choice two correct implementations may make
+    differently.  With tol = NEAR_TIE_REL times the token's largest |score|
+    (exact float64 selection scores sel64), a token is a near tie when its k-th
+    and (k+1)-th eligible scores differ by less than tol, or, for group-limited
+    routing that drops groups, its topk_group-th and (topk_group+1)-th largest
+    group scores do."""
+    T, E = sel64.shape
     scale = np.abs(sel64).max(axis=1)
     near = np.zeros(T, bool)
     n_elig = elig.sum(axis=1)
@@ -218,8 +232,7 @@ def route(logits: np.ndarray, bias: Optional[np.ndarray], cfg: OracleConfig) -> 
         g64 = -np.sort(-_group_scores64(sel64, cfg), axis=1)
         ggap = g64[:, cfg.topk_group - 1] - g64[:, cfg.topk_group]
         near |= ggap < NEAR_TIE_REL * scale
-    counts = np.bincount(idx.ravel(), minlength=E).astype(np.int64)
-    return Routing(idx=idx, gates=g, scores=s, sel32=sel32, near_tie=near, counts=counts)
+    return near
 
 
 def route_tokens(x, wg, bias, cfg: OracleConfig) -> Routing:
@@ -346,9 +359,18 @@ def relative_error(got: np.ndarray, ref: np.ndarray) -> float:
 
 def is_valid_selection(idx_row: Sequence[int], sel32_row: np.ndarray, cfg: OracleConfig) -> bool:
     """True when ``idx_row`` is a correct top-k choice up to the near-tie
-    tolerance: every picked expert is eligible under some near-optimal group
-    choice and no unpicked eligible expert beats a picked one by more than the
-    tolerance.  Used to accept the other side's choice on near-tie tokens."""
+    tolerance tol (NEAR_TIE_REL times the token's largest |score|).  Used to
+    accept the other side's choice on near-tie tokens.
+
+    The choice is valid when some set K of kept groups (every expert's group
+    for greedy routing; topk_group groups otherwise) satisfies all of:
+      (a) K holds the group of every picked expert;
+      (b) no group outside K has a group score above the lowest group score
+          in K by more than tol (K is a top-topk_group set up to tol);
+      (c) no expert of K left unpicked has a selection score above the
+          lowest picked score by more than tol (the k experts are a top-k
+          set of K's experts up to tol).
+    The k experts must be distinct.  Every K is tried (at most C(8, 4) = 70)."""
     sel = np.asarray(sel32_row, np.float64)
     picked = np.asarray(list(idx_row), np.int64)
     if len(set(picked.tolist())) != cfg.k:
@@ -357,25 +379,25 @@ def is_valid_selection(idx_row: Sequence[int], sel32_row: np.ndarray, cfg: Oracl
     if cfg.topk_method == "group_limited_greedy":
         gsize = cfg.E // cfg.n_group
         g = _group_scores64(sel[None, :], cfg)[0]
-        groups = sorted(set((picked // gsize).tolist()))
-        if len(groups) > cfg.topk_group:
-            return False
-        thresh = np.sort(g)[::-1][cfg.topk_group - 1]
-        if any(g[x] < thresh - tol for x in groups):
-            return False
-        kept = set(groups)
-        # pad the kept set with the best remaining groups
-        for gg in np.argsort(-g, kind="stable"):
-            if len(kept) >= cfg.topk_group:
-                break
-            kept.add(int(gg))
-        elig = np.array([(e // gsize) in kept for e in range(cfg.E)])
+        need = set((picked // gsize).tolist())
+        candidates = []
+        for K in combinations(range(cfg.n_group), cfg.topk_group):
+            if not need <= set(K):                                   # (a)
+                continue
+            in_k = np.zeros(cfg.n_group, bool)
+            in_k[list(K)] = True
+            if (~in_k).any() and g[~in_k].max() > g[in_k].min() + tol:   # (b)
+                continue
+            candidates.append(np.repeat(in_k, gsize))
     else:
-        elig = np.ones(cfg.E, bool)
+        candidates = [np.ones(cfg.E, bool)]
     worst_picked = sel[picked].min()
-    others = np.where(elig, sel, -np.inf)
-    others[picked] = -np.inf
-    return bool(others.max() <= worst_picked + tol)
+    for elig in candidates:
+        others = np.where(elig, sel, -np.inf)
+        others[picked] = -np.inf
+        if others.max() <= worst_picked + tol:                        # (c)
+            return True
+    return False
 
 
 # ------------------------------------------------------------ load balancing

@@ -23,6 +23,7 @@ plants plausible mistakes in the oracle and checks that these pins catch them.
 from dataclasses import replace
 from fractions import Fraction
 from itertools import combinations
+import math
 
 import numpy as np
 import scipy.special
@@ -476,7 +477,150 @@ def pin_backward_homogeneity(o=orc):
     assert np.abs(g1["dwg"]).max() <= 1e-12 * max(1.0, np.abs(g1["dw1"]).max()), np.abs(g1["dwg"]).max()
 
 
+# ------------------------------------------------- acceptance functions
+
+def _perturbed_top(values, chosen, m, tol):
+    """Whether the index set `chosen` (m of them) is a top-m set by sum, under
+    some tie-break, after every chosen value is raised by tol/2 and every other
+    value lowered by tol/2 (exact rationals throughout)."""
+    v = [Fraction(x) + (tol / 2 if i in chosen else -tol / 2) for i, x in enumerate(values)]
+    best = max(sum(v[i] for i in c) for c in combinations(range(len(v)), m))
+    return sum(v[i] for i in chosen) == best
+
+
+def brute_force_valid_sets(sel_row, cfg, tol):
+    """Every k-subset of experts that the exact routing rule picks once the
+    group scores and the expert scores are each moved by at most tol/2 (the
+    two independently): a set K of topk_group groups that is a top set of the
+    perturbed group scores, then k experts of K that are a top set of the
+    perturbed expert scores.  Enumerates every K and every subset."""
+    E = sel_row.size
+    vals = [Fraction(float(v)) for v in sel_row]
+    if cfg.topk_method == "group_limited_greedy":
+        gs = E // cfg.n_group
+        gscore = []
+        for g in range(cfg.n_group):
+            members = sorted(vals[g * gs:(g + 1) * gs], reverse=True)
+            gscore.append(members[0] if cfg.group_score == "max" else sum(members[:cfg.group_top]))
+        eligible_sets = [[e for e in range(E) if e // gs in K]
+                         for K in combinations(range(cfg.n_group), cfg.topk_group)
+                         if _perturbed_top(gscore, set(K), cfg.topk_group, tol)]
+    else:
+        gscore = []
+        eligible_sets = [list(range(E))]
+    valid = set()
+    for elig in eligible_sets:
+        ev = [vals[e] for e in elig]
+        for S in combinations(range(len(elig)), cfg.k):
+            if _perturbed_top(ev, set(S), cfg.k, tol):
+                valid.add(frozenset(elig[i] for i in S))
+    return valid, gscore
+
+
+def _clear_of_boundary(vals, tol):
+    """No two values differ by tol to within 2 % (so float rounding of tol
+    cannot change a decision the test relies on)."""
+    for a, b in combinations(vals, 2):
+        if abs(abs(a - b) - tol) < tol / 50:
+            return False
+    return True
+
+
+VALID_CASES = [
+    dict(E=8, k=2, topk_method="group_limited_greedy", n_group=4, topk_group=2, group_score="max"),
+    dict(E=8, k=3, topk_method="group_limited_greedy", n_group=4, topk_group=2, group_score="sum_top",
+         group_top=2),
+    dict(E=12, k=3, topk_method="group_limited_greedy", n_group=4, topk_group=2, group_score="max"),
+    dict(E=12, k=2, topk_method="group_limited_greedy", n_group=4, topk_group=3, group_score="sum_top",
+         group_top=2),
+    dict(E=8, k=3, topk_method="greedy"),
+]
+
+
+def pin_valid_selection_brute_force(o=orc, tokens=40):
+    """is_valid_selection (the acceptance of the other side's choice on a
+    near-tie token) against brute-force enumeration: on tokens whose scores
+    crowd within a few tolerances of each other, every k-subset of experts is
+    accepted exactly when some perturbation of the scores by at most half the
+    tolerance makes the exact rule pick it."""
+    u = orc.NEAR_TIE_REL                      # tolerance per unit of the token's largest |score| (1.0 here)
+    deficits = np.array([0.0, 0.0, 0.3, 0.7, 1.6, 2.5, 4.0, 40.0]) * u
+    n_multi = 0
+    for ci, case in enumerate(VALID_CASES):
+        cfg = orc.OracleConfig(T=1, d=1, I=1, n_shared=0, score_fn="sigmoid", **case)
+        r = _rng(300 + ci)
+        kept_tokens = 0
+        for _ in range(tokens * 4):
+            base = r.choice([0.9, 0.8, 0.5], size=cfg.E, p=[0.5, 0.3, 0.2])
+            sel = (base - r.choice(deficits, size=cfg.E)).astype(np.float32)
+            sel[r.integers(cfg.E)] = np.float32(1.0)          # the token's largest |score|
+            tol = Fraction(float(np.float64(orc.NEAR_TIE_REL) * float(np.abs(sel).max())))
+            valid, gscore = brute_force_valid_sets(sel, cfg, tol)
+            if not (_clear_of_boundary([Fraction(float(v)) for v in sel], tol)
+                    and _clear_of_boundary(gscore, tol)):
+                continue
+            kept_tokens += 1
+            n_multi += len(valid) > 1
+            for S in combinations(range(cfg.E), cfg.k):
+                got = o.is_valid_selection(list(S), sel, cfg)
+                assert got == (frozenset(S) in valid), (ci, S, sel.tolist(), sorted(map(sorted, valid)))
+            if kept_tokens == tokens:
+                break
+        assert kept_tokens == tokens, (ci, kept_tokens)
+    assert n_multi >= 20, n_multi     # the cases do exercise several valid choices per token
+
+
+def _route_with_scores(o, sel_rows, cfg, shift=0.0):
+    """route() on sigmoid logits that reproduce the given selection scores
+    (before a constant selection bias `shift`)."""
+    p = np.asarray(sel_rows, np.float64)
+    logits = np.log(p / (1.0 - p))
+    bias = np.full(cfg.E, shift, np.float32) if shift else None
+    return o.route(logits, bias, cfg)
+
+
+def pin_group_near_tie_gap(o=orc):
+    """The group near-tie flag of route(): a token whose topk_group-th and
+    (topk_group+1)-th group scores differ by half the tolerance is a near tie,
+    by twice the tolerance it is not; gaps between other ranks of groups do
+    not count; the tolerance is relative to the token's largest |score|."""
+    for score, top in (("max", 1), ("sum_top", 2)):
+        cfg = orc.OracleConfig(T=4, d=1, E=8, I=1, k=2, n_shared=0, score_fn="sigmoid",
+                               topk_method="group_limited_greedy", n_group=4, topk_group=2, group_score=score,
+                               group_top=top)
+        for shift in (0.0, 9.0):
+            scale = 0.9 + shift
+            tol = orc.NEAR_TIE_REL * scale
+
+            def tok(g0, g1, g2, g3):
+                # the first expert of each group carries the group's score, the second a low 0.1
+                return [g0, 0.1, g1, 0.1, g2, 0.1, g3, 0.1]
+            rows = [tok(0.9, 0.8, 0.8 - 0.5 * tol, 0.5),     # 2nd vs 3rd group: half the tolerance
+                    tok(0.9, 0.8, 0.8 - 2.0 * tol, 0.5),     # 2nd vs 3rd group: twice the tolerance
+                    tok(0.9, 0.9 - 0.5 * tol, 0.6, 0.5),     # 1st vs 2nd group close: no effect
+                    tok(0.9, 0.8, 0.6, 0.6 - 0.5 * tol)]     # 3rd vs 4th group close: no effect
+            r = _route_with_scores(o, rows, cfg, shift)
+            assert r.near_tie.tolist() == [True, False, False, False], (score, shift, r.near_tie.tolist())
+            # the kept groups are the first two in every row, so the expert gap (0.8 -> 0.1) is wide
+            assert [sorted(i.tolist()) for i in r.idx] == [[0, 2]] * 4, r.idx
+
+
+def pin_relative_error(o=orc):
+    """relative_error = max |got - ref| / RMS(ref) over every element, on
+    hand-worked arrays (the RMS is not the mean or the largest |ref|)."""
+    ref = np.array([[3.0, 4.0]])
+    assert abs(o.relative_error(np.array([[3.5, 3.0]]), ref) - 1.0 / math.sqrt(12.5)) <= 1e-15
+    ref = np.array([1.0, -1.0, 1.0, 7.0])                       # RMS sqrt(13), mean |ref| 2.5, max |ref| 7
+    got = ref + np.array([0.0, 0.5, 0.0, -0.25])
+    assert abs(o.relative_error(got, ref) - 0.5 / math.sqrt(13.0)) <= 1e-15
+    ref = np.array([[1.0, 2.0], [3.0, 4.0]])                    # RMS sqrt(7.5)
+    got = np.array([[1.0, 2.0], [3.0, 2.5]])
+    assert abs(o.relative_error(got, ref) - 1.5 / math.sqrt(7.5)) <= 1e-15
+    assert o.relative_error(ref, ref) == 0.0
+
+
 ALL_PINS = [pin_backward_finite_differences, pin_backward_homogeneity, pin_brute_force_selection, pin_greedy_is_torch_topk, pin_invariants,
             pin_bias_only_steers_selection, pin_zero_gates_give_shared, pin_group1_is_greedy,
             pin_single_expert, pin_dense_einsum, pin_top1, pin_permutation, pin_symmetries, pin_combine,
-            pin_balance_update, pin_fp8_quantization]
+            pin_balance_update, pin_fp8_quantization, pin_valid_selection_brute_force,
+            pin_group_near_tie_gap, pin_relative_error]

@@ -167,6 +167,111 @@ def _swiglu_backward_dw2_from_gate(u, w1, w3, w2, dy):
     return du, g1, g3, np.asarray(dy, np.float64).T @ orc.silu(a)
 
 
+def _valid_selection_variant(old_threshold=False, group_tol_sign=1.0, require_groups=True, expert_tol_sign=1.0):
+    """is_valid_selection with one planted mistake (flags name it)."""
+    from itertools import combinations
+
+    def valid(idx_row, sel32_row, cfg):
+        sel = np.asarray(sel32_row, np.float64)
+        picked = np.asarray(list(idx_row), np.int64)
+        if len(set(picked.tolist())) != cfg.k:
+            return False
+        tol = orc.NEAR_TIE_REL * np.abs(sel).max()
+        if cfg.topk_method == "group_limited_greedy":
+            gsize = cfg.E // cfg.n_group
+            g = orc._group_scores64(sel[None, :], cfg)[0]
+            need = set((picked // gsize).tolist())
+            if old_threshold:
+                # groups judged against the topk_group-th best group, padded with the best others
+                if len(need) > cfg.topk_group:
+                    return False
+                thresh = np.sort(g)[::-1][cfg.topk_group - 1]
+                if any(g[x] < thresh - tol for x in need):
+                    return False
+                kept = set(need)
+                for gg in np.argsort(-g, kind="stable"):
+                    if len(kept) >= cfg.topk_group:
+                        break
+                    kept.add(int(gg))
+                cands = [np.array([(e // gsize) in kept for e in range(cfg.E)])]
+            else:
+                cands = []
+                for K in combinations(range(cfg.n_group), cfg.topk_group):
+                    if require_groups and not need <= set(K):
+                        continue
+                    in_k = np.zeros(cfg.n_group, bool)
+                    in_k[list(K)] = True
+                    if (~in_k).any() and g[~in_k].max() > g[in_k].min() + group_tol_sign * tol:
+                        continue
+                    cands.append(np.repeat(in_k, gsize))
+        else:
+            cands = [np.ones(cfg.E, bool)]
+        worst = sel[picked].min()
+        for elig in cands:
+            others = np.where(elig, sel, -np.inf)
+            others[picked] = -np.inf
+            if others.max() <= worst + expert_tol_sign * tol:
+                return True
+        return False
+    return valid
+
+
+_valid_old_threshold_rule = _valid_selection_variant(old_threshold=True)
+_valid_old_threshold_rule.__name__ = "_valid_old_threshold_rule"
+_valid_group_tol_reversed = _valid_selection_variant(group_tol_sign=-1.0)
+_valid_group_tol_reversed.__name__ = "_valid_group_tol_reversed"
+_valid_groups_not_required = _valid_selection_variant(require_groups=False)
+_valid_groups_not_required.__name__ = "_valid_groups_not_required"
+_valid_expert_tol_reversed = _valid_selection_variant(expert_tol_sign=-1.0)
+_valid_expert_tol_reversed.__name__ = "_valid_expert_tol_reversed"
+
+
+def _near_ties_variant(group_offset=0, absolute=False, group_gap=True):
+    def near(sel64, elig, cfg):
+        T, E = sel64.shape
+        scale = 1.0 if absolute else np.abs(sel64).max(axis=1)
+        out = np.zeros(T, bool)
+        if cfg.k < E:
+            e64 = np.where(elig, sel64, -np.inf)
+            desc = -np.sort(-e64, axis=1)
+            gap = np.where(elig.sum(axis=1) > cfg.k, desc[:, cfg.k - 1] - desc[:, cfg.k], np.inf)
+            out |= gap < orc.NEAR_TIE_REL * scale
+        if group_gap and cfg.topk_method == "group_limited_greedy" and cfg.topk_group < cfg.n_group:
+            g64 = -np.sort(-orc._group_scores64(sel64, cfg), axis=1)
+            j = min(cfg.topk_group - 1 + group_offset, cfg.n_group - 2)
+            out |= g64[:, j] - g64[:, j + 1] < orc.NEAR_TIE_REL * scale
+        return out
+    return near
+
+
+_near_group_gap_off_by_one = _near_ties_variant(group_offset=1)
+_near_group_gap_off_by_one.__name__ = "_near_group_gap_off_by_one"
+_near_absolute_tolerance = _near_ties_variant(absolute=True)
+_near_absolute_tolerance.__name__ = "_near_absolute_tolerance"
+_near_no_group_gap = _near_ties_variant(group_gap=False)
+_near_no_group_gap.__name__ = "_near_no_group_gap"
+
+
+def _rel_err_mean(got, ref):
+    ref, got = np.asarray(ref, np.float64), np.asarray(got, np.float64)
+    return float(np.mean(np.abs(got - ref))) / float(np.sqrt(np.mean(ref * ref)))
+
+
+def _rel_err_over_max_ref(got, ref):
+    ref, got = np.asarray(ref, np.float64), np.asarray(got, np.float64)
+    return float(np.max(np.abs(got - ref))) / float(np.max(np.abs(ref)))
+
+
+def _rel_err_over_mean_abs(got, ref):
+    ref, got = np.asarray(ref, np.float64), np.asarray(got, np.float64)
+    return float(np.max(np.abs(got - ref))) / float(np.mean(np.abs(ref)))
+
+
+def _rel_err_no_sqrt(got, ref):
+    ref, got = np.asarray(ref, np.float64), np.asarray(got, np.float64)
+    return float(np.max(np.abs(got - ref))) / float(np.mean(ref * ref))
+
+
 _ORIG_SWIGLU_BACKWARD = orc.swiglu_backward
 _ORIG_GATE_BACKWARD = orc.gate_backward
 
@@ -195,6 +300,17 @@ MUTANTS = [
     ("gate_backward", _gate_backward_softmax_diag, pins.pin_backward_finite_differences),
     ("swiglu_backward", _swiglu_backward_dw2_from_gate, pins.pin_backward_homogeneity),
     ("gate_backward", _gate_backward_no_renorm_term, pins.pin_backward_homogeneity),
+    ("is_valid_selection", _valid_old_threshold_rule, pins.pin_valid_selection_brute_force),
+    ("is_valid_selection", _valid_group_tol_reversed, pins.pin_valid_selection_brute_force),
+    ("is_valid_selection", _valid_groups_not_required, pins.pin_valid_selection_brute_force),
+    ("is_valid_selection", _valid_expert_tol_reversed, pins.pin_valid_selection_brute_force),
+    ("near_ties", _near_group_gap_off_by_one, pins.pin_group_near_tie_gap),
+    ("near_ties", _near_absolute_tolerance, pins.pin_group_near_tie_gap),
+    ("near_ties", _near_no_group_gap, pins.pin_group_near_tie_gap),
+    ("relative_error", _rel_err_mean, pins.pin_relative_error),
+    ("relative_error", _rel_err_over_max_ref, pins.pin_relative_error),
+    ("relative_error", _rel_err_over_mean_abs, pins.pin_relative_error),
+    ("relative_error", _rel_err_no_sqrt, pins.pin_relative_error),
 ]
 
 

@@ -15,10 +15,18 @@
  * Conventions shared by every call:
  *  - All tensor pointers are DEVICE pointers, owned by the caller, 16-byte
  *    aligned, dense row-major.  Weights use the nn.Linear layout (out x in).
- *    The library never allocates or frees device memory.
+ *    The forward calls never allocate or free device memory (moe_backward's
+ *    exception is stated at its declaration).
  *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
  *    stream).  Arguments are validated on the host first; on any error the call
  *    returns a non-zero moe_status and launches nothing.
+ *  - Every call's kernels start only after all earlier work in `stream` has
+ *    completed (the call begins with an ordinary stream operation, clearing
+ *    its status word, or with a kernel that waits for its predecessor before
+ *    letting its successors start).  Inside one call, a kernel may begin while
+ *    its predecessor finishes, but only where it touches nothing that
+ *    predecessor writes.  So a layer's output may be the next call's input on
+ *    the same stream.
  *  - `ws` is the caller's workspace of at least moe_workspace_size() bytes.
  *    Each compute call clears and then uses a device status word at its start;
  *    moe_get_device_status() reads it (bounds violations, device-side wait
@@ -178,6 +186,9 @@ MOE_API moe_status moe_forward(const moe_config* cfg, const void* x, const void*
  *   word (as read by moe_get_device_status for the workspace calls).
  *   The first call on each device looks up the array's device address with
  *   cudaGetSymbolAddress; make that first call before any stream capture.
+ *   The address is kept for the life of the process: after a context reset
+ *   (cudaDeviceReset) do not call this entry point on that device again.
+ *   With T = 0 it writes empty counts/offsets and a zero device_status.
  *   All calls share the one array, so calls whose kernels overlap on the GPU
  *   (other streams, other host threads) race: serialise them.  No cudaMalloc,
  *   cudaFree or allocating library routine is called. */
@@ -241,6 +252,22 @@ MOE_API moe_status moe_get_device_status(const void* ws, void* stream, int32_t* 
 
 /* Human-readable name of a status code (static storage). */
 MOE_API const char* moe_status_string(moe_status s);
+
+/* Fault injection for tests of the device-side time-out path (the pages have
+ * no counterpart: it exists to show that a stalled pipeline reports an error
+ * instead of hanging, and that the next call runs normally).
+ *   what = MOE_DEBUG_WAIT_LIMIT_NS: the limit of every bounded wait in the
+ *     expert GEMM kernel for later calls, in ns (0 restores the default of
+ *     2 s; otherwise 1e5 .. 1e10).
+ *   what = MOE_DEBUG_STALL_GEMM2 (value 0 or 1): when 1, every GEMM2 tile of
+ *     a one-launch expert GEMM (T*k <= 8192) waits for one more GEMM1
+ *     completion than its group produces, so that wait runs out: the call
+ *     sets DEV_TIMEOUT in its status word (moe_get_device_status returns
+ *     MOE_ERR_DEVICE_TIMEOUT), its kernels end, and its outputs are undefined.
+ * Process-wide settings read when a call launches its kernels; not
+ * thread-safe.  Returns MOE_ERR_INVALID_ARG for an unknown knob or value. */
+typedef enum moe_debug_knob { MOE_DEBUG_WAIT_LIMIT_NS = 0, MOE_DEBUG_STALL_GEMM2 = 1 } moe_debug_knob;
+MOE_API moe_status moe_debug_inject(int32_t what, int64_t value);
 
 /* Number of kernels this library has launched in the process so far. */
 MOE_API uint64_t moe_launch_count(void);

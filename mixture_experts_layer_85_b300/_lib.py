@@ -30,8 +30,10 @@ MOE_GROUP_MAX, MOE_GROUP_SUM_TOP = 0, 1
 EXPORTED = ["moe_workspace_size", "moe_packed_size", "moe_prepack_experts", "moe_gate_topk", "moe_permute",
             "moe_grouped_swiglu", "moe_combine", "moe_forward", "moe_get_device_status", "moe_status_string",
             "moe_launch_count", "moe_forward_kernel_count", "moe_profile_arm", "moe_forward_stage_name",
-            "moe_permute_noalloc", "moe_balance_update", "moe_backward_workspace_size", "moe_backward"]
+            "moe_permute_noalloc", "moe_balance_update", "moe_backward_workspace_size", "moe_backward",
+            "moe_debug_inject"]
 MOE_FORWARD_STAGES = 4
+MOE_DEBUG_WAIT_LIMIT_NS, MOE_DEBUG_STALL_GEMM2 = 0, 1
 
 
 class moe_config(ctypes.Structure):
@@ -66,6 +68,7 @@ _sigs = {
     "moe_balance_update": [_CFG, _P, _P, ctypes.c_float, _P, _P, _P],
     "moe_backward_workspace_size": [_CFG, ctypes.POINTER(_SZ)],
     "moe_backward": [_CFG] + [_P] * 19 + [_SZ, _P],
+    "moe_debug_inject": [ctypes.c_int32, ctypes.c_int64],
 }
 for _name, _args in _sigs.items():
     _f = getattr(_lib, _name)
@@ -241,6 +244,11 @@ def moe_profile_arm(events) -> None:
 def moe_forward_stage_name(i: int) -> Optional[str]:
     n = _lib.moe_forward_stage_name(int(i))
     return None if n is None else n.decode()
+
+
+def moe_debug_inject(what: int, value: int):
+    """Test-only fault injection of the expert kernel's bounded waits."""
+    _check(_lib.moe_debug_inject(int(what), int(value)), "moe_debug_inject")
 
 
 def raw_call(name: str, *args) -> int:

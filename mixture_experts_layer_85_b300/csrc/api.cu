@@ -569,6 +569,24 @@ const char* moe_status_string(moe_status s) {
 
 uint64_t moe_launch_count(void) { return g_launches.load(); }
 
+moe_status moe_debug_inject(int32_t what, int64_t value) {
+  unsigned long long wait_ns = 0;
+  int extra = 0;
+  get_expert_fault(&wait_ns, &extra);
+  switch (what) {
+    case MOE_DEBUG_WAIT_LIMIT_NS:
+      if (value < 0 || value > 10000000000LL) return MOE_ERR_INVALID_ARG;
+      if (value != 0 && value < 100000) return MOE_ERR_INVALID_ARG;   // at least 0.1 ms
+      set_expert_fault((unsigned long long)value, extra);
+      return MOE_OK;
+    case MOE_DEBUG_STALL_GEMM2:
+      if (value != 0 && value != 1) return MOE_ERR_INVALID_ARG;
+      set_expert_fault(wait_ns, int(value));
+      return MOE_OK;
+  }
+  return MOE_ERR_INVALID_ARG;
+}
+
 moe_status moe_profile_arm(void* const* events, int32_t n_events) {
   if (events != nullptr && n_events < 0) return MOE_ERR_INVALID_ARG;
   g_prof_events = n_events > 0 ? events : nullptr;

@@ -33,8 +33,10 @@ __device__ __forceinline__ double block_sum_f64(double v, double* red) {
 __global__ void __launch_bounds__(BAL_THREADS) balance_update_kernel(const int32_t* __restrict__ counts, int E,
                                                                      float* __restrict__ bias, float gamma,
                                                                      float* __restrict__ stats, int* status) {
-  pdl_launch_dependents();
+  // the only kernel of its call: dependents start after it has begun, and it
+  // reads the counts only once the kernels before it have completed
   pdl_wait();
+  pdl_launch_dependents();
   __shared__ double red[BAL_THREADS / 32];
   __shared__ int imax[BAL_THREADS / 32], imin[BAL_THREADS / 32];
   const int e = threadIdx.x, lane = e & 31, warp = e >> 5;

@@ -19,8 +19,10 @@ namespace {
 // fp32 W_g -> [hi | mid | lo] bf16 along K, so that x . w = x . hi + x . mid + x . lo
 // exactly in fp32 products (bf16 x times bf16 parts) for the tensor-core gate.
 __global__ void gate_split_kernel(const float* __restrict__ wg, int E, int d, __nv_bfloat16* __restrict__ out) {
-  pdl_launch_dependents();
+  // first kernel of a call: its dependents may start only once everything
+  // earlier in the stream has completed
   pdl_wait();
+  pdl_launch_dependents();
   const long long n = (long long)E * d;
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
     const long long e = i / d, c = i % d;
@@ -286,13 +288,13 @@ template <typename TX, typename TW, int TB>
 static cudaError_t gate_simt_typed(const moe_config& c, const void* x, const void* wg, float* logits,
                                    cudaStream_t s) {
   const size_t smem = size_t(TB) * c.d * sizeof(float);
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(gate_logits_simt_kernel<TX, TW, TB>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  static PerDevice<int> attr;
+  int unused = 0;
+  cudaError_t e = attr.get(&unused, [](int*) {
+    return cudaFuncSetAttribute(gate_logits_simt_kernel<TX, TW, TB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                200 * 1024);
+  });
+  if (e != cudaSuccess) return e;
   const int tblocks = (c.T + TB - 1) / TB;
   // split the experts across blocks until the grid covers the GPU
   int epb = c.E;

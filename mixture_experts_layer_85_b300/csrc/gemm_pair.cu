@@ -28,10 +28,16 @@
 // a GEMM1 tile of that group, so GEMM2 work starts expert by expert while
 // other clusters still run GEMM1 tiles; every cluster finishes its own GEMM1
 // tiles before its first GEMM2 tile, so the waits always resolve.  The
-// shared expert's GEMM1 tiles need only x and may start before the preceding
-// dispatch kernel completes (programmatic dependent launch); routed tiles
-// wait for the routed tile table, which a scheduler warp builds from the
-// dispatch offsets once that kernel has completed.
+// shared expert's GEMM1 tiles read only x and write only the shared hidden
+// rows, so they may start before the preceding kernels of the same layer call
+// (router, dispatch) complete (programmatic dependent launch): those kernels
+// touch neither.  Early starts never reach further back: every call of the
+// library begins with an ordinary stream operation (clearing its status word),
+// which starts only after all earlier work in the stream has completed, so a
+// previous call that still reads the hidden rows, or a previous layer that
+// writes x, has finished.  Routed tiles wait for the routed tile table, which
+// a scheduler warp builds from the dispatch offsets once the dispatch has
+// completed.
 //
 // Each TMA copy moves two k-blocks (3-D tensor maps: 64 columns x rows x 2
 // k-blocks): a copy instruction has a fixed cost in the copy engine, so fewer,
@@ -53,6 +59,8 @@
 // stop too.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+
+#include <atomic>
 
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
@@ -145,6 +153,11 @@ struct PairParams {
   int x_kb_bytes;           // bytes of one k-block of the largest token box of the launch
   int a_tmem;               // FP8: the converted A operand lives in tensor memory (A_TMEM_STAGES buffers)
   uint32_t acc_stride;      // tensor-memory columns between the two accumulators
+  // Limit of every bounded wait (ns of %globaltimer), and completions a GEMM2
+  // tile waits for beyond its group's GEMM1 tiles (0; a positive value makes
+  // those waits run out: host-side fault injection for tests).
+  unsigned long long wait_ns;
+  int need_extra;
 };
 
 struct PairCtrl {
@@ -157,6 +170,7 @@ struct PairCtrl {
   uint64_t f8_empty[MAX_F8]; // FP8: the MMAs that read a slot completed (this CTA)
   uint32_t tmem_base;
   int abort;
+  unsigned long long wait_ns;   // copy of PairParams::wait_ns
   int seg[5];                // tile numbers where the four segments start, and the total
   int routed_ready;          // the routed tile tables (and seg[2..4]) are built
   int tile_start[2][MAX_GROUPS + 1];   // per phase: exclusive prefix of routed tiles
@@ -196,7 +210,7 @@ __device__ __forceinline__ int pair_group_tiles(const PairParams& p, int cls, in
 // GEMM1 counter value at which a group's hidden rows are complete: every
 // epilogue warp of both CTAs bumps it once per GEMM1 tile of the group.
 __device__ __forceinline__ int gemm1_need(const PairParams& p, int cls1, int rows) {
-  return 2 * EPI_WARPS * pair_group_tiles(p, cls1, rows);
+  return 2 * EPI_WARPS * pair_group_tiles(p, cls1, rows) + p.need_extra;
 }
 
 // Warp-cooperative: row ranges of the routed groups (from the dispatch
@@ -299,7 +313,7 @@ __device__ __forceinline__ bool wait_routed_ready(PairCtrl* c, int* status) {
     const unsigned long long t0 = globaltimer_ns();
     while (!*ready) {
       if (*reinterpret_cast<volatile int*>(&c->abort)) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      if (globaltimer_ns() - t0 > c->wait_ns) {
         c->abort = 1;
         flag_status(status, DEV_TIMEOUT);
         return false;
@@ -320,8 +334,11 @@ __device__ __forceinline__ bool pair_tile_exists(PairCtrl* c, int tile, int* sta
 }
 
 // Bounded wait; on giving up it flags the status word and stops both CTAs.
+// It also gives up as soon as this CTA has been told to stop, unless
+// honor_abort is false (the final waits for this CTA's own copies and MMAs,
+// which complete whatever else happened).
 __device__ __forceinline__ bool pair_wait(uint64_t* bar, uint32_t parity, PairCtrl* c, uint32_t peer_abort,
-                                          int* status, bool cluster_scope = false) {
+                                          int* status, bool cluster_scope = false, bool honor_abort = true) {
   if (cluster_scope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
   volatile int* ab = &c->abort;
   const unsigned long long t0 = globaltimer_ns();
@@ -329,13 +346,52 @@ __device__ __forceinline__ bool pair_wait(uint64_t* bar, uint32_t parity, PairCt
   while (true) {
     if (cluster_scope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
     if ((++n & 63u) == 0u) {
-      if (*ab) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      if (honor_abort && *ab) return false;
+      if (globaltimer_ns() - t0 > c->wait_ns) {
         *ab = 1;
         st_remote_u32(peer_abort, 1u);
         flag_status(status, DEV_TIMEOUT);
         return false;
       }
+    }
+  }
+}
+
+// A GEMM2 tile of group t.g needs the group's hidden rows: wait (acquire, GPU
+// scope) until every epilogue warp of every GEMM1 tile of the group has
+// published its part.  Returns false when the wait gave up or the CTA stopped.
+__device__ bool wait_gemm1_done(PairCtrl* c, const PairParams& p, const PairTile& t, uint32_t peer_abort) {
+  const int need = gemm1_need(p, t.cls == C2R ? C1R : C1S, t.rows);
+  const unsigned long long t0 = globaltimer_ns();
+  while (ld_acquire_gpu(p.done + t.g) < need) {
+    if (*reinterpret_cast<volatile int*>(&c->abort)) return false;
+    if (globaltimer_ns() - t0 > c->wait_ns) {
+      c->abort = 1;
+      st_remote_u32(peer_abort, 1u);
+      flag_status(p.status, DEV_TIMEOUT);
+      return false;
+    }
+    __nanosleep(128);
+  }
+  fence_proxy_async_global();   // the copy engine reads what the acquire made visible
+  return true;
+}
+
+// Before a producer leaves, every copy it issued into its ring must have
+// landed.  The last use of each ring position (bit s of `used`, parity bit s
+// of `par`) completes once the MMAs consumed it, which on the normal path has
+// happened or soon will.  After a stop some positions are never consumed;
+// the wait then ends after min(limit, kDrainAfterStopNs), far longer than a
+// copy takes to land, so no copy still lands once the CTA has left.
+constexpr unsigned long long kDrainAfterStopNs = 1000000ull;
+__device__ void pair_drain(uint64_t* bars, int n, uint32_t used, uint32_t par, PairCtrl* c) {
+  const unsigned long long t0 = globaltimer_ns();
+  for (int s = 0; s < n; ++s) {
+    if (!(used & (1u << s))) continue;
+    while (!mbar_try_wait(&bars[s], (par >> s) & 1u)) {
+      const unsigned long long dt = globaltimer_ns() - t0;
+      const bool stopped = *reinterpret_cast<volatile int*>(&c->abort) != 0;
+      if (dt > c->wait_ns || (stopped && dt > kDrainAfterStopNs)) return;
     }
   }
 }
@@ -356,24 +412,10 @@ __device__ void pair_producer(PairCtrl* c, const PairParams& p, uint8_t* stages,
     }
     if ((t.cls == C2R || t.cls == C2S) && p.phases == 3 && t.g != ready_group) {
       // the group's GEMM1 tiles (any cluster) have stored its hidden rows
-      const int need = gemm1_need(p, t.cls == C2R ? C1R : C1S, t.rows);
-      const unsigned long long t0 = globaltimer_ns();
-      while (ld_acquire_gpu(p.done + t.g) < need) {
-        if (*reinterpret_cast<volatile int*>(&c->abort)) {
-          ok = false;
-          break;
-        }
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
-          c->abort = 1;
-          st_remote_u32(peer_abort, 1u);
-          flag_status(p.status, DEV_TIMEOUT);
-          ok = false;
-          break;
-        }
-        __nanosleep(128);
+      if (!wait_gemm1_done(c, p, t, peer_abort)) {
+        ok = false;
+        break;
       }
-      if (!ok) break;
-      fence_proxy_async_global();   // the copy engine reads what the acquire made visible
       ready_group = t.g;
     }
     const bool routed = t.cls == C1R || t.cls == C2R;
@@ -401,10 +443,7 @@ __device__ void pair_producer(PairCtrl* c, const PairParams& p, uint8_t* stages,
       }
     }
   }
-  // The last copy into each stage was consumed (so it landed) before this CTA
-  // may leave; on the normal path these waits return at once.
-  for (int s = 0; s < p.stages; ++s)
-    if (issued & (1u << s)) pair_wait(&c->empty[s], (issued_par >> s) & 1u, c, peer_abort, p.status);
+  pair_drain(c->empty, p.stages, issued, issued_par, c);
 }
 
 // Position in a ring of n barriers/buffers and the parity of its current use,
@@ -448,24 +487,10 @@ __device__ void pair_producer_fp8(PairCtrl* c, const PairParams& p, uint8_t* sta
     }
     if ((t.cls == C2R || t.cls == C2S) && p.phases == 3 && t.g != ready_group) {
       // the group's GEMM1 tiles (any cluster) have stored its hidden rows
-      const int need = gemm1_need(p, t.cls == C2R ? C1R : C1S, t.rows);
-      const unsigned long long t0 = globaltimer_ns();
-      while (ld_acquire_gpu(p.done + t.g) < need) {
-        if (*reinterpret_cast<volatile int*>(&c->abort)) {
-          ok = false;
-          break;
-        }
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
-          c->abort = 1;
-          st_remote_u32(peer_abort, 1u);
-          flag_status(p.status, DEV_TIMEOUT);
-          ok = false;
-          break;
-        }
-        __nanosleep(128);
+      if (!wait_gemm1_done(c, p, t, peer_abort)) {
+        ok = false;
+        break;
       }
-      if (!ok) break;
-      fence_proxy_async_global();   // the copy engine reads what the acquire made visible
       ready_group = t.g;
     }
     const int nks = p.K[t.cls] / 128;   // stages of this tile (K is a multiple of 128)
@@ -497,10 +522,7 @@ __device__ void pair_producer_fp8(PairCtrl* c, const PairParams& p, uint8_t* sta
       slot.next(p.nf);
     }
   }
-  // The last copies into each slot were consumed (so they landed) before this
-  // CTA may leave; on the normal path these waits return at once.
-  for (int s = 0; s < p.nf; ++s)
-    if (used & (1u << s)) pair_wait(&c->f8_empty[s], (used_par >> s) & 1u, c, peer_abort, p.status);
+  pair_drain(c->f8_empty, p.nf, used, used_par, c);
 }
 
 // 16 e4m3 values (k order) times a power-of-two scale -> 8 words of bf16 pairs
@@ -671,9 +693,10 @@ __device__ void pair_mma(PairCtrl* c, const PairParams& p, uint8_t* stages, uint
     }
     if (ok) mma_commit_pair(&c->tfull[acc], 0x3);
   }
-  // Every MMA issued here completes before tensor memory is released.
+  // Every MMA issued here completes before tensor memory is released (this
+  // wait holds after a stop too: issued MMAs always complete).
   mma_commit_pair(&c->drain, 0x1);
-  pair_wait(&c->drain, 0u, c, peer_abort, p.status);
+  pair_wait(&c->drain, 0u, c, peer_abort, p.status, false, false);
 }
 
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + __expf(-z)); }
@@ -787,6 +810,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FP8 ? THREADS_FP8 : 
     }
     mbar_init(&c->drain, 1);
     c->abort = 0;
+    c->wait_ns = p.wait_ns;
     c->routed_ready = 0;
     c->seg[0] = 0;
     c->seg[1] = (p.phases & 1) && p.shared_rows > 0 ? pair_group_tiles(p, C1S, p.shared_rows) : 0;
@@ -844,11 +868,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FP8 ? THREADS_FP8 : 
 template <bool FP8>
 cudaError_t launch_pair(const PairParams& p, long long max_tiles, cudaStream_t stream) {
   constexpr int kThreads = FP8 ? THREADS_FP8 : THREADS;
-  static int max_clusters = -1;
-  if (max_clusters < 0) {
-    cudaError_t e = cudaFuncSetAttribute(pair_gemm_kernel<FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         int(kPairSmem));
-    if (e != cudaSuccess) return e;
+  static PerDevice<int> clusters;
+  int max_clusters = 0;
+  cudaError_t e = clusters.get(&max_clusters, [](int* n) {
+    cudaError_t err = cudaFuncSetAttribute(pair_gemm_kernel<FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           int(kPairSmem));
+    if (err != cudaSuccess) return err;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * (num_sms() / 2), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
@@ -860,20 +885,34 @@ cudaError_t launch_pair(const PairParams& p, long long max_tiles, cudaStream_t s
     attr.val.clusterDim.z = 1;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, pair_gemm_kernel<FP8>, &cfg) != cudaSuccess || n <= 0) {
+    *n = 0;
+    if (cudaOccupancyMaxActiveClusters(n, pair_gemm_kernel<FP8>, &cfg) != cudaSuccess || *n <= 0) {
       cudaGetLastError();
-      n = num_sms() / 2;
+      *n = num_sms() / 2;
     }
-    max_clusters = n;
-  }
+    return cudaSuccess;
+  });
+  if (e != cudaSuccess) return e;
   // every cluster must be resident at once: GEMM2 tiles wait for GEMM1 tiles
   // of other clusters
   const long long pairs = max_tiles < max_clusters ? max_tiles : max_clusters;
   return launch_pdl(pair_gemm_kernel<FP8>, dim3(int(2 * pairs)), dim3(kThreads), kPairSmem, stream, p);
 }
 
+std::atomic<unsigned long long> g_wait_ns{0};   // 0: kWaitLimitNs
+std::atomic<int> g_need_extra{0};
+
 }  // namespace
+
+void set_expert_fault(unsigned long long wait_ns, int need_extra) {
+  g_wait_ns.store(wait_ns);
+  g_need_extra.store(need_extra);
+}
+
+void get_expert_fault(unsigned long long* wait_ns, int* need_extra) {
+  *wait_ns = g_wait_ns.load();
+  *need_extra = g_need_extra.load();
+}
 
 cudaError_t launch_pair_experts(const PairClass cls[4], const int32_t* offsets, int num_routed, int shared_rows,
                                 int max_group_rows, int phases, int* done, int* status, long long max_tiles,
@@ -911,6 +950,9 @@ cudaError_t launch_pair_experts(const PairClass cls[4], const int32_t* offsets, 
   p.done = done;
   p.phases = phases;
   p.status = status;
+  const unsigned long long wns = g_wait_ns.load();
+  p.wait_ns = wns > 0 ? wns : kWaitLimitNs;
+  p.need_extra = phases == 3 ? g_need_extra.load() : 0;
   // A group never holds more tokens than the batch, so with at most 64 tokens
   // every tile takes the 32-row token box: use the deeper ring of small stages.
   const bool small = max_group_rows <= 2 * XSMALL;

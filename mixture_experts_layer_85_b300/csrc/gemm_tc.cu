@@ -382,12 +382,14 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const __grid_c
     tmem_relinquish();
   }
   if (warp == 2) build_schedule<EPI>(c, p, lane);
-  if (threadIdx.x == 0) pdl_launch_dependents();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  // the inputs (tokens) come from earlier work in the stream
+  // the inputs (tokens) come from earlier work in the stream.  The gate is the
+  // first kernel of a call (or follows the W_g split), so its dependents are
+  // released only after that earlier work has completed.
   pdl_wait();
+  if (threadIdx.x == 0) pdl_launch_dependents();
 
   const uint32_t tmem = c->tmem_base;
   const int total = c->tile_start[c->ngroups];
@@ -504,28 +506,30 @@ namespace {
 
 template <int EPI>
 cudaError_t launch_epi(const Params& p, int grid, cudaStream_t stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         int(kSmemBytes));
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static PerDevice<int> attr;
+  int unused = 0;
+  cudaError_t e = attr.get(&unused, [](int*) {
+    return cudaFuncSetAttribute(grouped_gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                int(kSmemBytes));
+  });
+  if (e != cudaSuccess) return e;
   return launch_pdl(grouped_gemm_kernel<EPI>, dim3(grid), dim3(THREADS), kSmemBytes, stream, p);
 }
 
 }  // namespace
 
 int num_sms() {
-  int dev = 0, n = 0;
-  cudaGetDevice(&dev);
-  static int cached_dev = -1, cached_n = 0;
-  if (dev != cached_dev) {
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    cached_dev = dev;
-    cached_n = n > 0 ? n : 1;
-  }
-  return cached_n;
+  static PerDevice<int> sms;
+  int n = 1;
+  if (sms.get(&n, [](int* v) {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(v, cudaDevAttrMultiProcessorCount, dev);
+        if (e == cudaSuccess && *v <= 0) *v = 1;
+        return e;
+      }) != cudaSuccess)
+    return 1;
+  return n;
 }
 
 cudaError_t launch_grouped_gemm(int epi, const GemmClass& c0, const GemmClass* c1, const int32_t* offsets,

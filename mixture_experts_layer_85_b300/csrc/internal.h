@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "../../include/moe.h"
 #include "common.cuh"
 
@@ -29,6 +31,39 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
+
+// One-time set-up per device (a kernel's shared-memory attribute, an
+// occupancy figure, a symbol address): get() runs `init` the first time it
+// is called with a given current device and returns the stored value on
+// later calls on that device.  Thread-safe.  A context reset
+// (cudaDeviceReset) does not clear it.
+constexpr int kMaxDevices = 64;
+template <typename T>
+class PerDevice {
+ public:
+  template <typename F>
+  cudaError_t get(T* out, F&& init) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu_);
+    if (!ready_[dev]) {
+      T v{};
+      e = init(&v);
+      if (e != cudaSuccess) return e;
+      value_[dev] = v;
+      ready_[dev] = true;
+    }
+    *out = value_[dev];
+    return cudaSuccess;
+  }
+
+ private:
+  std::mutex mu_;
+  bool ready_[kMaxDevices] = {};
+  T value_[kMaxDevices] = {};
+};
 
 // ---------------------------------------------------------------- grouped GEMM
 // One operand class of the grouped GEMM: A [a_rows, K'] and B [b_rows, K] bf16,
@@ -108,6 +143,13 @@ struct PairClass {
 cudaError_t launch_pair_experts(const PairClass cls[4], const int32_t* offsets, int num_routed, int shared_rows,
                                 int max_group_rows, int phases, int* done, int* status, long long max_tiles,
                                 cudaStream_t stream, int* launches, bool fp8 = false);
+
+// Fault injection for tests of the device-side time-out path
+// (moe_debug_inject): the expert kernel's wait limit for later launches
+// (0 = kWaitLimitNs) and the extra GEMM1 completions each GEMM2 tile of a
+// one-launch expert kernel waits for (> 0 makes those waits run out).
+void set_expert_fault(unsigned long long wait_ns, int need_extra);
+void get_expert_fault(unsigned long long* wait_ns, int* need_extra);
 
 // ---------------------------------------------------------------------- router
 cudaError_t launch_gate_split(const float* wg, int E, int d, void* wsplit, cudaStream_t s, int* launches);

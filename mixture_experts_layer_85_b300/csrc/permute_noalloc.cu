@@ -7,8 +7,6 @@
 // whole device and can fail when memory is fragmented).  This entry point runs
 // the same permutation kernels with their scratch in a fixed-size array that
 // lives in the library's own device image, so nothing is allocated per call.
-#include <mutex>
-
 #include "internal.h"
 
 namespace moe {
@@ -22,26 +20,19 @@ constexpr int kTableInts = 32768;
 constexpr int kHeaderInts = 64;
 static __device__ __align__(256) int32_t g_permute_scratch[kHeaderInts + 2 * kTableInts];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-int32_t* g_scratch[kMaxDevices] = {};
-
 // Device address of g_permute_scratch on the current device, looked up once
-// per device.  In host code the array's name is only a host-side stand-in.
+// per device (in host code the array's name is only a host-side stand-in).
+// After a context reset (cudaDeviceReset) the module is loaded again at
+// another address, which this cache does not see: a process that resets a
+// device must not call moe_permute_noalloc on it afterwards.
 cudaError_t scratch_on_current_device(int32_t** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (g_scratch[dev] == nullptr) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_permute_scratch);
-    if (e != cudaSuccess) return e;
-    g_scratch[dev] = static_cast<int32_t*>(p);
-  }
-  *out = g_scratch[dev];
-  return cudaSuccess;
+  static PerDevice<int32_t*> addr;
+  return addr.get(out, [](int32_t** p) {
+    void* a = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&a, g_permute_scratch);
+    *p = static_cast<int32_t*>(a);
+    return e;
+  });
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -66,7 +57,10 @@ extern "C" MOE_API moe_status moe_permute_noalloc(const moe_config* cfg, const v
   if ((long long)permute_chunks(c.T) * c.E > kTableInts) return MOE_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (c.T == 0) {
+    // no tokens: every expert is empty, and nothing can go wrong on the device
     if (cudaMemsetAsync(offsets, 0, size_t(c.E + 1) * 4, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (device_status != nullptr && cudaMemsetAsync(device_status, 0, sizeof(int32_t), s) != cudaSuccess)
+      return MOE_ERR_CUDA;
     return cudaMemsetAsync(counts, 0, size_t(c.E) * 4, s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
   }
   int32_t* base = nullptr;

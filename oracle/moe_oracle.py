@@ -197,18 +197,24 @@ def route(logits: np.ndarray, bias: Optional[np.ndarray], cfg: OracleConfig) -> 
     order = np.argsort(-key, axis=1, kind="stable")
     idx = order[:, : cfg.k].astype(np.int64)
 
-    # gate values from the unbiased affinity (V3 page, section 1.2)
-    rows = np.arange(T)[:, None]
-    g = s[rows, idx]
-    if cfg.norm_topk:
-        g = g / g.sum(axis=1, keepdims=True)
-    g = g * float(cfg.routed_scaling_factor)
+    g = gate_values(s, idx, cfg)
 
     # near ties, judged on exact float64 selection scores
     sel64 = s + (0.0 if bias is None else np.asarray(bias, np.float64)[None, :])
     near = near_ties(sel64, elig, cfg)
     counts = np.bincount(idx.ravel(), minlength=E).astype(np.int64)
     return Routing(idx=idx, gates=g, scores=s, sel32=sel32, near_tie=near, counts=counts)
+
+
+def gate_values(s: np.ndarray, idx: np.ndarray, cfg: OracleConfig) -> np.ndarray:
+    """Gate values [T,k] of a choice idx: the unbiased affinities of the chosen
+    experts (V3 page, section 1.2), divided by their sum when norm_topk, times
+    routed_scaling_factor."""
+    rows = np.arange(idx.shape[0])[:, None]
+    g = np.asarray(s, np.float64)[rows, idx]
+    if cfg.norm_topk:
+        g = g / g.sum(axis=1, keepdims=True)
+    return g * float(cfg.routed_scaling_factor)
 
 
 def near_ties(sel64: np.ndarray, elig: np.ndarray, cfg: OracleConfig) -> np.ndarray:
@@ -334,11 +340,7 @@ def moe_forward(x, wg, bias, expert: ExpertFn, shared, cfg: OracleConfig,
     idx, gates = r.idx, r.gates
     if idx_override is not None:
         idx = np.asarray(idx_override, np.int64)
-        rows = np.arange(idx.shape[0])[:, None]
-        gates = r.scores[rows, idx]
-        if cfg.norm_topk:
-            gates = gates / gates.sum(axis=1, keepdims=True)
-        gates = gates * float(cfg.routed_scaling_factor)
+        gates = gate_values(r.scores, idx, cfg)
     out = experts_forward(x, idx, gates, expert, shared, cfg.E)
     return out, Routing(idx=idx, gates=gates, scores=r.scores, sel32=r.sel32,
                         near_tie=r.near_tie, counts=np.bincount(idx.ravel(), minlength=cfg.E))

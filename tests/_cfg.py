@@ -32,3 +32,19 @@ def expert_accessor(w1, w3, w2):
             cache[e] = (f64(w1[e]), f64(w3[e]), f64(w2[e]))
         return cache[e]
     return get
+
+
+def output_error(got, want, out_dtype: str) -> float:
+    """max |got - want| / RMS(want), the layer's acceptance measure.  A bf16-
+    stored output also carries its own rounding, at most half a bf16 ulp
+    (2^-8 of the value, 8 significant bits), which the fp64 oracle does not
+    have; that allowance is taken off each element first, so the budget
+    applies to the computation alone."""
+    from oracle import moe_oracle as orc
+    got = np.asarray(got, np.float64)
+    want = np.asarray(want, np.float64)
+    if out_dtype != "bf16":
+        return orc.relative_error(got, want)
+    allow = 2.0 ** -8 * np.maximum(np.abs(got), np.abs(want)) * 1.01
+    excess = np.maximum(np.abs(got - want) - allow, 0.0)
+    return orc.relative_error(want + excess, want)

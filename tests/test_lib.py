@@ -154,3 +154,13 @@ def test_fp8_packed_size_is_the_stage_image_layout(name):
     # about 1.0625 bytes per weight (plus one padding tile per matrix)
     weights = 3 * E * I * d + 3 * Is * d
     assert 1.0625 * weights <= total <= 1.0625 * weights + 4 * (d // 128 + I // 128) * stage * 2
+
+
+def test_debug_inject_validates_knobs():
+    assert _lib.raw_call("moe_debug_inject", 7, 0) == _lib.MOE_ERR_INVALID_ARG
+    assert _lib.raw_call("moe_debug_inject", _lib.MOE_DEBUG_WAIT_LIMIT_NS, -1) == _lib.MOE_ERR_INVALID_ARG
+    assert _lib.raw_call("moe_debug_inject", _lib.MOE_DEBUG_WAIT_LIMIT_NS, 10) == _lib.MOE_ERR_INVALID_ARG
+    assert _lib.raw_call("moe_debug_inject", _lib.MOE_DEBUG_STALL_GEMM2, 2) == _lib.MOE_ERR_INVALID_ARG
+    assert _lib.raw_call("moe_debug_inject", _lib.MOE_DEBUG_WAIT_LIMIT_NS, 1000000) == _lib.MOE_OK
+    assert _lib.raw_call("moe_debug_inject", _lib.MOE_DEBUG_WAIT_LIMIT_NS, 0) == _lib.MOE_OK
+    assert _lib.raw_call("moe_debug_inject", _lib.MOE_DEBUG_STALL_GEMM2, 0) == _lib.MOE_OK

@@ -4,9 +4,10 @@ The no-allocation entry point serves callers that cannot call cudaMalloc or
 hand the library a workspace (a host framework owns their device memory, a
 hard memory budget, or a loop that must not risk cudaMalloc blocking the
 device).  Its scratch is one fixed array in the library's device image that
-every call reuses, so two calls in a row must both match the workspace
-version exactly (integer outputs and copied rows: bit for bit).  This file is
-collected last on purpose."""
+every call reuses, so calls in a row must each match the workspace version
+exactly (integer outputs and copied rows: bit for bit).  Batches above 4096
+tokens take the multi-block dispatch, the only path that reads the array's
+per-chunk tables.  This file is collected last on purpose."""
 import ctypes
 
 import pytest
@@ -43,15 +44,36 @@ def _run_both(T, E, k, d, seed):
                              got["x_perm"], status)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
+    assert _lib.moe_get_device_status(ws)[0] == _lib.MOE_OK
     for name in ref:
         assert torch.equal(got[name], ref[name]), name
 
 
-def test_noalloc_matches_workspace_version_twice_in_a_row():
-    # the second call reuses the array the first one left behind; different
-    # sizes make stale table entries visible if anything read them
+def test_noalloc_matches_workspace_version_calls_in_a_row():
+    # Every call reuses the array the one before left behind.  Both shapes take
+    # the multi-block path; the second has more chunks and fewer experts, so a
+    # table entry the first call wrote and the second failed to overwrite would
+    # show up in its counts or rows.
     _run_both(T=4133, E=256, k=8, d=256, seed=1)
-    _run_both(T=777, E=160, k=6, d=128, seed=2)
+    _run_both(T=9000, E=160, k=6, d=128, seed=2)
+    _run_both(T=777, E=160, k=6, d=128, seed=3)     # one-block path after the multi-block ones
+
+
+def test_noalloc_at_its_exact_capacity():
+    # 128 chunks of 128 tokens times 256 experts fill both tables exactly
+    _run_both(T=16384, E=256, k=8, d=128, seed=4)
+
+
+def test_noalloc_empty_batch_clears_status():
+    wl, cfg, idx, x = _case(T=8, E=16, k=2, d=128, seed=5)
+    cfg.T = 0
+    out = _outputs(8, 16, 2, 128)
+    status = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    _lib.moe_permute_noalloc(cfg, x, idx, out["counts"], out["offsets"], out["row2tok"], out["tok2row"],
+                             out["x_perm"], status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert int(out["counts"].abs().sum()) == 0 and int(out["offsets"].abs().sum()) == 0
 
 
 def test_noalloc_rejects_sizes_beyond_its_array():

@@ -13,6 +13,7 @@ the layer on its own batch (tokens are independent, no collective on the
 data path); the value is all ranks' tokens over the slowest rank's time.
 """
 import argparse
+import dataclasses
 import datetime
 import json
 import math
@@ -44,7 +45,10 @@ def parse_args(argv=None):
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(inputs.WORKLOADS))
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-per-config", dest="per_config", action="store_false",
+                   help="skip the per_config lines (every other config, measured after the headline)")
     p.add_argument("--cpu-sample", type=int, default=0, help="tokens in the oracle's timed sample (0 = auto)")
+    p.add_argument("--oracle-one-core", default=None, help=argparse.SUPPRESS)
     p.add_argument("--pass", dest="pass_", choices=["forward", "backward"], default="forward",
                    help="backward: time moe_backward (gradients of the layer) instead of the forward")
     return p.parse_args(argv)
@@ -340,6 +344,198 @@ def time_end_to_end(layer, x, out_dtype, K, stream, world) -> float:
     return max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
 
 
+# ------------------------------------------------------------- measurement
+
+# Every config of the layer, beside the headline line: the fp32 reference
+# layer, the V2-shaped layers and the V3 decode batches (the V3 prefill layer
+# is the headline itself).
+PER_CONFIG = ["tiny_fp32_t128", "v2lite_t4096", "v2_t8192", "v3_decode_t1", "v3_decode_t8", "v3_decode_t64",
+              "v3_decode_t512"]
+NOMINAL_HBM_GBS = 8000.0
+
+
+class L2Flush:
+    """Writes a buffer of twice the device's L2 size, so the next step reads
+    its weights from HBM (the decode batches are smaller than L2 otherwise)."""
+
+    def __init__(self, dev):
+        l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 126 << 20)) or (126 << 20)
+        self.buf = torch.empty(2 * l2 // 4 + 256, dtype=torch.int32, device=dev)
+        self.n = 0
+
+    def __call__(self):
+        self.n += 1
+        self.buf.fill_(self.n)
+
+
+def needs_flush(wl) -> bool:
+    """Decode batches: the token batch fits in L2, and so might the weights
+    touched by the previous step."""
+    return wl.T <= 512
+
+
+def time_steps(layer, x, out, counts, K, flush=None, stream=None):
+    """Average ms of one layer step over K timed steps (CUDA events on the
+    stream).  With `flush`, L2 is flushed before every step and each step is
+    timed on its own, the flush outside the events."""
+    stream = stream or torch.cuda.current_stream()
+    if flush is None:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(K):
+            layer.forward(x, out, counts=counts)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / K
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for a, b in evs:
+        flush()
+        a.record(stream)
+        layer.forward(x, out, counts=counts)
+        b.record(stream)
+    torch.cuda.synchronize()
+    return sum(a.elapsed_time(b) for a, b in evs) / K
+
+
+def stage_times(layer, x, out, counts, n, flush=None):
+    """Average ms of each stage of moe_forward over n steps (events between the
+    stages split the kernels' launch overlap, so this runs outside the timed
+    steps)."""
+    from mixture_experts_layer_85_b300 import _lib
+    S = _lib.MOE_FORWARD_STAGES
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(n * (S + 1))]
+    _lib.moe_profile_arm(ev)
+    for _ in range(n):
+        if flush is not None:
+            flush()
+        layer.forward(x, out, counts=counts)
+    torch.cuda.synchronize()
+    _lib.moe_profile_arm(None)
+    res = {}
+    for s_ in range(S):
+        v = [ev[i * (S + 1) + s_].elapsed_time(ev[i * (S + 1) + s_ + 1]) for i in range(n)]
+        res[_lib.moe_forward_stage_name(s_)] = sum(v) / len(v)
+    return res
+
+
+def expert_roofline(wl, cnt, expert_ms, peaks):
+    """The expert kernel (the dominant one) against its roof: tensor when its
+    FLOP per algorithmic byte reaches the ridge of the measured peaks, else HBM."""
+    flops, byts = experts_work(wl, cnt)
+    secs = expert_ms / 1e3
+    ridge = peaks["bf16_tflops_sustained"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    if flops / byts >= ridge:
+        achieved = flops / secs / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops_sustained"],
+                "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops_sustained"], 4),
+                "frac_of_burst_peak": round(achieved / peaks["bf16_tflops"], 4),
+                "peak_source": peaks["source"] + " sustained bf16"}
+    else:
+        achieved = byts / secs / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(achieved / peaks["hbm_gbs"], 4), "peak_source": peaks["source"] + " HBM copy"}
+    roof.update({"kernel": "pair_gemm_kernel (GEMM1 + SwiGLU and GEMM2)", "traffic": None,
+                 "per_launch_flops": flops, "per_launch_algorithmic_bytes": byts,
+                 "avg_launch_ms": round(expert_ms, 4)})
+    return roof
+
+
+def layer_summary(wl, ms_step, cnt, peaks):
+    flops = wl.flops()
+    byts = layer_bytes(wl, cnt)
+    sec = ms_step / 1e3
+    tf = flops / sec / 1e12
+    gbs = byts / sec / 1e9
+    return {"ms_per_step": round(ms_step, 4), "tokens_per_s": round(wl.T / sec, 1),
+            "assignments_per_s": round(wl.T * wl.k / sec, 1), "tflops": round(tf, 2),
+            "tflops_frac_of_peak": {"burst": round(tf / peaks["bf16_tflops"], 4),
+                                    "sustained": round(tf / peaks["bf16_tflops_sustained"], 4)},
+            "gbs_algorithmic": round(gbs, 1),
+            "gbs_frac_of_hbm": {"measured": round(gbs / peaks["hbm_gbs"], 4),
+                                "nominal_8tbs": round(gbs / NOMINAL_HBM_GBS, 4)},
+            "experts_touched": int((cnt > 0).sum())}
+
+
+def blas_threads() -> int:
+    """Threads numpy's BLAS (OpenBLAS) uses: OPENBLAS_NUM_THREADS / OMP_NUM_THREADS
+    when set, else one per usable core (at most 64, the library's build limit)."""
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        v = os.environ.get(var)
+        if v and v.isdigit() and int(v) > 0:
+            return int(v)
+    return min(64, host_threads())
+
+
+def oracle_rate(wl, li, n_tok, seed=0):
+    """Oracle tokens/s on a seeded sample of n_tok tokens, on this process's cores."""
+    toks = np.sort(np.random.default_rng(seed).choice(wl.T, min(n_tok, wl.T), replace=False))
+    secs = time_oracle(wl, li, toks)
+    return {"value": round(toks.size / secs, 3), "unit": UNIT, "cores": blas_threads(), "host_cpus": host_threads(),
+            "kind": "oracle", "sample": f"{toks.size} seeded tokens of {wl.name} through the fp64 oracle "
+                                        f"(routing + experts + shared), {secs:.1f} s"}
+
+
+def oracle_rate_one_core(name: str, n_tok: int):
+    """The oracle on a single host core: a child process whose BLAS is held to
+    one thread (the thread count is fixed when numpy loads)."""
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-one-core", name, "--cpu-sample",
+                        str(n_tok)], env=env, capture_output=True, text=True, timeout=600)
+    if r.returncode != 0:
+        return {"unavailable": r.stderr.strip().splitlines()[-1] if r.stderr.strip() else f"rc {r.returncode}"}
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def per_config_lines(base_layer, base_li, dev, K, W, peaks, with_oracle):
+    """One summary per config of PER_CONFIG: the V3 decode batches reuse the
+    headline layer's packed experts (same layer, another batch and bias)."""
+    from mixture_experts_layer_85_b300.layer import MoELayer
+    flush = L2Flush(dev)
+    res = {}
+    for name in PER_CONFIG:
+        wl = inputs.WORKLOADS[name]
+        if name.startswith("v3_decode") and base_layer is not None:
+            x = inputs.make_tokens(wl).to(dev)
+            _, bias = inputs.make_router(wl)
+            layer = base_layer.variant(wl, bias)
+            li = dataclasses.replace(base_li, wl=wl, x=x, bias=bias)
+        else:
+            li = inputs.make_inputs(wl, dev)
+            layer = MoELayer(wl, li, dev)
+            x = li.x
+        out = torch.empty((wl.T, wl.d), dtype=inputs.torch_dtype(wl.out_dtype), device=dev)
+        counts = torch.empty((wl.E,), dtype=torch.int32, device=dev)
+        fl = flush if needs_flush(wl) else None
+        for _ in range(max(W, 0)):
+            layer.forward(x, out, counts=counts)
+        code, word = layer.device_status()
+        if code != 0:
+            raise RuntimeError(f"{name}: device status after warm-up {code} ({word})")
+        clocks = ClockSampler()
+        clocks.start()
+        t0 = time.time()
+        ms = time_steps(layer, x, out, counts, K, fl)
+        clk = clocks.stop(t0, time.time())
+        st = stage_times(layer, x, out, counts, max(3, min(K, 10)), fl)
+        code, word = layer.device_status()
+        if code != 0:
+            raise RuntimeError(f"{name}: device status after timed steps {code} ({word})")
+        cnt = counts.cpu().numpy()
+        line = {"workload": name, "T": wl.T, "d": wl.d, "E": wl.E, "I": wl.I, "k": wl.k,
+                "dtype": "bf16" if wl.act_dtype == "bf16" else "f32",
+                "l2": "flushed (2x L2 written) before every timed step" if fl else
+                      "no flush: weights larger than L2",
+                **layer_summary(wl, ms, cnt, peaks), "stage_ms": {k: round(v, 4) for k, v in st.items()},
+                "roofline": expert_roofline(wl, cnt, st["experts"], peaks), "clocks": clk}
+        if with_oracle:
+            line["oracle"] = oracle_rate(wl, li, oracle_sample_size(wl, 0))
+        res[name] = line
+        del layer, li, out, counts
+        torch.cuda.empty_cache()
+    return res
+
+
 # ---------------------------------------------------------------- our arm
 
 def run_ours(args, world, rank):
@@ -363,7 +559,6 @@ def run_ours(args, world, rank):
     torch.cuda.synchronize()
 
     K = args.steps
-    S = _lib.MOE_FORWARD_STAGES
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler()
@@ -391,39 +586,14 @@ def run_ours(args, world, rank):
 
     # Stage breakdown in a separate pass: events recorded between the stages
     # split the kernels' launch overlap, so they stay out of the timed steps.
-    n_prof = max(3, min(K, 10))
-    stage_ev = [torch.cuda.Event(enable_timing=True) for _ in range(n_prof * (S + 1))]
-    _lib.moe_profile_arm(stage_ev)
-    for _ in range(n_prof):
-        layer.forward(x, out, counts=counts)
-    torch.cuda.synchronize()
-    _lib.moe_profile_arm(None)
-    stage_ms = {}
-    for s in range(S):
-        v = [stage_ev[i * (S + 1) + s].elapsed_time(stage_ev[i * (S + 1) + s + 1]) for i in range(n_prof)]
-        stage_ms[_lib.moe_forward_stage_name(s)] = sum(v) / len(v)
+    stage_ms = stage_times(layer, x, out, counts, max(3, min(K, 10)))
 
     cnt = counts.cpu().numpy()
     peaks = measured_peaks()
     ms_step = elapsed_s * 1e3 / K
     flops = wl.flops()
     byts = layer_bytes(wl, cnt)
-    g1_flops, g1_bytes = experts_work(wl, cnt)
-    g1_s = stage_ms["experts"] / 1e3
-    ridge = peaks["bf16_tflops_sustained"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
-    if g1_flops / g1_bytes >= ridge:
-        achieved = g1_flops / g1_s / 1e12
-        roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops_sustained"],
-                "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops_sustained"], 4),
-                "frac_of_burst_peak": round(achieved / peaks["bf16_tflops"], 4)}
-    else:
-        achieved = g1_bytes / g1_s / 1e9
-        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": round(achieved / peaks["hbm_gbs"], 4)}
-    roof.update({"kernel": "pair_gemm_kernel (GEMM1 + SwiGLU and GEMM2, one launch)", "traffic": None,
-                 "peak_source": peaks["source"] + (" sustained bf16" if roof["bound"] == "tensor" else " HBM copy"),
-                 "per_launch_flops": g1_flops, "per_launch_algorithmic_bytes": g1_bytes,
-                 "avg_launch_ms": round(stage_ms["experts"], 4)})
+    roof = expert_roofline(wl, cnt, stage_ms["experts"], peaks)
 
     # end to end through the C ABI with host buffers: every step copies its
     # tokens host -> device, runs the layer and copies h' device -> host.  Two
@@ -452,14 +622,15 @@ def run_ours(args, world, rank):
     torch.cuda.synchronize()
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        S_tok = oracle_sample_size(wl, args.cpu_sample)
-        toks = np.sort(np.random.default_rng(0).choice(wl.T, S_tok, replace=False))
-        secs = time_oracle(wl, li, toks)
-        cpu = {"value": round(S_tok / secs, 3), "unit": UNIT, "cores": torch.get_num_threads(),
-               "host_cpus": host_threads(), "kind": "oracle",
-               "sample": f"{S_tok} seeded tokens of {wl.name} through the fp64 oracle (routing + experts + shared), "
-                         f"{secs:.1f} s"}
+    with_oracle = rank == 0 and world == 1 and not args.no_cpu_baseline
+    if with_oracle:
+        cpu = oracle_rate(wl, li, oracle_sample_size(wl, args.cpu_sample))
+        # the same oracle on one host core, on a 64-token sample of a smaller layer
+        cpu["one_core"] = oracle_rate_one_core("v2lite_t4096", 64)
+
+    per_config = None
+    if args.per_config and args.workload == DEFAULT_WORKLOAD:
+        per_config = per_config_lines(layer, li, dev, max(3, min(K, 20)), args.warmup, peaks, with_oracle)
 
     res = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": K,
@@ -476,10 +647,12 @@ def run_ours(args, world, rank):
                                 "sustained": round(flops / (elapsed_s / K) / 1e12 / peaks["bf16_tflops_sustained"], 4)},
         "gbs_algorithmic": round(byts / (elapsed_s / K) / 1e9, 1),
         "gbs_frac_of_hbm": round(byts / (elapsed_s / K) / 1e9 / peaks["hbm_gbs"], 4),
+        "gbs_frac_of_nominal_8tbs": round(byts / (elapsed_s / K) / 1e9 / NOMINAL_HBM_GBS, 4),
         "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()},
         "experts_touched": int((cnt > 0).sum()),
         "roofline": roof,
         "cpu_baseline": cpu,
+        "per_config": per_config,
         "e2e": e2e,
         "gpu_launches": int(launches),
         "host_us_per_forward_call": round(host_us, 1),
@@ -586,6 +759,11 @@ def run_reference(args, world, rank):
 
 def main(argv=None):
     args = parse_args(argv)
+    if args.oracle_one_core:
+        # child of oracle_rate_one_core: BLAS already held to one thread by the environment
+        wl = inputs.WORKLOADS[args.oracle_one_core]
+        print(json.dumps(oracle_rate(wl, inputs.make_inputs(wl, "cpu"), args.cpu_sample or 64)))
+        return
     world, rank, _ = dist_setup()
     if args.impl == "reference":
         res = run_reference(args, world, rank)

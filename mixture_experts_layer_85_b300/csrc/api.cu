@@ -146,8 +146,13 @@ moe_status check_ws(const moe_config& c, void* ws, size_t ws_bytes, Ws* out) {
   return MOE_OK;
 }
 
+// The status word's 256-byte block also holds the expert kernel's tile ticket
+// counters: [1] for a one-launch or GEMM1 launch, [2] for a GEMM2 launch.  Every
+// call clears the status word and the counters with this one memset, an
+// ordinary stream operation, before any of its kernels can start.
+constexpr int kTicketFirst = 1, kTicketSecond = 2;
 moe_status reset_status(const Ws& w, cudaStream_t s) {
-  return cuda_status(cudaMemsetAsync(w.status(), 0, sizeof(int), s));
+  return cuda_status(cudaMemsetAsync(w.status(), 0, 4 * sizeof(int), s));
 }
 
 moe_status run_gate(const moe_config& c, const void* x, const void* wg, const float* bias, int32_t* idx, float* w,
@@ -230,16 +235,17 @@ moe_status run_experts(const moe_config& c, const void* x_perm, const int32_t* o
   const long long tiles1 = tb_routed * ((2LL * c.I + 255) / 256) + tb_shared * ((2 * Is + 255) / 256);
   const long long tiles2 = (tb_routed + tb_shared) * ((c.d + 255) / 256);
   const int shared_rows = Is > 0 ? c.T : 0;
+  int* tickets = ws.status();
   if (fuse_expert_gemms(c)) {
     // one launch: GEMM2 tiles start expert by expert while GEMM1 finishes
-    return cuda_status(launch_pair_experts(cls, offsets, c.E, shared_rows, c.T, 3, done, ws.status(),
-                                           tiles1 + tiles2, s, launches, fp8));
+    return cuda_status(launch_pair_experts(cls, offsets, c.E, shared_rows, c.T, 3, done, tickets + kTicketFirst,
+                                           ws.status(), tiles1 + tiles2, s, launches, fp8));
   }
-  cudaError_t e = launch_pair_experts(cls, offsets, c.E, shared_rows, c.T, 1, nullptr, ws.status(), tiles1, s,
-                                      launches, fp8);
+  cudaError_t e = launch_pair_experts(cls, offsets, c.E, shared_rows, c.T, 1, nullptr, tickets + kTicketFirst,
+                                      ws.status(), tiles1, s, launches, fp8);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
-  return cuda_status(launch_pair_experts(cls, offsets, c.E, shared_rows, c.T, 2, nullptr, ws.status(), tiles2, s,
-                                         launches, fp8));
+  return cuda_status(launch_pair_experts(cls, offsets, c.E, shared_rows, c.T, 2, nullptr, tickets + kTicketSecond,
+                                         ws.status(), tiles2, s, launches, fp8));
 }
 
 }  // namespace

@@ -23,11 +23,17 @@
 //   phase 2 (GEMM2): W = W2 rows, X = H rows; Y[token][f] in fp32.
 //
 // Tiles are numbered [GEMM1 shared][GEMM1 routed][GEMM2 shared][GEMM2 routed]
-// and dealt round-robin to the clusters.  A GEMM2 tile of a group waits on a
-// per-group counter that every CTA bumps (release) after storing its part of
-// a GEMM1 tile of that group, so GEMM2 work starts expert by expert while
-// other clusters still run GEMM1 tiles; every cluster finishes its own GEMM1
-// tiles before its first GEMM2 tile, so the waits always resolve.  The
+// and handed out in that order at run time: a dispatcher warp of each cluster
+// draws the next tile number from a global ticket counter whenever a slot of
+// its cluster's tile ring frees up, and every role of both CTAs takes the
+// cluster's tiles from that ring in order.  An idle cluster so takes the next
+// tile wherever it is, and only running clusters hold tiles.  A GEMM2 tile of
+// a group waits on a per-group counter that every CTA bumps (release) after
+// storing its part of a GEMM1 tile of that group, so GEMM2 work starts expert
+// by expert while other clusters still run GEMM1 tiles.  Every GEMM1 ticket
+// is drawn before any GEMM2 ticket, by a cluster that is running and that
+// finishes the tile without waiting on anything later, so the waits resolve
+// whether or not every cluster of the grid is resident at once.  The
 // shared expert's GEMM1 tiles read only x and write only the shared hidden
 // rows, so they may start before the preceding kernels of the same layer call
 // (router, dispatch) complete (programmatic dependent launch): those kernels
@@ -43,14 +49,15 @@
 // k-blocks): a copy instruction has a fixed cost in the copy engine, so fewer,
 // larger copies raise the rate at which an SM's shared memory fills.
 //
-// CTA layout (224 threads, one CTA per SM, clusters of two CTAs):
+// CTA layout (256 threads, one CTA per SM, clusters of two CTAs):
 //   warp 0      TMA producer of this CTA's halves (3-stage ring of 2 k-blocks,
 //               128-byte swizzle); completion bytes count on rank 0's barrier
 //   warp 1      tensor-memory allocation (both CTAs); on rank 0 one thread
 //               issues the M=256 MMAs and commits to both CTAs' barriers
 //   warps 2..5  epilogue: tcgen05.ld of this CTA's 128 accumulator rows
-//   warp 6      tile scheduler (routed tile tables)
-//   warps 7..22 FP8 weights only (736 threads): converter warps that turn
+//   warp 6      routed tile tables (from the dispatch offsets)
+//   warp 7      rank 0: tile dispatcher (ticket counter -> tile ring)
+//   warps 8..23 FP8 weights only (768 threads): converter warps that turn
 //               each stage's e4m3 weight image into the bf16 A operand (in
 //               shared memory, or in tensor memory for decode-sized launches)
 // Two accumulators per CTA (256 columns each; 64 for FP8 decode-sized
@@ -82,7 +89,10 @@ constexpr int KB_STAGE = 2;           // k-blocks per stage and per TMA copy
 // every tile uses the 32-row token box): 5 stages of 40 KB, a deeper queue of
 // weight copies for streaming-bound work.
 constexpr int MAX_STAGES = 5;
-constexpr int THREADS = 224;
+constexpr int THREADS = 256;
+constexpr int TABLE_WARP = 6;
+constexpr int DISPATCH_WARP = 7;
+constexpr int TILE_RING = 4;         // tile numbers a cluster holds ahead of its slowest role
 constexpr int A_KB_BYTES = PM * BK * 2;          // one k-block of this CTA's weight rows
 constexpr int B_KB_BYTES = XB * BK * 2;          // one k-block of this CTA's token rows
 constexpr int A_BYTES = KB_STAGE * A_KB_BYTES;
@@ -141,6 +151,7 @@ struct PairParams {
   int shared_rows;      // tokens of the shared expert (0: none)
   int phases;           // bit 0: GEMM1 tiles, bit 1: GEMM2 tiles in this launch
   int* done;            // [num_routed + 1] GEMM1 completion counters, zero at launch (both phases only)
+  int* ticket;          // tile ticket counter of this launch, zero at launch
   int* status;
   int stages;           // ring depth (3, or MAX_STAGES for decode-sized launches; FP8: bf16 A buffers)
   int stage_bytes;      // bytes of one stage in this CTA's shared memory (FP8: of one A buffer)
@@ -168,6 +179,9 @@ struct PairCtrl {
   uint64_t drain;            // rank 0: every issued MMA completed
   uint64_t f8_full[MAX_F8];  // FP8: a slot's weight images landed (this CTA)
   uint64_t f8_empty[MAX_F8]; // FP8: the MMAs that read a slot completed (this CTA)
+  uint64_t tile_full[TILE_RING];    // each CTA: the dispatcher wrote a tile number into the slot
+  uint64_t tile_empty[TILE_RING];   // rank 0: every role of both CTAs read the slot
+  int tile_ring[TILE_RING];         // tile number, or -1: no more tiles
   uint32_t tmem_base;
   int abort;
   unsigned long long wait_ns;   // copy of PairParams::wait_ns
@@ -325,13 +339,18 @@ __device__ __forceinline__ bool wait_routed_ready(PairCtrl* c, int* status) {
   return true;
 }
 
-// Whether `tile` exists.  GEMM1 shared-expert tiles need nothing; any other
-// tile needs the routed tables.
-__device__ __forceinline__ bool pair_tile_exists(PairCtrl* c, int tile, int* status) {
-  if (tile < c->seg[1]) return true;
-  if (!wait_routed_ready(c, status)) return false;
-  return tile < c->seg[4];
-}
+// Position in a ring of n barriers/buffers and the parity of its current use,
+// advanced one step at a time (no division on the per-stage path).
+struct RingPos {
+  int i = 0;
+  uint32_t par = 0;
+  __device__ __forceinline__ void next(int n) {
+    if (++i == n) {
+      i = 0;
+      par ^= 1u;
+    }
+  }
+};
 
 // Bounded wait; on giving up it flags the status word and stops both CTAs.
 // It also gives up as soon as this CTA has been told to stop, unless
@@ -355,6 +374,42 @@ __device__ __forceinline__ bool pair_wait(uint64_t* bar, uint32_t parity, PairCt
       }
     }
   }
+}
+
+// Roles that take tiles from the ring: per CTA the producer thread, the
+// epilogue warps and the FP8 converter warps, plus the MMA issuer on rank 0.
+__host__ __device__ constexpr int tile_readers(bool fp8) { return 2 * (1 + EPI_WARPS + (fp8 ? CONV_WARPS : 0)) + 1; }
+
+// Rank 0's dispatcher thread: whenever a ring slot is free (every reader of
+// both CTAs took its last tile number), draw the next ticket from the
+// launch's counter and publish it to both CTAs (-1 once the tiles run out).
+__device__ void pair_dispatch(PairCtrl* c, const PairParams& p, uint32_t peer_abort) {
+  RingPos slot;
+  const uint32_t peer_ring = map_to_rank(smem_u32(&c->tile_ring[0]), 1);
+  const uint32_t peer_full = map_to_rank(smem_u32(&c->tile_full[0]), 1);
+  while (true) {
+    if (!pair_wait(&c->tile_empty[slot.i], slot.par ^ 1u, c, peer_abort, p.status, true)) return;
+    int t = atomicAdd(p.ticket, 1);
+    // tiles past the shared expert's GEMM1 tiles are counted by the routed tables
+    if (t >= c->seg[1] && (!wait_routed_ready(c, p.status) || t >= c->seg[4])) t = -1;
+    c->tile_ring[slot.i] = t;
+    st_remote_u32(peer_ring + 4u * uint32_t(slot.i), uint32_t(t));
+    mbar_arrive_remote(peer_full + 8u * uint32_t(slot.i));   // release (cluster): orders the store above
+    mbar_arrive(&c->tile_full[slot.i]);
+    if (t < 0) return;
+    slot.next(TILE_RING);
+  }
+}
+
+// The cluster's next tile number from the ring (position r), or -1 when the
+// tiles ran out or this CTA stopped.  Frees the slot on rank 0.
+__device__ int next_tile(PairCtrl* c, const PairParams& p, RingPos& r, uint32_t peer_abort) {
+  if (!pair_wait(&c->tile_full[r.i], r.par, c, peer_abort, p.status, true)) return -1;
+  const int t = *reinterpret_cast<volatile int*>(&c->tile_ring[r.i]);
+  mbar_arrive_remote(map_to_rank(smem_u32(&c->tile_empty[r.i]), 0));
+  r.next(TILE_RING);
+  if (t >= c->seg[1] && !wait_routed_ready(c, p.status)) return -1;
+  return t;
 }
 
 // A GEMM2 tile of group t.g needs the group's hidden rows: wait (acquire, GPU
@@ -404,7 +459,10 @@ __device__ void pair_producer(PairCtrl* c, const PairParams& p, uint8_t* stages,
   bool ok = true;
   bool waited = false;
   int ready_group = -1;   // GEMM2 group whose hidden rows are known complete
-  for (int tile = (int)cluster_id_x(); ok && pair_tile_exists(c, tile, p.status); tile += (int)cluster_count_x()) {
+  RingPos tr;
+  while (ok) {
+    const int tile = next_tile(c, p, tr, peer_abort);
+    if (tile < 0) break;
     const PairTile t = pair_tile(c, p, tile);
     if (t.cls == C1R && !waited) {
       pdl_wait();   // the permuted token rows come from the preceding grid
@@ -446,19 +504,6 @@ __device__ void pair_producer(PairCtrl* c, const PairParams& p, uint8_t* stages,
   pair_drain(c->empty, p.stages, issued, issued_par, c);
 }
 
-// Position in a ring of n barriers/buffers and the parity of its current use,
-// advanced one step at a time (no division on the per-stage path).
-struct RingPos {
-  int i = 0;
-  uint32_t par = 0;
-  __device__ __forceinline__ void next(int n) {
-    if (++i == n) {
-      i = 0;
-      par ^= 1u;
-    }
-  }
-};
-
 __device__ __forceinline__ int weight_row(const PairParams& p, const PairTile& t, uint32_t rank) {
   const bool routed = t.cls == C1R || t.cls == C2R;
   return (routed ? t.g * p.w_step[t.cls] : 0) + t.fb * PAIR_M + int(rank) * PM;
@@ -479,7 +524,10 @@ __device__ void pair_producer_fp8(PairCtrl* c, const PairParams& p, uint8_t* sta
   bool ok = true;
   bool waited = false;
   int ready_group = -1;
-  for (int tile = (int)cluster_id_x(); ok && pair_tile_exists(c, tile, p.status); tile += (int)cluster_count_x()) {
+  RingPos tr;
+  while (ok) {
+    const int tile = next_tile(c, p, tr, peer_abort);
+    if (tile < 0) break;
     const PairTile t = pair_tile(c, p, tile);
     if (t.cls == C1R && !waited) {
       pdl_wait();   // the permuted token rows come from the preceding grid
@@ -565,10 +613,12 @@ __device__ void pair_converter(PairCtrl* c, const PairParams& p, uint8_t* stages
   RingPos slot, stage, fpos;      // slot ring, A buffers, per-stage barriers
   const int nfull = p.nf * p.sps;
   bool ok = true;
-  for (int tile = (int)cluster_id_x(); ok; tile += (int)cluster_count_x()) {
-    int exists = 0;
-    if (lane == 0) exists = pair_tile_exists(c, tile, p.status) ? 1 : 0;
-    if (!__shfl_sync(0xffffffffu, exists, 0)) break;
+  RingPos tr;
+  while (ok) {
+    int tile = 0;
+    if (lane == 0) tile = next_tile(c, p, tr, peer_abort);
+    tile = __shfl_sync(0xffffffffu, tile, 0);
+    if (tile < 0) break;
     const PairTile t = pair_tile(c, p, tile);
     const int nks = p.K[t.cls] / 128;
     for (int ks = 0; ks < nks; ++ks) {
@@ -640,8 +690,10 @@ __device__ void pair_mma(PairCtrl* c, const PairParams& p, uint8_t* stages, uint
   RingPos fpos;   // FP8: per-stage barriers full[0 .. nf * sps)
   int ctr = 0;
   bool ok = true;
-  for (int tile = (int)cluster_id_x(); ok && pair_tile_exists(c, tile, p.status);
-       tile += (int)cluster_count_x(), ++ctr) {
+  RingPos tr;
+  for (; ok; ++ctr) {
+    const int tile = next_tile(c, p, tr, peer_abort);
+    if (tile < 0) break;
     const PairTile t = pair_tile(c, p, tile);
     const uint32_t idesc = idesc_bf16_f32(PAIR_M, t.n_mma);
     const int acc = ctr & 1;
@@ -714,10 +766,12 @@ __device__ void pair_epilogue(PairCtrl* c, const PairParams& p, uint32_t tmem, i
                               uint32_t peer_abort) {
   const int q = warp & 3;   // the tensor-memory lane quarter this warp may read
   int ctr = 0;
-  for (int tile = (int)cluster_id_x();; tile += (int)cluster_count_x(), ++ctr) {
-    int exists = 0;
-    if (lane == 0) exists = pair_tile_exists(c, tile, p.status) ? 1 : 0;
-    if (!__shfl_sync(0xffffffffu, exists, 0)) break;
+  RingPos tr;
+  for (;; ++ctr) {
+    int tile = 0;
+    if (lane == 0) tile = next_tile(c, p, tr, peer_abort);
+    tile = __shfl_sync(0xffffffffu, tile, 0);
+    if (tile < 0) break;
     const PairTile t = pair_tile(c, p, tile);
     const int acc = ctr & 1;
     if (!pair_warp_wait(&c->tfull[acc], uint32_t(ctr >> 1) & 1u, c, peer_abort, p.status, lane)) break;
@@ -809,6 +863,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FP8 ? THREADS_FP8 : 
       mbar_init(&c->tempty[a], 2 * EPI_WARPS);
     }
     mbar_init(&c->drain, 1);
+    for (int i = 0; i < TILE_RING; ++i) {
+      mbar_init(&c->tile_full[i], 1);
+      mbar_init(&c->tile_empty[i], tile_readers(FP8));
+    }
     c->abort = 0;
     c->wait_ns = p.wait_ns;
     c->routed_ready = 0;
@@ -848,13 +906,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FP8 ? THREADS_FP8 : 
     pair_epilogue(c, p, tmem, warp, lane, rank, peer_abort);
   } else if (warp >= THREADS / 32) {
     pair_converter(c, p, stages, tmem, warp, lane, peer_abort);
-  } else {
-    // scheduler warp: the routed tables need the dispatch offsets
+  } else if (warp == TABLE_WARP) {
+    // the routed tables need the dispatch offsets
     pdl_wait();
     pair_schedule(c, p, lane);
     __syncwarp();
     __threadfence_block();
     if (lane == 0) *reinterpret_cast<volatile int*>(&c->routed_ready) = 1;
+  } else if (warp == DISPATCH_WARP) {
+    if (lane == 0 && rank == 0) pair_dispatch(c, p, peer_abort);
   }
   tc_fence_before();
   // neither CTA leaves while the other may still signal its barriers
@@ -893,8 +953,7 @@ cudaError_t launch_pair(const PairParams& p, long long max_tiles, cudaStream_t s
     return cudaSuccess;
   });
   if (e != cudaSuccess) return e;
-  // every cluster must be resident at once: GEMM2 tiles wait for GEMM1 tiles
-  // of other clusters
+  // one cluster per pair of SMs that can hold one (more would only queue)
   const long long pairs = max_tiles < max_clusters ? max_tiles : max_clusters;
   return launch_pdl(pair_gemm_kernel<FP8>, dim3(int(2 * pairs)), dim3(kThreads), kPairSmem, stream, p);
 }
@@ -915,10 +974,11 @@ void get_expert_fault(unsigned long long* wait_ns, int* need_extra) {
 }
 
 cudaError_t launch_pair_experts(const PairClass cls[4], const int32_t* offsets, int num_routed, int shared_rows,
-                                int max_group_rows, int phases, int* done, int* status, long long max_tiles,
-                                cudaStream_t stream, int* launches, bool fp8) {
+                                int max_group_rows, int phases, int* done, int* ticket, int* status,
+                                long long max_tiles, cudaStream_t stream, int* launches, bool fp8) {
   if (max_tiles <= 0) return cudaSuccess;
   if (num_routed < 1 || num_routed + 1 > MAX_GROUPS || phases < 1 || phases > 3) return cudaErrorInvalidValue;
+  if (ticket == nullptr) return cudaErrorInvalidValue;
   if (phases == 3 && done == nullptr) return cudaErrorInvalidValue;
   PairParams p;
   memset(&p, 0, sizeof(p));
@@ -948,6 +1008,7 @@ cudaError_t launch_pair_experts(const PairClass cls[4], const int32_t* offsets, 
   p.num_routed = num_routed;
   p.shared_rows = shared_rows;
   p.done = done;
+  p.ticket = ticket;
   p.phases = phases;
   p.status = status;
   const unsigned long long wns = g_wait_ns.load();

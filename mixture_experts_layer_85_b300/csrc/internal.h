@@ -135,14 +135,15 @@ struct PairClass {
 // 16-row interleave), GEMM2 fp32.  phases: 1 = GEMM1 tiles, 2 = GEMM2 tiles,
 // 3 = both in one launch, GEMM2 tiles of a group waiting on per-group GEMM1
 // completion counters done [num_routed + 1], which must then be zero when the
-// launch starts.  max_group_rows: an upper bound of any group's rows (the
-// batch size T).  The shared expert's GEMM1 tiles may run before the
-// preceding grid completes.
+// launch starts.  ticket: the launch's tile ticket counter, zero when the
+// launch starts (and not touched by anything that may still run then).
+// max_group_rows: an upper bound of any group's rows (the batch size T).  The
+// shared expert's GEMM1 tiles may run before the preceding grid completes.
 // fp8: the weights are FP8 stage images (one bulk copy per stage), dequantized
 // to bf16 in shared memory by converter warps before each MMA.
 cudaError_t launch_pair_experts(const PairClass cls[4], const int32_t* offsets, int num_routed, int shared_rows,
-                                int max_group_rows, int phases, int* done, int* status, long long max_tiles,
-                                cudaStream_t stream, int* launches, bool fp8 = false);
+                                int max_group_rows, int phases, int* done, int* ticket, int* status,
+                                long long max_tiles, cudaStream_t stream, int* launches, bool fp8 = false);
 
 // Fault injection for tests of the device-side time-out path
 // (moe_debug_inject): the expert kernel's wait limit for later launches

@@ -28,6 +28,21 @@ class MoELayer:
         if keep_unpacked:
             self.unpacked = (li.w1, li.w3, li.w2, li.ws1, li.ws3, li.ws2)
 
+    def variant(self, wl: Workload, bias: Optional[torch.Tensor]) -> "MoELayer":
+        """The same layer (packed experts and gate weight shared, not copied)
+        under another workload of identical shape: another batch size or
+        selection bias.  It owns its own workspace."""
+        for f in ("d", "E", "I", "n_shared", "act_dtype", "gate_w_dtype", "expert_w_dtype"):
+            if getattr(wl, f) != getattr(self.wl, f):
+                raise ValueError(f"variant changes the layer's {f}")
+        v = object.__new__(MoELayer)
+        v.wl, v.cfg, v.device = wl, _lib.make_config(wl), self.device
+        v.act, v.out_dtype = self.act, torch_dtype(wl.out_dtype)
+        v.wg, v.packed = self.wg, self.packed
+        v.bias = None if bias is None else bias.to(self.device, torch.float32).contiguous()
+        v.ws = torch.empty(_lib.moe_workspace_size(v.cfg), dtype=torch.uint8, device=self.device)
+        return v
+
     def forward(self, x: torch.Tensor, out: Optional[torch.Tensor] = None, idx=None, w=None, counts=None,
                 stream=None) -> torch.Tensor:
         if out is None:

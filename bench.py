@@ -665,8 +665,7 @@ def run_ours(args, world, rank):
 
 def run_backward(args, world, rank):
     """Layer backward (moe_backward) on the workload: W warm-ups, then K timed
-    calls bracketed by CUDA events on the stream (each call synchronises the
-    stream once to read the group sizes, inside the timed region)."""
+    calls bracketed by CUDA events on the stream."""
     from mixture_experts_layer_85_b300 import _lib
 
     wl = inputs.WORKLOADS[args.workload]
@@ -724,7 +723,7 @@ def run_backward(args, world, rank):
             "tflops": round(tflops, 2),
             "roofline": {"bound": "tensor", "achieved": round(tflops, 2), "peak": peaks["bf16_tflops_sustained"],
                          "unit": "TFLOP/s", "frac": round(tflops / peaks["bf16_tflops_sustained"], 4),
-                         "kernel": "whole backward (cuBLAS expert GEMMs + own kernels)", "traffic": None,
+                         "kernel": "whole backward (expert-kernel products + elementwise kernels)", "traffic": None,
                          "peak_source": peaks["source"] + " sustained bf16"},
             "clocks": clk}
 

@@ -15,8 +15,7 @@
  * Conventions shared by every call:
  *  - All tensor pointers are DEVICE pointers, owned by the caller, 16-byte
  *    aligned, dense row-major.  Weights use the nn.Linear layout (out x in).
- *    The forward calls never allocate or free device memory (moe_backward's
- *    exception is stated at its declaration).
+ *    The library never allocates or frees device memory.
  *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
  *    stream).  Arguments are validated on the host first; on any error the call
  *    returns a non-zero moe_status and launches nothing.
@@ -198,8 +197,8 @@ MOE_API moe_status moe_permute_noalloc(const moe_config* cfg, const void* x, con
                                        void* stream);
 
 /* Bytes of workspace moe_backward needs for `cfg` (the forward's workspace
- * plus the backward's buffers).  bf16 activations and bf16 expert weights
- * only (MOE_ERR_UNSUPPORTED otherwise). */
+ * plus the backward's buffers).  bf16 activations and bf16 expert weights,
+ * d a multiple of 128 (MOE_ERR_UNSUPPORTED otherwise). */
 MOE_API moe_status moe_backward_workspace_size(const moe_config* cfg, size_t* bytes);
 
 /* Backward of the layer: the gradient of L = <dout, out> with respect to x,
@@ -217,12 +216,15 @@ MOE_API moe_status moe_backward_workspace_size(const moe_config* cfg, size_t* by
  *   Outputs (device, fp32, written, not accumulated): dx [T,d], dWg [E,d],
  *   dW1, dW3 [E,I,d], dW2 [E,d,I], dWs1, dWs3 [I_s,d], dWs2 [d,I_s].
  *   ws: >= moe_backward_workspace_size bytes, 16-byte aligned.
- * The per-expert matrix products run in cuBLAS (bf16 operands, fp32
- * accumulation and outputs); the routed rows' intermediate gradients are
- * rounded to bf16 before their products, as the forward rounds H.  The call
- * reads the group sizes back to the host and so synchronises `stream` once.
- * All calls share one cuBLAS handle (created on the first call, its stream set
- * per call): serialise backward calls made from several host threads.
+ * Every matrix product runs on the library's CTA-pair tensor-core kernel
+ * (bf16 operands, fp32 accumulation and outputs): the expert weights are read
+ * in place through transposed views where a product needs W^T, and the
+ * routed rows use a padded per-expert layout so each weight gradient reduces
+ * over its own rows.  The routed rows' intermediate gradients are rounded to
+ * bf16 before their products, as the forward rounds H; the router's d logits
+ * are rounded to bf16 for dW_g and for their part of dx.  Group sizes stay on
+ * the device: the call neither synchronises `stream` nor allocates.
+ * d must be a multiple of 128 (MOE_ERR_UNSUPPORTED otherwise).
  * All pointers 16-byte aligned. */
 MOE_API moe_status moe_backward(const moe_config* cfg, const void* x, const void* Wg, const float* bias,
                                 const void* W1, const void* W3, const void* W2, const void* Ws1,

@@ -42,9 +42,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     with ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 1)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
     tmp = LIB + ".tmp"
-    r = subprocess.run([NVCC, *ARCH, "-shared", "-o", tmp, *objs, "-lcublas", "-Xlinker", "-rpath",
-                        "-Xlinker", os.path.join(os.path.dirname(os.path.dirname(NVCC)), "lib64")],
-                       capture_output=True, text=True)
+    r = subprocess.run([NVCC, *ARCH, "-shared", "-o", tmp, *objs], capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr}")
     os.replace(tmp, LIB)

@@ -147,12 +147,15 @@ moe_status check_ws(const moe_config& c, void* ws, size_t ws_bytes, Ws* out) {
 }
 
 // The status word's 256-byte block also holds the expert kernel's tile ticket
-// counters: [1] for a one-launch or GEMM1 launch, [2] for a GEMM2 launch.  Every
-// call clears the status word and the counters with this one memset, an
-// ordinary stream operation, before any of its kernels can start.
-constexpr int kTicketFirst = 1, kTicketSecond = 2;
+// counters: [1] for a one-launch or GEMM1 launch, [2] for a GEMM2 launch, and
+// [3 .. 3 + kBackwardTickets) for the backward's launches.  Every call clears
+// the status word and the counters with this one memset, an ordinary stream
+// operation, before any of its kernels can start.
+constexpr int kTicketFirst = 1, kTicketSecond = 2, kTicketBackward = 3;
+constexpr int kStatusInts = 16;
+static_assert(kTicketBackward + kBackwardTickets <= kStatusInts, "status block");
 moe_status reset_status(const Ws& w, cudaStream_t s) {
-  return cuda_status(cudaMemsetAsync(w.status(), 0, 4 * sizeof(int), s));
+  return cuda_status(cudaMemsetAsync(w.status(), 0, kStatusInts * sizeof(int), s));
 }
 
 moe_status run_gate(const moe_config& c, const void* x, const void* wg, const float* bias, int32_t* idx, float* w,
@@ -426,7 +429,9 @@ moe_status moe_backward_workspace_size(const moe_config* cfg, size_t* bytes) {
   if (st != MOE_OK) return st;
   if (bytes == nullptr) return MOE_ERR_INVALID_ARG;
   const moe_config& c = *cfg;
-  if (!is_bf16(c) || c.expert_w_dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  // bf16 only; d a multiple of 128 (the products read each expert's weights in
+  // whole 128-row stages through transposed views)
+  if (!is_bf16(c) || c.expert_w_dtype != MOE_BF16 || c.d % 128 != 0) return MOE_ERR_UNSUPPORTED;
   *bytes = ws_layout(c).total + backward_extra_bytes(c);
   return MOE_OK;
 }
@@ -438,7 +443,9 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const void* Wg, co
   moe_status st = check_config(cfg);
   if (st != MOE_OK) return st;
   const moe_config& c = *cfg;
-  if (!is_bf16(c) || c.expert_w_dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  // bf16 only; d a multiple of 128 (the products read each expert's weights in
+  // whole 128-row stages through transposed views)
+  if (!is_bf16(c) || c.expert_w_dtype != MOE_BF16 || c.d % 128 != 0) return MOE_ERR_UNSUPPORTED;
   const bool shared = c.n_shared > 0;
   const void* need[] = {x, Wg, W1, W3, W2, dout, dx, dWg, dW1, dW3, dW2};
   for (const void* q : need)
@@ -474,9 +481,10 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const void* Wg, co
   int32_t* idx = W.at<int32_t>(W.L.idx);
   float* w = W.at<float>(W.L.w);
   st = run_gate(c, x, Wg, bias, idx, w, W, s, &n);
+  // the dispatch tables only: the backward gathers the tokens into its own padded layout
   if (st == MOE_OK)
-    st = cuda_status(launch_permute(c, x, idx, W.at<int32_t>(W.L.counts), W.at<int32_t>(W.L.offsets),
-                                    W.at<int32_t>(W.L.row2tok), W.at<int32_t>(W.L.tok2row), W.at<void>(W.L.x_perm),
+    st = cuda_status(launch_permute(c, nullptr, idx, W.at<int32_t>(W.L.counts), W.at<int32_t>(W.L.offsets),
+                                    W.at<int32_t>(W.L.row2tok), W.at<int32_t>(W.L.tok2row), nullptr,
                                     W.at<int32_t>(W.L.chunk_counts), W.at<int32_t>(W.L.chunk_base), W.status(), s, &n,
                                     nullptr, 0));
   count_launches(n);
@@ -502,34 +510,14 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const void* Wg, co
   p.idx = idx;
   p.gates = w;
   p.offsets = W.at<int32_t>(W.L.offsets);
-  p.row2tok = W.at<int32_t>(W.L.row2tok);
   p.tok2row = W.at<int32_t>(W.L.tok2row);
-  p.x_perm = W.at<void>(W.L.x_perm);
-  p.Y = W.at<float>(W.L.y);
-  char* b = W.base;
-  p.G = reinterpret_cast<float*>(b + B.G);
-  p.U = reinterpret_cast<float*>(b + B.U);
-  p.dH = reinterpret_cast<float*>(b + B.dH);
-  p.dXr = reinterpret_cast<float*>(b + B.dXr);
-  p.Gs = reinterpret_cast<float*>(b + B.Gs);
-  p.Us = reinterpret_cast<float*>(b + B.Us);
-  p.dHs = reinterpret_cast<float*>(b + B.dHs);
-  p.dXs = reinterpret_cast<float*>(b + B.dXs);
-  p.dout32 = reinterpret_cast<float*>(b + B.dout32);
-  p.x32 = reinterpret_cast<float*>(b + B.x32);
-  p.wg32 = reinterpret_cast<float*>(b + B.wg32);
-  p.logits = reinterpret_cast<float*>(b + B.logits);
-  p.dl = reinterpret_cast<float*>(b + B.dl);
-  p.dg = reinterpret_cast<float*>(b + B.dg);
-  p.Hb = reinterpret_cast<__nv_bfloat16*>(b + B.Hb);
-  p.dYb = reinterpret_cast<__nv_bfloat16*>(b + B.dYb);
-  p.dGb = reinterpret_cast<__nv_bfloat16*>(b + B.dGb);
-  p.dUb = reinterpret_cast<__nv_bfloat16*>(b + B.dUb);
-  p.Hsb = reinterpret_cast<__nv_bfloat16*>(b + B.Hsb);
-  p.dGsb = reinterpret_cast<__nv_bfloat16*>(b + B.dGsb);
-  p.dUsb = reinterpret_cast<__nv_bfloat16*>(b + B.dUsb);
-  p.doutb = reinterpret_cast<__nv_bfloat16*>(b + B.doutb);
-  return cuda_status(run_backward_core(c, p, s));
+  p.logits = W.at<float>(W.L.logits);
+  p.ksplit = gate_ksplit(c);
+  p.plane = (long long)c.T * c.E;
+  p.status = W.status();
+  p.tickets = W.status() + kTicketBackward;
+  p.base = W.base;
+  return cuda_status(run_backward_core(c, p, B, s));
 }
 
 moe_status moe_balance_update(const moe_config* cfg, const int32_t* counts, float* bias, float gamma, float* stats,

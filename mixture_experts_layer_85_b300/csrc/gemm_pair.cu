@@ -68,6 +68,7 @@
 #include <cudaTypedefs.h>
 
 #include <atomic>
+#include <climits>
 
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
@@ -169,6 +170,28 @@ struct PairParams {
   // those waits run out: host-side fault injection for tests).
   unsigned long long wait_ns;
   int need_extra;
+  // Operand layouts beyond the forward's (all zero there).  a_mn / b_mn: the
+  // weight (A) / token (B) operand is MN-major, read through a 2-D map over
+  // [K rows][M or N columns] in boxes of 64 x 128 (a transposed view of a
+  // row-major buffer).  MN-major A: group g's K rows start at g * a_kstep, and
+  // K indices from K1 on come from tmW2 (a second matrix: K concatenated).
+  int a_mn[NCLS];
+  int b_mn[NCLS];
+  int K1[NCLS];
+  int a_kstep[NCLS];
+  CUtensorMap tmW2[NCLS];
+  // kmode = 1: the reduction runs over each group's token rows (K of group g
+  // = offsets[g+1] - offsets[g] rows from offsets[g], a multiple of 128, zero
+  // rows allowed), every group has N[cls] columns, and the routed class's
+  // output moves out_gstride elements per group (weight gradients).
+  int kmode;
+  int N[NCLS];
+  int b_col0[NCLS];          // MN-major B: first column of the class's N range in its buffer
+  long long out_gstride[NCLS];
+  // Token rows of group g start at row_base[g] when given (a padded layout),
+  // else at offsets[g]; row_bound bounds every group's rows.
+  const int32_t* row_base;
+  long long row_bound;
 };
 
 struct PairCtrl {
@@ -204,6 +227,9 @@ struct PairTile {
   int fb, tb, row_start, rows;
   int n_valid;   // token rows of this tile
   int n_mma;     // MMA N = n_valid rounded up to 16
+  int n0;        // first N index of the tile (token row, or column in kmode)
+  int k0;        // first K index (kmode: the group's first token row)
+  int nks;       // stages of 128 K
 };
 
 __device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
@@ -217,8 +243,10 @@ __device__ __forceinline__ const CUtensorMap* x_map(const PairParams& p, int cls
   return n_mma / 2 <= XTINY ? &p.tmXt[cls] : (n_mma / 2 <= XSMALL ? &p.tmXs[cls] : &p.tmX[cls]);
 }
 
+// Tiles of a group with `rows` token rows: token blocks x weight blocks (in
+// kmode the N extent is fixed and the rows are the reduction).
 __device__ __forceinline__ int pair_group_tiles(const PairParams& p, int cls, int rows) {
-  return cdiv(rows, PN) * cdiv(p.M[cls], PAIR_M);
+  return cdiv(p.kmode ? p.N[cls] : rows, PN) * cdiv(p.M[cls], PAIR_M);
 }
 
 // GEMM1 counter value at which a group's hidden rows are complete: every
@@ -236,9 +264,9 @@ __device__ void pair_schedule(PairCtrl* c, const PairParams& p, int lane) {
   const int lo = min(ng, lane * per), hi = min(ng, lo + per);
   int local1 = 0, local2 = 0;
   for (int g = lo; g < hi; ++g) {
-    int rs = p.offsets[g];
-    int rows = p.offsets[g + 1] - rs;
-    if (rows < 0 || rs < 0 || (long long)rs + rows > p.out_rows[C1R]) {
+    int rows = p.offsets[g + 1] - p.offsets[g];
+    int rs = p.row_base != nullptr ? p.row_base[g] : p.offsets[g];
+    if (rows < 0 || rs < 0 || (long long)rs + rows > p.row_bound || (p.kmode && (rows & 127))) {
       flag_status(p.status, DEV_BAD_ROW);
       rs = 0;
       rows = 0;
@@ -306,7 +334,8 @@ __device__ __forceinline__ PairTile pair_tile(const PairCtrl* c, const PairParam
     t.rows = c->rows[lo];
     local -= ts[lo];
   }
-  const int tbn = cdiv(t.rows, PN), fbn = cdiv(p.M[t.cls], PAIR_M);
+  const int ncols = p.kmode ? p.N[t.cls] : t.rows;   // N extent of the group
+  const int tbn = cdiv(ncols, PN), fbn = cdiv(p.M[t.cls], PAIR_M);
   if (tbn > fbn) {
     t.tb = local / fbn;
     t.fb = local % fbn;
@@ -314,8 +343,11 @@ __device__ __forceinline__ PairTile pair_tile(const PairCtrl* c, const PairParam
     t.fb = local / tbn;
     t.tb = local % tbn;
   }
-  t.n_valid = min(PN, t.rows - t.tb * PN);
+  t.n_valid = min(PN, ncols - t.tb * PN);
   t.n_mma = (t.n_valid + 15) & ~15;
+  t.n0 = (p.kmode ? 0 : t.row_start) + t.tb * PN;
+  t.k0 = p.kmode ? t.row_start : 0;
+  t.nks = p.kmode ? t.rows / 128 : (p.K[t.cls] / BK + KB_STAGE - 1) / KB_STAGE;
   return t;
 }
 
@@ -477,13 +509,16 @@ __device__ void pair_producer(PairCtrl* c, const PairParams& p, uint8_t* stages,
       ready_group = t.g;
     }
     const bool routed = t.cls == C1R || t.cls == C2R;
-    const int w_row = (routed ? t.g * p.w_step[t.cls] : 0) + t.fb * PAIR_M + int(rank) * PM;
-    const int x_row = t.row_start + t.tb * PN + int(rank) * (t.n_mma / 2);
-    const int nks = (p.K[t.cls] / BK + KB_STAGE - 1) / KB_STAGE;   // stages of this tile
-    const CUtensorMap* xmap = x_map(p, t.cls, t.n_mma);
-    // both CTAs' full boxes (a k-block past K reads as zeros and still counts)
-    const uint32_t bytes = 2u * uint32_t(A_BYTES + KB_STAGE * x_kb_bytes(t.n_mma));
-    for (int ks = 0; ks < nks; ++ks) {
+    const int cls = t.cls;
+    const int w_row = (routed ? t.g * p.w_step[cls] : 0) + t.fb * PAIR_M + int(rank) * PM;
+    const int x_row = t.n0 + int(rank) * (t.n_mma / 2);
+    const CUtensorMap* xmap = x_map(p, cls, t.n_mma);
+    // MN-major B: this CTA's n_mma / 2 columns in boxes of 64
+    const int nbx = (t.n_mma / 2 + 63) / 64;
+    // both CTAs' full boxes (a box past the tensor's end reads as zeros and still counts)
+    const uint32_t bytes =
+        2u * uint32_t(A_BYTES + (p.b_mn[cls] ? nbx * B_KB_BYTES : KB_STAGE * x_kb_bytes(t.n_mma)));
+    for (int ks = 0; ks < t.nks; ++ks) {
       if (!pair_wait(&c->empty[stage], phase ^ 1u, c, peer_abort, p.status)) {
         ok = false;
         break;
@@ -491,8 +526,23 @@ __device__ void pair_producer(PairCtrl* c, const PairParams& p, uint8_t* stages,
       uint8_t* sa = stages + stage * p.stage_bytes;
       if (rank == 0) mbar_arrive_expect_tx(&c->full[stage], bytes);
       const uint32_t fb = map_to_rank(smem_u32(&c->full[stage]), 0);   // rank 0's barrier
-      tma_load_3d_pair(sa, &p.tmW[t.cls], fb, w_row, ks * KB_STAGE);
-      tma_load_3d_pair(sa + A_BYTES, xmap, fb, x_row, ks * KB_STAGE);
+      const int kk = t.k0 + ks * (KB_STAGE * BK);                     // first K index of the stage
+      if (!p.a_mn[cls]) {
+        tma_load_3d_pair(sa, &p.tmW[cls], fb, w_row, kk / BK);
+      } else {
+        const bool second = kk >= p.K1[cls];
+        const CUtensorMap* wm = second ? &p.tmW2[cls] : &p.tmW[cls];
+        const int krow = (routed ? t.g * p.a_kstep[cls] : 0) + (second ? kk - p.K1[cls] : kk);
+        const int mn = t.fb * PAIR_M + int(rank) * PM;
+        tma_load_2d_pair(sa, wm, fb, mn, krow);
+        tma_load_2d_pair(sa + A_KB_BYTES, wm, fb, mn + BK, krow);
+      }
+      if (!p.b_mn[cls]) {
+        tma_load_3d_pair(sa + A_BYTES, xmap, fb, x_row, kk / BK);
+      } else {
+        for (int h = 0; h < nbx; ++h)
+          tma_load_2d_pair(sa + A_BYTES + h * B_KB_BYTES, &p.tmX[cls], fb, p.b_col0[cls] + x_row + h * BK, kk);
+      }
       issued |= 1u << stage;
       issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
       if (++stage == p.stages) {
@@ -695,12 +745,13 @@ __device__ void pair_mma(PairCtrl* c, const PairParams& p, uint8_t* stages, uint
     const int tile = next_tile(c, p, tr, peer_abort);
     if (tile < 0) break;
     const PairTile t = pair_tile(c, p, tile);
-    const uint32_t idesc = idesc_bf16_f32(PAIR_M, t.n_mma);
+    const uint32_t a_mn = FP8 ? 0u : uint32_t(p.a_mn[t.cls]), b_mn = FP8 ? 0u : uint32_t(p.b_mn[t.cls]);
+    const uint32_t idesc = idesc_bf16_f32(PAIR_M, t.n_mma) | (a_mn << 15) | (b_mn << 16);
     const int acc = ctr & 1;
     if (!pair_wait(&c->tempty[acc], (uint32_t(ctr >> 1) & 1u) ^ 1u, c, peer_abort, p.status, true)) break;
     tc_fence_after();
     const uint32_t d_tmem = tmem + uint32_t(acc) * p.acc_stride;
-    const int nks = (p.K[t.cls] / BK + KB_STAGE - 1) / KB_STAGE;
+    const int nks = t.nks;
     const uint32_t b_kb = uint32_t(x_kb_bytes(t.n_mma));
     for (int ks = 0; ks < nks; ++ks) {
       const int half = FP8 ? (ks & (p.sps - 1)) : 0;
@@ -722,6 +773,19 @@ __device__ void pair_mma(PairCtrl* c, const PairParams& p, uint8_t* stages, uint
           for (int kk = 0; kk < BK / 16; ++kk)
             mma_bf16_pair_ta(d_tmem, a_t + uint32_t(j * 32 + kk * 8), sw128_kmajor_desc(b0 + j * b_kb + kk * 32),
                              idesc, (ks | j | kk) != 0 ? 1u : 0u);
+      } else if (!FP8 && (a_mn | b_mn)) {
+        // MN-major operands: a stage is 128 K rows of 128-byte MN rows, 16 K per MMA
+#pragma unroll
+        for (int j = 0; j < KB_STAGE; ++j)
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const int s16 = j * (BK / 16) + kk;
+            const uint64_t ad = a_mn ? sw128_mnmajor_desc(a0 + s16 * 2048, KB_STAGE * BK)
+                                     : sw128_kmajor_desc(a0 + j * A_KB_BYTES + kk * 32);
+            const uint64_t bd = b_mn ? sw128_mnmajor_desc(b0 + s16 * 2048, KB_STAGE * BK)
+                                     : sw128_kmajor_desc(b0 + j * b_kb + kk * 32);
+            mma_bf16_pair(d_tmem, ad, bd, idesc, (ks | j | kk) != 0 ? 1u : 0u);
+          }
       } else {
 #pragma unroll
         for (int j = 0; j < KB_STAGE; ++j)
@@ -777,7 +841,7 @@ __device__ void pair_epilogue(PairCtrl* c, const PairParams& p, uint32_t tmem, i
     if (!pair_warp_wait(&c->tfull[acc], uint32_t(ctr >> 1) & 1u, c, peer_abort, p.status, lane)) break;
     tc_fence_after();
     const uint32_t tbase = tmem + uint32_t(acc) * p.acc_stride + (uint32_t(q * 32) << 16);
-    const long long row0 = (long long)t.row_start + (long long)t.tb * PN;
+    const long long row0 = t.n0;
     const int ncols = (t.n_valid + 15) & ~15;
     const bool gemm1 = t.cls == C1R || t.cls == C1S;
     if (gemm1) {
@@ -809,12 +873,19 @@ __device__ void pair_epilogue(PairCtrl* c, const PairParams& p, uint32_t tmem, i
     } else {
       const int f = t.fb * PAIR_M + int(rank) * PM + q * 32 + lane;
       const bool fvalid = f < p.M[t.cls];
-      float* out = static_cast<float*>(p.out[t.cls]) + f;
+      float* out = static_cast<float*>(p.out[t.cls]) + f +
+                   (p.kmode && t.cls == C2R ? (long long)t.g * p.out_gstride[C2R] : 0LL);
       const long long ld = p.ld_out[t.cls];
 #pragma unroll 1
       for (int cc = 0; cc < ncols; cc += 16) {
         float v[16];
-        tmem_ld16(tbase + cc, v);
+        if (t.nks > 0) {
+          tmem_ld16(tbase + cc, v);
+        } else {
+          // a group without rows to reduce over (kmode): its block of D is zero
+#pragma unroll
+          for (int i = 0; i < 16; ++i) v[i] = 0.0f;
+        }
         if (fvalid) {
 #pragma unroll
           for (int i = 0; i < 16; ++i)
@@ -1002,9 +1073,11 @@ cudaError_t launch_pair_experts(const PairClass cls[4], const int32_t* offsets, 
     p.out_rows[i] = g.out_rows;
     p.M[i] = g.M;
     p.K[i] = g.K;
+    p.K1[i] = INT_MAX;
     p.w_step[i] = g.w_step;
   }
   p.offsets = offsets;
+  p.row_bound = cls[C1R].out_rows;
   p.num_routed = num_routed;
   p.shared_rows = shared_rows;
   p.done = done;
@@ -1044,6 +1117,81 @@ cudaError_t launch_pair_experts(const PairClass cls[4], const int32_t* offsets, 
     p.acc_stride = ACC_STRIDE;
     e = launch_pair<false>(p, max_tiles, stream);
   }
+  if (e == cudaSuccess && launches) ++*launches;
+  return e;
+}
+
+cudaError_t launch_pair_gemm(const PairOperands* routed, const PairOperands* shared, const int32_t* offsets,
+                             const int32_t* row_base, long long row_bound, int num_routed, int shared_rows,
+                             int kmode, int* ticket, int* status, long long max_tiles, cudaStream_t stream,
+                             int* launches) {
+  if (max_tiles <= 0) return cudaSuccess;
+  if (num_routed < 0 || num_routed + 1 > MAX_GROUPS || ticket == nullptr) return cudaErrorInvalidValue;
+  if ((routed == nullptr) != (num_routed == 0) || (shared == nullptr) != (shared_rows <= 0))
+    return cudaErrorInvalidValue;
+  PairParams p;
+  memset(&p, 0, sizeof(p));
+  bool any_b_mn = false;
+  const PairOperands* ops[2] = {routed, shared};
+  for (int r = 0; r < 2; ++r) {
+    const int i = r == 0 ? C2R : C2S;
+    const PairOperands* o = ops[r] != nullptr ? ops[r] : ops[1 - r];   // an absent class repeats the other (unused)
+    if (o == nullptr) return cudaErrorInvalidValue;
+    if (o->K % (KB_STAGE * BK) != 0 || o->M <= 0) return cudaErrorInvalidValue;
+    if (o->a_mn) {
+      if (!encode_bf16_map(&p.tmW[i], o->A, o->a_rows, o->a_cols, KB_STAGE * BK, 1)) return cudaErrorInvalidValue;
+      const void* a2 = o->A2 != nullptr ? o->A2 : o->A;
+      const int64_t a2_rows = o->A2 != nullptr ? o->a2_rows : o->a_rows;
+      if (!encode_bf16_map(&p.tmW2[i], a2, a2_rows, o->a_cols, KB_STAGE * BK, 1)) return cudaErrorInvalidValue;
+      if (o->K1 % (KB_STAGE * BK) != 0) return cudaErrorInvalidValue;
+    } else if (!encode_bf16_map(&p.tmW[i], o->A, o->a_rows, o->a_cols, PM, KB_STAGE)) {
+      return cudaErrorInvalidValue;
+    }
+    if (o->b_mn) {
+      if (!encode_bf16_map(&p.tmX[i], o->B, o->b_rows, o->b_cols, KB_STAGE * BK, 1)) return cudaErrorInvalidValue;
+      any_b_mn = true;
+    } else {
+      if (!encode_bf16_map(&p.tmX[i], o->B, o->b_rows, o->b_cols, XB, KB_STAGE)) return cudaErrorInvalidValue;
+      if (!encode_bf16_map(&p.tmXs[i], o->B, o->b_rows, o->b_cols, XSMALL, KB_STAGE)) return cudaErrorInvalidValue;
+      if (!encode_bf16_map(&p.tmXt[i], o->B, o->b_rows, o->b_cols, XTINY, KB_STAGE)) return cudaErrorInvalidValue;
+    }
+    p.a_mn[i] = o->a_mn ? 1 : 0;
+    p.b_mn[i] = o->b_mn ? 1 : 0;
+    p.K1[i] = o->a_mn && o->A2 != nullptr ? o->K1 : INT_MAX;   // no second source: never switch
+    p.a_kstep[i] = o->a_kstep;
+    p.out[i] = o->out;
+    p.ld_out[i] = o->ld_out;
+    p.out_rows[i] = o->out_rows;
+    p.out_gstride[i] = o->out_gstride;
+    p.M[i] = o->M;
+    p.K[i] = o->K;
+    p.N[i] = o->N;
+    p.b_col0[i] = o->b_col0;
+    p.w_step[i] = o->w_step;
+  }
+  // the GEMM1 classes are not used (GEMM2 tiles only); keep them well-formed
+  p.tmW[C1R] = p.tmW[C2R];
+  p.tmW[C1S] = p.tmW[C2S];
+  p.M[C1R] = p.M[C2R];
+  p.M[C1S] = p.M[C2S];
+  p.K[C1R] = p.K[C2R];
+  p.K[C1S] = p.K[C2S];
+  p.offsets = offsets;
+  p.row_base = row_base;
+  p.row_bound = row_bound;
+  p.num_routed = num_routed;
+  p.shared_rows = shared != nullptr ? shared_rows : 0;
+  p.kmode = kmode;
+  p.phases = 2;
+  p.ticket = ticket;
+  p.status = status;
+  const unsigned long long wns = g_wait_ns.load();
+  p.wait_ns = wns > 0 ? wns : kWaitLimitNs;
+  p.stages = 3;
+  p.stage_bytes = STAGE_BYTES;
+  p.acc_stride = ACC_STRIDE;
+  (void)any_b_mn;
+  cudaError_t e = launch_pair<false>(p, max_tiles, stream);
   if (e == cudaSuccess && launches) ++*launches;
   return e;
 }

@@ -152,6 +152,42 @@ cudaError_t launch_pair_experts(const PairClass cls[4], const int32_t* offsets, 
 void set_expert_fault(unsigned long long wait_ns, int need_extra);
 void get_expert_fault(unsigned long long* wait_ns, int* need_extra);
 
+// One operand class of a launch of the expert kernel with fp32 output rows
+// (GEMM2 tiles only), for products beyond the forward's: D[f][j] = sum_k
+// A[f][k] * B[j][k], out[j][f] (row j, column f, ld_out).
+//   A: K-major rows [a_rows, a_cols = K] (group g from row g * w_step), or
+//      MN-major (a_mn): a row-major [a_rows = K rows][a_cols = M] buffer read
+//      transposed, group g's K rows from g * a_kstep; with A2 the K indices
+//      from K1 on come from A2 (same layout, a2_rows rows).
+//   B: K-major token rows [b_rows, b_cols = K], or MN-major (b_mn): a
+//      row-major [b_rows = K rows][b_cols = N] buffer read transposed.
+//   kmode launches (weight gradients): the token rows are K, N is fixed, and
+//   the routed output moves out_gstride elements per group.
+struct PairOperands {
+  const void* A = nullptr;
+  int64_t a_rows = 0, a_cols = 0;
+  bool a_mn = false;
+  const void* A2 = nullptr;
+  int64_t a2_rows = 0;
+  int K1 = 0;
+  int a_kstep = 0;
+  int w_step = 0;
+  const void* B = nullptr;
+  int64_t b_rows = 0, b_cols = 0;
+  bool b_mn = false;
+  int b_col0 = 0;           // MN-major B: first column of N within the buffer's b_cols
+  int M = 0, K = 0, N = 0;
+  float* out = nullptr;
+  int64_t ld_out = 0, out_rows = 0, out_gstride = 0;
+};
+// routed (nullable when num_routed = 0) over groups g with rows offsets[g] ..
+// offsets[g+1] (starting at row_base[g] when given), shared (nullable) over
+// shared_rows token rows (kmode: the K extent, a multiple of 128).
+cudaError_t launch_pair_gemm(const PairOperands* routed, const PairOperands* shared, const int32_t* offsets,
+                             const int32_t* row_base, long long row_bound, int num_routed, int shared_rows,
+                             int kmode, int* ticket, int* status, long long max_tiles, cudaStream_t stream,
+                             int* launches);
+
 // ---------------------------------------------------------------------- router
 cudaError_t launch_gate_split(const float* wg, int E, int d, void* wsplit, cudaStream_t s, int* launches);
 cudaError_t launch_gate_logits_simt(const moe_config& c, const void* x, const void* wg, float* logits,
@@ -170,6 +206,10 @@ cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* id
                            int32_t* offsets, int32_t* row2tok, int32_t* tok2row, void* x_perm,
                            int32_t* chunk_counts, int32_t* chunk_base, int* status, cudaStream_t s,
                            int* launches, int* zero = nullptr, int n_zero = 0);
+
+// x rows [T, row_bytes] -> x_perm rows tok2row[t][j] (rows < `rows`; -1 skipped).
+cudaError_t launch_gather_rows(const void* x, const int32_t* tok2row, int T, int k, long long rows, size_t row_bytes,
+                               void* x_perm, int* status, cudaStream_t s, int* launches);
 
 // -------------------------------------------------------------------- experts
 cudaError_t launch_prepack(const moe_config& c, const void* W1, const void* W3, const void* W2,
@@ -207,28 +247,35 @@ struct PackedLayout {
 PackedLayout packed_layout(const moe_config& c);
 
 // --------------------------------------------------------------- backward
-// Backward-only workspace (byte offsets from `base`, 256-byte aligned).
+// Backward-only workspace (byte offsets from the forward workspace's start,
+// 256-byte aligned).  Routed rows use a padded layout of R_max rows: expert g's
+// rows start at koff[g], a multiple of 128, pad rows zero.
 struct BwdLayout {
-  size_t G, U, Hb, dYb, dH, dGb, dUb, dXr, Gs, Us, Hsb, dHs, dGsb, dUsb, dXs, dout32, doutb, x32, wg32, logits, dl,
-      dg, total;
+  size_t koff, tok2row_pad, Xp, G, U, H, Y, dY, dH, dGU, Gs, Us, Hs, dHs, dGUs, dXs, doutb, dout32, dlb, dg, dXg, wgb,
+      total;
+  long long R_max;
+  int E_pad;
 };
 BwdLayout backward_layout(const moe_config& c, size_t base);
 size_t backward_extra_bytes(const moe_config& c);
 
-// Pointers of one backward call: the caller's tensors, the forward dispatch
-// (idx, gates, offsets, row2tok, tok2row, x_perm) and the scratch buffers.
+// One backward call: the caller's tensors and the forward router's results
+// in the workspace (routing, dispatch, the logits planes).
 struct BwdPtrs {
   const void *x, *Wg, *W1, *W3, *W2, *Ws1, *Ws3, *Ws2, *dout;
   float *dx, *dWg, *dW1, *dW3, *dW2, *dWs1, *dWs3, *dWs2;
-  const int32_t *idx, *offsets, *row2tok, *tok2row;
+  const int32_t *idx, *offsets, *tok2row;
   const float* gates;
-  const void* x_perm;
-  float* Y;   // [T*k, d] fp32 expert outputs (recomputed)
-  float *G, *U, *dH, *dXr, *Gs, *Us, *dHs, *dXs, *dout32, *x32, *wg32, *logits, *dl, *dg;
-  __nv_bfloat16 *Hb, *dYb, *dGb, *dUb, *Hsb, *dGsb, *dUsb, *doutb;
+  const float* logits;   // `ksplit` fp32 partial planes of [T, E], `plane` elements apart
+  int ksplit;
+  long long plane;
+  int* status;
+  int* tickets;          // zeroed tile ticket counters, one per expert-kernel launch (10)
+  char* base;            // workspace base
 };
-// Everything after the dispatch: synchronises `s` once (group sizes).
-cudaError_t run_backward_core(const moe_config& c, const BwdPtrs& p, cudaStream_t s);
+constexpr int kBackwardTickets = 10;
+// Everything after the routing and dispatch, stream-ordered, no host synchronisation.
+cudaError_t run_backward_core(const moe_config& c, const BwdPtrs& p, const BwdLayout& L, cudaStream_t s);
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 inline size_t dtype_bytes(int dt) { return dt == MOE_BF16 ? 2 : 4; }

@@ -128,9 +128,26 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t smem_addr) {
   return d;
 }
 
+// Shared-memory matrix descriptor of an MN-major operand tile stored with the
+// 128-byte swizzle: each 128-byte row holds 64 consecutive MN elements of one
+// K index, 8-row (K) atoms of 1024 B.  The tile is laid out as the 2-D TMA
+// boxes of 64 MN x `krows` K rows write it, one box after the other along MN:
+// stride byte offset = 1024 B between 8-row K groups, leading byte offset =
+// krows * 128 B between 64-element MN chunks.
+__device__ __forceinline__ uint64_t sw128_mnmajor_desc(uint32_t smem_addr, uint32_t krows) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(((krows * 128u) >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>(1024u >> 4) << 32;
+  d |= static_cast<uint64_t>(1u) << 46;
+  d |= static_cast<uint64_t>(2u) << 61;
+  return d;
+}
+
 // Instruction descriptor of kind::f16 with bf16 A/B, fp32 D, both K-major:
 // D format F32 (bit 4), A format BF16 (bits 7-9 = 1), B format BF16 (bits
-// 10-12 = 1), N >> 3 (bits 17-22), M >> 4 (bits 24-28).
+// 10-12 = 1), N >> 3 (bits 17-22), M >> 4 (bits 24-28).  Bit 15 (A) and bit 16
+// (B) select an MN-major operand.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
          (static_cast<uint32_t>(M >> 4) << 24);
@@ -248,6 +265,16 @@ __device__ __forceinline__ void tma_load_3d_pair(void* smem_dst, const CUtensorM
       "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes "
       "[%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(smem_dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster_addr), "r"(0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
+// 2-D variant (c0 = inner coordinate, c1 = row) of the pair-form tiled load.
+__device__ __forceinline__ void tma_load_2d_pair(void* smem_dst, const CUtensorMap* map, uint32_t bar_cluster_addr,
+                                                 int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster_addr), "r"(c0), "r"(c1)
       : "memory");
 }
 

@@ -128,6 +128,13 @@ WORKLOADS["v3_profile_fp8_e16_t1"] = Workload(
     norm_topk=True, routed_scaling_factor=2.5, act_dtype="bf16", gate_w_dtype="bf16", bias="zipf",
     expert_w_dtype="fp8")
 
+# The V3 prefill layer's routing at full size (T=16384, d=7168, 256 experts,
+# top-8, the same gate weights and bias) with the expert hidden size cut to 128:
+# the router, dispatch, gather and combine kernels see exactly the prefill
+# shapes in about 8 GB of device memory (the profiler's case for them).
+WORKLOADS["v3_profile_route_t16384"] = replace(WORKLOADS["v3_prefill_t16384"], name="v3_profile_route_t16384",
+                                               I=128)
+
 CONFIG_ORDER = ["tiny_fp32_t128", "v2lite_t4096", "v2_t8192", "v3_prefill_t16384",
                 "v3_decode_t1", "v3_decode_t8", "v3_decode_t64", "v3_decode_t512"]
 DECODE_T = (1, 8, 64, 512)

@@ -44,6 +44,10 @@ CASES = {
     # one token: most experts receive no row (their gradients are exact zeros)
     "v3_bwd_t1": inputs.small_workload(W["v3_decode_t1"], name="v3_bwd_t1", T=1, d=256, E=32, I=128, n_group=8,
                                        topk_group=4),
+    # the V3 expert shape (d 7168, I 2048): full 256-row weight tiles, many 128-row
+    # reduction stages per expert, shared expert and router at their real widths
+    "v3_bwd_fullshape_t256": inputs.small_workload(W["v3_prefill_t16384"], name="v3_bwd_fullshape_t256", T=256,
+                                                   E=8, k=4, n_group=4, topk_group=2),
 }
 
 

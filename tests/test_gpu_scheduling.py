@@ -64,6 +64,11 @@ def _hold_kernel():
     return driver, mod, fn
 
 
+def _nonblocking_stream(driver):
+    st = _check(driver.cuStreamCreate(driver.CUstream_flags.CU_STREAM_NON_BLOCKING.value))
+    return st, torch.cuda.ExternalStream(int(st))
+
+
 def test_expert_kernel_finishes_while_other_work_holds_most_sms():
     T = 64
     wl = inputs.small_workload(inputs.WORKLOADS["v3_prefill_t16384"], name="v3_sched_t64", T=T, d=1024, E=64,
@@ -76,34 +81,43 @@ def test_expert_kernel_finishes_while_other_work_holds_most_sms():
 
     driver, mod, fn = _hold_kernel()
     n_sm = torch.cuda.get_device_properties(0).multi_processor_count
-    n_hold = n_sm - 48                                     # leaves 24 pairs of SMs (n_sm is even)
-    side = torch.cuda.Stream()
+    n_hold = 2 * (n_sm // 4)                               # half the SMs, in pairs
+    hold_raw, hold_s = _nonblocking_stream(driver)
+    run_raw, run_s = _nonblocking_stream(driver)
     out = torch.zeros(n_hold, dtype=torch.int32, device="cuda")
     args = ((HOLD_NS, out.data_ptr()), (ctypes.c_ulonglong, ctypes.c_void_p))
     idx = torch.empty((T, wl.k), dtype=torch.int32, device="cuda")
     w = torch.empty((T, wl.k), dtype=torch.float32, device="cuda")
     counts = torch.empty((wl.E,), dtype=torch.int32, device="cuda")
+    y = torch.empty((T, wl.d), dtype=torch.float32, device="cuda")
+    ev = {n: torch.cuda.Event(enable_timing=True) for n in ("start", "held", "layer0", "layer1")}
+    # load every kernel used below before the SMs are held (a first launch may
+    # load its module, which waits for the device)
+    with torch.cuda.stream(run_s):
+        torch.cuda._sleep(1000)
+        layer.forward(li.x, y, idx=idx, w=w, counts=counts, stream=run_s)
+    torch.cuda.synchronize()
     _lib.moe_debug_inject(_lib.MOE_DEBUG_WAIT_LIMIT_NS, 20_000_000)
     try:
-        start = torch.cuda.Event(enable_timing=True)
-        start.record(side)
-        _check(driver.cuLaunchKernel(fn, n_hold, 1, 1, 32, 1, 1, HOLD_SMEM, driver.CUstream(side.cuda_stream),
-                                     args, 0))
-        # the layer on the default stream, while the SMs are held
-        torch.cuda._sleep(1_000_000)                       # let the holding CTAs become resident first
-        y = layer.forward(li.x, idx=idx, w=w, counts=counts)
-        done = torch.cuda.Event(enable_timing=True)
-        done.record()
-        held = torch.cuda.Event(enable_timing=True)
-        held.record(side)
+        ev["start"].record(hold_s)
+        _check(driver.cuLaunchKernel(fn, n_hold, 1, 1, 32, 1, 1, HOLD_SMEM, hold_raw, args, 0))
+        ev["held"].record(hold_s)
+        with torch.cuda.stream(run_s):
+            torch.cuda._sleep(2_000_000)                   # let the holding CTAs become resident first
+            ev["layer0"].record(run_s)
+            layer.forward(li.x, y, idx=idx, w=w, counts=counts, stream=run_s)
+            ev["layer1"].record(run_s)
         torch.cuda.synchronize()
         code, word = layer.device_status()
     finally:
         _lib.moe_debug_inject(_lib.MOE_DEBUG_WAIT_LIMIT_NS, 0)
         torch.cuda.synchronize()
         driver.cuModuleUnload(mod)
-    assert code == _lib.MOE_OK, (_lib.moe_status_string(code), word)
+        driver.cuStreamDestroy(hold_raw)
+        driver.cuStreamDestroy(run_raw)
+    t = {n: ev["start"].elapsed_time(e) for n, e in ev.items() if n != "start"}
+    assert code == _lib.MOE_OK, (_lib.moe_status_string(code), word, t)
     assert int((out > 0).sum()) == n_hold
     # the layer ran while the SMs were held (it finished before the holder did)
-    assert start.elapsed_time(done) < start.elapsed_time(held), (start.elapsed_time(done), start.elapsed_time(held))
+    assert t["layer1"] < t["held"], t
     check_layer(wl, li, y, idx, w, counts)

@@ -235,7 +235,6 @@ __global__ void __launch_bounds__(SMALL_BLOCK) permute_small_kernel(const int32_
 // row once (chunks of 8 vectors per lane) and stores it k times, so x streams
 // from memory once and the k copies are plain writes.
 constexpr int GATHER_CHUNK = 8;   // 16-byte vectors per lane per chunk
-constexpr long long kGatherBlocksPerSm = 2;
 __global__ void __launch_bounds__(256) gather_tokens_kernel(const uint4* __restrict__ x,
                                                             const int32_t* __restrict__ tok2row, int T, int k,
                                                             long long R, int vec_per_row, uint4* __restrict__ x_perm,
@@ -319,10 +318,7 @@ cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* id
   const long long R = (long long)c.T * c.k;
   const int vec = int((size_t)c.d * dtype_bytes(c.act_dtype) / 16);
   long long blocks = (c.T + 7) / 8;
-  // Two blocks per SM keep HBM busy and leave registers for one CTA of the
-  // expert kernel that follows: its shared-expert tiles (which read only x)
-  // then run beside the gather instead of after it.
-  const long long cap = kGatherBlocksPerSm * num_sms();
+  const long long cap = 8LL * num_sms();
   if (blocks > cap) blocks = cap;
   cudaError_t e = launch_pdl(gather_tokens_kernel, dim3((int)blocks), dim3(256), 0, s, static_cast<const uint4*>(x),
                              tok2row, c.T, c.k, R, vec, static_cast<uint4*>(x_perm), status, zero, n_zero);

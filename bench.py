@@ -355,17 +355,23 @@ NOMINAL_HBM_GBS = 8000.0
 
 
 class L2Flush:
-    """Writes a buffer of twice the device's L2 size, so the next step reads
-    its weights from HBM (the decode batches are smaller than L2 otherwise)."""
+    """Before a timed decode step: writes a buffer of twice the device's L2
+    size, so nothing the previous step read is left in L2, then reads another
+    buffer as large, so the lines that write left dirty go back to HBM now and
+    not inside the timed step."""
 
     def __init__(self, dev):
         l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 126 << 20)) or (126 << 20)
-        self.buf = torch.empty(2 * l2 // 4 + 256, dtype=torch.int32, device=dev)
+        n = 2 * l2 // 4 + 256
+        self.buf = torch.empty(n, dtype=torch.int32, device=dev)
+        self.rd = torch.zeros(n, dtype=torch.int32, device=dev)
+        self.sink = torch.zeros((), dtype=torch.int64, device=dev)
         self.n = 0
 
     def __call__(self):
         self.n += 1
         self.buf.fill_(self.n)
+        torch.sum(self.rd, dim=0, dtype=torch.int64, out=self.sink)
 
 
 def needs_flush(wl) -> bool:
@@ -524,8 +530,8 @@ def per_config_lines(base_layer, base_li, dev, K, W, peaks, with_oracle):
         cnt = counts.cpu().numpy()
         line = {"workload": name, "T": wl.T, "d": wl.d, "E": wl.E, "I": wl.I, "k": wl.k,
                 "dtype": "bf16" if wl.act_dtype == "bf16" else "f32",
-                "l2": "flushed (2x L2 written) before every timed step" if fl else
-                      "no flush: weights larger than L2",
+                "l2": "flushed before every timed step (2x L2 written, then 2x L2 read, outside the timed step)"
+                      if fl else "no flush: weights larger than L2",
                 **layer_summary(wl, ms, cnt, peaks), "stage_ms": {k: round(v, 4) for k, v in st.items()},
                 "roofline": expert_roofline(wl, cnt, st["experts"], peaks), "clocks": clk}
         if with_oracle:

@@ -29,6 +29,10 @@ constexpr int kMaxK = 16;
 constexpr int kGateTargetTiles = 296;
 constexpr int kGatePromoteK = 256;   // K per fp32-promoted tensor-core partial sum
 
+constexpr int kTicketFirst = 1, kTicketSecond = 2, kTicketBackward = 3;
+constexpr int kStatusInts = 16;
+static_assert(kTicketBackward + kBackwardTickets <= kStatusInts, "status block");
+
 struct WsLayout {
   size_t status, logits, wsplit, chunk_counts, chunk_base, counts, offsets, row2tok, tok2row, idx, w, x_perm, h, hs,
       y, ys, done, total;
@@ -71,7 +75,10 @@ WsLayout ws_layout(const moe_config& c) {
     off = align_up(off + bytes, 256);
     return at;
   };
-  L.status = take(256);
+  // the status word, the expert kernel's tile tickets and its GEMM1
+  // completion counters: one block that the call's first memset clears
+  L.status = take(size_t(kStatusInts) * 4 + size_t(c.E + 1) * 4);
+  L.done = L.status + size_t(kStatusInts) * 4;
   L.logits = take(size_t(gate_ksplit(c)) * c.T * c.E * 4);
   L.wsplit = take(use_tc_gate(c) && c.gate_w_dtype == MOE_F32 ? size_t(c.E) * 3 * c.d * 2 : 0);
   L.chunk_counts = take(nch * c.E * 4);
@@ -87,7 +94,6 @@ WsLayout ws_layout(const moe_config& c) {
   L.hs = take(size_t(c.T) * I_s(c) * eb);
   L.y = take(R * c.d * 4);
   L.ys = take(size_t(c.T) * c.d * 4);
-  L.done = take(size_t(c.E + 1) * 4);   // per-group GEMM1 completion counters
   L.total = off;
   return L;
 }
@@ -146,16 +152,13 @@ moe_status check_ws(const moe_config& c, void* ws, size_t ws_bytes, Ws* out) {
   return MOE_OK;
 }
 
-// The status word's 256-byte block also holds the expert kernel's tile ticket
-// counters: [1] for a one-launch or GEMM1 launch, [2] for a GEMM2 launch, and
-// [3 .. 3 + kBackwardTickets) for the backward's launches.  Every call clears
-// the status word and the counters with this one memset, an ordinary stream
-// operation, before any of its kernels can start.
-constexpr int kTicketFirst = 1, kTicketSecond = 2, kTicketBackward = 3;
-constexpr int kStatusInts = 16;
-static_assert(kTicketBackward + kBackwardTickets <= kStatusInts, "status block");
-moe_status reset_status(const Ws& w, cudaStream_t s) {
-  return cuda_status(cudaMemsetAsync(w.status(), 0, kStatusInts * sizeof(int), s));
+// The status word's block also holds the expert kernel's tile ticket counters
+// ([1] for a one-launch or GEMM1 launch, [2] for a GEMM2 launch, [3 .. 3 +
+// kBackwardTickets) for the backward's launches) and, after kStatusInts ints,
+// its E + 1 GEMM1 completion counters.  Every call clears the block with this
+// one memset, an ordinary stream operation, before any of its kernels can start.
+moe_status reset_status(const Ws& w, cudaStream_t s, int E) {
+  return cuda_status(cudaMemsetAsync(w.status(), 0, (kStatusInts + size_t(E) + 1) * sizeof(int), s));
 }
 
 moe_status run_gate(const moe_config& c, const void* x, const void* wg, const float* bias, int32_t* idx, float* w,
@@ -200,7 +203,7 @@ moe_status run_gate(const moe_config& c, const void* x, const void* wg, const fl
 
 moe_status run_experts(const moe_config& c, const void* x_perm, const int32_t* offsets, const void* x,
                        const void* packed, void* y_perm, void* y_shared, const Ws& ws, cudaStream_t s,
-                       int* launches, bool counters_zeroed = false) {
+                       int* launches) {
   const PackedLayout P = packed_layout(c);
   const char* pb = static_cast<const char*>(packed);
   const long long R = (long long)c.T * c.k;
@@ -213,9 +216,7 @@ moe_status run_experts(const moe_config& c, const void* x_perm, const int32_t* o
   }
   void* h = ws.at<void>(ws.L.h);
   void* hs = ws.at<void>(ws.L.hs);
-  int* done = ws.at<int>(ws.L.done);
-  if (!counters_zeroed && fuse_expert_gemms(c) && cudaMemsetAsync(done, 0, size_t(c.E + 1) * 4, s) != cudaSuccess)
-    return MOE_ERR_CUDA;
+  int* done = ws.at<int>(ws.L.done);   // cleared with the status word
   PairClass cls[4];
   // GEMM1 + SwiGLU: H[rows, I] = silu(X W1^T) * (X W3^T), packed W1/W3 rows [2I, d] per expert
   const bool fp8 = P.fp8;
@@ -303,7 +304,7 @@ moe_status moe_gate_topk(const moe_config* cfg, const void* x, const void* Wg, c
   if ((st = check_ws(c, ws, ws_bytes, &W)) != MOE_OK) return st;
   if (c.T == 0) return MOE_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if ((st = reset_status(W, s)) != MOE_OK) return st;
+  if ((st = reset_status(W, s, c.E)) != MOE_OK) return st;
   int n = 0;
   st = run_gate(c, x, Wg, bias, idx, w, W, s, &n);
   count_launches(n);
@@ -327,7 +328,7 @@ moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* idx,
     if (cudaMemsetAsync(offsets, 0, size_t(c.E + 1) * 4, s) != cudaSuccess) return MOE_ERR_CUDA;
     return cuda_status(cudaMemsetAsync(counts, 0, size_t(c.E) * 4, s));
   }
-  if ((st = reset_status(W, s)) != MOE_OK) return st;
+  if ((st = reset_status(W, s, c.E)) != MOE_OK) return st;
   int n = 0;
   cudaError_t e = launch_permute(c, x, idx, counts, offsets, row2tok, tok2row, x_perm, W.at<int32_t>(W.L.chunk_counts),
                                  W.at<int32_t>(W.L.chunk_base), W.status(), s, &n);
@@ -349,7 +350,7 @@ moe_status moe_grouped_swiglu(const moe_config* cfg, const void* x_perm, const i
   if ((st = check_ws(c, ws, ws_bytes, &W)) != MOE_OK) return st;
   if (c.T == 0) return MOE_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if ((st = reset_status(W, s)) != MOE_OK) return st;
+  if ((st = reset_status(W, s, c.E)) != MOE_OK) return st;
   int n = 0;
   st = run_experts(c, x_perm, offsets, x, packed, y_perm, y_shared, W, s, &n);
   count_launches(n);
@@ -368,7 +369,7 @@ moe_status moe_combine(const moe_config* cfg, const void* y_perm, const void* y_
   if ((st = check_ws(c, ws, ws_bytes, &W)) != MOE_OK) return st;
   if (c.T == 0) return MOE_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if ((st = reset_status(W, s)) != MOE_OK) return st;
+  if ((st = reset_status(W, s, c.E)) != MOE_OK) return st;
   int n = 0;
   cudaError_t e = launch_combine(c, y_perm, y_shared, tok2row, w, out, W.status(), s, &n);
   count_launches(n);
@@ -390,7 +391,7 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const void* Wg, con
   if ((st = check_ws(c, ws, ws_bytes, &W)) != MOE_OK) return st;
   if (c.T == 0) return MOE_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if ((st = reset_status(W, s)) != MOE_OK) return st;
+  if ((st = reset_status(W, s, c.E)) != MOE_OK) return st;
   int n = 0;
   int32_t* idx = idx_out ? idx_out : W.at<int32_t>(W.L.idx);
   float* w = w_out ? w_out : W.at<float>(W.L.w);
@@ -404,16 +405,13 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const void* Wg, con
   st = run_gate(c, x, Wg, bias, idx, w, W, s, &n);
   if (st == MOE_OK) {
     profile_mark(s);
-    // the gather also zeroes the expert GEMMs' completion counters
-    const bool tc = is_bf16(c);
     cudaError_t e = launch_permute(c, x, idx, counts, offsets, W.at<int32_t>(W.L.row2tok), tok2row, x_perm,
-                                   W.at<int32_t>(W.L.chunk_counts), W.at<int32_t>(W.L.chunk_base), W.status(), s, &n,
-                                   tc ? W.at<int>(W.L.done) : nullptr, tc ? c.E + 1 : 0);
+                                   W.at<int32_t>(W.L.chunk_counts), W.at<int32_t>(W.L.chunk_base), W.status(), s, &n);
     st = cuda_status(e);
   }
   if (st == MOE_OK) {
     profile_mark(s);
-    st = run_experts(c, x_perm, offsets, x, packed, y, ys, W, s, &n, true);
+    st = run_experts(c, x_perm, offsets, x, packed, y, ys, W, s, &n);
   }
   if (st == MOE_OK) {
     profile_mark(s);
@@ -476,7 +474,7 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const void* Wg, co
       if (q.p && q.n && cudaMemsetAsync(q.p, 0, q.n * sizeof(float), s) != cudaSuccess) return MOE_ERR_CUDA;
     return MOE_OK;
   }
-  if ((st = reset_status(W, s)) != MOE_OK) return st;
+  if ((st = reset_status(W, s, c.E)) != MOE_OK) return st;
   int n = 0;
   int32_t* idx = W.at<int32_t>(W.L.idx);
   float* w = W.at<float>(W.L.w);
@@ -485,8 +483,7 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const void* Wg, co
   if (st == MOE_OK)
     st = cuda_status(launch_permute(c, nullptr, idx, W.at<int32_t>(W.L.counts), W.at<int32_t>(W.L.offsets),
                                     W.at<int32_t>(W.L.row2tok), W.at<int32_t>(W.L.tok2row), nullptr,
-                                    W.at<int32_t>(W.L.chunk_counts), W.at<int32_t>(W.L.chunk_base), W.status(), s, &n,
-                                    nullptr, 0));
+                                    W.at<int32_t>(W.L.chunk_counts), W.at<int32_t>(W.L.chunk_base), W.status(), s, &n));
   count_launches(n);
   if (st != MOE_OK) return st;
   BwdPtrs p;

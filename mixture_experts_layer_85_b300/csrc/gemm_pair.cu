@@ -22,7 +22,7 @@
 //     lane l+16 by a warp shuffle and stores H[token][f] = silu(g)*u in bf16.
 //   phase 2 (GEMM2): W = W2 rows, X = H rows; Y[token][f] in fp32.
 //
-// Tiles are numbered [GEMM1 shared][GEMM1 routed][GEMM2 shared][GEMM2 routed]
+// Tiles are numbered [GEMM1 shared][GEMM2 shared][GEMM1 routed][GEMM2 routed]
 // and handed out in that order at run time: a dispatcher warp of each cluster
 // draws the next tile number from a global ticket counter whenever a slot of
 // its cluster's tile ring frees up, and every role of both CTAs takes the
@@ -30,14 +30,15 @@
 // tile wherever it is, and only running clusters hold tiles.  A GEMM2 tile of
 // a group waits on a per-group counter that every CTA bumps (release) after
 // storing its part of a GEMM1 tile of that group, so GEMM2 work starts expert
-// by expert while other clusters still run GEMM1 tiles.  Every GEMM1 ticket
-// is drawn before any GEMM2 ticket, by a cluster that is running and that
-// finishes the tile without waiting on anything later, so the waits resolve
-// whether or not every cluster of the grid is resident at once.  The
-// shared expert's GEMM1 tiles read only x and write only the shared hidden
-// rows, so they may start before the preceding kernels of the same layer call
+// by expert while other clusters still run GEMM1 tiles.  A group's GEMM1
+// tickets are all drawn before its GEMM2 tickets, by clusters that are running
+// and that finish those tiles without waiting on anything drawn later, so the
+// waits resolve whether or not every cluster of the grid is resident at once.
+// The shared expert's tiles read only x and their own hidden rows, so the
+// whole shared FFN may run before the preceding kernels of the same layer call
 // (router, dispatch) complete (programmatic dependent launch): those kernels
-// touch neither.  Early starts never reach further back: every call of the
+// touch neither, and the completion counters were cleared with the call's
+// status word before any of its kernels started.  Early starts never reach further back: every call of the
 // library begins with an ordinary stream operation (clearing its status word),
 // which starts only after all earlier work in the stream has completed, so a
 // previous call that still reads the hidden rows, or a previous layer that
@@ -209,7 +210,7 @@ struct PairCtrl {
   int abort;
   unsigned long long wait_ns;   // copy of PairParams::wait_ns
   int seg[5];                // tile numbers where the four segments start, and the total
-  int routed_ready;          // the routed tile tables (and seg[2..4]) are built
+  int routed_ready;          // the routed tile tables (and seg[3..4]) are built
   int tile_start[2][MAX_GROUPS + 1];   // per phase: exclusive prefix of routed tiles
   int row_start[MAX_GROUPS];
   int rows[MAX_GROUPS];
@@ -296,10 +297,9 @@ __device__ void pair_schedule(PairCtrl* c, const PairParams& p, int lane) {
   if (lane == 31) {
     c->tile_start[0][ng] = incl1;
     c->tile_start[1][ng] = incl2;
-    // seg[0] = 0 and seg[1] = GEMM1 shared tiles were set at start-up
+    // seg[0..2] (the shared expert's segments) were set at start-up
     const bool g1 = p.phases & 1, g2 = p.phases & 2;
-    c->seg[2] = c->seg[1] + (g1 ? incl1 : 0);
-    c->seg[3] = c->seg[2] + (g2 && p.shared_rows > 0 ? pair_group_tiles(p, C2S, p.shared_rows) : 0);
+    c->seg[3] = c->seg[2] + (g1 ? incl1 : 0);
     c->seg[4] = c->seg[3] + (g2 ? incl2 : 0);
   }
 }
@@ -314,13 +314,13 @@ __device__ __forceinline__ PairTile pair_tile(const PairCtrl* c, const PairParam
   int seg = 0;
   if (tile >= c->seg[1]) seg = tile < c->seg[2] ? 1 : (tile < c->seg[3] ? 2 : 3);
   local = tile - c->seg[seg];
-  if (seg == 0 || seg == 2) {
+  if (seg < 2) {
     t.cls = seg == 0 ? C1S : C2S;
     t.g = p.num_routed;
     t.row_start = 0;
     t.rows = p.shared_rows;
   } else {
-    const int ph = seg == 1 ? 0 : 1;
+    const int ph = seg == 2 ? 0 : 1;
     const int* ts = c->tile_start[ph];
     int lo = 0, hi = p.num_routed - 1;
     while (lo < hi) {
@@ -422,8 +422,8 @@ __device__ void pair_dispatch(PairCtrl* c, const PairParams& p, uint32_t peer_ab
   while (true) {
     if (!pair_wait(&c->tile_empty[slot.i], slot.par ^ 1u, c, peer_abort, p.status, true)) return;
     int t = atomicAdd(p.ticket, 1);
-    // tiles past the shared expert's GEMM1 tiles are counted by the routed tables
-    if (t >= c->seg[1] && (!wait_routed_ready(c, p.status) || t >= c->seg[4])) t = -1;
+    // tiles past the shared expert's are counted by the routed tables
+    if (t >= c->seg[2] && (!wait_routed_ready(c, p.status) || t >= c->seg[4])) t = -1;
     c->tile_ring[slot.i] = t;
     st_remote_u32(peer_ring + 4u * uint32_t(slot.i), uint32_t(t));
     mbar_arrive_remote(peer_full + 8u * uint32_t(slot.i));   // release (cluster): orders the store above
@@ -440,7 +440,7 @@ __device__ int next_tile(PairCtrl* c, const PairParams& p, RingPos& r, uint32_t 
   const int t = *reinterpret_cast<volatile int*>(&c->tile_ring[r.i]);
   mbar_arrive_remote(map_to_rank(smem_u32(&c->tile_empty[r.i]), 0));
   r.next(TILE_RING);
-  if (t >= c->seg[1] && !wait_routed_ready(c, p.status)) return -1;
+  if (t >= c->seg[2] && !wait_routed_ready(c, p.status)) return -1;
   return t;
 }
 
@@ -898,12 +898,10 @@ __device__ void pair_epilogue(PairCtrl* c, const PairParams& p, uint32_t tmem, i
     if (lane == 0) mbar_arrive_remote(map_to_rank(smem_u32(&c->tempty[acc]), 0));
     if (gemm1 && p.phases == 3) {
       // publish this warp's part of the tile: the lanes' stores, then one
-      // release increment of the group's counter.  The counters are zeroed by
-      // the preceding grid, so the increment waits for the routed tables
-      // (built after that grid completed).
+      // release increment of the group's counter (zero since the call began)
       __threadfence();
       __syncwarp();
-      if (lane == 0 && wait_routed_ready(c, p.status)) red_release_gpu_add(p.done + t.g, 1);
+      if (lane == 0) red_release_gpu_add(p.done + t.g, 1);
     }
   }
 }
@@ -943,6 +941,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FP8 ? THREADS_FP8 : 
     c->routed_ready = 0;
     c->seg[0] = 0;
     c->seg[1] = (p.phases & 1) && p.shared_rows > 0 ? pair_group_tiles(p, C1S, p.shared_rows) : 0;
+    c->seg[2] = c->seg[1] + ((p.phases & 2) && p.shared_rows > 0 ? pair_group_tiles(p, C2S, p.shared_rows) : 0);
     fence_mbar_init();
     pdl_launch_dependents();
   }

@@ -134,8 +134,8 @@ struct PairClass {
 // shared}; GEMM1 outputs bf16 silu(W1 x) * (W3 x) (W = packed W1/W3 rows,
 // 16-row interleave), GEMM2 fp32.  phases: 1 = GEMM1 tiles, 2 = GEMM2 tiles,
 // 3 = both in one launch, GEMM2 tiles of a group waiting on per-group GEMM1
-// completion counters done [num_routed + 1], which must then be zero when the
-// launch starts.  ticket: the launch's tile ticket counter, zero when the
+// completion counters done [num_routed + 1], which must then be zero before
+// anything of the call that launches it starts (the kernel may start early).  ticket: the launch's tile ticket counter, zero when the
 // launch starts (and not touched by anything that may still run then).
 // max_group_rows: an upper bound of any group's rows (the batch size T).  The
 // shared expert's GEMM1 tiles may run before the preceding grid completes.
@@ -200,12 +200,11 @@ cudaError_t launch_topk(const moe_config& c, const float* logits, int nsplit, lo
 // ---------------------------------------------------------------- permutation
 int permute_chunks(int T);
 int permute_launches(int T);   // kernels of steps 1-3 (the gather is one more)
-// zero [n_zero] (nullable): counters the gather kernel clears for the expert
-// GEMMs that follow it.
+// x or x_perm null: the dispatch tables only (no gather).
 cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* idx, int32_t* counts,
                            int32_t* offsets, int32_t* row2tok, int32_t* tok2row, void* x_perm,
                            int32_t* chunk_counts, int32_t* chunk_base, int* status, cudaStream_t s,
-                           int* launches, int* zero = nullptr, int n_zero = 0);
+                           int* launches);
 
 // x rows [T, row_bytes] -> x_perm rows tok2row[t][j] (rows < `rows`; -1 skipped).
 cudaError_t launch_gather_rows(const void* x, const int32_t* tok2row, int T, int k, long long rows, size_t row_bytes,

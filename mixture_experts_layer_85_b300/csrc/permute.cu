@@ -238,11 +238,9 @@ constexpr int GATHER_CHUNK = 8;   // 16-byte vectors per lane per chunk
 __global__ void __launch_bounds__(256) gather_tokens_kernel(const uint4* __restrict__ x,
                                                             const int32_t* __restrict__ tok2row, int T, int k,
                                                             long long R, int vec_per_row, uint4* __restrict__ x_perm,
-                                                            int* status, int* zero, int n_zero) {
+                                                            int* status) {
   pdl_launch_dependents();
   pdl_wait();
-  if (blockIdx.x == 0)
-    for (int i = threadIdx.x; i < n_zero; i += blockDim.x) zero[i] = 0;
   const int lane = threadIdx.x & 31;
   const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
   for (long long t = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < T; t += warps) {
@@ -282,8 +280,7 @@ cudaError_t launch_gather_rows(const void* x, const int32_t* tok2row, int T, int
   const long long cap = 8LL * num_sms();
   if (blocks > cap) blocks = cap;
   cudaError_t e = launch_pdl(gather_tokens_kernel, dim3((int)blocks), dim3(256), 0, s, static_cast<const uint4*>(x),
-                             tok2row, T, k, rows, int(row_bytes / 16), static_cast<uint4*>(x_perm), status,
-                             static_cast<int*>(nullptr), 0);
+                             tok2row, T, k, rows, int(row_bytes / 16), static_cast<uint4*>(x_perm), status);
   if (launches) ++*launches;
   return e;
 }
@@ -294,7 +291,7 @@ int permute_launches(int T) { return T <= SMALL_T ? 1 : 4; }
 cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* idx, int32_t* counts,
                            int32_t* offsets, int32_t* row2tok, int32_t* tok2row, void* x_perm,
                            int32_t* chunk_counts, int32_t* chunk_base, int* status, cudaStream_t s,
-                           int* launches, int* zero, int n_zero) {
+                           int* launches) {
   const int nch = permute_chunks(c.T);
   if (c.T <= SMALL_T) {
     cudaError_t e = launch_pdl(permute_small_kernel, dim3(1), dim3(SMALL_BLOCK), 0, s, idx, c.T, c.E, c.k, counts,
@@ -321,7 +318,7 @@ cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* id
   const long long cap = 8LL * num_sms();
   if (blocks > cap) blocks = cap;
   cudaError_t e = launch_pdl(gather_tokens_kernel, dim3((int)blocks), dim3(256), 0, s, static_cast<const uint4*>(x),
-                             tok2row, c.T, c.k, R, vec, static_cast<uint4*>(x_perm), status, zero, n_zero);
+                             tok2row, c.T, c.k, R, vec, static_cast<uint4*>(x_perm), status);
   if (launches) ++*launches;
   return e;
 }

@@ -424,6 +424,14 @@ def stage_times(layer, x, out, counts, n, flush=None):
     return res
 
 
+# DRAM traffic of the expert kernel per forward (dram__bytes_read.sum + dram__bytes_write.sum over the
+# launches of one forward, one ncu pass on the full-size workload) for the workloads captured with the
+# current kernel source; the summary and the command that made it are in the named profiles/ file.
+EXPERT_TRAFFIC = {
+    "v3_prefill_t16384": (32.49e9, "profiles/expert_dram_v3_prefill_t16384.md"),
+}
+
+
 def expert_roofline(wl, cnt, expert_ms, peaks):
     """The expert kernel (the dominant one) against its roof: tensor when its
     FLOP per algorithmic byte reaches the ridge of the measured peaks, else HBM."""
@@ -440,7 +448,11 @@ def expert_roofline(wl, cnt, expert_ms, peaks):
         achieved = byts / secs / 1e9
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": round(achieved / peaks["hbm_gbs"], 4), "peak_source": peaks["source"] + " HBM copy"}
-    roof.update({"kernel": "pair_gemm_kernel (GEMM1 + SwiGLU and GEMM2)", "traffic": None,
+    traffic, source = EXPERT_TRAFFIC.get(wl.name, (None, None))
+    if traffic is not None:
+        roof["traffic_source"] = source
+        roof["traffic_over_algorithmic"] = round(traffic / byts, 3)
+    roof.update({"kernel": "pair_gemm_kernel (GEMM1 + SwiGLU and GEMM2)", "traffic": traffic,
                  "per_launch_flops": flops, "per_launch_algorithmic_bytes": byts,
                  "avg_launch_ms": round(expert_ms, 4)})
     return roof

@@ -110,7 +110,13 @@ MOE_API moe_status moe_packed_size(const moe_config* cfg, size_t* bytes);
  *   W1, W3 [E,I,d], W2 [E,d,I]; Ws1, Ws3 [I_s,d], Ws2 [d,I_s]; act_dtype.
  *   `packed` (>= moe_packed_size bytes) receives W1/W3 rows interleaved in
  *   blocks of 16 so that one GEMM tile holds matching gate and up rows, and
- *   W2 / Ws2; with expert_w_dtype = MOE_FP8_E4M3 every matrix is quantised
+ *   W2 / Ws2.  bf16: every matrix (per expert, and the shared one) is stored as
+ *   stage blocks, one per tile of 128 rows and stage of 128 columns, in
+ *   row-tile-major then stage order: each 32 KB block holds the two 64-column
+ *   halves of the stage one after the other, each 128 rows x 64 bf16 row-major,
+ *   zero past the matrix's rows or columns (so the expert kernel streams each
+ *   stage as one contiguous read).  fp32: row-major.
+ *   With expert_w_dtype = MOE_FP8_E4M3 every matrix is quantised
  *   block by block on the way and stored as the expert GEMM's shared-memory
  *   images: per tile of 128 rows (same row order), cols/128 stage blocks of
  *   17408 bytes, each the tile's 128 x 128 e4m3 values (row r at byte r*128,

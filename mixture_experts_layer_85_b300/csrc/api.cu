@@ -233,6 +233,7 @@ moe_status run_experts(const moe_config& c, const void* x_perm, const int32_t* o
   PairClass& s2 = cls[3];
   s2.W = pb + P.w2s; s2.w_rows = c.d; s2.X = hs; s2.x_rows = c.T; s2.K = int(Is);
   s2.M = c.d; s2.w_step = 0; s2.out = y_shared; s2.ld_out = c.d; s2.out_rows = c.T;
+  for (PairClass& q : cls) q.img = P.img;   // bf16 weights: contiguous stage blocks
   // upper bound of the pair tiles (256 tokens x 256 weight rows), for sizing the grid
   const long long tb_routed = R / 256 + c.E;
   const long long tb_shared = Is > 0 ? (c.T + 255) / 256 : 0;

@@ -109,6 +109,40 @@ __global__ void quantize_fp8_kernel(const __nv_bfloat16* __restrict__ src_a, con
   }
 }
 
+// bf16 weights -> stage blocks (layout in internal.h), one thread per 16-byte
+// chunk of the output: output row p of group g comes from src_a (or, with
+// src_b, from W1 / W3 interleaved in blocks of `bi` rows as in
+// interleave_w13_kernel); columns and rows past the matrix are zeros.
+__global__ void pack_bf16_stages_kernel(const uint4* __restrict__ src_a, const uint4* __restrict__ src_b, long long G,
+                                        int H, int bi, int M, int cols, int tpg, int nst, uint4* __restrict__ dst) {
+  const long long n = G * tpg * nst * (IMG_BLOCK_BYTES / 16);
+  const int vrow = cols / 8;   // 16-byte chunks of a source row
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+    const int c8 = int(i & 7);                 // chunk of the 64-column k-block row
+    const int r = int((i >> 3) & 127);         // row within the tile
+    const int kb = int((i >> 10) & 1);         // k-block within the stage
+    const long long blk = i >> 11;
+    const int st = int(blk % nst);
+    const long long t = blk / nst;
+    const int tr = int(t % tpg);
+    const long long g = t / tpg;
+    const int prow = tr * IMG_ROWS + r;
+    const int k = st * IMG_COLS + kb * 64 + c8 * 8;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (prow < M && k < cols) {
+      const uint4* row;
+      if (src_b != nullptr) {
+        const int blk2 = prow / (2 * bi), rr = prow % (2 * bi);
+        row = (rr < bi ? src_a : src_b) + (g * H + (long long)blk2 * bi + (rr % bi)) * vrow;
+      } else {
+        row = src_a + (g * M + prow) * vrow;
+      }
+      v = row[k / 8];
+    }
+    dst[i] = v;
+  }
+}
+
 __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
 
 // Expert of routed row r: the last e with offsets[e] <= r.
@@ -358,6 +392,12 @@ PackedLayout packed_layout(const moe_config& c) {
     L.w2 = take(fp8_tiled_bytes((long long)c.E * c.d, c.I));
     L.w13s = take(Is > 0 ? fp8_tiled_bytes(2 * Is, c.d) : 0);
     L.w2s = take(Is > 0 ? fp8_tiled_bytes(c.d, Is) : 0);
+  } else if (c.act_dtype == MOE_BF16) {
+    L.img = true;
+    L.w13 = take(img_bytes(c.E, 2LL * c.I, c.d));
+    L.w2 = take(img_bytes(c.E, c.d, c.I));
+    L.w13s = take(Is > 0 ? img_bytes(1, 2 * Is, c.d) : 0);
+    L.w2s = take(Is > 0 ? img_bytes(1, c.d, Is) : 0);
   } else {
     L.w13 = take(size_t(c.E) * 2 * c.I * c.d * eb);
     L.w2 = take(size_t(c.E) * c.d * c.I * eb);
@@ -395,6 +435,21 @@ cudaError_t launch_prepack(const moe_config& c, const void* W1, const void* W3, 
     if (e == cudaSuccess) e = q(W2, nullptr, 1, c.E * c.d, 1, c.I, L.w2);
     if (e == cudaSuccess && Is > 0) e = q(Ws1, Ws3, 1, int(Is), L.bis, c.d, L.w13s);
     if (e == cudaSuccess && Is > 0) e = q(Ws2, nullptr, 1, c.d, 1, int(Is), L.w2s);
+    return e;
+  }
+  if (L.img) {
+    auto pk = [&](const void* a, const void* b, long long G, int H, int bi, int M, int cols, size_t off) {
+      const long long n = G * img_tiles(M) * img_stages(cols) * (IMG_BLOCK_BYTES / 16);
+      pack_bf16_stages_kernel<<<grid_for(n), 256, 0, s>>>(static_cast<const uint4*>(a), static_cast<const uint4*>(b),
+                                                          G, H, bi, M, cols, img_tiles(M), img_stages(cols),
+                                                          reinterpret_cast<uint4*>(base + off));
+      if (launches) ++*launches;
+      return cudaGetLastError();
+    };
+    cudaError_t e = pk(W1, W3, c.E, c.I, L.bi, 2 * c.I, c.d, L.w13);
+    if (e == cudaSuccess) e = pk(W2, nullptr, c.E, c.d, 1, c.d, c.I, L.w2);
+    if (e == cudaSuccess && Is > 0) e = pk(Ws1, Ws3, 1, int(Is), L.bis, int(2 * Is), c.d, L.w13s);
+    if (e == cudaSuccess && Is > 0) e = pk(Ws2, nullptr, 1, c.d, 1, c.d, int(Is), L.w2s);
     return e;
   }
   interleave_w13_kernel<<<grid_for((long long)c.E * 2 * c.I * vec), 256, 0, s>>>(

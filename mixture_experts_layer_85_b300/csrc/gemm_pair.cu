@@ -193,6 +193,11 @@ struct PairParams {
   // else at offsets[g]; row_bound bounds every group's rows.
   const int32_t* row_base;
   long long row_bound;
+  // bf16 stage blocks (w_img): the weight map is 4-D {64, 128 rows, 2 k-blocks,
+  // blocks}; group g's row tile tr and stage s is block (g * w_tpg + tr) * w_nst + s.
+  int w_img[NCLS];
+  int w_tpg[NCLS];
+  int w_nst[NCLS];
 };
 
 struct PairCtrl {
@@ -527,7 +532,11 @@ __device__ void pair_producer(PairCtrl* c, const PairParams& p, uint8_t* stages,
       if (rank == 0) mbar_arrive_expect_tx(&c->full[stage], bytes);
       const uint32_t fb = map_to_rank(smem_u32(&c->full[stage]), 0);   // rank 0's barrier
       const int kk = t.k0 + ks * (KB_STAGE * BK);                     // first K index of the stage
-      if (!p.a_mn[cls]) {
+      if (p.w_img[cls]) {
+        // one contiguous 32 KB stage block: this CTA's 128 rows x 128 columns
+        const int tr = (routed ? t.g * p.w_tpg[cls] : 0) + t.fb * 2 + int(rank);
+        tma_load_4d_pair(sa, &p.tmW[cls], fb, 0, 0, 0, tr * p.w_nst[cls] + kk / (KB_STAGE * BK));
+      } else if (!p.a_mn[cls]) {
         tma_load_3d_pair(sa, &p.tmW[cls], fb, w_row, kk / BK);
       } else {
         const bool second = kk >= p.K1[cls];
@@ -1061,6 +1070,15 @@ cudaError_t launch_pair_experts(const PairClass cls[4], const int32_t* offsets, 
       if (g.K % 128 != 0 || g.w_rows % PM != 0 || reinterpret_cast<uintptr_t>(g.W) % 16 != 0)
         return cudaErrorInvalidValue;
       p.wimg[i] = g.W;
+    } else if (g.img) {
+      // stage blocks: groups of M rows (w_rows / M groups), K columns
+      if (g.M <= 0 || g.w_rows % g.M != 0) return cudaErrorInvalidValue;
+      p.w_img[i] = 1;
+      p.w_tpg[i] = img_tiles(g.M);
+      p.w_nst[i] = img_stages(g.K);
+      if (g.w_step != 0 && g.w_step != g.M) return cudaErrorInvalidValue;
+      const long long blocks = (g.w_rows / g.M) * (long long)p.w_tpg[i] * p.w_nst[i];
+      if (!encode_stage_block_map(&p.tmW[i], g.W, blocks)) return cudaErrorInvalidValue;
     } else if (!encode_bf16_map(&p.tmW[i], g.W, g.w_rows, g.K, PM, KB_STAGE)) {
       return cudaErrorInvalidValue;
     }

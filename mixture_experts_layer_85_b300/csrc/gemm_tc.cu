@@ -501,6 +501,19 @@ bool encode_tiled_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t col
   return true;
 }
 
+bool encode_stage_block_map(CUtensorMap* m, const void* ptr, long long blocks) {
+  auto enc = tensor_map_encoder();
+  if (enc == nullptr || blocks <= 0) return false;
+  // {64 columns, 128 rows, 2 k-blocks, blocks}: one box is one contiguous block
+  cuuint64_t dims[4] = {64u, cuuint64_t(IMG_ROWS), 2u, cuuint64_t(blocks)};
+  cuuint64_t strides[3] = {128u, cuuint64_t(IMG_ROWS) * 128u, cuuint64_t(IMG_BLOCK_BYTES)};
+  cuuint32_t box[4] = {64u, cuuint32_t(IMG_ROWS), 2u, 1u};
+  cuuint32_t es[4] = {1u, 1u, 1u, 1u};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 namespace {
 
 

@@ -99,6 +99,9 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 // (box_kblocks = 1: a plain 2-D map).  Cached by argument.
 bool encode_bf16_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, uint32_t box_rows,
                      uint32_t box_kblocks);
+// 4-D bf16 map over `blocks` stage blocks (the layout of IMG_BLOCK_BYTES
+// blocks above), one block per box, 128-byte swizzle.
+bool encode_stage_block_map(CUtensorMap* m, const void* ptr, long long blocks);
 // The same for elem_bytes 1 (bytes: FP8 weights) or 2 (bf16); the inner box
 // extent is one 128-byte row.
 bool encode_tiled_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int elem_bytes,
@@ -118,8 +121,9 @@ cudaError_t launch_grouped_gemm(int epi, const GemmClass& c0, const GemmClass* c
 // per group), X [x_rows, K] token rows (class 0: rows offsets[g] ..
 // offsets[g+1]; class 1: one group of shared_rows rows), both bf16 K-major.
 struct PairClass {
-  const void* W = nullptr;   // bf16 rows, or FP8 stage images (fp8_tiled_bytes layout)
+  const void* W = nullptr;   // bf16 rows, bf16 stage blocks (img), or FP8 stage images (fp8_tiled_bytes layout)
   int64_t w_rows = 0;
+  bool img = false;          // W holds bf16 stage blocks of groups of M rows and K columns
   const void* X = nullptr;
   int64_t x_rows = 0;
   int K = 0;               // multiple of 64
@@ -238,9 +242,22 @@ inline size_t fp8_tiled_bytes(long long rows, long long cols) {
 }
 
 // Packed expert blob layout (byte offsets, each 256-byte aligned).
+// bf16 expert weights are stored as stage blocks: per group, per tile of 128
+// output rows and per stage of 128 reduction columns, the two 64-column
+// k-blocks of the tile, each 128 rows x 64 bf16 (16 KB, rows of 128 B), so one
+// stage is 32 KB contiguous (zero-padded past the matrix's rows or columns).
+constexpr int IMG_ROWS = 128, IMG_COLS = 128;
+constexpr int IMG_BLOCK_BYTES = IMG_ROWS * IMG_COLS * 2;
+inline int img_tiles(long long rows_per_group) { return int((rows_per_group + IMG_ROWS - 1) / IMG_ROWS); }
+inline int img_stages(long long cols) { return int((cols + IMG_COLS - 1) / IMG_COLS); }
+inline size_t img_bytes(long long groups, long long rows_per_group, long long cols) {
+  return size_t(groups) * img_tiles(rows_per_group) * img_stages(cols) * IMG_BLOCK_BYTES;
+}
+
 struct PackedLayout {
   size_t w13 = 0, w2 = 0, w13s = 0, w2s = 0, total = 0;
   bool fp8 = false;
+  bool img = false;      // bf16 stage blocks (otherwise row-major, the fp32 path)
   int bi = 0, bis = 0;   // interleave block of W1/W3 rows (routed, shared)
 };
 PackedLayout packed_layout(const moe_config& c);

@@ -128,6 +128,11 @@ WORKLOADS["v3_profile_fp8_e16_t1"] = Workload(
     norm_topk=True, routed_scaling_factor=2.5, act_dtype="bf16", gate_w_dtype="bf16", bias="zipf",
     expert_w_dtype="fp8")
 
+# A V3-shaped decode step (one token, top-8) over 16 experts with bf16 weights
+# (1.4 GB): the profiler's case for the decode-sized expert kernel.
+WORKLOADS["v3_profile_e16_t1"] = replace(WORKLOADS["v3_profile_fp8_e16_t1"], name="v3_profile_e16_t1",
+                                         expert_w_dtype="act")
+
 # The V3 prefill layer's routing at full size (T=16384, d=7168, 256 experts,
 # top-8, the same gate weights and bias) with the expert hidden size cut to 128:
 # the router, dispatch, gather and combine kernels see exactly the prefill

@@ -39,6 +39,9 @@ SMALL = {
     # tensor-core gate path with bf16 gate weights, ragged last tile
     "v3_small_t1100": inputs.small_workload(W["v3_prefill_t16384"], name="v3_small_t1100", T=1100, d=512,
                                             E=64, I=128, n_group=8, topk_group=4),
+    # d not a multiple of 128: zero-padded weight stages and row tiles that end inside a pair tile
+    "v3_small_d320_t97": inputs.small_workload(W["v3_prefill_t16384"], name="v3_small_d320_t97", T=97, d=320, E=32,
+                                               I=128, n_group=8, topk_group=4),
     # decode-sized batches
     "v3_small_t1": inputs.small_workload(W["v3_prefill_t16384"], name="v3_small_t1", T=1, d=512, E=64, I=256,
                                          n_group=8, topk_group=4),

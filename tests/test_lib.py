@@ -164,3 +164,23 @@ def test_debug_inject_validates_knobs():
     assert _lib.raw_call("moe_debug_inject", _lib.MOE_DEBUG_WAIT_LIMIT_NS, 1000000) == _lib.MOE_OK
     assert _lib.raw_call("moe_debug_inject", _lib.MOE_DEBUG_WAIT_LIMIT_NS, 0) == _lib.MOE_OK
     assert _lib.raw_call("moe_debug_inject", _lib.MOE_DEBUG_STALL_GEMM2, 0) == _lib.MOE_OK
+
+
+@pytest.mark.parametrize("d,I,E,n_shared", [(320, 128, 12, 1), (2048, 1408, 64, 2), (7168, 2048, 256, 1)])
+def test_bf16_packed_size_is_the_stage_block_layout(d, I, E, n_shared):
+    """bf16 packed experts: each matrix as groups x ceil(rows / 128) x ceil(cols / 128)
+    blocks of 128 x 128 bf16 (32 KB), each matrix 256-byte aligned."""
+    wl = inputs.small_workload(inputs.WORKLOADS["v3_prefill_t16384"], name="pk", T=8, d=d, E=E, I=I,
+                               n_shared=n_shared, n_group=4, topk_group=2, k=4)
+    cfg = _lib.make_config(wl)
+    blk = 128 * 128 * 2
+
+    def mat(groups, rows, cols):
+        return groups * -(-rows // 128) * -(-cols // 128) * blk
+
+    Is = n_shared * I
+    parts = [mat(E, 2 * I, d), mat(E, d, I), mat(1, 2 * Is, d), mat(1, d, Is)]
+    total = 0
+    for part in parts:
+        total = -(-(total + part) // 256) * 256
+    assert _lib.moe_packed_size(cfg) == total

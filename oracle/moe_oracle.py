@@ -536,14 +536,30 @@ def gate_backward(dg: np.ndarray, s: np.ndarray, idx: np.ndarray, cfg: OracleCon
     return s * (ds - np.sum(ds * s, axis=1, keepdims=True))
 
 
+def expert_backward(x, dout, idx, gates, e: int, w1e, w3e, w2e):
+    """Expert e's share of the gradient of L = <dout, out> (step 10): its rows
+    are the (token, slot) pairs with idx[t,j] = e, whose outputs enter out_t
+    with weight g_{t,j}.  Returns (tokens, slots, dL/dg for those slots, the
+    rows' dL/dx [n,d], dW1 [h,d], dW3 [h,d], dW2 [d,h])."""
+    x = np.asarray(x, np.float64)
+    dout = np.asarray(dout, np.float64)
+    tok, slot = np.nonzero(np.asarray(idx) == e)
+    y = swiglu_ffn(x[tok], w1e, w3e, w2e)                # expert output rows
+    dg = np.sum(dout[tok] * y, axis=1)                   # d L / d g_{t,j}
+    dy = np.asarray(gates, np.float64)[tok, slot][:, None] * dout[tok]
+    du, g1, g3, g2 = swiglu_backward(x[tok], w1e, w3e, w2e, dy)
+    return tok, slot, dg, du, g1, g3, g2
+
+
 def moe_backward(x, wg, bias, w1, w3, w2, shared, dout, cfg: OracleConfig,
-                 idx_override: Optional[np.ndarray] = None):
+                 idx_override: Optional[np.ndarray] = None, weight_grads: bool = True):
     """Gradient of L = <dout, out> for the layer of ``moe_forward`` (step 10).
 
-    w1, w3 [E,I,d] and w2 [E,d,I] are the routed experts, ``shared`` the
-    shared expert's (W1, W3, W2) or None.  Returns a dict with dx [T,d],
-    dwg [E,d], dw1, dw3, dw2 (stacked like the weights) and dws1, dws3, dws2,
-    plus the Routing used."""
+    w1, w3 [E,I,d] and w2 [E,d,I] are the routed experts (anything that
+    yields expert e's matrix as w[e]), ``shared`` the shared expert's
+    (W1, W3, W2) or None.  Returns a dict with dx [T,d], dwg [E,d], dw1, dw3,
+    dw2 (stacked like the weights; None when ``weight_grads`` is False) and
+    dws1, dws3, dws2, plus the Routing used."""
     x = np.asarray(x, np.float64)
     wg = np.asarray(wg, np.float64)
     dout = np.asarray(dout, np.float64)
@@ -553,29 +569,23 @@ def moe_backward(x, wg, bias, w1, w3, w2, shared, dout, cfg: OracleConfig,
     r = route(logits, bias, cfg)
     idx = r.idx if idx_override is None else np.asarray(idx_override, np.int64)
     s = r.scores
-    rows = np.arange(T)[:, None]
-    raw = s[rows, idx]                                   # [T,k] unbiased affinities of the choice
-    ssum = raw.sum(axis=1, keepdims=True)
-    c = float(cfg.routed_scaling_factor)
-    gates = c * (raw / ssum if cfg.norm_topk else raw)
+    gates = gate_values(s, idx, cfg)
 
     dx = np.zeros((T, d), np.float64)
-    dw1 = np.zeros(np.shape(w1), np.float64)
-    dw3 = np.zeros(np.shape(w3), np.float64)
-    dw2 = np.zeros(np.shape(w2), np.float64)
+    dw1 = np.zeros(np.shape(w1), np.float64) if weight_grads else None
+    dw3 = np.zeros(np.shape(w3), np.float64) if weight_grads else None
+    dw2 = np.zeros(np.shape(w2), np.float64) if weight_grads else None
     dg = np.zeros((T, k), np.float64)
     for e in range(E):
-        tok, slot = np.nonzero(idx == e)
-        if tok.size == 0:
+        if not (idx == e).any():
             continue
-        y = swiglu_ffn(x[tok], w1[e], w3[e], w2[e])       # expert output rows
-        dg[tok, slot] = np.sum(dout[tok] * y, axis=1)     # d L / d g_{t,j}
-        dy = gates[tok, slot][:, None] * dout[tok]
-        du, g1, g3, g2 = swiglu_backward(x[tok], w1[e], w3[e], w2[e], dy)
+        tok, slot, dg_e, du, g1, g3, g2 = expert_backward(x, dout, idx, gates, e, w1[e], w3[e], w2[e])
+        dg[tok, slot] = dg_e
         np.add.at(dx, tok, du)
-        dw1[e] += g1
-        dw3[e] += g3
-        dw2[e] += g2
+        if weight_grads:
+            dw1[e] += g1
+            dw3[e] += g3
+            dw2[e] += g2
     out = {"dw1": dw1, "dw3": dw3, "dw2": dw2, "dws1": None, "dws3": None, "dws2": None}
     if shared is not None:
         du, g1, g3, g2 = swiglu_backward(x, *shared, dout)

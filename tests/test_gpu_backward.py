@@ -116,3 +116,75 @@ def test_backward_matches_oracle(name):
         assert a <= TOL_FRO, (key, a)
         if key not in ("dw1", "dw3", "dw2"):
             assert b <= TOL_MAX, (key, b)
+
+
+class _PerExpert:
+    """w[e] of a device tensor as float64 numpy, fetched when asked for."""
+
+    def __init__(self, t):
+        self.t = t
+
+    def __getitem__(self, e):
+        return f64(self.t[e])
+
+
+def test_backward_full_size_sampled():
+    """V3 prefill at full size (T=16384, E=256, d=7168, I=2048, top-8): every
+    gradient the oracle can form from part of the batch.  dx of sampled tokens
+    depends on those tokens alone; a routed expert's weight gradients are sums
+    over the rows routed to it (the most loaded expert, the least loaded one
+    with rows, and a row count that is not a multiple of 128); the shared
+    expert's are sums over every token (one fp64 pass over the batch).  Experts
+    without rows must get exact zeros, and no gradient may hold a NaN.  dW_g
+    sums dL/dlogits of every token, which needs every expert output of the
+    batch in fp64: it is compared at the reduced sizes above, including the V3
+    expert shape."""
+    wl = W["v3_prefill_t16384"]
+    li, dout, outs, gidx = _run(wl)
+    cfg = oracle_cfg(wl)
+    bias = None if li.bias is None else li.bias.float().cpu().numpy()
+    x = f64(li.x)
+    r = orc.route(orc.gate_logits(x, f64(li.wg)), bias, cfg)
+    same = (np.sort(gidx, 1) == np.sort(r.idx, 1)).all(1)
+    assert (same | r.near_tie).all(), "expert sets differ on non-tie tokens"
+    for t in np.nonzero(~same)[0]:
+        assert orc.is_valid_selection(gidx[t], r.sel32[t], cfg), t
+    for key in ("dx", "dwg", "dw1", "dw3", "dw2", "dws1", "dws3", "dws2"):
+        assert not torch.isnan(outs[key]).any(), key
+    counts = np.bincount(gidx.ravel(), minlength=wl.E)
+    unused = torch.from_numpy(counts == 0).cuda()
+    for key in ("dw1", "dw3", "dw2"):
+        assert not outs[key][unused].any(), key
+
+    def fro(got, want):
+        return float(np.linalg.norm(got - want) / max(np.linalg.norm(want), 1e-300))
+
+    errs = {}
+    dout64 = f64(dout)
+    # dx of sampled tokens (token-local: their own experts and router row)
+    sample = np.sort(np.random.default_rng(11).choice(wl.T, 8, replace=False))
+    ref = orc.moe_backward(x[sample], f64(li.wg), bias, _PerExpert(li.w1), _PerExpert(li.w3), _PerExpert(li.w2),
+                           (f64(li.ws1), f64(li.ws3), f64(li.ws2)), dout64[sample], cfg,
+                           idx_override=gidx[sample], weight_grads=False)
+    got = f64(outs["dx"][torch.from_numpy(sample).cuda()])
+    errs["dx"] = (fro(got, ref["dx"]), orc.relative_error(got, ref["dx"]))
+    # routed experts' weight gradients over all their rows
+    used = np.nonzero(counts)[0]
+    ragged = [e for e in used if counts[e] % 128 != 0]
+    picks = sorted({int(used[np.argmax(counts[used])]), int(used[np.argmin(counts[used])]), int(ragged[0])})
+    gates = orc.gate_values(r.scores, gidx, cfg)
+    for e in picks:
+        _, _, _, _, g1, g3, g2 = orc.expert_backward(x, dout64, gidx, gates, e, f64(li.w1[e]), f64(li.w3[e]),
+                                                     f64(li.w2[e]))
+        for key, want in (("dw1", g1), ("dw3", g3), ("dw2", g2)):
+            errs[f"{key}[{e}] ({counts[e]} rows)"] = (fro(f64(outs[key][e]), want), None)
+    # the shared expert over the whole batch
+    _, g1, g3, g2 = orc.swiglu_backward(x, f64(li.ws1), f64(li.ws3), f64(li.ws2), dout64)
+    for key, want in (("dws1", g1), ("dws3", g3), ("dws2", g2)):
+        got = f64(outs[key])
+        errs[key] = (fro(got, want), orc.relative_error(got, want))
+    print({k: f"fro {a:.1e}" + ("" if b is None else f" max {b:.1e}") for k, (a, b) in errs.items()})
+    for key, (a, b) in errs.items():
+        assert a <= TOL_FRO, (key, a)
+        if b is not None:
+            assert b <= TOL_MAX, (key, b)

@@ -74,3 +74,28 @@ def test_near_tie_flag():
     assert r.near_tie.tolist() == [True, False]
     assert orc.is_valid_selection([0], r.sel32[0], cfg) and orc.is_valid_selection([1], r.sel32[0], cfg)
     assert not orc.is_valid_selection([0], r.sel32[1], cfg)
+
+
+def test_backward_parts_agree_with_the_whole():
+    """The partial forms the full-size GPU test uses: dx without the weight
+    gradients, and one expert's gradients from its own rows, equal the full
+    backward's (same arithmetic, bit for bit)."""
+    wl = inputs.small_workload(inputs.WORKLOADS["v3_prefill_t16384"], name="v3_parts", T=19, d=32, E=16, I=8,
+                               n_group=4, topk_group=2)
+    li = inputs.make_inputs(wl, "cpu")
+    cfg = oracle_cfg(wl)
+    f = lambda t: t.double().numpy()
+    bias = li.bias.float().numpy()
+    shared = (f(li.ws1), f(li.ws3), f(li.ws2))
+    dout = np.random.default_rng(3).standard_normal((wl.T, wl.d))
+    full = orc.moe_backward(f(li.x), f(li.wg), bias, f(li.w1), f(li.w3), f(li.w2), shared, dout, cfg)
+    part = orc.moe_backward(f(li.x), f(li.wg), bias, f(li.w1), f(li.w3), f(li.w2), shared, dout, cfg,
+                            weight_grads=False)
+    assert part["dw1"] is None and np.array_equal(part["dx"], full["dx"])
+    r = full["routing"]
+    gates = orc.gate_values(r.scores, r.idx, cfg)
+    for e in np.unique(r.idx):
+        _, _, _, _, g1, g3, g2 = orc.expert_backward(f(li.x), dout, r.idx, gates, int(e), f(li.w1)[e],
+                                                     f(li.w3)[e], f(li.w2)[e])
+        assert np.array_equal(g1, full["dw1"][e]) and np.array_equal(g3, full["dw3"][e])
+        assert np.array_equal(g2, full["dw2"][e])

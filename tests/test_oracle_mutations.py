@@ -167,6 +167,18 @@ def _swiglu_backward_dw2_from_gate(u, w1, w3, w2, dy):
     return du, g1, g3, np.asarray(dy, np.float64).T @ orc.silu(a)
 
 
+def _expert_backward_ungated(x, dout, idx, gates, e, w1e, w3e, w2e):
+    # the expert's rows back-propagate dout itself, not g * dout
+    return _ORIG_EXPERT_BACKWARD(x, dout, idx, np.ones_like(np.asarray(gates, np.float64)), e, w1e, w3e, w2e)
+
+
+def _expert_backward_dg_unsummed(x, dout, idx, gates, e, w1e, w3e, w2e):
+    tok, slot, dg, du, g1, g3, g2 = _ORIG_EXPERT_BACKWARD(x, dout, idx, gates, e, w1e, w3e, w2e)
+    # dL/dg from the first output column only instead of <dout_t, y_t>
+    y = orc.swiglu_ffn(np.asarray(x, np.float64)[tok], w1e, w3e, w2e)
+    return tok, slot, np.asarray(dout, np.float64)[tok, 0] * y[:, 0], du, g1, g3, g2
+
+
 def _valid_selection_variant(old_threshold=False, group_tol_sign=1.0, require_groups=True, expert_tol_sign=1.0):
     """is_valid_selection with one planted mistake (flags name it)."""
     from itertools import combinations
@@ -274,6 +286,7 @@ def _rel_err_no_sqrt(got, ref):
 
 _ORIG_SWIGLU_BACKWARD = orc.swiglu_backward
 _ORIG_GATE_BACKWARD = orc.gate_backward
+_ORIG_EXPERT_BACKWARD = orc.expert_backward
 
 
 MUTANTS = [
@@ -299,6 +312,8 @@ MUTANTS = [
     ("gate_backward", _gate_backward_no_renorm_term, pins.pin_backward_finite_differences),
     ("gate_backward", _gate_backward_softmax_diag, pins.pin_backward_finite_differences),
     ("swiglu_backward", _swiglu_backward_dw2_from_gate, pins.pin_backward_homogeneity),
+    ("expert_backward", _expert_backward_ungated, pins.pin_backward_finite_differences),
+    ("expert_backward", _expert_backward_dg_unsummed, pins.pin_backward_finite_differences),
     ("gate_backward", _gate_backward_no_renorm_term, pins.pin_backward_homogeneity),
     ("is_valid_selection", _valid_old_threshold_rule, pins.pin_valid_selection_brute_force),
     ("is_valid_selection", _valid_group_tol_reversed, pins.pin_valid_selection_brute_force),

@@ -61,7 +61,8 @@ typedef enum moe_status {
   MOE_ERR_WORKSPACE = 3,       /* ws or packed buffer smaller than required      */
   MOE_ERR_CUDA = 4,            /* a CUDA runtime call or kernel launch failed    */
   MOE_ERR_DEVICE_TIMEOUT = 5,  /* a device-side wait gave up (status word)       */
-  MOE_ERR_DEVICE_BOUNDS = 6    /* a device-side index was out of range           */
+  MOE_ERR_DEVICE_BOUNDS = 6,   /* a device-side index was out of range           */
+  MOE_ERR_DEVICE_RANGE = 7     /* FP8 layer: an activation beyond f16 range      */
 } moe_status;
 
 typedef enum moe_dtype { MOE_F32 = 0, MOE_BF16 = 1, MOE_FP8_E4M3 = 2 } moe_dtype;
@@ -95,8 +96,19 @@ typedef struct moe_config {
                               e4m3 values with one power-of-two scale per 64
                               consecutive weights of a row (intelliparadigm.com
                               page section 4, block quantisation; d and I
-                              multiples of 128).  The GEMMs dequantize to bf16
-                              exactly and multiply on the bf16 tensor cores. */
+                              multiples of 128).  The GEMMs dequantize on the
+                              fly and multiply on the f16 tensor cores, as the
+                              page's fp8 matmul does: each weight enters as
+                              e4m3 x 2^(e - e_ref), exact in f16 whenever its
+                              block's exponent e is within 15 of the largest
+                              one of its matrix (e_ref), and the product is
+                              scaled by 2^e_ref in fp32.  Token rows and the
+                              SwiGLU hidden rows enter as f16 (the bf16 x is
+                              exact in f16 between 2^-14 and 65504; smaller
+                              values round to multiples of 2^-24, larger ones
+                              set MOE_ERR_DEVICE_RANGE); the shared expert's
+                              first GEMM reads x as bf16 and dequantizes its
+                              weights to bf16 (exact). */
 } moe_config;
 
 /* Bytes of workspace every compute call needs for `cfg`. */
@@ -120,9 +132,14 @@ MOE_API moe_status moe_packed_size(const moe_config* cfg, size_t* bytes);
  *   block by block on the way and stored as the expert GEMM's shared-memory
  *   images: per tile of 128 rows (same row order), cols/128 stage blocks of
  *   17408 bytes, each the tile's 128 x 128 e4m3 values (row r at byte r*128,
- *   its 16-byte chunk c at chunk position c ^ (r % 8)) followed by their fp32
- *   scales [2][128] (64-value block h of row r at [h][r]); a zero tile
- *   follows each matrix's last row.  FP8 needs d and I multiples of 128.
+ *   its 16-byte chunk c at chunk position c ^ (r % 8)) followed by their
+ *   int32 scale exponents [2][128] (64-value block h of row r at [h][r]; the
+ *   block's scale is 2^e); a zero tile follows each matrix's last row.  After
+ *   the four matrices, int32 e_ref [E+1][3]: for each expert (the shared one
+ *   last) the exponent its W1's, W3's and W2's largest |w| gets by the block
+ *   rule (the largest exponent among the matrix's nonzero blocks; 0 for a
+ *   zero matrix).  FP8 needs d and I
+ *   multiples of 128.
  *   Inputs may be freed once the stream reaches this call. */
 MOE_API moe_status moe_prepack_experts(const moe_config* cfg, const void* W1, const void* W3, const void* W2,
                                const void* Ws1, const void* Ws3, const void* Ws2,
@@ -254,7 +271,8 @@ MOE_API moe_status moe_balance_update(const moe_config* cfg, const int32_t* coun
                                       float* stats, int32_t* device_status, void* stream);
 
 /* Synchronises `stream`, reads the device status word of `ws` and returns
- * MOE_OK, MOE_ERR_DEVICE_TIMEOUT or MOE_ERR_DEVICE_BOUNDS.  `detail` (nullable)
+ * MOE_OK, MOE_ERR_DEVICE_TIMEOUT, MOE_ERR_DEVICE_BOUNDS or
+ * MOE_ERR_DEVICE_RANGE (in that order of precedence).  `detail` (nullable)
  * receives the raw word. */
 MOE_API moe_status moe_get_device_status(const void* ws, void* stream, int32_t* detail);
 

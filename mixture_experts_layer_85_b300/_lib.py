@@ -21,7 +21,7 @@ if not os.path.exists(LIB_PATH):
 _lib = ctypes.CDLL(LIB_PATH)
 
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE, MOE_ERR_CUDA, \
-    MOE_ERR_DEVICE_TIMEOUT, MOE_ERR_DEVICE_BOUNDS = range(7)
+    MOE_ERR_DEVICE_TIMEOUT, MOE_ERR_DEVICE_BOUNDS, MOE_ERR_DEVICE_RANGE = range(8)
 MOE_F32, MOE_BF16, MOE_FP8_E4M3 = 0, 1, 2
 MOE_SCORE_SOFTMAX, MOE_SCORE_SIGMOID = 0, 1
 MOE_TOPK_GREEDY, MOE_TOPK_GROUP_LIMITED = 0, 1

@@ -218,8 +218,9 @@ moe_status run_experts(const moe_config& c, const void* x_perm, const int32_t* o
   void* hs = ws.at<void>(ws.L.hs);
   int* done = ws.at<int>(ws.L.done);   // cleared with the status word
   PairClass cls[4];
-  // GEMM1 + SwiGLU: H[rows, I] = silu(X W1^T) * (X W3^T), packed W1/W3 rows [2I, d] per expert
-  const bool fp8 = P.fp8;
+  // GEMM1 + SwiGLU: H[rows, I] = silu(X W1^T) * (X W3^T), packed W1/W3 rows [2I, d] per expert.
+  // FP8 weights: x_perm and H hold f16 rows (see launch_pair_experts).
+  const int32_t* eref = P.fp8 ? reinterpret_cast<const int32_t*>(pb + P.eref) : nullptr;
   PairClass& r1 = cls[0];
   r1.W = pb + P.w13; r1.w_rows = 2LL * c.E * c.I; r1.X = x_perm; r1.x_rows = R; r1.K = c.d;
   r1.M = 2 * c.I; r1.w_step = 2 * c.I; r1.out = h; r1.ld_out = c.I; r1.out_rows = R;
@@ -244,13 +245,13 @@ moe_status run_experts(const moe_config& c, const void* x_perm, const int32_t* o
   if (fuse_expert_gemms(c)) {
     // one launch: GEMM2 tiles start expert by expert while GEMM1 finishes
     return cuda_status(launch_pair_experts(cls, offsets, c.E, shared_rows, c.T, 3, done, tickets + kTicketFirst,
-                                           ws.status(), tiles1 + tiles2, s, launches, fp8));
+                                           ws.status(), tiles1 + tiles2, s, launches, eref));
   }
   cudaError_t e = launch_pair_experts(cls, offsets, c.E, shared_rows, c.T, 1, nullptr, tickets + kTicketFirst,
-                                      ws.status(), tiles1, s, launches, fp8);
+                                      ws.status(), tiles1, s, launches, eref);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   return cuda_status(launch_pair_experts(cls, offsets, c.E, shared_rows, c.T, 2, nullptr, tickets + kTicketSecond,
-                                         ws.status(), tiles2, s, launches, fp8));
+                                         ws.status(), tiles2, s, launches, eref));
 }
 
 }  // namespace
@@ -353,6 +354,15 @@ moe_status moe_grouped_swiglu(const moe_config* cfg, const void* x_perm, const i
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if ((st = reset_status(W, s, c.E)) != MOE_OK) return st;
   int n = 0;
+  if (c.expert_w_dtype == MOE_FP8_E4M3) {
+    // the FP8 expert GEMM takes f16 token rows: convert into the workspace's x_perm
+    void* x16 = W.at<void>(W.L.x_perm);
+    if (launch_bf16_to_f16(x_perm, x16, (long long)c.T * c.k * c.d, W.status(), s, &n) != cudaSuccess) {
+      count_launches(n);
+      return MOE_ERR_CUDA;
+    }
+    x_perm = x16;
+  }
   st = run_experts(c, x_perm, offsets, x, packed, y_perm, y_shared, W, s, &n);
   count_launches(n);
   return st;
@@ -407,7 +417,8 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const void* Wg, con
   if (st == MOE_OK) {
     profile_mark(s);
     cudaError_t e = launch_permute(c, x, idx, counts, offsets, W.at<int32_t>(W.L.row2tok), tok2row, x_perm,
-                                   W.at<int32_t>(W.L.chunk_counts), W.at<int32_t>(W.L.chunk_base), W.status(), s, &n);
+                                   W.at<int32_t>(W.L.chunk_counts), W.at<int32_t>(W.L.chunk_base), W.status(), s, &n,
+                                   c.expert_w_dtype == MOE_FP8_E4M3);
     st = cuda_status(e);
   }
   if (st == MOE_OK) {
@@ -543,6 +554,7 @@ moe_status moe_get_device_status(const void* ws, void* stream, int32_t* detail) 
   if (detail) *detail = word;
   if (word & DEV_TIMEOUT) return MOE_ERR_DEVICE_TIMEOUT;
   if (word & (DEV_BAD_EXPERT | DEV_BAD_ROW)) return MOE_ERR_DEVICE_BOUNDS;
+  if (word & DEV_RANGE) return MOE_ERR_DEVICE_RANGE;
   return MOE_OK;
 }
 
@@ -555,6 +567,7 @@ const char* moe_status_string(moe_status s) {
     case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
     case MOE_ERR_DEVICE_TIMEOUT: return "MOE_ERR_DEVICE_TIMEOUT";
     case MOE_ERR_DEVICE_BOUNDS: return "MOE_ERR_DEVICE_BOUNDS";
+    case MOE_ERR_DEVICE_RANGE: return "MOE_ERR_DEVICE_RANGE";
   }
   return "MOE_ERR_UNKNOWN";
 }

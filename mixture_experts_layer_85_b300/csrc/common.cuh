@@ -13,6 +13,7 @@ enum DevStatusBits : int {
   DEV_TIMEOUT = 1,       // a bounded mbarrier wait gave up
   DEV_BAD_EXPERT = 2,    // an expert index outside [0,E)
   DEV_BAD_ROW = 4,       // a row index outside its buffer
+  DEV_RANGE = 8,         // FP8 layer: an activation beyond the f16 range of its operands
 };
 
 // Wait limit of every device-side spin (ns of %globaltimer).  A legitimate

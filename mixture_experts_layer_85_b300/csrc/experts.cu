@@ -44,8 +44,8 @@ __global__ void interleave_w13_kernel(const uint4* __restrict__ w1, const uint4*
 //   bytes [0, 16384): row r's 128 e4m3 values at r * 128, its 16-byte chunk c
 //     (values 16c .. 16c + 15 of the stage) at chunk position c ^ (r % 8)
 //     (the 128-byte swizzle);
-//   bytes [16384, 17408): fp32 scales [2][128], [h][r] for the stage's 64-value
-//     block h of row r.
+//   bytes [16384, 17408): int32 scale exponents [2][128], [h][r] for the
+//     stage's 64-value block h of row r (its scale is 2^e).
 __global__ void quantize_fp8_kernel(const __nv_bfloat16* __restrict__ src_a, const __nv_bfloat16* __restrict__ src_b,
                                     long long G, int H, int bi, int cols, uint8_t* __restrict__ dst) {
   const int nb = cols / 64, n_st = cols / 128;
@@ -105,8 +105,46 @@ __global__ void quantize_fp8_kernel(const __nv_bfloat16* __restrict__ src_a, con
       *reinterpret_cast<uint4*>(blk + r * 128 + ((c ^ (r & 7)) << 4)) =
           make_uint4(out[4 * q], out[4 * q + 1], out[4 * q + 2], out[4 * q + 3]);
     }
-    reinterpret_cast<float*>(blk + FP8_IMAGE_BYTES)[h * 128 + r] = ldexpf(1.0f, e);
+    reinterpret_cast<int32_t*>(blk + FP8_IMAGE_BYTES)[h * 128 + r] = e;
   }
+}
+
+// Largest |w| of each of G matrices of vec_per_matrix 16-byte vectors of bf16
+// (the matrix of blockIdx.y), into amax[(g0 + g) * 3 + slot] as float bits: one
+// atomicMax per block (non-negative floats order like their bit patterns).
+__global__ void __launch_bounds__(256) matrix_amax_kernel(const uint4* __restrict__ src, long long vec_per_matrix,
+                                                          int g0, int slot, uint32_t* __restrict__ amax) {
+  __shared__ float part[8];
+  const uint4* m = src + (long long)blockIdx.y * vec_per_matrix;
+  float a = 0.0f;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < vec_per_matrix;
+       i += (long long)gridDim.x * blockDim.x) {
+    const uint4 v = m[i];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int t = 0; t < 4; ++t)
+      a = fmaxf(a, fmaxf(fabsf(__uint_as_float(w[t] << 16)), fabsf(__uint_as_float(w[t] & 0xffff0000u))));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+  if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = a;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int wi = 1; wi < 8; ++wi) a = fmaxf(a, part[wi]);
+    atomicMax(&amax[(g0 + (long long)blockIdx.y) * 3 + slot], __float_as_uint(a));
+  }
+}
+
+// A matrix's reference exponent: the scale exponent its largest |w| gets by
+// the block rule above (the largest block exponent of the matrix; 0 when the
+// matrix is zero).  In place over the amax bits.
+__global__ void eref_from_amax_kernel(int32_t* eref, int n) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const float amax = __uint_as_float(uint32_t(eref[i]));
+  int x = 0;
+  const float f = frexpf(amax, &x);
+  eref[i] = amax == 0.0f ? 0 : (f <= 0.875f ? x - 9 : x - 8);
 }
 
 // bf16 weights -> stage blocks (layout in internal.h), one thread per 16-byte
@@ -392,6 +430,7 @@ PackedLayout packed_layout(const moe_config& c) {
     L.w2 = take(fp8_tiled_bytes((long long)c.E * c.d, c.I));
     L.w13s = take(Is > 0 ? fp8_tiled_bytes(2 * Is, c.d) : 0);
     L.w2s = take(Is > 0 ? fp8_tiled_bytes(c.d, Is) : 0);
+    L.eref = take(size_t(c.E + 1) * 3 * sizeof(int32_t));
   } else if (c.act_dtype == MOE_BF16) {
     L.img = true;
     L.w13 = take(img_bytes(c.E, 2LL * c.I, c.d));
@@ -431,7 +470,31 @@ cudaError_t launch_prepack(const moe_config& c, const void* W1, const void* W3, 
       if (launches) ++*launches;
       return cudaGetLastError();
     };
-    cudaError_t e = q(W1, W3, c.E, c.I, L.bi, c.d, L.w13);
+    // reference exponents: the largest |w| of every matrix, then its exponent
+    int32_t* eref = reinterpret_cast<int32_t*>(base + L.eref);
+    const int n_ref = (c.E + 1) * 3;
+    cudaError_t e = cudaMemsetAsync(eref, 0, size_t(n_ref) * sizeof(int32_t), s);
+    auto amax = [&](const void* w, long long G, long long rows, long long cols, int g0, int slot) {
+      const long long vec = rows * cols / 8;
+      long long bx = (vec + 255) / 256;
+      if (bx > 64) bx = 64;
+      matrix_amax_kernel<<<dim3(unsigned(bx), unsigned(G)), 256, 0, s>>>(static_cast<const uint4*>(w), vec, g0, slot,
+                                                                      reinterpret_cast<uint32_t*>(eref));
+      if (launches) ++*launches;
+      return cudaGetLastError();
+    };
+    if (e == cudaSuccess) e = amax(W1, c.E, c.I, c.d, 0, 0);
+    if (e == cudaSuccess) e = amax(W3, c.E, c.I, c.d, 0, 1);
+    if (e == cudaSuccess) e = amax(W2, c.E, c.d, c.I, 0, 2);
+    if (e == cudaSuccess && Is > 0) e = amax(Ws1, 1, Is, c.d, c.E, 0);
+    if (e == cudaSuccess && Is > 0) e = amax(Ws3, 1, Is, c.d, c.E, 1);
+    if (e == cudaSuccess && Is > 0) e = amax(Ws2, 1, c.d, Is, c.E, 2);
+    if (e == cudaSuccess) {
+      eref_from_amax_kernel<<<(n_ref + 255) / 256, 256, 0, s>>>(eref, n_ref);
+      if (launches) ++*launches;
+      e = cudaGetLastError();
+    }
+    if (e == cudaSuccess) e = q(W1, W3, c.E, c.I, L.bi, c.d, L.w13);
     if (e == cudaSuccess) e = q(W2, nullptr, 1, c.E * c.d, 1, c.I, L.w2);
     if (e == cudaSuccess && Is > 0) e = q(Ws1, Ws3, 1, int(Is), L.bis, c.d, L.w13s);
     if (e == cudaSuccess && Is > 0) e = q(Ws2, nullptr, 1, c.d, 1, int(Is), L.w2s);

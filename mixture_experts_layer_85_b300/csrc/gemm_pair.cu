@@ -89,8 +89,10 @@ constexpr int KB_STAGE = 2;           // k-blocks per stage and per TMA copy
 // Ring geometry.  Regular launches: 3 stages of 64 KB (weights 32 KB + tokens
 // 32 KB per CTA).  Decode-sized launches (every group at most 64 tokens, so
 // every tile uses the 32-row token box): 5 stages of 40 KB, a deeper queue of
-// weight copies for streaming-bound work.
-constexpr int MAX_STAGES = 5;
+// weight copies for streaming-bound work; at most 16 tokens (the 8-row box):
+// 6 stages of 34 KB.  A cluster streams about (weights in flight) / (DRAM
+// latency under load), so the depth of the queue sets its rate.
+constexpr int MAX_STAGES = 6;
 constexpr int THREADS = 256;
 constexpr int TABLE_WARP = 6;
 constexpr int DISPATCH_WARP = 7;
@@ -106,7 +108,11 @@ constexpr int XS_KB_BYTES = XSMALL * BK * 2;
 constexpr int XTINY = 8;                         // token rows of the tiny box (tiles of at most 16 tokens)
 constexpr int XT_KB_BYTES = XTINY * BK * 2;
 constexpr int SMALL_STAGE_BYTES = A_BYTES + KB_STAGE * XS_KB_BYTES;
-static_assert(3 * STAGE_BYTES <= RING_BYTES && MAX_STAGES * SMALL_STAGE_BYTES <= RING_BYTES, "ring");
+constexpr int TINY_STAGE_BYTES = A_BYTES + KB_STAGE * XT_KB_BYTES;
+static_assert(3 * STAGE_BYTES <= RING_BYTES && 5 * SMALL_STAGE_BYTES <= RING_BYTES &&
+                  MAX_STAGES * TINY_STAGE_BYTES <= RING_BYTES && TINY_STAGE_BYTES % 1024 == 0 &&
+                  SMALL_STAGE_BYTES % 1024 == 0,
+              "ring");
 constexpr int MAX_GROUPS = 272;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_STRIDE = 256;  // columns between the two accumulators
@@ -165,6 +171,13 @@ struct PairParams {
   int slot_bytes;           // bytes of one slot
   int x_kb_bytes;           // bytes of one k-block of the largest token box of the launch
   int a_tmem;               // FP8: the converted A operand lives in tensor memory (A_TMEM_STAGES buffers)
+  // FP8: per group the reference exponents of its W1, W3 and W2 ([num_routed
+  // + 1][3], the shared expert last), and per class whether its operands are
+  // f16 (weights dequantized relative to the reference exponent, token rows
+  // f16, accumulator scaled by 2^e_ref) or bf16 (full block scales; the
+  // shared expert's GEMM1, which reads the bf16 x).
+  const int32_t* eref;
+  int f16op[NCLS];
   uint32_t acc_stride;      // tensor-memory columns between the two accumulators
   // Limit of every bounded wait (ns of %globaltimer), and completions a GEMM2
   // tile waits for beyond its group's GEMM1 tiles (0; a positive value makes
@@ -648,6 +661,58 @@ __device__ __forceinline__ void convert_e4m3x16(const uint4 q, float scale, uint
   }
 }
 
+// 16 e4m3 values (k order) times 2^rel, rel in [-24, 0] -> 8 words of f16
+// pairs: the e4m3 -> f16 conversion is exact, and so is the product whenever
+// it is a multiple of 2^-24 (always for rel >= -15).  `fac` holds 2^rel twice.
+__device__ __forceinline__ void convert_e4m3x16_f16(const uint4 q, __half2 fac, uint32_t* o) {
+  const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __half2 lo = __hmul2(__half2(__nv_cvt_fp8x2_to_halfraw2(__nv_fp8x2_storage_t(qw[i] & 0xffffu), __NV_E4M3)),
+                               fac);
+    const __half2 hi = __hmul2(__half2(__nv_cvt_fp8x2_to_halfraw2(__nv_fp8x2_storage_t(qw[i] >> 16), __NV_E4M3)), fac);
+    o[2 * i] = *reinterpret_cast<const uint32_t*>(&lo);
+    o[2 * i + 1] = *reinterpret_cast<const uint32_t*>(&hi);
+  }
+}
+
+// 2^rel as an f16 pair (rel <= 0 clamped to 0 above; below -24 it is zero).
+__device__ __forceinline__ __half2 f16_pow2_pair(int rel) {
+  rel = min(rel, 0);
+  const unsigned short b = rel >= -14 ? (unsigned short)((rel + 15) << 10)
+                                      : (rel >= -24 ? (unsigned short)(1u << (rel + 24)) : (unsigned short)0);
+  __half_raw h;
+  h.x = b;
+  return __half2(__half(h), __half(h));
+}
+
+// Reference-exponent slot of weight row r of a CTA's 128 rows: GEMM1 rows
+// alternate 16 W1 and 16 W3 rows (tiles start on multiples of 32 rows), GEMM2
+// rows are W2's.
+__device__ __forceinline__ int eref_slot(int cls, int r) { return (cls == C1R || cls == C1S) ? ((r >> 4) & 1) : 2; }
+
+// One converter thread's part of a stage image `img`: chunks c0 .. c0 +
+// CONV_CPT - 1 (16 weights each, 64-weight block h) of weight row r, as f16
+// relative to the matrix's reference exponent or as bf16 with the full block
+// scale, into o [8 * CONV_CPT] words.
+__device__ __forceinline__ void convert_stage_part(const uint8_t* img, int h, int r, int c0, bool f16, int e_ref,
+                                                   uint32_t* o) {
+  const int e_blk = reinterpret_cast<const int32_t*>(img + FP8_IMAGE_BYTES)[h * PM + r];
+  const uint8_t* src = img + r * 128;
+  const int sw = r & 7;   // 128-byte swizzle phase of the row
+  if (f16) {
+    const __half2 fac = f16_pow2_pair(e_blk - e_ref);
+#pragma unroll
+    for (int qc = 0; qc < CONV_CPT; ++qc)
+      convert_e4m3x16_f16(*reinterpret_cast<const uint4*>(src + (((c0 + qc) ^ sw) << 4)), fac, o + 8 * qc);
+  } else {
+    const float scale = ldexpf(1.0f, e_blk);
+#pragma unroll
+    for (int qc = 0; qc < CONV_CPT; ++qc)
+      convert_e4m3x16(*reinterpret_cast<const uint4*>(src + (((c0 + qc) ^ sw) << 4)), scale, o + 8 * qc);
+  }
+}
+
 // FP8 converter warps: thread i owns 16-weight chunks (i / 128) * CONV_CPT ..
 // of weight row i % 128 of this CTA's 128 (all in one 64-weight k-block).
 // Per stage it reads those e4m3 bytes (128-byte swizzle) and the block's scale
@@ -680,6 +745,8 @@ __device__ void pair_converter(PairCtrl* c, const PairParams& p, uint8_t* stages
     if (tile < 0) break;
     const PairTile t = pair_tile(c, p, tile);
     const int nks = p.K[t.cls] / 128;
+    const bool f16 = p.f16op[t.cls] != 0;
+    const int e_ref = p.eref[t.g * 3 + eref_slot(t.cls, r)];
     for (int ks = 0; ks < nks; ++ks) {
       const int half = ks & (p.sps - 1);   // sps is 1 or 2
       int good = 1;
@@ -691,19 +758,13 @@ __device__ void pair_converter(PairCtrl* c, const PairParams& p, uint8_t* stages
         ok = false;
         break;
       }
-      const uint8_t* src = ring + size_t(slot.i) * p.slot_bytes + size_t(half) * FP8_STAGE_BYTES;
-      const float scale = reinterpret_cast<const float*>(src + FP8_IMAGE_BYTES)[h * PM + r];
-      src += r * 128;
+      const uint8_t* img = ring + size_t(slot.i) * p.slot_bytes + size_t(half) * FP8_STAGE_BYTES;
       if (p.a_tmem) {
         // the MMAs that read this A buffer completed (empty wait above)
         tc_fence_after();
         uint32_t o[16];
-#pragma unroll
-        for (int qc = 0; qc < CONV_CPT; ++qc) {
-          const uint4 q = *reinterpret_cast<const uint4*>(src + (((c0 + qc) ^ sw) << 4));
-          convert_e4m3x16(q, scale, o + 8 * qc);
-        }
-        // 32 bf16 = 16 columns at k offset 16 * c0 of the stage
+        convert_stage_part(img, h, r, c0, f16, e_ref, o);
+        // 32 values = 16 columns at k offset 16 * c0 of the stage
         tmem_st16(tmem + a_lane + A_TMEM_COL0 + uint32_t(stage.i) * 64u + uint32_t(c0) * 8u, o);
         tmem_wait_st();
         tc_fence_before();
@@ -715,17 +776,17 @@ __device__ void pair_converter(PairCtrl* c, const PairParams& p, uint8_t* stages
         continue;
       }
       uint8_t* kb = stages + size_t(stage.i) * p.stage_bytes + h * A_KB_BYTES + r * 128;
+      uint32_t o[8 * CONV_CPT];
+      convert_stage_part(img, h, r, c0, f16, e_ref, o);
 #pragma unroll
       for (int qc = 0; qc < CONV_CPT; ++qc) {
-        // e4m3 chunk c0 + qc of the stage row: weights 16 q4 .. 16 q4 + 15 of k-block h
-        const int q4 = (c0 + qc) & 3;
-        const uint4 q = *reinterpret_cast<const uint4*>(src + (((c0 + qc) ^ sw) << 4));
-        uint32_t o[8];
-        convert_e4m3x16(q, scale, o);
-        // bf16 16-byte chunks 2 q4 and 2 q4 + 1 of row r of k-block h
-        const int j = 2 * q4;
-        *reinterpret_cast<uint4*>(kb + ((j ^ sw) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-        *reinterpret_cast<uint4*>(kb + (((j + 1) ^ sw) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+        // chunk c0 + qc of the stage row (weights 16 q4 .. 16 q4 + 15 of k-block h)
+        // -> 16-byte chunks 2 q4 and 2 q4 + 1 of row r of the A buffer's k-block h
+        const int j = 2 * ((c0 + qc) & 3);
+        *reinterpret_cast<uint4*>(kb + ((j ^ sw) << 4)) =
+            make_uint4(o[8 * qc], o[8 * qc + 1], o[8 * qc + 2], o[8 * qc + 3]);
+        *reinterpret_cast<uint4*>(kb + (((j + 1) ^ sw) << 4)) =
+            make_uint4(o[8 * qc + 4], o[8 * qc + 5], o[8 * qc + 6], o[8 * qc + 7]);
       }
       // the tensor cores read the A buffer through the async proxy
       fence_proxy_async_shared();
@@ -755,7 +816,8 @@ __device__ void pair_mma(PairCtrl* c, const PairParams& p, uint8_t* stages, uint
     if (tile < 0) break;
     const PairTile t = pair_tile(c, p, tile);
     const uint32_t a_mn = FP8 ? 0u : uint32_t(p.a_mn[t.cls]), b_mn = FP8 ? 0u : uint32_t(p.b_mn[t.cls]);
-    const uint32_t idesc = idesc_bf16_f32(PAIR_M, t.n_mma) | (a_mn << 15) | (b_mn << 16);
+    const uint32_t idesc = (FP8 && p.f16op[t.cls] ? idesc_f16_f32(PAIR_M, t.n_mma) : idesc_bf16_f32(PAIR_M, t.n_mma)) |
+                           (a_mn << 15) | (b_mn << 16);
     const int acc = ctr & 1;
     if (!pair_wait(&c->tempty[acc], (uint32_t(ctr >> 1) & 1u) ^ 1u, c, peer_abort, p.status, true)) break;
     tc_fence_after();
@@ -835,6 +897,7 @@ __device__ __forceinline__ bool pair_warp_wait(uint64_t* bar, uint32_t parity, P
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
+template <bool FP8>
 __device__ void pair_epilogue(PairCtrl* c, const PairParams& p, uint32_t tmem, int warp, int lane, uint32_t rank,
                               uint32_t peer_abort) {
   const int q = warp & 3;   // the tensor-memory lane quarter this warp may read
@@ -853,16 +916,25 @@ __device__ void pair_epilogue(PairCtrl* c, const PairParams& p, uint32_t tmem, i
     const long long row0 = t.n0;
     const int ncols = (t.n_valid + 15) & ~15;
     const bool gemm1 = t.cls == C1R || t.cls == C1S;
+    // FP8 weights with f16 operands: the accumulator carries 2^-e_ref of the
+    // product (this lane's weight row's matrix)
+    const bool fp8 = FP8 && p.eref != nullptr;
+    const float acc_scale = fp8 && p.f16op[t.cls] ? ldexpf(1.0f, p.eref[t.g * 3 + eref_slot(t.cls, q * 32 + lane)])
+                                                   : 1.0f;
     if (gemm1) {
       // lane l < 16: W1 row of feature f; lane l + 16: the W3 row of the same f
       const int f = t.fb * (PAIR_M / 2) + int(rank) * (PM / 2) + q * 16 + (lane & 15);
       __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out[t.cls]) + f;
+      __half* out16 = static_cast<__half*>(p.out[t.cls]) + f;   // FP8 layers: f16 hidden rows
       const long long ld = p.ld_out[t.cls];
       const bool lo_half = lane < 16;
+      bool over = false;
 #pragma unroll 1
       for (int cc = 0; cc < ncols; cc += 16) {
         float v[16];
         tmem_ld16(tbase + cc, v);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] *= acc_scale;
         // lanes < 16 keep tokens cc..cc+7, lanes >= 16 tokens cc+8..cc+15
         float mine[8], other[8];
 #pragma unroll
@@ -876,9 +948,18 @@ __device__ void pair_epilogue(PairCtrl* c, const PairParams& p, uint32_t tmem, i
         for (int i = 0; i < 8; ++i) {
           const float g = lo_half ? mine[i] : other[i];
           const float u = lo_half ? other[i] : mine[i];
-          if (j0 + i < t.n_valid) out[(row0 + j0 + i) * ld] = __float2bfloat16_rn(silu_f(g) * u);
+          const float h = silu_f(g) * u;
+          if (j0 + i < t.n_valid) {
+            if (fp8) {
+              over |= fabsf(h) >= 65520.0f;
+              out16[(row0 + j0 + i) * ld] = __float2half_rn(h);
+            } else {
+              out[(row0 + j0 + i) * ld] = __float2bfloat16_rn(h);
+            }
+          }
         }
       }
+      if (over) flag_status(p.status, DEV_RANGE);
     } else {
       const int f = t.fb * PAIR_M + int(rank) * PM + q * 32 + lane;
       const bool fvalid = f < p.M[t.cls];
@@ -898,7 +979,7 @@ __device__ void pair_epilogue(PairCtrl* c, const PairParams& p, uint32_t tmem, i
         if (fvalid) {
 #pragma unroll
           for (int i = 0; i < 16; ++i)
-            if (cc + i < t.n_valid) out[(row0 + cc + i) * ld] = v[i];
+            if (cc + i < t.n_valid) out[(row0 + cc + i) * ld] = v[i] * acc_scale;
         }
       }
     }
@@ -982,7 +1063,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FP8 ? THREADS_FP8 : 
   } else if (warp == 1) {
     if (lane == 0 && rank == 0) pair_mma<FP8>(c, p, stages, tmem, peer_abort);
   } else if (warp < 2 + EPI_WARPS) {
-    pair_epilogue(c, p, tmem, warp, lane, rank, peer_abort);
+    pair_epilogue<FP8>(c, p, tmem, warp, lane, rank, peer_abort);
   } else if (warp >= THREADS / 32) {
     pair_converter(c, p, stages, tmem, warp, lane, peer_abort);
   } else if (warp == TABLE_WARP) {
@@ -1054,8 +1135,9 @@ void get_expert_fault(unsigned long long* wait_ns, int* need_extra) {
 
 cudaError_t launch_pair_experts(const PairClass cls[4], const int32_t* offsets, int num_routed, int shared_rows,
                                 int max_group_rows, int phases, int* done, int* ticket, int* status,
-                                long long max_tiles, cudaStream_t stream, int* launches, bool fp8) {
+                                long long max_tiles, cudaStream_t stream, int* launches, const int32_t* fp8_eref) {
   if (max_tiles <= 0) return cudaSuccess;
+  const bool fp8 = fp8_eref != nullptr;
   if (num_routed < 1 || num_routed + 1 > MAX_GROUPS || phases < 1 || phases > 3) return cudaErrorInvalidValue;
   if (ticket == nullptr) return cudaErrorInvalidValue;
   if (phases == 3 && done == nullptr) return cudaErrorInvalidValue;
@@ -1070,6 +1152,7 @@ cudaError_t launch_pair_experts(const PairClass cls[4], const int32_t* offsets, 
       if (g.K % 128 != 0 || g.w_rows % PM != 0 || reinterpret_cast<uintptr_t>(g.W) % 16 != 0)
         return cudaErrorInvalidValue;
       p.wimg[i] = g.W;
+      p.f16op[i] = i != C1S ? 1 : 0;   // the shared expert's GEMM1 reads the bf16 x
     } else if (g.img) {
       // stage blocks: groups of M rows (w_rows / M groups), K columns
       if (g.M <= 0 || g.w_rows % g.M != 0) return cudaErrorInvalidValue;
@@ -1094,6 +1177,7 @@ cudaError_t launch_pair_experts(const PairClass cls[4], const int32_t* offsets, 
     p.w_step[i] = g.w_step;
   }
   p.offsets = offsets;
+  p.eref = fp8_eref;
   p.row_bound = cls[C1R].out_rows;
   p.num_routed = num_routed;
   p.shared_rows = shared_rows;
@@ -1105,9 +1189,11 @@ cudaError_t launch_pair_experts(const PairClass cls[4], const int32_t* offsets, 
   p.wait_ns = wns > 0 ? wns : kWaitLimitNs;
   p.need_extra = phases == 3 ? g_need_extra.load() : 0;
   // A group never holds more tokens than the batch, so with at most 64 tokens
-  // every tile takes the 32-row token box: use the deeper ring of small stages.
+  // every tile takes the 32-row token box (at most 16: the 8-row box): use the
+  // deeper rings of smaller stages.
   const bool small = max_group_rows <= 2 * XSMALL;
-  p.stage_bytes = small ? SMALL_STAGE_BYTES : STAGE_BYTES;
+  const bool tiny_box = max_group_rows <= 2 * XTINY;
+  p.stage_bytes = tiny_box ? TINY_STAGE_BYTES : (small ? SMALL_STAGE_BYTES : STAGE_BYTES);
   cudaError_t e;
   if (fp8) {
     // two bf16 A buffers (written by the converters) and a ring of slots,
@@ -1130,7 +1216,7 @@ cudaError_t launch_pair_experts(const PairClass cls[4], const int32_t* offsets, 
     if (p.nf > MAX_F8) p.nf = MAX_F8;
     e = launch_pair<true>(p, max_tiles, stream);
   } else {
-    p.stages = small ? MAX_STAGES : 3;
+    p.stages = tiny_box ? MAX_STAGES : (small ? 5 : 3);
     p.acc_stride = ACC_STRIDE;
     e = launch_pair<false>(p, max_tiles, stream);
   }

@@ -143,11 +143,17 @@ struct PairClass {
 // launch starts (and not touched by anything that may still run then).
 // max_group_rows: an upper bound of any group's rows (the batch size T).  The
 // shared expert's GEMM1 tiles may run before the preceding grid completes.
-// fp8: the weights are FP8 stage images (one bulk copy per stage), dequantized
-// to bf16 in shared memory by converter warps before each MMA.
+// fp8_eref (non-null: FP8 weights): the weights are FP8 stage images (one
+// bulk copy per stage), dequantized by converter warps before each MMA, and
+// fp8_eref [num_routed + 1][3] holds each group's reference exponents of its
+// W1, W3 and W2.  The shared expert's GEMM1 (bf16 x) then dequantizes to bf16
+// with the full block scales; every other tile takes f16 token rows (x_perm as
+// f16, and the hidden rows GEMM1 writes as f16), dequantizes to f16 relative
+// to the reference exponent and scales its fp32 accumulator by 2^e_ref.
 cudaError_t launch_pair_experts(const PairClass cls[4], const int32_t* offsets, int num_routed, int shared_rows,
                                 int max_group_rows, int phases, int* done, int* ticket, int* status,
-                                long long max_tiles, cudaStream_t stream, int* launches, bool fp8 = false);
+                                long long max_tiles, cudaStream_t stream, int* launches,
+                                const int32_t* fp8_eref = nullptr);
 
 // Fault injection for tests of the device-side time-out path
 // (moe_debug_inject): the expert kernel's wait limit for later launches
@@ -204,11 +210,15 @@ cudaError_t launch_topk(const moe_config& c, const float* logits, int nsplit, lo
 // ---------------------------------------------------------------- permutation
 int permute_chunks(int T);
 int permute_launches(int T);   // kernels of steps 1-3 (the gather is one more)
-// x or x_perm null: the dispatch tables only (no gather).
+// x or x_perm null: the dispatch tables only (no gather).  x_perm_f16: bf16
+// rows of x are written to x_perm as f16 (the FP8 expert GEMM's token
+// operand); a value that rounds beyond the f16 range sets DEV_RANGE.
 cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* idx, int32_t* counts,
                            int32_t* offsets, int32_t* row2tok, int32_t* tok2row, void* x_perm,
                            int32_t* chunk_counts, int32_t* chunk_base, int* status, cudaStream_t s,
-                           int* launches);
+                           int* launches, bool x_perm_f16 = false);
+// n bf16 values (n a multiple of 8, 16-byte aligned) to f16, DEV_RANGE as above.
+cudaError_t launch_bf16_to_f16(const void* src, void* dst, long long n, int* status, cudaStream_t s, int* launches);
 
 // x rows [T, row_bytes] -> x_perm rows tok2row[t][j] (rows < `rows`; -1 skipped).
 cudaError_t launch_gather_rows(const void* x, const int32_t* tok2row, int T, int k, long long rows, size_t row_bytes,
@@ -233,8 +243,11 @@ cudaError_t launch_balance_update(const moe_config& c, const int32_t* counts, fl
 
 // FP8 expert weights are stored as the expert GEMM's shared-memory images:
 // tiles of 128 rows, each a run of cols / 128 stage blocks of FP8_STAGE_BYTES
-// (128 x 128 e4m3 values with the 128-byte swizzle, then their fp32 scales
-// [2][128]), plus one zero tile after the last row.
+// (128 x 128 e4m3 values with the 128-byte swizzle, then their int32 scale
+// exponents [2][128]), plus one zero tile after the last row.  The layout's
+// eref area holds int32 [E+1][3]: for each group's W1, W3 and W2 (the shared
+// expert at E) the exponent its largest |w| gets by the block rule (the
+// largest exponent among its nonzero blocks; 0 for a zero matrix).
 constexpr int FP8_IMAGE_BYTES = 128 * 128;
 constexpr int FP8_STAGE_BYTES = FP8_IMAGE_BYTES + 2 * 128 * 4;
 inline size_t fp8_tiled_bytes(long long rows, long long cols) {
@@ -255,7 +268,7 @@ inline size_t img_bytes(long long groups, long long rows_per_group, long long co
 }
 
 struct PackedLayout {
-  size_t w13 = 0, w2 = 0, w13s = 0, w2s = 0, total = 0;
+  size_t w13 = 0, w2 = 0, w13s = 0, w2s = 0, eref = 0, total = 0;
   bool fp8 = false;
   bool img = false;      // bf16 stage blocks (otherwise row-major, the fp32 path)
   int bi = 0, bis = 0;   // interleave block of W1/W3 rows (routed, shared)

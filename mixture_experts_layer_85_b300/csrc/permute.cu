@@ -20,6 +20,8 @@
 // (permute_small_kernel: the same masks and ranks over 1024-token chunks taken
 // in order), so the dispatch costs two launches, not five.  Its results are
 // identical to the multi-block path.
+#include <cuda_fp16.h>
+
 #include "internal.h"
 
 namespace moe {
@@ -235,13 +237,29 @@ __global__ void __launch_bounds__(SMALL_BLOCK) permute_small_kernel(const int32_
 // row once (chunks of 8 vectors per lane) and stores it k times, so x streams
 // from memory once and the k copies are plain writes.
 constexpr int GATHER_CHUNK = 8;   // 16-byte vectors per lane per chunk
+
+// Eight bf16 values to f16 (round to nearest even); `over` is set when one
+// lands beyond the f16 range (|v| >= 65520 rounds to infinity).
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v, bool& over) {
+  uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float lo = __uint_as_float(w[i] << 16), hi = __uint_as_float(w[i] & 0xffff0000u);
+    over |= fabsf(lo) >= 65520.0f || fabsf(hi) >= 65520.0f;
+    const __half2 h = __floats2half2_rn(lo, hi);
+    w[i] = *reinterpret_cast<const uint32_t*>(&h);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
 __global__ void __launch_bounds__(256) gather_tokens_kernel(const uint4* __restrict__ x,
                                                             const int32_t* __restrict__ tok2row, int T, int k,
                                                             long long R, int vec_per_row, uint4* __restrict__ x_perm,
-                                                            int* status) {
+                                                            int to_f16, int* status) {
   pdl_launch_dependents();
   pdl_wait();
   const int lane = threadIdx.x & 31;
+  bool over = false;
   const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
   for (long long t = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < T; t += warps) {
     const int32_t* rows = tok2row + t * k;
@@ -251,7 +269,7 @@ __global__ void __launch_bounds__(256) gather_tokens_kernel(const uint4* __restr
 #pragma unroll
       for (int i = 0; i < GATHER_CHUNK; ++i) {
         const int v = v0 + i * 32 + lane;
-        if (v < vec_per_row) buf[i] = src[v];
+        if (v < vec_per_row) buf[i] = to_f16 ? bf16x8_to_f16x8(src[v], over) : src[v];
       }
       for (int j = 0; j < k; ++j) {
         const long long r = rows[j];   // warp-uniform, cached after the first chunk
@@ -269,6 +287,18 @@ __global__ void __launch_bounds__(256) gather_tokens_kernel(const uint4* __restr
       }
     }
   }
+  if (over) flag_status(status, DEV_RANGE);
+}
+
+__global__ void __launch_bounds__(256) bf16_to_f16_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
+                                                          long long n_vec, int* status) {
+  // heads its call's chain: predecessors complete before dependents start
+  pdl_wait();
+  pdl_launch_dependents();
+  bool over = false;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n_vec; i += (long long)gridDim.x * blockDim.x)
+    dst[i] = bf16x8_to_f16x8(src[i], over);
+  if (over) flag_status(status, DEV_RANGE);
 }
 
 }  // namespace
@@ -280,7 +310,19 @@ cudaError_t launch_gather_rows(const void* x, const int32_t* tok2row, int T, int
   const long long cap = 8LL * num_sms();
   if (blocks > cap) blocks = cap;
   cudaError_t e = launch_pdl(gather_tokens_kernel, dim3((int)blocks), dim3(256), 0, s, static_cast<const uint4*>(x),
-                             tok2row, T, k, rows, int(row_bytes / 16), static_cast<uint4*>(x_perm), status);
+                             tok2row, T, k, rows, int(row_bytes / 16), static_cast<uint4*>(x_perm), 0, status);
+  if (launches) ++*launches;
+  return e;
+}
+
+cudaError_t launch_bf16_to_f16(const void* src, void* dst, long long n, int* status, cudaStream_t s, int* launches) {
+  if (n <= 0) return cudaSuccess;
+  const long long n_vec = n / 8;
+  long long blocks = (n_vec + 255) / 256;
+  const long long cap = 8LL * num_sms();
+  if (blocks > cap) blocks = cap;
+  cudaError_t e = launch_pdl(bf16_to_f16_kernel, dim3((int)blocks), dim3(256), 0, s, static_cast<const uint4*>(src),
+                             static_cast<uint4*>(dst), n_vec, status);
   if (launches) ++*launches;
   return e;
 }
@@ -291,7 +333,7 @@ int permute_launches(int T) { return T <= SMALL_T ? 1 : 4; }
 cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* idx, int32_t* counts,
                            int32_t* offsets, int32_t* row2tok, int32_t* tok2row, void* x_perm,
                            int32_t* chunk_counts, int32_t* chunk_base, int* status, cudaStream_t s,
-                           int* launches) {
+                           int* launches, bool x_perm_f16) {
   const int nch = permute_chunks(c.T);
   if (c.T <= SMALL_T) {
     cudaError_t e = launch_pdl(permute_small_kernel, dim3(1), dim3(SMALL_BLOCK), 0, s, idx, c.T, c.E, c.k, counts,
@@ -318,7 +360,7 @@ cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* id
   const long long cap = 8LL * num_sms();
   if (blocks > cap) blocks = cap;
   cudaError_t e = launch_pdl(gather_tokens_kernel, dim3((int)blocks), dim3(256), 0, s, static_cast<const uint4*>(x),
-                             tok2row, c.T, c.k, R, vec, static_cast<uint4*>(x_perm), status);
+                             tok2row, c.T, c.k, R, vec, static_cast<uint4*>(x_perm), x_perm_f16 ? 1 : 0, status);
   if (launches) ++*launches;
   return e;
 }

@@ -439,7 +439,7 @@ def _fp8_copy(wl):
     return inputs.small_workload(wl, name=wl.name + "_fp8", expert_w_dtype="fp8")
 
 
-FP8_STAGE = 128 * 128 + 2 * 128 * 4   # one stage image: 128 x 128 e4m3 values, then fp32 scales [2][128]
+FP8_STAGE = 128 * 128 + 2 * 128 * 4   # one stage image: 128 x 128 e4m3 values, then int32 scale exponents [2][128]
 
 
 def _fp8_tiled_bytes(rows, cols):
@@ -450,8 +450,8 @@ def _decode_fp8_tiles(packed, off, rows, cols):
     """e4m3 values [rows, cols] and scales [rows, cols / 64] (float64) of one
     matrix stored as stage images: 128-row tiles of cols / 128 stages, each a
     128-byte-swizzled 128 x 128 byte image (16-byte chunk c of row r at chunk
-    position c ^ (r % 8)) followed by its scales [2][128]; one zero tile
-    follows the last row."""
+    position c ^ (r % 8)) followed by its scale exponents [2][128] (int32, the
+    scale is 2^e); one zero tile follows the last row."""
     nst, tiles = cols // 128, rows // 128 + 1
     blob = packed[off: off + tiles * nst * FP8_STAGE].view(tiles, nst, FP8_STAGE)
     img = blob[:, :, :128 * 128].reshape(tiles, nst, 128, 8, 16)
@@ -459,11 +459,11 @@ def _decode_fp8_tiles(packed, off, rows, cols):
     pos = torch.arange(8, device=blob.device)[None, :] ^ (r[:, None] % 8)          # [128 rows, 8 logical chunks]
     logical = img[:, :, r[:, None], pos, :]                                            # [tiles, nst, 128, 8, 16]
     q = logical.permute(0, 2, 1, 3, 4).reshape(tiles * 128, cols).contiguous()
-    sc = blob[:, :, 128 * 128:].contiguous().view(torch.float32).view(tiles, nst, 2, 128)
+    sc = blob[:, :, 128 * 128:].contiguous().view(torch.int32).view(tiles, nst, 2, 128)
     sc = sc.permute(0, 3, 1, 2).reshape(tiles * 128, cols // 64)
     assert int(q[rows:].count_nonzero()) == 0 and int(sc[rows:].count_nonzero()) == 0   # the zero tile
     qf = q[:rows].view(torch.float8_e4m3fn).to(torch.float64).cpu().numpy()
-    return qf, sc[:rows].to(torch.float64).cpu().numpy()
+    return qf, np.ldexp(1.0, sc[:rows].cpu().numpy().astype(np.int64))
 
 
 def test_fp8_prepack_matches_oracle_quantization():
@@ -482,18 +482,44 @@ def test_fp8_prepack_matches_oracle_quantization():
     o_w2 = al(o_w13 + _fp8_tiled_bytes(E * 2 * I, d))
     o_w13s = al(o_w2 + _fp8_tiled_bytes(E * d, I))
     o_w2s = al(o_w13s + _fp8_tiled_bytes(2 * Is, d))
-    assert al(o_w2s + _fp8_tiled_bytes(d, Is)) == packed.numel()
+    o_eref = al(o_w2s + _fp8_tiled_bytes(d, Is))
+    assert al(o_eref + (E + 1) * 3 * 4) == packed.numel()
+    eref = packed[o_eref: o_eref + (E + 1) * 3 * 4].view(torch.int32).view(E + 1, 3).cpu().numpy()
     q, s = _decode_fp8_tiles(packed, o_w2, E * d, I)
     wq, ws = orc.quantize_fp8_blocks(f64(w2).reshape(E * d, I))
     assert np.array_equal(q, wq) and np.array_equal(s, ws)
+    # reference exponents: the largest block exponent of each matrix
+    assert np.array_equal(eref[:E, 2], np.log2(ws).reshape(E, -1).max(1))
     q, s = _decode_fp8_tiles(packed, o_w2s, d, Is)
     wq, ws = orc.quantize_fp8_blocks(f64(ws2))
     assert np.array_equal(q, wq) and np.array_equal(s, ws)
+    assert eref[E, 2] == np.log2(ws).max()
     # W13: rows in the 16-row interleave (16 W1 rows, then the 16 W3 rows of the same units)
     q, s = _decode_fp8_tiles(packed, o_w13, E * 2 * I, d)
     w13 = torch.stack([w1, w3], 1).view(E, 2, I // 16, 16, d).transpose(1, 2).reshape(E * 2 * I, d)
     wq, ws = orc.quantize_fp8_blocks(f64(w13))
     assert np.array_equal(q, wq) and np.array_equal(s, ws)
+    for m, w in ((0, w1), (1, w3)):
+        _, ws_m = orc.quantize_fp8_blocks(f64(w).reshape(E * I, d))
+        assert np.array_equal(eref[:E, m], np.log2(ws_m).reshape(E, -1).max(1))
+        _, ws_s = orc.quantize_fp8_blocks(f64((ws1, ws3)[m]))
+        assert eref[E, m] == np.log2(ws_s).max()
+
+
+def test_fp8_layer_flags_activations_beyond_f16():
+    """An FP8 layer takes its token rows as f16: an input value beyond the f16
+    range is reported (MOE_ERR_DEVICE_RANGE), while the bf16 layer takes it."""
+    base = SMALL["v3_small_t333"]
+    for wl, want in ((_fp8_copy(base), _lib.MOE_ERR_DEVICE_RANGE), (base, _lib.MOE_OK)):
+        li = inputs.make_inputs(wl, "cuda")
+        x = li.x.clone()
+        x[17, 5] = 1.0e5
+        layer = MoELayer(wl, li, "cuda")
+        layer.forward(x)
+        code, word = layer.device_status()
+        assert code == want, (wl.name, _lib.moe_status_string(code), word)
+        layer.forward(li.x)
+        assert layer.device_status()[0] == _lib.MOE_OK
 
 
 def _dq(t):

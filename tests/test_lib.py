@@ -140,7 +140,8 @@ def test_backward_workspace_and_argument_checks():
 @pytest.mark.parametrize("name", ["v3_decode_fp8_t1", "v3_prefill_fp8_t16384", "v3_profile_fp8_e16_t1"])
 def test_fp8_packed_size_is_the_stage_image_layout(name):
     """FP8 packed experts: each matrix as (rows / 128 + 1) tiles of K / 128 stage
-    blocks of 128 x 128 e4m3 bytes plus 2 x 128 fp32 scales, 256-byte aligned."""
+    blocks of 128 x 128 e4m3 bytes plus 2 x 128 int32 scale exponents, 256-byte
+    aligned, then the reference exponents int32 [E + 1][3]."""
     wl = inputs.WORKLOADS[name]
     cfg = _lib.make_config(wl)
     stage = 128 * 128 + 2 * 128 * 4
@@ -150,10 +151,11 @@ def test_fp8_packed_size_is_the_stage_image_layout(name):
     total = 0
     for rows, cols in ((2 * E * I, d), (E * d, I), (2 * Is, d), (d, Is)):
         total = al(total + tiled(rows, cols))
+    total = al(total + (E + 1) * 3 * 4)
     assert _lib.moe_packed_size(cfg) == total
     # about 1.0625 bytes per weight (plus one padding tile per matrix)
     weights = 3 * E * I * d + 3 * Is * d
-    assert 1.0625 * weights <= total <= 1.0625 * weights + 4 * (d // 128 + I // 128) * stage * 2
+    assert 1.0625 * weights <= total <= 1.0625 * weights + 4 * (d // 128 + I // 128) * stage * 2 + 4096
 
 
 def test_debug_inject_validates_knobs():

@@ -14,7 +14,7 @@ NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "-DMOE_BUILD", "-I", os.path.join(ROOT, "include")]
-SOURCES = ["api.cu", "gate.cu", "permute.cu", "gemm_tc.cu", "gemm_pair.cu", "experts.cu", "balance.cu", "permute_noalloc.cu", "backward.cu"]
+SOURCES = ["api.cu", "gate.cu", "permute.cu", "gemm_tc.cu", "gemm_pair.cu", "experts.cu", "balance.cu", "permute_noalloc.cu", "backward.cu", "gemv_fp8.cu"]
 
 
 def _newest_input():

@@ -241,6 +241,22 @@ moe_status run_experts(const moe_config& c, const void* x_perm, const int32_t* o
   const long long tiles1 = tb_routed * ((2LL * c.I + 255) / 256) + tb_shared * ((2 * Is + 255) / 256);
   const long long tiles2 = (tb_routed + tb_shared) * ((c.d + 255) / 256);
   const int shared_rows = Is > 0 ? c.T : 0;
+  if (P.fp8 && c.T <= GEMV_MAX_ROWS) {
+    // decode batches of FP8 experts: CUDA-core GEMV (a group holds at most T rows)
+    GemvOperands g1, g1s, g2, g2s;
+    g1.w = pb + P.w13; g1.x = x_perm; g1.x_f16 = true; g1.out = h; g1.out_ld = c.I; g1.M = 2 * c.I; g1.K = c.d;
+    g1s.w = pb + P.w13s; g1s.x = x; g1s.x_f16 = false; g1s.out = hs; g1s.out_ld = Is; g1s.M = int(2 * Is);
+    g1s.K = c.d;
+    g2.w = pb + P.w2; g2.x = h; g2.x_f16 = true; g2.out = y_perm; g2.out_ld = c.d; g2.M = c.d; g2.K = c.I;
+    g2s.w = pb + P.w2s; g2s.x = hs; g2s.x_f16 = true; g2s.out = y_shared; g2s.out_ld = c.d; g2s.M = c.d;
+    g2s.K = int(Is);
+    cudaError_t e = launch_fp8_gemv(g1, Is > 0 ? &g1s : nullptr, offsets, c.E, shared_rows, R, true, false,
+                                    ws.status(), s, launches);
+    if (e == cudaSuccess)
+      e = launch_fp8_gemv(g2, Is > 0 ? &g2s : nullptr, offsets, c.E, shared_rows, R, false, true, ws.status(), s,
+                          launches);
+    return cuda_status(e);
+  }
   int* tickets = ws.status();
   if (fuse_expert_gemms(c)) {
     // one launch: GEMM2 tiles start expert by expert while GEMM1 finishes

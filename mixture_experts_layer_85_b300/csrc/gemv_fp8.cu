@@ -1,0 +1,445 @@
+// Expert FFNs with FP8 weights for decode batches (every group at most
+// GEMV_MAX_ROWS token rows): CUDA-core GEMV over the packed FP8 stage images.
+//
+// At a handful of tokens per expert the tensor cores have almost nothing to
+// multiply (an MMA of N = 16 for one token) and the FP8 tensor-core path pays
+// a per-stage hand-off (converter warps -> MMA -> freed buffer) that caps it
+// well below the HBM rate.  Here each CTA streams whole stage images (128
+// weight rows x 128 columns of e4m3 plus their block exponents, one bulk copy)
+// and the token rows' 128 matching values through a ring of shared-memory
+// stages, and every weight is used straight from the image: e4m3 -> f16 by
+// integer operations (exact, as 2^-8 of the value), times the token values as
+// f16 with an fp32 result (fma.f32.f16: exact products, 4 + 11 significant
+// bits), summed in fp32 per 16-column chunk, times the block's 2^(e+8)
+// (exact) and added to the row's fp32 accumulator.  The expert FFN is w2(silu(w1 x) * w3 x)
+// (intelliparadigm.com page, section 3.3.1) with the FP8 block quantisation of
+// its section 4; two launches: GEMM1 with the SwiGLU epilogue (f16 hidden
+// rows), then GEMM2 (fp32 rows).
+//
+// Work items are (group, 128-row weight tile), the shared expert's first:
+// their token rows do not depend on the dispatch, so in the GEMM1 launch they
+// stream while the preceding kernels still run; the routed groups' items wait
+// for the dispatch (griddepcontrol.wait), after which the producer warp lists
+// the groups that received rows.  CTA b takes items b, b + G, b + 2G, ...
+// (one CTA per SM, a ring of 12 stages: 221 KB of weights and token values in
+// flight per SM).  Every wait is bounded; a CTA that gives up flags the status
+// word and its roles leave without waiting on each other.
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
+#include "internal.h"
+#include "tc_ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int GV_WARPS = 16;                         // compute warps
+constexpr int GV_RPT = 2;                            // weight rows per compute thread
+constexpr int GV_THREADS = 32 * (GV_WARPS + 1);      // plus the producer warp
+constexpr int GV_STAGES = 12;
+constexpr int GV_XBYTES = 128 * 2;                   // one token row's 128 values of a stage (2-byte types)
+constexpr int GV_STAGE_BYTES = FP8_STAGE_BYTES + GEMV_MAX_ROWS * GV_XBYTES;
+constexpr int GV_MAX_GROUPS = 272;
+static_assert(GV_STAGE_BYTES % 128 == 0 && GV_RPT == 2, "stage alignment; the float2 row stores");
+
+struct GemvClass {
+  const uint8_t* w;    // stage images: tiles of 128 rows, nst stages each; group g's first tile is g * tpg
+  const uint8_t* x;    // token rows, K 2-byte values each
+  int x_f16;           // 1: f16 values, 0: bf16
+  void* out;           // GEMM1: f16 [rows, M / 2]; GEMM2: fp32 [rows, M]
+  long long out_ld;    // elements per output row
+  int tpg;             // 128-row weight tiles per group (M / 128)
+  int nst;             // stages per tile (K / 128)
+  int K;
+};
+
+constexpr int GV_IMG_ROWS = FP8_STAGE_BYTES / 128;   // a stage image as rows of 128 bytes
+static_assert(FP8_STAGE_BYTES % 128 == 0 && GV_IMG_ROWS <= 256, "image box");
+
+struct GemvParams {
+  CUtensorMap tm[2];   // the classes' stage images as [images * GV_IMG_ROWS][128] bytes, box = one image
+  GemvClass cls[2];    // 0: routed, 1: shared
+  const int32_t* offsets;   // [num_routed + 1] routed rows of each group
+  int num_routed;
+  int shared_rows;          // 0: no shared expert
+  long long routed_rows;    // bound of every routed row index
+  int gemm1;                // 1: SwiGLU epilogue, 0: fp32 rows
+  int x_from_prev;          // 1: every item's token rows come from the preceding grid
+  int* status;
+};
+
+struct GemvCtrl {
+  uint64_t full[GV_STAGES];    // a stage's image and token values landed
+  uint64_t empty[GV_STAGES];   // every compute warp finished with a stage
+  uint64_t list_ready;         // the active-group list is built
+  uint64_t sums_full;          // GEMM1: every compute warp wrote its rows' sums
+  uint64_t sums_free;          // GEMM1: every compute warp read the sums
+  int abort;
+  int n_active;
+  int active[GV_MAX_GROUPS];
+  float sums[128][GEMV_MAX_ROWS];   // GEMM1: the tile's row sums, for the SwiGLU pairing
+};
+
+struct GemvItem {
+  int cls, rows, tile_w;        // class, token rows, weight tile (of the class's whole matrix)
+  int tile;                     // tile within the group
+  long long row0;               // first token row (x) and output row
+};
+
+// Item -> operands, or false past the last item.  nsh: the shared expert's items.
+__device__ __forceinline__ bool gemv_item(const GemvParams& p, const GemvCtrl* c, int nsh, int item, GemvItem& it) {
+  if (item < nsh) {
+    it.cls = 1;
+    it.rows = p.shared_rows;
+    it.tile = item;
+    it.tile_w = item;
+    it.row0 = 0;
+    return true;
+  }
+  const int tpg = p.cls[0].tpg;
+  const int j = item - nsh;
+  const int gi = j / tpg;
+  if (gi >= c->n_active) return false;
+  const int g = c->active[gi];
+  it.cls = 0;
+  it.tile = j - gi * tpg;
+  it.tile_w = g * tpg + it.tile;
+  it.row0 = p.offsets[g];
+  it.rows = p.offsets[g + 1] - p.offsets[g];
+  return true;
+}
+
+// Producer warp: lists the routed groups with rows (after the dispatch), then
+// lane 0 streams every item's stages.  Returns with all its copies landed.
+__device__ void gemv_producer(const GemvParams& p, GemvCtrl* c, uint8_t* ring, int lane) {
+  const int nsh = p.shared_rows > 0 ? p.cls[1].tpg : 0;
+  const int G = gridDim.x;
+  bool waited = false, listed = false;
+  int s = 0;
+  uint32_t ph = 0;
+  uint32_t used = 0, used_par = 0;
+  for (int item = blockIdx.x;; item += G) {
+    if ((item >= nsh || p.x_from_prev) && !waited) {
+      pdl_wait();   // the dispatch (and, for GEMM2, the hidden rows) come from the preceding grids
+      waited = true;
+    }
+    if (item >= nsh && !listed) {
+      // warp-wide scan of the groups: the ones with rows, in index order
+      int base = 0;
+      for (int g0 = 0; g0 < p.num_routed; g0 += 32) {
+        const int g = g0 + lane;
+        int rows = 0;
+        if (g < p.num_routed) {
+          const long long lo = p.offsets[g], hi = p.offsets[g + 1];
+          rows = int(hi - lo);
+          if (lo < 0 || hi > p.routed_rows || rows < 0 || rows > GEMV_MAX_ROWS) {
+            flag_status(p.status, DEV_BAD_ROW);
+            rows = 0;
+          }
+        }
+        const uint32_t m = __ballot_sync(0xffffffffu, rows > 0);
+        if (rows > 0) c->active[base + __popc(m & ((1u << lane) - 1u))] = g;
+        base += __popc(m);
+      }
+      if (lane == 0) {
+        c->n_active = base;
+        mbar_arrive(&c->list_ready);   // release (CTA): orders the list above
+      }
+      __syncwarp();
+      listed = true;
+    }
+    GemvItem it;
+    if (!gemv_item(p, c, nsh, item, it)) break;
+    if (lane == 0) {
+      const GemvClass& k = p.cls[it.cls];
+      const uint32_t bytes = uint32_t(FP8_STAGE_BYTES + it.rows * GV_XBYTES);
+      for (int ks = 0; ks < k.nst; ++ks) {
+        if (!mbar_wait(&c->empty[s], ph ^ 1u, &c->abort, p.status)) break;
+        uint8_t* st = ring + size_t(s) * GV_STAGE_BYTES;
+        mbar_arrive_expect_tx(&c->full[s], bytes);
+        tma_load_2d(st, &p.tm[it.cls], &c->full[s], 0, (it.tile_w * k.nst + ks) * GV_IMG_ROWS);
+        for (int t = 0; t < it.rows; ++t)
+          bulk_load(st + FP8_STAGE_BYTES + t * GV_XBYTES,
+                    k.x + ((it.row0 + t) * (long long)k.K + (long long)ks * 128) * 2, GV_XBYTES, &c->full[s]);
+        used |= 1u << s;
+        used_par = (used_par & ~(1u << s)) | (ph << s);
+        if (++s == GV_STAGES) {
+          s = 0;
+          ph ^= 1u;
+        }
+      }
+    }
+    if (__shfl_sync(0xffffffffu, *reinterpret_cast<volatile int*>(&c->abort), 0)) break;
+  }
+  if (!listed && lane == 0) {
+    c->n_active = 0;
+    mbar_arrive(&c->list_ready);
+  }
+  if (lane == 0) {
+    // every copy issued here lands before the CTA may leave (bounded)
+    const unsigned long long t0 = globaltimer_ns();
+    for (int i = 0; i < GV_STAGES; ++i) {
+      if (!(used & (1u << i))) continue;
+      while (!mbar_try_wait(&c->full[i], (used_par >> i) & 1u))
+        if (globaltimer_ns() - t0 > kWaitLimitNs) break;
+    }
+  }
+}
+
+// 16 e4m3 values -> 8 f16 pairs holding each value times 2^-8, with integer
+// operations only.  An e4m3 byte s.eeee.mmm read as the f16 bits
+// s.0eeee.mmm0000000 is 2^-8 of its value: normal e4m3 (e >= 1) is
+// 2^(e-7) (1 + m/8) and those bits read 2^(e-15) (1 + m/8); e = 0 is m 2^-9
+// and those bits are the f16 subnormal m 2^7 2^-24 = m 2^-17.  A byte permute
+// puts bytes 0 and 1 (or 2 and 3) of a word in the high bytes of two f16
+// lanes; the sign stays in place and the other seven bits move down by one.
+__device__ __forceinline__ void e4m3x16_to_f16x2_scaled(const uint4 q, uint32_t* w) {
+  const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t lo = __byte_perm(qw[i], 0u, 0x1404u);   // bytes 0, 1 -> bits 8..15, 24..31
+    const uint32_t hi = __byte_perm(qw[i], 0u, 0x3424u);   // bytes 2, 3
+    w[2 * i] = (lo & 0x80008000u) | ((lo >> 1) & 0x3f803f80u);
+    w[2 * i + 1] = (hi & 0x80008000u) | ((hi >> 1) & 0x3f803f80u);
+  }
+}
+
+// 16 two-byte token values -> 8 f16 pairs: f16 values as they are; bf16 ones
+// rounded to f16 (exact between 2^-14 and 65504; the gather reports values
+// beyond the f16 range for FP8 layers).
+__device__ __forceinline__ void x16_to_f16x2(const uint8_t* src, bool f16, uint32_t* x) {
+  const uint4 a = *reinterpret_cast<const uint4*>(src);
+  const uint4 b = *reinterpret_cast<const uint4*>(src + 16);
+  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    if (f16) {
+      x[i] = w[i];
+    } else {
+      const __half2 h = __floats2half2_rn(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
+      x[i] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+  }
+}
+
+// acc + lo(w) * lo(x) + hi(w) * hi(x): f16 operands, products exact in fp32
+// (11 + 11 significant bits), fp32 sums.
+__device__ __forceinline__ float fma_f16x2_f32(uint32_t w, uint32_t x, float acc) {
+  asm("{\n\t.reg .f16 wl, wh, xl, xh;\n\t"
+      "mov.b32 {wl, wh}, %1;\n\t"
+      "mov.b32 {xl, xh}, %2;\n\t"
+      "fma.rn.f32.f16 %0, wl, xl, %0;\n\t"
+      "fma.rn.f32.f16 %0, wh, xh, %0;\n\t}"
+      : "+f"(acc)
+      : "r"(w), "r"(x));
+  return acc;
+}
+
+// 2^e as a float (exact; normal range directly).
+__device__ __forceinline__ float pow2f(int e) {
+  return (e >= -126 && e <= 127) ? __int_as_float((e + 127) << 23) : ldexpf(1.0f, e);
+}
+
+__device__ __forceinline__ float silu_f(float z) { return z / (1.0f + __expf(-z)); }
+
+// Compute warps: thread (row group rg, chunk ch) owns weight rows GV_RPT rg ..
+// GV_RPT rg + GV_RPT - 1 of the tile and columns 16 ch .. 16 ch + 15 of every
+// stage; each dot product runs as two independent partial sums (16 warps and
+// short dependency chains keep the FMA pipes fed).  Every lane waits on each
+// barrier itself (bounded) and the warp leaves together when any lane gave up.
+__device__ void gemv_compute(const GemvParams& p, GemvCtrl* c, uint8_t* ring, int warp, int lane) {
+  const int nsh = p.shared_rows > 0 ? p.cls[1].tpg : 0;
+  const int G = gridDim.x;
+  const int rg = warp * 4 + (lane >> 3), ch = lane & 7, h = ch >> 2;   // 4 row groups per warp
+  const int tid = warp * 32 + lane;
+  bool listed = false;
+  int s = 0;
+  uint32_t ph = 0;
+  uint32_t n1 = 0;   // GEMM1 items done (parity of the sums barriers)
+  for (int item = blockIdx.x;; item += G) {
+    if (item >= nsh && !listed) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&c->list_ready, 0u, &c->abort, p.status))) return;
+      listed = true;
+    }
+    GemvItem it;
+    if (!gemv_item(p, c, nsh, item, it)) return;
+    const GemvClass& k = p.cls[it.cls];
+    const bool f16 = k.x_f16 != 0;
+    float acc[GV_RPT][GEMV_MAX_ROWS];
+#pragma unroll
+    for (int r = 0; r < GV_RPT; ++r)
+#pragma unroll
+      for (int t = 0; t < GEMV_MAX_ROWS; ++t) acc[r][t] = 0.0f;
+    for (int ks = 0; ks < k.nst; ++ks) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&c->full[s], ph, &c->abort, p.status))) return;
+      const uint8_t* st = ring + size_t(s) * GV_STAGE_BYTES;
+      uint32_t xv[GEMV_MAX_ROWS][8];
+#pragma unroll
+      for (int t = 0; t < GEMV_MAX_ROWS; ++t)
+        if (t < it.rows) x16_to_f16x2(st + FP8_STAGE_BYTES + t * GV_XBYTES + ch * 32, f16, xv[t]);
+#pragma unroll
+      for (int r = 0; r < GV_RPT; ++r) {
+        const int row = rg * GV_RPT + r;
+        const uint4 q = *reinterpret_cast<const uint4*>(st + row * 128 + ((ch ^ (row & 7)) << 4));
+        // the block's 2^e, times 2^8 for the scaled f16 weights
+        const float sc = pow2f(reinterpret_cast<const int32_t*>(st + FP8_IMAGE_BYTES)[h * 128 + row] + 8);
+        uint32_t wv[8];
+        e4m3x16_to_f16x2_scaled(q, wv);
+#pragma unroll
+        for (int t = 0; t < GEMV_MAX_ROWS; ++t) {
+          if (t < it.rows) {
+            float p0 = 0.0f, p1 = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 8; i += 2) {
+              p0 = fma_f16x2_f32(wv[i], xv[t][i], p0);
+              p1 = fma_f16x2_f32(wv[i + 1], xv[t][i + 1], p1);
+            }
+            acc[r][t] = fmaf(p0 + p1, sc, acc[r][t]);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&c->empty[s]);
+      if (++s == GV_STAGES) {
+        s = 0;
+        ph ^= 1u;
+      }
+    }
+    // the 8 chunk threads of a row group hold partial sums of the same rows
+#pragma unroll
+    for (int r = 0; r < GV_RPT; ++r)
+#pragma unroll
+      for (int t = 0; t < GEMV_MAX_ROWS; ++t) {
+        float v = acc[r][t];
+        v += __shfl_xor_sync(0xffffffffu, v, 1);
+        v += __shfl_xor_sync(0xffffffffu, v, 2);
+        v += __shfl_xor_sync(0xffffffffu, v, 4);
+        acc[r][t] = v;
+      }
+    if (!p.gemm1) {
+      if (ch == 0) {
+        float* out = static_cast<float*>(k.out);
+#pragma unroll
+        for (int t = 0; t < GEMV_MAX_ROWS; ++t)
+          if (t < it.rows)
+            *reinterpret_cast<float2*>(out + (it.row0 + t) * k.out_ld + it.tile * 128 + rg * GV_RPT) =  // GV_RPT = 2
+                make_float2(acc[0][t], acc[1][t]);
+      }
+      continue;
+    }
+    // GEMM1: rows come in blocks of 32 (16 W1 rows of 16 features, then their
+    // W3 rows); pair them through shared memory (bounded barrier waits)
+    if (!__all_sync(0xffffffffu, mbar_wait(&c->sums_free, (n1 & 1u) ^ 1u, &c->abort, p.status))) return;
+    if (ch == 0) {
+#pragma unroll
+      for (int r = 0; r < GV_RPT; ++r)
+#pragma unroll
+        for (int t = 0; t < GEMV_MAX_ROWS; ++t) c->sums[rg * GV_RPT + r][t] = acc[r][t];
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&c->sums_full);
+    if (!__all_sync(0xffffffffu, mbar_wait(&c->sums_full, n1 & 1u, &c->abort, p.status))) return;
+    bool over = false;
+    __half* out = static_cast<__half*>(k.out);
+    for (int i = tid; i < 64 * it.rows; i += 32 * GV_WARPS) {
+      const int f = i & 63, t = i >> 6;
+      const int r1 = (f >> 4) * 32 + (f & 15);
+      const float hv = silu_f(c->sums[r1][t]) * c->sums[r1 + 16][t];
+      over |= fabsf(hv) >= 65520.0f;
+      out[(it.row0 + t) * k.out_ld + it.tile * 64 + f] = __float2half_rn(hv);
+    }
+    if (over) flag_status(p.status, DEV_RANGE);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&c->sums_free);
+    ++n1;
+  }
+}
+
+__global__ void __launch_bounds__(GV_THREADS, 1) gemv_fp8_kernel(const __grid_constant__ GemvParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+  GemvCtrl* c = reinterpret_cast<GemvCtrl*>(ring + size_t(GV_STAGES) * GV_STAGE_BYTES);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < GV_STAGES; ++i) {
+      mbar_init(&c->full[i], 1);
+      mbar_init(&c->empty[i], GV_WARPS);
+    }
+    mbar_init(&c->list_ready, 1);
+    mbar_init(&c->sums_full, GV_WARPS);
+    mbar_init(&c->sums_free, GV_WARPS);
+    c->abort = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  pdl_launch_dependents();
+  if (warp == GV_WARPS) gemv_producer(p, c, ring, lane);
+  else gemv_compute(p, c, ring, warp, lane);
+}
+
+constexpr size_t kGemvSmem = 128 + size_t(GV_STAGES) * GV_STAGE_BYTES + sizeof(GemvCtrl);
+
+}  // namespace
+
+cudaError_t launch_fp8_gemv(const GemvOperands& routed, const GemvOperands* shared, const int32_t* offsets,
+                            int num_routed, int shared_rows, long long routed_rows, bool gemm1, bool x_from_prev,
+                            int* status, cudaStream_t stream, int* launches) {
+  if (num_routed < 1 || num_routed > GV_MAX_GROUPS || offsets == nullptr) return cudaErrorInvalidValue;
+  if ((shared == nullptr) != (shared_rows <= 0) || shared_rows > GEMV_MAX_ROWS) return cudaErrorInvalidValue;
+  GemvParams p;
+  memset(&p, 0, sizeof(p));
+  const GemvOperands* ops[2] = {&routed, shared};
+  for (int i = 0; i < 2; ++i) {
+    const GemvOperands* o = ops[i] != nullptr ? ops[i] : ops[0];
+    if (o->M % 128 != 0 || o->K % 128 != 0 || o->M <= 0 || o->K <= 0) return cudaErrorInvalidValue;
+    if (reinterpret_cast<uintptr_t>(o->w) % 16 != 0 || reinterpret_cast<uintptr_t>(o->x) % 16 != 0 ||
+        reinterpret_cast<uintptr_t>(o->out) % 16 != 0 || (!gemm1 && o->out_ld % 4 != 0))
+      return cudaErrorInvalidValue;
+    GemvClass& k = p.cls[i];
+    k.w = static_cast<const uint8_t*>(o->w);
+    k.x = static_cast<const uint8_t*>(o->x);
+    k.x_f16 = o->x_f16 ? 1 : 0;
+    k.out = o->out;
+    k.out_ld = o->out_ld;
+    k.tpg = o->M / 128;
+    k.nst = o->K / 128;
+    k.K = o->K;
+  }
+  // each class's images as a 2-D byte tensor, one box per image (no swizzle:
+  // the images are stored in their shared-memory layout)
+  auto enc = tensor_map_encoder();
+  if (enc == nullptr) return cudaErrorInvalidValue;
+  for (int i = 0; i < 2; ++i) {
+    const GemvOperands* o = ops[i] != nullptr ? ops[i] : ops[0];
+    const long long groups = (i == 0 || ops[i] == nullptr) ? num_routed : 1;
+    const long long rows = groups * (o->M / 128) * (o->K / 128) * GV_IMG_ROWS;
+    if (rows >= (1LL << 31)) return cudaErrorInvalidValue;
+    cuuint64_t dims[2] = {128u, cuuint64_t(rows)};
+    cuuint64_t strides[1] = {128u};
+    cuuint32_t box[2] = {128u, cuuint32_t(GV_IMG_ROWS)};
+    cuuint32_t es[2] = {1u, 1u};
+    if (enc(&p.tm[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(o->w), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  p.offsets = offsets;
+  p.num_routed = num_routed;
+  p.shared_rows = shared != nullptr ? shared_rows : 0;
+  p.routed_rows = routed_rows;
+  p.gemm1 = gemm1 ? 1 : 0;
+  p.x_from_prev = x_from_prev ? 1 : 0;
+  p.status = status;
+  static PerDevice<int> attr;
+  int ok = 0;
+  cudaError_t e = attr.get(&ok, [](int* v) {
+    *v = 1;
+    return cudaFuncSetAttribute(gemv_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kGemvSmem));
+  });
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(gemv_fp8_kernel, dim3(num_sms()), dim3(GV_THREADS), kGemvSmem, stream, p);
+  if (e == cudaSuccess && launches) ++*launches;
+  return e;
+}
+
+}  // namespace moe

@@ -217,12 +217,16 @@ def make_router(wl: Workload):
 
 
 def make_experts(wl: Workload, device="cpu"):
-    """Routed and shared expert weights in nn.Linear layout, drawn on ``device``."""
+    """Routed and shared expert weights in nn.Linear layout, drawn on ``device``
+    (the shared ones None for a layer without a shared expert)."""
     act = torch_dtype(wl.act_dtype)
-    bd, bi, bs = 1.0 / math.sqrt(wl.d), 1.0 / math.sqrt(wl.I), 1.0 / math.sqrt(wl.I_s)
+    bd, bi = 1.0 / math.sqrt(wl.d), 1.0 / math.sqrt(wl.I)
     w1 = _uniform((wl.E, wl.I, wl.d), bd, SEED_W1, device, act, per_leading=True)
     w3 = _uniform((wl.E, wl.I, wl.d), bd, SEED_W3, device, act, per_leading=True)
     w2 = _uniform((wl.E, wl.d, wl.I), bi, SEED_W2, device, act, per_leading=True)
+    if wl.I_s == 0:
+        return w1, w3, w2, None, None, None
+    bs = 1.0 / math.sqrt(wl.I_s)
     ws1 = _uniform((wl.I_s, wl.d), bd, SEED_WS1, device, act, per_leading=False)
     ws3 = _uniform((wl.I_s, wl.d), bd, SEED_WS3, device, act, per_leading=False)
     ws2 = _uniform((wl.d, wl.I_s), bs, SEED_WS2, device, act, per_leading=False)

@@ -47,6 +47,9 @@ SMALL = {
                                          n_group=8, topk_group=4),
     "v3_small_t3": inputs.small_workload(W["v3_prefill_t16384"], name="v3_small_t3", T=3, d=512, E=64, I=256,
                                          n_group=8, topk_group=4),
+    # no shared expert: the expert kernel's shared classes are absent
+    "v2lite_small_t77_noshared": inputs.small_workload(W["v2lite_t4096"], name="v2lite_small_t77_noshared", T=77,
+                                                       d=256, E=16, I=256, k=6, n_shared=0),
 }
 
 
@@ -541,6 +544,8 @@ def _dequantized_accessor(li):
 
 
 def _dequantized_shared(li):
+    if li.wl.n_shared == 0:
+        return None
     return _dq(li.ws1), _dq(li.ws3), _dq(li.ws2)
 
 
@@ -550,11 +555,18 @@ FP8_ODD = {
                                        n_group=8, topk_group=4),
     "v3_odd_t40": inputs.small_workload(W["v3_prefill_t16384"], name="v3_odd_t40", T=40, d=384, E=64, I=384,
                                         n_group=8, topk_group=4),
+    # batches of at most 4 tokens take the CUDA-core FP8 path: the largest such
+    # batch with an odd number of stages, and one without a shared expert
+    "v3_gemv_t4": inputs.small_workload(W["v3_prefill_t16384"], name="v3_gemv_t4", T=4, d=384, E=64, I=384,
+                                        n_group=8, topk_group=4),
+    "v2lite_gemv_t2_noshared": inputs.small_workload(W["v2lite_t4096"], name="v2lite_gemv_t2_noshared", T=2, d=256,
+                                                     E=16, I=256, k=6, n_shared=0),
 }
 
 
 @pytest.mark.parametrize("name", ["v3_small_t333", "v2lite_small_t1037", "v3_small_t1", "v3_small_t3",
-                                  "v3_small_t1100", "v3_odd_t5", "v3_odd_t40"])
+                                  "v3_small_t1100", "v3_odd_t5", "v3_odd_t40", "v3_gemv_t4",
+                                  "v2lite_gemv_t2_noshared"])
 def test_fp8_layer_matches_oracle_on_dequantized_weights(name):
     wl = _fp8_copy(SMALL[name] if name in SMALL else FP8_ODD[name])
     li = inputs.make_inputs(wl, "cuda")

@@ -250,11 +250,11 @@ moe_status run_experts(const moe_config& c, const void* x_perm, const int32_t* o
     g2.w = pb + P.w2; g2.x = h; g2.x_f16 = true; g2.out = y_perm; g2.out_ld = c.d; g2.M = c.d; g2.K = c.I;
     g2s.w = pb + P.w2s; g2s.x = hs; g2s.x_f16 = true; g2s.out = y_shared; g2s.out_ld = c.d; g2s.M = c.d;
     g2s.K = int(Is);
-    cudaError_t e = launch_fp8_gemv(g1, Is > 0 ? &g1s : nullptr, offsets, c.E, shared_rows, R, true, false,
+    cudaError_t e = launch_fp8_gemv(g1, Is > 0 ? &g1s : nullptr, offsets, c.E, shared_rows, c.T, R, true, false,
                                     ws.status(), s, launches);
     if (e == cudaSuccess)
-      e = launch_fp8_gemv(g2, Is > 0 ? &g2s : nullptr, offsets, c.E, shared_rows, R, false, true, ws.status(), s,
-                          launches);
+      e = launch_fp8_gemv(g2, Is > 0 ? &g2s : nullptr, offsets, c.E, shared_rows, c.T, R, false, true,
+                          ws.status(), s, launches);
     return cuda_status(e);
   }
   int* tickets = ws.status();

@@ -7,11 +7,11 @@
 // well below the HBM rate.  Here each CTA streams whole stage images (128
 // weight rows x 128 columns of e4m3 plus their block exponents, one bulk copy)
 // and the token rows' 128 matching values through a ring of shared-memory
-// stages, and every weight is used straight from the image: e4m3 -> f16 by
-// integer operations (exact, as 2^-8 of the value), times the token values as
-// f16 with an fp32 result (fma.f32.f16: exact products, 4 + 11 significant
-// bits), summed in fp32 per 16-column chunk, times the block's 2^(e+8)
-// (exact) and added to the row's fp32 accumulator.  The expert FFN is w2(silu(w1 x) * w3 x)
+// stages, and every weight is used straight from the image: e4m3 -> f16
+// (exact), times the token values as f16 with an fp32 result (fma.f32.f16:
+// exact products, 4 + 11 significant bits), summed in fp32 per 16-column
+// chunk, times the block's 2^e (exact) and added to the row's fp32
+// accumulator.  The expert FFN is w2(silu(w1 x) * w3 x)
 // (intelliparadigm.com page, section 3.3.1) with the FP8 block quantisation of
 // its section 4; two launches: GEMM1 with the SwiGLU epilogue (f16 hidden
 // rows), then GEMM2 (fp32 rows).
@@ -62,6 +62,7 @@ struct GemvParams {
   const int32_t* offsets;   // [num_routed + 1] routed rows of each group
   int num_routed;
   int shared_rows;          // 0: no shared expert
+  int max_rows;             // bound of every group's token rows (the kernel's MAXR or less)
   long long routed_rows;    // bound of every routed row index
   int gemm1;                // 1: SwiGLU epilogue, 0: fp32 rows
   int x_from_prev;          // 1: every item's token rows come from the preceding grid
@@ -132,7 +133,7 @@ __device__ void gemv_producer(const GemvParams& p, GemvCtrl* c, uint8_t* ring, i
         if (g < p.num_routed) {
           const long long lo = p.offsets[g], hi = p.offsets[g + 1];
           rows = int(hi - lo);
-          if (lo < 0 || hi > p.routed_rows || rows < 0 || rows > GEMV_MAX_ROWS) {
+          if (lo < 0 || hi > p.routed_rows || rows < 0 || rows > p.max_rows) {
             flag_status(p.status, DEV_BAD_ROW);
             rows = 0;
           }
@@ -186,21 +187,15 @@ __device__ void gemv_producer(const GemvParams& p, GemvCtrl* c, uint8_t* ring, i
   }
 }
 
-// 16 e4m3 values -> 8 f16 pairs holding each value times 2^-8, with integer
-// operations only.  An e4m3 byte s.eeee.mmm read as the f16 bits
-// s.0eeee.mmm0000000 is 2^-8 of its value: normal e4m3 (e >= 1) is
-// 2^(e-7) (1 + m/8) and those bits read 2^(e-15) (1 + m/8); e = 0 is m 2^-9
-// and those bits are the f16 subnormal m 2^7 2^-24 = m 2^-17.  A byte permute
-// puts bytes 0 and 1 (or 2 and 3) of a word in the high bytes of two f16
-// lanes; the sign stays in place and the other seven bits move down by one.
-__device__ __forceinline__ void e4m3x16_to_f16x2_scaled(const uint4 q, uint32_t* w) {
+// 16 e4m3 values -> 8 f16 pairs (exact: every e4m3 value is an f16 number).
+__device__ __forceinline__ void e4m3x16_to_f16x2(const uint4 q, uint32_t* w) {
   const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const uint32_t lo = __byte_perm(qw[i], 0u, 0x1404u);   // bytes 0, 1 -> bits 8..15, 24..31
-    const uint32_t hi = __byte_perm(qw[i], 0u, 0x3424u);   // bytes 2, 3
-    w[2 * i] = (lo & 0x80008000u) | ((lo >> 1) & 0x3f803f80u);
-    w[2 * i + 1] = (hi & 0x80008000u) | ((hi >> 1) & 0x3f803f80u);
+    const __half2_raw a = __nv_cvt_fp8x2_to_halfraw2(__nv_fp8x2_storage_t(qw[i] & 0xffffu), __NV_E4M3);
+    const __half2_raw b = __nv_cvt_fp8x2_to_halfraw2(__nv_fp8x2_storage_t(qw[i] >> 16), __NV_E4M3);
+    w[2 * i] = uint32_t(a.x) | (uint32_t(a.y) << 16);
+    w[2 * i + 1] = uint32_t(b.x) | (uint32_t(b.y) << 16);
   }
 }
 
@@ -242,15 +237,49 @@ __device__ __forceinline__ float pow2f(int e) {
 
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + __expf(-z)); }
 
+// One stage of a thread's dot products: rows GV_RPT rg .. (+ GV_RPT - 1),
+// columns 16 ch .. 16 ch + 15, token rows t < rows; adds 2^e times each row's
+// partial sum into acc.
+template <int MAXR>
+__device__ __forceinline__ void gemv_stage(const uint8_t* st, int rg, int ch, int rows, bool f16,
+                                           float (&acc)[GV_RPT][MAXR]) {
+  const int h = ch >> 2;
+  uint32_t xv[MAXR][8];
+#pragma unroll
+  for (int t = 0; t < MAXR; ++t)
+    if (t < rows) x16_to_f16x2(st + FP8_STAGE_BYTES + t * GV_XBYTES + ch * 32, f16, xv[t]);
+#pragma unroll
+  for (int r = 0; r < GV_RPT; ++r) {
+    const int row = rg * GV_RPT + r;
+    const uint4 q = *reinterpret_cast<const uint4*>(st + row * 128 + ((ch ^ (row & 7)) << 4));
+    const float sc = pow2f(reinterpret_cast<const int32_t*>(st + FP8_IMAGE_BYTES)[h * 128 + row]);
+    uint32_t wv[8];
+    e4m3x16_to_f16x2(q, wv);
+#pragma unroll
+    for (int t = 0; t < MAXR; ++t) {
+      if (t < rows) {
+        float p0 = 0.0f, p1 = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 8; i += 2) {
+          p0 = fma_f16x2_f32(wv[i], xv[t][i], p0);
+          p1 = fma_f16x2_f32(wv[i + 1], xv[t][i + 1], p1);
+        }
+        acc[r][t] = fmaf(p0 + p1, sc, acc[r][t]);
+      }
+    }
+  }
+}
+
 // Compute warps: thread (row group rg, chunk ch) owns weight rows GV_RPT rg ..
 // GV_RPT rg + GV_RPT - 1 of the tile and columns 16 ch .. 16 ch + 15 of every
 // stage; each dot product runs as two independent partial sums (16 warps and
 // short dependency chains keep the FMA pipes fed).  Every lane waits on each
 // barrier itself (bounded) and the warp leaves together when any lane gave up.
+template <int MAXR>
 __device__ void gemv_compute(const GemvParams& p, GemvCtrl* c, uint8_t* ring, int warp, int lane) {
   const int nsh = p.shared_rows > 0 ? p.cls[1].tpg : 0;
   const int G = gridDim.x;
-  const int rg = warp * 4 + (lane >> 3), ch = lane & 7, h = ch >> 2;   // 4 row groups per warp
+  const int rg = warp * 4 + (lane >> 3), ch = lane & 7;   // 4 row groups per warp
   const int tid = warp * 32 + lane;
   bool listed = false;
   int s = 0;
@@ -265,51 +294,57 @@ __device__ void gemv_compute(const GemvParams& p, GemvCtrl* c, uint8_t* ring, in
     if (!gemv_item(p, c, nsh, item, it)) return;
     const GemvClass& k = p.cls[it.cls];
     const bool f16 = k.x_f16 != 0;
-    float acc[GV_RPT][GEMV_MAX_ROWS];
+    float acc[GV_RPT][MAXR];
 #pragma unroll
     for (int r = 0; r < GV_RPT; ++r)
 #pragma unroll
-      for (int t = 0; t < GEMV_MAX_ROWS; ++t) acc[r][t] = 0.0f;
-    for (int ks = 0; ks < k.nst; ++ks) {
-      if (!__all_sync(0xffffffffu, mbar_wait(&c->full[s], ph, &c->abort, p.status))) return;
-      const uint8_t* st = ring + size_t(s) * GV_STAGE_BYTES;
-      uint32_t xv[GEMV_MAX_ROWS][8];
+      for (int t = 0; t < MAXR; ++t) acc[r][t] = 0.0f;
+    // several stages per wait (more independent work between synchronisations):
+    // four with one token row, two with two; with more rows the registers would spill
+    constexpr int kPer = MAXR == 1 ? 4 : (MAXR == 2 ? 2 : 1);
+    for (int ks = 0; ks < k.nst; ks += kPer) {
+      const int n = min(kPer, k.nst - ks);
+      int si[kPer];
+      uint32_t pi[kPer];
+      si[0] = s;
+      pi[0] = ph;
 #pragma unroll
-      for (int t = 0; t < GEMV_MAX_ROWS; ++t)
-        if (t < it.rows) x16_to_f16x2(st + FP8_STAGE_BYTES + t * GV_XBYTES + ch * 32, f16, xv[t]);
+      for (int j = 1; j < kPer; ++j) {
+        si[j] = si[j - 1] + 1 == GV_STAGES ? 0 : si[j - 1] + 1;
+        pi[j] = si[j - 1] + 1 == GV_STAGES ? pi[j - 1] ^ 1u : pi[j - 1];
+      }
+      bool got = true;
 #pragma unroll
-      for (int r = 0; r < GV_RPT; ++r) {
-        const int row = rg * GV_RPT + r;
-        const uint4 q = *reinterpret_cast<const uint4*>(st + row * 128 + ((ch ^ (row & 7)) << 4));
-        // the block's 2^e, times 2^8 for the scaled f16 weights
-        const float sc = pow2f(reinterpret_cast<const int32_t*>(st + FP8_IMAGE_BYTES)[h * 128 + row] + 8);
-        uint32_t wv[8];
-        e4m3x16_to_f16x2_scaled(q, wv);
+      for (int j = 0; j < kPer; ++j)
+        if (j < n) got = got && mbar_wait(&c->full[si[j]], pi[j], &c->abort, p.status);
+      if (!__all_sync(0xffffffffu, got)) return;
+      if (n == kPer) {
 #pragma unroll
-        for (int t = 0; t < GEMV_MAX_ROWS; ++t) {
-          if (t < it.rows) {
-            float p0 = 0.0f, p1 = 0.0f;
-#pragma unroll
-            for (int i = 0; i < 8; i += 2) {
-              p0 = fma_f16x2_f32(wv[i], xv[t][i], p0);
-              p1 = fma_f16x2_f32(wv[i + 1], xv[t][i + 1], p1);
-            }
-            acc[r][t] = fmaf(p0 + p1, sc, acc[r][t]);
-          }
-        }
+        for (int j = 0; j < kPer; ++j)
+          gemv_stage<MAXR>(ring + size_t(si[j]) * GV_STAGE_BYTES, rg, ch, it.rows, f16, acc);
+      } else {
+        for (int j = 0; j < n; ++j)
+          gemv_stage<MAXR>(ring + size_t(si[j]) * GV_STAGE_BYTES, rg, ch, it.rows, f16, acc);
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&c->empty[s]);
-      if (++s == GV_STAGES) {
-        s = 0;
-        ph ^= 1u;
+      if (lane == 0) {
+#pragma unroll
+        for (int j = 0; j < kPer; ++j)
+          if (j < n) mbar_arrive(&c->empty[si[j]]);
+      }
+      // advance past the n stages
+      for (int j = 0; j < n; ++j) {
+        if (++s == GV_STAGES) {
+          s = 0;
+          ph ^= 1u;
+        }
       }
     }
     // the 8 chunk threads of a row group hold partial sums of the same rows
 #pragma unroll
     for (int r = 0; r < GV_RPT; ++r)
 #pragma unroll
-      for (int t = 0; t < GEMV_MAX_ROWS; ++t) {
+      for (int t = 0; t < MAXR; ++t) {
         float v = acc[r][t];
         v += __shfl_xor_sync(0xffffffffu, v, 1);
         v += __shfl_xor_sync(0xffffffffu, v, 2);
@@ -320,7 +355,7 @@ __device__ void gemv_compute(const GemvParams& p, GemvCtrl* c, uint8_t* ring, in
       if (ch == 0) {
         float* out = static_cast<float*>(k.out);
 #pragma unroll
-        for (int t = 0; t < GEMV_MAX_ROWS; ++t)
+        for (int t = 0; t < MAXR; ++t)
           if (t < it.rows)
             *reinterpret_cast<float2*>(out + (it.row0 + t) * k.out_ld + it.tile * 128 + rg * GV_RPT) =  // GV_RPT = 2
                 make_float2(acc[0][t], acc[1][t]);
@@ -334,7 +369,7 @@ __device__ void gemv_compute(const GemvParams& p, GemvCtrl* c, uint8_t* ring, in
 #pragma unroll
       for (int r = 0; r < GV_RPT; ++r)
 #pragma unroll
-        for (int t = 0; t < GEMV_MAX_ROWS; ++t) c->sums[rg * GV_RPT + r][t] = acc[r][t];
+        for (int t = 0; t < MAXR; ++t) c->sums[rg * GV_RPT + r][t] = acc[r][t];
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&c->sums_full);
@@ -355,6 +390,8 @@ __device__ void gemv_compute(const GemvParams& p, GemvCtrl* c, uint8_t* ring, in
   }
 }
 
+// MAXR: the most token rows any group of the launch holds (1, 2 or 4).
+template <int MAXR>
 __global__ void __launch_bounds__(GV_THREADS, 1) gemv_fp8_kernel(const __grid_constant__ GemvParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
@@ -374,7 +411,7 @@ __global__ void __launch_bounds__(GV_THREADS, 1) gemv_fp8_kernel(const __grid_co
   __syncthreads();
   pdl_launch_dependents();
   if (warp == GV_WARPS) gemv_producer(p, c, ring, lane);
-  else gemv_compute(p, c, ring, warp, lane);
+  else gemv_compute<MAXR>(p, c, ring, warp, lane);
 }
 
 constexpr size_t kGemvSmem = 128 + size_t(GV_STAGES) * GV_STAGE_BYTES + sizeof(GemvCtrl);
@@ -382,9 +419,10 @@ constexpr size_t kGemvSmem = 128 + size_t(GV_STAGES) * GV_STAGE_BYTES + sizeof(G
 }  // namespace
 
 cudaError_t launch_fp8_gemv(const GemvOperands& routed, const GemvOperands* shared, const int32_t* offsets,
-                            int num_routed, int shared_rows, long long routed_rows, bool gemm1, bool x_from_prev,
-                            int* status, cudaStream_t stream, int* launches) {
+                            int num_routed, int shared_rows, int max_rows, long long routed_rows, bool gemm1,
+                            bool x_from_prev, int* status, cudaStream_t stream, int* launches) {
   if (num_routed < 1 || num_routed > GV_MAX_GROUPS || offsets == nullptr) return cudaErrorInvalidValue;
+  if (max_rows < 1 || max_rows > GEMV_MAX_ROWS || shared_rows > max_rows) return cudaErrorInvalidValue;
   if ((shared == nullptr) != (shared_rows <= 0) || shared_rows > GEMV_MAX_ROWS) return cudaErrorInvalidValue;
   GemvParams p;
   memset(&p, 0, sizeof(p));
@@ -426,6 +464,7 @@ cudaError_t launch_fp8_gemv(const GemvOperands& routed, const GemvOperands* shar
   p.offsets = offsets;
   p.num_routed = num_routed;
   p.shared_rows = shared != nullptr ? shared_rows : 0;
+  p.max_rows = max_rows;
   p.routed_rows = routed_rows;
   p.gemm1 = gemm1 ? 1 : 0;
   p.x_from_prev = x_from_prev ? 1 : 0;
@@ -434,10 +473,19 @@ cudaError_t launch_fp8_gemv(const GemvOperands& routed, const GemvOperands* shar
   int ok = 0;
   cudaError_t e = attr.get(&ok, [](int* v) {
     *v = 1;
-    return cudaFuncSetAttribute(gemv_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kGemvSmem));
+    cudaError_t err = cudaFuncSetAttribute(gemv_fp8_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           int(kGemvSmem));
+    if (err == cudaSuccess)
+      err = cudaFuncSetAttribute(gemv_fp8_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kGemvSmem));
+    if (err == cudaSuccess)
+      err = cudaFuncSetAttribute(gemv_fp8_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kGemvSmem));
+    return err;
   });
   if (e != cudaSuccess) return e;
-  e = launch_pdl(gemv_fp8_kernel, dim3(num_sms()), dim3(GV_THREADS), kGemvSmem, stream, p);
+  const int maxr = max_rows <= 1 ? 1 : (max_rows <= 2 ? 2 : 4);
+  if (maxr == 1) e = launch_pdl(gemv_fp8_kernel<1>, dim3(num_sms()), dim3(GV_THREADS), kGemvSmem, stream, p);
+  else if (maxr == 2) e = launch_pdl(gemv_fp8_kernel<2>, dim3(num_sms()), dim3(GV_THREADS), kGemvSmem, stream, p);
+  else e = launch_pdl(gemv_fp8_kernel<4>, dim3(num_sms()), dim3(GV_THREADS), kGemvSmem, stream, p);
   if (e == cudaSuccess && launches) ++*launches;
   return e;
 }

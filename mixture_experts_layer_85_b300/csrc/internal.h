@@ -161,8 +161,10 @@ cudaError_t launch_pair_experts(const PairClass cls[4], const int32_t* offsets, 
 // GEMM2 (fp32 rows [rows, M]).  w: FP8 stage images of groups of M rows and K
 // columns; x: token rows, K 2-byte values each (x_f16: f16, else bf16).  The
 // routed class's groups take rows offsets[g] .. offsets[g+1] (all below
-// routed_rows); the shared class, rows 0 .. shared_rows.  x_from_prev: every
-// item's token rows come from the preceding grid (else only the routed ones).
+// routed_rows); the shared class, rows 0 .. shared_rows; no group holds more
+// than max_rows (<= GEMV_MAX_ROWS; a group that does is flagged and skipped).
+// x_from_prev: every item's token rows come from the preceding grid (else
+// only the routed ones).
 constexpr int GEMV_MAX_ROWS = 4;
 struct GemvOperands {
   const void* w = nullptr;
@@ -173,8 +175,8 @@ struct GemvOperands {
   int M = 0, K = 0;
 };
 cudaError_t launch_fp8_gemv(const GemvOperands& routed, const GemvOperands* shared, const int32_t* offsets,
-                            int num_routed, int shared_rows, long long routed_rows, bool gemm1, bool x_from_prev,
-                            int* status, cudaStream_t stream, int* launches);
+                            int num_routed, int shared_rows, int max_rows, long long routed_rows, bool gemm1,
+                            bool x_from_prev, int* status, cudaStream_t stream, int* launches);
 
 // Fault injection for tests of the device-side time-out path
 // (moe_debug_inject): the expert kernel's wait limit for later launches

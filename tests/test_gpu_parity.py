@@ -580,7 +580,7 @@ def test_fp8_layer_matches_oracle_on_dequantized_weights(name):
     assert orc.relative_error(f64(out)[toks], want) <= TOL["bf16"]
 
 
-@pytest.mark.parametrize("name", ["v3_decode_t1", "v3_decode_t64"])
+@pytest.mark.parametrize("name", ["v3_decode_t1", "v3_decode_t8", "v3_decode_t64"])
 def test_fp8_full_size_decode(name):
     wl = _fp8_copy(W[name])
     li = inputs.make_inputs(wl, "cuda")

@@ -380,10 +380,11 @@ def needs_flush(wl) -> bool:
     return wl.T <= 512
 
 
-def time_steps(layer, x, out, counts, K, flush=None, stream=None):
+def time_steps(layer, x, out, counts, K, flush=None, stream=None, per_step=None):
     """Average ms of one layer step over K timed steps (CUDA events on the
     stream).  With `flush`, L2 is flushed before every step and each step is
-    timed on its own, the flush outside the events."""
+    timed on its own, the flush outside the events (their times are appended
+    to `per_step` when given)."""
     stream = stream or torch.cuda.current_stream()
     if flush is None:
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -400,7 +401,10 @@ def time_steps(layer, x, out, counts, K, flush=None, stream=None):
         layer.forward(x, out, counts=counts)
         b.record(stream)
     torch.cuda.synchronize()
-    return sum(a.elapsed_time(b) for a, b in evs) / K
+    times = [a.elapsed_time(b) for a, b in evs]
+    if per_step is not None:
+        per_step.extend(times)
+    return sum(times) / K
 
 
 def stage_times(layer, x, out, counts, n, flush=None):
@@ -533,7 +537,8 @@ def per_config_lines(base_layer, base_li, dev, K, W, peaks, with_oracle):
         clocks = ClockSampler()
         clocks.start()
         t0 = time.time()
-        ms = time_steps(layer, x, out, counts, K, fl)
+        steps_ms = []
+        ms = time_steps(layer, x, out, counts, K, fl, per_step=steps_ms)
         clk = clocks.stop(t0, time.time())
         st = stage_times(layer, x, out, counts, max(3, min(K, 10)), fl)
         code, word = layer.device_status()
@@ -546,6 +551,8 @@ def per_config_lines(base_layer, base_li, dev, K, W, peaks, with_oracle):
                       if fl else "no flush: weights larger than L2",
                 **layer_summary(wl, ms, cnt, peaks), "stage_ms": {k: round(v, 4) for k, v in st.items()},
                 "roofline": expert_roofline(wl, cnt, st["experts"], peaks), "clocks": clk}
+        if steps_ms:
+            line["ms_per_step_median"] = round(statistics.median(steps_ms), 4)
         if with_oracle:
             line["oracle"] = oracle_rate(wl, li, oracle_sample_size(wl, 0))
         res[name] = line
@@ -599,7 +606,8 @@ def run_ours(args, world, rank):
         torch.cuda.synchronize()
         step_ms = None
     else:
-        step_ms = time_steps(layer, x, out, counts, K, fl, stream)
+        per_step = []
+        step_ms = time_steps(layer, x, out, counts, K, fl, stream, per_step=per_step)
     host_t1 = time.time()
     launches = _lib.moe_launch_count() - launches0
     barrier(world)
@@ -686,6 +694,8 @@ def run_ours(args, world, rank):
         "host_us_per_forward_call": round(host_us, 1),
         "clocks": clk,
     }
+    if step_ms is not None:
+        res["ms_per_step_median"] = round(statistics.median(per_step), 4)
     return res
 
 

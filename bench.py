@@ -432,7 +432,7 @@ def stage_times(layer, x, out, counts, n, flush=None):
 # launches of one forward, one ncu pass on the full-size workload) for the workloads captured with the
 # current kernel source; the summary and the command that made it are in the named profiles/ file.
 EXPERT_TRAFFIC = {
-    "v3_prefill_t16384": (32.49e9, "profiles/expert_dram_v3_prefill_t16384.md"),
+    "v3_prefill_t16384": (32.03e9, "profiles/launches_v3_prefill_t16384.md"),
 }
 
 

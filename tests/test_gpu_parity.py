@@ -283,6 +283,23 @@ def test_forward_equals_staged_calls():
     assert torch.equal(out, o["out"])
 
 
+@pytest.mark.parametrize("name", ["v3_small_t3", "v3_small_t333"])
+def test_fp8_forward_equals_staged_calls(name):
+    """FP8 weights through the staged calls: moe_grouped_swiglu converts the
+    caller's bf16 x_perm to the f16 rows the FP8 expert kernels take (the
+    CUDA-core kernel at T=3, the tensor-core kernel at T=333), and the outputs
+    equal moe_forward's bit for bit."""
+    wl = _fp8_copy(SMALL[name])
+    li = inputs.make_inputs(wl, "cuda")
+    layer = MoELayer(wl, li, "cuda")
+    out = layer.forward(li.x)
+    assert layer.device_status()[0] == _lib.MOE_OK
+    o = layer.forward_staged(li.x)
+    torch.cuda.synchronize()
+    assert layer.device_status()[0] == _lib.MOE_OK
+    assert torch.equal(out, o["out"])
+
+
 def test_deterministic_across_runs():
     wl = SMALL["v2_small_t515"]
     li = inputs.make_inputs(wl, "cuda")

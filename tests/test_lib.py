@@ -26,8 +26,9 @@ def test_exports_every_declared_symbol():
 
 
 def test_status_strings():
-    for code in range(7):
+    for code in range(8):
         assert _lib.moe_status_string(code).startswith("MOE_")
+    assert _lib.moe_status_string(_lib.MOE_ERR_DEVICE_RANGE) == "MOE_ERR_DEVICE_RANGE"
     assert _lib.moe_status_string(99) == "MOE_ERR_UNKNOWN"
 
 

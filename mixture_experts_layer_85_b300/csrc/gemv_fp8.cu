@@ -5,13 +5,13 @@
 // multiply (an MMA of N = 16 for one token) and the FP8 tensor-core path pays
 // a per-stage hand-off (converter warps -> MMA -> freed buffer) that caps it
 // well below the HBM rate.  Here each CTA streams whole stage images (128
-// weight rows x 128 columns of e4m3 plus their block exponents, one bulk copy)
-// and the token rows' 128 matching values through a ring of shared-memory
-// stages, and every weight is used straight from the image: e4m3 -> f16
-// (exact), times the token values as f16 with an fp32 result (fma.f32.f16:
-// exact products, 4 + 11 significant bits), summed in fp32 per 16-column
-// chunk, times the block's 2^e (exact) and added to the row's fp32
-// accumulator.  The expert FFN is w2(silu(w1 x) * w3 x)
+// weight rows x 128 columns of e4m3 plus their block exponents, one 2-D TMA
+// box) and the token rows' 128 matching values (bulk copies) through a ring of
+// shared-memory stages, and every weight is used straight from the image:
+// e4m3 -> f16 (exact), times the token values as f16 (the shared expert's bf16
+// x rounded to f16) with an fp32 result (fma.f32.f16: exact products, 4 + 11
+// significant bits), summed in fp32 per 16-column chunk, times the block's 2^e
+// (exact) and added to the row's fp32 accumulator.  The expert FFN is w2(silu(w1 x) * w3 x)
 // (intelliparadigm.com page, section 3.3.1) with the FP8 block quantisation of
 // its section 4; two launches: GEMM1 with the SwiGLU epilogue (f16 hidden
 // rows), then GEMM2 (fp32 rows).

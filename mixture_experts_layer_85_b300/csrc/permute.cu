@@ -252,37 +252,50 @@ __device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v, bool& over) {
   return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+// seg warps share a token's row (seg > 1 for small batches, so that more
+// than one warp's loads are in flight per row).
 __global__ void __launch_bounds__(256) gather_tokens_kernel(const uint4* __restrict__ x,
                                                             const int32_t* __restrict__ tok2row, int T, int k,
                                                             long long R, int vec_per_row, uint4* __restrict__ x_perm,
-                                                            int to_f16, int* status) {
+                                                            int to_f16, int seg, int* status) {
   pdl_launch_dependents();
   pdl_wait();
   const int lane = threadIdx.x & 31;
   bool over = false;
   const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
-  for (long long t = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < T; t += warps) {
+  const int per = (vec_per_row + seg - 1) / seg;
+  for (long long item = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); item < (long long)T * seg;
+       item += warps) {
+    const long long t = item / seg;
+    const int sg = int(item % seg);
+    const int v_begin = sg * per, v_end = min(vec_per_row, v_begin + per);
     const int32_t* rows = tok2row + t * k;
     const uint4* src = x + t * vec_per_row;
-    for (int v0 = 0; v0 < vec_per_row; v0 += 32 * GATHER_CHUNK) {
+    for (int v0 = v_begin; v0 < v_end; v0 += 32 * GATHER_CHUNK) {
       uint4 buf[GATHER_CHUNK];
 #pragma unroll
       for (int i = 0; i < GATHER_CHUNK; ++i) {
         const int v = v0 + i * 32 + lane;
-        if (v < vec_per_row) buf[i] = to_f16 ? bf16x8_to_f16x8(src[v], over) : src[v];
+        if (v < v_end) buf[i] = src[v];
+      }
+      if (to_f16) {
+        // after all the chunk's loads are in flight
+#pragma unroll
+        for (int i = 0; i < GATHER_CHUNK; ++i)
+          if (v0 + i * 32 + lane < v_end) buf[i] = bf16x8_to_f16x8(buf[i], over);
       }
       for (int j = 0; j < k; ++j) {
         const long long r = rows[j];   // warp-uniform, cached after the first chunk
         if (r < 0) continue;           // an expert index the dispatch already flagged
         if (r >= R) {
-          if (lane == 0 && v0 == 0) flag_status(status, DEV_BAD_ROW);
+          if (lane == 0 && v0 == v_begin && sg == 0) flag_status(status, DEV_BAD_ROW);
           continue;
         }
         uint4* dst = x_perm + r * vec_per_row;
 #pragma unroll
         for (int i = 0; i < GATHER_CHUNK; ++i) {
           const int v = v0 + i * 32 + lane;
-          if (v < vec_per_row) dst[v] = buf[i];
+          if (v < v_end) dst[v] = buf[i];
         }
       }
     }
@@ -310,7 +323,7 @@ cudaError_t launch_gather_rows(const void* x, const int32_t* tok2row, int T, int
   const long long cap = 8LL * num_sms();
   if (blocks > cap) blocks = cap;
   cudaError_t e = launch_pdl(gather_tokens_kernel, dim3((int)blocks), dim3(256), 0, s, static_cast<const uint4*>(x),
-                             tok2row, T, k, rows, int(row_bytes / 16), static_cast<uint4*>(x_perm), 0, status);
+                             tok2row, T, k, rows, int(row_bytes / 16), static_cast<uint4*>(x_perm), 0, 1, status);
   if (launches) ++*launches;
   return e;
 }
@@ -356,11 +369,13 @@ cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* id
   if (x == nullptr || x_perm == nullptr) return cudaSuccess;
   const long long R = (long long)c.T * c.k;
   const int vec = int((size_t)c.d * dtype_bytes(c.act_dtype) / 16);
-  long long blocks = (c.T + 7) / 8;
+  // small batches: the 8 warps of a block share each token's row
+  const int seg = c.T <= 64 ? 8 : 1;
+  long long blocks = ((long long)c.T * seg + 7) / 8;
   const long long cap = 8LL * num_sms();
   if (blocks > cap) blocks = cap;
   cudaError_t e = launch_pdl(gather_tokens_kernel, dim3((int)blocks), dim3(256), 0, s, static_cast<const uint4*>(x),
-                             tok2row, c.T, c.k, R, vec, static_cast<uint4*>(x_perm), x_perm_f16 ? 1 : 0, status);
+                             tok2row, c.T, c.k, R, vec, static_cast<uint4*>(x_perm), x_perm_f16 ? 1 : 0, seg, status);
   if (launches) ++*launches;
   return e;
 }

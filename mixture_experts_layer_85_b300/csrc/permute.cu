@@ -233,6 +233,79 @@ __global__ void __launch_bounds__(SMALL_BLOCK) permute_small_kernel(const int32_
   }
 }
 
+// The same tables for batches of at most TINY_T tokens, by one warp: counts
+// with shared-memory atomics, a warp scan for the offsets, then the ranks in
+// token order (a running row per expert; equal experts within one token, which
+// valid input does not have, are ordered by slot).  A one-token step pays a few
+// warp instructions instead of the one-block kernel's passes over 1024 threads.
+constexpr int TINY_T = 32;
+__global__ void __launch_bounds__(32) permute_tiny_kernel(const int32_t* __restrict__ idx, int T, int E, int k,
+                                                          int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                                                          int32_t* __restrict__ row2tok,
+                                                          int32_t* __restrict__ tok2row, int* status) {
+  pdl_launch_dependents();
+  pdl_wait();
+  __shared__ int cnt[MAX_E];
+  __shared__ int run[MAX_E];
+  const int lane = threadIdx.x;
+  const long long R = (long long)T * k;
+  for (int e = lane; e < E; e += 32) cnt[e] = 0;
+  __syncwarp();
+  for (int a = lane; a < T * k; a += 32) {
+    const int e = idx[a];
+    if (e < 0 || e >= E) flag_status(status, DEV_BAD_EXPERT);
+    else atomicAdd(&cnt[e], 1);
+  }
+  __syncwarp();
+  // exclusive scan over the experts: each lane sums a contiguous run of them
+  const int per = (E + 31) / 32;
+  const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
+  int mine = 0;
+  for (int e = e0; e < e1; ++e) mine += cnt[e];
+  int incl = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  int ex = incl - mine;
+  for (int e = e0; e < e1; ++e) {
+    counts[e] = cnt[e];
+    offsets[e] = ex;
+    run[e] = ex;
+    ex += cnt[e];
+  }
+  if (lane == 31) offsets[E] = incl;
+  __syncwarp();
+  // rows in token order; slot order among equal experts of one token
+  for (int t = 0; t < T; ++t) {
+    for (int j0 = 0; j0 < k; j0 += 32) {
+      const int j = j0 + lane;
+      const bool act = j < k;
+      const int e = act ? idx[(long long)t * k + j] : -1;
+      const bool ok = act && e >= 0 && e < E;
+      const unsigned m = __match_any_sync(0xffffffffu, ok ? e : -1);
+      if (ok) {
+        const long long row = (long long)run[e] + __popc(m & ((1u << lane) - 1u));
+        if (row < 0 || row >= R) {
+          flag_status(status, DEV_BAD_ROW);
+          tok2row[(long long)t * k + j] = -1;
+        } else {
+          row2tok[row] = t;
+          tok2row[(long long)t * k + j] = (int32_t)row;
+        }
+      } else if (act) {
+        tok2row[(long long)t * k + j] = -1;
+      }
+      __syncwarp();
+      // the lowest lane of each group of equal experts advances its run
+      if (ok && (m & ((1u << lane) - 1u)) == 0u) run[e] += __popc(m);
+      __syncwarp();
+    }
+  }
+}
+
+
 // x_perm[tok2row[t][j]] = x[t] for every slot j: one warp per token reads the
 // row once (chunks of 8 vectors per lane) and stores it k times, so x streams
 // from memory once and the k copies are plain writes.
@@ -348,7 +421,12 @@ cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* id
                            int32_t* chunk_counts, int32_t* chunk_base, int* status, cudaStream_t s,
                            int* launches, bool x_perm_f16) {
   const int nch = permute_chunks(c.T);
-  if (c.T <= SMALL_T) {
+  if (c.T <= TINY_T && c.E <= MAX_E) {
+    cudaError_t e = launch_pdl(permute_tiny_kernel, dim3(1), dim3(32), 0, s, idx, c.T, c.E, c.k, counts, offsets,
+                               row2tok, tok2row, status);
+    if (launches) *launches += 1;
+    if (e != cudaSuccess) return e;
+  } else if (c.T <= SMALL_T) {
     cudaError_t e = launch_pdl(permute_small_kernel, dim3(1), dim3(SMALL_BLOCK), 0, s, idx, c.T, c.E, c.k, counts,
                                offsets, row2tok, tok2row, status);
     if (launches) *launches += 1;

@@ -327,7 +327,8 @@ def test_gate_topk_full_size(name):
     print(name, {"near_tie_tokens": n_near, "near_tie_differ": n_differ})
 
 
-@pytest.mark.parametrize("T,E,k,one_hot", [(1, 256, 8, None), (5, 12, 4, None), (128, 64, 6, None),
+@pytest.mark.parametrize("T,E,k,one_hot", [(1, 256, 8, None), (5, 12, 4, None), (17, 160, 6, 0),
+                                           (32, 256, 8, None), (33, 256, 8, None), (128, 64, 6, None),
                                            (129, 64, 6, None), (4133, 256, 8, None), (300, 16, 1, 3),
                                            (777, 160, 6, 0)])
 def test_permute_bit_exact(T, E, k, one_hot):
@@ -348,6 +349,44 @@ def test_permute_bit_exact(T, E, k, one_hot):
     assert np.array_equal(_np(dev["row2tok"]), row2tok)
     assert np.array_equal(_np(dev["tok2row"]), tok2row)
     assert torch.equal(x_perm.cpu(), x[torch.from_numpy(row2tok)])
+
+
+@pytest.mark.parametrize("T", [3, 100, 5000])
+def test_permute_flags_out_of_range_expert(T):
+    """An expert index outside [0, E) sets MOE_ERR_DEVICE_BOUNDS; that slot gets
+    row -1 and no row, and the valid slots still form a dispatch of their own
+    (one row each, grouped by expert in token order)."""
+    E, k = 64, 6
+    wl = inputs.small_workload(W["v2lite_t4096"], name="perm_bad", T=T, d=128, E=E, I=128, k=k)
+    cfg = _lib.make_config(wl)
+    idx = inputs.random_idx(T, E, k, seed=T, one_hot_expert=None)
+    bad = [(0, 2, E), (T - 1, k - 1, -1)]
+    for t, j, e in bad:
+        idx[t, j] = e
+    x = inputs.random_rows(T, wl.d, seed=T)
+    ws = torch.empty(_lib.moe_workspace_size(cfg), dtype=torch.uint8, device="cuda")
+    dev = {n: torch.full(s, -7, dtype=torch.int32, device="cuda") for n, s in
+           [("counts", (E,)), ("offsets", (E + 1,)), ("row2tok", (T * k,)), ("tok2row", (T, k))]}
+    x_perm = torch.zeros((T * k, wl.d), dtype=torch.bfloat16, device="cuda")
+    _lib.moe_permute(cfg, x.cuda(), idx.cuda(), dev["counts"], dev["offsets"], dev["row2tok"], dev["tok2row"],
+                     x_perm, ws)
+    assert _lib.moe_get_device_status(ws)[0] == _lib.MOE_ERR_DEVICE_BOUNDS
+    ix = idx.numpy()
+    ok = (ix >= 0) & (ix < E)
+    tok2row = _np(dev["tok2row"])
+    assert (tok2row[~ok] == -1).all()
+    assert np.array_equal(_np(dev["counts"]), np.bincount(ix[ok], minlength=E))
+    n_rows = int(ok.sum())
+    assert _np(dev["offsets"])[E] == n_rows
+    rows = tok2row[ok]
+    assert np.array_equal(np.sort(rows), np.arange(n_rows))
+    row2tok = _np(dev["row2tok"])
+    tt = np.nonzero(ok)[0]
+    assert np.array_equal(row2tok[rows], tt)
+    # grouped by expert, token order within an expert
+    order = np.lexsort((tt, ix[ok]))
+    assert np.array_equal(rows[order], np.arange(n_rows))
+    assert torch.equal(x_perm.cpu()[torch.from_numpy(rows).long()], x[torch.from_numpy(tt)])
 
 
 @pytest.mark.parametrize("name,seed", [("v3_small_t333", 1), ("v2lite_small_t1037", 2), ("v3_small_t1", 3)])

@@ -108,11 +108,12 @@ typedef struct moe_config {
                               values round to multiples of 2^-24, larger ones
                               set MOE_ERR_DEVICE_RANGE); the shared expert's
                               first GEMM reads x as bf16 and dequantizes its
-                              weights to bf16 (exact).  Batches of at most 4
-                              tokens run on the CUDA cores instead: e4m3 -> f16
-                              weights times f16 token values (the shared
-                              expert's too) with exact fp32 products, fp32
-                              sums, then 2^e per 64-weight block. */
+                              weights to bf16 (exact).  Batches of at most 8
+                              tokens run as a GEMV with warp-level MMAs
+                              instead: e4m3 -> f16 weights times f16 token
+                              values (the shared expert's too), exact
+                              products summed in fp32 per 64-weight block,
+                              then 2^e per block. */
 } moe_config;
 
 /* Bytes of workspace every compute call needs for `cfg`. */

@@ -242,7 +242,7 @@ moe_status run_experts(const moe_config& c, const void* x_perm, const int32_t* o
   const long long tiles2 = (tb_routed + tb_shared) * ((c.d + 255) / 256);
   const int shared_rows = Is > 0 ? c.T : 0;
   if (P.fp8 && c.T <= GEMV_MAX_ROWS) {
-    // decode batches of FP8 experts: CUDA-core GEMV (a group holds at most T rows)
+    // decode batches of FP8 experts: GEMV with warp-level MMAs (a group holds at most T rows)
     GemvOperands g1, g1s, g2, g2s;
     g1.w = pb + P.w13; g1.x = x_perm; g1.x_f16 = true; g1.out = h; g1.out_ld = c.I; g1.M = 2 * c.I; g1.K = c.d;
     g1s.w = pb + P.w13s; g1s.x = x; g1s.x_f16 = false; g1s.out = hs; g1s.out_ld = Is; g1s.M = int(2 * Is);

@@ -1,27 +1,31 @@
 // Expert FFNs with FP8 weights for decode batches (every group at most
-// GEMV_MAX_ROWS token rows): CUDA-core GEMV over the packed FP8 stage images.
+// GEMV_MAX_ROWS token rows): a GEMV over the packed FP8 stage images whose dot
+// products run as warp-level MMAs.
 //
-// At a handful of tokens per expert the tensor cores have almost nothing to
-// multiply (an MMA of N = 16 for one token) and the FP8 tensor-core path pays
-// a per-stage hand-off (converter warps -> MMA -> freed buffer) that caps it
-// well below the HBM rate.  Here each CTA streams whole stage images (128
-// weight rows x 128 columns of e4m3 plus their block exponents, one 2-D TMA
-// box) and the token rows' 128 matching values (bulk copies) through a ring of
-// shared-memory stages, and every weight is used straight from the image:
-// e4m3 -> f16 (exact), times the token values as f16 (the shared expert's bf16
-// x rounded to f16) with an fp32 result (fma.f32.f16: exact products, 4 + 11
-// significant bits), summed in fp32 per 16-column chunk, times the block's 2^e
-// (exact) and added to the row's fp32 accumulator.  The expert FFN is w2(silu(w1 x) * w3 x)
-// (intelliparadigm.com page, section 3.3.1) with the FP8 block quantisation of
-// its section 4; two launches: GEMM1 with the SwiGLU epilogue (f16 hidden
-// rows), then GEMM2 (fp32 rows).
+// At a handful of tokens per expert the op is a matrix-vector product bound
+// by the weight stream.  The tcgen05 FP8 path pays a per-stage hand-off
+// (converter warps of two CTAs -> one MMA issuer -> freed buffer) that caps it
+// well below the HBM rate, and FMAs on the CUDA cores cost one instruction per
+// weight and token.  Here each CTA streams whole stage images (128 weight rows
+// x 128 columns of e4m3 plus their block exponents, one 2-D TMA box) and the
+// token rows' 128 matching values (bulk copies) through a ring of shared-memory
+// stages; every warp turns its 16 x 64 piece of a stage into f16 (e4m3 -> f16
+// is exact) and multiplies it by the token values (f16; the shared expert's
+// bf16 x rounded to f16) with four m16n8k16 MMAs, the up to 8 token rows being
+// the 8 columns of B.  Products of f16 values are exact and the MMA sums them
+// in fp32; each 64-column partial times its block's 2^e (exact) is added to
+// the fp32 accumulator.  One MMA serves 1 to 8 tokens at the same cost, so the
+// instruction count per weight no longer grows with the batch.  The expert
+// FFN is w2(silu(w1 x) * w3 x) (intelliparadigm.com page, section 3.3.1) with
+// the FP8 block quantisation of its section 4; two launches: GEMM1 with the
+// SwiGLU epilogue (f16 hidden rows), then GEMM2 (fp32 rows).
 //
 // Work items are (group, 128-row weight tile), the shared expert's first:
 // their token rows do not depend on the dispatch, so in the GEMM1 launch they
 // stream while the preceding kernels still run; the routed groups' items wait
 // for the dispatch (griddepcontrol.wait), after which the producer warp lists
 // the groups that received rows.  CTA b takes items b, b + G, b + 2G, ...
-// (one CTA per SM, a ring of 12 stages: 221 KB of weights and token values in
+// (one CTA per SM, a ring of 11 stages: 215 KB of weights and token values in
 // flight per SM).  Every wait is bounded; a CTA that gives up flags the status
 // word and its roles leave without waiting on each other.
 #include <cuda_fp16.h>
@@ -33,14 +37,14 @@
 namespace moe {
 namespace {
 
-constexpr int GV_WARPS = 16;                         // compute warps
-constexpr int GV_RPT = 2;                            // weight rows per compute thread
+constexpr int GV_WARPS = 16;                         // compute warps: 8 row tiles x 2 k-blocks of a stage
 constexpr int GV_THREADS = 32 * (GV_WARPS + 1);      // plus the producer warp
-constexpr int GV_STAGES = 12;
+constexpr int GV_STAGES = 11;
 constexpr int GV_XBYTES = 128 * 2;                   // one token row's 128 values of a stage (2-byte types)
-constexpr int GV_STAGE_BYTES = FP8_STAGE_BYTES + GEMV_MAX_ROWS * GV_XBYTES;
+constexpr int GV_XSTRIDE = GV_XBYTES + 16;           // token rows 16 bytes apart in the banks
+constexpr int GV_STAGE_BYTES = FP8_STAGE_BYTES + GEMV_MAX_ROWS * GV_XSTRIDE;
 constexpr int GV_MAX_GROUPS = 272;
-static_assert(GV_STAGE_BYTES % 128 == 0 && GV_RPT == 2, "stage alignment; the float2 row stores");
+static_assert(GV_STAGE_BYTES % 128 == 0 && GEMV_MAX_ROWS == 8, "stage alignment; one MMA column per token row");
 
 struct GemvClass {
   const uint8_t* w;    // stage images: tiles of 128 rows, nst stages each; group g's first tile is g * tpg
@@ -62,7 +66,7 @@ struct GemvParams {
   const int32_t* offsets;   // [num_routed + 1] routed rows of each group
   int num_routed;
   int shared_rows;          // 0: no shared expert
-  int max_rows;             // bound of every group's token rows (the kernel's MAXR or less)
+  int max_rows;             // bound of every group's token rows (GEMV_MAX_ROWS or less)
   long long routed_rows;    // bound of every routed row index
   int gemm1;                // 1: SwiGLU epilogue, 0: fp32 rows
   int x_from_prev;          // 1: every item's token rows come from the preceding grid
@@ -73,12 +77,12 @@ struct GemvCtrl {
   uint64_t full[GV_STAGES];    // a stage's image and token values landed
   uint64_t empty[GV_STAGES];   // every compute warp finished with a stage
   uint64_t list_ready;         // the active-group list is built
-  uint64_t sums_full;          // GEMM1: every compute warp wrote its rows' sums
-  uint64_t sums_free;          // GEMM1: every compute warp read the sums
+  uint64_t sums_full;          // every compute warp wrote its rows' sums
+  uint64_t sums_free;          // every compute warp read the sums
   int abort;
   int n_active;
   int active[GV_MAX_GROUPS];
-  float sums[128][GEMV_MAX_ROWS];   // GEMM1: the tile's row sums, for the SwiGLU pairing
+  float sums[2][128][GEMV_MAX_ROWS];   // the tile's row sums of each k-block half, [half][row][token]
 };
 
 // Bounded wait with a short sleep between polls, the give-up rule of mbar_wait:
@@ -180,7 +184,7 @@ __device__ void gemv_producer(const GemvParams& p, GemvCtrl* c, uint8_t* ring, i
         mbar_arrive_expect_tx(&c->full[s], bytes);
         tma_load_2d(st, &p.tm[it.cls], &c->full[s], 0, (it.tile_w * k.nst + ks) * GV_IMG_ROWS);
         for (int t = 0; t < it.rows; ++t)
-          bulk_load(st + FP8_STAGE_BYTES + t * GV_XBYTES,
+          bulk_load(st + FP8_STAGE_BYTES + t * GV_XSTRIDE,
                     k.x + ((it.row0 + t) * (long long)k.K + (long long)ks * 128) * 2, GV_XBYTES, &c->full[s]);
         used |= 1u << s;
         used_par = (used_par & ~(1u << s)) | (ph << s);
@@ -237,17 +241,17 @@ __device__ __forceinline__ void x16_to_f16x2(const uint8_t* src, bool f16, uint3
   }
 }
 
-// acc + lo(w) * lo(x) + hi(w) * hi(x): f16 operands, products exact in fp32
-// (11 + 11 significant bits), fp32 sums.
-__device__ __forceinline__ float fma_f16x2_f32(uint32_t w, uint32_t x, float acc) {
-  asm("{\n\t.reg .f16 wl, wh, xl, xh;\n\t"
-      "mov.b32 {wl, wh}, %1;\n\t"
-      "mov.b32 {xl, xh}, %2;\n\t"
-      "fma.rn.f32.f16 %0, wl, xl, %0;\n\t"
-      "fma.rn.f32.f16 %0, wh, xh, %0;\n\t}"
-      : "+f"(acc)
-      : "r"(w), "r"(x));
-  return acc;
+// D += A B for one m16n8k16 tile: f16 operands (A row-major 16 x 16, B
+// column-major 16 x 8), fp32 accumulators.  Lane (g, t) = (lane / 4, lane % 4)
+// holds A rows g and g + 8 at columns 2t, 2t + 1 (a0, a1) and 2t + 8, 2t + 9
+// (a2, a3), B column g at rows 2t, 2t + 1 (b0) and 2t + 8, 2t + 9 (b1), and D
+// rows g (d0, d1) and g + 8 (d2, d3) at columns 2t, 2t + 1.
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                          uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
 // 2^e as a float (exact; normal range directly).
@@ -257,54 +261,67 @@ __device__ __forceinline__ float pow2f(int e) {
 
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + __expf(-z)); }
 
-// One stage of a thread's dot products: rows GV_RPT rg .. (+ GV_RPT - 1),
-// columns 16 ch .. 16 ch + 15, token rows t < rows; adds 2^e times each row's
-// partial sum into acc.
-template <int MAXR>
-__device__ __forceinline__ void gemv_stage(const uint8_t* st, int rg, int ch, int rows, bool f16,
-                                           float (&acc)[GV_RPT][MAXR]) {
-  const int h = ch >> 2;
-  uint32_t xv[MAXR][8];
+// Weight row of MMA row g (0..7) within a 16-row tile; MMA row g + 8 takes the
+// row 8 below.  Lanes 8q .. 8q + 7 of a warp (MMA rows 2q, 2q + 1) then read
+// rows whose 128-byte swizzle phases differ by 4, so their 16-byte chunks of a
+// k-block land in different banks.
+__device__ __forceinline__ int gv_tile_row(int g) { return (g >> 1) + 4 * (g & 1); }
+
+// One stage of a warp's products: weight rows r0 = 16 rt + gv_tile_row(g) and
+// r0 + 8 (MMA rows g and g + 8), the 64 columns of k-block kh, and the group's
+// token rows as the 8 columns of B (zero beyond `rows`).  Lane (g, t) reads
+// 16-byte chunk 4 kh + t of both weight rows and the same 16 columns of token
+// row g.  The MMAs take the 64 columns in a permuted order, the same for A and
+// B (step s, MMA column slot j of thread t <- column 16 t + 4 s + j), so each
+// thread's operands are contiguous in shared memory.  Each row's 64-column sum
+// times 2^e of its block is added into acc (d0, d1: row r0; d2, d3: row r0 + 8;
+// tokens 2t and 2t + 1).
+__device__ __forceinline__ void gemv_stage(const uint8_t* st, int r0, int kh, int g, int t, int rows, bool f16,
+                                           float (&acc)[4]) {
+  const int r1 = r0 + 8;
+  const int c = kh * 4 + t;
+  const uint4 q0 = *reinterpret_cast<const uint4*>(st + r0 * 128 + ((c ^ (r0 & 7)) << 4));
+  const uint4 q1 = *reinterpret_cast<const uint4*>(st + r1 * 128 + ((c ^ (r1 & 7)) << 4));
+  const int32_t* ex = reinterpret_cast<const int32_t*>(st + FP8_IMAGE_BYTES) + kh * 128;
+  const float s0 = pow2f(ex[r0]), s1 = pow2f(ex[r1]);
+  uint32_t xv[8];
+  if (g < rows) {
+    x16_to_f16x2(st + FP8_STAGE_BYTES + g * GV_XSTRIDE + c * 32, f16, xv);
+  } else {
 #pragma unroll
-  for (int t = 0; t < MAXR; ++t)
-    if (t < rows) x16_to_f16x2(st + FP8_STAGE_BYTES + t * GV_XBYTES + ch * 32, f16, xv[t]);
-#pragma unroll
-  for (int r = 0; r < GV_RPT; ++r) {
-    const int row = rg * GV_RPT + r;
-    const uint4 q = *reinterpret_cast<const uint4*>(st + row * 128 + ((ch ^ (row & 7)) << 4));
-    const float sc = pow2f(reinterpret_cast<const int32_t*>(st + FP8_IMAGE_BYTES)[h * 128 + row]);
-    uint32_t wv[8];
-    e4m3x16_to_f16x2(q, wv);
-#pragma unroll
-    for (int t = 0; t < MAXR; ++t) {
-      if (t < rows) {
-        float p0 = 0.0f, p1 = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 8; i += 2) {
-          p0 = fma_f16x2_f32(wv[i], xv[t][i], p0);
-          p1 = fma_f16x2_f32(wv[i + 1], xv[t][i + 1], p1);
-        }
-        acc[r][t] = fmaf(p0 + p1, sc, acc[r][t]);
-      }
-    }
+    for (int i = 0; i < 8; ++i) xv[i] = 0u;
   }
+  uint32_t w0[8], w1[8];
+  e4m3x16_to_f16x2(q0, w0);
+  e4m3x16_to_f16x2(q1, w1);
+  float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+  for (int st4 = 0; st4 < 4; ++st4)
+    mma_16816(d, w0[2 * st4], w1[2 * st4], w0[2 * st4 + 1], w1[2 * st4 + 1], xv[2 * st4], xv[2 * st4 + 1]);
+  acc[0] = fmaf(d[0], s0, acc[0]);
+  acc[1] = fmaf(d[1], s0, acc[1]);
+  acc[2] = fmaf(d[2], s1, acc[2]);
+  acc[3] = fmaf(d[3], s1, acc[3]);
 }
 
-// Compute warps: thread (row group rg, chunk ch) owns weight rows GV_RPT rg ..
-// GV_RPT rg + GV_RPT - 1 of the tile and columns 16 ch .. 16 ch + 15 of every
-// stage; each dot product runs as two independent partial sums (16 warps and
-// short dependency chains keep the FMA pipes fed).  Every lane waits on each
-// barrier itself (bounded) and the warp leaves together when any lane gave up.
-template <int MAXR>
+// Compute warps: warp w multiplies row tile rt = w % 8 (16 weight rows of the
+// item's 128) by k-block kh = w / 8 of every stage, GV_PER stages per wait (more
+// independent MMA chains between synchronisations).  At the item's end the two
+// k-block halves of each row meet in shared memory and every compute thread
+// takes part in the epilogue.  Every lane waits on each barrier itself
+// (bounded) and the warp leaves together when any lane gave up.
+constexpr int GV_PER = 4;
 __device__ void gemv_compute(const GemvParams& p, GemvCtrl* c, uint8_t* ring, int warp, int lane) {
   const int nsh = p.shared_rows > 0 ? p.cls[1].tpg : 0;
   const int G = gridDim.x;
-  const int rg = warp * 4 + (lane >> 3), ch = lane & 7;   // 4 row groups per warp
+  const int rt = warp & 7, kh = warp >> 3;
+  const int g = lane >> 2, t = lane & 3;
+  const int r0 = rt * 16 + gv_tile_row(g);
   const int tid = warp * 32 + lane;
   bool listed = false;
   int s = 0;
   uint32_t ph = 0;
-  uint32_t n1 = 0;   // GEMM1 items done (parity of the sums barriers)
+  uint32_t n1 = 0;   // items done (parity of the sums barriers)
   for (int item = blockIdx.x;; item += G) {
     if (item >= nsh && !listed) {
       if (!__all_sync(0xffffffffu, mbar_wait(&c->list_ready, 0u, &c->abort, p.status))) return;
@@ -314,42 +331,35 @@ __device__ void gemv_compute(const GemvParams& p, GemvCtrl* c, uint8_t* ring, in
     if (!gemv_item(p, c, nsh, item, it)) return;
     const GemvClass& k = p.cls[it.cls];
     const bool f16 = k.x_f16 != 0;
-    float acc[GV_RPT][MAXR];
-#pragma unroll
-    for (int r = 0; r < GV_RPT; ++r)
-#pragma unroll
-      for (int t = 0; t < MAXR; ++t) acc[r][t] = 0.0f;
-    // several stages per wait (more independent work between synchronisations):
-    // four with one token row, two with two; with more rows the registers would spill
-    constexpr int kPer = MAXR == 1 ? 4 : (MAXR == 2 ? 2 : 1);
-    for (int ks = 0; ks < k.nst; ks += kPer) {
-      const int n = min(kPer, k.nst - ks);
-      int si[kPer];
-      uint32_t pi[kPer];
+    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    for (int ks = 0; ks < k.nst; ks += GV_PER) {
+      const int n = min(GV_PER, k.nst - ks);
+      int si[GV_PER];
+      uint32_t pi[GV_PER];
       si[0] = s;
       pi[0] = ph;
 #pragma unroll
-      for (int j = 1; j < kPer; ++j) {
+      for (int j = 1; j < GV_PER; ++j) {
         si[j] = si[j - 1] + 1 == GV_STAGES ? 0 : si[j - 1] + 1;
         pi[j] = si[j - 1] + 1 == GV_STAGES ? pi[j - 1] ^ 1u : pi[j - 1];
       }
       bool got = true;
 #pragma unroll
-      for (int j = 0; j < kPer; ++j)
+      for (int j = 0; j < GV_PER; ++j)
         if (j < n) got = got && mbar_wait_sleep(&c->full[si[j]], pi[j], &c->abort, p.status);
       if (!__all_sync(0xffffffffu, got)) return;
-      if (n == kPer) {
+      if (n == GV_PER) {
 #pragma unroll
-        for (int j = 0; j < kPer; ++j)
-          gemv_stage<MAXR>(ring + size_t(si[j]) * GV_STAGE_BYTES, rg, ch, it.rows, f16, acc);
+        for (int j = 0; j < GV_PER; ++j)
+          gemv_stage(ring + size_t(si[j]) * GV_STAGE_BYTES, r0, kh, g, t, it.rows, f16, acc);
       } else {
         for (int j = 0; j < n; ++j)
-          gemv_stage<MAXR>(ring + size_t(si[j]) * GV_STAGE_BYTES, rg, ch, it.rows, f16, acc);
+          gemv_stage(ring + size_t(si[j]) * GV_STAGE_BYTES, r0, kh, g, t, it.rows, f16, acc);
       }
       __syncwarp();
       if (lane == 0) {
 #pragma unroll
-        for (int j = 0; j < kPer; ++j)
+        for (int j = 0; j < GV_PER; ++j)
           if (j < n) mbar_arrive(&c->empty[si[j]]);
       }
       // advance past the n stages
@@ -360,58 +370,40 @@ __device__ void gemv_compute(const GemvParams& p, GemvCtrl* c, uint8_t* ring, in
         }
       }
     }
-    // the 8 chunk threads of a row group hold partial sums of the same rows
-#pragma unroll
-    for (int r = 0; r < GV_RPT; ++r)
-#pragma unroll
-      for (int t = 0; t < MAXR; ++t) {
-        float v = acc[r][t];
-        v += __shfl_xor_sync(0xffffffffu, v, 1);
-        v += __shfl_xor_sync(0xffffffffu, v, 2);
-        v += __shfl_xor_sync(0xffffffffu, v, 4);
-        acc[r][t] = v;
-      }
-    if (!p.gemm1) {
-      if (ch == 0) {
-        float* out = static_cast<float*>(k.out);
-#pragma unroll
-        for (int t = 0; t < MAXR; ++t)
-          if (t < it.rows)
-            *reinterpret_cast<float2*>(out + (it.row0 + t) * k.out_ld + it.tile * 128 + rg * GV_RPT) =  // GV_RPT = 2
-                make_float2(acc[0][t], acc[1][t]);
-      }
-      continue;
-    }
-    // GEMM1: rows come in blocks of 32 (16 W1 rows of 16 features, then their
-    // W3 rows); pair them through shared memory (bounded barrier waits)
+    // the two k-block halves of every row meet in shared memory (bounded barrier waits)
     if (!__all_sync(0xffffffffu, mbar_wait(&c->sums_free, (n1 & 1u) ^ 1u, &c->abort, p.status))) return;
-    if (ch == 0) {
-#pragma unroll
-      for (int r = 0; r < GV_RPT; ++r)
-#pragma unroll
-        for (int t = 0; t < MAXR; ++t) c->sums[rg * GV_RPT + r][t] = acc[r][t];
-    }
+    *reinterpret_cast<float2*>(&c->sums[kh][r0][2 * t]) = make_float2(acc[0], acc[1]);
+    *reinterpret_cast<float2*>(&c->sums[kh][r0 + 8][2 * t]) = make_float2(acc[2], acc[3]);
     __syncwarp();
     if (lane == 0) mbar_arrive(&c->sums_full);
     if (!__all_sync(0xffffffffu, mbar_wait(&c->sums_full, n1 & 1u, &c->abort, p.status))) return;
-    bool over = false;
-    __half* out = static_cast<__half*>(k.out);
-    for (int i = tid; i < 64 * it.rows; i += 32 * GV_WARPS) {
-      const int f = i & 63, t = i >> 6;
-      const int r1 = (f >> 4) * 32 + (f & 15);
-      const float hv = silu_f(c->sums[r1][t]) * c->sums[r1 + 16][t];
-      over |= fabsf(hv) >= 65520.0f;
-      out[(it.row0 + t) * k.out_ld + it.tile * 64 + f] = __float2half_rn(hv);
+    if (!p.gemm1) {
+      float* out = static_cast<float*>(k.out);
+      for (int i = tid; i < 128 * it.rows; i += 32 * GV_WARPS) {
+        const int r = i & 127, tk = i >> 7;
+        out[(it.row0 + tk) * k.out_ld + it.tile * 128 + r] = c->sums[0][r][tk] + c->sums[1][r][tk];
+      }
+    } else {
+      // GEMM1: rows come in blocks of 32 (16 W1 rows of 16 features, then their W3 rows)
+      bool over = false;
+      __half* out = static_cast<__half*>(k.out);
+      for (int i = tid; i < 64 * it.rows; i += 32 * GV_WARPS) {
+        const int f = i & 63, tk = i >> 6;
+        const int r1 = (f >> 4) * 32 + (f & 15);
+        const float gv = c->sums[0][r1][tk] + c->sums[1][r1][tk];
+        const float uv = c->sums[0][r1 + 16][tk] + c->sums[1][r1 + 16][tk];
+        const float hv = silu_f(gv) * uv;
+        over |= fabsf(hv) >= 65520.0f;
+        out[(it.row0 + tk) * k.out_ld + it.tile * 64 + f] = __float2half_rn(hv);
+      }
+      if (over) flag_status(p.status, DEV_RANGE);
     }
-    if (over) flag_status(p.status, DEV_RANGE);
     __syncwarp();
     if (lane == 0) mbar_arrive(&c->sums_free);
     ++n1;
   }
 }
 
-// MAXR: the most token rows any group of the launch holds (1, 2 or 4).
-template <int MAXR>
 __global__ void __launch_bounds__(GV_THREADS, 1) gemv_fp8_kernel(const __grid_constant__ GemvParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
@@ -431,10 +423,11 @@ __global__ void __launch_bounds__(GV_THREADS, 1) gemv_fp8_kernel(const __grid_co
   __syncthreads();
   pdl_launch_dependents();
   if (warp == GV_WARPS) gemv_producer(p, c, ring, lane);
-  else gemv_compute<MAXR>(p, c, ring, warp, lane);
+  else gemv_compute(p, c, ring, warp, lane);
 }
 
 constexpr size_t kGemvSmem = 128 + size_t(GV_STAGES) * GV_STAGE_BYTES + sizeof(GemvCtrl);
+static_assert(kGemvSmem <= 232448, "shared memory of one CTA");
 
 }  // namespace
 
@@ -493,19 +486,10 @@ cudaError_t launch_fp8_gemv(const GemvOperands& routed, const GemvOperands* shar
   int ok = 0;
   cudaError_t e = attr.get(&ok, [](int* v) {
     *v = 1;
-    cudaError_t err = cudaFuncSetAttribute(gemv_fp8_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           int(kGemvSmem));
-    if (err == cudaSuccess)
-      err = cudaFuncSetAttribute(gemv_fp8_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kGemvSmem));
-    if (err == cudaSuccess)
-      err = cudaFuncSetAttribute(gemv_fp8_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kGemvSmem));
-    return err;
+    return cudaFuncSetAttribute(gemv_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kGemvSmem));
   });
   if (e != cudaSuccess) return e;
-  const int maxr = max_rows <= 1 ? 1 : (max_rows <= 2 ? 2 : 4);
-  if (maxr == 1) e = launch_pdl(gemv_fp8_kernel<1>, dim3(num_sms()), dim3(GV_THREADS), kGemvSmem, stream, p);
-  else if (maxr == 2) e = launch_pdl(gemv_fp8_kernel<2>, dim3(num_sms()), dim3(GV_THREADS), kGemvSmem, stream, p);
-  else e = launch_pdl(gemv_fp8_kernel<4>, dim3(num_sms()), dim3(GV_THREADS), kGemvSmem, stream, p);
+  e = launch_pdl(gemv_fp8_kernel, dim3(num_sms()), dim3(GV_THREADS), kGemvSmem, stream, p);
   if (e == cudaSuccess && launches) ++*launches;
   return e;
 }

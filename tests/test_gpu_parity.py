@@ -287,7 +287,7 @@ def test_forward_equals_staged_calls():
 def test_fp8_forward_equals_staged_calls(name):
     """FP8 weights through the staged calls: moe_grouped_swiglu converts the
     caller's bf16 x_perm to the f16 rows the FP8 expert kernels take (the
-    CUDA-core kernel at T=3, the tensor-core kernel at T=333), and the outputs
+    GEMV at T=3, the tensor-core kernel at T=333), and the outputs
     equal moe_forward's bit for bit."""
     wl = _fp8_copy(SMALL[name])
     li = inputs.make_inputs(wl, "cuda")
@@ -609,10 +609,15 @@ def _dequantized_shared(li):
 FP8_ODD = {
     "v3_odd_t5": inputs.small_workload(W["v3_prefill_t16384"], name="v3_odd_t5", T=5, d=384, E=64, I=384,
                                        n_group=8, topk_group=4),
+    "v3_odd_t9": inputs.small_workload(W["v3_prefill_t16384"], name="v3_odd_t9", T=9, d=384, E=64, I=384,
+                                       n_group=8, topk_group=4),
     "v3_odd_t40": inputs.small_workload(W["v3_prefill_t16384"], name="v3_odd_t40", T=40, d=384, E=64, I=384,
                                         n_group=8, topk_group=4),
-    # batches of at most 4 tokens take the CUDA-core FP8 path: the largest such
-    # batch with an odd number of stages, and one without a shared expert
+    # batches of at most 8 tokens take the FP8 GEMV (warp-level MMAs): the
+    # largest such batch and a middle one with an odd number of stages, and one
+    # without a shared expert
+    "v3_gemv_t8": inputs.small_workload(W["v3_prefill_t16384"], name="v3_gemv_t8", T=8, d=384, E=64, I=384,
+                                        n_group=8, topk_group=4),
     "v3_gemv_t4": inputs.small_workload(W["v3_prefill_t16384"], name="v3_gemv_t4", T=4, d=384, E=64, I=384,
                                         n_group=8, topk_group=4),
     "v2lite_gemv_t2_noshared": inputs.small_workload(W["v2lite_t4096"], name="v2lite_gemv_t2_noshared", T=2, d=256,
@@ -621,8 +626,8 @@ FP8_ODD = {
 
 
 @pytest.mark.parametrize("name", ["v3_small_t333", "v2lite_small_t1037", "v3_small_t1", "v3_small_t3",
-                                  "v3_small_t1100", "v3_odd_t5", "v3_odd_t40", "v3_gemv_t4",
-                                  "v2lite_gemv_t2_noshared"])
+                                  "v3_small_t1100", "v3_odd_t5", "v3_odd_t9", "v3_odd_t40", "v3_gemv_t8",
+                                  "v3_gemv_t4", "v2lite_gemv_t2_noshared"])
 def test_fp8_layer_matches_oracle_on_dequantized_weights(name):
     wl = _fp8_copy(SMALL[name] if name in SMALL else FP8_ODD[name])
     li = inputs.make_inputs(wl, "cuda")

@@ -108,7 +108,7 @@ typedef struct moe_config {
                               values round to multiples of 2^-24, larger ones
                               set MOE_ERR_DEVICE_RANGE); the shared expert's
                               first GEMM reads x as bf16 and dequantizes its
-                              weights to bf16 (exact).  Batches of at most 8
+                              weights to bf16 (exact).  Batches of at most 64
                               tokens run as a GEMV with warp-level MMAs
                               instead: e4m3 -> f16 weights times f16 token
                               values (the shared expert's too), exact

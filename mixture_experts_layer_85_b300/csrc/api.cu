@@ -241,7 +241,7 @@ moe_status run_experts(const moe_config& c, const void* x_perm, const int32_t* o
   const long long tiles1 = tb_routed * ((2LL * c.I + 255) / 256) + tb_shared * ((2 * Is + 255) / 256);
   const long long tiles2 = (tb_routed + tb_shared) * ((c.d + 255) / 256);
   const int shared_rows = Is > 0 ? c.T : 0;
-  if (P.fp8 && c.T <= GEMV_MAX_ROWS) {
+  if (P.fp8 && c.T <= GEMV_MAX_T) {
     // decode batches of FP8 experts: GEMV with warp-level MMAs (a group holds at most T rows)
     GemvOperands g1, g1s, g2, g2s;
     g1.w = pb + P.w13; g1.x = x_perm; g1.x_f16 = true; g1.out = h; g1.out_ld = c.I; g1.M = 2 * c.I; g1.K = c.d;
@@ -628,7 +628,8 @@ int32_t moe_forward_kernel_count(const moe_config* cfg) {
   int n = 2;                                                        // logits + top-k
   if (use_tc_gate(c) && c.gate_w_dtype == MOE_F32) n += 1;          // W_g split
   n += permute_launches(c.T) + 1;                                   // permute + gather
-  n += is_bf16(c) ? (fuse_expert_gemms(c) ? 1 : 2) : 2;              // expert GEMMs
+  const bool gemv = c.expert_w_dtype == MOE_FP8_E4M3 && c.T <= GEMV_MAX_T;
+  n += is_bf16(c) && !gemv && fuse_expert_gemms(c) ? 1 : 2;         // expert GEMMs
   n += 1;                                                           // combine
   return n;
 }

@@ -1,6 +1,6 @@
 // Expert FFNs with FP8 weights for decode batches (every group at most
-// GEMV_MAX_ROWS token rows): a GEMV over the packed FP8 stage images whose dot
-// products run as warp-level MMAs.
+// GEMV_MAX_T token rows): a GEMV over the packed FP8 stage images whose dot
+// products run as warp-level MMAs, GEMV_MAX_ROWS token rows at a time.
 //
 // At a handful of tokens per expert the op is a matrix-vector product bound
 // by the weight stream.  The tcgen05 FP8 path pays a per-stage hand-off
@@ -11,8 +11,8 @@
 // token rows' 128 matching values (bulk copies) through a ring of shared-memory
 // stages; every warp turns its 16 x 64 piece of a stage into f16 (e4m3 -> f16
 // is exact) and multiplies it by the token values (f16; the shared expert's
-// bf16 x rounded to f16) with four m16n8k16 MMAs, the up to 8 token rows being
-// the 8 columns of B.  Products of f16 values are exact and the MMA sums them
+// bf16 x rounded to f16) with four m16n8k16 MMAs, the item's up to 8 token
+// rows being the 8 columns of B.  Products of f16 values are exact and the MMA sums them
 // in fp32; each 64-column partial times its block's 2^e (exact) is added to
 // the fp32 accumulator.  One MMA serves 1 to 8 tokens at the same cost, so the
 // instruction count per weight no longer grows with the batch.  The expert
@@ -20,11 +20,14 @@
 // the FP8 block quantisation of its section 4; two launches: GEMM1 with the
 // SwiGLU epilogue (f16 hidden rows), then GEMM2 (fp32 rows).
 //
-// Work items are (group, 128-row weight tile), the shared expert's first:
-// their token rows do not depend on the dispatch, so in the GEMM1 launch they
-// stream while the preceding kernels still run; the routed groups' items wait
-// for the dispatch (griddepcontrol.wait), after which the producer warp lists
-// the groups that received rows.  CTA b takes items b, b + G, b + 2G, ...
+// Work items are (group, 128-row weight tile, chunk of up to 8 token rows),
+// the shared expert's first: their token rows do not depend on the dispatch,
+// so in the GEMM1 launch they stream while the preceding kernels still run;
+// the routed groups' items wait for the dispatch (griddepcontrol.wait), after
+// which the producer warp lists the groups that received rows and their item
+// counts.  A tile's chunks are consecutive items, so the CTAs that take them
+// stream the same weights at about the same time and all but one read them
+// from L2.  CTA b takes items b, b + G, b + 2G, ...
 // (one CTA per SM, a ring of 11 stages: 215 KB of weights and token values in
 // flight per SM).  Every wait is bounded; a CTA that gives up flags the status
 // word and its roles leave without waiting on each other.
@@ -66,7 +69,7 @@ struct GemvParams {
   const int32_t* offsets;   // [num_routed + 1] routed rows of each group
   int num_routed;
   int shared_rows;          // 0: no shared expert
-  int max_rows;             // bound of every group's token rows (GEMV_MAX_ROWS or less)
+  int max_rows;             // bound of every group's token rows (GEMV_MAX_T or less)
   long long routed_rows;    // bound of every routed row index
   int gemm1;                // 1: SwiGLU epilogue, 0: fp32 rows
   int x_from_prev;          // 1: every item's token rows come from the preceding grid
@@ -81,7 +84,8 @@ struct GemvCtrl {
   uint64_t sums_free;          // every compute warp read the sums
   int abort;
   int n_active;
-  int active[GV_MAX_GROUPS];
+  int active[GV_MAX_GROUPS];     // groups with rows, in index order
+  int item_end[GV_MAX_GROUPS];   // routed items of active groups 0 .. i (running sum)
   float sums[2][128][GEMV_MAX_ROWS];   // the tile's row sums of each k-block half, [half][row][token]
 };
 
@@ -106,38 +110,59 @@ __device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, 
 }
 
 struct GemvItem {
-  int cls, rows, tile_w;        // class, token rows, weight tile (of the class's whole matrix)
+  int cls, rows, tile_w;        // class, token rows (<= GEMV_MAX_ROWS), weight tile (of the class's whole matrix)
   int tile;                     // tile within the group
   long long row0;               // first token row (x) and output row
 };
 
-// Item -> operands, or false past the last item.  nsh: the shared expert's items.
+// Items of a group with `rows` token rows, per weight tile.
+__device__ __forceinline__ int gv_chunks(int rows) { return (rows + GEMV_MAX_ROWS - 1) / GEMV_MAX_ROWS; }
+
+// The shared expert's items (they come first).
+__device__ __forceinline__ int gv_shared_items(const GemvParams& p) {
+  return p.shared_rows > 0 ? p.cls[1].tpg * gv_chunks(p.shared_rows) : 0;
+}
+
+// Item -> operands, or false past the last item.  nsh: the shared expert's
+// items.  Within a group, item = tile * chunks + chunk.
 __device__ __forceinline__ bool gemv_item(const GemvParams& p, const GemvCtrl* c, int nsh, int item, GemvItem& it) {
   if (item < nsh) {
+    const int nch = gv_chunks(p.shared_rows);
+    const int tile = item / nch, ch = item - tile * nch;
     it.cls = 1;
-    it.rows = p.shared_rows;
-    it.tile = item;
-    it.tile_w = item;
-    it.row0 = 0;
+    it.tile = tile;
+    it.tile_w = tile;
+    it.row0 = (long long)ch * GEMV_MAX_ROWS;
+    it.rows = min(GEMV_MAX_ROWS, p.shared_rows - ch * GEMV_MAX_ROWS);
     return true;
   }
-  const int tpg = p.cls[0].tpg;
   const int j = item - nsh;
-  const int gi = j / tpg;
-  if (gi >= c->n_active) return false;
-  const int g = c->active[gi];
+  const int n = c->n_active;
+  if (n == 0 || j >= c->item_end[n - 1]) return false;
+  int lo = 0, hi = n - 1;   // the first active group whose items end past j
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (c->item_end[mid] > j) hi = mid;
+    else lo = mid + 1;
+  }
+  const int g = c->active[lo];
+  const long long r0 = p.offsets[g];
+  const int rows = int(p.offsets[g + 1] - r0);
+  const int nch = gv_chunks(rows);
+  const int local = j - (lo > 0 ? c->item_end[lo - 1] : 0);
+  const int tile = local / nch, ch = local - tile * nch;
   it.cls = 0;
-  it.tile = j - gi * tpg;
-  it.tile_w = g * tpg + it.tile;
-  it.row0 = p.offsets[g];
-  it.rows = p.offsets[g + 1] - p.offsets[g];
+  it.tile = tile;
+  it.tile_w = g * p.cls[0].tpg + tile;
+  it.row0 = r0 + (long long)ch * GEMV_MAX_ROWS;
+  it.rows = min(GEMV_MAX_ROWS, rows - ch * GEMV_MAX_ROWS);
   return true;
 }
 
 // Producer warp: lists the routed groups with rows (after the dispatch), then
 // lane 0 streams every item's stages.  Returns with all its copies landed.
 __device__ void gemv_producer(const GemvParams& p, GemvCtrl* c, uint8_t* ring, int lane) {
-  const int nsh = p.shared_rows > 0 ? p.cls[1].tpg : 0;
+  const int nsh = gv_shared_items(p);
   const int G = gridDim.x;
   bool waited = false, listed = false;
   int s = 0;
@@ -149,8 +174,9 @@ __device__ void gemv_producer(const GemvParams& p, GemvCtrl* c, uint8_t* ring, i
       waited = true;
     }
     if (item >= nsh && !listed) {
-      // warp-wide scan of the groups: the ones with rows, in index order
-      int base = 0;
+      // warp-wide scan of the groups: the ones with rows, in index order, and
+      // the running count of their items
+      int base = 0, items = 0;
       for (int g0 = 0; g0 < p.num_routed; g0 += 32) {
         const int g = g0 + lane;
         int rows = 0;
@@ -163,8 +189,19 @@ __device__ void gemv_producer(const GemvParams& p, GemvCtrl* c, uint8_t* ring, i
           }
         }
         const uint32_t m = __ballot_sync(0xffffffffu, rows > 0);
-        if (rows > 0) c->active[base + __popc(m & ((1u << lane) - 1u))] = g;
+        int incl = rows > 0 ? p.cls[0].tpg * gv_chunks(rows) : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int v = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += v;
+        }
+        if (rows > 0) {
+          const int pos = base + __popc(m & ((1u << lane) - 1u));
+          c->active[pos] = g;
+          c->item_end[pos] = items + incl;
+        }
         base += __popc(m);
+        items += __shfl_sync(0xffffffffu, incl, 31);
       }
       if (lane == 0) {
         c->n_active = base;
@@ -312,7 +349,7 @@ __device__ __forceinline__ void gemv_stage(const uint8_t* st, int r0, int kh, in
 // (bounded) and the warp leaves together when any lane gave up.
 constexpr int GV_PER = 4;
 __device__ void gemv_compute(const GemvParams& p, GemvCtrl* c, uint8_t* ring, int warp, int lane) {
-  const int nsh = p.shared_rows > 0 ? p.cls[1].tpg : 0;
+  const int nsh = gv_shared_items(p);
   const int G = gridDim.x;
   const int rt = warp & 7, kh = warp >> 3;
   const int g = lane >> 2, t = lane & 3;
@@ -435,8 +472,8 @@ cudaError_t launch_fp8_gemv(const GemvOperands& routed, const GemvOperands* shar
                             int num_routed, int shared_rows, int max_rows, long long routed_rows, bool gemm1,
                             bool x_from_prev, int* status, cudaStream_t stream, int* launches) {
   if (num_routed < 1 || num_routed > GV_MAX_GROUPS || offsets == nullptr) return cudaErrorInvalidValue;
-  if (max_rows < 1 || max_rows > GEMV_MAX_ROWS || shared_rows > max_rows) return cudaErrorInvalidValue;
-  if ((shared == nullptr) != (shared_rows <= 0) || shared_rows > GEMV_MAX_ROWS) return cudaErrorInvalidValue;
+  if (max_rows < 1 || max_rows > GEMV_MAX_T || shared_rows > max_rows) return cudaErrorInvalidValue;
+  if ((shared == nullptr) != (shared_rows <= 0)) return cudaErrorInvalidValue;
   GemvParams p;
   memset(&p, 0, sizeof(p));
   const GemvOperands* ops[2] = {&routed, shared};

@@ -156,16 +156,18 @@ cudaError_t launch_pair_experts(const PairClass cls[4], const int32_t* offsets, 
                                 const int32_t* fp8_eref = nullptr);
 
 // FP8 expert FFNs for decode batches as a GEMV with warp-level MMAs
-// (csrc/gemv_fp8.cu): every group holds at most GEMV_MAX_ROWS token rows.  One launch per GEMM:
-// gemm1 = GEMM1 with the SwiGLU epilogue (f16 hidden rows [rows, M/2]), else
-// GEMM2 (fp32 rows [rows, M]).  w: FP8 stage images of groups of M rows and K
+// (csrc/gemv_fp8.cu): every group holds at most GEMV_MAX_T token rows, taken
+// GEMV_MAX_ROWS at a time (the MMA's N).  One launch per GEMM: gemm1 = GEMM1
+// with the SwiGLU epilogue (f16 hidden rows [rows, M/2]), else GEMM2 (fp32
+// rows [rows, M]).  w: FP8 stage images of groups of M rows and K
 // columns; x: token rows, K 2-byte values each (x_f16: f16, else bf16).  The
 // routed class's groups take rows offsets[g] .. offsets[g+1] (all below
 // routed_rows); the shared class, rows 0 .. shared_rows; no group holds more
-// than max_rows (<= GEMV_MAX_ROWS; a group that does is flagged and skipped).
+// than max_rows (<= GEMV_MAX_T; a group that does is flagged and skipped).
 // x_from_prev: every item's token rows come from the preceding grid (else
 // only the routed ones).
 constexpr int GEMV_MAX_ROWS = 8;
+constexpr int GEMV_MAX_T = 64;
 struct GemvOperands {
   const void* w = nullptr;
   const void* x = nullptr;

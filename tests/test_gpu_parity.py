@@ -611,11 +611,16 @@ FP8_ODD = {
                                        n_group=8, topk_group=4),
     "v3_odd_t9": inputs.small_workload(W["v3_prefill_t16384"], name="v3_odd_t9", T=9, d=384, E=64, I=384,
                                        n_group=8, topk_group=4),
+    "v3_odd_t72": inputs.small_workload(W["v3_prefill_t16384"], name="v3_odd_t72", T=72, d=384, E=64, I=384,
+                                        n_group=8, topk_group=4),
+    # the GEMV's largest batch with the decode layers' skewed bias: 512 rows
+    # over 64 experts (8 on average) and the shared expert's 64, in items of 8
+    "v3_gemv_t64_zipf": inputs.small_workload(W["v3_prefill_t16384"], name="v3_gemv_t64_zipf", T=64, d=384,
+                                              E=64, I=384, n_group=8, topk_group=4, bias="zipf"),
     "v3_odd_t40": inputs.small_workload(W["v3_prefill_t16384"], name="v3_odd_t40", T=40, d=384, E=64, I=384,
                                         n_group=8, topk_group=4),
-    # batches of at most 8 tokens take the FP8 GEMV (warp-level MMAs): the
-    # largest such batch and a middle one with an odd number of stages, and one
-    # without a shared expert
+    # batches of at most 64 tokens take the FP8 GEMV (warp-level MMAs, 8 token
+    # rows per item): one item per group, and one without a shared expert
     "v3_gemv_t8": inputs.small_workload(W["v3_prefill_t16384"], name="v3_gemv_t8", T=8, d=384, E=64, I=384,
                                         n_group=8, topk_group=4),
     "v3_gemv_t4": inputs.small_workload(W["v3_prefill_t16384"], name="v3_gemv_t4", T=4, d=384, E=64, I=384,
@@ -626,8 +631,8 @@ FP8_ODD = {
 
 
 @pytest.mark.parametrize("name", ["v3_small_t333", "v2lite_small_t1037", "v3_small_t1", "v3_small_t3",
-                                  "v3_small_t1100", "v3_odd_t5", "v3_odd_t9", "v3_odd_t40", "v3_gemv_t8",
-                                  "v3_gemv_t4", "v2lite_gemv_t2_noshared"])
+                                  "v3_small_t1100", "v3_odd_t5", "v3_odd_t9", "v3_odd_t40", "v3_odd_t72",
+                                  "v3_gemv_t64_zipf", "v3_gemv_t8", "v3_gemv_t4", "v2lite_gemv_t2_noshared"])
 def test_fp8_layer_matches_oracle_on_dequantized_weights(name):
     wl = _fp8_copy(SMALL[name] if name in SMALL else FP8_ODD[name])
     li = inputs.make_inputs(wl, "cuda")

@@ -55,6 +55,17 @@ def test_sizes_for_every_workload(name):
     assert _lib.moe_forward_kernel_count(cfg) == gate + dispatch + 1 + experts + 1
 
 
+@pytest.mark.parametrize("name,experts", [("v3_decode_fp8_t1", 2), ("v3_decode_fp8_t64", 2),
+                                          ("v3_decode_fp8_t512", 1), ("v3_prefill_fp8_t16384", 2)])
+def test_fp8_kernel_count(name, experts):
+    """FP8 layers: batches of at most 64 tokens run the GEMV (GEMM1, then
+    GEMM2); larger ones the tensor-core kernel, fused up to 8192 rows."""
+    wl = inputs.WORKLOADS[name]
+    cfg = _lib.make_config(wl)
+    dispatch = 1 if wl.T <= 4096 else 4
+    assert _lib.moe_forward_kernel_count(cfg) == 2 + dispatch + 1 + experts + 1
+
+
 def _cfg(**kw):
     c = _lib.make_config(inputs.WORKLOADS["v3_prefill_t16384"])
     for k, v in kw.items():

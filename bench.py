@@ -433,7 +433,22 @@ def stage_times(layer, x, out, counts, n, flush=None):
 # current kernel source; the summary and the command that made it are in the named profiles/ file.
 EXPERT_TRAFFIC = {
     "v3_prefill_t16384": (32.03e9, "profiles/launches_v3_prefill_t16384.md"),
+    # the same 9 experts' weights (8 routed + shared) as the 16-expert capture
+    "v3_decode_fp8_t1": (424.9e6, "profiles/gemv_fp8_decode_v3shape_e16_t1.md"),
 }
+GEMV_MAX_T = 64   # FP8 layers of at most this many tokens run the expert GEMV
+
+
+def expert_kernel(wl):
+    """The expert stage's kernel and its launches per forward."""
+    if wl.act_dtype != "bf16":
+        return "swiglu_simt_h_kernel, swiglu_simt_y_kernel (fp32 SIMT)", 2
+    if wl.expert_w_dtype == "fp8" and wl.T <= GEMV_MAX_T:
+        return "gemv_fp8_kernel (GEMM1 + SwiGLU, then GEMM2)", 2
+    name = "pair_gemm_kernel<true> (FP8 weights; " if wl.expert_w_dtype == "fp8" else "pair_gemm_kernel ("
+    if wl.T * wl.k <= 8192:
+        return name + "GEMM1 + SwiGLU and GEMM2 in one launch)", 1
+    return name + "GEMM1 + SwiGLU, then GEMM2)", 2
 
 
 def expert_roofline(wl, cnt, expert_ms, peaks):
@@ -456,7 +471,8 @@ def expert_roofline(wl, cnt, expert_ms, peaks):
     if traffic is not None:
         roof["traffic_source"] = source
         roof["traffic_over_algorithmic"] = round(traffic / byts, 3)
-    roof.update({"kernel": "pair_gemm_kernel (GEMM1 + SwiGLU and GEMM2)", "traffic": traffic,
+    kernel, launches = expert_kernel(wl)
+    roof.update({"kernel": kernel, "launches_per_forward": launches, "traffic": traffic,
                  "per_launch_flops": flops, "per_launch_algorithmic_bytes": byts,
                  "avg_launch_ms": round(expert_ms, 4)})
     return roof

@@ -198,3 +198,20 @@ def test_bf16_packed_size_is_the_stage_block_layout(d, I, E, n_shared):
     for part in parts:
         total = -(-(total + part) // 256) * 256
     assert _lib.moe_packed_size(cfg) == total
+
+
+@pytest.mark.parametrize("name", sorted(inputs.WORKLOADS))
+def test_bench_expert_kernel_matches_the_library(name):
+    """The bench line's roofline names the expert stage's kernel and its
+    launches per forward; the count agrees with the library's own."""
+    import sys
+    sys.path.insert(0, ROOT)
+    import bench
+    wl = inputs.WORKLOADS[name]
+    cfg = _lib.make_config(wl)
+    kernel, launches = bench.expert_kernel(wl)
+    bf16 = wl.act_dtype == "bf16"
+    gate = 2 + (1 if bf16 and wl.gate_w_dtype == "f32" else 0)
+    dispatch = 1 if wl.T <= 4096 else 4
+    assert _lib.moe_forward_kernel_count(cfg) == gate + dispatch + 1 + launches + 1
+    assert kernel.startswith("gemv_fp8_kernel") == (wl.expert_w_dtype == "fp8" and wl.T <= 64)

@@ -203,6 +203,7 @@ __device__ void gemv_producer(const GemvParams& p, GemvCtrl* c, uint8_t* ring, i
         base += __popc(m);
         items += __shfl_sync(0xffffffffu, incl, 31);
       }
+      __syncwarp();   // every lane's entries are ordered before lane 0's release
       if (lane == 0) {
         c->n_active = base;
         mbar_arrive(&c->list_ready);   // release (CTA): orders the list above
